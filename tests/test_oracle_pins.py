@@ -1,0 +1,354 @@
+"""Pins of the CPU oracle against what the llm.c pages and the mathematics fix.
+
+Each test names the fact it pins (P1..P12).  The oracle is never compared
+with itself here: the expected values are printed numbers from the pages
+(tests/golden/pages_console_log.json), closed forms, invariants, brute force
+or finite differences.
+"""
+import json
+import math
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import ref
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+GOLDEN = json.load(open(os.path.join(HERE, "golden", "pages_console_log.json")))
+
+TINY = synth.WORKLOADS["tiny_L2_C64"]
+G124 = synth.WORKLOADS["gpt2_124m_B4_T64_fp32"]
+
+
+def cfg_124m_from_log():
+    g = GOLDEN
+    return ref.make_config(g["max_seq_len"], g["vocab_size"], 50304, g["num_layers"], g["num_heads"], g["channels"])
+
+
+# --------------------------------------------------------------------------
+# P1-P3: the counts printed in the console log
+# --------------------------------------------------------------------------
+def test_P1_parameter_count_matches_console_log():
+    cfg = cfg_124m_from_log()
+    assert ref.num_parameters(cfg, padded=False) == GOLDEN["num_parameters"] == 124439808
+    # padded layout: 47 extra zero rows of wte
+    assert ref.num_parameters(cfg, padded=True) == 124439808 + (50304 - 50257) * 768
+    assert ref.num_parameters(ref.config_from(TINY)) == 134912
+
+
+def test_P1_layout_agrees_with_input_generator():
+    for w in (TINY, G124):
+        offs = ref.param_offsets(ref.config_from(w))
+        assert offs == synth.param_offsets(w)
+        assert ref.num_parameters(ref.config_from(w)) == synth.num_params(w)
+
+
+def test_P2_activation_count_matches_console_log():
+    cfg = cfg_124m_from_log()
+    # B*T = 256 (P3) with T = 64; unpadded vocab as printed
+    assert ref.num_activations(cfg, 4, 64, padded=False) == GOLDEN["num_activations"] == 73323776
+
+
+def test_P3_batch_counts_fix_BT_256():
+    g = GOLDEN
+    cands = [bt for bt in range(1, 4097) if g["train_tokens"] // bt == g["train_num_batches"]
+             and g["val_tokens"] // bt == g["val_num_batches"]]
+    assert cands == [256]
+    assert G124.B * G124.T == 256
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+def perturbed_params(w, seed=7, scale=1.0):
+    """Initial params plus seeded noise on biases and layernorm affine terms,
+    so that every gradient is generic (not structurally zero)."""
+    p = synth.init_params(w).astype(np.float64)
+    rng = np.random.default_rng(seed)
+    offs = synth.param_offsets(w)
+    for name in ("ln1w", "ln2w", "lnfw"):
+        o, n = offs[name]
+        p[o:o + n] += scale * 0.1 * rng.standard_normal(n)
+    for name in ("ln1b", "ln2b", "lnfb", "qkvb", "attprojb", "fcb", "fcprojb"):
+        o, n = offs[name]
+        p[o:o + n] = scale * 0.02 * rng.standard_normal(n)
+    # padded wte rows stay zero
+    o, _ = offs["wte"]
+    p[o + w.vocab_size * w.channels: o + w.padded_vocab_size * w.channels] = 0.0
+    return p
+
+
+def tiny_model(dtype=np.float64, params=None, maxB=None, maxT=None, w=TINY):
+    m = ref.RefModel(ref.config_from(w), maxB or w.B, maxT or w.T, dtype)
+    m.set_params(perturbed_params(w) if params is None else params)
+    return m
+
+
+# --------------------------------------------------------------------------
+# P4: layernorm moments
+# --------------------------------------------------------------------------
+def test_P4_layernorm_output_moments():
+    ops = ref.ops(np.float64)
+    rng = np.random.default_rng(0)
+    for sigma in (0.03, 1.0, 10.0):
+        x = 0.5 + sigma * rng.standard_normal((37, 96))
+        y, mean, rstd = ops.layernorm_forward(x, np.ones(96), np.zeros(96))
+        var_in = x.var(axis=1)
+        assert np.all(np.abs(y.mean(axis=1)) < 1e-6)
+        np.testing.assert_allclose(y.var(axis=1), var_in / (var_in + 1e-5), rtol=1e-10)
+        np.testing.assert_allclose(mean, x.mean(axis=1), rtol=1e-12)
+        np.testing.assert_allclose(rstd, 1.0 / np.sqrt(var_in + 1e-5), rtol=1e-12)
+    # affine: gamma scales, beta shifts
+    x = rng.standard_normal((5, 32))
+    g, b = rng.standard_normal(32), rng.standard_normal(32)
+    y0, _, _ = ops.layernorm_forward(x, np.ones(32), np.zeros(32))
+    y1, _, _ = ops.layernorm_forward(x, g, b)
+    np.testing.assert_allclose(y1, y0 * g + b, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# P5: attention rows and vocab rows are probability distributions
+# --------------------------------------------------------------------------
+def test_P5_attention_and_probs_rows_sum_to_one():
+    m = tiny_model(np.float64)
+    inp, tgt = synth.batch(TINY)
+    m.forward(inp, tgt)
+    B, T, NH, L = TINY.B, TINY.T, TINY.num_heads, TINY.num_layers
+    att = m.act("att").reshape(L, B, NH, T, T)
+    rows = att.sum(axis=-1)
+    np.testing.assert_allclose(rows, 1.0, atol=1e-12)
+    mask = np.triu(np.ones((T, T), bool), k=1)
+    assert np.all(att[..., mask] == 0.0)
+    assert np.all(att[..., ~mask] > 0.0)
+    probs = m.act("probs").reshape(B * T, -1)
+    np.testing.assert_allclose(probs.sum(axis=1), 1.0, atol=1e-12)
+
+
+def test_P5_padded_vocab_columns_have_zero_probability():
+    w = synth.Workload("pad", 1, 32, 2, 100, 128, 16, 2, 8, "fp32", "uniform", 3)
+    m = ref.RefModel(ref.config_from(w), 2, 8, np.float32)
+    m.set_params(perturbed_params(w))
+    inp, tgt = synth.batch(w)
+    m.forward(inp, tgt)
+    probs = m.act("probs").reshape(16, 128)
+    assert np.all(probs[:, 100:] == 0.0)
+    np.testing.assert_allclose(probs.sum(axis=1, dtype=np.float64), 1.0, atol=1e-6)
+
+
+# --------------------------------------------------------------------------
+# P6: initial loss near ln V
+# --------------------------------------------------------------------------
+def test_P6_initial_loss_tiny():
+    inp, tgt = synth.batch(TINY)
+    m = ref.RefModel(ref.config_from(TINY), TINY.B, TINY.T, np.float64)
+    m.set_params(synth.init_params(TINY, wte_std=1e-4))
+    assert abs(m.forward(inp, tgt) - math.log(512)) < 1e-3
+    m.set_params(synth.init_params(TINY))
+    assert abs(m.forward(inp, tgt) - math.log(512)) < 0.05 * math.log(512)
+
+
+@pytest.mark.slow
+def test_P6_initial_loss_124m():
+    w = G124
+    m = ref.RefModel(ref.config_from(w), w.B, w.T, np.float32)
+    m.set_params(synth.init_params(w))
+    inp, tgt = synth.batch(w)
+    loss = m.forward(inp, tgt)
+    # logits std ~ 0.02*sqrt(C) gives E[loss] ~ ln V + (0.02^2 C)/2 ~ 10.98
+    assert abs(loss - math.log(50257)) < 0.05 * math.log(50257)
+    assert 10.8 < loss < 11.2
+    m.close()
+
+
+# --------------------------------------------------------------------------
+# P7: gradients against central finite differences (double build)
+# --------------------------------------------------------------------------
+def test_P7_finite_difference_gradients():
+    w = synth.Workload("fd", 2, 32, 4, 64, 64, 16, 2, 12, "fp32", "uniform", 1)
+    p0 = perturbed_params(w, seed=11)
+    inp, tgt = synth.batch(w)
+    m = ref.RefModel(ref.config_from(w), w.B, w.T, np.float64)
+    m.set_params(p0)
+    m.forward(inp, tgt)
+    m.zero_grad()
+    assert m.backward() == 0
+    g = m.grads.copy()
+
+    def loss_at(p):
+        m.set_params(p)
+        return m.forward(inp, tgt)
+
+    h = 1e-5
+    rng = np.random.default_rng(3)
+    offs = synth.param_offsets(w)
+    worst = 0.0
+    for name, (o, n) in offs.items():
+        idx = o + rng.choice(n, size=min(n, 12), replace=False)
+        if name == "wpe":  # only rows < T receive gradient; also test those
+            idx = o + rng.choice(w.T * w.channels, size=12, replace=False)
+        for i in idx:
+            pp = p0.copy(); pp[i] += h
+            pm = p0.copy(); pm[i] -= h
+            fd = (loss_at(pp) - loss_at(pm)) / (2 * h)
+            err = abs(fd - g[i])
+            assert err <= 1e-6 * abs(g[i]) + 2e-9, (name, i, fd, g[i])
+            worst = max(worst, err)
+        # directional derivative along a random direction inside the tensor
+        d = np.zeros_like(p0)
+        d[o:o + n] = rng.standard_normal(n)
+        fd = (loss_at(p0 + h * d) - loss_at(p0 - h * d)) / (2 * h)
+        gd = float(g[o:o + n] @ d[o:o + n])
+        assert abs(fd - gd) <= 1e-6 * abs(gd) + 1e-8, (name, fd, gd)
+    m.close()
+
+
+# --------------------------------------------------------------------------
+# P8: brute-force causality
+# --------------------------------------------------------------------------
+def test_P8_causality_changing_token_t_leaves_earlier_logits_bit_identical():
+    m = tiny_model(np.float32)
+    inp, tgt = synth.batch(TINY)
+    m.forward(inp, tgt)
+    l0 = m.act("logits").reshape(TINY.B, TINY.T, -1).copy()
+    t = 17
+    inp2 = inp.copy()
+    inp2[:, t] = (inp2[:, t] + 123) % TINY.vocab_size
+    m.forward(inp2, tgt)
+    l1 = m.act("logits").reshape(TINY.B, TINY.T, -1)
+    assert np.array_equal(l0[:, :t], l1[:, :t])
+    assert not np.array_equal(l0[:, t], l1[:, t])
+
+
+def test_P8_zero_queries_give_uniform_causal_average():
+    ops = ref.ops(np.float64)
+    rng = np.random.default_rng(5)
+    B, T, C, NH = 2, 9, 24, 3
+    qkv = rng.standard_normal((B, T, 3 * C))
+    qkv[:, :, :C] = 0.0  # q = 0 -> all scores 0
+    out, _, att = ops.attention_forward(qkv, NH)
+    for t in range(T):
+        np.testing.assert_allclose(att[:, :, t, :t + 1], 1.0 / (t + 1), rtol=1e-14)
+        v = qkv[:, :t + 1, 2 * C:]
+        np.testing.assert_allclose(out[:, t], v.mean(axis=1), rtol=1e-12, atol=1e-14)
+
+
+def test_P8_single_position_attention_returns_v():
+    ops = ref.ops(np.float64)
+    rng = np.random.default_rng(6)
+    qkv = rng.standard_normal((3, 1, 3 * 40))
+    out, _, att = ops.attention_forward(qkv, 5)
+    np.testing.assert_array_equal(out[:, 0], qkv[:, 0, 80:])
+    assert np.all(att == 1.0)
+
+
+# --------------------------------------------------------------------------
+# P10: AdamW first step closed form
+# --------------------------------------------------------------------------
+def test_P10_adamw_first_step_closed_form():
+    ops = ref.ops(np.float64)
+    rng = np.random.default_rng(8)
+    n = 4096
+    p = rng.standard_normal(n)
+    g = rng.standard_normal(n) * np.exp(rng.uniform(-12, 2, n))
+    lr, eps = 1e-4, 1e-8
+    p1, m1, v1 = ops.adamw_update(p, g, np.zeros(n), np.zeros(n), lr, 0.9, 0.999, eps, 0.0, 1)
+    np.testing.assert_allclose(p1, p - lr * g / (np.abs(g) + eps), rtol=1e-13, atol=1e-19)
+    big = np.abs(g) > 1e-3
+    np.testing.assert_allclose(p1[big] - p[big], -lr * np.sign(g[big]), rtol=1e-4)
+    np.testing.assert_allclose(m1, 0.1 * g, rtol=1e-12)
+    np.testing.assert_allclose(v1, 0.001 * g * g, rtol=1e-12)
+    # decoupled weight decay: a zero gradient leaves only the decay term
+    p2, _, _ = ops.adamw_update(p, np.zeros(n), np.zeros(n), np.zeros(n), lr, 0.9, 0.999, eps, 0.1, 1)
+    np.testing.assert_allclose(p2, p * (1 - lr * 0.1), rtol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# P11: invariants
+# --------------------------------------------------------------------------
+def test_P11_backward_accumulates():
+    m = tiny_model(np.float32)
+    inp, tgt = synth.batch(TINY)
+    m.forward(inp, tgt)
+    m.zero_grad()
+    assert m.backward() == 0
+    g1 = m.grads.copy()
+    assert m.backward() == 0
+    g2 = m.grads.copy()
+    offs = synth.param_offsets(TINY)
+    for name, (o, n) in offs.items():
+        if name == "wte":  # two contributions per backward (LM head + embedding): rounding differs
+            np.testing.assert_allclose(g2[o:o + n], 2 * g1[o:o + n], rtol=1e-5, atol=1e-9)
+        else:
+            assert np.array_equal(g2[o:o + n], 2 * g1[o:o + n]), name
+    m.zero_grad()
+    assert np.all(m.grads == 0)
+
+
+def test_P11_backward_needs_forward_with_targets():
+    m = tiny_model(np.float32)
+    inp, _ = synth.batch(TINY)
+    assert m.backward() == -4
+    assert m.forward(inp, None) == -1.0
+    assert m.backward() == -4
+
+
+def test_P11_fixed_batch_loss_strictly_decreases_and_pad_rows_stay_zero():
+    w = synth.Workload("pad", 2, 32, 2, 100, 128, 16, 2, 16, "fp32", "uniform", 10)
+    m = ref.RefModel(ref.config_from(w), w.B, w.T, np.float32)
+    m.set_params(synth.init_params(w))
+    inp, tgt = synth.batch(w)
+    losses = [m.step(inp, tgt, t, lr=1e-3) for t in range(1, 11)]
+    assert all(b < a for a, b in zip(losses, losses[1:])), losses
+    o, _ = synth.param_offsets(w)["wte"]
+    pad = slice(o + 100 * 32, o + 128 * 32)
+    assert np.all(m.params[pad] == 0.0) and np.all(m.grads[pad] == 0.0)
+
+
+def test_P11_tiny_config_ten_steps_lr_1e4_decreases():
+    m = ref.RefModel(ref.config_from(TINY), TINY.B, TINY.T, np.float32)
+    m.set_params(synth.init_params(TINY))
+    inp, tgt = synth.batch(TINY)
+    losses = [m.step(inp, tgt, t) for t in range(1, 11)]
+    assert all(b < a for a, b in zip(losses, losses[1:])), losses
+
+
+def test_P11_zipf_unigram_entropy_floor():
+    p = np.diff(np.concatenate([[0.0], synth.zipf_cdf(50257)]))
+    H = float(-(p * np.log(p)).sum())
+    assert abs(H - 6.4647) < 5e-4
+    assert abs(p[0] - 0.139) < 1e-3
+
+
+# --------------------------------------------------------------------------
+# P12: determinism across thread counts
+# --------------------------------------------------------------------------
+_DET_SCRIPT = r"""
+import sys, hashlib, numpy as np
+sys.path.insert(0, %r)
+import synth
+from oracle import ref
+w = synth.Workload("det", 2, 48, 4, 200, 256, 24, 3, 24, "fp32", "uniform", 2)
+m = ref.RefModel(ref.config_from(w), w.B, w.T, np.float32)
+m.set_params(synth.init_params(w))
+inp, tgt = synth.batch(w)
+for t in (1, 2):
+    m.step(inp, tgt, t)
+m.forward(inp, tgt); m.zero_grad(); m.backward()
+h = hashlib.sha256(m.params.tobytes() + m.grads.tobytes() + m.act("logits").tobytes()).hexdigest()
+print(h)
+"""
+
+
+def test_P12_oracle_bit_identical_across_thread_counts():
+    root = os.path.dirname(HERE)
+    outs = []
+    for nt in ("1", "3", "8"):
+        env = dict(os.environ, OMP_NUM_THREADS=nt)
+        r = subprocess.run([sys.executable, "-c", _DET_SCRIPT % root], env=env, capture_output=True, text=True,
+                           check=True)
+        outs.append(r.stdout.strip())
+    assert outs[0] == outs[1] == outs[2]
