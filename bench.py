@@ -1,0 +1,349 @@
+#!/usr/bin/env python
+"""Throughput of one GPT-2 training step (forward + zero_grad + backward +
+AdamW) on B300 GPUs, through libgpt2b300's C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...     # the CPU oracle, timed alone
+
+Default workload: GPT-2 124M (L=12, C=768, NH=12, V=50257 padded to 50304),
+fp32, B=4, T=64 -- the configuration of the llm.c console log (page
+«千行C代码训完GPT-2», section «快速入门»: 124,439,808 parameters, B*T = 256,
+about 1.3 s per step on an M3 Max CPU).  Inputs are synthetic: seeded
+Zipf(1.1) token streams and a seeded N(0, 0.02) init.
+
+Prints one JSON line (rank 0).  ``value`` is whole-job tokens/s with the
+token batches resident in HBM; ``e2e`` is the same metric through
+``gpt2_train_step`` with pinned host token arrays copied every step and the
+loss read back every step.  Multi-GPU runs are independent replicas (the path
+is not sharded across GPUs), so ``scaling`` is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "GPT-2 124M train tokens/sec (fwd+bwd+AdamW) on 1 B300; MFU; per-kernel HBM GB/s"
+DEFAULT_WORKLOAD = "gpt2_124m_B4_T64_fp32"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "sm_max_mhz": p.get("sm_max_mhz", 2032.0),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "sm_max_mhz": 2032.0,
+            "source": "fallback"}
+
+
+def flops_per_token(w) -> float:
+    """Algorithmic training FLOPs per token: 3 x forward, causal attention
+    counts only keys t2 <= t, the LM head over the real vocabulary."""
+    L, C, T, V = w.num_layers, w.channels, w.T, w.vocab_size
+    return 3.0 * (L * (24.0 * C * C + 4.0 * C * (T + 1) / 2.0) + 2.0 * C * V)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (rank 0)
+# ---------------------------------------------------------------------------
+def oracle_sample_run(w, seconds_target: float = 12.0, max_steps: int = 50, B_sample: int | None = None):
+    """Times full oracle training steps (forward, zero_grad, backward, AdamW)
+    on B_sample sequences of the workload's batch until seconds_target has
+    passed.  Returns (tokens/s, steps, tokens per step, seconds)."""
+    from oracle import ref
+
+    B = B_sample or w.B
+    m = ref.RefModel(ref.config_from(w), B, w.T, np.float32)
+    m.set_params(synth.init_params(w))
+    inp, tgt = synth.batch(w, step=0)
+    inp, tgt = inp[:B].copy(), tgt[:B].copy()
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        m.step(inp, tgt, steps + 1, lr=w.lr)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_target or steps >= max_steps:
+            break
+    m.close()
+    return B * w.T * steps / el, steps, B * w.T, el
+
+
+def cpu_cores() -> int:
+    n = int(os.environ.get("OMP_NUM_THREADS", "0") or 0)
+    return n if n > 0 else len(os.sched_getaffinity(0))
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    # each step: one full oracle training step on one sequence of the batch
+    B_sample = 1 if w.BT >= 256 else w.B
+    from oracle import ref
+
+    m = ref.RefModel(ref.config_from(w), B_sample, w.T, np.float32)
+    m.set_params(synth.init_params(w))
+    steps = min(args.steps, 8)
+    warm = min(args.warmup, 1)
+    batches = [synth.batch(w, step=s) for s in range(warm + steps)]
+    for s in range(warm):
+        m.step(batches[s][0][:B_sample], batches[s][1][:B_sample], s + 1, lr=w.lr)
+    t0 = time.perf_counter()
+    for s in range(steps):
+        i, t = batches[warm + s]
+        m.step(i[:B_sample], t[:B_sample], warm + s + 1, lr=w.lr)
+    el = time.perf_counter() - t0
+    m.close()
+    tok = B_sample * w.T * steps
+    value = tok / el
+    sample = (f"{steps} oracle training steps (forward, zero_grad, backward, AdamW) on {B_sample} of the "
+              f"{w.B} sequences of each batch (T={w.T}); tokens/s counts the tokens processed")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": warm, "ms_per_step": 1000.0 * el / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, n_gpus):
+    return {"workload": w.name, "B": w.B, "T": w.T, "tokens_per_step_per_gpu": w.BT,
+            "global_batch_tokens": w.BT * n_gpus, "precision": w.precision, "tokens": f"{w.tokens} (seeded)",
+            "parallelism": "replicas" if n_gpus > 1 else "single",
+            "l2": "no flush: each step streams params+grads+AdamW moments (> 126 MB L2)"}
+
+
+def run_ours(args, w):
+    import torch
+
+    import gpt2_train_step_02_b300 as g
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    K, W = args.steps, args.warmup
+    peaks = load_peaks()
+    model = g.GPT2(w, seed=synth.INIT_SEED)
+    stream = model.stream
+    # token batches for every step, resident in HBM before timing (distinct per rank)
+    nb = W + K
+    host_in = np.empty((nb, w.B, w.T), np.int32)
+    host_tg = np.empty((nb, w.B, w.T), np.int32)
+    for s in range(nb):
+        host_in[s], host_tg[s] = synth.batch(w, step=rank * 1_000_003 + s)
+    d_in = torch.from_numpy(host_in).cuda()
+    d_tg = torch.from_numpy(host_tg).cuda()
+    torch.cuda.synchronize()
+
+    t = 0
+    for s in range(W):
+        t += 1
+        model.train_step_device(d_in[s], d_tg[s], t, lr=w.lr)
+    torch.cuda.synchronize()
+    barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.25)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    start.record(stream)
+    for s in range(K):
+        t += 1
+        model.train_step_device(d_in[W + s], d_tg[W + s], t, lr=w.lr)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    launches_per_step = model.last_launch_count()
+    last_loss = model.sync()
+    if dist is not None:
+        x = torch.tensor([ms], device="cuda")
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        ms = float(x.item())
+    ms_per_step = ms / K
+    value = world * w.BT * K / (ms / 1000.0)
+
+    # per-kernel-class timing (events around each launch, direct launches)
+    kinds = {}
+    ksteps = min(K, 5)
+    for kind in ("gemm", "adamw", "xent", "layernorm"):
+        g.gpt2_kernel_timer(model.h, kind)
+        for s in range(ksteps):
+            t += 1
+            model.train_step_device(d_in[s % nb], d_tg[s % nb], t, lr=w.lr)
+        kms, kn, kwork = g.gpt2_kernel_timer_read(model.h)
+        kinds[kind] = {"ms_per_step": kms / ksteps, "launches_per_step": kn / ksteps,
+                       "work_per_launch": kwork / max(kn, 1), "avg_launch_ms": kms / max(kn, 1)}
+    g.gpt2_kernel_timer(model.h, "off")
+    dom = max(kinds, key=lambda k: kinds[k]["ms_per_step"])
+    roof = roofline_for(dom, kinds[dom], peaks, w)
+
+    # end to end: pinned host tokens, H2D every step, loss read back every step
+    pin_in = torch.from_numpy(host_in).pin_memory().numpy()
+    pin_tg = torch.from_numpy(host_tg).pin_memory().numpy()
+    for s in range(min(W, 3)):
+        t += 1
+        model.train_step(pin_in[s], pin_tg[s], t, lr=w.lr)
+    barrier()
+    t0 = time.perf_counter()
+    for s in range(K):
+        t += 1
+        model.train_step(pin_in[W + s], pin_tg[W + s], t, lr=w.lr)
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        x = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        e2e_s = float(x.item())
+    barrier()
+    e2e = {"value": world * w.BT * K / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 2 * w.BT * 4,
+           "d2h_bytes_per_step": 4, "api": "gpt2_train_step (host tokens, loss returned every step)"}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, steps, tok, el = oracle_sample_run(w, seconds_target=args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{steps} full oracle training step(s) of the same workload ({tok} tokens each), "
+                         f"{el:.1f} s of CPU time"}
+    f_tok = flops_per_token(w)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if w.precision == "fp32" else "bf16", "data": "synthetic",
+        "config": workload_config(w, world),
+        "mfu": {"vs_bf16_dense_measured": value * f_tok / (peaks["bf16_tflops"] * 1e12 * world),
+                "flops_per_token": f_tok},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches_per_step * K),
+        "clocks": clk,
+        "kernels": kinds,
+        "last_loss": last_loss,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def roofline_for(kind, k, peaks, w):
+    if kind == "gemm":
+        achieved = k["work_per_launch"] / (k["avg_launch_ms"] * 1e-3) / 1e12
+        # CUDA-core fp32 FMA peak: 148 SMs x 128 lanes x 2 FLOP x max SM clock
+        peak = 148 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        return {"kernel": "gemm (all matmul launches)", "bound": "alu", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 x max SM clock"}
+    achieved = k["work_per_launch"] / (k["avg_launch_ms"] * 1e-3) / 1e9
+    return {"kernel": kind, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peaks["source"]}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,63 @@
+// common.cuh -- shared device helpers of libgpt2b300: warp reductions,
+// bf16 rounding, the device-side error word and bounded waits.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define GPT2_DEV __device__ __forceinline__
+
+// Device-side error codes written into the handle's error word.  The host
+// maps them onto the public status codes at the next synchronisation.
+enum DevError : int {
+  DEV_OK = 0,
+  DEV_ERR_TOKEN_RANGE = 1,  // a token id outside [0, V)
+  DEV_ERR_TIMEOUT = 2,      // a bounded mbarrier / flag wait gave up
+  DEV_ERR_SHAPE = 3,        // a kernel was launched with a shape it cannot handle
+};
+
+GPT2_DEV void dev_set_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+GPT2_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+GPT2_DEV float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Round an fp32 value to the nearest bf16 (ties to even) and return it as
+// fp32; NaN stays NaN.
+GPT2_DEV float round_bf16(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7f800000u) == 0x7f800000u) return x;
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return __uint_as_float(u & 0xffff0000u);
+}
+
+GPT2_DEV uint16_t to_bf16_bits(float x) {
+  return (uint16_t)(__float_as_uint(round_bf16(x)) >> 16);
+}
+
+// tanh-form GELU used by GPT-2 and its derivative.
+#define GELU_SQRT_2_OVER_PI 0.7978845608028654f
+#define GELU_COEF 0.044715f
+
+GPT2_DEV float gelu_fwd(float x) {
+  float u = GELU_SQRT_2_OVER_PI * (x + GELU_COEF * x * x * x);
+  return 0.5f * x * (1.0f + tanhf(u));
+}
+
+GPT2_DEV float gelu_grad(float x) {
+  float u = GELU_SQRT_2_OVER_PI * (x + GELU_COEF * x * x * x);
+  float th = tanhf(u);
+  return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * GELU_SQRT_2_OVER_PI * (1.0f + 3.0f * GELU_COEF * x * x);
+}
+
+static inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }

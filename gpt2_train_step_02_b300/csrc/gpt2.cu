@@ -1,0 +1,842 @@
+// gpt2.cu -- the GPT-2 training-step runtime behind the C ABI of
+// include/gpt2b300.h: arena planning and carving, the forward / backward /
+// AdamW kernel sequences on the handle's stream, CUDA-graph replay of whole
+// steps, status codes and host-side validation.
+//
+// Structure follows llm.c's train_gpt2.c as described on the page
+// «llm.c：Andrej Karpathy带你从零复现LLM», section «核心代码解读：train_gpt2.c»
+// (items 1-3: layer functions, model structs, build/forward/zero_grad/
+// backward/update) and the single preallocated buffer of page
+// «千行C代码训完GPT-2», section «纯CUDA也可训».  Unlike the CPU design, the
+// activation arena never stores the (T,T) attention matrices: the attention
+// kernels keep only the per-row log-sum-exp and recompute probabilities in
+// the backward pass.
+#include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <cuda_runtime.h>
+
+#include "../../include/gpt2b300.h"
+#include "common.cuh"
+#include "k_attention_simt.cuh"
+#include "k_gemm_simt.cuh"
+#include "k_layernorm.cuh"
+#include "k_misc.cuh"
+#include "k_xent.cuh"
+
+#define EXPORT extern "C" __attribute__((visibility("default")))
+
+enum {
+  P_WTE, P_WPE, P_LN1W, P_LN1B, P_QKVW, P_QKVB, P_ATTPROJW, P_ATTPROJB,
+  P_LN2W, P_LN2B, P_FCW, P_FCB, P_FCPROJW, P_FCPROJB, P_LNFW, P_LNFB, NUM_PARAMS
+};
+
+// ---------------------------------------------------------------------------
+// arena plan
+// ---------------------------------------------------------------------------
+struct Plan {
+  size_t total;
+  size_t params, grads, m, v, params_bf;
+  size_t encoded, ln1, ln1_mean, ln1_rstd, qkv, atty, lse, res2, ln2, ln2_mean, ln2_rstd, fch, fchg, res3;
+  size_t lnf, lnf_mean, lnf_rstd, logits, dlogits, losses, loss;
+  size_t dres, dln, datty, dqkv, dfch, attD, scratch, sorted, tokens, targets, err, hparams;
+  size_t scratch_floats;
+};
+
+static long long param_count(const gpt2_config* c, long long sizes[NUM_PARAMS]) {
+  long long L = c->num_layers, C = c->channels;
+  long long s[NUM_PARAMS] = {(long long)c->padded_vocab_size * C, (long long)c->max_seq_len * C, L * C, L * C,
+                             L * 3 * C * C, L * 3 * C, L * C * C, L * C, L * C, L * C, L * 4 * C * C, L * 4 * C,
+                             L * C * 4 * C, L * C, C, C};
+  long long n = 0;
+  for (int i = 0; i < NUM_PARAMS; i++) {
+    if (sizes) sizes[i] = s[i];
+    n += s[i];
+  }
+  return n;
+}
+
+static int config_ok(const gpt2_config* c) {
+  if (!c) return 0;
+  if (c->num_layers < 1 || c->channels < 64 || c->num_heads < 1 || c->max_seq_len < 1) return 0;
+  if (c->channels % 64 || c->channels % c->num_heads) return 0;
+  int hs = c->channels / c->num_heads;
+  if (hs != 16 && hs != 32 && hs != 64 && hs != 128) return 0;
+  if (c->channels > 32 * 4 * LN_MAXV4) return 0;
+  if (c->vocab_size < 1 || c->vocab_size > c->padded_vocab_size || c->padded_vocab_size % 64) return 0;
+  if (c->padded_vocab_size > 65536) return 0;
+  if (c->gemm_precision != GPT2_PREC_FP32 && c->gemm_precision != GPT2_PREC_BF16) return 0;
+  return 1;
+}
+
+static int shape_ok(const gpt2_config* c, int maxB, int maxT) {
+  return maxB >= 1 && maxT >= 1 && maxT <= c->max_seq_len && (long long)maxB * maxT <= SORT_MAX;
+}
+
+static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off += (bytes + 255) & ~(size_t)255;
+    return at;
+  };
+  long long np = param_count(c, nullptr);
+  size_t L = c->num_layers, C = c->channels, NH = c->num_heads, Vp = c->padded_vocab_size;
+  size_t BT = (size_t)maxB * maxT;
+  size_t F = sizeof(float);
+  p->params = take(np * F);
+  p->grads = take(np * F);
+  p->m = take(np * F);
+  p->v = take(np * F);
+  p->params_bf = take(c->gemm_precision == GPT2_PREC_BF16 ? np * 2 : 0);
+  p->encoded = take(BT * C * F);
+  p->ln1 = take(L * BT * C * F);
+  p->ln1_mean = take(L * BT * F);
+  p->ln1_rstd = take(L * BT * F);
+  p->qkv = take(L * BT * 3 * C * F);
+  p->atty = take(L * BT * C * F);
+  p->lse = take(L * BT * NH * F);
+  p->res2 = take(L * BT * C * F);
+  p->ln2 = take(L * BT * C * F);
+  p->ln2_mean = take(L * BT * F);
+  p->ln2_rstd = take(L * BT * F);
+  p->fch = take(L * BT * 4 * C * F);
+  p->fchg = take(L * BT * 4 * C * F);
+  p->res3 = take(L * BT * C * F);
+  p->lnf = take(BT * C * F);
+  p->lnf_mean = take(BT * F);
+  p->lnf_rstd = take(BT * F);
+  p->logits = take(BT * Vp * F);
+  p->dlogits = take(BT * Vp * F);
+  p->losses = take(BT * F);
+  p->loss = take(F);
+  p->dres = take(BT * C * F);
+  p->dln = take(BT * C * F);
+  p->datty = take(BT * C * F);
+  p->dqkv = take(BT * 3 * C * F);
+  p->dfch = take(BT * 4 * C * F);
+  p->attD = take(BT * NH * F);
+  // scratch: column-sum partials (<= ceil(BT/64) x 4C) and layernorm
+  // partials (ceil(BT/32) x 2C)
+  size_t s1 = ((BT + 63) / 64) * 4 * C, s2 = ((BT + LNB_ROWS - 1) / LNB_ROWS) * 2 * C;
+  p->scratch_floats = s1 > s2 ? s1 : s2;
+  p->scratch = take(p->scratch_floats * F);
+  p->sorted = take(BT * sizeof(uint32_t));
+  p->tokens = take(BT * sizeof(int));
+  p->targets = take(BT * sizeof(int));
+  p->err = take(sizeof(int));
+  p->hparams = take(16 * F);
+  p->total = off;
+  return off;
+}
+
+// ---------------------------------------------------------------------------
+// the handle
+// ---------------------------------------------------------------------------
+struct gpt2_t {
+  gpt2_config cfg;
+  int maxB, maxT;
+  long long np;
+  long long psize[NUM_PARAMS];
+  Plan plan;
+  char* arena;
+  int own_arena;
+  cudaStream_t stream;
+  float *params, *grads, *m, *v;
+  uint16_t* params_bf;
+  float* P[NUM_PARAMS];
+  float* G[NUM_PARAMS];
+  float *encoded, *ln1, *ln1_mean, *ln1_rstd, *qkv, *atty, *lse, *res2, *ln2, *ln2_mean, *ln2_rstd, *fch, *fchg,
+      *res3;
+  float *lnf, *lnf_mean, *lnf_rstd, *logits, *dlogits, *losses, *loss;
+  float *dres, *dln, *datty, *dqkv, *dfch, *attD, *scratch;
+  uint32_t* sorted;
+  int *tokens, *targets, *err;
+  float* hparams;
+  int B, T, have_targets, fwd_done;
+  int poisoned;
+  long long launches;
+  // graph replay of whole steps
+  cudaGraphExec_t gexec;
+  int gB, gT;
+  long long g_launches;
+  int capturing;
+  // kernel timer: event pairs around every launch of one kernel class
+  int timer_kind;
+  cudaEvent_t* tev;
+  double* twork;
+  int tcap, tused;
+  double t_ms, t_work;
+  long long t_launches;
+};
+
+// Kernel classes the timer can bracket.
+enum TimerKind { TK_NONE = 0, TK_GEMM = 1, TK_ADAMW = 2, TK_XENT = 3, TK_ATTN_FWD = 4, TK_ATTN_BWD = 5,
+                 TK_LAYERNORM = 6, TK_ENCODER = 7 };
+
+static void timer_drain(gpt2_t* m) {
+  if (!m->tused) return;
+  cudaEventSynchronize(m->tev[2 * m->tused - 1]);
+  for (int i = 0; i < m->tused; i++) {
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, m->tev[2 * i], m->tev[2 * i + 1]);
+    m->t_ms += ms;
+    m->t_work += m->twork[i];
+    m->t_launches++;
+  }
+  m->tused = 0;
+}
+
+static inline void timer_begin(gpt2_t* m, int kind, double work) {
+  if (m->timer_kind != kind || m->capturing || !m->tev) return;
+  if (m->tused == m->tcap) timer_drain(m);
+  m->twork[m->tused] = work;
+  cudaEventRecord(m->tev[2 * m->tused], m->stream);
+}
+
+static inline void timer_end(gpt2_t* m, int kind) {
+  if (m->timer_kind != kind || m->capturing || !m->tev) return;
+  cudaEventRecord(m->tev[2 * m->tused + 1], m->stream);
+  m->tused++;
+}
+
+#define KCHECK(m)                                  \
+  do {                                             \
+    cudaError_t e_ = cudaGetLastError();           \
+    if (e_ != cudaSuccess) {                       \
+      (m)->poisoned = GPT2_ERR_CUDA;               \
+      fprintf(stderr, "gpt2b300: %s (%s:%d)\n", cudaGetErrorString(e_), __FILE__, __LINE__); \
+      return GPT2_ERR_CUDA;                        \
+    }                                              \
+  } while (0)
+
+#define CCHECK(m, call)                            \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) {                       \
+      (m)->poisoned = GPT2_ERR_CUDA;               \
+      fprintf(stderr, "gpt2b300: %s (%s:%d)\n", cudaGetErrorString(e_), __FILE__, __LINE__); \
+      return GPT2_ERR_CUDA;                        \
+    }                                              \
+  } while (0)
+
+static int grid_for(long long n, int threads, int cap = 148 * 16) {
+  long long g = (n + threads - 1) / threads;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
+// ---------------------------------------------------------------------------
+// matmul helpers for a linear layer y = x W^T + b with x (N, IC), W (OC, IC)
+// ---------------------------------------------------------------------------
+static void mm_forward(gpt2_t* m, float* out, const float* x, const float* W, const float* bias, int N, int IC, int OC,
+                       int epi, const float* R, float* pre) {
+  GemmArgs a = {};
+  a.M = N; a.N = OC; a.K = IC;
+  a.A = x; a.a_rs = IC; a.a_cs = 1;
+  a.B = W; a.b_rs = 1; a.b_cs = IC;
+  a.C = out; a.ldc = OC;
+  a.bias = bias; a.R = R; a.ldr = OC; a.pre = pre; a.ldpre = OC;
+  a.epi = epi;
+  a.bf16_ops = m->cfg.gemm_precision == GPT2_PREC_BF16;
+  timer_begin(m, TK_GEMM, 2.0 * N * (double)IC * OC);
+  gemm_simt_launch(a, m->stream);
+  timer_end(m, TK_GEMM);
+  m->launches++;
+}
+
+// dx = dy W (optionally times gelu'(pre))
+static void mm_dx(gpt2_t* m, float* dx, const float* dy, const float* W, int N, int IC, int OC, const float* pre) {
+  GemmArgs a = {};
+  a.M = N; a.N = IC; a.K = OC;
+  a.A = dy; a.a_rs = OC; a.a_cs = 1;
+  a.B = W; a.b_rs = IC; a.b_cs = 1;
+  a.C = dx; a.ldc = IC;
+  a.R = pre; a.ldr = IC;
+  a.epi = pre ? EPI_DGELU : EPI_STORE;
+  a.bf16_ops = m->cfg.gemm_precision == GPT2_PREC_BF16;
+  timer_begin(m, TK_GEMM, 2.0 * N * (double)IC * OC);
+  gemm_simt_launch(a, m->stream);
+  timer_end(m, TK_GEMM);
+  m->launches++;
+}
+
+// dW += dy^T x
+static void mm_dw(gpt2_t* m, float* dW, const float* dy, const float* x, int N, int IC, int OC) {
+  GemmArgs a = {};
+  a.M = OC; a.N = IC; a.K = N;
+  a.A = dy; a.a_rs = 1; a.a_cs = OC;
+  a.B = x; a.b_rs = IC; a.b_cs = 1;
+  a.C = dW; a.ldc = IC;
+  a.epi = EPI_ACCUM;
+  a.bf16_ops = m->cfg.gemm_precision == GPT2_PREC_BF16;
+  timer_begin(m, TK_GEMM, 2.0 * N * (double)IC * OC);
+  gemm_simt_launch(a, m->stream);
+  timer_end(m, TK_GEMM);
+  m->launches++;
+}
+
+// db += column sums of dy (N, OC)
+static void bias_grad(gpt2_t* m, float* db, const float* dy, int N, int OC) {
+  int rows = 64;
+  int chunks = ceil_div(N, rows);
+  col_partial_kernel<<<dim3(ceil_div(OC, 256), chunks), 256, 0, m->stream>>>(dy, N, OC, OC, rows, m->scratch);
+  col_finish_kernel<<<ceil_div(OC, 256), 256, 0, m->stream>>>(m->scratch, chunks, OC, db);
+  m->launches += 2;
+}
+
+static void ln_forward(gpt2_t* m, float* y, float* mean, float* rstd, const float* x, const float* w, const float* b,
+                       int N) {
+  int C = m->cfg.channels;
+  layernorm_fwd_kernel<<<ceil_div(N, 8), 256, 0, m->stream>>>(y, nullptr, mean, rstd, x, w, b, N, C);
+  m->launches++;
+}
+
+static void ln_backward(gpt2_t* m, float* dx, float* dw, float* db, const float* dy, const float* x, const float* w,
+                        const float* mean, const float* rstd, int N) {
+  int C = m->cfg.channels;
+  int nb = ceil_div(N, LNB_ROWS);
+  layernorm_bwd_kernel<<<nb, LNB_WARPS * 32, 2 * C * sizeof(float), m->stream>>>(dx, m->scratch, dy, x, w, mean,
+                                                                                    rstd, N, C);
+  layernorm_param_grad_kernel<<<ceil_div(C, 256), 256, 0, m->stream>>>(dw, db, m->scratch, nb, C);
+  m->launches += 2;
+}
+
+// ---------------------------------------------------------------------------
+// the three phases
+// ---------------------------------------------------------------------------
+static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, int T, int validate) {
+  const gpt2_config& c = m->cfg;
+  int L = c.num_layers, C = c.channels, NH = c.num_heads, V = c.vocab_size, Vp = c.padded_vocab_size;
+  int N = B * T;
+  size_t cap = (size_t)m->maxB * m->maxT;  // per-layer stride in rows
+  cudaStream_t s = m->stream;
+  int bf = c.gemm_precision == GPT2_PREC_BF16;
+  if (validate) {
+    validate_tokens_kernel<<<grid_for(N, 256, 64), 256, 0, s>>>(d_in, d_tgt, N, V, m->err);
+    m->launches++;
+  }
+  encoder_fwd_kernel<<<grid_for((long long)N * C / 4, 256), 256, 0, s>>>(m->encoded, d_in, m->P[P_WTE], m->P[P_WPE],
+                                                                          N, T, C, V);
+  m->launches++;
+  for (int l = 0; l < L; l++) {
+    const float* x = l == 0 ? m->encoded : m->res3 + (size_t)(l - 1) * cap * C;
+    float* ln1 = m->ln1 + (size_t)l * cap * C;
+    float* qkv = m->qkv + (size_t)l * cap * 3 * C;
+    float* atty = m->atty + (size_t)l * cap * C;
+    float* lse = m->lse + (size_t)l * cap * NH;
+    float* res2 = m->res2 + (size_t)l * cap * C;
+    float* ln2 = m->ln2 + (size_t)l * cap * C;
+    float* fch = m->fch + (size_t)l * cap * 4 * C;
+    float* fchg = m->fchg + (size_t)l * cap * 4 * C;
+    float* res3 = m->res3 + (size_t)l * cap * C;
+    ln_forward(m, ln1, m->ln1_mean + (size_t)l * cap, m->ln1_rstd + (size_t)l * cap, x, m->P[P_LN1W] + (size_t)l * C,
+               m->P[P_LN1B] + (size_t)l * C, N);
+    mm_forward(m, qkv, ln1, m->P[P_QKVW] + (size_t)l * 3 * C * C, m->P[P_QKVB] + (size_t)l * 3 * C, N, C, 3 * C,
+               EPI_BIAS, nullptr, nullptr);
+    attn_fwd_simt_kernel<<<ceil_div((long long)B * NH * T * 32, 256), 256, 0, s>>>(atty, lse, qkv, B, T, C, NH, bf);
+    m->launches++;
+    mm_forward(m, res2, atty, m->P[P_ATTPROJW] + (size_t)l * C * C, m->P[P_ATTPROJB] + (size_t)l * C, N, C, C,
+               EPI_BIAS_RESID, x, nullptr);
+    ln_forward(m, ln2, m->ln2_mean + (size_t)l * cap, m->ln2_rstd + (size_t)l * cap, res2,
+               m->P[P_LN2W] + (size_t)l * C, m->P[P_LN2B] + (size_t)l * C, N);
+    mm_forward(m, fchg, ln2, m->P[P_FCW] + (size_t)l * 4 * C * C, m->P[P_FCB] + (size_t)l * 4 * C, N, C, 4 * C,
+               EPI_BIAS_GELU, nullptr, fch);
+    mm_forward(m, res3, fchg, m->P[P_FCPROJW] + (size_t)l * 4 * C * C, m->P[P_FCPROJB] + (size_t)l * C, N, 4 * C, C,
+               EPI_BIAS_RESID, res2, nullptr);
+  }
+  ln_forward(m, m->lnf, m->lnf_mean, m->lnf_rstd, m->res3 + (size_t)(L - 1) * cap * C, m->P[P_LNFW], m->P[P_LNFB], N);
+  mm_forward(m, m->logits, m->lnf, m->P[P_WTE], nullptr, N, C, Vp, EPI_STORE, nullptr, nullptr);
+  if (d_tgt) {
+    timer_begin(m, TK_XENT, 8.0 * (double)N * Vp);
+    xent_fused_kernel<<<N, XENT_THREADS, 0, s>>>(m->dlogits, nullptr, m->losses, m->logits, d_tgt, V, Vp,
+                                                 1.0f / (float)N);
+    timer_end(m, TK_XENT);
+    mean_kernel<<<1, 1024, 0, s>>>(m->losses, N, m->loss);
+    m->launches += 2;
+  }
+  KCHECK(m);
+  m->B = B;
+  m->T = T;
+  m->have_targets = d_tgt != nullptr;
+  m->fwd_done = 1;
+  return GPT2_OK;
+}
+
+static int enqueue_backward(gpt2_t* m) {
+  const gpt2_config& c = m->cfg;
+  int L = c.num_layers, C = c.channels, NH = c.num_heads, Vp = c.padded_vocab_size;
+  int B = m->B, T = m->T, N = B * T;
+  size_t cap = (size_t)m->maxB * m->maxT;
+  cudaStream_t s = m->stream;
+  int bf = c.gemm_precision == GPT2_PREC_BF16;
+  float** P = m->P;
+  float** G = m->G;
+  // LM head (tied to wte): dlnf = dlogits wte; dwte += dlogits^T lnf
+  mm_dx(m, m->dln, m->dlogits, P[P_WTE], N, C, Vp, nullptr);
+  mm_dw(m, G[P_WTE], m->dlogits, m->lnf, N, C, Vp);
+  CCHECK(m, cudaMemsetAsync(m->dres, 0, (size_t)N * C * sizeof(float), s));
+  ln_backward(m, m->dres, G[P_LNFW], G[P_LNFB], m->dln, m->res3 + (size_t)(L - 1) * cap * C, P[P_LNFW], m->lnf_mean,
+              m->lnf_rstd, N);
+  for (int l = L - 1; l >= 0; l--) {
+    const float* x = l == 0 ? m->encoded : m->res3 + (size_t)(l - 1) * cap * C;
+    float* ln1 = m->ln1 + (size_t)l * cap * C;
+    float* qkv = m->qkv + (size_t)l * cap * 3 * C;
+    float* atty = m->atty + (size_t)l * cap * C;
+    float* lse = m->lse + (size_t)l * cap * NH;
+    float* res2 = m->res2 + (size_t)l * cap * C;
+    float* ln2 = m->ln2 + (size_t)l * cap * C;
+    float* fch = m->fch + (size_t)l * cap * 4 * C;
+    float* fchg = m->fchg + (size_t)l * cap * 4 * C;
+    // MLP output projection: res3 = res2 + fchg fcprojw^T + fcprojb
+    mm_dw(m, G[P_FCPROJW] + (size_t)l * 4 * C * C, m->dres, fchg, N, 4 * C, C);
+    bias_grad(m, G[P_FCPROJB] + (size_t)l * C, m->dres, N, C);
+    mm_dx(m, m->dfch, m->dres, P[P_FCPROJW] + (size_t)l * 4 * C * C, N, 4 * C, C, fch);  // x gelu'(fch)
+    // MLP input projection: fch = ln2 fcw^T + fcb
+    mm_dw(m, G[P_FCW] + (size_t)l * 4 * C * C, m->dfch, ln2, N, C, 4 * C);
+    bias_grad(m, G[P_FCB] + (size_t)l * 4 * C, m->dfch, N, 4 * C);
+    mm_dx(m, m->dln, m->dfch, P[P_FCW] + (size_t)l * 4 * C * C, N, C, 4 * C, nullptr);
+    ln_backward(m, m->dres, G[P_LN2W] + (size_t)l * C, G[P_LN2B] + (size_t)l * C, m->dln, res2,
+                P[P_LN2W] + (size_t)l * C, m->ln2_mean + (size_t)l * cap, m->ln2_rstd + (size_t)l * cap, N);
+    // attention output projection: res2 = x + atty attprojw^T + attprojb
+    mm_dw(m, G[P_ATTPROJW] + (size_t)l * C * C, m->dres, atty, N, C, C);
+    bias_grad(m, G[P_ATTPROJB] + (size_t)l * C, m->dres, N, C);
+    mm_dx(m, m->datty, m->dres, P[P_ATTPROJW] + (size_t)l * C * C, N, C, C, nullptr);
+    // attention
+    int nw = B * NH * T;
+    attn_bwd_D_kernel<<<ceil_div((long long)nw * 32, 256), 256, 0, s>>>(m->attD, m->datty, atty, B, T, C, NH);
+    attn_bwd_dq_kernel<<<ceil_div((long long)nw * 32, 256), 256, 0, s>>>(m->dqkv, qkv, m->datty, lse, m->attD, B, T,
+                                                                        C, NH, bf);
+    attn_bwd_dkv_kernel<<<ceil_div((long long)nw * 32, 256), 256, 0, s>>>(m->dqkv, qkv, m->datty, lse, m->attD, B,
+                                                                         T, C, NH, bf);
+    m->launches += 3;
+    // qkv projection: qkv = ln1 qkvw^T + qkvb
+    mm_dw(m, G[P_QKVW] + (size_t)l * 3 * C * C, m->dqkv, ln1, N, C, 3 * C);
+    bias_grad(m, G[P_QKVB] + (size_t)l * 3 * C, m->dqkv, N, 3 * C);
+    mm_dx(m, m->dln, m->dqkv, P[P_QKVW] + (size_t)l * 3 * C * C, N, C, 3 * C, nullptr);
+    ln_backward(m, m->dres, G[P_LN1W] + (size_t)l * C, G[P_LN1B] + (size_t)l * C, m->dln, x,
+                P[P_LN1W] + (size_t)l * C, m->ln1_mean + (size_t)l * cap, m->ln1_rstd + (size_t)l * cap, N);
+  }
+  // embeddings
+  size_t smem = 1;
+  while ((int)smem < N) smem <<= 1;
+  sort_tokens_kernel<<<1, 1024, smem * sizeof(uint32_t), s>>>(m->tokens, N, c.vocab_size, m->sorted);
+  wte_grad_kernel<<<dim3(N, ceil_div(C, 128)), 32, 0, s>>>(G[P_WTE], m->dres, m->sorted, N, C);
+  wpe_grad_kernel<<<grid_for((long long)T * C / 4, 256), 256, 0, s>>>(G[P_WPE], m->dres, B, T, C);
+  m->launches += 3;
+  KCHECK(m);
+  return GPT2_OK;
+}
+
+// AdamW hyper-parameters live in device memory so that a captured step can
+// be replayed with a new step number: {lr, b1, b2, eps, wd, 1/(1-b1^t), 1/(1-b2^t)}.
+static int write_hparams(gpt2_t* m, float lr, float b1, float b2, float eps, float wd, int t) {
+  double c1 = 1.0 - pow((double)b1, t), c2 = 1.0 - pow((double)b2, t);
+  float h[8] = {lr, b1, b2, eps, wd, (float)(1.0 / c1), (float)(1.0 / c2), 0.f};
+  // pageable source: the copy is staged before the call returns, so h may go out of scope
+  CCHECK(m, cudaMemcpyAsync(m->hparams, h, sizeof(h), cudaMemcpyHostToDevice, m->stream));
+  return GPT2_OK;
+}
+
+static int enqueue_update(gpt2_t* m) {
+  long long n4 = m->np / 4;
+  timer_begin(m, TK_ADAMW, 28.0 * (double)m->np + (m->params_bf ? 2.0 * (double)m->np : 0.0));
+  adamw_kernel<<<grid_for(n4, 256, 148 * 8), 256, 0, m->stream>>>(m->params, m->grads, m->m, m->v, n4, m->hparams,
+                                                                   m->params_bf);
+  timer_end(m, TK_ADAMW);
+  m->launches++;
+  KCHECK(m);
+  return GPT2_OK;
+}
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+EXPORT size_t gpt2_arena_bytes(const gpt2_config* cfg, int maxB, int maxT) {
+  if (!config_ok(cfg) || !shape_ok(cfg, maxB, maxT)) return 0;
+  Plan p;
+  return plan_arena(cfg, maxB, maxT, &p);
+}
+
+EXPORT const char* gpt2_status_string(int s) {
+  switch (s) {
+    case GPT2_OK: return "ok";
+    case GPT2_ERR_ARG: return "invalid argument";
+    case GPT2_ERR_SHAPE: return "invalid shape (B, T outside the handle's limits)";
+    case GPT2_ERR_TOKEN_RANGE: return "token id outside [0, vocab_size)";
+    case GPT2_ERR_STATE: return "backward without a forward that had targets";
+    case GPT2_ERR_ARENA: return "arena too small or misaligned";
+    case GPT2_ERR_CUDA: return "CUDA error (handle poisoned)";
+    case GPT2_ERR_DEVICE_TIMEOUT: return "device-side wait timed out (handle poisoned)";
+    case GPT2_WARN_NONFINITE: return "loss is not finite";
+    default: return "unknown status";
+  }
+}
+
+static void carve(gpt2_t* m) {
+  char* a = m->arena;
+  const Plan& p = m->plan;
+  m->params = (float*)(a + p.params);
+  m->grads = (float*)(a + p.grads);
+  m->m = (float*)(a + p.m);
+  m->v = (float*)(a + p.v);
+  m->params_bf = m->cfg.gemm_precision == GPT2_PREC_BF16 ? (uint16_t*)(a + p.params_bf) : nullptr;
+  long long off = 0;
+  for (int i = 0; i < NUM_PARAMS; i++) {
+    m->P[i] = m->params + off;
+    m->G[i] = m->grads + off;
+    off += m->psize[i];
+  }
+#define CARVE(f) m->f = (decltype(m->f))(a + p.f)
+  CARVE(encoded); CARVE(ln1); CARVE(ln1_mean); CARVE(ln1_rstd); CARVE(qkv); CARVE(atty); CARVE(lse);
+  CARVE(res2); CARVE(ln2); CARVE(ln2_mean); CARVE(ln2_rstd); CARVE(fch); CARVE(fchg); CARVE(res3);
+  CARVE(lnf); CARVE(lnf_mean); CARVE(lnf_rstd); CARVE(logits); CARVE(dlogits); CARVE(losses); CARVE(loss);
+  CARVE(dres); CARVE(dln); CARVE(datty); CARVE(dqkv); CARVE(dfch); CARVE(attD); CARVE(scratch); CARVE(sorted);
+  CARVE(tokens); CARVE(targets); CARVE(err); CARVE(hparams);
+#undef CARVE
+}
+
+static int init_params(gpt2_t* m, uint64_t seed) {
+  const gpt2_config& c = m->cfg;
+  float proj = 0.02f / sqrtf(2.0f * c.num_layers);
+  long long off = 0;
+  for (int i = 0; i < NUM_PARAMS; i++) {
+    long long n = m->psize[i], nrand = 0;
+    float stdv = 0.f, fill = 0.f;
+    switch (i) {
+      case P_WTE: nrand = (long long)c.vocab_size * c.channels; stdv = 0.02f; break;
+      case P_WPE: case P_QKVW: case P_FCW: nrand = n; stdv = 0.02f; break;
+      case P_ATTPROJW: case P_FCPROJW: nrand = n; stdv = proj; break;
+      case P_LN1W: case P_LN2W: case P_LNFW: fill = 1.f; break;
+      default: break;
+    }
+    init_tensor_kernel<<<grid_for(n, 256), 256, 0, m->stream>>>(m->P[i], off, n, nrand, stdv, fill, seed);
+    off += n;
+  }
+  KCHECK(m);
+  return GPT2_OK;
+}
+
+static int refresh_bf16(gpt2_t* m) {
+  if (!m->params_bf) return GPT2_OK;
+  to_bf16_kernel<<<grid_for(m->np, 256), 256, 0, m->stream>>>(m->params, m->params_bf, m->np);
+  KCHECK(m);
+  return GPT2_OK;
+}
+
+EXPORT int gpt2_build(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, int maxB, int maxT, void* dev_arena,
+                      size_t arena_bytes, void* cuda_stream) {
+  if (!out || !config_ok(cfg)) return GPT2_ERR_ARG;
+  *out = nullptr;
+  if (!shape_ok(cfg, maxB, maxT)) return GPT2_ERR_SHAPE;
+  gpt2_t* m = (gpt2_t*)calloc(1, sizeof(gpt2_t));
+  if (!m) return GPT2_ERR_ARG;
+  m->cfg = *cfg;
+  m->maxB = maxB;
+  m->maxT = maxT;
+  m->np = param_count(cfg, m->psize);
+  size_t need = plan_arena(cfg, maxB, maxT, &m->plan);
+  m->stream = (cudaStream_t)cuda_stream;
+  if (dev_arena) {
+    if (arena_bytes < need || ((uintptr_t)dev_arena & 255)) {
+      free(m);
+      return GPT2_ERR_ARENA;
+    }
+    m->arena = (char*)dev_arena;
+  } else {
+    if (cudaMalloc((void**)&m->arena, need) != cudaSuccess) {
+      cudaGetLastError();
+      free(m);
+      return GPT2_ERR_CUDA;
+    }
+    m->own_arena = 1;
+  }
+  carve(m);
+  int rc;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(sort_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SORT_MAX * (int)sizeof(uint32_t))) != cudaSuccess)
+    goto cuda_fail;
+  if ((e = cudaMemsetAsync(m->grads, 0, m->np * sizeof(float), m->stream)) != cudaSuccess) goto cuda_fail;
+  if ((e = cudaMemsetAsync(m->m, 0, m->np * sizeof(float), m->stream)) != cudaSuccess) goto cuda_fail;
+  if ((e = cudaMemsetAsync(m->v, 0, m->np * sizeof(float), m->stream)) != cudaSuccess) goto cuda_fail;
+  if ((e = cudaMemsetAsync(m->err, 0, sizeof(int), m->stream)) != cudaSuccess) goto cuda_fail;
+  if ((rc = init_params(m, seed)) != GPT2_OK) goto fail;
+  if ((rc = refresh_bf16(m)) != GPT2_OK) goto fail;
+  if ((e = cudaStreamSynchronize(m->stream)) != cudaSuccess) goto cuda_fail;
+  *out = m;
+  return GPT2_OK;
+cuda_fail:
+  fprintf(stderr, "gpt2b300: build failed: %s\n", cudaGetErrorString(e));
+  cudaGetLastError();
+  rc = GPT2_ERR_CUDA;
+fail:
+  if (m->own_arena) cudaFree(m->arena);
+  free(m);
+  return rc;
+}
+
+EXPORT int gpt2_free(gpt2_t* m) {
+  if (!m) return GPT2_ERR_ARG;
+  cudaStreamSynchronize(m->stream);
+  if (m->gexec) cudaGraphExecDestroy(m->gexec);
+  if (m->tev) {
+    for (int i = 0; i < 2 * m->tcap; i++) cudaEventDestroy(m->tev[i]);
+    free(m->tev);
+    free(m->twork);
+  }
+  if (m->own_arena) cudaFree(m->arena);
+  free(m);
+  return GPT2_OK;
+}
+
+static int check_shape(gpt2_t* m, int B, int T) {
+  if (B < 1 || T < 1 || B > m->maxB || T > m->maxT || T > m->cfg.max_seq_len) return GPT2_ERR_SHAPE;
+  return GPT2_OK;
+}
+
+static int read_device_status(gpt2_t* m) {
+  int err = 0;
+  CCHECK(m, cudaStreamSynchronize(m->stream));
+  CCHECK(m, cudaMemcpy(&err, m->err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (err == DEV_OK) return GPT2_OK;
+  CCHECK(m, cudaMemset(m->err, 0, sizeof(int)));
+  if (err == DEV_ERR_TOKEN_RANGE) return GPT2_ERR_TOKEN_RANGE;
+  if (err == DEV_ERR_TIMEOUT) {
+    m->poisoned = GPT2_ERR_DEVICE_TIMEOUT;
+    return GPT2_ERR_DEVICE_TIMEOUT;
+  }
+  return GPT2_ERR_SHAPE;
+}
+
+EXPORT int gpt2_sync(gpt2_t* m, float* loss_out) {
+  if (!m) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  int rc = read_device_status(m);
+  if (rc != GPT2_OK) return rc;
+  if (loss_out) {
+    if (!m->have_targets) {
+      *loss_out = -1.0f;
+      return GPT2_OK;
+    }
+    CCHECK(m, cudaMemcpy(loss_out, m->loss, sizeof(float), cudaMemcpyDeviceToHost));
+    if (!isfinite(*loss_out)) return GPT2_WARN_NONFINITE;
+  }
+  return GPT2_OK;
+}
+
+EXPORT int gpt2_forward(gpt2_t* m, const int32_t* inputs, const int32_t* targets, int B, int T, float* loss_out) {
+  if (!m || !inputs) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  int rc = check_shape(m, B, T);
+  if (rc) return rc;
+  int N = B * T, V = m->cfg.vocab_size;
+  for (int i = 0; i < N; i++) {
+    if (inputs[i] < 0 || inputs[i] >= V) return GPT2_ERR_TOKEN_RANGE;
+    if (targets && (targets[i] < 0 || targets[i] >= V)) return GPT2_ERR_TOKEN_RANGE;
+  }
+  m->launches = 0;
+  CCHECK(m, cudaMemcpyAsync(m->tokens, inputs, N * sizeof(int), cudaMemcpyHostToDevice, m->stream));
+  if (targets) CCHECK(m, cudaMemcpyAsync(m->targets, targets, N * sizeof(int), cudaMemcpyHostToDevice, m->stream));
+  rc = enqueue_forward(m, m->tokens, targets ? m->targets : nullptr, B, T, 0);
+  if (rc) return rc;
+  if (loss_out) return gpt2_sync(m, loss_out);
+  return GPT2_OK;
+}
+
+EXPORT int gpt2_forward_device(gpt2_t* m, const int32_t* d_inputs, const int32_t* d_targets, int B, int T) {
+  if (!m || !d_inputs) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  int rc = check_shape(m, B, T);
+  if (rc) return rc;
+  int N = B * T;
+  m->launches = 0;
+  // stage into the handle's buffers: the embedding backward reads the ids later
+  if (d_inputs != m->tokens)
+    CCHECK(m, cudaMemcpyAsync(m->tokens, d_inputs, N * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+  if (d_targets && d_targets != m->targets)
+    CCHECK(m, cudaMemcpyAsync(m->targets, d_targets, N * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+  return enqueue_forward(m, m->tokens, d_targets ? m->targets : nullptr, B, T, 1);
+}
+
+EXPORT int gpt2_zero_grad(gpt2_t* m) {
+  if (!m) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  m->launches = 0;
+  CCHECK(m, cudaMemsetAsync(m->grads, 0, m->np * sizeof(float), m->stream));
+  return GPT2_OK;
+}
+
+EXPORT int gpt2_backward(gpt2_t* m) {
+  if (!m) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  if (!m->fwd_done || !m->have_targets) return GPT2_ERR_STATE;
+  m->launches = 0;
+  return enqueue_backward(m);
+}
+
+EXPORT int gpt2_update(gpt2_t* m, float lr, float beta1, float beta2, float eps, float weight_decay, int t) {
+  if (!m || t < 1) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  m->launches = 0;
+  int rc = write_hparams(m, lr, beta1, beta2, eps, weight_decay, t);
+  return rc ? rc : enqueue_update(m);
+}
+
+// forward (device-side token check) -> zero_grad -> backward -> AdamW, all
+// reading the staged tokens and the device-resident hyper-parameters.
+static int enqueue_step(gpt2_t* m, int B, int T) {
+  int rc;
+  if ((rc = enqueue_forward(m, m->tokens, m->targets, B, T, 1))) return rc;
+  CCHECK(m, cudaMemsetAsync(m->grads, 0, m->np * sizeof(float), m->stream));
+  if ((rc = enqueue_backward(m))) return rc;
+  return enqueue_update(m);
+}
+
+static int run_step(gpt2_t* m, int B, int T, int use_graph) {
+  m->launches = 0;
+  // the legacy default stream cannot be captured; the timer needs direct launches
+  if (!use_graph || m->stream == nullptr || m->timer_kind != TK_NONE) return enqueue_step(m, B, T);
+  if (!m->gexec || m->gB != B || m->gT != T) {
+    if (m->gexec) {
+      cudaGraphExecDestroy(m->gexec);
+      m->gexec = nullptr;
+    }
+    CCHECK(m, cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
+    m->capturing = 1;
+    int rc = enqueue_step(m, B, T);
+    m->capturing = 0;
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamEndCapture(m->stream, &g);
+    if (rc) {
+      if (g) cudaGraphDestroy(g);
+      return rc;
+    }
+    CCHECK(m, e);
+    e = cudaGraphInstantiate(&m->gexec, g, 0);
+    cudaGraphDestroy(g);
+    CCHECK(m, e);
+    m->gB = B;
+    m->gT = T;
+    m->g_launches = m->launches;
+  }
+  CCHECK(m, cudaGraphLaunch(m->gexec, m->stream));
+  m->launches = m->g_launches;
+  m->B = B;
+  m->T = T;
+  m->have_targets = 1;
+  m->fwd_done = 1;
+  return GPT2_OK;
+}
+
+EXPORT int gpt2_train_step_device(gpt2_t* m, const int32_t* d_inputs, const int32_t* d_targets, int B, int T,
+                                  float lr, float beta1, float beta2, float eps, float weight_decay, int t,
+                                  int use_graph) {
+  if (!m || !d_inputs || !d_targets || t < 1) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  int rc = check_shape(m, B, T);
+  if (rc) return rc;
+  int N = B * T;
+  if (d_inputs != m->tokens)
+    CCHECK(m, cudaMemcpyAsync(m->tokens, d_inputs, N * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+  if (d_targets != m->targets)
+    CCHECK(m, cudaMemcpyAsync(m->targets, d_targets, N * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+  if ((rc = write_hparams(m, lr, beta1, beta2, eps, weight_decay, t))) return rc;
+  return run_step(m, B, T, use_graph);
+}
+
+EXPORT int gpt2_train_step(gpt2_t* m, const int32_t* inputs, const int32_t* targets, int B, int T, float lr,
+                           float beta1, float beta2, float eps, float weight_decay, int t, float* loss_out) {
+  if (!m || !inputs || !targets || t < 1) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  int rc = check_shape(m, B, T);
+  if (rc) return rc;
+  int N = B * T, V = m->cfg.vocab_size;
+  for (int i = 0; i < N; i++)
+    if (inputs[i] < 0 || inputs[i] >= V || targets[i] < 0 || targets[i] >= V) return GPT2_ERR_TOKEN_RANGE;
+  CCHECK(m, cudaMemcpyAsync(m->tokens, inputs, N * sizeof(int), cudaMemcpyHostToDevice, m->stream));
+  CCHECK(m, cudaMemcpyAsync(m->targets, targets, N * sizeof(int), cudaMemcpyHostToDevice, m->stream));
+  if ((rc = write_hparams(m, lr, beta1, beta2, eps, weight_decay, t))) return rc;
+  if ((rc = run_step(m, B, T, 1))) return rc;
+  return gpt2_sync(m, loss_out);
+}
+
+EXPORT int gpt2_kernel_timer(gpt2_t* m, int kind) {
+  if (!m || kind < 0 || kind > TK_ENCODER) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  if (!m->tev) {
+    m->tcap = 4096;
+    m->tev = (cudaEvent_t*)calloc(2 * m->tcap, sizeof(cudaEvent_t));
+    m->twork = (double*)calloc(m->tcap, sizeof(double));
+    for (int i = 0; i < 2 * m->tcap; i++) CCHECK(m, cudaEventCreate(&m->tev[i]));
+  }
+  timer_drain(m);
+  m->timer_kind = kind;
+  m->t_ms = 0.0;
+  m->t_work = 0.0;
+  m->t_launches = 0;
+  return GPT2_OK;
+}
+
+EXPORT int gpt2_kernel_timer_read(gpt2_t* m, double* total_ms, long long* launches, double* total_work) {
+  if (!m || !total_ms || !launches || !total_work) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  timer_drain(m);
+  *total_ms = m->t_ms;
+  *launches = m->t_launches;
+  *total_work = m->t_work;
+  return GPT2_OK;
+}
+
+EXPORT long long gpt2_num_parameters(const gpt2_t* m) { return m ? m->np : -1; }
+
+EXPORT long long gpt2_last_launch_count(const gpt2_t* m) { return m ? m->launches : -1; }
+
+static int copy_flat(gpt2_t* m, void* dst, const void* src, long long n, cudaMemcpyKind kind) {
+  if (!m || !dst || !src) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  if (n != m->np) return GPT2_ERR_ARG;
+  CCHECK(m, cudaStreamSynchronize(m->stream));
+  CCHECK(m, cudaMemcpy(dst, src, n * sizeof(float), kind));
+  return GPT2_OK;
+}
+
+EXPORT int gpt2_get_params(gpt2_t* m, float* host, long long n) {
+  return copy_flat(m, host, m ? m->params : nullptr, n, cudaMemcpyDeviceToHost);
+}
+
+EXPORT int gpt2_set_params(gpt2_t* m, const float* host, long long n) {
+  int rc = copy_flat(m, m ? m->params : nullptr, host, n, cudaMemcpyHostToDevice);
+  if (rc) return rc;
+  rc = refresh_bf16(m);
+  if (rc) return rc;
+  CCHECK(m, cudaStreamSynchronize(m->stream));
+  return GPT2_OK;
+}
+
+EXPORT int gpt2_get_grads(gpt2_t* m, float* host, long long n) {
+  return copy_flat(m, host, m ? m->grads : nullptr, n, cudaMemcpyDeviceToHost);
+}
+
+EXPORT int gpt2_get_opt_state(gpt2_t* m, float* hm, float* hv, long long n) {
+  int rc = copy_flat(m, hm, m ? m->m : nullptr, n, cudaMemcpyDeviceToHost);
+  return rc ? rc : copy_flat(m, hv, m->v, n, cudaMemcpyDeviceToHost);
+}
+
+EXPORT int gpt2_set_opt_state(gpt2_t* m, const float* hm, const float* hv, long long n) {
+  int rc = copy_flat(m, m ? m->m : nullptr, hm, n, cudaMemcpyHostToDevice);
+  return rc ? rc : copy_flat(m, m->v, hv, n, cudaMemcpyHostToDevice);
+}
+
+EXPORT int gpt2_get_logits(gpt2_t* m, float* host, long long n) {
+  if (!m || !host) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  if (!m->fwd_done) return GPT2_ERR_STATE;
+  if (n != (long long)m->B * m->T * m->cfg.padded_vocab_size) return GPT2_ERR_ARG;
+  CCHECK(m, cudaStreamSynchronize(m->stream));
+  CCHECK(m, cudaMemcpy(host, m->logits, n * sizeof(float), cudaMemcpyDeviceToHost));
+  return GPT2_OK;
+}

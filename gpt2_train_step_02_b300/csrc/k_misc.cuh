@@ -1,0 +1,223 @@
+// k_misc.cuh -- parameter init, token validation, embedding forward and
+// backward, AdamW, and deterministic column / scalar reductions.
+#pragma once
+#include "common.cuh"
+
+// ---------------------------------------------------------------------------
+// Parameter init: SplitMix64 (Vigna) draw i of stream `seed` is
+// mix(seed + (i+1) * golden_gamma); uniforms take the top 53 bits; normal i
+// is Box-Muller on the uniform pair (2j, 2j+1), j = i/2, cosine branch for
+// even i and sine branch for odd i.
+// ---------------------------------------------------------------------------
+GPT2_DEV uint64_t splitmix64_at(uint64_t seed, uint64_t i) {
+  uint64_t z = seed + (i + 1ull) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+GPT2_DEV double uniform53_at(uint64_t seed, uint64_t i) {
+  return (double)(splitmix64_at(seed, i) >> 11) * 0x1p-53;
+}
+
+GPT2_DEV double normal_at(uint64_t seed, uint64_t i) {
+  uint64_t j = i >> 1;
+  double u0 = uniform53_at(seed, 2 * j), u1 = uniform53_at(seed, 2 * j + 1);
+  double r = sqrt(-2.0 * log1p(-u0));
+  double a = (2.0 * 3.141592653589793) * u1;
+  return (i & 1) ? r * sin(a) : r * cos(a);
+}
+
+// Fills p[0 .. n) of the flat buffer that starts at flat offset `base`:
+// elements [0, nrand) get std * normal(base + i), the rest `fill`.
+__global__ void init_tensor_kernel(float* p, long long base, long long n, long long nrand, float stdv, float fill,
+                                   uint64_t seed) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    p[i] = i < nrand ? (float)((double)stdv * normal_at(seed, (uint64_t)(base + i))) : fill;
+}
+
+// ---------------------------------------------------------------------------
+// Token ids must lie in [0, V).
+// ---------------------------------------------------------------------------
+__global__ void validate_tokens_kernel(const int* ids, const int* tgt, int n, int V, int* err) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    int a = ids[i];
+    int b = tgt ? tgt[i] : 0;
+    if (a < 0 || a >= V || b < 0 || b >= V) dev_set_error(err, DEV_ERR_TOKEN_RANGE);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Token + position embedding: x[b,t,:] = wte[id,:] + wpe[t,:].  One thread
+// per float4; C % 4 == 0.  Ids are clamped so that a bad id (already flagged
+// by validate_tokens_kernel) cannot read out of bounds.
+// ---------------------------------------------------------------------------
+__global__ void encoder_fwd_kernel(float* __restrict__ x, const int* __restrict__ ids, const float* __restrict__ wte,
+                                   const float* __restrict__ wpe, int BT, int T, int C, int V) {
+  int C4 = C >> 2;
+  long long total = (long long)BT * C4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+    int bt = (int)(i / C4), c4 = (int)(i % C4);
+    int id = min(max(ids[bt], 0), V - 1);
+    int t = bt % T;
+    float4 e = reinterpret_cast<const float4*>(wte + (size_t)id * C)[c4];
+    float4 p = reinterpret_cast<const float4*>(wpe + (size_t)t * C)[c4];
+    reinterpret_cast<float4*>(x + (size_t)bt * C)[c4] = make_float4(e.x + p.x, e.y + p.y, e.z + p.z, e.w + p.w);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Embedding backward, deterministic under skewed token frequencies.
+//  1. sort_tokens_kernel: one CTA bitonic-sorts the keys (id << 14 | pos),
+//     which groups positions by id and keeps them in position order.
+//  2. wte_grad_kernel: the CTA at the first key of each id sums that id's
+//     gradient rows in position order and adds the sum to dwte[id] once.
+//  3. wpe_grad_kernel: dwpe[t] += sum over b of dx[b,t].
+// Limits: B*T <= 16384 and V <= 65536 (keys fit 30 bits).
+// ---------------------------------------------------------------------------
+#define SORT_MAX 16384
+
+__global__ void __launch_bounds__(1024) sort_tokens_kernel(const int* __restrict__ ids, int n, int V,
+                                                          uint32_t* __restrict__ sorted) {
+  extern __shared__ uint32_t keys[];
+  int P = 1;
+  while (P < n) P <<= 1;
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    uint32_t id = i < n ? (uint32_t)min(max(ids[i], 0), V - 1) : 0xFFFFu;
+    keys[i] = i < n ? ((id << 14) | (uint32_t)i) : 0xFFFFFFFFu;
+  }
+  __syncthreads();
+  for (int k = 2; k <= P; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < P; i += blockDim.x) {
+        int l = i ^ j;
+        if (l > i) {
+          uint32_t a = keys[i], b = keys[l];
+          bool up = (i & k) == 0;
+          if ((a > b) == up) {
+            keys[i] = b;
+            keys[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) sorted[i] = keys[i];
+}
+
+// grid: (n, ceil(C/128)); block: 32 threads, one float4 of channels each.
+__global__ void wte_grad_kernel(float* __restrict__ dwte, const float* __restrict__ dx,
+                                const uint32_t* __restrict__ sorted, int n, int C) {
+  int i = blockIdx.x;
+  uint32_t id = sorted[i] >> 14;
+  if (i > 0 && (sorted[i - 1] >> 14) == id) return;
+  int c = (blockIdx.y * 32 + threadIdx.x) * 4;
+  if (c >= C) return;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = i; j < n && (sorted[j] >> 14) == id; j++) {
+    int pos = (int)(sorted[j] & 0x3FFFu);
+    float4 g = *reinterpret_cast<const float4*>(dx + (size_t)pos * C + c);
+    s.x += g.x; s.y += g.y; s.z += g.z; s.w += g.w;
+  }
+  float4* d = reinterpret_cast<float4*>(dwte + (size_t)id * C + c);
+  float4 o = *d;
+  *d = make_float4(o.x + s.x, o.y + s.y, o.z + s.z, o.w + s.w);
+}
+
+__global__ void wpe_grad_kernel(float* __restrict__ dwpe, const float* __restrict__ dx, int B, int T, int C) {
+  int C4 = C >> 2;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T * C4; i += gridDim.x * blockDim.x) {
+    int t = i / C4, c4 = i % C4;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int b = 0; b < B; b++) {
+      float4 g = reinterpret_cast<const float4*>(dx + ((size_t)b * T + t) * C)[c4];
+      s.x += g.x; s.y += g.y; s.z += g.z; s.w += g.w;
+    }
+    float4* d = reinterpret_cast<float4*>(dwpe + (size_t)t * C) + c4;
+    float4 o = *d;
+    *d = make_float4(o.x + s.x, o.y + s.y, o.z + s.z, o.w + s.w);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Deterministic column sums of a (M, N) row-major matrix, in two stages:
+// partial[chunk][col] over row chunks of `rows` rows, then out[col] += the
+// chunk partials summed in chunk order.
+// ---------------------------------------------------------------------------
+__global__ void col_partial_kernel(const float* __restrict__ Y, int M, int N, long long ldy, int rows,
+                                   float* __restrict__ partial) {
+  int col = blockIdx.x * blockDim.x + threadIdx.x;
+  if (col >= N) return;
+  int r0 = blockIdx.y * rows, r1 = min(M, r0 + rows);
+  float s = 0.f;
+  for (int r = r0; r < r1; r++) s += Y[(size_t)r * ldy + col];
+  partial[(size_t)blockIdx.y * N + col] = s;
+}
+
+__global__ void col_finish_kernel(const float* __restrict__ partial, int nchunks, int N, float* __restrict__ out) {
+  int col = blockIdx.x * blockDim.x + threadIdx.x;
+  if (col >= N) return;
+  float s = 0.f;
+  for (int k = 0; k < nchunks; k++) s += partial[(size_t)k * N + col];
+  out[col] += s;
+}
+
+// Mean of n values in a fixed order (one CTA of 1024 threads).
+__global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ x, int n, float* __restrict__ out) {
+  __shared__ float sh[32];
+  float s = 0.f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) s += x[i];
+  s = warp_sum(s);
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? sh[threadIdx.x] : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) out[0] = v / (float)n;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// AdamW over the flat buffers (float4 granularity; n % 4 == 0).  hp holds
+// {lr, beta1, beta2, eps, weight_decay, 1/(1-beta1^t), 1/(1-beta2^t)}.  When pbf16 != NULL the bf16
+// copy of the updated parameters is written too.
+// ---------------------------------------------------------------------------
+__global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
+                             float* __restrict__ v, long long n4, const float* __restrict__ hp,
+                             uint16_t* __restrict__ pbf16) {
+  const float lr = hp[0], b1 = hp[1], b2 = hp[2], eps = hp[3], wd = hp[4], c1inv = hp[5], c2inv = hp[6];
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    float4 pp = reinterpret_cast<float4*>(p)[i];
+    float4 gg = reinterpret_cast<const float4*>(g)[i];
+    float4 mm = reinterpret_cast<float4*>(m)[i];
+    float4 vv = reinterpret_cast<float4*>(v)[i];
+    float* P = &pp.x;
+    const float* G = &gg.x;
+    float* Mm = &mm.x;
+    float* Vv = &vv.x;
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      Mm[k] = b1 * Mm[k] + (1.0f - b1) * G[k];
+      Vv[k] = b2 * Vv[k] + (1.0f - b2) * G[k] * G[k];
+      float mh = Mm[k] * c1inv, vh = Vv[k] * c2inv;
+      P[k] = P[k] - lr * (mh / (sqrtf(vh) + eps) + wd * P[k]);
+    }
+    reinterpret_cast<float4*>(p)[i] = pp;
+    reinterpret_cast<float4*>(m)[i] = mm;
+    reinterpret_cast<float4*>(v)[i] = vv;
+    if (pbf16) {
+      ushort4 o;
+      o.x = to_bf16_bits(pp.x);
+      o.y = to_bf16_bits(pp.y);
+      o.z = to_bf16_bits(pp.z);
+      o.w = to_bf16_bits(pp.w);
+      reinterpret_cast<ushort4*>(pbf16)[i] = o;
+    }
+  }
+}
+
+__global__ void to_bf16_kernel(const float* __restrict__ x, uint16_t* __restrict__ y, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    y[i] = to_bf16_bits(x[i]);
+}

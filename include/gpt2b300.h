@@ -1,0 +1,185 @@
+/*
+ * gpt2b300.h -- C ABI of libgpt2b300.so: one GPT-2 training step (forward
+ * with loss, zero_grad, backward, AdamW update) on one NVIDIA B300 (sm_103a).
+ *
+ * The calls follow the decomposition of llm.c's train_gpt2.c as described on
+ * the page «llm.c：Andrej Karpathy带你从零复现LLM», section
+ * «核心代码解读：train_gpt2.c»: item 2 (GPT2Config, ParameterTensors,
+ * ActivationTensors, the GPT2 struct) and item 3 (build, gpt2_forward,
+ * gpt2_zero_grad, gpt2_backward, gpt2_update with AdamW).  The single
+ * preallocated buffer that every weight and activation points into is the
+ * design of page «千行C代码训完GPT-2», section «纯CUDA也可训».
+ *
+ * Conventions shared by every call:
+ *  - Every function returns a status code (GPT2_OK = 0, negative = error,
+ *    positive = warning) unless stated otherwise; gpt2_status_string() names it.
+ *  - A handle orders all of its device work on the CUDA stream given to
+ *    gpt2_build().  Calls on one handle must not run concurrently (the handle
+ *    is not thread-safe); different handles are independent.
+ *  - Host pointers are read or written during the call only and never kept.
+ *  - After GPT2_ERR_DEVICE_TIMEOUT or GPT2_ERR_CUDA the handle is poisoned:
+ *    every later call except gpt2_free() returns the same error.
+ *  - Flat parameter layout (elements, fp32), each per-layer tensor stacked
+ *    over L: wte (Vp,C), wpe (maxT,C), ln1w (L,C), ln1b (L,C),
+ *    qkvw (L,3C,C), qkvb (L,3C), attprojw (L,C,C), attprojb (L,C),
+ *    ln2w (L,C), ln2b (L,C), fcw (L,4C,C), fcb (L,4C), fcprojw (L,C,4C),
+ *    fcprojb (L,C), lnfw (C), lnfb (C).  Linear weights are (out, in)
+ *    row-major: y = x W^T + b.  wte rows [V, Vp) are padding and stay 0.
+ *    Gradients and the AdamW moments m, v use the same layout.
+ */
+#ifndef GPT2B300_H
+#define GPT2B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define GPT2_OK 0
+#define GPT2_ERR_ARG (-1)            /* NULL handle/pointer, t < 1, bad config */
+#define GPT2_ERR_SHAPE (-2)          /* B > maxB, T > maxT, T > max_seq_len, B or T < 1 */
+#define GPT2_ERR_TOKEN_RANGE (-3)    /* a token id outside [0, vocab_size) */
+#define GPT2_ERR_STATE (-4)          /* backward without a forward that had targets */
+#define GPT2_ERR_ARENA (-5)          /* caller arena too small or not 256-byte aligned */
+#define GPT2_ERR_CUDA (-6)           /* a CUDA runtime/driver error; handle poisoned */
+#define GPT2_ERR_DEVICE_TIMEOUT (-7) /* a bounded device-side wait expired; handle poisoned */
+#define GPT2_WARN_NONFINITE 1        /* the loss is NaN or Inf; it is still returned */
+
+/* gemm_precision values. */
+#define GPT2_PREC_FP32 0 /* fp32 operands (3xTF32 split products), fp32 everything */
+#define GPT2_PREC_BF16 1 /* bf16 matmul/attention operands, fp32 accumulate, fp32 master/AdamW */
+
+/* GPT2Config (item 2 of the page above) plus the padded vocabulary and the
+ * matmul operand precision.  Requirements: channels % num_heads == 0,
+ * channels % 64 == 0, head size (channels/num_heads) in {16, 32, 64, 128},
+ * vocab_size <= padded_vocab_size, padded_vocab_size % 64 == 0. */
+typedef struct {
+  int max_seq_len;
+  int vocab_size;
+  int padded_vocab_size;
+  int num_layers;
+  int num_heads;
+  int channels;
+  int gemm_precision;
+} gpt2_config;
+
+typedef struct gpt2_t gpt2_t;
+
+/* Device bytes one handle needs for batches up to (maxB, maxT): parameters,
+ * gradients, AdamW m and v, activations, activation gradients and scratch.
+ * Returns 0 for an invalid config or shape. */
+size_t gpt2_arena_bytes(const gpt2_config* cfg, int maxB, int maxT);
+
+/* Creates a handle and initialises the parameters from `seed`: matrices
+ * N(0, 0.02) (attprojw, fcprojw additionally x 1/sqrt(2L)), biases 0,
+ * layernorm gains 1, shifts 0, padded wte rows 0, drawn with SplitMix64 +
+ * Box-Muller so that flat element i uses normal number i of the stream.
+ * AdamW moments start at 0.
+ *  dev_arena   : NULL -> the library allocates (and frees) the arena;
+ *                otherwise a device buffer of >= gpt2_arena_bytes() bytes,
+ *                256-byte aligned, owned by the caller and kept alive until
+ *                gpt2_free().
+ *  cuda_stream : a cudaStream_t, or NULL for the legacy default stream.
+ * The call synchronises the stream once before returning. */
+int gpt2_build(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, int maxB, int maxT, void* dev_arena,
+               size_t arena_bytes, void* cuda_stream);
+
+/* gpt2_forward (item 3): token embedding, L transformer blocks, final
+ * layernorm, tied LM head, and -- when targets != NULL -- the softmax
+ * cross-entropy over the vocab_size real columns with the loss gradient
+ * dlogits = (softmax - onehot)/(B*T) computed in the same pass.
+ *  inputs, targets : host int32 arrays of B*T token ids (row-major (B,T));
+ *                    targets may be NULL (logits only; backward then fails
+ *                    with GPT2_ERR_STATE).
+ *  loss_out        : host float, or NULL.  When non-NULL the call
+ *                    synchronises the stream and stores the mean loss over
+ *                    the B*T positions (-1.0f when targets is NULL); it
+ *                    returns GPT2_WARN_NONFINITE for a NaN/Inf loss.  When
+ *                    NULL the call returns once the work is enqueued.
+ * Token ids are validated on the host before any work is enqueued. */
+int gpt2_forward(gpt2_t* m, const int32_t* inputs, const int32_t* targets, int B, int T, float* loss_out);
+
+/* Same as gpt2_forward with device-resident token arrays (B*T int32 each,
+ * targets may be NULL).  Never synchronises.  An out-of-range id is detected
+ * on the device: the step's results are then undefined and the next
+ * gpt2_sync() returns GPT2_ERR_TOKEN_RANGE. */
+int gpt2_forward_device(gpt2_t* m, const int32_t* d_inputs, const int32_t* d_targets, int B, int T);
+
+/* Synchronises the handle's stream; reports device-side errors recorded since
+ * the previous sync and, when loss_out != NULL, stores the last mean loss. */
+int gpt2_sync(gpt2_t* m, float* loss_out);
+
+/* gpt2_zero_grad (item 3): sets every parameter gradient to 0.  Activation
+ * gradients are overwritten by gpt2_backward and need no clearing. */
+int gpt2_zero_grad(gpt2_t* m);
+
+/* gpt2_backward (item 3): ACCUMULATES (+=) the gradient of the mean loss of
+ * the last forward into the parameter gradients.  GPT2_ERR_STATE if the last
+ * forward had no targets.  Does not synchronise. */
+int gpt2_backward(gpt2_t* m);
+
+/* gpt2_update (item 3): one AdamW step over every parameter, step number
+ * t >= 1 (bias corrections 1 - beta^t), decoupled weight decay:
+ *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+ *   p -= lr * ((m/(1-b1^t)) / (sqrt(v/(1-b2^t)) + eps) + weight_decay * p).
+ * Does not synchronise. */
+int gpt2_update(gpt2_t* m, float lr, float beta1, float beta2, float eps, float weight_decay, int t);
+
+/* One whole step -- forward (device tokens), zero_grad, backward, update --
+ * enqueued as a single unit; with use_graph != 0 the sequence is captured
+ * once per (B, T) into a CUDA graph and replayed.  Never synchronises. */
+int gpt2_train_step_device(gpt2_t* m, const int32_t* d_inputs, const int32_t* d_targets, int B, int T, float lr,
+                           float beta1, float beta2, float eps, float weight_decay, int t, int use_graph);
+
+/* One whole step from HOST token arrays, the call a training loop makes:
+ * copies the B*T inputs and targets to the device (pinned host memory makes
+ * the copies asynchronous), validates them on the host, replays the
+ * captured step (forward with loss, zero_grad, backward, AdamW step t) and
+ * synchronises to store the step's mean loss in *loss_out (non-NULL).
+ * Returns GPT2_WARN_NONFINITE for a NaN/Inf loss. */
+int gpt2_train_step(gpt2_t* m, const int32_t* inputs, const int32_t* targets, int B, int T, float lr, float beta1,
+                    float beta2, float eps, float weight_decay, int t, float* loss_out);
+
+/* Kernel timer for roofline measurement.  kind selects one kernel class
+ * (0 off, 1 matmuls, 2 AdamW, 3 fused cross-entropy, 4 attention forward,
+ * 5 attention backward, 6 layernorm, 7 embedding); while it is on, every
+ * launch of that class is bracketed by CUDA events on the handle's stream
+ * and steps run without graph replay.  gpt2_kernel_timer() resets the
+ * totals; gpt2_kernel_timer_read() synchronises and returns the summed
+ * event time (ms), the number of launches and their summed algorithmic work
+ * (FLOPs for matmuls, bytes for the others). */
+int gpt2_kernel_timer(gpt2_t* m, int kind);
+int gpt2_kernel_timer_read(gpt2_t* m, double* total_ms, long long* launches, double* total_work);
+
+/* Frees the handle (and the arena if the library allocated it). */
+int gpt2_free(gpt2_t* m);
+
+/* Number of elements of the flat (padded) parameter buffer; -1 for NULL. */
+long long gpt2_num_parameters(const gpt2_t* m);
+
+/* Host <-> device copies of the flat buffers (n = gpt2_num_parameters());
+ * each synchronises the stream.  Used for parity tests and checkpoints. */
+int gpt2_get_params(gpt2_t* m, float* host, long long n);
+int gpt2_set_params(gpt2_t* m, const float* host, long long n);
+int gpt2_get_grads(gpt2_t* m, float* host, long long n);
+int gpt2_get_opt_state(gpt2_t* m, float* host_m, float* host_v, long long n);
+int gpt2_set_opt_state(gpt2_t* m, const float* host_m, const float* host_v, long long n);
+
+/* Logits of the last forward, (B, T, Vp) fp32, n = B*T*Vp elements. */
+int gpt2_get_logits(gpt2_t* m, float* host, long long n);
+
+/* Number of kernels the last gpt2_forward/backward/update/train_step call
+ * enqueued (for launch accounting). */
+long long gpt2_last_launch_count(const gpt2_t* m);
+
+/* Static description of a status code (never NULL). */
+const char* gpt2_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPT2B300_H */
