@@ -501,14 +501,15 @@ static void carve(gpt2_t* m) {
 
 static int init_params(gpt2_t* m, uint64_t seed) {
   const gpt2_config& c = m->cfg;
-  float proj = 0.02f / sqrtf(2.0f * c.num_layers);
+  double proj = 0.02 / sqrt(2.0 * c.num_layers);
   long long off = 0;
   for (int i = 0; i < NUM_PARAMS; i++) {
     long long n = m->psize[i], nrand = 0;
-    float stdv = 0.f, fill = 0.f;
+    double stdv = 0.0;
+    float fill = 0.f;
     switch (i) {
-      case P_WTE: nrand = (long long)c.vocab_size * c.channels; stdv = 0.02f; break;
-      case P_WPE: case P_QKVW: case P_FCW: nrand = n; stdv = 0.02f; break;
+      case P_WTE: nrand = (long long)c.vocab_size * c.channels; stdv = 0.02; break;
+      case P_WPE: case P_QKVW: case P_FCW: nrand = n; stdv = 0.02; break;
       case P_ATTPROJW: case P_FCPROJW: nrand = n; stdv = proj; break;
       case P_LN1W: case P_LN2W: case P_LNFW: fill = 1.f; break;
       default: break;

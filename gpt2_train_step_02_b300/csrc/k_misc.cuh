@@ -30,10 +30,10 @@ GPT2_DEV double normal_at(uint64_t seed, uint64_t i) {
 
 // Fills p[0 .. n) of the flat buffer that starts at flat offset `base`:
 // elements [0, nrand) get std * normal(base + i), the rest `fill`.
-__global__ void init_tensor_kernel(float* p, long long base, long long n, long long nrand, float stdv, float fill,
+__global__ void init_tensor_kernel(float* p, long long base, long long n, long long nrand, double stdv, float fill,
                                    uint64_t seed) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
-    p[i] = i < nrand ? (float)((double)stdv * normal_at(seed, (uint64_t)(base + i))) : fill;
+    p[i] = i < nrand ? (float)(stdv * normal_at(seed, (uint64_t)(base + i))) : fill;
 }
 
 // ---------------------------------------------------------------------------
