@@ -39,7 +39,7 @@ EXPORTS = [
     "gpt2_backward", "gpt2_update", "gpt2_train_step_device", "gpt2_free", "gpt2_num_parameters",
     "gpt2_get_params", "gpt2_set_params", "gpt2_get_grads", "gpt2_get_opt_state", "gpt2_set_opt_state",
     "gpt2_get_logits", "gpt2_last_launch_count", "gpt2_status_string", "gpt2_train_step", "gpt2_kernel_timer",
-    "gpt2_kernel_timer_read",
+    "gpt2_kernel_timer_read", "gpt2op_matmul_workspace_bytes", "gpt2op_matmul_forward", "gpt2op_matmul_backward",
 ]
 
 
@@ -88,6 +88,9 @@ def lib() -> ct.CDLL:
             "gpt2_status_string": (ct.c_char_p, [I]),
             "gpt2_train_step": (I, [P, P, P, I, I, F, F, F, F, F, I, P]),
             "gpt2_kernel_timer": (I, [P, I]),
+            "gpt2op_matmul_workspace_bytes": (SZ, [I, I]),
+            "gpt2op_matmul_forward": (I, [P, P, P, P, I, I, I, I, P, P]),
+            "gpt2op_matmul_backward": (I, [P, P, P, P, P, P, I, I, I, I, P, P]),
             "gpt2_kernel_timer_read": (I, [P, ct.POINTER(ct.c_double), ct.POINTER(LL), ct.POINTER(ct.c_double)]),
         }
         for name, (res, args) in sig.items():
@@ -320,3 +323,39 @@ class GPT2:
 
     def last_launch_count(self) -> int:
         return int(lib().gpt2_last_launch_count(self.h))
+
+
+# --- kernel-level entry points (torch CUDA tensors in, results in place) -------
+def _dptr(t):
+    """Device pointer of a contiguous fp32 CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    import torch
+
+    if t.dtype not in (torch.float32, torch.uint8) or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"expected a contiguous float32 CUDA tensor, got {t.dtype} on {t.device}")
+    return t.data_ptr()
+
+
+def matmul_forward(out, x, W, bias=None, precision=GPT2_PREC_FP32, stream=None):
+    """out = x W^T (+ bias), on the library's tensor-core kernels."""
+    import torch
+
+    OC, IC = W.shape
+    N = x.numel() // IC
+    ws = torch.empty(lib().gpt2op_matmul_workspace_bytes(N, OC), dtype=torch.uint8, device=x.device)
+    s = stream or torch.cuda.current_stream()
+    _check(lib().gpt2op_matmul_forward(_dptr(out), _dptr(x), _dptr(W), _dptr(bias), N, IC, OC, precision,
+                                       _dptr(ws), s.cuda_stream), "gpt2op_matmul_forward")
+
+
+def matmul_backward(dx, dW, dbias, dy, x, W, precision=GPT2_PREC_FP32, stream=None):
+    """dx = dy W; dW += dy^T x; dbias += column sums of dy."""
+    import torch
+
+    OC, IC = W.shape
+    N = x.numel() // IC
+    ws = torch.empty(lib().gpt2op_matmul_workspace_bytes(N, OC), dtype=torch.uint8, device=x.device)
+    s = stream or torch.cuda.current_stream()
+    _check(lib().gpt2op_matmul_backward(_dptr(dx), _dptr(dW), _dptr(dbias), _dptr(dy), _dptr(x), _dptr(W), N, IC,
+                                        OC, precision, _dptr(ws), s.cuda_stream), "gpt2op_matmul_backward")

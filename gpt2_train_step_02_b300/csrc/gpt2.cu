@@ -16,17 +16,23 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "../../include/gpt2b300.h"
 #include "common.cuh"
 #include "k_attention_simt.cuh"
 #include "k_gemm_simt.cuh"
+#include "k_gemm_tc.cuh"
 #include "k_layernorm.cuh"
 #include "k_misc.cuh"
 #include "k_xent.cuh"
 
 #define EXPORT extern "C" __attribute__((visibility("default")))
+
+// split-K workspace: at most 148 partial 128x128 tiles
+#define SPLITK_WS_FLOATS ((long long)148 * 128 * 128)
 
 enum {
   P_WTE, P_WPE, P_LN1W, P_LN1B, P_QKVW, P_QKVB, P_ATTPROJW, P_ATTPROJB,
@@ -41,7 +47,7 @@ struct Plan {
   size_t params, grads, m, v, params_bf;
   size_t encoded, ln1, ln1_mean, ln1_rstd, qkv, atty, lse, res2, ln2, ln2_mean, ln2_rstd, fch, fchg, res3;
   size_t lnf, lnf_mean, lnf_rstd, logits, dlogits, losses, loss;
-  size_t dres, dln, datty, dqkv, dfch, attD, scratch, sorted, tokens, targets, err, hparams;
+  size_t dres, dln, datty, dqkv, dfch, attD, scratch, sorted, tokens, targets, err, hparams, splitk;
   size_t scratch_floats;
 };
 
@@ -128,6 +134,7 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->targets = take(BT * sizeof(int));
   p->err = take(sizeof(int));
   p->hparams = take(16 * F);
+  p->splitk = take(SPLITK_WS_FLOATS * F);
   p->total = off;
   return off;
 }
@@ -151,7 +158,7 @@ struct gpt2_t {
   float *encoded, *ln1, *ln1_mean, *ln1_rstd, *qkv, *atty, *lse, *res2, *ln2, *ln2_mean, *ln2_rstd, *fch, *fchg,
       *res3;
   float *lnf, *lnf_mean, *lnf_rstd, *logits, *dlogits, *losses, *loss;
-  float *dres, *dln, *datty, *dqkv, *dfch, *attD, *scratch;
+  float *dres, *dln, *datty, *dqkv, *dfch, *attD, *scratch, *splitk;
   uint32_t* sorted;
   int *tokens, *targets, *err;
   float* hparams;
@@ -230,53 +237,144 @@ static int grid_for(long long n, int threads, int cap = 148 * 16) {
 }
 
 // ---------------------------------------------------------------------------
-// matmul helpers for a linear layer y = x W^T + b with x (N, IC), W (OC, IC)
+// matmul launcher
 // ---------------------------------------------------------------------------
-static void mm_forward(gpt2_t* m, float* out, const float* x, const float* W, const float* bias, int N, int IC, int OC,
-                       int epi, const float* R, float* pre) {
-  GemmArgs a = {};
-  a.M = N; a.N = OC; a.K = IC;
-  a.A = x; a.a_rs = IC; a.a_cs = 1;
-  a.B = W; a.b_rs = 1; a.b_cs = IC;
-  a.C = out; a.ldc = OC;
-  a.bias = bias; a.R = R; a.ldr = OC; a.pre = pre; a.ldpre = OC;
-  a.epi = epi;
-  a.bf16_ops = m->cfg.gemm_precision == GPT2_PREC_BF16;
-  timer_begin(m, TK_GEMM, 2.0 * N * (double)IC * OC);
-  gemm_simt_launch(a, m->stream);
-  timer_end(m, TK_GEMM);
-  m->launches++;
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+
+static int get_encoder() {
+  if (g_encode_tiled) return 1;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    cudaGetLastError();
+    return 0;
+  }
+  g_encode_tiled = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  return 1;
 }
 
-// dx = dy W (optionally times gelu'(pre))
-static void mm_dx(gpt2_t* m, float* dx, const float* dy, const float* W, int N, int IC, int OC, const float* pre) {
-  GemmArgs a = {};
-  a.M = N; a.N = IC; a.K = OC;
-  a.A = dy; a.a_rs = OC; a.a_cs = 1;
-  a.B = W; a.b_rs = IC; a.b_cs = 1;
-  a.C = dx; a.ldc = IC;
-  a.R = pre; a.ldr = IC;
-  a.epi = pre ? EPI_DGELU : EPI_STORE;
-  a.bf16_ops = m->cfg.gemm_precision == GPT2_PREC_BF16;
-  timer_begin(m, TK_GEMM, 2.0 * N * (double)IC * OC);
-  gemm_simt_launch(a, m->stream);
+// Tensor map of an fp32 operand stored as `outer` rows of pitch `ld` elements
+// with `inner` valid (contiguous) elements per row.  K-major tiles are
+// 32 x 128 boxes with the 128-byte swizzle; MN-major tiles are unswizzled
+// 128 x 32 boxes.  Out-of-range elements load as zero.
+static int make_operand_map(CUtensorMap* tm, const float* base, int kmajor, long long outer, long long inner,
+                            long long ld) {
+  if (!get_encoder()) return 0;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * sizeof(float)};
+  cuuint32_t box_k[2] = {(cuuint32_t)tc::BK, (cuuint32_t)tc::BM};
+  cuuint32_t box_mn[2] = {(cuuint32_t)tc::BM, (cuuint32_t)tc::BK};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode_tiled(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, (void*)base, dims, strides,
+                              kmajor ? box_k : box_mn, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              kmajor ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// One matmul acc(i,j) = sum_k A(i,k) B(j,k) with a fused epilogue.
+struct MatmulDesc {
+  int M, N, K;
+  const float* A;
+  long long lda;
+  int a_kmajor;  // 1: A stored (M, lda) with K contiguous; 0: stored (K, lda) with M contiguous
+  const float* B;
+  long long ldb;
+  int b_kmajor;  // 1: B stored (N, ldb) with K contiguous; 0: stored (K, ldb) with N contiguous
+  EpiArgs epi;
+};
+
+// Split K so that small-M products still fill the 148 SMs; the split-K
+// partial sums (<= SPLITK_WS_FLOATS) are reduced in a fixed order.
+static int choose_splits(int M, int N, int K) {
+  long long tiles = (long long)ceil_div(M, tc::BM) * ceil_div(N, tc::BN);
+  int kt = ceil_div(K, tc::BK);
+  if (tiles >= 148 || kt < 4) return 1;
+  int s = (int)(148 / tiles);
+  s = s < kt / 2 ? s : kt / 2;
+  while (s > 1 && (long long)s * M * N > SPLITK_WS_FLOATS) s--;
+  if (s < 1) s = 1;
+  int per = ceil_div(kt, s);
+  return ceil_div(kt, per);
+}
+
+// Launches the tensor-core matmul (+ the split-K reduction when K is split).
+// Returns the number of kernels launched, or -1 on a host-side failure.
+static int launch_matmul(const MatmulDesc& d, float* ws, int* err, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  if (!make_operand_map(&ta, d.A, d.a_kmajor, d.a_kmajor ? d.M : d.K, d.a_kmajor ? d.K : d.M, d.lda)) return -1;
+  if (!make_operand_map(&tb, d.B, d.b_kmajor, d.b_kmajor ? d.N : d.K, d.b_kmajor ? d.K : d.N, d.ldb)) return -1;
+  int splits = choose_splits(d.M, d.N, d.K);
+  tc::Params p;
+  p.M = d.M;
+  p.N = d.N;
+  p.K = d.K;
+  p.a_kmajor = d.a_kmajor;
+  p.b_kmajor = d.b_kmajor;
+  p.k_tiles = ceil_div(d.K, tc::BK);
+  p.kt_per_split = ceil_div(p.k_tiles, splits);
+  p.epi = d.epi;
+  p.partial = splits > 1 ? ws : nullptr;
+  p.err = err;
+  dim3 grid(ceil_div(d.N, tc::BN), ceil_div(d.M, tc::BM), splits);
+  tc::gemm_tf32x3_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, s>>>(ta, tb, p);
+  if (splits == 1) return 1;
+  long long total = (long long)d.M * d.N;
+  splitk_reduce_kernel<<<grid_for(total, 256), 256, 0, s>>>(ws, splits, d.M, d.N, d.epi);
+  return 2;
+}
+
+static int matmul(gpt2_t* m, const MatmulDesc& d) {
+  if (m->cfg.gemm_precision == GPT2_PREC_BF16) {
+    // bf16 operands: CUDA-core product with operands rounded to bf16
+    GemmArgs a = {};
+    a.M = d.M; a.N = d.N; a.K = d.K;
+    a.A = d.A; a.a_rs = d.a_kmajor ? d.lda : 1; a.a_cs = d.a_kmajor ? 1 : d.lda;
+    a.B = d.B; a.b_rs = d.b_kmajor ? 1 : d.ldb; a.b_cs = d.b_kmajor ? d.ldb : 1;
+    a.epi = d.epi;
+    a.bf16_ops = 1;
+    timer_begin(m, TK_GEMM, 2.0 * d.M * (double)d.N * d.K);
+    gemm_simt_launch(a, m->stream);
+    timer_end(m, TK_GEMM);
+    m->launches++;
+    return GPT2_OK;
+  }
+  timer_begin(m, TK_GEMM, 2.0 * d.M * (double)d.N * d.K);
+  int n = launch_matmul(d, m->splitk, m->err, m->stream);
   timer_end(m, TK_GEMM);
-  m->launches++;
+  if (n < 0) {
+    m->poisoned = GPT2_ERR_CUDA;
+    return GPT2_ERR_CUDA;
+  }
+  m->launches += n;
+  return GPT2_OK;
+}
+
+static EpiArgs epi_args(float* C, long long ldc, int epi, const float* bias = nullptr, const float* R = nullptr,
+                        long long ldr = 0, float* pre = nullptr, long long ldpre = 0) {
+  EpiArgs e;
+  e.C = C; e.ldc = ldc; e.bias = bias; e.R = R; e.ldr = ldr; e.pre = pre; e.ldpre = ldpre; e.epi = epi;
+  return e;
+}
+
+// linear layer y = x W^T + b with x (N, IC), W (OC, IC)
+static void mm_forward(gpt2_t* m, float* out, const float* x, const float* W, const float* bias, int N, int IC, int OC,
+                       int epi, const float* R, float* pre) {
+  MatmulDesc d = {N, OC, IC, x, IC, 1, W, IC, 1, epi_args(out, OC, epi, bias, R, OC, pre, OC)};
+  matmul(m, d);
+}
+
+// dx = dy W (times gelu'(pre) when pre != NULL)
+static void mm_dx(gpt2_t* m, float* dx, const float* dy, const float* W, int N, int IC, int OC, const float* pre) {
+  MatmulDesc d = {N, IC, OC, dy, OC, 1, W, IC, 0, epi_args(dx, IC, pre ? EPI_DGELU : EPI_STORE, nullptr, pre, IC)};
+  matmul(m, d);
 }
 
 // dW += dy^T x
 static void mm_dw(gpt2_t* m, float* dW, const float* dy, const float* x, int N, int IC, int OC) {
-  GemmArgs a = {};
-  a.M = OC; a.N = IC; a.K = N;
-  a.A = dy; a.a_rs = 1; a.a_cs = OC;
-  a.B = x; a.b_rs = IC; a.b_cs = 1;
-  a.C = dW; a.ldc = IC;
-  a.epi = EPI_ACCUM;
-  a.bf16_ops = m->cfg.gemm_precision == GPT2_PREC_BF16;
-  timer_begin(m, TK_GEMM, 2.0 * N * (double)IC * OC);
-  gemm_simt_launch(a, m->stream);
-  timer_end(m, TK_GEMM);
-  m->launches++;
+  MatmulDesc d = {OC, IC, N, dy, OC, 0, x, IC, 0, epi_args(dW, IC, EPI_ACCUM)};
+  matmul(m, d);
 }
 
 // db += column sums of dy (N, OC)
@@ -495,7 +593,7 @@ static void carve(gpt2_t* m) {
   CARVE(res2); CARVE(ln2); CARVE(ln2_mean); CARVE(ln2_rstd); CARVE(fch); CARVE(fchg); CARVE(res3);
   CARVE(lnf); CARVE(lnf_mean); CARVE(lnf_rstd); CARVE(logits); CARVE(dlogits); CARVE(losses); CARVE(loss);
   CARVE(dres); CARVE(dln); CARVE(datty); CARVE(dqkv); CARVE(dfch); CARVE(attD); CARVE(scratch); CARVE(sorted);
-  CARVE(tokens); CARVE(targets); CARVE(err); CARVE(hparams);
+  CARVE(tokens); CARVE(targets); CARVE(err); CARVE(hparams); CARVE(splitk);
 #undef CARVE
 }
 
@@ -560,6 +658,9 @@ EXPORT int gpt2_build(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, int m
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(sort_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 SORT_MAX * (int)sizeof(uint32_t))) != cudaSuccess)
+    goto cuda_fail;
+  if ((e = cudaFuncSetAttribute(tc::gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                tc::SMEM_BYTES)) != cudaSuccess)
     goto cuda_fail;
   if ((e = cudaMemsetAsync(m->grads, 0, m->np * sizeof(float), m->stream)) != cudaSuccess) goto cuda_fail;
   if ((e = cudaMemsetAsync(m->m, 0, m->np * sizeof(float), m->stream)) != cudaSuccess) goto cuda_fail;
@@ -840,4 +941,98 @@ EXPORT int gpt2_get_logits(gpt2_t* m, float* host, long long n) {
   CCHECK(m, cudaStreamSynchronize(m->stream));
   CCHECK(m, cudaMemcpy(host, m->logits, n * sizeof(float), cudaMemcpyDeviceToHost));
   return GPT2_OK;
+}
+
+// ---------------------------------------------------------------------------
+// kernel-level entry points (device buffers), for per-layer parity tests
+// ---------------------------------------------------------------------------
+// workspace layout: [error word (256 B)][bias partials ceil(N/64) x OC][split-K partials]
+EXPORT size_t gpt2op_matmul_workspace_bytes(int N, int OC) {
+  if (N < 1 || OC < 1) return 0;
+  size_t bias = (size_t)ceil_div(N, 64) * OC * sizeof(float);
+  return 256 + ((bias + 255) & ~(size_t)255) + SPLITK_WS_FLOATS * sizeof(float);
+}
+
+struct OpWs {
+  int* err;
+  float* bias_partial;
+  float* splitk;
+};
+
+static OpWs op_ws(void* ws, int N, int OC) {
+  OpWs w;
+  char* b = (char*)ws;
+  size_t bias = (size_t)ceil_div(N, 64) * OC * sizeof(float);
+  w.err = (int*)b;
+  w.bias_partial = (float*)(b + 256);
+  w.splitk = (float*)(b + 256 + ((bias + 255) & ~(size_t)255));
+  return w;
+}
+
+static int op_matmul(const MatmulDesc& d, int precision, const OpWs& w, cudaStream_t s) {
+  if (precision == GPT2_PREC_BF16) {
+    GemmArgs a = {};
+    a.M = d.M; a.N = d.N; a.K = d.K;
+    a.A = d.A; a.a_rs = d.a_kmajor ? d.lda : 1; a.a_cs = d.a_kmajor ? 1 : d.lda;
+    a.B = d.B; a.b_rs = d.b_kmajor ? 1 : d.ldb; a.b_cs = d.b_kmajor ? d.ldb : 1;
+    a.epi = d.epi;
+    a.bf16_ops = 1;
+    gemm_simt_launch(a, s);
+    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+  }
+  if (launch_matmul(d, w.splitk, w.err, s) < 0) return GPT2_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+static int op_status(const OpWs& w, cudaStream_t s) {
+  int err = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GPT2_ERR_CUDA;
+  if (cudaMemcpy(&err, w.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GPT2_ERR_CUDA;
+  if (err == DEV_ERR_TIMEOUT) return GPT2_ERR_DEVICE_TIMEOUT;
+  return err ? GPT2_ERR_SHAPE : GPT2_OK;
+}
+
+static int op_prepare(void* workspace, cudaStream_t s) {
+  static int attr_done = 0;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(tc::gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES) !=
+        cudaSuccess)
+      return GPT2_ERR_CUDA;
+    attr_done = 1;
+  }
+  return cudaMemsetAsync(workspace, 0, 256, s) == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+EXPORT int gpt2op_matmul_forward(float* out, const float* x, const float* W, const float* bias, int N, int IC, int OC,
+                                 int precision, void* workspace, void* stream) {
+  if (!out || !x || !W || !workspace || N < 1 || IC < 1 || OC < 1) return GPT2_ERR_ARG;
+  if ((IC * 4) % 16 || (OC * 4) % 16) return GPT2_ERR_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  int rc = op_prepare(workspace, s);
+  if (rc) return rc;
+  OpWs w = op_ws(workspace, N, OC);
+  MatmulDesc d = {N, OC, IC, x, IC, 1, W, IC, 1, epi_args(out, OC, bias ? EPI_BIAS : EPI_STORE, bias)};
+  rc = op_matmul(d, precision, w, s);
+  return rc ? rc : op_status(w, s);
+}
+
+EXPORT int gpt2op_matmul_backward(float* dx, float* dW, float* dbias, const float* dy, const float* x, const float* W,
+                                  int N, int IC, int OC, int precision, void* workspace, void* stream) {
+  if (!dx || !dW || !dy || !x || !W || !workspace || N < 1 || IC < 1 || OC < 1) return GPT2_ERR_ARG;
+  if ((IC * 4) % 16 || (OC * 4) % 16) return GPT2_ERR_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  int rc = op_prepare(workspace, s);
+  if (rc) return rc;
+  OpWs w = op_ws(workspace, N, OC);
+  MatmulDesc ddx = {N, IC, OC, dy, OC, 1, W, IC, 0, epi_args(dx, IC, EPI_STORE)};
+  if ((rc = op_matmul(ddx, precision, w, s))) return rc;
+  MatmulDesc ddw = {OC, IC, N, dy, OC, 0, x, IC, 0, epi_args(dW, IC, EPI_ACCUM)};
+  if ((rc = op_matmul(ddw, precision, w, s))) return rc;
+  if (dbias) {
+    int chunks = ceil_div(N, 64);
+    col_partial_kernel<<<dim3(ceil_div(OC, 256), chunks), 256, 0, s>>>(dy, N, OC, OC, 64, w.bias_partial);
+    col_finish_kernel<<<ceil_div(OC, 256), 256, 0, s>>>(w.bias_partial, chunks, OC, dbias);
+    if (cudaGetLastError() != cudaSuccess) return GPT2_ERR_CUDA;
+  }
+  return op_status(w, s);
 }

@@ -6,15 +6,7 @@
 // (A = dy, B = W) and weight gradient (A = dy^T, B = x).
 #pragma once
 #include "common.cuh"
-
-enum GemmEpi : int {
-  EPI_STORE = 0,       // C = acc
-  EPI_BIAS = 1,        // C = acc + bias[j]
-  EPI_BIAS_RESID = 2,  // C = acc + bias[j] + R(i,j)
-  EPI_BIAS_GELU = 3,   // pre(i,j) = acc + bias[j]; C = gelu(pre)
-  EPI_DGELU = 4,       // C = acc * gelu'(R(i,j))
-  EPI_ACCUM = 5,       // C += acc
-};
+#include "gemm_common.cuh"
 
 struct GemmArgs {
   int M, N, K;
@@ -22,37 +14,9 @@ struct GemmArgs {
   long long a_rs, a_cs;
   const float* B;
   long long b_rs, b_cs;
-  float* C;
-  long long ldc;
-  const float* bias;
-  const float* R;
-  long long ldr;
-  float* pre;
-  long long ldpre;
-  uint16_t* Cbf;  // optional bf16 copy of the stored C (ldc)
-  int epi;
+  EpiArgs epi;
   int bf16_ops;  // round both operands to bf16 before multiplying
 };
-
-GPT2_DEV void gemm_epilogue(const GemmArgs& p, int i, int j, float acc) {
-  size_t ci = (size_t)i * p.ldc + j;
-  float out;
-  switch (p.epi) {
-    case EPI_BIAS: out = acc + p.bias[j]; break;
-    case EPI_BIAS_RESID: out = acc + p.bias[j] + p.R[(size_t)i * p.ldr + j]; break;
-    case EPI_BIAS_GELU: {
-      float h = acc + p.bias[j];
-      p.pre[(size_t)i * p.ldpre + j] = h;
-      out = gelu_fwd(h);
-      break;
-    }
-    case EPI_DGELU: out = acc * gelu_grad(p.R[(size_t)i * p.ldr + j]); break;
-    case EPI_ACCUM: out = p.C[ci] + acc; break;
-    default: out = acc;
-  }
-  p.C[ci] = out;
-  if (p.Cbf) p.Cbf[ci] = to_bf16_bits(out);
-}
 
 #define SG_BM 64
 #define SG_BN 64
@@ -103,7 +67,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs p) {
 #pragma unroll
     for (int c = 0; c < 4; c++) {
       int i = i0 + ty * 4 + r, j = j0 + tx * 4 + c;
-      if (i < p.M && j < p.N) gemm_epilogue(p, i, j, acc[r][c]);
+      if (i < p.M && j < p.N) epi_store(p.epi, i, j, acc[r][c]);
     }
 }
 

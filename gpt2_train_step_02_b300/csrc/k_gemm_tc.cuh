@@ -1,0 +1,369 @@
+// k_gemm_tc.cuh -- fp32-accurate matmul on the 5th-generation tensor cores
+// (tcgen05.mma kind::tf32, accumulator in TMEM), fed by TMA.
+//
+//   acc(i,j) = sum_k A(i,k) B(j,k),  i < M, j < N, k < K,
+// where each operand is stored either K-major (row i holds its K values
+// contiguously) or MN-major (row k holds the M or N values contiguously).
+// The three products of a linear layer map onto it as
+//   forward          A = x  (K-major), B = W   (K-major)
+//   input gradient   A = dy (K-major), B = W   (MN-major)
+//   weight gradient  A = dy (MN-major), B = x  (MN-major).
+//
+// fp32 accuracy with TF32 tensor cores ("3xTF32", the split-precision
+// scheme of Ootomo & Yokota, 2022): every operand value is split as
+// x = hi + lo with hi = x rounded to TF32 and lo = x - hi (exact), and
+// a*b ~ ah*bh + ah*bl + al*bh, three MMAs into one fp32 accumulator.  The
+// dropped al*bl term and the TF32 rounding of lo are ~2^-20 relative.
+//
+// CTA = one 128 x 128 output tile over a range of K (split-K), 6 warps:
+//   warp 0      one lane issues the TMA loads of raw fp32 tiles (raw ring)
+//   warp 1      allocates TMEM; one lane issues tcgen05.mma and commits
+//   warps 2..5  split each raw tile into hi/lo tiles laid out K-major with
+//               the 128-byte swizzle (transposing MN-major tiles), then run
+//               the epilogue: tcgen05.ld TMEM -> registers -> global.
+// Every mbarrier wait is bounded; on expiry the CTA records DEV_ERR_TIMEOUT
+// in the error word, stops issuing work, frees its TMEM and returns.
+#pragma once
+#include <cuda.h>
+
+#include "common.cuh"
+#include "gemm_common.cuh"
+
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 32;  // fp32 elements = 128 bytes: one swizzle row
+constexpr int RAW_STAGES = 2;
+constexpr int COMP_STAGES = 2;
+constexpr int TILE_BYTES = BM * BK * 4;  // 16 KB (A or B tile)
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 128;
+constexpr uint32_t SPIN_LIMIT = 1u << 26;  // polls per wait before giving up (seconds)
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr int OFF_RAW_A = 0;
+constexpr int OFF_RAW_B = OFF_RAW_A + RAW_STAGES * TILE_BYTES;
+constexpr int OFF_HI_A = OFF_RAW_B + RAW_STAGES * TILE_BYTES;
+constexpr int OFF_LO_A = OFF_HI_A + COMP_STAGES * TILE_BYTES;
+constexpr int OFF_HI_B = OFF_LO_A + COMP_STAGES * TILE_BYTES;
+constexpr int OFF_LO_B = OFF_HI_B + COMP_STAGES * TILE_BYTES;
+constexpr int OFF_BAR = OFF_LO_B + COMP_STAGES * TILE_BYTES;
+constexpr int NUM_BARS = 2 * RAW_STAGES + 2 * COMP_STAGES + 1;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+
+struct Params {
+  int M, N, K;
+  int a_kmajor, b_kmajor;
+  int k_tiles, kt_per_split;
+  EpiArgs epi;
+  float* partial;  // split-K partials [splits][M][N], or NULL for a direct epilogue
+  int* err;
+};
+
+// ---- PTX wrappers ----------------------------------------------------------
+GPT2_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+GPT2_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+GPT2_DEV void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+GPT2_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+GPT2_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: returns false (and raises the CTA's abort flag and the
+// device error word) if the phase does not complete within SPIN_LIMIT polls
+// or another role of the CTA has aborted.
+GPT2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  for (uint32_t i = 0; i < SPIN_LIMIT; i++) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023) == 1023 && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  dev_set_error(err, DEV_ERR_TIMEOUT);
+  return false;
+}
+
+GPT2_DEV void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"((uint64_t)tm), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+GPT2_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+GPT2_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// K-major operand, 128-byte swizzle: 8-row atoms of 1024 bytes (SBO), start
+// address in 16-byte units, descriptor version 1, layout type 2 (SWIZZLE_128B).
+GPT2_DEV uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;            // version
+  d |= (uint64_t)2 << 61;            // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor: D fp32, A/B tf32, both K-major, M = 128, N = BN.
+constexpr uint32_t IDESC_TF32 = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                ((uint32_t)(BM >> 4) << 24);
+
+GPT2_DEV void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(IDESC_TF32), "r"(accumulate)
+      : "memory");
+}
+
+GPT2_DEV void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+GPT2_DEV void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int k = 0; k < 32; k++) v[k] = __uint_as_float(r[k]);
+}
+
+// ---- 3xTF32 split ----------------------------------------------------------
+// hi = x rounded to 10 mantissa bits (nearest, ties away); lo = x - hi exactly.
+GPT2_DEV float tf32_hi(float x) { return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u); }
+
+GPT2_DEV void split4(float4 x, float4& h, float4& l) {
+  h = make_float4(tf32_hi(x.x), tf32_hi(x.y), tf32_hi(x.z), tf32_hi(x.w));
+  l = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+}
+
+// raw tile already K-major SW128 (as TMA wrote it): split in place order.
+GPT2_DEV void split_kmajor(const float4* raw, float4* hi, float4* lo, int t) {
+#pragma unroll
+  for (int j = 0; j < (BM * BK / 4) / 128; j++) {
+    int q = t + 128 * j;
+    float4 h, l;
+    split4(raw[q], h, l);
+    hi[q] = h;
+    lo[q] = l;
+  }
+}
+
+// raw tile MN-major, unswizzled [BK rows of k][128 of m]: thread t owns row
+// m = t and writes its 32 k-values as 8 swizzled 16-byte chunks.
+GPT2_DEV void split_mnmajor(const float* raw, float* hi, float* lo, int t) {
+#pragma unroll
+  for (int c = 0; c < BK / 4; c++) {
+    float4 x = make_float4(raw[(4 * c + 0) * BM + t], raw[(4 * c + 1) * BM + t], raw[(4 * c + 2) * BM + t],
+                           raw[(4 * c + 3) * BM + t]);
+    float4 h, l;
+    split4(x, h, l);
+    int off = t * 32 + ((c ^ (t & 7)) << 2);
+    *reinterpret_cast<float4*>(hi + off) = h;
+    *reinterpret_cast<float4*>(lo + off) = l;
+  }
+}
+
+// ---- the kernel -------------------------------------------------------------
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = bars + RAW_STAGES;
+  uint64_t* comp_full = bars + 2 * RAW_STAGES;
+  uint64_t* comp_empty = bars + 2 * RAW_STAGES + COMP_STAGES;
+  uint64_t* acc_full = bars + 2 * RAW_STAGES + 2 * COMP_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int kt0 = blockIdx.z * p.kt_per_split;
+  const int kt1 = min(p.k_tiles, kt0 + p.kt_per_split);
+  const int nk = kt1 - kt0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RAW_STAGES; s++) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], 128);
+    }
+    for (int s = 0; s < COMP_STAGES; s++) {
+      mbar_init(&comp_full[s], 128);
+      mbar_init(&comp_empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nk; i++) {
+        int s = i % RAW_STAGES;
+        uint32_t ph = (i / RAW_STAGES) & 1;
+        if (!mbar_wait(&raw_empty[s], ph ^ 1, abort_flag, p.err)) break;
+        int k = (kt0 + i) * BK;
+        mbar_expect_tx(&raw_full[s], 2 * TILE_BYTES);
+        uint8_t* ra = smem + OFF_RAW_A + s * TILE_BYTES;
+        uint8_t* rb = smem + OFF_RAW_B + s * TILE_BYTES;
+        if (p.a_kmajor) tma_load_2d(ra, &tmA, k, m0, &raw_full[s]);
+        else tma_load_2d(ra, &tmA, m0, k, &raw_full[s]);
+        if (p.b_kmajor) tma_load_2d(rb, &tmB, k, n0, &raw_full[s]);
+        else tma_load_2d(rb, &tmB, n0, k, &raw_full[s]);
+        issued = i + 1;
+      }
+      // on abort, let the copies already in flight land before the CTA exits
+      if (*abort_flag) {
+        for (int i = max(0, issued - RAW_STAGES); i < issued; i++) {
+          int s = i % RAW_STAGES;
+          for (uint32_t q = 0; q < SPIN_LIMIT && !mbar_try_wait(&raw_full[s], (i / RAW_STAGES) & 1); q++) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = true;
+      for (int i = 0; i < nk && ok; i++) {
+        int c = i % COMP_STAGES;
+        uint32_t ph = (i / COMP_STAGES) & 1;
+        if (!mbar_wait(&comp_full[c], ph, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t ah = smem_u32(smem + OFF_HI_A + c * TILE_BYTES), al = smem_u32(smem + OFF_LO_A + c * TILE_BYTES);
+        uint32_t bh = smem_u32(smem + OFF_HI_B + c * TILE_BYTES), bl = smem_u32(smem + OFF_LO_B + c * TILE_BYTES);
+#pragma unroll
+        for (int j = 0; j < BK / 8; j++) {  // kind::tf32 consumes K = 8 (32 bytes) per instruction
+          uint32_t kb = j * 32;
+          uint64_t dah = smem_desc_kmajor_sw128(ah + kb), dal = smem_desc_kmajor_sw128(al + kb);
+          uint64_t dbh = smem_desc_kmajor_sw128(bh + kb), dbl = smem_desc_kmajor_sw128(bl + kb);
+          mma_tf32(tmem, dah, dbh, (i > 0 || j > 0) ? 1u : 0u);
+          mma_tf32(tmem, dah, dbl, 1u);
+          mma_tf32(tmem, dal, dbh, 1u);
+        }
+        mma_commit(&comp_empty[c]);  // frees the hi/lo stage once these MMAs have read it
+      }
+      // acc_full tracks completion of every MMA this thread issued; on abort
+      // wait for it here so that TMEM is not freed under running MMAs
+      if (nk > 0) mma_commit(acc_full);
+      if (!ok && nk > 0) {
+        for (uint32_t q = 0; q < SPIN_LIMIT && !mbar_try_wait(acc_full, 0); q++) {
+        }
+      }
+    }
+  } else {
+    // ---------------- splitters, then epilogue ----------------
+    const int t = threadIdx.x - 64;  // 0..127
+    bool ok = true;
+    for (int i = 0; i < nk; i++) {
+      int s = i % RAW_STAGES, c = i % COMP_STAGES;
+      if (!mbar_wait(&raw_full[s], (i / RAW_STAGES) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      if (!mbar_wait(&comp_empty[c], ((i / COMP_STAGES) & 1) ^ 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* ra = smem + OFF_RAW_A + s * TILE_BYTES;
+      const uint8_t* rb = smem + OFF_RAW_B + s * TILE_BYTES;
+      float* ha = reinterpret_cast<float*>(smem + OFF_HI_A + c * TILE_BYTES);
+      float* la = reinterpret_cast<float*>(smem + OFF_LO_A + c * TILE_BYTES);
+      float* hb = reinterpret_cast<float*>(smem + OFF_HI_B + c * TILE_BYTES);
+      float* lb = reinterpret_cast<float*>(smem + OFF_LO_B + c * TILE_BYTES);
+      if (p.a_kmajor)
+        split_kmajor(reinterpret_cast<const float4*>(ra), reinterpret_cast<float4*>(ha), reinterpret_cast<float4*>(la), t);
+      else
+        split_mnmajor(reinterpret_cast<const float*>(ra), ha, la, t);
+      if (p.b_kmajor)
+        split_kmajor(reinterpret_cast<const float4*>(rb), reinterpret_cast<float4*>(hb), reinterpret_cast<float4*>(lb), t);
+      else
+        split_mnmajor(reinterpret_cast<const float*>(rb), hb, lb, t);
+      // make the generic-proxy smem writes visible to the tensor core (async proxy)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&raw_empty[s]);
+      mbar_arrive(&comp_full[c]);
+    }
+    if (ok && nk > 0) ok = mbar_wait(acc_full, 0, abort_flag, p.err);
+    // tcgen05.ld is warp-collective: take the epilogue only if the whole warp can
+    if (__all_sync(0xffffffffu, ok && nk > 0 && !*abort_flag)) {
+      tc_fence_after();
+      const int q = warp & 3;  // TMEM lane quadrant this warp may access
+      const int row = q * 32 + lane;
+      const int i = m0 + row;
+      const bool split = p.partial != nullptr;
+      const size_t zoff = split ? (size_t)blockIdx.z * p.M * p.N : 0;
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 32; cc++) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cc * 32), v);
+        if (i < p.M) {
+          int j0 = n0 + cc * 32;
+          if (split) {
+            float* dst = p.partial + zoff + (size_t)i * p.N;
+#pragma unroll
+            for (int e = 0; e < 32; e++)
+              if (j0 + e < p.N) dst[j0 + e] = v[e];
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e++)
+              if (j0 + e < p.N) epi_store(p.epi, i, j0 + e, v[e]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+}  // namespace tc

@@ -175,6 +175,23 @@ int gpt2_get_logits(gpt2_t* m, float* host, long long n);
  * enqueued (for launch accounting). */
 long long gpt2_last_launch_count(const gpt2_t* m);
 
+/* ---- kernel-level entry points (device buffers, row-major fp32) ----------
+ * The per-layer matmul of the page's item 1 (matmul_forward /
+ * matmul_backward), run by the same tensor-core kernels the model uses; for
+ * per-layer parity tests.  x (N, IC), W (OC, IC), bias (OC), out (N, OC).
+ * precision is GPT2_PREC_FP32 or GPT2_PREC_BF16.  workspace: a device buffer
+ * of gpt2op_matmul_workspace_bytes(N, OC) bytes (scratch; contents not
+ * kept).  stream: cudaStream_t or NULL.  Both calls synchronise the stream.
+ * IC and OC must be multiples of 4 (16-byte rows for TMA). */
+size_t gpt2op_matmul_workspace_bytes(int N, int OC);
+/* out = x W^T (+ bias when bias != NULL). */
+int gpt2op_matmul_forward(float* out, const float* x, const float* W, const float* bias, int N, int IC, int OC,
+                          int precision, void* workspace, void* stream);
+/* dx = dy W (overwritten); dW += dy^T x; dbias += column sums of dy (dbias
+ * may be NULL).  dy (N, OC). */
+int gpt2op_matmul_backward(float* dx, float* dW, float* dbias, const float* dy, const float* x, const float* W,
+                           int N, int IC, int OC, int precision, void* workspace, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* gpt2_status_string(int status);
 

@@ -242,3 +242,9 @@ def batch(w: Workload, step: int = 0, seed: int = TOKEN_SEED, B: int | None = No
     n = B * T + 1
     x = token_stream(w, step * n, n, seed)
     return x[:-1].reshape(B, T).copy(), x[1:].reshape(B, T).copy()
+
+
+def randn(seed: int, shape, scale: float = 1.0, dtype=np.float32) -> np.ndarray:
+    """Seeded standard normals (counter-based, as above) of the given shape."""
+    n = int(np.prod(shape))
+    return (scale * normals(seed, 0, n)).astype(dtype).reshape(shape)

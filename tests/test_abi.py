@@ -22,7 +22,7 @@ def built():
 def header_symbols():
     src = open(os.path.join(ROOT, "include", "gpt2b300.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(gpt2_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(gpt2(?:op)?_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_library_exports_every_declared_symbol():

@@ -1,0 +1,89 @@
+"""Per-layer parity of the tensor-core matmul (tcgen05, 3xTF32) against the
+oracle's matmul_forward / matmul_backward (the page «llm.c：Andrej Karpathy
+带你从零复现LLM», section «核心代码解读：train_gpt2.c», item 1).  Shapes cover
+ragged M, N and K (partial 128x128 tiles and partial 32-wide K tiles),
+split-K (small N with long K) and both operand layouts of each product."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import ref
+
+pytestmark = pytest.mark.gpu
+
+OPS = ref.ops(np.float32)
+
+SHAPES = [  # (N rows, IC, OC)
+    (64, 64, 192),      # tiny config QKV
+    (13, 68, 100),      # ragged everything
+    (1, 64, 64),        # one row
+    (300, 96, 260),     # M spans 3 tiles with a tail
+    (256, 768, 2304),   # 124M QKV at B*T=256: split-K
+    (256, 3072, 768),   # 124M MLP output projection: split-K over 3072
+    (256, 768, 50304),  # LM head (tied wte), 393 column tiles
+]
+
+
+def tol(K):
+    """3xTF32 products are ~2^-20 relative; the tensor core's fp32
+    accumulation adds an error that grows with the summed length K."""
+    return 1e-5 if K <= 4096 else 1e-4
+
+
+def rel_err(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return np.abs(a - b).max() / max(np.abs(b).max(), 1e-30)
+
+
+@pytest.mark.parametrize("N,IC,OC", SHAPES)
+def test_matmul_forward_backward_fp32(N, IC, OC):
+    import torch
+    import gpt2_train_step_02_b300 as g
+
+    x = synth.randn(101, (N, IC))
+    W = synth.randn(102, (OC, IC), 0.02)
+    b = synth.randn(103, (OC,), 0.1)
+    dy = synth.randn(104, (N, OC))
+    dW0 = synth.randn(105, (OC, IC), 0.01)
+    db0 = synth.randn(106, (OC,), 0.01)
+
+    tx, tW, tb, tdy = (torch.tensor(a, device="cuda") for a in (x, W, b, dy))
+    out = torch.empty((N, OC), dtype=torch.float32, device="cuda")
+    g.matmul_forward(out, tx, tW, tb)
+    ref_out = OPS.matmul_forward(x, W, b)
+    assert rel_err(out.cpu().numpy(), ref_out) < tol(IC)
+
+    out0 = torch.empty((N, OC), dtype=torch.float32, device="cuda")
+    g.matmul_forward(out0, tx, tW, None)
+    assert rel_err(out0.cpu().numpy(), OPS.matmul_forward(x, W, None)) < tol(IC)
+
+    dx = torch.empty((N, IC), dtype=torch.float32, device="cuda")
+    tdW = torch.tensor(dW0, device="cuda")
+    tdb = torch.tensor(db0, device="cuda")
+    g.matmul_backward(dx, tdW, tdb, tdy, tx, tW)
+    rdx, rdW, rdb = OPS.matmul_backward(dy, x, W, True)
+    assert rel_err(dx.cpu().numpy(), rdx) < tol(OC)
+    assert rel_err(tdW.cpu().numpy() - dW0, rdW) < tol(N)
+    assert rel_err(tdb.cpu().numpy() - db0, rdb) < 1e-5
+
+
+def test_matmul_bf16_operands():
+    import torch
+    import gpt2_train_step_02_b300 as g
+
+    N, IC, OC = 256, 768, 2304
+    x = synth.randn(111, (N, IC))
+    W = synth.randn(112, (OC, IC), 0.02)
+    out = torch.empty((N, OC), dtype=torch.float32, device="cuda")
+    g.matmul_forward(out, torch.tensor(x, device="cuda"), torch.tensor(W, device="cuda"), None,
+                     precision=g.GPT2_PREC_BF16)
+
+    def bf16(a):  # round to nearest even at 16 bits
+        u = a.astype(np.float32).view(np.uint32).astype(np.uint64)
+        u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+        return u.astype(np.uint32).view(np.float32)
+
+    ref_out = OPS.matmul_forward(bf16(x), bf16(W), None)
+    assert rel_err(out.cpu().numpy(), ref_out) < 1e-5
+    assert rel_err(out.cpu().numpy(), OPS.matmul_forward(x, W, None)) > 1e-4  # really bf16

@@ -15,7 +15,6 @@ import torch.nn.functional as F
 import synth
 from oracle import ref
 
-torch.set_default_dtype(torch.float64)
 OPS = ref.ops(np.float64)
 RTOL = 1e-10
 
@@ -29,7 +28,7 @@ def close(a, b, rtol=RTOL):
 
 
 def leaf(x):
-    return torch.tensor(np.asarray(x), dtype=torch.float64, requires_grad=True)
+    return torch.tensor(np.asarray(x, dtype=np.float64), dtype=torch.float64, requires_grad=True)
 
 
 def test_encoder_vs_embedding():
