@@ -187,7 +187,7 @@ def workload_config(w, n_gpus):
 def run_ours(args, w):
     import torch
 
-    import gpt2_train_step_02_b300 as g
+    import gpt_train_step_02_b300 as g
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -62,7 +62,7 @@ def lib() -> ct.CDLL:
     global _LIB
     if _LIB is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m gpt2_train_step_02_b300.build`")
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m gpt_train_step_02_b300.build`")
         L = ct.CDLL(LIB_PATH)
         P, I, F, LL, SZ = ct.c_void_p, ct.c_int, ct.c_float, ct.c_longlong, ct.c_size_t
         CFG = ct.POINTER(gpt2_config)

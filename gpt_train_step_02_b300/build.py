@@ -1,6 +1,6 @@
 """Build libgpt2b300.so in-tree with nvcc for sm_103a.
 
-    python -m gpt2_train_step_02_b300.build [--force]
+    python -m gpt_train_step_02_b300.build [--force]
 
 The library is compiled from csrc/gpt2.cu (which includes the kernel headers)
 with the CUDA runtime linked statically, so loading it needs no GPU and no

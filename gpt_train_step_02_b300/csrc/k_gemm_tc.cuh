@@ -39,7 +39,7 @@ constexpr int COMP_STAGES = 2;
 constexpr int TILE_BYTES = BM * BK * 4;  // 16 KB (A or B tile)
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 128;
-constexpr uint32_t SPIN_LIMIT = 1u << 26;  // polls per wait before giving up (seconds)
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s of wall time per wait before giving up
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int OFF_RAW_A = 0;
@@ -87,17 +87,41 @@ GPT2_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+GPT2_DEV uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
 // Bounded wait: returns false (and raises the CTA's abort flag and the
-// device error word) if the phase does not complete within SPIN_LIMIT polls
-// or another role of the CTA has aborted.
+// device error word) if the phase does not complete within WAIT_LIMIT_NS of
+// wall time or another role of the CTA has aborted.  try_wait may suspend
+// the thread for a hardware-defined interval, so the bound is taken on the
+// global timer rather than on a poll count.
 GPT2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
-  for (uint32_t i = 0; i < SPIN_LIMIT; i++) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; i++) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023) == 1023 && *abort_flag) return false;
+    if ((i & 255) == 0) {
+      if (*abort_flag) return false;
+      uint64_t now = globaltimer_ns();
+      if (i == 0) t0 = now;
+      else if (now - t0 > WAIT_LIMIT_NS) break;
+    }
   }
   *abort_flag = 1;
   dev_set_error(err, DEV_ERR_TIMEOUT);
   return false;
+}
+
+// Drain wait used on the abort path (copies or MMAs already in flight must
+// land before the CTA frees its resources); bounded the same way.
+GPT2_DEV void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; i++) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 255) == 255 && globaltimer_ns() - t0 > WAIT_LIMIT_NS) return;
+  }
 }
 
 GPT2_DEV void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
@@ -257,8 +281,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (*abort_flag) {
         for (int i = max(0, issued - RAW_STAGES); i < issued; i++) {
           int s = i % RAW_STAGES;
-          for (uint32_t q = 0; q < SPIN_LIMIT && !mbar_try_wait(&raw_full[s], (i / RAW_STAGES) & 1); q++) {
-          }
+          mbar_wait_drain(&raw_full[s], (i / RAW_STAGES) & 1);
         }
       }
     }
@@ -291,8 +314,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // wait for it here so that TMEM is not freed under running MMAs
       if (nk > 0) mma_commit(acc_full);
       if (!ok && nk > 0) {
-        for (uint32_t q = 0; q < SPIN_LIMIT && !mbar_try_wait(acc_full, 0); q++) {
-        }
+        mbar_wait_drain(acc_full, 0);
       }
     }
   } else {

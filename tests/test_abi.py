@@ -7,9 +7,9 @@ import re
 
 import pytest
 
-import gpt2_train_step_02_b300 as g
+import gpt_train_step_02_b300 as g
 import synth
-from gpt2_train_step_02_b300 import build as gbuild
+from gpt_train_step_02_b300 import build as gbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 

@@ -39,7 +39,7 @@ def rel_err(a, b):
 @pytest.mark.parametrize("N,IC,OC", SHAPES)
 def test_matmul_forward_backward_fp32(N, IC, OC):
     import torch
-    import gpt2_train_step_02_b300 as g
+    import gpt_train_step_02_b300 as g
 
     x = synth.randn(101, (N, IC))
     W = synth.randn(102, (OC, IC), 0.02)
@@ -70,7 +70,7 @@ def test_matmul_forward_backward_fp32(N, IC, OC):
 
 def test_matmul_bf16_operands():
     import torch
-    import gpt2_train_step_02_b300 as g
+    import gpt_train_step_02_b300 as g
 
     N, IC, OC = 256, 768, 2304
     x = synth.randn(111, (N, IC))

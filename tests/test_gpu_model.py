@@ -22,7 +22,7 @@ G124 = synth.WORKLOADS["gpt2_124m_B4_T64_fp32"]
 
 def gpu_model(w, **kw):
     import torch
-    import gpt2_train_step_02_b300 as g
+    import gpt_train_step_02_b300 as g
 
     assert torch.cuda.is_available()
     return g.GPT2(w, **kw)
@@ -115,7 +115,7 @@ def test_tiny_trajectory_10_steps():
 
 
 def test_forward_without_targets_and_state_errors():
-    import gpt2_train_step_02_b300 as g
+    import gpt_train_step_02_b300 as g
 
     w = TINY
     p0 = perturbed(w)
@@ -137,7 +137,7 @@ def test_forward_without_targets_and_state_errors():
 
 def test_token_range_errors_host_and_device():
     import torch
-    import gpt2_train_step_02_b300 as g
+    import gpt_train_step_02_b300 as g
 
     w = TINY
     m = gpu_model(w)
