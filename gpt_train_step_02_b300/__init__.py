@@ -40,6 +40,7 @@ EXPORTS = [
     "gpt2_get_params", "gpt2_set_params", "gpt2_get_grads", "gpt2_get_opt_state", "gpt2_set_opt_state",
     "gpt2_get_logits", "gpt2_last_launch_count", "gpt2_status_string", "gpt2_train_step", "gpt2_kernel_timer",
     "gpt2_kernel_timer_read", "gpt2op_matmul_workspace_bytes", "gpt2op_matmul_forward", "gpt2op_matmul_backward",
+    "gpt2op_matmul_backward_noalloc",
 ]
 
 
@@ -91,6 +92,7 @@ def lib() -> ct.CDLL:
             "gpt2op_matmul_workspace_bytes": (SZ, [I, I]),
             "gpt2op_matmul_forward": (I, [P, P, P, P, I, I, I, I, P, P]),
             "gpt2op_matmul_backward": (I, [P, P, P, P, P, P, I, I, I, I, P, P]),
+            "gpt2op_matmul_backward_noalloc": (I, [P, P, P, P, P, P, I, I, I, I, P]),
             "gpt2_kernel_timer_read": (I, [P, ct.POINTER(ct.c_double), ct.POINTER(LL), ct.POINTER(ct.c_double)]),
         }
         for name, (res, args) in sig.items():
@@ -359,3 +361,19 @@ def matmul_backward(dx, dW, dbias, dy, x, W, precision=GPT2_PREC_FP32, stream=No
     s = stream or torch.cuda.current_stream()
     _check(lib().gpt2op_matmul_backward(_dptr(dx), _dptr(dW), _dptr(dbias), _dptr(dy), _dptr(x), _dptr(W), N, IC,
                                         OC, precision, _dptr(ws), s.cuda_stream), "gpt2op_matmul_backward")
+
+
+def matmul_backward_noalloc(dx, dW, dbias, dy, x, W, precision=GPT2_PREC_FP32, stream=None):
+    """matmul_backward for callers that cannot allocate device memory: the
+    library takes its scratch from a fixed array of its own (8 MiB per GPU,
+    held until exit) instead of a workspace.  Calls that overlap on one GPU
+    race on that array.  Raises GPT2Error (GPT2_ERR_SHAPE) when
+    ceil(N/64) * OC > 1,048,576 with a bias gradient."""
+    import torch
+
+    OC, IC = W.shape
+    N = x.numel() // IC
+    s = stream or torch.cuda.current_stream()
+    _check(lib().gpt2op_matmul_backward_noalloc(_dptr(dx), _dptr(dW), _dptr(dbias), _dptr(dy), _dptr(x), _dptr(W),
+                                                N, IC, OC, precision, s.cuda_stream),
+           "gpt2op_matmul_backward_noalloc")

@@ -16,6 +16,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -287,13 +289,13 @@ struct MatmulDesc {
 
 // Split K so that small-M products still fill the 148 SMs; the split-K
 // partial sums (<= SPLITK_WS_FLOATS) are reduced in a fixed order.
-static int choose_splits(int M, int N, int K) {
+static int choose_splits(int M, int N, int K, long long ws_floats = SPLITK_WS_FLOATS) {
   long long tiles = (long long)ceil_div(M, tc::BM) * ceil_div(N, tc::BN);
   int kt = ceil_div(K, tc::BK);
   if (tiles >= 148 || kt < 4) return 1;
   int s = (int)(148 / tiles);
   s = s < kt / 2 ? s : kt / 2;
-  while (s > 1 && (long long)s * M * N > SPLITK_WS_FLOATS) s--;
+  while (s > 1 && (long long)s * M * N > ws_floats) s--;
   if (s < 1) s = 1;
   int per = ceil_div(kt, s);
   return ceil_div(kt, per);
@@ -301,11 +303,12 @@ static int choose_splits(int M, int N, int K) {
 
 // Launches the tensor-core matmul (+ the split-K reduction when K is split).
 // Returns the number of kernels launched, or -1 on a host-side failure.
-static int launch_matmul(const MatmulDesc& d, float* ws, int* err, cudaStream_t s) {
+static int launch_matmul(const MatmulDesc& d, float* ws, int* err, cudaStream_t s,
+                         long long ws_floats = SPLITK_WS_FLOATS) {
   CUtensorMap ta, tb;
   if (!make_operand_map(&ta, d.A, d.a_kmajor, d.a_kmajor ? d.M : d.K, d.a_kmajor ? d.K : d.M, d.lda)) return -1;
   if (!make_operand_map(&tb, d.B, d.b_kmajor, d.b_kmajor ? d.N : d.K, d.b_kmajor ? d.K : d.N, d.ldb)) return -1;
-  int splits = choose_splits(d.M, d.N, d.K);
+  int splits = choose_splits(d.M, d.N, d.K, ws_floats);
   tc::Params p;
   p.M = d.M;
   p.N = d.N;
@@ -957,6 +960,7 @@ struct OpWs {
   int* err;
   float* bias_partial;
   float* splitk;
+  long long splitk_floats;
 };
 
 static OpWs op_ws(void* ws, int N, int OC) {
@@ -966,6 +970,7 @@ static OpWs op_ws(void* ws, int N, int OC) {
   w.err = (int*)b;
   w.bias_partial = (float*)(b + 256);
   w.splitk = (float*)(b + 256 + ((bias + 255) & ~(size_t)255));
+  w.splitk_floats = SPLITK_WS_FLOATS;
   return w;
 }
 
@@ -980,7 +985,7 @@ static int op_matmul(const MatmulDesc& d, int precision, const OpWs& w, cudaStre
     gemm_simt_launch(a, s);
     return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
   }
-  if (launch_matmul(d, w.splitk, w.err, s) < 0) return GPT2_ERR_CUDA;
+  if (launch_matmul(d, w.splitk, w.err, s, w.splitk_floats) < 0) return GPT2_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
@@ -1024,6 +1029,81 @@ EXPORT int gpt2op_matmul_backward(float* dx, float* dW, float* dbias, const floa
   int rc = op_prepare(workspace, s);
   if (rc) return rc;
   OpWs w = op_ws(workspace, N, OC);
+  MatmulDesc ddx = {N, IC, OC, dy, OC, 1, W, IC, 0, epi_args(dx, IC, EPI_STORE)};
+  if ((rc = op_matmul(ddx, precision, w, s))) return rc;
+  MatmulDesc ddw = {OC, IC, N, dy, OC, 0, x, IC, 0, epi_args(dW, IC, EPI_ACCUM)};
+  if ((rc = op_matmul(ddw, precision, w, s))) return rc;
+  if (dbias) {
+    int chunks = ceil_div(N, 64);
+    col_partial_kernel<<<dim3(ceil_div(OC, 256), chunks), 256, 0, s>>>(dy, N, OC, OC, 64, w.bias_partial);
+    col_finish_kernel<<<ceil_div(OC, 256), 256, 0, s>>>(w.bias_partial, chunks, OC, dbias);
+    if (cudaGetLastError() != cudaSuccess) return GPT2_ERR_CUDA;
+  }
+  return op_status(w, s);
+}
+
+// ---------------------------------------------------------------------------
+// matmul backward with library-owned scratch (no allocation by anyone)
+// ---------------------------------------------------------------------------
+// The scratch of gpt2op_matmul_backward (error word, column-sum partials of
+// the bias gradient, split-K partials) is taken from one fixed array in the
+// library's device memory.  Every GPU that loads the library holds it until
+// the process exits.  Layout: [error word, 256 B][column-sum partials,
+// NOALLOC_BIAS_FLOATS][split-K partials, the rest].
+#define NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+#define NOALLOC_BIAS_FLOATS ((long long)1 << 20)
+#define NOALLOC_SPLITK_OFFSET ((size_t)256 + (size_t)NOALLOC_BIAS_FLOATS * sizeof(float))
+#define NOALLOC_MAX_DEVICES 64
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+// In host code g_noalloc_scratch names a host-side stand-in, not the device
+// array, so the device address is looked up once per device (with that
+// device current) and cached.
+static void* g_noalloc_addr[NOALLOC_MAX_DEVICES];
+static std::mutex g_noalloc_mu;
+
+static int noalloc_scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES) {
+    cudaGetLastError();
+    return GPT2_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      fprintf(stderr, "gpt2b300: cudaGetSymbolAddress(scratch) failed on device %d: %s\n", dev,
+              cudaGetErrorString(e));
+      cudaGetLastError();
+      return GPT2_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return GPT2_OK;
+}
+
+EXPORT int gpt2op_matmul_backward_noalloc(float* dx, float* dW, float* dbias, const float* dy, const float* x,
+                                          const float* W, int N, int IC, int OC, int precision, void* stream) {
+  if (!dx || !dW || !dy || !x || !W || N < 1 || IC < 1 || OC < 1) return GPT2_ERR_ARG;
+  if ((IC * 4) % 16 || (OC * 4) % 16) return GPT2_ERR_SHAPE;
+  if (dbias && (long long)ceil_div(N, 64) * OC > NOALLOC_BIAS_FLOATS) {
+    fprintf(stderr, "gpt2b300: gpt2op_matmul_backward_noalloc: ceil(N/64)*OC = %lld exceeds the fixed scratch "
+            "(%lld floats)\n", (long long)ceil_div(N, 64) * OC, NOALLOC_BIAS_FLOATS);
+    return GPT2_ERR_SHAPE;
+  }
+  void* base = nullptr;
+  int rc = noalloc_scratch_address(&base);
+  if (rc) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((rc = op_prepare(base, s))) return rc;  // clears the error word
+  OpWs w;
+  w.err = (int*)base;
+  w.bias_partial = (float*)((char*)base + 256);
+  w.splitk = (float*)((char*)base + NOALLOC_SPLITK_OFFSET);
+  w.splitk_floats = (long long)((NOALLOC_SCRATCH_BYTES - NOALLOC_SPLITK_OFFSET) / sizeof(float));
   MatmulDesc ddx = {N, IC, OC, dy, OC, 1, W, IC, 0, epi_args(dx, IC, EPI_STORE)};
   if ((rc = op_matmul(ddx, precision, w, s))) return rc;
   MatmulDesc ddw = {OC, IC, N, dy, OC, 0, x, IC, 0, epi_args(dW, IC, EPI_ACCUM)};

@@ -192,6 +192,29 @@ int gpt2op_matmul_forward(float* out, const float* x, const float* W, const floa
 int gpt2op_matmul_backward(float* dx, float* dW, float* dbias, const float* dy, const float* x, const float* W,
                            int N, int IC, int OC, int precision, void* workspace, void* stream);
 
+/* gpt2op_matmul_backward without a workspace argument: the same products
+ * (dx = dy W; dW += dy^T x; dbias += column sums of dy, dbias may be NULL)
+ * with the same arguments minus `workspace`.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory --
+ * for example a plugin inside a host application whose allocator already
+ * owns the device's memory, or a loop that must not call cudaMalloc because
+ * it can synchronise the device.  It allocates nothing and calls no
+ * allocating routine.
+ * Scratch: one fixed 8 MiB array in the library's device memory, which every
+ * GPU that loads the library holds until the process exits.  The first call
+ * on a device looks up that array's device address (cudaGetSymbolAddress,
+ * with the device current) and caches it; make that first call before any
+ * stream capture.  Every call on a device shares the array, and each call
+ * clears the part that must start at zero: calls that overlap on the GPU
+ * (different streams, or different host threads on one device) race and
+ * give wrong results.
+ * Limit: with dbias != NULL, ceil(N/64) * OC must be <= 1,048,576 (for
+ * example N = 16384 with OC <= 4096); larger shapes return GPT2_ERR_SHAPE
+ * before any device work.  The split-K partials use the rest of the array,
+ * which only lowers how far K is split.  Synchronises the stream. */
+int gpt2op_matmul_backward_noalloc(float* dx, float* dW, float* dbias, const float* dy, const float* x,
+                                   const float* W, int N, int IC, int OC, int precision, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* gpt2_status_string(int status);
 
