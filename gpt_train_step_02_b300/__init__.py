@@ -40,7 +40,7 @@ EXPORTS = [
     "gpt2_get_params", "gpt2_set_params", "gpt2_get_grads", "gpt2_get_opt_state", "gpt2_set_opt_state",
     "gpt2_get_logits", "gpt2_last_launch_count", "gpt2_status_string", "gpt2_train_step", "gpt2_kernel_timer",
     "gpt2_kernel_timer_read", "gpt2op_matmul_workspace_bytes", "gpt2op_matmul_forward", "gpt2op_matmul_backward",
-    "gpt2op_matmul_backward_noalloc",
+    "gpt2op_matmul_backward_noalloc", "gpt2op_attention_workspace_bytes", "gpt2op_attention_forward",
 ]
 
 
@@ -89,10 +89,12 @@ def lib() -> ct.CDLL:
             "gpt2_status_string": (ct.c_char_p, [I]),
             "gpt2_train_step": (I, [P, P, P, I, I, F, F, F, F, F, I, P]),
             "gpt2_kernel_timer": (I, [P, I]),
-            "gpt2op_matmul_workspace_bytes": (SZ, [I, I]),
+            "gpt2op_matmul_workspace_bytes": (SZ, [I, I, I]),
             "gpt2op_matmul_forward": (I, [P, P, P, P, I, I, I, I, P, P]),
             "gpt2op_matmul_backward": (I, [P, P, P, P, P, P, I, I, I, I, P, P]),
             "gpt2op_matmul_backward_noalloc": (I, [P, P, P, P, P, P, I, I, I, I, P]),
+            "gpt2op_attention_workspace_bytes": (SZ, [I, I, I]),
+            "gpt2op_attention_forward": (I, [P, P, P, I, I, I, I, I, P, P]),
             "gpt2_kernel_timer_read": (I, [P, ct.POINTER(ct.c_double), ct.POINTER(LL), ct.POINTER(ct.c_double)]),
         }
         for name, (res, args) in sig.items():
@@ -345,7 +347,7 @@ def matmul_forward(out, x, W, bias=None, precision=GPT2_PREC_FP32, stream=None):
 
     OC, IC = W.shape
     N = x.numel() // IC
-    ws = torch.empty(lib().gpt2op_matmul_workspace_bytes(N, OC), dtype=torch.uint8, device=x.device)
+    ws = torch.empty(lib().gpt2op_matmul_workspace_bytes(N, IC, OC), dtype=torch.uint8, device=x.device)
     s = stream or torch.cuda.current_stream()
     _check(lib().gpt2op_matmul_forward(_dptr(out), _dptr(x), _dptr(W), _dptr(bias), N, IC, OC, precision,
                                        _dptr(ws), s.cuda_stream), "gpt2op_matmul_forward")
@@ -357,10 +359,22 @@ def matmul_backward(dx, dW, dbias, dy, x, W, precision=GPT2_PREC_FP32, stream=No
 
     OC, IC = W.shape
     N = x.numel() // IC
-    ws = torch.empty(lib().gpt2op_matmul_workspace_bytes(N, OC), dtype=torch.uint8, device=x.device)
+    ws = torch.empty(lib().gpt2op_matmul_workspace_bytes(N, IC, OC), dtype=torch.uint8, device=x.device)
     s = stream or torch.cuda.current_stream()
     _check(lib().gpt2op_matmul_backward(_dptr(dx), _dptr(dW), _dptr(dbias), _dptr(dy), _dptr(x), _dptr(W), N, IC,
                                         OC, precision, _dptr(ws), s.cuda_stream), "gpt2op_matmul_backward")
+
+
+def attention_forward(y, lse, qkv, NH, precision=GPT2_PREC_FP32, stream=None):
+    """Causal attention forward: y (B,T,C), lse (B,NH,T) from qkv (B,T,3C)."""
+    import torch
+
+    B, T, C3 = qkv.shape
+    C = C3 // 3
+    ws = torch.empty(lib().gpt2op_attention_workspace_bytes(B, T, C), dtype=torch.uint8, device=qkv.device)
+    s = stream or torch.cuda.current_stream()
+    _check(lib().gpt2op_attention_forward(_dptr(y), _dptr(lse), _dptr(qkv), B, T, C, NH, precision, _dptr(ws),
+                                          s.cuda_stream), "gpt2op_attention_forward")
 
 
 def matmul_backward_noalloc(dx, dW, dbias, dy, x, W, precision=GPT2_PREC_FP32, stream=None):

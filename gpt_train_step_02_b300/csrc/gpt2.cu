@@ -25,7 +25,8 @@
 #include "../../include/gpt2b300.h"
 #include "common.cuh"
 #include "k_attention_simt.cuh"
-#include "k_gemm_simt.cuh"
+#include "k_attention_tc.cuh"
+#include "k_gemm_bf16.cuh"
 #include "k_gemm_tc.cuh"
 #include "k_layernorm.cuh"
 #include "k_misc.cuh"
@@ -33,8 +34,14 @@
 
 #define EXPORT extern "C" __attribute__((visibility("default")))
 
-// split-K workspace: at most 148 partial 128x128 tiles
-#define SPLITK_WS_FLOATS ((long long)148 * 128 * 128)
+// split-K workspace (fp32 partial tiles), 32 MB
+#define SPLITK_WS_FLOATS ((long long)8 << 20)
+// split-K arrival counters: K is split only when there are fewer than 148 tiles
+#define TILE_CTRS 256
+// op workspaces start with [error word, 256 B][tile counters, 1 KB]
+#define OP_HDR_BYTES 1280
+// smallest row chunk of the bias-gradient column sums
+#define BIAS_MIN_ROWS 16
 
 enum {
   P_WTE, P_WPE, P_LN1W, P_LN1B, P_QKVW, P_QKVB, P_ATTPROJW, P_ATTPROJB,
@@ -49,7 +56,9 @@ struct Plan {
   size_t params, grads, m, v, params_bf;
   size_t encoded, ln1, ln1_mean, ln1_rstd, qkv, atty, lse, res2, ln2, ln2_mean, ln2_rstd, fch, fchg, res3;
   size_t lnf, lnf_mean, lnf_rstd, logits, dlogits, losses, loss;
-  size_t dres, dln, datty, dqkv, dfch, attD, scratch, sorted, tokens, targets, err, hparams, splitk;
+  size_t dres, dln, datty, dqkv, dfch, attD, scratch, sorted, tokens, targets, err, hparams, splitk, tilectr;
+  // bf16 operand copies (bf16 matmuls only)
+  size_t ln1_bf, qkv_bf, atty_bf, ln2_bf, fchg_bf, lnf_bf, dlogits_bf, dres_bf, dfch_bf, dqkv_bf;
   size_t scratch_floats;
 };
 
@@ -126,9 +135,10 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->dqkv = take(BT * 3 * C * F);
   p->dfch = take(BT * 4 * C * F);
   p->attD = take(BT * NH * F);
-  // scratch: column-sum partials (<= ceil(BT/64) x 4C) and layernorm
-  // partials (ceil(BT/32) x 2C)
-  size_t s1 = ((BT + 63) / 64) * 4 * C, s2 = ((BT + LNB_ROWS - 1) / LNB_ROWS) * 2 * C;
+  // scratch: column-sum partials (<= ceil(BT/BIAS_MIN_ROWS) x 4C) and
+  // layernorm partials (<= ceil(BT/LNB_MIN_ROWS) x 2C)
+  size_t s1 = ((BT + BIAS_MIN_ROWS - 1) / BIAS_MIN_ROWS) * 4 * C;
+  size_t s2 = ((BT + LNB_MIN_ROWS - 1) / LNB_MIN_ROWS) * 2 * C;
   p->scratch_floats = s1 > s2 ? s1 : s2;
   p->scratch = take(p->scratch_floats * F);
   p->sorted = take(BT * sizeof(uint32_t));
@@ -137,6 +147,18 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->err = take(sizeof(int));
   p->hparams = take(16 * F);
   p->splitk = take(SPLITK_WS_FLOATS * F);
+  p->tilectr = take(TILE_CTRS * sizeof(int));
+  const size_t H = c->gemm_precision == GPT2_PREC_BF16 ? 2 : 0;  // bytes per bf16 copy element (0: none)
+  p->ln1_bf = take(L * BT * C * H);
+  p->qkv_bf = take(L * BT * 3 * C * H);
+  p->atty_bf = take(L * BT * C * H);
+  p->ln2_bf = take(L * BT * C * H);
+  p->fchg_bf = take(L * BT * 4 * C * H);
+  p->lnf_bf = take(BT * C * H);
+  p->dlogits_bf = take(BT * Vp * H);
+  p->dres_bf = take(BT * C * H);
+  p->dfch_bf = take(BT * 4 * C * H);
+  p->dqkv_bf = take(BT * 3 * C * H);
   p->total = off;
   return off;
 }
@@ -162,7 +184,8 @@ struct gpt2_t {
   float *lnf, *lnf_mean, *lnf_rstd, *logits, *dlogits, *losses, *loss;
   float *dres, *dln, *datty, *dqkv, *dfch, *attD, *scratch, *splitk;
   uint32_t* sorted;
-  int *tokens, *targets, *err;
+  int *tokens, *targets, *err, *tilectr;
+  uint16_t *ln1_bf, *qkv_bf, *atty_bf, *ln2_bf, *fchg_bf, *lnf_bf, *dlogits_bf, *dres_bf, *dfch_bf, *dqkv_bf;
   float* hparams;
   int B, T, have_targets, fwd_done;
   int poisoned;
@@ -275,7 +298,8 @@ static int make_operand_map(CUtensorMap* tm, const float* base, int kmajor, long
   return r == CUDA_SUCCESS;
 }
 
-// One matmul acc(i,j) = sum_k A(i,k) B(j,k) with a fused epilogue.
+// One matmul acc(i,j) = sum_k A(i,k) B(j,k) with a fused epilogue.  The
+// fp32 pointers feed the 3xTF32 kernel, the bf16 ones the bf16 kernel.
 struct MatmulDesc {
   int M, N, K;
   const float* A;
@@ -285,30 +309,33 @@ struct MatmulDesc {
   long long ldb;
   int b_kmajor;  // 1: B stored (N, ldb) with K contiguous; 0: stored (K, ldb) with N contiguous
   EpiArgs epi;
+  const uint16_t* Abf;  // the same operands in bf16 (bf16 matmuls)
+  const uint16_t* Bbf;
 };
 
-// Split K so that small-M products still fill the 148 SMs; the split-K
-// partial sums (<= SPLITK_WS_FLOATS) are reduced in a fixed order.
-static int choose_splits(int M, int N, int K, long long ws_floats = SPLITK_WS_FLOATS) {
+// Split K so that small-M products still fill the 148 SMs.  The splits of a
+// tile form one thread-block cluster (at most 8 CTAs, the portable cluster
+// size) and are reduced through distributed shared memory in split order.
+static int choose_splits(int M, int N, int K) {
   long long tiles = (long long)ceil_div(M, tc::BM) * ceil_div(N, tc::BN);
   int kt = ceil_div(K, tc::BK);
   if (tiles >= 148 || kt < 4) return 1;
   int s = (int)(148 / tiles);
   s = s < kt / 2 ? s : kt / 2;
-  while (s > 1 && (long long)s * M * N > ws_floats) s--;
+  s = s < 8 ? s : 8;
   if (s < 1) s = 1;
   int per = ceil_div(kt, s);
   return ceil_div(kt, per);
 }
 
-// Launches the tensor-core matmul (+ the split-K reduction when K is split).
-// Returns the number of kernels launched, or -1 on a host-side failure.
-static int launch_matmul(const MatmulDesc& d, float* ws, int* err, cudaStream_t s,
-                         long long ws_floats = SPLITK_WS_FLOATS) {
+// Launches the 3xTF32 tensor-core matmul (one launch; K splits reduced in
+// the cluster).  Returns the number of kernels launched, or -1 on a host-side
+// failure.
+static int launch_matmul(const MatmulDesc& d, cudaStream_t s, int* err) {
   CUtensorMap ta, tb;
   if (!make_operand_map(&ta, d.A, d.a_kmajor, d.a_kmajor ? d.M : d.K, d.a_kmajor ? d.K : d.M, d.lda)) return -1;
   if (!make_operand_map(&tb, d.B, d.b_kmajor, d.b_kmajor ? d.N : d.K, d.b_kmajor ? d.K : d.N, d.ldb)) return -1;
-  int splits = choose_splits(d.M, d.N, d.K, ws_floats);
+  int splits = choose_splits(d.M, d.N, d.K);
   tc::Params p;
   p.M = d.M;
   p.N = d.N;
@@ -318,33 +345,99 @@ static int launch_matmul(const MatmulDesc& d, float* ws, int* err, cudaStream_t 
   p.k_tiles = ceil_div(d.K, tc::BK);
   p.kt_per_split = ceil_div(p.k_tiles, splits);
   p.epi = d.epi;
-  p.partial = splits > 1 ? ws : nullptr;
+  p.splits = splits;
   p.err = err;
-  dim3 grid(ceil_div(d.N, tc::BN), ceil_div(d.M, tc::BM), splits);
-  tc::gemm_tf32x3_kernel<<<grid, tc::THREADS, tc::SMEM_BYTES, s>>>(ta, tb, p);
-  if (splits == 1) return 1;
-  long long total = (long long)d.M * d.N;
-  splitk_reduce_kernel<<<grid_for(total, 256), 256, 0, s>>>(ws, splits, d.M, d.N, d.epi);
-  return 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ceil_div(d.N, tc::BN), ceil_div(d.M, tc::BM), splits);
+  cfg.blockDim = dim3(tc::THREADS);
+  cfg.dynamicSmemBytes = tc::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = splits;
+  cfg.attrs = attr;
+  cfg.numAttrs = splits > 1 ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, tc::gemm_tf32x3_kernel, ta, tb, p) != cudaSuccess) return -1;
+  return 1;
+}
+
+// Tensor map of a bf16 operand stored as `outer` rows of pitch `ld` elements
+// with `inner` valid contiguous elements per row, 128-byte swizzle.  K-major
+// boxes are 64 (K) x box_rows; MN-major boxes are 64 (MN) x 64 (K).
+// Out-of-range elements load as zero.
+static int make_bf16_map(CUtensorMap* tm, const uint16_t* base, int kmajor, long long outer, long long inner,
+                         long long ld, int box_rows) {
+  if (!get_encoder()) return 0;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box_k[2] = {(cuuint32_t)tcb::BK, (cuuint32_t)box_rows};
+  cuuint32_t box_mn[2] = {(cuuint32_t)tcb::MN_BOX, (cuuint32_t)tcb::BK};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode_tiled(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)base, dims, strides,
+                              kmajor ? box_k : box_mn, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// K splits for the persistent bf16 kernel: only when there are fewer output
+// tiles than SMs, keeping at least four 64-wide K tiles per split.
+static int choose_splits_bf16(int M, int N, int K, int BN, long long ws_floats) {
+  long long tiles = (long long)ceil_div(M, tcb::BM) * ceil_div(N, BN);
+  int kt = ceil_div(K, tcb::BK);
+  if (tiles >= 148 || kt < 8) return 1;
+  int s = (int)(148 / tiles);
+  s = s < kt / 4 ? s : kt / 4;
+  while (s > 1 && (long long)s * M * N > ws_floats) s--;
+  if (s < 1) s = 1;
+  int per = ceil_div(kt, s);
+  return ceil_div(kt, per);
+}
+
+template <int BN>
+static void launch_bf16_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const tcb::Params& p, int grid,
+                               cudaStream_t s) {
+  tcb::gemm_bf16_kernel<BN><<<grid, tcb::THREADS, tcb::Cfg<BN>::SMEM_BYTES, s>>>(ta, tb, p);
+}
+
+// Launches the persistent bf16 tensor-core matmul.  Output tiles are 128 x 256
+// (128 x 128 when N <= 128).  Returns 1, or -1 on a host-side failure.
+static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int* err, cudaStream_t s,
+                              long long ws_floats = SPLITK_WS_FLOATS) {
+  if (!d.Abf || !d.Bbf) return -1;
+  const int BN = d.N > 128 ? 256 : 128;
+  CUtensorMap ta, tb;
+  if (!make_bf16_map(&ta, d.Abf, d.a_kmajor, d.a_kmajor ? d.M : d.K, d.a_kmajor ? d.K : d.M, d.lda, tcb::BM))
+    return -1;
+  if (!make_bf16_map(&tb, d.Bbf, d.b_kmajor, d.b_kmajor ? d.N : d.K, d.b_kmajor ? d.K : d.N, d.ldb, BN)) return -1;
+  tcb::Params p;
+  p.M = d.M;
+  p.N = d.N;
+  p.K = d.K;
+  p.a_kmajor = d.a_kmajor;
+  p.b_kmajor = d.b_kmajor;
+  p.splits = choose_splits_bf16(d.M, d.N, d.K, BN, ws_floats);
+  p.k_tiles = ceil_div(d.K, tcb::BK);
+  p.kt_per_split = ceil_div(p.k_tiles, p.splits);
+  p.tiles_m = ceil_div(d.M, tcb::BM);
+  p.tiles_n = ceil_div(d.N, BN);
+  p.units = p.tiles_m * p.tiles_n * p.splits;
+  p.epi = d.epi;
+  p.partial = p.splits > 1 ? ws : nullptr;
+  p.tile_ctr = tile_ctr;
+  p.err = err;
+  int grid = p.units < 148 ? p.units : 148;
+  if (BN == 256) launch_bf16_kernel<256>(ta, tb, p, grid, s);
+  else launch_bf16_kernel<128>(ta, tb, p, grid, s);
+  return 1;
 }
 
 static int matmul(gpt2_t* m, const MatmulDesc& d) {
-  if (m->cfg.gemm_precision == GPT2_PREC_BF16) {
-    // bf16 operands: CUDA-core product with operands rounded to bf16
-    GemmArgs a = {};
-    a.M = d.M; a.N = d.N; a.K = d.K;
-    a.A = d.A; a.a_rs = d.a_kmajor ? d.lda : 1; a.a_cs = d.a_kmajor ? 1 : d.lda;
-    a.B = d.B; a.b_rs = d.b_kmajor ? 1 : d.ldb; a.b_cs = d.b_kmajor ? d.ldb : 1;
-    a.epi = d.epi;
-    a.bf16_ops = 1;
-    timer_begin(m, TK_GEMM, 2.0 * d.M * (double)d.N * d.K);
-    gemm_simt_launch(a, m->stream);
-    timer_end(m, TK_GEMM);
-    m->launches++;
-    return GPT2_OK;
-  }
   timer_begin(m, TK_GEMM, 2.0 * d.M * (double)d.N * d.K);
-  int n = launch_matmul(d, m->splitk, m->err, m->stream);
+  int n = m->cfg.gemm_precision == GPT2_PREC_BF16 ? launch_matmul_bf16(d, m->splitk, m->tilectr, m->err, m->stream)
+                                                  : launch_matmul(d, m->stream, m->err);
   timer_end(m, TK_GEMM);
   if (n < 0) {
     m->poisoned = GPT2_ERR_CUDA;
@@ -355,67 +448,220 @@ static int matmul(gpt2_t* m, const MatmulDesc& d) {
 }
 
 static EpiArgs epi_args(float* C, long long ldc, int epi, const float* bias = nullptr, const float* R = nullptr,
-                        long long ldr = 0, float* pre = nullptr, long long ldpre = 0) {
+                        long long ldr = 0, float* pre = nullptr, long long ldpre = 0, uint16_t* Cbf = nullptr,
+                        long long ldcbf = 0) {
   EpiArgs e;
   e.C = C; e.ldc = ldc; e.bias = bias; e.R = R; e.ldr = ldr; e.pre = pre; e.ldpre = ldpre; e.epi = epi;
+  e.Cbf = Cbf; e.ldcbf = ldcbf;
+  uintptr_t addr = (uintptr_t)C | (uintptr_t)bias | (uintptr_t)R | (uintptr_t)pre | (uintptr_t)Cbf;
+  e.vec4 = (addr & 15) == 0 && (ldc & 3) == 0 && (ldr & 3) == 0 && (ldpre & 3) == 0 && (ldcbf & 7) == 0;
   return e;
 }
 
-// linear layer y = x W^T + b with x (N, IC), W (OC, IC)
-static void mm_forward(gpt2_t* m, float* out, const float* x, const float* W, const float* bias, int N, int IC, int OC,
-                       int epi, const float* R, float* pre) {
-  MatmulDesc d = {N, OC, IC, x, IC, 1, W, IC, 1, epi_args(out, OC, epi, bias, R, OC, pre, OC)};
+// A matmul operand: the fp32 array and, for bf16 matmuls, its bf16 copy.
+struct Opnd {
+  const float* f;
+  const uint16_t* h;
+};
+
+// linear layer y = x W^T + b with x (N, IC), W (OC, IC); ybf: optional bf16 copy of y
+static void mm_forward(gpt2_t* m, float* out, uint16_t* outbf, Opnd x, Opnd W, const float* bias, int N, int IC,
+                       int OC, int epi, const float* R, float* pre) {
+  MatmulDesc d = {N, OC, IC, x.f, IC, 1, W.f, IC, 1, epi_args(out, OC, epi, bias, R, OC, pre, OC, outbf, OC), x.h, W.h};
   matmul(m, d);
 }
 
 // dx = dy W (times gelu'(pre) when pre != NULL)
-static void mm_dx(gpt2_t* m, float* dx, const float* dy, const float* W, int N, int IC, int OC, const float* pre) {
-  MatmulDesc d = {N, IC, OC, dy, OC, 1, W, IC, 0, epi_args(dx, IC, pre ? EPI_DGELU : EPI_STORE, nullptr, pre, IC)};
+static void mm_dx(gpt2_t* m, float* dx, uint16_t* dxbf, Opnd dy, Opnd W, int N, int IC, int OC, const float* pre) {
+  MatmulDesc d = {N,    IC,   OC,   dy.f, OC, 1, W.f, IC, 0,
+                  epi_args(dx, IC, pre ? EPI_DGELU : EPI_STORE, nullptr, pre, IC, nullptr, 0, dxbf, IC), dy.h, W.h};
   matmul(m, d);
 }
 
 // dW += dy^T x
-static void mm_dw(gpt2_t* m, float* dW, const float* dy, const float* x, int N, int IC, int OC) {
-  MatmulDesc d = {OC, IC, N, dy, OC, 0, x, IC, 0, epi_args(dW, IC, EPI_ACCUM)};
+static void mm_dw(gpt2_t* m, float* dW, Opnd dy, Opnd x, int N, int IC, int OC) {
+  MatmulDesc d = {OC, IC, N, dy.f, OC, 0, x.f, IC, 0, epi_args(dW, IC, EPI_ACCUM), dy.h, x.h};
   matmul(m, d);
 }
 
-// db += column sums of dy (N, OC)
+// db += column sums of dy (N, OC): row chunks of at least BIAS_MIN_ROWS rows,
+// as many as fill about two CTAs per SM, reduced in chunk order.
 static void bias_grad(gpt2_t* m, float* db, const float* dy, int N, int OC) {
-  int rows = 64;
+  int colb = ceil_div(OC, 256);
+  int want = ceil_div(2 * 148, colb);
+  int rows = ceil_div(N, want);
+  if (rows < BIAS_MIN_ROWS) rows = BIAS_MIN_ROWS;
   int chunks = ceil_div(N, rows);
-  col_partial_kernel<<<dim3(ceil_div(OC, 256), chunks), 256, 0, m->stream>>>(dy, N, OC, OC, rows, m->scratch);
-  col_finish_kernel<<<ceil_div(OC, 256), 256, 0, m->stream>>>(m->scratch, chunks, OC, db);
+  col_partial_kernel<<<dim3(colb, chunks), 256, 0, m->stream>>>(dy, N, OC, OC, rows, m->scratch);
+  col_finish_kernel<<<colb, 256, 0, m->stream>>>(m->scratch, chunks, OC, db);
   m->launches += 2;
 }
 
-static void ln_forward(gpt2_t* m, float* y, float* mean, float* rstd, const float* x, const float* w, const float* b,
-                       int N) {
+static void ln_forward(gpt2_t* m, float* y, uint16_t* ybf, float* mean, float* rstd, const float* x, const float* w,
+                       const float* b, int N) {
   int C = m->cfg.channels;
-  layernorm_fwd_kernel<<<ceil_div(N, 8), 256, 0, m->stream>>>(y, nullptr, mean, rstd, x, w, b, N, C);
+  timer_begin(m, TK_LAYERNORM, (8.0 * C + 8.0) * N);
+  layernorm_fwd_kernel<<<ceil_div(N, 8), 256, 0, m->stream>>>(y, ybf, mean, rstd, x, w, b, N, C);
+  timer_end(m, TK_LAYERNORM);
   m->launches++;
 }
 
-static void ln_backward(gpt2_t* m, float* dx, float* dw, float* db, const float* dy, const float* x, const float* w,
-                        const float* mean, const float* rstd, int N) {
+static void ln_backward(gpt2_t* m, float* dx, uint16_t* dxbf, float* dw, float* db, const float* dy, const float* x,
+                        const float* w, const float* mean, const float* rstd, int N) {
   int C = m->cfg.channels;
-  int nb = ceil_div(N, LNB_ROWS);
-  layernorm_bwd_kernel<<<nb, LNB_WARPS * 32, 2 * C * sizeof(float), m->stream>>>(dx, m->scratch, dy, x, w, mean,
-                                                                                    rstd, N, C);
+  // rows per block: a multiple of the warp count, enough blocks for two per SM
+  int rows = ceil_div(ceil_div(N, 2 * 148), LNB_WARPS) * LNB_WARPS;
+  if (rows < LNB_MIN_ROWS) rows = LNB_MIN_ROWS;
+  int nb = ceil_div(N, rows);
+  timer_begin(m, TK_LAYERNORM, (16.0 * C + 8.0) * N);
+  layernorm_bwd_kernel<<<nb, LNB_WARPS * 32, 2 * C * sizeof(float), m->stream>>>(dx, dxbf, m->scratch, dy, x, w,
+                                                                                    mean, rstd, N, C, rows);
   layernorm_param_grad_kernel<<<ceil_div(C, 256), 256, 0, m->stream>>>(dw, db, m->scratch, nb, C);
+  timer_end(m, TK_LAYERNORM);
   m->launches += 2;
+}
+
+// causal attention on CUDA cores; the template argument is the number of head
+// dimensions each lane holds (hs <= 32 * ND)
+// Causal attention forward: the tensor-core kernel for bf16 operands with
+// head size 64 and T % 128 == 0, else the CUDA-core kernel (the template
+// argument is the number of head dimensions each lane holds, hs <= 32 * ND).
+// Returns the number of launches, or -1 on a host-side failure.
+static int launch_attn_fwd(float* atty, uint16_t* attybf, float* lse, const float* qkv, const uint16_t* qkv_bf, int B,
+                           int T, int C, int NH, int bf, int* err, cudaStream_t s) {
+  const int hs = C / NH;
+  if (bf && qkv_bf && hs == tca::HS && T % tca::BQ == 0) {
+    CUtensorMap tm;
+    if (!make_bf16_map(&tm, qkv_bf, 1, (long long)B * T, 3LL * C, 3LL * C, tca::BQ)) return -1;
+    tca::Params p;
+    p.B = B; p.T = T; p.C = C; p.NH = NH;
+    p.scale = 1.0f / sqrtf((float)hs);
+    p.y = atty; p.ybf = attybf; p.lse = lse; p.err = err;
+    tca::attn_fwd_tc_kernel<<<dim3(T / tca::BQ, NH, B), tca::THREADS, tca::SMEM_BYTES, s>>>(tm, p);
+    return 1;
+  }
+  int grid = ceil_div((long long)B * NH * T * 32, 256);
+  if (hs <= 32) attn_fwd_simt_kernel<1><<<grid, 256, 0, s>>>(atty, attybf, lse, qkv, B, T, C, NH, bf);
+  else if (hs <= 64) attn_fwd_simt_kernel<2><<<grid, 256, 0, s>>>(atty, attybf, lse, qkv, B, T, C, NH, bf);
+  else attn_fwd_simt_kernel<4><<<grid, 256, 0, s>>>(atty, attybf, lse, qkv, B, T, C, NH, bf);
+  return 1;
+}
+
+static void attn_forward(gpt2_t* m, float* atty, uint16_t* attybf, float* lse, const float* qkv,
+                         const uint16_t* qkv_bf, int B, int T, int bf) {
+  int C = m->cfg.channels, NH = m->cfg.num_heads, hs = C / NH;
+  timer_begin(m, TK_ATTN_FWD, 4.0 * (double)B * NH * T * (T + 1) / 2.0 * hs);
+  int n = launch_attn_fwd(atty, attybf, lse, qkv, qkv_bf, B, T, C, NH, bf, m->err, m->stream);
+  timer_end(m, TK_ATTN_FWD);
+  if (n < 0) {
+    m->poisoned = GPT2_ERR_CUDA;
+    return;
+  }
+  m->launches += n;
+}
+
+static void attn_backward(gpt2_t* m, const float* qkv, const float* atty, const float* lse, int B, int T, int bf) {
+  int C = m->cfg.channels, NH = m->cfg.num_heads, hs = C / NH;
+  int grid = ceil_div((long long)B * NH * T * 32, 256);
+  cudaStream_t s = m->stream;
+  timer_begin(m, TK_ATTN_BWD, 8.0 * (double)B * NH * T * (T + 1) / 2.0 * hs);
+  attn_bwd_D_kernel<<<grid, 256, 0, s>>>(m->attD, m->datty, atty, B, T, C, NH);
+  if (hs <= 32) {
+    attn_bwd_dq_kernel<1><<<grid, 256, 0, s>>>(m->dqkv, m->dqkv_bf, qkv, m->datty, lse, m->attD, B, T, C, NH, bf);
+    attn_bwd_dkv_kernel<1><<<grid, 256, 0, s>>>(m->dqkv, m->dqkv_bf, qkv, m->datty, lse, m->attD, B, T, C, NH, bf);
+  } else if (hs <= 64) {
+    attn_bwd_dq_kernel<2><<<grid, 256, 0, s>>>(m->dqkv, m->dqkv_bf, qkv, m->datty, lse, m->attD, B, T, C, NH, bf);
+    attn_bwd_dkv_kernel<2><<<grid, 256, 0, s>>>(m->dqkv, m->dqkv_bf, qkv, m->datty, lse, m->attD, B, T, C, NH, bf);
+  } else {
+    attn_bwd_dq_kernel<4><<<grid, 256, 0, s>>>(m->dqkv, m->dqkv_bf, qkv, m->datty, lse, m->attD, B, T, C, NH, bf);
+    attn_bwd_dkv_kernel<4><<<grid, 256, 0, s>>>(m->dqkv, m->dqkv_bf, qkv, m->datty, lse, m->attD, B, T, C, NH, bf);
+  }
+  timer_end(m, TK_ATTN_BWD);
+  m->launches += 3;
+}
+
+// Dynamic shared memory limits of the large-smem kernels, set once per process.
+static std::once_flag g_attr_once;
+static int g_attr_status = GPT2_ERR_CUDA;
+
+static int set_kernel_attributes() {
+  std::call_once(g_attr_once, [] {
+    cudaError_t e = cudaFuncSetAttribute(sort_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SORT_MAX * (int)sizeof(uint32_t));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc::gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               tcb::Cfg<256>::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               tcb::Cfg<128>::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tca::attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               tca::SMEM_BYTES);
+    if (e != cudaSuccess) {
+      fprintf(stderr, "gpt2b300: cudaFuncSetAttribute failed: %s\n", cudaGetErrorString(e));
+      cudaGetLastError();
+    } else {
+      g_attr_status = GPT2_OK;
+    }
+  });
+  return g_attr_status;
 }
 
 // ---------------------------------------------------------------------------
 // the three phases
 // ---------------------------------------------------------------------------
+// Per-layer views of the activation arena (rows strided by maxB * maxT).  The
+// bf16 copies exist only for bf16 matmuls (NULL otherwise).
+struct LayerActs {
+  const float* x;  // layer input (residual stream)
+  float *ln1, *qkv, *atty, *lse, *res2, *ln2, *fch, *fchg, *res3;
+  float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd;
+  uint16_t *ln1_bf, *qkv_bf, *atty_bf, *ln2_bf, *fchg_bf;
+};
+
+static LayerActs layer_acts(gpt2_t* m, int l) {
+  const size_t cap = (size_t)m->maxB * m->maxT, C = m->cfg.channels, NH = m->cfg.num_heads;
+  LayerActs a;
+  a.x = l == 0 ? m->encoded : m->res3 + (size_t)(l - 1) * cap * C;
+  a.ln1 = m->ln1 + l * cap * C;
+  a.qkv = m->qkv + l * cap * 3 * C;
+  a.atty = m->atty + l * cap * C;
+  a.lse = m->lse + l * cap * NH;
+  a.res2 = m->res2 + l * cap * C;
+  a.ln2 = m->ln2 + l * cap * C;
+  a.fch = m->fch + l * cap * 4 * C;
+  a.fchg = m->fchg + l * cap * 4 * C;
+  a.res3 = m->res3 + l * cap * C;
+  a.ln1_mean = m->ln1_mean + l * cap;
+  a.ln1_rstd = m->ln1_rstd + l * cap;
+  a.ln2_mean = m->ln2_mean + l * cap;
+  a.ln2_rstd = m->ln2_rstd + l * cap;
+  const bool bf = m->params_bf != nullptr;
+  a.ln1_bf = bf ? m->ln1_bf + l * cap * C : nullptr;
+  a.qkv_bf = bf ? m->qkv_bf + l * cap * 3 * C : nullptr;
+  a.atty_bf = bf ? m->atty_bf + l * cap * C : nullptr;
+  a.ln2_bf = bf ? m->ln2_bf + l * cap * C : nullptr;
+  a.fchg_bf = bf ? m->fchg_bf + l * cap * 4 * C : nullptr;
+  return a;
+}
+
+// fp32 parameter tensor i (+ offset) and its bf16 copy
+static Opnd wparam(gpt2_t* m, int i, size_t off) {
+  Opnd o;
+  o.f = m->P[i] + off;
+  o.h = m->params_bf ? m->params_bf + (m->P[i] - m->params) + off : nullptr;
+  return o;
+}
+
 static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, int T, int validate) {
   const gpt2_config& c = m->cfg;
-  int L = c.num_layers, C = c.channels, NH = c.num_heads, V = c.vocab_size, Vp = c.padded_vocab_size;
+  int L = c.num_layers, C = c.channels, V = c.vocab_size, Vp = c.padded_vocab_size;
   int N = B * T;
-  size_t cap = (size_t)m->maxB * m->maxT;  // per-layer stride in rows
   cudaStream_t s = m->stream;
   int bf = c.gemm_precision == GPT2_PREC_BF16;
+  const size_t CC = (size_t)C * C;
   if (validate) {
     validate_tokens_kernel<<<grid_for(N, 256, 64), 256, 0, s>>>(d_in, d_tgt, N, V, m->err);
     m->launches++;
@@ -424,36 +670,28 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
                                                                           N, T, C, V);
   m->launches++;
   for (int l = 0; l < L; l++) {
-    const float* x = l == 0 ? m->encoded : m->res3 + (size_t)(l - 1) * cap * C;
-    float* ln1 = m->ln1 + (size_t)l * cap * C;
-    float* qkv = m->qkv + (size_t)l * cap * 3 * C;
-    float* atty = m->atty + (size_t)l * cap * C;
-    float* lse = m->lse + (size_t)l * cap * NH;
-    float* res2 = m->res2 + (size_t)l * cap * C;
-    float* ln2 = m->ln2 + (size_t)l * cap * C;
-    float* fch = m->fch + (size_t)l * cap * 4 * C;
-    float* fchg = m->fchg + (size_t)l * cap * 4 * C;
-    float* res3 = m->res3 + (size_t)l * cap * C;
-    ln_forward(m, ln1, m->ln1_mean + (size_t)l * cap, m->ln1_rstd + (size_t)l * cap, x, m->P[P_LN1W] + (size_t)l * C,
+    LayerActs a = layer_acts(m, l);
+    ln_forward(m, a.ln1, a.ln1_bf, a.ln1_mean, a.ln1_rstd, a.x, m->P[P_LN1W] + (size_t)l * C,
                m->P[P_LN1B] + (size_t)l * C, N);
-    mm_forward(m, qkv, ln1, m->P[P_QKVW] + (size_t)l * 3 * C * C, m->P[P_QKVB] + (size_t)l * 3 * C, N, C, 3 * C,
-               EPI_BIAS, nullptr, nullptr);
-    attn_fwd_simt_kernel<<<ceil_div((long long)B * NH * T * 32, 256), 256, 0, s>>>(atty, lse, qkv, B, T, C, NH, bf);
-    m->launches++;
-    mm_forward(m, res2, atty, m->P[P_ATTPROJW] + (size_t)l * C * C, m->P[P_ATTPROJB] + (size_t)l * C, N, C, C,
-               EPI_BIAS_RESID, x, nullptr);
-    ln_forward(m, ln2, m->ln2_mean + (size_t)l * cap, m->ln2_rstd + (size_t)l * cap, res2,
-               m->P[P_LN2W] + (size_t)l * C, m->P[P_LN2B] + (size_t)l * C, N);
-    mm_forward(m, fchg, ln2, m->P[P_FCW] + (size_t)l * 4 * C * C, m->P[P_FCB] + (size_t)l * 4 * C, N, C, 4 * C,
-               EPI_BIAS_GELU, nullptr, fch);
-    mm_forward(m, res3, fchg, m->P[P_FCPROJW] + (size_t)l * 4 * C * C, m->P[P_FCPROJB] + (size_t)l * C, N, 4 * C, C,
-               EPI_BIAS_RESID, res2, nullptr);
+    mm_forward(m, a.qkv, a.qkv_bf, {a.ln1, a.ln1_bf}, wparam(m, P_QKVW, l * 3 * CC),
+               m->P[P_QKVB] + (size_t)l * 3 * C, N, C, 3 * C, EPI_BIAS, nullptr, nullptr);
+    attn_forward(m, a.atty, a.atty_bf, a.lse, a.qkv, a.qkv_bf, B, T, bf);
+    mm_forward(m, a.res2, nullptr, {a.atty, a.atty_bf}, wparam(m, P_ATTPROJW, l * CC), m->P[P_ATTPROJB] + (size_t)l * C,
+               N, C, C, EPI_BIAS_RESID, a.x, nullptr);
+    ln_forward(m, a.ln2, a.ln2_bf, a.ln2_mean, a.ln2_rstd, a.res2, m->P[P_LN2W] + (size_t)l * C,
+               m->P[P_LN2B] + (size_t)l * C, N);
+    mm_forward(m, a.fchg, a.fchg_bf, {a.ln2, a.ln2_bf}, wparam(m, P_FCW, l * 4 * CC), m->P[P_FCB] + (size_t)l * 4 * C,
+               N, C, 4 * C, EPI_BIAS_GELU, nullptr, a.fch);
+    mm_forward(m, a.res3, nullptr, {a.fchg, a.fchg_bf}, wparam(m, P_FCPROJW, l * 4 * CC),
+               m->P[P_FCPROJB] + (size_t)l * C, N, 4 * C, C, EPI_BIAS_RESID, a.res2, nullptr);
   }
-  ln_forward(m, m->lnf, m->lnf_mean, m->lnf_rstd, m->res3 + (size_t)(L - 1) * cap * C, m->P[P_LNFW], m->P[P_LNFB], N);
-  mm_forward(m, m->logits, m->lnf, m->P[P_WTE], nullptr, N, C, Vp, EPI_STORE, nullptr, nullptr);
+  LayerActs last = layer_acts(m, L - 1);
+  ln_forward(m, m->lnf, m->lnf_bf, m->lnf_mean, m->lnf_rstd, last.res3, m->P[P_LNFW], m->P[P_LNFB], N);
+  mm_forward(m, m->logits, nullptr, {m->lnf, m->lnf_bf}, wparam(m, P_WTE, 0), nullptr, N, C, Vp, EPI_STORE, nullptr,
+             nullptr);
   if (d_tgt) {
     timer_begin(m, TK_XENT, 8.0 * (double)N * Vp);
-    xent_fused_kernel<<<N, XENT_THREADS, 0, s>>>(m->dlogits, nullptr, m->losses, m->logits, d_tgt, V, Vp,
+    xent_fused_kernel<<<N, XENT_THREADS, 0, s>>>(m->dlogits, m->dlogits_bf, m->losses, m->logits, d_tgt, V, Vp,
                                                  1.0f / (float)N);
     timer_end(m, TK_XENT);
     mean_kernel<<<1, 1024, 0, s>>>(m->losses, N, m->loss);
@@ -469,57 +707,45 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
 
 static int enqueue_backward(gpt2_t* m) {
   const gpt2_config& c = m->cfg;
-  int L = c.num_layers, C = c.channels, NH = c.num_heads, Vp = c.padded_vocab_size;
+  int L = c.num_layers, C = c.channels, Vp = c.padded_vocab_size;
   int B = m->B, T = m->T, N = B * T;
-  size_t cap = (size_t)m->maxB * m->maxT;
   cudaStream_t s = m->stream;
   int bf = c.gemm_precision == GPT2_PREC_BF16;
+  const size_t CC = (size_t)C * C;
   float** P = m->P;
   float** G = m->G;
+  const Opnd dres = {m->dres, m->dres_bf}, dfch = {m->dfch, m->dfch_bf}, dqkv = {m->dqkv, m->dqkv_bf};
   // LM head (tied to wte): dlnf = dlogits wte; dwte += dlogits^T lnf
-  mm_dx(m, m->dln, m->dlogits, P[P_WTE], N, C, Vp, nullptr);
-  mm_dw(m, G[P_WTE], m->dlogits, m->lnf, N, C, Vp);
+  mm_dx(m, m->dln, nullptr, {m->dlogits, m->dlogits_bf}, wparam(m, P_WTE, 0), N, C, Vp, nullptr);
+  mm_dw(m, G[P_WTE], {m->dlogits, m->dlogits_bf}, {m->lnf, m->lnf_bf}, N, C, Vp);
   CCHECK(m, cudaMemsetAsync(m->dres, 0, (size_t)N * C * sizeof(float), s));
-  ln_backward(m, m->dres, G[P_LNFW], G[P_LNFB], m->dln, m->res3 + (size_t)(L - 1) * cap * C, P[P_LNFW], m->lnf_mean,
-              m->lnf_rstd, N);
+  LayerActs last = layer_acts(m, L - 1);
+  ln_backward(m, m->dres, m->dres_bf, G[P_LNFW], G[P_LNFB], m->dln, last.res3, P[P_LNFW], m->lnf_mean, m->lnf_rstd,
+              N);
   for (int l = L - 1; l >= 0; l--) {
-    const float* x = l == 0 ? m->encoded : m->res3 + (size_t)(l - 1) * cap * C;
-    float* ln1 = m->ln1 + (size_t)l * cap * C;
-    float* qkv = m->qkv + (size_t)l * cap * 3 * C;
-    float* atty = m->atty + (size_t)l * cap * C;
-    float* lse = m->lse + (size_t)l * cap * NH;
-    float* res2 = m->res2 + (size_t)l * cap * C;
-    float* ln2 = m->ln2 + (size_t)l * cap * C;
-    float* fch = m->fch + (size_t)l * cap * 4 * C;
-    float* fchg = m->fchg + (size_t)l * cap * 4 * C;
+    LayerActs a = layer_acts(m, l);
     // MLP output projection: res3 = res2 + fchg fcprojw^T + fcprojb
-    mm_dw(m, G[P_FCPROJW] + (size_t)l * 4 * C * C, m->dres, fchg, N, 4 * C, C);
+    mm_dw(m, G[P_FCPROJW] + l * 4 * CC, dres, {a.fchg, a.fchg_bf}, N, 4 * C, C);
     bias_grad(m, G[P_FCPROJB] + (size_t)l * C, m->dres, N, C);
-    mm_dx(m, m->dfch, m->dres, P[P_FCPROJW] + (size_t)l * 4 * C * C, N, 4 * C, C, fch);  // x gelu'(fch)
+    mm_dx(m, m->dfch, m->dfch_bf, dres, wparam(m, P_FCPROJW, l * 4 * CC), N, 4 * C, C, a.fch);  // x gelu'(fch)
     // MLP input projection: fch = ln2 fcw^T + fcb
-    mm_dw(m, G[P_FCW] + (size_t)l * 4 * C * C, m->dfch, ln2, N, C, 4 * C);
+    mm_dw(m, G[P_FCW] + l * 4 * CC, dfch, {a.ln2, a.ln2_bf}, N, C, 4 * C);
     bias_grad(m, G[P_FCB] + (size_t)l * 4 * C, m->dfch, N, 4 * C);
-    mm_dx(m, m->dln, m->dfch, P[P_FCW] + (size_t)l * 4 * C * C, N, C, 4 * C, nullptr);
-    ln_backward(m, m->dres, G[P_LN2W] + (size_t)l * C, G[P_LN2B] + (size_t)l * C, m->dln, res2,
-                P[P_LN2W] + (size_t)l * C, m->ln2_mean + (size_t)l * cap, m->ln2_rstd + (size_t)l * cap, N);
+    mm_dx(m, m->dln, nullptr, dfch, wparam(m, P_FCW, l * 4 * CC), N, C, 4 * C, nullptr);
+    ln_backward(m, m->dres, m->dres_bf, G[P_LN2W] + (size_t)l * C, G[P_LN2B] + (size_t)l * C, m->dln, a.res2,
+                P[P_LN2W] + (size_t)l * C, a.ln2_mean, a.ln2_rstd, N);
     // attention output projection: res2 = x + atty attprojw^T + attprojb
-    mm_dw(m, G[P_ATTPROJW] + (size_t)l * C * C, m->dres, atty, N, C, C);
+    mm_dw(m, G[P_ATTPROJW] + l * CC, dres, {a.atty, a.atty_bf}, N, C, C);
     bias_grad(m, G[P_ATTPROJB] + (size_t)l * C, m->dres, N, C);
-    mm_dx(m, m->datty, m->dres, P[P_ATTPROJW] + (size_t)l * C * C, N, C, C, nullptr);
+    mm_dx(m, m->datty, nullptr, dres, wparam(m, P_ATTPROJW, l * CC), N, C, C, nullptr);
     // attention
-    int nw = B * NH * T;
-    attn_bwd_D_kernel<<<ceil_div((long long)nw * 32, 256), 256, 0, s>>>(m->attD, m->datty, atty, B, T, C, NH);
-    attn_bwd_dq_kernel<<<ceil_div((long long)nw * 32, 256), 256, 0, s>>>(m->dqkv, qkv, m->datty, lse, m->attD, B, T,
-                                                                        C, NH, bf);
-    attn_bwd_dkv_kernel<<<ceil_div((long long)nw * 32, 256), 256, 0, s>>>(m->dqkv, qkv, m->datty, lse, m->attD, B,
-                                                                         T, C, NH, bf);
-    m->launches += 3;
+    attn_backward(m, a.qkv, a.atty, a.lse, B, T, bf);
     // qkv projection: qkv = ln1 qkvw^T + qkvb
-    mm_dw(m, G[P_QKVW] + (size_t)l * 3 * C * C, m->dqkv, ln1, N, C, 3 * C);
+    mm_dw(m, G[P_QKVW] + l * 3 * CC, dqkv, {a.ln1, a.ln1_bf}, N, C, 3 * C);
     bias_grad(m, G[P_QKVB] + (size_t)l * 3 * C, m->dqkv, N, 3 * C);
-    mm_dx(m, m->dln, m->dqkv, P[P_QKVW] + (size_t)l * 3 * C * C, N, C, 3 * C, nullptr);
-    ln_backward(m, m->dres, G[P_LN1W] + (size_t)l * C, G[P_LN1B] + (size_t)l * C, m->dln, x,
-                P[P_LN1W] + (size_t)l * C, m->ln1_mean + (size_t)l * cap, m->ln1_rstd + (size_t)l * cap, N);
+    mm_dx(m, m->dln, nullptr, dqkv, wparam(m, P_QKVW, l * 3 * CC), N, C, 3 * C, nullptr);
+    ln_backward(m, m->dres, m->dres_bf, G[P_LN1W] + (size_t)l * C, G[P_LN1B] + (size_t)l * C, m->dln, a.x,
+                P[P_LN1W] + (size_t)l * C, a.ln1_mean, a.ln1_rstd, N);
   }
   // embeddings
   size_t smem = 1;
@@ -596,8 +822,12 @@ static void carve(gpt2_t* m) {
   CARVE(res2); CARVE(ln2); CARVE(ln2_mean); CARVE(ln2_rstd); CARVE(fch); CARVE(fchg); CARVE(res3);
   CARVE(lnf); CARVE(lnf_mean); CARVE(lnf_rstd); CARVE(logits); CARVE(dlogits); CARVE(losses); CARVE(loss);
   CARVE(dres); CARVE(dln); CARVE(datty); CARVE(dqkv); CARVE(dfch); CARVE(attD); CARVE(scratch); CARVE(sorted);
-  CARVE(tokens); CARVE(targets); CARVE(err); CARVE(hparams); CARVE(splitk);
+  CARVE(tokens); CARVE(targets); CARVE(err); CARVE(hparams); CARVE(splitk); CARVE(tilectr);
 #undef CARVE
+#define CARVE_BF(f) m->f = m->params_bf ? (uint16_t*)(a + p.f) : nullptr
+  CARVE_BF(ln1_bf); CARVE_BF(qkv_bf); CARVE_BF(atty_bf); CARVE_BF(ln2_bf); CARVE_BF(fchg_bf); CARVE_BF(lnf_bf); CARVE_BF(dlogits_bf);
+  CARVE_BF(dres_bf); CARVE_BF(dfch_bf); CARVE_BF(dqkv_bf);
+#undef CARVE_BF
 }
 
 static int init_params(gpt2_t* m, uint64_t seed) {
@@ -659,16 +889,15 @@ EXPORT int gpt2_build(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, int m
   carve(m);
   int rc;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(sort_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SORT_MAX * (int)sizeof(uint32_t))) != cudaSuccess)
-    goto cuda_fail;
-  if ((e = cudaFuncSetAttribute(tc::gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                tc::SMEM_BYTES)) != cudaSuccess)
-    goto cuda_fail;
+  if (set_kernel_attributes() != GPT2_OK) {
+    rc = GPT2_ERR_CUDA;
+    goto fail;
+  }
   if ((e = cudaMemsetAsync(m->grads, 0, m->np * sizeof(float), m->stream)) != cudaSuccess) goto cuda_fail;
   if ((e = cudaMemsetAsync(m->m, 0, m->np * sizeof(float), m->stream)) != cudaSuccess) goto cuda_fail;
   if ((e = cudaMemsetAsync(m->v, 0, m->np * sizeof(float), m->stream)) != cudaSuccess) goto cuda_fail;
   if ((e = cudaMemsetAsync(m->err, 0, sizeof(int), m->stream)) != cudaSuccess) goto cuda_fail;
+  if ((e = cudaMemsetAsync(m->tilectr, 0, TILE_CTRS * sizeof(int), m->stream)) != cudaSuccess) goto cuda_fail;
   if ((rc = init_params(m, seed)) != GPT2_OK) goto fail;
   if ((rc = refresh_bf16(m)) != GPT2_OK) goto fail;
   if ((e = cudaStreamSynchronize(m->stream)) != cudaSuccess) goto cuda_fail;
@@ -949,43 +1178,51 @@ EXPORT int gpt2_get_logits(gpt2_t* m, float* host, long long n) {
 // ---------------------------------------------------------------------------
 // kernel-level entry points (device buffers), for per-layer parity tests
 // ---------------------------------------------------------------------------
-// workspace layout: [error word (256 B)][bias partials ceil(N/64) x OC][split-K partials]
-EXPORT size_t gpt2op_matmul_workspace_bytes(int N, int OC) {
-  if (N < 1 || OC < 1) return 0;
+// workspace layout: [error word (256 B)][tile counters][bias partials ceil(N/64) x OC][split-K partials]
+// [bf16 copies of x (N x IC), W (OC x IC), dy (N x OC)]
+static size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+EXPORT size_t gpt2op_matmul_workspace_bytes(int N, int IC, int OC) {
+  if (N < 1 || IC < 1 || OC < 1) return 0;
   size_t bias = (size_t)ceil_div(N, 64) * OC * sizeof(float);
-  return 256 + ((bias + 255) & ~(size_t)255) + SPLITK_WS_FLOATS * sizeof(float);
+  return OP_HDR_BYTES + al256(bias) + SPLITK_WS_FLOATS * sizeof(float) + al256((size_t)N * IC * 2) +
+         al256((size_t)OC * IC * 2) + al256((size_t)N * OC * 2);
 }
 
 struct OpWs {
   int* err;
+  int* tile_ctr;
   float* bias_partial;
   float* splitk;
   long long splitk_floats;
+  uint16_t *xbf, *Wbf, *dybf;  // bf16 operand copies (bf16 precision)
 };
 
-static OpWs op_ws(void* ws, int N, int OC) {
+static OpWs op_ws(void* ws, int N, int IC, int OC) {
   OpWs w;
   char* b = (char*)ws;
-  size_t bias = (size_t)ceil_div(N, 64) * OC * sizeof(float);
+  size_t bias = al256((size_t)ceil_div(N, 64) * OC * sizeof(float));
   w.err = (int*)b;
-  w.bias_partial = (float*)(b + 256);
-  w.splitk = (float*)(b + 256 + ((bias + 255) & ~(size_t)255));
+  w.tile_ctr = (int*)(b + 256);
+  w.bias_partial = (float*)(b + OP_HDR_BYTES);
+  w.splitk = (float*)(b + OP_HDR_BYTES + bias);
   w.splitk_floats = SPLITK_WS_FLOATS;
+  char* h = b + OP_HDR_BYTES + bias + SPLITK_WS_FLOATS * sizeof(float);
+  w.xbf = (uint16_t*)h;
+  w.Wbf = (uint16_t*)(h + al256((size_t)N * IC * 2));
+  w.dybf = (uint16_t*)(h + al256((size_t)N * IC * 2) + al256((size_t)OC * IC * 2));
   return w;
 }
 
+static int op_to_bf16(const float* x, uint16_t* y, long long n, cudaStream_t s) {
+  to_bf16_kernel<<<grid_for(n, 256), 256, 0, s>>>(x, y, n);
+  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
 static int op_matmul(const MatmulDesc& d, int precision, const OpWs& w, cudaStream_t s) {
-  if (precision == GPT2_PREC_BF16) {
-    GemmArgs a = {};
-    a.M = d.M; a.N = d.N; a.K = d.K;
-    a.A = d.A; a.a_rs = d.a_kmajor ? d.lda : 1; a.a_cs = d.a_kmajor ? 1 : d.lda;
-    a.B = d.B; a.b_rs = d.b_kmajor ? 1 : d.ldb; a.b_cs = d.b_kmajor ? d.ldb : 1;
-    a.epi = d.epi;
-    a.bf16_ops = 1;
-    gemm_simt_launch(a, s);
-    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
-  }
-  if (launch_matmul(d, w.splitk, w.err, s, w.splitk_floats) < 0) return GPT2_ERR_CUDA;
+  int n = precision == GPT2_PREC_BF16 ? launch_matmul_bf16(d, w.splitk, w.tile_ctr, w.err, s, w.splitk_floats)
+                                      : launch_matmul(d, s, w.err);
+  if (n < 0) return GPT2_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
@@ -998,40 +1235,47 @@ static int op_status(const OpWs& w, cudaStream_t s) {
 }
 
 static int op_prepare(void* workspace, cudaStream_t s) {
-  static int attr_done = 0;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(tc::gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES) !=
-        cudaSuccess)
-      return GPT2_ERR_CUDA;
-    attr_done = 1;
-  }
-  return cudaMemsetAsync(workspace, 0, 256, s) == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+  if (set_kernel_attributes() != GPT2_OK) return GPT2_ERR_CUDA;
+  // clears the error word and the split-K tile counters
+  return cudaMemsetAsync(workspace, 0, OP_HDR_BYTES, s) == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+static int op_check_shape(int N, int IC, int OC, int precision) {
+  if (precision != GPT2_PREC_FP32 && precision != GPT2_PREC_BF16) return GPT2_ERR_ARG;
+  // TMA rows must be multiples of 16 bytes
+  int q = precision == GPT2_PREC_BF16 ? 8 : 4;
+  if (IC % q || OC % q) return GPT2_ERR_SHAPE;
+  return GPT2_OK;
 }
 
 EXPORT int gpt2op_matmul_forward(float* out, const float* x, const float* W, const float* bias, int N, int IC, int OC,
                                  int precision, void* workspace, void* stream) {
   if (!out || !x || !W || !workspace || N < 1 || IC < 1 || OC < 1) return GPT2_ERR_ARG;
-  if ((IC * 4) % 16 || (OC * 4) % 16) return GPT2_ERR_SHAPE;
-  cudaStream_t s = (cudaStream_t)stream;
-  int rc = op_prepare(workspace, s);
+  int rc = op_check_shape(N, IC, OC, precision);
   if (rc) return rc;
-  OpWs w = op_ws(workspace, N, OC);
-  MatmulDesc d = {N, OC, IC, x, IC, 1, W, IC, 1, epi_args(out, OC, bias ? EPI_BIAS : EPI_STORE, bias)};
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((rc = op_prepare(workspace, s))) return rc;
+  OpWs w = op_ws(workspace, N, IC, OC);
+  if (precision == GPT2_PREC_BF16) {
+    if ((rc = op_to_bf16(x, w.xbf, (long long)N * IC, s)) || (rc = op_to_bf16(W, w.Wbf, (long long)OC * IC, s)))
+      return rc;
+  }
+  MatmulDesc d = {N, OC, IC, x, IC, 1, W, IC, 1, epi_args(out, OC, bias ? EPI_BIAS : EPI_STORE, bias), w.xbf, w.Wbf};
   rc = op_matmul(d, precision, w, s);
   return rc ? rc : op_status(w, s);
 }
 
-EXPORT int gpt2op_matmul_backward(float* dx, float* dW, float* dbias, const float* dy, const float* x, const float* W,
-                                  int N, int IC, int OC, int precision, void* workspace, void* stream) {
-  if (!dx || !dW || !dy || !x || !W || !workspace || N < 1 || IC < 1 || OC < 1) return GPT2_ERR_ARG;
-  if ((IC * 4) % 16 || (OC * 4) % 16) return GPT2_ERR_SHAPE;
-  cudaStream_t s = (cudaStream_t)stream;
-  int rc = op_prepare(workspace, s);
-  if (rc) return rc;
-  OpWs w = op_ws(workspace, N, OC);
-  MatmulDesc ddx = {N, IC, OC, dy, OC, 1, W, IC, 0, epi_args(dx, IC, EPI_STORE)};
+static int op_backward(float* dx, float* dW, float* dbias, const float* dy, const float* x, const float* W, int N,
+                       int IC, int OC, int precision, const OpWs& w, cudaStream_t s) {
+  int rc;
+  if (precision == GPT2_PREC_BF16) {
+    if ((rc = op_to_bf16(x, w.xbf, (long long)N * IC, s)) || (rc = op_to_bf16(W, w.Wbf, (long long)OC * IC, s)) ||
+        (rc = op_to_bf16(dy, w.dybf, (long long)N * OC, s)))
+      return rc;
+  }
+  MatmulDesc ddx = {N, IC, OC, dy, OC, 1, W, IC, 0, epi_args(dx, IC, EPI_STORE), w.dybf, w.Wbf};
   if ((rc = op_matmul(ddx, precision, w, s))) return rc;
-  MatmulDesc ddw = {OC, IC, N, dy, OC, 0, x, IC, 0, epi_args(dW, IC, EPI_ACCUM)};
+  MatmulDesc ddw = {OC, IC, N, dy, OC, 0, x, IC, 0, epi_args(dW, IC, EPI_ACCUM), w.dybf, w.xbf};
   if ((rc = op_matmul(ddw, precision, w, s))) return rc;
   if (dbias) {
     int chunks = ceil_div(N, 64);
@@ -1042,17 +1286,51 @@ EXPORT int gpt2op_matmul_backward(float* dx, float* dW, float* dbias, const floa
   return op_status(w, s);
 }
 
+EXPORT int gpt2op_matmul_backward(float* dx, float* dW, float* dbias, const float* dy, const float* x, const float* W,
+                                  int N, int IC, int OC, int precision, void* workspace, void* stream) {
+  if (!dx || !dW || !dy || !x || !W || !workspace || N < 1 || IC < 1 || OC < 1) return GPT2_ERR_ARG;
+  int rc = op_check_shape(N, IC, OC, precision);
+  if (rc) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((rc = op_prepare(workspace, s))) return rc;
+  return op_backward(dx, dW, dbias, dy, x, W, N, IC, OC, precision, op_ws(workspace, N, IC, OC), s);
+}
+
+// attention forward: workspace = [error word, 256 B][bf16 copy of qkv]
+EXPORT size_t gpt2op_attention_workspace_bytes(int B, int T, int C) {
+  if (B < 1 || T < 1 || C < 1) return 0;
+  return 256 + al256((size_t)B * T * 3 * C * 2);
+}
+
+EXPORT int gpt2op_attention_forward(float* y, float* lse, const float* qkv, int B, int T, int C, int NH, int precision,
+                                    void* workspace, void* stream) {
+  if (!y || !lse || !qkv || !workspace || B < 1 || T < 1 || C < 1 || NH < 1) return GPT2_ERR_ARG;
+  if (precision != GPT2_PREC_FP32 && precision != GPT2_PREC_BF16) return GPT2_ERR_ARG;
+  if (C % NH || C / NH > 128 || C % 8) return GPT2_ERR_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (set_kernel_attributes() != GPT2_OK) return GPT2_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, 256, s) != cudaSuccess) return GPT2_ERR_CUDA;
+  OpWs w = {};
+  w.err = (int*)workspace;
+  uint16_t* qkv_bf = (uint16_t*)((char*)workspace + 256);
+  const int bf = precision == GPT2_PREC_BF16;
+  if (bf && op_to_bf16(qkv, qkv_bf, (long long)B * T * 3 * C, s)) return GPT2_ERR_CUDA;
+  if (launch_attn_fwd(y, nullptr, lse, qkv, bf ? qkv_bf : nullptr, B, T, C, NH, bf, w.err, s) < 0) return GPT2_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return GPT2_ERR_CUDA;
+  return op_status(w, s);
+}
+
 // ---------------------------------------------------------------------------
 // matmul backward with library-owned scratch (no allocation by anyone)
 // ---------------------------------------------------------------------------
 // The scratch of gpt2op_matmul_backward (error word, column-sum partials of
 // the bias gradient, split-K partials) is taken from one fixed array in the
 // library's device memory.  Every GPU that loads the library holds it until
-// the process exits.  Layout: [error word, 256 B][column-sum partials,
-// NOALLOC_BIAS_FLOATS][split-K partials, the rest].
+// the process exits.  Layout: [error word, 256 B][split-K tile counters]
+// [column-sum partials, NOALLOC_BIAS_FLOATS][split-K partials, the rest].
 #define NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 #define NOALLOC_BIAS_FLOATS ((long long)1 << 20)
-#define NOALLOC_SPLITK_OFFSET ((size_t)256 + (size_t)NOALLOC_BIAS_FLOATS * sizeof(float))
+#define NOALLOC_SPLITK_OFFSET ((size_t)OP_HDR_BYTES + (size_t)NOALLOC_BIAS_FLOATS * sizeof(float))
 #define NOALLOC_MAX_DEVICES 64
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
@@ -1088,31 +1366,24 @@ static int noalloc_scratch_address(void** out) {
 EXPORT int gpt2op_matmul_backward_noalloc(float* dx, float* dW, float* dbias, const float* dy, const float* x,
                                           const float* W, int N, int IC, int OC, int precision, void* stream) {
   if (!dx || !dW || !dy || !x || !W || N < 1 || IC < 1 || OC < 1) return GPT2_ERR_ARG;
-  if ((IC * 4) % 16 || (OC * 4) % 16) return GPT2_ERR_SHAPE;
+  // bf16 operand copies would need scratch that scales with the inputs
+  if (precision != GPT2_PREC_FP32) return GPT2_ERR_ARG;
+  int rc = op_check_shape(N, IC, OC, precision);
+  if (rc) return rc;
   if (dbias && (long long)ceil_div(N, 64) * OC > NOALLOC_BIAS_FLOATS) {
     fprintf(stderr, "gpt2b300: gpt2op_matmul_backward_noalloc: ceil(N/64)*OC = %lld exceeds the fixed scratch "
             "(%lld floats)\n", (long long)ceil_div(N, 64) * OC, NOALLOC_BIAS_FLOATS);
     return GPT2_ERR_SHAPE;
   }
   void* base = nullptr;
-  int rc = noalloc_scratch_address(&base);
-  if (rc) return rc;
+  if ((rc = noalloc_scratch_address(&base))) return rc;
   cudaStream_t s = (cudaStream_t)stream;
-  if ((rc = op_prepare(base, s))) return rc;  // clears the error word
-  OpWs w;
+  if ((rc = op_prepare(base, s))) return rc;  // clears the error word and the tile counters
+  OpWs w = {};
   w.err = (int*)base;
-  w.bias_partial = (float*)((char*)base + 256);
+  w.tile_ctr = (int*)((char*)base + 256);
+  w.bias_partial = (float*)((char*)base + OP_HDR_BYTES);
   w.splitk = (float*)((char*)base + NOALLOC_SPLITK_OFFSET);
   w.splitk_floats = (long long)((NOALLOC_SCRATCH_BYTES - NOALLOC_SPLITK_OFFSET) / sizeof(float));
-  MatmulDesc ddx = {N, IC, OC, dy, OC, 1, W, IC, 0, epi_args(dx, IC, EPI_STORE)};
-  if ((rc = op_matmul(ddx, precision, w, s))) return rc;
-  MatmulDesc ddw = {OC, IC, N, dy, OC, 0, x, IC, 0, epi_args(dW, IC, EPI_ACCUM)};
-  if ((rc = op_matmul(ddw, precision, w, s))) return rc;
-  if (dbias) {
-    int chunks = ceil_div(N, 64);
-    col_partial_kernel<<<dim3(ceil_div(OC, 256), chunks), 256, 0, s>>>(dy, N, OC, OC, 64, w.bias_partial);
-    col_finish_kernel<<<ceil_div(OC, 256), 256, 0, s>>>(w.bias_partial, chunks, OC, dbias);
-    if (cudaGetLastError() != cudaSuccess) return GPT2_ERR_CUDA;
-  }
-  return op_status(w, s);
+  return op_backward(dx, dW, dbias, dy, x, W, N, IC, OC, precision, w, s);
 }

@@ -15,7 +15,9 @@
 // a*b ~ ah*bh + ah*bl + al*bh, three MMAs into one fp32 accumulator.  The
 // dropped al*bl term and the TF32 rounding of lo are ~2^-20 relative.
 //
-// CTA = one 128 x 128 output tile over a range of K (split-K), 6 warps:
+// CTA = one 128 x 128 output tile over a range of K, 6 warps.  When K is
+// split, the S splits of a tile form one thread-block cluster and are summed
+// through distributed shared memory (below).
 //   warp 0      one lane issues the TMA loads of raw fp32 tiles (raw ring)
 //   warp 1      allocates TMEM; one lane issues tcgen05.mma and commits
 //   warps 2..5  split each raw tile into hi/lo tiles laid out K-major with
@@ -49,6 +51,10 @@ constexpr int OFF_LO_A = OFF_HI_A + COMP_STAGES * TILE_BYTES;
 constexpr int OFF_HI_B = OFF_LO_A + COMP_STAGES * TILE_BYTES;
 constexpr int OFF_LO_B = OFF_HI_B + COMP_STAGES * TILE_BYTES;
 constexpr int OFF_BAR = OFF_LO_B + COMP_STAGES * TILE_BYTES;
+// after the main loop the hi/lo region holds this CTA's split-K partial tile
+constexpr int OFF_STAGE = OFF_HI_A;
+constexpr int STAGE_PITCH = BN + 4;  // floats per staged row (padding spreads the banks)
+static_assert(BM * STAGE_PITCH * 4 <= OFF_BAR - OFF_HI_A, "staged partial tile must fit the hi/lo region");
 constexpr int NUM_BARS = 2 * RAW_STAGES + 2 * COMP_STAGES + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
@@ -58,7 +64,7 @@ struct Params {
   int a_kmajor, b_kmajor;
   int k_tiles, kt_per_split;
   EpiArgs epi;
-  float* partial;  // split-K partials [splits][M][N], or NULL for a direct epilogue
+  int splits;  // K splits = CTAs per cluster (1: no cluster, direct epilogue)
   int* err;
 };
 
@@ -130,6 +136,36 @@ GPT2_DEV void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64
       ::"r"(smem_u32(dst)), "l"((uint64_t)tm), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+
+// Cluster helpers: CTA rank, barrier over every thread of the cluster, and
+// 16-byte loads from a peer CTA's shared memory (DSMEM).
+GPT2_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+GPT2_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+GPT2_DEV uint32_t map_peer(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+GPT2_DEV float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Barrier over the four splitter / epilogue warps only (threads 64..191).
+GPT2_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 GPT2_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 GPT2_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -228,6 +264,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* acc_full = bars + 2 * RAW_STAGES + 2 * COMP_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  volatile int* go_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
@@ -246,6 +283,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
+    *go_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -351,33 +389,70 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(&comp_full[c]);
     }
     if (ok && nk > 0) ok = mbar_wait(acc_full, 0, abort_flag, p.err);
-    // tcgen05.ld is warp-collective: take the epilogue only if the whole warp can
-    if (__all_sync(0xffffffffu, ok && nk > 0 && !*abort_flag)) {
+    // One decision for all four epilogue warps (tcgen05.ld is warp-collective
+    // and the split-K hand-off below uses a barrier over these 128 threads).
+    // Every epilogue thread reaches this barrier: all of its waits are bounded.
+    epi_bar();
+    if (t == 0) *go_flag = (nk > 0 && !*abort_flag) ? 1 : 0;
+    epi_bar();
+    if (*go_flag) {
       tc_fence_after();
       const int q = warp & 3;  // TMEM lane quadrant this warp may access
       const int row = q * 32 + lane;
       const int i = m0 + row;
-      const bool split = p.partial != nullptr;
-      const size_t zoff = split ? (size_t)blockIdx.z * p.M * p.N : 0;
+      float* stage = reinterpret_cast<float*>(smem + OFF_STAGE);
 #pragma unroll 1
       for (int cc = 0; cc < BN / 32; cc++) {
         float v[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cc * 32), v);
-        if (i < p.M) {
+        if (p.splits > 1) {
+          // this split's partial tile, row-major with a padded pitch, for the cluster reduction
+          float* dst = stage + row * STAGE_PITCH + cc * 32;
+#pragma unroll
+          for (int u = 0; u < 8; u++) st4(dst + 4 * u, make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]));
+        } else if (i < p.M) {
           int j0 = n0 + cc * 32;
-          if (split) {
-            float* dst = p.partial + zoff + (size_t)i * p.N;
-#pragma unroll
-            for (int e = 0; e < 32; e++)
-              if (j0 + e < p.N) dst[j0 + e] = v[e];
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; e++)
-              if (j0 + e < p.N) epi_store(p.epi, i, j0 + e, v[e]);
-          }
+          int nvalid = min(32, p.N - j0);
+          if (nvalid > 0) epi_store_row32(p.epi, i, j0, v, nvalid);
         }
       }
     }
+  }
+
+  if (p.splits > 1) {
+    // Split-K reduction inside the cluster: the K splits of this output tile
+    // are the CTAs of one cluster.  Once every partial is staged, CTA r sums
+    // rows [r*R, (r+1)*R) of the tile over the splits in split order, reading
+    // the peers' shared memory, and applies the epilogue.  Every thread of
+    // every CTA reaches both cluster barriers (all waits above are bounded).
+    cluster_sync();
+    if (warp >= 2 && *go_flag) {
+      const int S = p.splits;
+      const int rank = (int)cluster_rank();
+      const int R = (BM + S - 1) / S;
+      const int r0 = rank * R, r1 = min(BM, r0 + R);
+      const int t = threadIdx.x - 64;
+      const int c4 = t & 31;  // float4 column group of the 128-wide tile
+      const int j = n0 + 4 * c4;
+      const uint32_t stage = smem_u32(smem + OFF_STAGE);
+      for (int r = r0 + (t >> 5); r < r1; r += 4) {
+        const int ii = m0 + r;
+        if (ii >= p.M || j >= p.N) continue;
+        const uint32_t off = stage + (uint32_t)(r * STAGE_PITCH + 4 * c4) * 4u;
+        float4 acc = ld_dsmem_f4(map_peer(off, 0));
+        for (int z = 1; z < S; z++) {
+          float4 b = ld_dsmem_f4(map_peer(off, (uint32_t)z));
+          acc.x += b.x; acc.y += b.y; acc.z += b.z; acc.w += b.w;
+        }
+        if (j + 4 <= p.N) {
+          epi_store4(p.epi, ii, j, acc);
+        } else {
+          const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+          for (int c = 0; c < 4 && j + c < p.N; c++) epi_store(p.epi, ii, j + c, a4[c]);
+        }
+      }
+    }
+    cluster_sync();  // peers keep their shared memory until every CTA has read it
   }
 
   tc_fence_before();

@@ -3,7 +3,8 @@
 // Forward: mean and biased variance over C (two passes over the row held in
 // registers), rstd = 1/sqrt(var + 1e-5), y = (x - mean) * rstd * w + b.
 // Backward: with n = (x - mean) * rstd and g = dy * w,
-//   dx += rstd * (g - mean(g) - n * mean(g * n))     (accumulated in place)
+//   dx += rstd * (g - mean(g) - n * mean(g * n))     (accumulated in place;
+//                                                    optional bf16 copy of dx)
 //   dw += sum_rows dy * n,  db += sum_rows dy         (two-stage, fixed order)
 // C must be a multiple of 4 and at most 32 * 4 * LN_MAXV4.
 #pragma once
@@ -52,7 +53,7 @@ __global__ void layernorm_fwd_kernel(float* __restrict__ y, uint16_t* __restrict
       o.y = (v[k].y - mu) * rs * ww.y + bb.y;
       o.z = (v[k].z - mu) * rs * ww.z + bb.z;
       o.w = (v[k].w - mu) * rs * ww.w + bb.w;
-      *reinterpret_cast<float4*>(y + (size_t)warp * C + c) = o;
+      if (y) *reinterpret_cast<float4*>(y + (size_t)warp * C + c) = o;
       if (ybf) {
         ushort4 h;
         h.x = to_bf16_bits(o.x);
@@ -69,22 +70,24 @@ __global__ void layernorm_fwd_kernel(float* __restrict__ y, uint16_t* __restrict
   }
 }
 
-// Block = LNB_WARPS warps covering LNB_ROWS consecutive rows.  Writes the
-// block's dw/db partial sums (rows in order, warps in order) to
-// partial[blockIdx][0..C) and partial[blockIdx][C..2C).
+// Block = LNB_WARPS warps covering `rows` consecutive rows (a multiple of
+// LNB_WARPS, at least LNB_MIN_ROWS; the host picks it so that the grid
+// covers the SMs).  Writes the block's dw/db partial sums (rows in order,
+// warps in order) to partial[blockIdx][0..C) and partial[blockIdx][C..2C).
 #define LNB_WARPS 8
-#define LNB_ROWS 32
+#define LNB_MIN_ROWS 8
 
 __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
-    float* __restrict__ dx, float* __restrict__ partial, const float* __restrict__ dy, const float* __restrict__ x,
-    const float* __restrict__ w, const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C) {
+    float* __restrict__ dx, uint16_t* __restrict__ dxbf, float* __restrict__ partial, const float* __restrict__ dy,
+    const float* __restrict__ x, const float* __restrict__ w, const float* __restrict__ mean,
+    const float* __restrict__ rstd, int N, int C, int rows) {
   extern __shared__ float sh[];  // [2C]
   int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float4 aw[LN_MAXV4], ab[LN_MAXV4];
 #pragma unroll
   for (int k = 0; k < LN_MAXV4; k++) aw[k] = ab[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  int r0 = blockIdx.x * LNB_ROWS;
-  for (int r = r0 + warp; r < min(N, r0 + LNB_ROWS); r += LNB_WARPS) {
+  int r0 = blockIdx.x * rows;
+  for (int r = r0 + warp; r < min(N, r0 + rows); r += LNB_WARPS) {
     float mu = mean[r], rs = rstd[r];
     float4 n[LN_MAXV4], g[LN_MAXV4], d[LN_MAXV4];
     float sg = 0.f, sgn = 0.f;
@@ -113,6 +116,14 @@ __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
         a.z += rs * (g[k].z - mg - n[k].z * mgn);
         a.w += rs * (g[k].w - mg - n[k].w * mgn);
         *o = a;
+        if (dxbf) {
+          ushort4 hb;
+          hb.x = to_bf16_bits(a.x);
+          hb.y = to_bf16_bits(a.y);
+          hb.z = to_bf16_bits(a.z);
+          hb.w = to_bf16_bits(a.w);
+          *reinterpret_cast<ushort4*>(dxbf + (size_t)r * C + c) = hb;
+        }
         aw[k].x += d[k].x * n[k].x; aw[k].y += d[k].y * n[k].y;
         aw[k].z += d[k].z * n[k].z; aw[k].w += d[k].w * n[k].w;
         ab[k].x += d[k].x; ab[k].y += d[k].y; ab[k].z += d[k].z; ab[k].w += d[k].w;

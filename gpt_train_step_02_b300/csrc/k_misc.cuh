@@ -151,6 +151,7 @@ __global__ void col_partial_kernel(const float* __restrict__ Y, int M, int N, lo
   if (col >= N) return;
   int r0 = blockIdx.y * rows, r1 = min(M, r0 + rows);
   float s = 0.f;
+#pragma unroll 8
   for (int r = r0; r < r1; r++) s += Y[(size_t)r * ldy + col];
   partial[(size_t)blockIdx.y * N + col] = s;
 }

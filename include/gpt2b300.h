@@ -179,11 +179,14 @@ long long gpt2_last_launch_count(const gpt2_t* m);
  * The per-layer matmul of the page's item 1 (matmul_forward /
  * matmul_backward), run by the same tensor-core kernels the model uses; for
  * per-layer parity tests.  x (N, IC), W (OC, IC), bias (OC), out (N, OC).
- * precision is GPT2_PREC_FP32 or GPT2_PREC_BF16.  workspace: a device buffer
- * of gpt2op_matmul_workspace_bytes(N, OC) bytes (scratch; contents not
+ * precision is GPT2_PREC_FP32 (3xTF32 products) or GPT2_PREC_BF16 (the
+ * operands are rounded to bf16 into the workspace first, then multiplied by
+ * the bf16 kernel with fp32 accumulation).  workspace: a device buffer of
+ * gpt2op_matmul_workspace_bytes(N, IC, OC) bytes (scratch; contents not
  * kept).  stream: cudaStream_t or NULL.  Both calls synchronise the stream.
- * IC and OC must be multiples of 4 (16-byte rows for TMA). */
-size_t gpt2op_matmul_workspace_bytes(int N, int OC);
+ * IC and OC must be multiples of 4 (fp32) or 8 (bf16): 16-byte rows for TMA;
+ * otherwise GPT2_ERR_SHAPE. */
+size_t gpt2op_matmul_workspace_bytes(int N, int IC, int OC);
 /* out = x W^T (+ bias when bias != NULL). */
 int gpt2op_matmul_forward(float* out, const float* x, const float* W, const float* bias, int N, int IC, int OC,
                           int precision, void* workspace, void* stream);
@@ -191,6 +194,23 @@ int gpt2op_matmul_forward(float* out, const float* x, const float* W, const floa
  * may be NULL).  dy (N, OC). */
 int gpt2op_matmul_backward(float* dx, float* dW, float* dbias, const float* dy, const float* x, const float* W,
                            int N, int IC, int OC, int precision, void* workspace, void* stream);
+
+/* The per-layer causal attention forward of the page's item 1
+ * (attention_forward), run by the kernels the model uses; for per-layer
+ * parity tests.  qkv (B, T, 3C) row-major: q = columns [0, C), k = [C, 2C),
+ * v = [2C, 3C), head h = columns h*hs .. h*hs+hs-1 of each block, hs = C/NH.
+ * Writes y (B, T, C) = softmax(q k^T / sqrt(hs), keys t2 <= t) v and
+ * lse (B, NH, T), the log-sum-exp of each row of scaled scores.
+ * precision GPT2_PREC_FP32: CUDA-core kernel in fp32.  GPT2_PREC_BF16: qkv is
+ * rounded to bf16 in the workspace; with hs = 64 and T % 128 == 0 the
+ * tensor-core kernel computes the products (softmax in fp32, P rounded to
+ * bf16 for P V), otherwise the CUDA-core kernel with bf16-rounded operands.
+ * workspace: gpt2op_attention_workspace_bytes(B, T, C) device bytes.
+ * Requirements: C % NH == 0, hs <= 128, C % 8 == 0 (else GPT2_ERR_SHAPE).
+ * Synchronises the stream. */
+size_t gpt2op_attention_workspace_bytes(int B, int T, int C);
+int gpt2op_attention_forward(float* y, float* lse, const float* qkv, int B, int T, int C, int NH, int precision,
+                             void* workspace, void* stream);
 
 /* gpt2op_matmul_backward without a workspace argument: the same products
  * (dx = dy W; dW += dy^T x; dbias += column sums of dy, dbias may be NULL)
@@ -210,7 +230,9 @@ int gpt2op_matmul_backward(float* dx, float* dW, float* dbias, const float* dy, 
  * give wrong results.
  * Limit: with dbias != NULL, ceil(N/64) * OC must be <= 1,048,576 (for
  * example N = 16384 with OC <= 4096); larger shapes return GPT2_ERR_SHAPE
- * before any device work.  The split-K partials use the rest of the array,
+ * before any device work.  precision must be GPT2_PREC_FP32 (bf16 operand
+ * copies would need scratch that grows with the inputs): GPT2_ERR_ARG
+ * otherwise.  The split-K partials use the rest of the array,
  * which only lowers how far K is split.  Synchronises the stream. */
 int gpt2op_matmul_backward_noalloc(float* dx, float* dW, float* dbias, const float* dy, const float* x,
                                    const float* W, int N, int IC, int OC, int precision, void* stream);

@@ -1,0 +1,90 @@
+"""Per-layer parity of the causal attention forward against the oracle's
+attention_forward (the page «llm.c：Andrej Karpathy带你从零复现LLM», section
+«核心代码解读：train_gpt2.c», item 1), through the C ABI.
+
+* fp32: the CUDA-core kernel, against the fp32 oracle, 1e-5 relative.
+* bf16 with head size 64 and T % 128 == 0: the tensor-core kernel, against
+  the oracle fed the same bf16-rounded qkv.  The kernel also rounds the
+  softmax weights P to bf16 for the P V product; the row sums use the same
+  rounded weights, so y is a convex combination with weights perturbed by at
+  most 2^-9 relative.  Tolerance: max |dy| <= 1e-2 max |v|, |d lse| <= 1e-2.
+* bf16 with another head size: the CUDA-core kernel with rounded operands.
+Inputs come from ``synth``; expected values from ``oracle/`` only."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import ref
+
+pytestmark = pytest.mark.gpu
+
+OPS = ref.ops(np.float32)
+
+
+def bf16(a):
+    """Round to the nearest bf16 (ties to even), returned as float32."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+def oracle_lse(preatt):
+    """Row log-sum-exp of the scaled scores over the causal keys t2 <= t."""
+    B, NH, T, _ = preatt.shape
+    s = preatt.astype(np.float64)
+    mask = np.tril(np.ones((T, T), bool))
+    s = np.where(mask, s, -np.inf)
+    mx = s.max(-1, keepdims=True)
+    return (mx[..., 0] + np.log(np.exp(s - mx).sum(-1))).astype(np.float32)
+
+
+def run_gpu(qkv, NH, precision):
+    import torch
+    import gpt_train_step_02_b300 as g
+
+    B, T, C3 = qkv.shape
+    C = C3 // 3
+    y = torch.full((B, T, C), float("nan"), device="cuda")
+    lse = torch.full((B, NH, T), float("nan"), device="cuda")
+    g.attention_forward(y, lse, torch.tensor(qkv, device="cuda"), NH, precision=precision)
+    return y.cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("B,T,C,NH", [(2, 32, 64, 4), (1, 13, 64, 4), (2, 64, 768, 12), (1, 1, 64, 4)])
+def test_attention_forward_fp32(B, T, C, NH):
+    import gpt_train_step_02_b300 as g
+
+    qkv = synth.randn(301, (B, T, 3 * C))
+    y, lse = run_gpu(qkv, NH, g.GPT2_PREC_FP32)
+    ry, preatt, _ = OPS.attention_forward(qkv, NH)
+    assert np.abs(y - ry).max() <= 1e-5 * max(np.abs(ry).max(), 1.0)
+    assert np.abs(lse - oracle_lse(preatt)).max() <= 1e-4
+
+
+@pytest.mark.parametrize("B,T,C,NH", [(2, 128, 128, 2), (1, 256, 64, 1), (2, 384, 128, 2), (1, 1024, 768, 12)])
+def test_attention_forward_bf16_tensor_cores(B, T, C, NH):
+    import gpt_train_step_02_b300 as g
+
+    qkv = synth.randn(302, (B, T, 3 * C))
+    y, lse = run_gpu(qkv, NH, g.GPT2_PREC_BF16)
+    q = bf16(qkv)
+    ry, preatt, _ = OPS.attention_forward(q, NH)
+    vmax = np.abs(q[..., 2 * C:]).max()
+    assert np.isfinite(y).all() and np.isfinite(lse).all()
+    assert np.abs(y - ry).max() <= 1e-2 * vmax, np.abs(y - ry).max()
+    assert np.abs(lse - oracle_lse(preatt)).max() <= 1e-2
+    # the first query row attends to itself only: y = its own v exactly
+    hs = C // NH
+    np.testing.assert_allclose(y[:, 0, :], q[:, 0, 2 * C:], rtol=0, atol=0)
+    del hs
+
+
+def test_attention_forward_bf16_other_head_size():
+    import gpt_train_step_02_b300 as g
+
+    B, T, C, NH = 2, 32, 64, 4  # hs = 16: the CUDA-core kernel with bf16 operands
+    qkv = synth.randn(303, (B, T, 3 * C))
+    y, lse = run_gpu(qkv, NH, g.GPT2_PREC_BF16)
+    ry, preatt, _ = OPS.attention_forward(bf16(qkv), NH)
+    assert np.abs(y - ry).max() <= 1e-2 * np.abs(ry).max()
+    assert np.abs(lse - oracle_lse(preatt)).max() <= 1e-3

@@ -68,22 +68,67 @@ def test_matmul_forward_backward_fp32(N, IC, OC):
     assert rel_err(tdb.cpu().numpy() - db0, rdb) < 1e-5
 
 
-def test_matmul_bf16_operands():
+def bf16(a):
+    """Round to the nearest bf16 (ties to even), returned as float32."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+SHAPES_BF16 = [  # (N rows, IC, OC); IC and OC multiples of 8 (16-byte bf16 rows)
+    (64, 64, 192),      # tiny config QKV: one 128-wide column tile
+    (13, 72, 104),      # ragged everything, N <= 128 (128-wide tiles)
+    (300, 96, 264),     # M spans 3 tiles with a tail; 256-wide column tiles with a tail
+    (256, 768, 2304),   # 124M QKV at B*T=256
+    (256, 3072, 768),   # MLP output projection: K split for the weight gradient
+    (1024, 768, 768),   # attention projection at B*T=1024: K-split weight gradient
+    (256, 768, 50304),  # LM head (tied wte), 197 column tiles
+]
+
+
+@pytest.mark.parametrize("N,IC,OC", SHAPES_BF16)
+def test_matmul_bf16_forward_backward(N, IC, OC):
+    """bf16 tensor-core products against the oracle fed the same bf16-rounded
+    operands (the products are exact in fp32; only the fp32 accumulation
+    order differs)."""
     import torch
     import gpt_train_step_02_b300 as g
 
-    N, IC, OC = 256, 768, 2304
     x = synth.randn(111, (N, IC))
     W = synth.randn(112, (OC, IC), 0.02)
+    b = synth.randn(113, (OC,), 0.1)
+    dy = synth.randn(114, (N, OC))
+    dW0 = synth.randn(115, (OC, IC), 0.01)
+    db0 = synth.randn(116, (OC,), 0.01)
+    tx, tW, tb, tdy = (torch.tensor(a, device="cuda") for a in (x, W, b, dy))
+    P = g.GPT2_PREC_BF16
+
     out = torch.empty((N, OC), dtype=torch.float32, device="cuda")
-    g.matmul_forward(out, torch.tensor(x, device="cuda"), torch.tensor(W, device="cuda"), None,
-                     precision=g.GPT2_PREC_BF16)
+    g.matmul_forward(out, tx, tW, tb, precision=P)
+    ref_out = OPS.matmul_forward(bf16(x), bf16(W), b)
+    assert rel_err(out.cpu().numpy(), ref_out) < tol(IC)
+    if IC >= 64:  # really bf16: the unrounded product differs
+        assert rel_err(out.cpu().numpy() - b, OPS.matmul_forward(x, W, None)) > 1e-4
 
-    def bf16(a):  # round to nearest even at 16 bits
-        u = a.astype(np.float32).view(np.uint32).astype(np.uint64)
-        u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-        return u.astype(np.uint32).view(np.float32)
+    dx = torch.empty((N, IC), dtype=torch.float32, device="cuda")
+    tdW = torch.tensor(dW0, device="cuda")
+    tdb = torch.tensor(db0, device="cuda")
+    g.matmul_backward(dx, tdW, tdb, tdy, tx, tW, precision=P)
+    rdx, rdW, _ = OPS.matmul_backward(bf16(dy), bf16(x), bf16(W), False)
+    _, _, rdb = OPS.matmul_backward(dy, x, W, True)  # the bias gradient sums the fp32 dy
+    assert rel_err(dx.cpu().numpy(), rdx) < tol(OC)
+    assert rel_err(tdW.cpu().numpy() - dW0, rdW) < tol(N)
+    assert rel_err(tdb.cpu().numpy() - db0, rdb) < 1e-5
 
-    ref_out = OPS.matmul_forward(bf16(x), bf16(W), None)
-    assert rel_err(out.cpu().numpy(), ref_out) < 1e-5
-    assert rel_err(out.cpu().numpy(), OPS.matmul_forward(x, W, None)) > 1e-4  # really bf16
+
+def test_matmul_bf16_rejects_rows_that_are_not_16_bytes():
+    import torch
+    import gpt_train_step_02_b300 as g
+
+    N, IC, OC = 16, 68, 64  # IC % 8 != 0: a bf16 row of 136 bytes
+    x = torch.zeros((N, IC), device="cuda")
+    W = torch.zeros((OC, IC), device="cuda")
+    out = torch.zeros((N, OC), device="cuda")
+    with pytest.raises(g.GPT2Error) as e:
+        g.matmul_forward(out, x, W, None, precision=g.GPT2_PREC_BF16)
+    assert e.value.status == g.GPT2_ERR_SHAPE
