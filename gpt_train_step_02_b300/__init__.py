@@ -41,6 +41,7 @@ EXPORTS = [
     "gpt2_get_logits", "gpt2_last_launch_count", "gpt2_status_string", "gpt2_train_step", "gpt2_kernel_timer",
     "gpt2_kernel_timer_read", "gpt2op_matmul_workspace_bytes", "gpt2op_matmul_forward", "gpt2op_matmul_backward",
     "gpt2op_matmul_backward_noalloc", "gpt2op_attention_workspace_bytes", "gpt2op_attention_forward",
+    "gpt2op_attention_backward_workspace_bytes", "gpt2op_attention_backward",
 ]
 
 
@@ -95,6 +96,8 @@ def lib() -> ct.CDLL:
             "gpt2op_matmul_backward_noalloc": (I, [P, P, P, P, P, P, I, I, I, I, P]),
             "gpt2op_attention_workspace_bytes": (SZ, [I, I, I]),
             "gpt2op_attention_forward": (I, [P, P, P, I, I, I, I, I, P, P]),
+            "gpt2op_attention_backward_workspace_bytes": (SZ, [I, I, I, I]),
+            "gpt2op_attention_backward": (I, [P, P, P, I, I, I, I, I, P, P]),
             "gpt2_kernel_timer_read": (I, [P, ct.POINTER(ct.c_double), ct.POINTER(LL), ct.POINTER(ct.c_double)]),
         }
         for name, (res, args) in sig.items():
@@ -375,6 +378,19 @@ def attention_forward(y, lse, qkv, NH, precision=GPT2_PREC_FP32, stream=None):
     s = stream or torch.cuda.current_stream()
     _check(lib().gpt2op_attention_forward(_dptr(y), _dptr(lse), _dptr(qkv), B, T, C, NH, precision, _dptr(ws),
                                           s.cuda_stream), "gpt2op_attention_forward")
+
+
+def attention_backward(dqkv, dy, qkv, NH, precision=GPT2_PREC_FP32, stream=None):
+    """dqkv (B,T,3C) from the upstream gradient dy (B,T,C) of causal attention."""
+    import torch
+
+    B, T, C3 = qkv.shape
+    C = C3 // 3
+    ws = torch.empty(lib().gpt2op_attention_backward_workspace_bytes(B, T, C, NH), dtype=torch.uint8,
+                     device=qkv.device)
+    s = stream or torch.cuda.current_stream()
+    _check(lib().gpt2op_attention_backward(_dptr(dqkv), _dptr(dy), _dptr(qkv), B, T, C, NH, precision, _dptr(ws),
+                                           s.cuda_stream), "gpt2op_attention_backward")
 
 
 def matmul_backward_noalloc(dx, dW, dbias, dy, x, W, precision=GPT2_PREC_FP32, stream=None):

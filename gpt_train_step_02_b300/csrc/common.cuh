@@ -16,6 +16,14 @@ enum DevError : int {
   DEV_ERR_SHAPE = 3,        // a kernel was launched with a shape it cannot handle
 };
 
+// Programmatic dependent launch.  pdl_wait blocks until the kernels this one
+// depends on in the stream have completed and their memory is visible (a
+// no-op when the kernel was launched without the attribute);
+// pdl_launch_dependents lets the next kernel's CTAs be scheduled once every
+// CTA of this grid has issued it or exited.
+GPT2_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+GPT2_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 GPT2_DEV void dev_set_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }

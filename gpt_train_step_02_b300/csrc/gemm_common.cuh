@@ -4,7 +4,8 @@
 // gradient and weight gradient.  Each output element acc(i,j) of such a
 // product is finished by one epilogue (below).  When Cbf is set, every
 // output is also stored, rounded to bf16 (nearest even), at Cbf(i,j): the
-// operand copy the next bf16 matmul reads.
+// operand copy the next bf16 matmul reads.  C may be NULL when only the bf16
+// copy is wanted (not with EPI_ACCUM, which reads C).
 #pragma once
 #include "common.cuh"
 
@@ -47,7 +48,7 @@ GPT2_DEV void epi_store(const EpiArgs& e, int i, int j, float acc) {
     case EPI_ACCUM: out = e.C[ci] + acc; break;
     default: out = acc;
   }
-  e.C[ci] = out;
+  if (e.C) e.C[ci] = out;
   if (e.Cbf) e.Cbf[(size_t)i * e.ldcbf + j] = to_bf16_bits(out);
 }
 
@@ -102,7 +103,7 @@ GPT2_DEV void epi_store_row32(const EpiArgs& e, int i, int j0, const float* v, i
 #pragma unroll
       for (int c = 0; c < 4; c++) o[c] = gelu_fwd(o[c]);
     }
-    st4(crow + 4 * q, make_float4(o[0], o[1], o[2], o[3]));
+    if (e.C) st4(crow + 4 * q, make_float4(o[0], o[1], o[2], o[3]));
     if (e.Cbf) {
       uint2 h;
       h.x = (uint32_t)to_bf16_bits(o[0]) | ((uint32_t)to_bf16_bits(o[1]) << 16);
@@ -153,7 +154,7 @@ GPT2_DEV void epi_store4(const EpiArgs& e, int i, int j, float4 acc) {
     }
     default: break;
   }
-  st4(cp, o);
+  if (e.C) st4(cp, o);
   if (e.Cbf) {
     uint2 h;
     h.x = (uint32_t)to_bf16_bits(o.x) | ((uint32_t)to_bf16_bits(o.y) << 16);

@@ -17,6 +17,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <utility>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -58,7 +59,7 @@ struct Plan {
   size_t lnf, lnf_mean, lnf_rstd, logits, dlogits, losses, loss;
   size_t dres, dln, datty, dqkv, dfch, attD, scratch, sorted, tokens, targets, err, hparams, splitk, tilectr;
   // bf16 operand copies (bf16 matmuls only)
-  size_t ln1_bf, qkv_bf, atty_bf, ln2_bf, fchg_bf, lnf_bf, dlogits_bf, dres_bf, dfch_bf, dqkv_bf;
+  size_t ln1_bf, qkv_bf, atty_bf, ln2_bf, fchg_bf, lnf_bf, dlogits_bf, dres_bf, dfch_bf, dqkv_bf, datty_bf;
   size_t scratch_floats;
 };
 
@@ -159,6 +160,7 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->dres_bf = take(BT * C * H);
   p->dfch_bf = take(BT * 4 * C * H);
   p->dqkv_bf = take(BT * 3 * C * H);
+  p->datty_bf = take(BT * C * H);
   p->total = off;
   return off;
 }
@@ -185,7 +187,8 @@ struct gpt2_t {
   float *dres, *dln, *datty, *dqkv, *dfch, *attD, *scratch, *splitk;
   uint32_t* sorted;
   int *tokens, *targets, *err, *tilectr;
-  uint16_t *ln1_bf, *qkv_bf, *atty_bf, *ln2_bf, *fchg_bf, *lnf_bf, *dlogits_bf, *dres_bf, *dfch_bf, *dqkv_bf;
+  uint16_t *ln1_bf, *qkv_bf, *atty_bf, *ln2_bf, *fchg_bf, *lnf_bf, *dlogits_bf, *dres_bf, *dfch_bf, *dqkv_bf,
+      *datty_bf;
   float* hparams;
   int B, T, have_targets, fwd_done;
   int poisoned;
@@ -253,6 +256,28 @@ static inline void timer_end(gpt2_t* m, int kind) {
       return GPT2_ERR_CUDA;                        \
     }                                              \
   } while (0)
+
+// Every kernel is launched with programmatic stream serialization: the next
+// kernel in the stream may start (its CTAs run their set-up, then wait at
+// griddepcontrol.wait inside the kernel) while this one drains.  Kernels call
+// griddepcontrol.wait before their first global-memory access, so every
+// read-after-write and write-after-read on the stream stays ordered.
+static int g_pdl = 1;
+
+template <typename... KArgs, typename... Args>
+static void launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = g_pdl ? 1 : 0;
+  cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);  // errors surface at the next KCHECK
+}
 
 static int grid_for(long long n, int threads, int cap = 148 * 16) {
   long long g = (n + threads - 1) / threads;
@@ -352,13 +377,15 @@ static int launch_matmul(const MatmulDesc& d, cudaStream_t s, int* err) {
   cfg.blockDim = dim3(tc::THREADS);
   cfg.dynamicSmemBytes = tc::SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = splits;
-  cfg.attrs = attr;
-  cfg.numAttrs = splits > 1 ? 1 : 0;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = splits;
+  cfg.attrs = g_pdl ? attr : attr + 1;
+  cfg.numAttrs = (g_pdl ? 1 : 0) + (splits > 1 ? 1 : 0);
   if (cudaLaunchKernelEx(&cfg, tc::gemm_tf32x3_kernel, ta, tb, p) != cudaSuccess) return -1;
   return 1;
 }
@@ -399,7 +426,7 @@ static int choose_splits_bf16(int M, int N, int K, int BN, long long ws_floats) 
 template <int BN>
 static void launch_bf16_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const tcb::Params& p, int grid,
                                cudaStream_t s) {
-  tcb::gemm_bf16_kernel<BN><<<grid, tcb::THREADS, tcb::Cfg<BN>::SMEM_BYTES, s>>>(ta, tb, p);
+  launch_k(tcb::gemm_bf16_kernel<BN>, grid, tcb::THREADS, tcb::Cfg<BN>::SMEM_BYTES, s, ta, tb, p);
 }
 
 // Launches the persistent bf16 tensor-core matmul.  Output tiles are 128 x 256
@@ -492,8 +519,8 @@ static void bias_grad(gpt2_t* m, float* db, const float* dy, int N, int OC) {
   int rows = ceil_div(N, want);
   if (rows < BIAS_MIN_ROWS) rows = BIAS_MIN_ROWS;
   int chunks = ceil_div(N, rows);
-  col_partial_kernel<<<dim3(colb, chunks), 256, 0, m->stream>>>(dy, N, OC, OC, rows, m->scratch);
-  col_finish_kernel<<<colb, 256, 0, m->stream>>>(m->scratch, chunks, OC, db);
+  launch_k(col_partial_kernel, dim3(colb, chunks), 256, 0, m->stream, dy, N, OC, OC, rows, m->scratch);
+  launch_k(col_finish_kernel, colb, 256, 0, m->stream, m->scratch, chunks, OC, db);
   m->launches += 2;
 }
 
@@ -501,7 +528,7 @@ static void ln_forward(gpt2_t* m, float* y, uint16_t* ybf, float* mean, float* r
                        const float* b, int N) {
   int C = m->cfg.channels;
   timer_begin(m, TK_LAYERNORM, (8.0 * C + 8.0) * N);
-  layernorm_fwd_kernel<<<ceil_div(N, 8), 256, 0, m->stream>>>(y, ybf, mean, rstd, x, w, b, N, C);
+  launch_k(layernorm_fwd_kernel, ceil_div(N, 8), 256, 0, m->stream, y, ybf, mean, rstd, x, w, b, N, C);
   timer_end(m, TK_LAYERNORM);
   m->launches++;
 }
@@ -514,9 +541,9 @@ static void ln_backward(gpt2_t* m, float* dx, uint16_t* dxbf, float* dw, float* 
   if (rows < LNB_MIN_ROWS) rows = LNB_MIN_ROWS;
   int nb = ceil_div(N, rows);
   timer_begin(m, TK_LAYERNORM, (16.0 * C + 8.0) * N);
-  layernorm_bwd_kernel<<<nb, LNB_WARPS * 32, 2 * C * sizeof(float), m->stream>>>(dx, dxbf, m->scratch, dy, x, w,
+  launch_k(layernorm_bwd_kernel, nb, LNB_WARPS * 32, 2 * C * sizeof(float), m->stream, dx, dxbf, m->scratch, dy, x, w,
                                                                                     mean, rstd, N, C, rows);
-  layernorm_param_grad_kernel<<<ceil_div(C, 256), 256, 0, m->stream>>>(dw, db, m->scratch, nb, C);
+  launch_k(layernorm_param_grad_kernel, ceil_div(C, 256), 256, 0, m->stream, dw, db, m->scratch, nb, C);
   timer_end(m, TK_LAYERNORM);
   m->launches += 2;
 }
@@ -537,13 +564,13 @@ static int launch_attn_fwd(float* atty, uint16_t* attybf, float* lse, const floa
     p.B = B; p.T = T; p.C = C; p.NH = NH;
     p.scale = 1.0f / sqrtf((float)hs);
     p.y = atty; p.ybf = attybf; p.lse = lse; p.err = err;
-    tca::attn_fwd_tc_kernel<<<dim3(T / tca::BQ, NH, B), tca::THREADS, tca::SMEM_BYTES, s>>>(tm, p);
+    launch_k(tca::attn_fwd_tc_kernel, dim3(T / tca::BQ, NH, B), tca::THREADS, tca::fwd::SMEM_BYTES, s, tm, p);
     return 1;
   }
   int grid = ceil_div((long long)B * NH * T * 32, 256);
-  if (hs <= 32) attn_fwd_simt_kernel<1><<<grid, 256, 0, s>>>(atty, attybf, lse, qkv, B, T, C, NH, bf);
-  else if (hs <= 64) attn_fwd_simt_kernel<2><<<grid, 256, 0, s>>>(atty, attybf, lse, qkv, B, T, C, NH, bf);
-  else attn_fwd_simt_kernel<4><<<grid, 256, 0, s>>>(atty, attybf, lse, qkv, B, T, C, NH, bf);
+  if (hs <= 32) launch_k(attn_fwd_simt_kernel<1>, grid, 256, 0, s, atty, attybf, lse, qkv, B, T, C, NH, bf);
+  else if (hs <= 64) launch_k(attn_fwd_simt_kernel<2>, grid, 256, 0, s, atty, attybf, lse, qkv, B, T, C, NH, bf);
+  else launch_k(attn_fwd_simt_kernel<4>, grid, 256, 0, s, atty, attybf, lse, qkv, B, T, C, NH, bf);
   return 1;
 }
 
@@ -560,24 +587,53 @@ static void attn_forward(gpt2_t* m, float* atty, uint16_t* attybf, float* lse, c
   m->launches += n;
 }
 
-static void attn_backward(gpt2_t* m, const float* qkv, const float* atty, const float* lse, int B, int T, int bf) {
-  int C = m->cfg.channels, NH = m->cfg.num_heads, hs = C / NH;
-  int grid = ceil_div((long long)B * NH * T * 32, 256);
-  cudaStream_t s = m->stream;
-  timer_begin(m, TK_ATTN_BWD, 8.0 * (double)B * NH * T * (T + 1) / 2.0 * hs);
-  attn_bwd_D_kernel<<<grid, 256, 0, s>>>(m->attD, m->datty, atty, B, T, C, NH);
-  if (hs <= 32) {
-    attn_bwd_dq_kernel<1><<<grid, 256, 0, s>>>(m->dqkv, m->dqkv_bf, qkv, m->datty, lse, m->attD, B, T, C, NH, bf);
-    attn_bwd_dkv_kernel<1><<<grid, 256, 0, s>>>(m->dqkv, m->dqkv_bf, qkv, m->datty, lse, m->attD, B, T, C, NH, bf);
-  } else if (hs <= 64) {
-    attn_bwd_dq_kernel<2><<<grid, 256, 0, s>>>(m->dqkv, m->dqkv_bf, qkv, m->datty, lse, m->attD, B, T, C, NH, bf);
-    attn_bwd_dkv_kernel<2><<<grid, 256, 0, s>>>(m->dqkv, m->dqkv_bf, qkv, m->datty, lse, m->attD, B, T, C, NH, bf);
-  } else {
-    attn_bwd_dq_kernel<4><<<grid, 256, 0, s>>>(m->dqkv, m->dqkv_bf, qkv, m->datty, lse, m->attD, B, T, C, NH, bf);
-    attn_bwd_dkv_kernel<4><<<grid, 256, 0, s>>>(m->dqkv, m->dqkv_bf, qkv, m->datty, lse, m->attD, B, T, C, NH, bf);
+// Causal attention backward into dqkv (and its bf16 copy): D = rowsum(dy o y),
+// then the tensor-core dK/dV and dQ kernels (bf16, hs = 64, T % 128 == 0) or
+// the CUDA-core kernels.  Returns the number of launches, or -1.
+static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float* dy, const uint16_t* dy_bf,
+                           const float* qkv, const uint16_t* qkv_bf, const float* atty, const float* lse, int B, int T,
+                           int C, int NH, int bf, int* err, cudaStream_t s) {
+  const int hs = C / NH;
+  const int grid = ceil_div((long long)B * NH * T * 32, 256);
+  launch_k(attn_bwd_D_kernel, grid, 256, 0, s, D, dy, atty, B, T, C, NH);
+  if (bf && qkv_bf && dy_bf && hs == tca::HS && T % tca::BQ == 0) {
+    CUtensorMap tq, td;
+    if (!make_bf16_map(&tq, qkv_bf, 1, (long long)B * T, 3LL * C, 3LL * C, tca::BQ)) return -1;
+    if (!make_bf16_map(&td, dy_bf, 1, (long long)B * T, C, C, tca::BQ)) return -1;
+    tca::BwdParams p;
+    p.B = B; p.T = T; p.C = C; p.NH = NH;
+    p.scale = 1.0f / sqrtf((float)hs);
+    p.lse = lse; p.D = D; p.dqkv = dqkv; p.dqkv_bf = dqkv_bf; p.err = err;
+    dim3 g(T / tca::BQ, NH, B);
+    launch_k(tca::attn_bwd_dkv_tc_kernel, g, tca::THREADS, tca::dkv::SMEM_BYTES, s, tq, td, p);
+    launch_k(tca::attn_bwd_dq_tc_kernel, g, tca::THREADS, tca::dqk::SMEM_BYTES, s, tq, td, p);
+    return 3;
   }
+  if (hs <= 32) {
+    launch_k(attn_bwd_dq_kernel<1>, grid, 256, 0, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
+    launch_k(attn_bwd_dkv_kernel<1>, grid, 256, 0, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
+  } else if (hs <= 64) {
+    launch_k(attn_bwd_dq_kernel<2>, grid, 256, 0, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
+    launch_k(attn_bwd_dkv_kernel<2>, grid, 256, 0, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
+  } else {
+    launch_k(attn_bwd_dq_kernel<4>, grid, 256, 0, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
+    launch_k(attn_bwd_dkv_kernel<4>, grid, 256, 0, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
+  }
+  return 3;
+}
+
+static void attn_backward(gpt2_t* m, const float* qkv, const uint16_t* qkv_bf, const float* atty, const float* lse,
+                          int B, int T, int bf) {
+  int C = m->cfg.channels, NH = m->cfg.num_heads, hs = C / NH;
+  timer_begin(m, TK_ATTN_BWD, 8.0 * (double)B * NH * T * (T + 1) / 2.0 * hs);
+  int n = launch_attn_bwd(m->dqkv, m->dqkv_bf, m->attD, m->datty, m->datty_bf, qkv, qkv_bf, atty, lse, B, T, C, NH, bf,
+                          m->err, m->stream);
   timer_end(m, TK_ATTN_BWD);
-  m->launches += 3;
+  if (n < 0) {
+    m->poisoned = GPT2_ERR_CUDA;
+    return;
+  }
+  m->launches += n;
 }
 
 // Dynamic shared memory limits of the large-smem kernels, set once per process.
@@ -598,7 +654,13 @@ static int set_kernel_attributes() {
                                tcb::Cfg<128>::SMEM_BYTES);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tca::attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               tca::SMEM_BYTES);
+                               tca::fwd::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tca::attn_bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               tca::dkv::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tca::attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               tca::dqk::SMEM_BYTES);
     if (e != cudaSuccess) {
       fprintf(stderr, "gpt2b300: cudaFuncSetAttribute failed: %s\n", cudaGetErrorString(e));
       cudaGetLastError();
@@ -663,38 +725,43 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
   int bf = c.gemm_precision == GPT2_PREC_BF16;
   const size_t CC = (size_t)C * C;
   if (validate) {
-    validate_tokens_kernel<<<grid_for(N, 256, 64), 256, 0, s>>>(d_in, d_tgt, N, V, m->err);
+    launch_k(validate_tokens_kernel, grid_for(N, 256, 64), 256, 0, s, d_in, d_tgt, N, V, m->err);
     m->launches++;
   }
-  encoder_fwd_kernel<<<grid_for((long long)N * C / 4, 256), 256, 0, s>>>(m->encoded, d_in, m->P[P_WTE], m->P[P_WPE],
+  launch_k(encoder_fwd_kernel, grid_for((long long)N * C / 4, 256), 256, 0, s, m->encoded, d_in, m->P[P_WTE], m->P[P_WPE],
                                                                           N, T, C, V);
   m->launches++;
+  // bf16 matmuls read only the bf16 copies: the fp32 layernorm outputs, the
+  // fp32 GELU output and (with the tensor-core attention) the fp32 qkv are
+  // then not written at all
+  const bool tc_attn = bf && C / c.num_heads == tca::HS && T % tca::BQ == 0;
   for (int l = 0; l < L; l++) {
     LayerActs a = layer_acts(m, l);
-    ln_forward(m, a.ln1, a.ln1_bf, a.ln1_mean, a.ln1_rstd, a.x, m->P[P_LN1W] + (size_t)l * C,
+    ln_forward(m, bf ? nullptr : a.ln1, a.ln1_bf, a.ln1_mean, a.ln1_rstd, a.x, m->P[P_LN1W] + (size_t)l * C,
                m->P[P_LN1B] + (size_t)l * C, N);
-    mm_forward(m, a.qkv, a.qkv_bf, {a.ln1, a.ln1_bf}, wparam(m, P_QKVW, l * 3 * CC),
+    mm_forward(m, tc_attn ? nullptr : a.qkv, a.qkv_bf, {a.ln1, a.ln1_bf}, wparam(m, P_QKVW, l * 3 * CC),
                m->P[P_QKVB] + (size_t)l * 3 * C, N, C, 3 * C, EPI_BIAS, nullptr, nullptr);
     attn_forward(m, a.atty, a.atty_bf, a.lse, a.qkv, a.qkv_bf, B, T, bf);
     mm_forward(m, a.res2, nullptr, {a.atty, a.atty_bf}, wparam(m, P_ATTPROJW, l * CC), m->P[P_ATTPROJB] + (size_t)l * C,
                N, C, C, EPI_BIAS_RESID, a.x, nullptr);
-    ln_forward(m, a.ln2, a.ln2_bf, a.ln2_mean, a.ln2_rstd, a.res2, m->P[P_LN2W] + (size_t)l * C,
+    ln_forward(m, bf ? nullptr : a.ln2, a.ln2_bf, a.ln2_mean, a.ln2_rstd, a.res2, m->P[P_LN2W] + (size_t)l * C,
                m->P[P_LN2B] + (size_t)l * C, N);
-    mm_forward(m, a.fchg, a.fchg_bf, {a.ln2, a.ln2_bf}, wparam(m, P_FCW, l * 4 * CC), m->P[P_FCB] + (size_t)l * 4 * C,
-               N, C, 4 * C, EPI_BIAS_GELU, nullptr, a.fch);
+    mm_forward(m, bf ? nullptr : a.fchg, a.fchg_bf, {a.ln2, a.ln2_bf}, wparam(m, P_FCW, l * 4 * CC),
+               m->P[P_FCB] + (size_t)l * 4 * C, N, C, 4 * C, EPI_BIAS_GELU, nullptr, a.fch);
     mm_forward(m, a.res3, nullptr, {a.fchg, a.fchg_bf}, wparam(m, P_FCPROJW, l * 4 * CC),
                m->P[P_FCPROJB] + (size_t)l * C, N, 4 * C, C, EPI_BIAS_RESID, a.res2, nullptr);
   }
   LayerActs last = layer_acts(m, L - 1);
-  ln_forward(m, m->lnf, m->lnf_bf, m->lnf_mean, m->lnf_rstd, last.res3, m->P[P_LNFW], m->P[P_LNFB], N);
+  ln_forward(m, bf ? nullptr : m->lnf, m->lnf_bf, m->lnf_mean, m->lnf_rstd, last.res3, m->P[P_LNFW], m->P[P_LNFB], N);
   mm_forward(m, m->logits, nullptr, {m->lnf, m->lnf_bf}, wparam(m, P_WTE, 0), nullptr, N, C, Vp, EPI_STORE, nullptr,
              nullptr);
   if (d_tgt) {
     timer_begin(m, TK_XENT, 8.0 * (double)N * Vp);
-    xent_fused_kernel<<<N, XENT_THREADS, 0, s>>>(m->dlogits, m->dlogits_bf, m->losses, m->logits, d_tgt, V, Vp,
+    launch_k(xent_fused_kernel, N, XENT_THREADS, 0, s, bf ? nullptr : m->dlogits, m->dlogits_bf, m->losses, m->logits,
+             d_tgt, V, Vp,
                                                  1.0f / (float)N);
     timer_end(m, TK_XENT);
-    mean_kernel<<<1, 1024, 0, s>>>(m->losses, N, m->loss);
+    launch_k(mean_kernel, 1, 1024, 0, s, m->losses, N, m->loss);
     m->launches += 2;
   }
   KCHECK(m);
@@ -737,9 +804,9 @@ static int enqueue_backward(gpt2_t* m) {
     // attention output projection: res2 = x + atty attprojw^T + attprojb
     mm_dw(m, G[P_ATTPROJW] + l * CC, dres, {a.atty, a.atty_bf}, N, C, C);
     bias_grad(m, G[P_ATTPROJB] + (size_t)l * C, m->dres, N, C);
-    mm_dx(m, m->datty, nullptr, dres, wparam(m, P_ATTPROJW, l * CC), N, C, C, nullptr);
+    mm_dx(m, m->datty, m->datty_bf, dres, wparam(m, P_ATTPROJW, l * CC), N, C, C, nullptr);
     // attention
-    attn_backward(m, a.qkv, a.atty, a.lse, B, T, bf);
+    attn_backward(m, a.qkv, a.qkv_bf, a.atty, a.lse, B, T, bf);
     // qkv projection: qkv = ln1 qkvw^T + qkvb
     mm_dw(m, G[P_QKVW] + l * 3 * CC, dqkv, {a.ln1, a.ln1_bf}, N, C, 3 * C);
     bias_grad(m, G[P_QKVB] + (size_t)l * 3 * C, m->dqkv, N, 3 * C);
@@ -750,9 +817,9 @@ static int enqueue_backward(gpt2_t* m) {
   // embeddings
   size_t smem = 1;
   while ((int)smem < N) smem <<= 1;
-  sort_tokens_kernel<<<1, 1024, smem * sizeof(uint32_t), s>>>(m->tokens, N, c.vocab_size, m->sorted);
-  wte_grad_kernel<<<dim3(N, ceil_div(C, 128)), 32, 0, s>>>(G[P_WTE], m->dres, m->sorted, N, C);
-  wpe_grad_kernel<<<grid_for((long long)T * C / 4, 256), 256, 0, s>>>(G[P_WPE], m->dres, B, T, C);
+  launch_k(sort_tokens_kernel, 1, 1024, smem * sizeof(uint32_t), s, m->tokens, N, c.vocab_size, m->sorted);
+  launch_k(wte_grad_kernel, dim3(N, ceil_div(C, 128)), 32, 0, s, G[P_WTE], m->dres, m->sorted, N, C);
+  launch_k(wpe_grad_kernel, grid_for((long long)T * C / 4, 256), 256, 0, s, G[P_WPE], m->dres, B, T, C);
   m->launches += 3;
   KCHECK(m);
   return GPT2_OK;
@@ -771,7 +838,7 @@ static int write_hparams(gpt2_t* m, float lr, float b1, float b2, float eps, flo
 static int enqueue_update(gpt2_t* m) {
   long long n4 = m->np / 4;
   timer_begin(m, TK_ADAMW, 28.0 * (double)m->np + (m->params_bf ? 2.0 * (double)m->np : 0.0));
-  adamw_kernel<<<grid_for(n4, 256, 148 * 8), 256, 0, m->stream>>>(m->params, m->grads, m->m, m->v, n4, m->hparams,
+  launch_k(adamw_kernel, grid_for(n4, 256, 148 * 8), 256, 0, m->stream, m->params, m->grads, m->m, m->v, n4, m->hparams,
                                                                    m->params_bf);
   timer_end(m, TK_ADAMW);
   m->launches++;
@@ -826,7 +893,7 @@ static void carve(gpt2_t* m) {
 #undef CARVE
 #define CARVE_BF(f) m->f = m->params_bf ? (uint16_t*)(a + p.f) : nullptr
   CARVE_BF(ln1_bf); CARVE_BF(qkv_bf); CARVE_BF(atty_bf); CARVE_BF(ln2_bf); CARVE_BF(fchg_bf); CARVE_BF(lnf_bf); CARVE_BF(dlogits_bf);
-  CARVE_BF(dres_bf); CARVE_BF(dfch_bf); CARVE_BF(dqkv_bf);
+  CARVE_BF(dres_bf); CARVE_BF(dfch_bf); CARVE_BF(dqkv_bf); CARVE_BF(datty_bf);
 #undef CARVE_BF
 }
 
@@ -845,7 +912,7 @@ static int init_params(gpt2_t* m, uint64_t seed) {
       case P_LN1W: case P_LN2W: case P_LNFW: fill = 1.f; break;
       default: break;
     }
-    init_tensor_kernel<<<grid_for(n, 256), 256, 0, m->stream>>>(m->P[i], off, n, nrand, stdv, fill, seed);
+    launch_k(init_tensor_kernel, grid_for(n, 256), 256, 0, m->stream, m->P[i], off, n, nrand, stdv, fill, seed);
     off += n;
   }
   KCHECK(m);
@@ -854,7 +921,7 @@ static int init_params(gpt2_t* m, uint64_t seed) {
 
 static int refresh_bf16(gpt2_t* m) {
   if (!m->params_bf) return GPT2_OK;
-  to_bf16_kernel<<<grid_for(m->np, 256), 256, 0, m->stream>>>(m->params, m->params_bf, m->np);
+  launch_k(to_bf16_kernel, grid_for(m->np, 256), 256, 0, m->stream, m->params, m->params_bf, m->np);
   KCHECK(m);
   return GPT2_OK;
 }
@@ -1215,7 +1282,7 @@ static OpWs op_ws(void* ws, int N, int IC, int OC) {
 }
 
 static int op_to_bf16(const float* x, uint16_t* y, long long n, cudaStream_t s) {
-  to_bf16_kernel<<<grid_for(n, 256), 256, 0, s>>>(x, y, n);
+  launch_k(to_bf16_kernel, grid_for(n, 256), 256, 0, s, x, y, n);
   return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
@@ -1279,8 +1346,8 @@ static int op_backward(float* dx, float* dW, float* dbias, const float* dy, cons
   if ((rc = op_matmul(ddw, precision, w, s))) return rc;
   if (dbias) {
     int chunks = ceil_div(N, 64);
-    col_partial_kernel<<<dim3(ceil_div(OC, 256), chunks), 256, 0, s>>>(dy, N, OC, OC, 64, w.bias_partial);
-    col_finish_kernel<<<ceil_div(OC, 256), 256, 0, s>>>(w.bias_partial, chunks, OC, dbias);
+    launch_k(col_partial_kernel, dim3(ceil_div(OC, 256), chunks), 256, 0, s, dy, N, OC, OC, 64, w.bias_partial);
+    launch_k(col_finish_kernel, ceil_div(OC, 256), 256, 0, s, w.bias_partial, chunks, OC, dbias);
     if (cudaGetLastError() != cudaSuccess) return GPT2_ERR_CUDA;
   }
   return op_status(w, s);
@@ -1318,6 +1385,41 @@ EXPORT int gpt2op_attention_forward(float* y, float* lse, const float* qkv, int 
   if (launch_attn_fwd(y, nullptr, lse, qkv, bf ? qkv_bf : nullptr, B, T, C, NH, bf, w.err, s) < 0) return GPT2_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return GPT2_ERR_CUDA;
   return op_status(w, s);
+}
+
+// attention backward: workspace = [error word][bf16 qkv][bf16 dy][y][lse][D]
+EXPORT size_t gpt2op_attention_backward_workspace_bytes(int B, int T, int C, int NH) {
+  if (B < 1 || T < 1 || C < 1 || NH < 1) return 0;
+  size_t n = (size_t)B * T;
+  return 256 + al256(n * 3 * C * 2) + al256(n * C * 2) + al256(n * C * 4) + 2 * al256(n * NH * 4);
+}
+
+EXPORT int gpt2op_attention_backward(float* dqkv, const float* dy, const float* qkv, int B, int T, int C, int NH,
+                                     int precision, void* workspace, void* stream) {
+  if (!dqkv || !dy || !qkv || !workspace || B < 1 || T < 1 || C < 1 || NH < 1) return GPT2_ERR_ARG;
+  if (precision != GPT2_PREC_FP32 && precision != GPT2_PREC_BF16) return GPT2_ERR_ARG;
+  if (C % NH || C / NH > 128 || C % 8) return GPT2_ERR_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (set_kernel_attributes() != GPT2_OK) return GPT2_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, 256, s) != cudaSuccess) return GPT2_ERR_CUDA;
+  size_t n = (size_t)B * T;
+  char* w = (char*)workspace;
+  OpWs ws = {};
+  ws.err = (int*)w;
+  uint16_t* qkv_bf = (uint16_t*)(w + 256);
+  uint16_t* dy_bf = (uint16_t*)((char*)qkv_bf + al256(n * 3 * C * 2));
+  float* y = (float*)((char*)dy_bf + al256(n * C * 2));
+  float* lse = (float*)((char*)y + al256(n * C * 4));
+  float* D = (float*)((char*)lse + al256(n * NH * 4));
+  const int bf = precision == GPT2_PREC_BF16;
+  if (bf && (op_to_bf16(qkv, qkv_bf, (long long)n * 3 * C, s) || op_to_bf16(dy, dy_bf, (long long)n * C, s)))
+    return GPT2_ERR_CUDA;
+  if (launch_attn_fwd(y, nullptr, lse, qkv, bf ? qkv_bf : nullptr, B, T, C, NH, bf, ws.err, s) < 0) return GPT2_ERR_CUDA;
+  if (launch_attn_bwd(dqkv, nullptr, D, dy, bf ? dy_bf : nullptr, qkv, bf ? qkv_bf : nullptr, y, lse, B, T, C, NH, bf,
+                      ws.err, s) < 0)
+    return GPT2_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return GPT2_ERR_CUDA;
+  return op_status(ws, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -32,6 +32,8 @@ GPT2_DEV void att_load_row(float (&dst)[ND], const float* row, int lane, int hs,
 template <int ND>
 __global__ void attn_fwd_simt_kernel(float* __restrict__ y, uint16_t* __restrict__ ybf, float* __restrict__ lse,
                                      const float* __restrict__ qkv, int B, int T, int C, int NH, int bf16_ops) {
+  pdl_launch_dependents();
+  pdl_wait();
   int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   int lane = threadIdx.x & 31;
   if (gw >= B * NH * T) return;
@@ -93,6 +95,8 @@ __global__ void attn_fwd_simt_kernel(float* __restrict__ y, uint16_t* __restrict
 // D[b,h,t] = sum_d dy[b,t,h,d] * y[b,t,h,d]
 __global__ void attn_bwd_D_kernel(float* __restrict__ D, const float* __restrict__ dy, const float* __restrict__ y,
                                   int B, int T, int C, int NH) {
+  pdl_launch_dependents();
+  pdl_wait();
   int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   int lane = threadIdx.x & 31;
   if (gw >= B * NH * T) return;
@@ -109,6 +113,8 @@ template <int ND>
 __global__ void attn_bwd_dq_kernel(float* __restrict__ dqkv, uint16_t* __restrict__ dqkv_bf, const float* __restrict__ qkv,
                                    const float* __restrict__ dy, const float* __restrict__ lse,
                                    const float* __restrict__ D, int B, int T, int C, int NH, int bf16_ops) {
+  pdl_launch_dependents();
+  pdl_wait();
   int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   int lane = threadIdx.x & 31;
   if (gw >= B * NH * T) return;
@@ -162,6 +168,8 @@ template <int ND>
 __global__ void attn_bwd_dkv_kernel(float* __restrict__ dqkv, uint16_t* __restrict__ dqkv_bf, const float* __restrict__ qkv,
                                     const float* __restrict__ dy, const float* __restrict__ lse,
                                     const float* __restrict__ D, int B, int T, int C, int NH, int bf16_ops) {
+  pdl_launch_dependents();
+  pdl_wait();
   int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   int lane = threadIdx.x & 31;
   if (gw >= B * NH * T) return;

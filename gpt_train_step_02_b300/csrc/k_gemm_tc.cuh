@@ -15,14 +15,15 @@
 // a*b ~ ah*bh + ah*bl + al*bh, three MMAs into one fp32 accumulator.  The
 // dropped al*bl term and the TF32 rounding of lo are ~2^-20 relative.
 //
-// CTA = one 128 x 128 output tile over a range of K, 6 warps.  When K is
+// CTA = one 128 x 128 output tile over a range of K, 10 warps.  When K is
 // split, the S splits of a tile form one thread-block cluster and are summed
 // through distributed shared memory (below).
 //   warp 0      one lane issues the TMA loads of raw fp32 tiles (raw ring)
 //   warp 1      allocates TMEM; one lane issues tcgen05.mma and commits
-//   warps 2..5  split each raw tile into hi/lo tiles laid out K-major with
+//   warps 2..9  split each raw tile into hi/lo tiles laid out K-major with
 //               the 128-byte swizzle (transposing MN-major tiles), then run
-//               the epilogue: tcgen05.ld TMEM -> registers -> global.
+//               the epilogue: tcgen05.ld TMEM -> registers -> global (two
+//               warps per TMEM lane quadrant, 64 columns each).
 // Every mbarrier wait is bounded; on expiry the CTA records DEV_ERR_TIMEOUT
 // in the error word, stops issuing work, frees its TMEM and returns.
 #pragma once
@@ -36,10 +37,12 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int BK = 32;  // fp32 elements = 128 bytes: one swizzle row
-constexpr int RAW_STAGES = 2;
+constexpr int RAW_STAGES = 3;
 constexpr int COMP_STAGES = 2;
 constexpr int TILE_BYTES = BM * BK * 4;  // 16 KB (A or B tile)
-constexpr int THREADS = 192;
+constexpr int SPLIT_WARPS = 8;           // splitter / epilogue warps (two per TMEM lane quadrant)
+constexpr int SPLIT_THREADS = 32 * SPLIT_WARPS;
+constexpr int THREADS = 64 + SPLIT_THREADS;
 constexpr int TMEM_COLS = 128;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s of wall time per wait before giving up
 
@@ -164,8 +167,8 @@ GPT2_DEV float4 ld_dsmem_f4(uint32_t addr) {
   return v;
 }
 
-// Barrier over the four splitter / epilogue warps only (threads 64..191).
-GPT2_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier over the splitter / epilogue warps only (threads 64 ..).
+GPT2_DEV void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(SPLIT_THREADS) : "memory"); }
 
 GPT2_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 GPT2_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -226,8 +229,8 @@ GPT2_DEV void split4(float4 x, float4& h, float4& l) {
 // raw tile already K-major SW128 (as TMA wrote it): split in place order.
 GPT2_DEV void split_kmajor(const float4* raw, float4* hi, float4* lo, int t) {
 #pragma unroll
-  for (int j = 0; j < (BM * BK / 4) / 128; j++) {
-    int q = t + 128 * j;
+  for (int j = 0; j < (BM * BK / 4) / SPLIT_THREADS; j++) {
+    int q = t + SPLIT_THREADS * j;
     float4 h, l;
     split4(raw[q], h, l);
     hi[q] = h;
@@ -235,16 +238,19 @@ GPT2_DEV void split_kmajor(const float4* raw, float4* hi, float4* lo, int t) {
   }
 }
 
-// raw tile MN-major, unswizzled [BK rows of k][128 of m]: thread t owns row
-// m = t and writes its 32 k-values as 8 swizzled 16-byte chunks.
+// raw tile MN-major, unswizzled [BK rows of k][128 of m]: the two threads
+// t and t + 128 own row m = t % 128 and write half of its 32 k-values each
+// as swizzled 16-byte chunks.
 GPT2_DEV void split_mnmajor(const float* raw, float* hi, float* lo, int t) {
+  const int m = t & (BM - 1), c0 = (t / BM) * (BK / 8);
 #pragma unroll
-  for (int c = 0; c < BK / 4; c++) {
-    float4 x = make_float4(raw[(4 * c + 0) * BM + t], raw[(4 * c + 1) * BM + t], raw[(4 * c + 2) * BM + t],
-                           raw[(4 * c + 3) * BM + t]);
+  for (int cc = 0; cc < BK / 8; cc++) {
+    const int c = c0 + cc;
+    float4 x = make_float4(raw[(4 * c + 0) * BM + m], raw[(4 * c + 1) * BM + m], raw[(4 * c + 2) * BM + m],
+                           raw[(4 * c + 3) * BM + m]);
     float4 h, l;
     split4(x, h, l);
-    int off = t * 32 + ((c ^ (t & 7)) << 2);
+    int off = m * 32 + ((c ^ (m & 7)) << 2);
     *reinterpret_cast<float4*>(hi + off) = h;
     *reinterpret_cast<float4*>(lo + off) = l;
   }
@@ -254,6 +260,7 @@ GPT2_DEV void split_mnmajor(const float* raw, float* hi, float* lo, int t) {
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ Params p) {
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -275,10 +282,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RAW_STAGES; s++) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 128);
+      mbar_init(&raw_empty[s], SPLIT_THREADS);
     }
     for (int s = 0; s < COMP_STAGES; s++) {
-      mbar_init(&comp_full[s], 128);
+      mbar_init(&comp_full[s], SPLIT_THREADS);
       mbar_init(&comp_empty[s], 1);
     }
     mbar_init(acc_full, 1);
@@ -296,6 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the first global-memory access comes after this
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -357,7 +365,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ---------------- splitters, then epilogue ----------------
-    const int t = threadIdx.x - 64;  // 0..127
+    const int t = threadIdx.x - 64;  // 0 .. SPLIT_THREADS-1
+    // The epilogue's global reads (C for the accumulating product, R for the
+    // residual and GELU-derivative products) are only needed after the main
+    // loop: start pulling this thread's output row into L2 now.
+    if (p.splits == 1 && t < BM && m0 + t < p.M) {
+      const float* src = p.epi.epi == EPI_ACCUM ? p.epi.C + (size_t)(m0 + t) * p.epi.ldc
+                         : (p.epi.epi == EPI_BIAS_RESID || p.epi.epi == EPI_DGELU) ? p.epi.R + (size_t)(m0 + t) * p.epi.ldr
+                                                                                   : nullptr;
+      if (src) {
+#pragma unroll
+        for (int c = 0; c < BN * 4 / 128; c++)
+          if (n0 + c * 32 < p.N) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + n0 + c * 32));
+      }
+    }
     bool ok = true;
     for (int i = 0; i < nk; i++) {
       int s = i % RAW_STAGES, c = i % COMP_STAGES;
@@ -389,8 +410,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(&comp_full[c]);
     }
     if (ok && nk > 0) ok = mbar_wait(acc_full, 0, abort_flag, p.err);
-    // One decision for all four epilogue warps (tcgen05.ld is warp-collective
-    // and the split-K hand-off below uses a barrier over these 128 threads).
+    // One decision for all epilogue warps (tcgen05.ld is warp-collective and
+    // the split-K hand-off below uses a barrier over these threads).
     // Every epilogue thread reaches this barrier: all of its waits are bounded.
     epi_bar();
     if (t == 0) *go_flag = (nk > 0 && !*abort_flag) ? 1 : 0;
@@ -400,9 +421,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int q = warp & 3;  // TMEM lane quadrant this warp may access
       const int row = q * 32 + lane;
       const int i = m0 + row;
+      const int half = (warp - 2) >> 2;  // which half of the 128 columns this warp finishes
       float* stage = reinterpret_cast<float*>(smem + OFF_STAGE);
 #pragma unroll 1
-      for (int cc = 0; cc < BN / 32; cc++) {
+      for (int cc = half * (BN / 64); cc < (half + 1) * (BN / 64); cc++) {
         float v[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cc * 32), v);
         if (p.splits > 1) {
@@ -435,7 +457,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int c4 = t & 31;  // float4 column group of the 128-wide tile
       const int j = n0 + 4 * c4;
       const uint32_t stage = smem_u32(smem + OFF_STAGE);
-      for (int r = r0 + (t >> 5); r < r1; r += 4) {
+      for (int r = r0 + (t >> 5); r < r1; r += SPLIT_WARPS) {
         const int ii = m0 + r;
         if (ii >= p.M || j >= p.N) continue;
         const uint32_t off = stage + (uint32_t)(r * STAGE_PITCH + 4 * c4) * 4u;

@@ -16,6 +16,8 @@
 __global__ void layernorm_fwd_kernel(float* __restrict__ y, uint16_t* __restrict__ ybf, float* __restrict__ mean,
                                      float* __restrict__ rstd, const float* __restrict__ x,
                                      const float* __restrict__ w, const float* __restrict__ b, int N, int C) {
+  pdl_launch_dependents();
+  pdl_wait();
   int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   int lane = threadIdx.x & 31;
   if (warp >= N) return;
@@ -81,6 +83,8 @@ __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
     float* __restrict__ dx, uint16_t* __restrict__ dxbf, float* __restrict__ partial, const float* __restrict__ dy,
     const float* __restrict__ x, const float* __restrict__ w, const float* __restrict__ mean,
     const float* __restrict__ rstd, int N, int C, int rows) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ float sh[];  // [2C]
   int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float4 aw[LN_MAXV4], ab[LN_MAXV4];
@@ -158,6 +162,8 @@ __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
 // dw[c] += sum_k partial[k][c], db[c] += sum_k partial[k][C + c].
 __global__ void layernorm_param_grad_kernel(float* __restrict__ dw, float* __restrict__ db,
                                             const float* __restrict__ partial, int nblocks, int C) {
+  pdl_launch_dependents();
+  pdl_wait();
   int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= C) return;
   float sw = 0.f, sb = 0.f;

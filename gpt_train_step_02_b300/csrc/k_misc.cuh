@@ -32,6 +32,8 @@ GPT2_DEV double normal_at(uint64_t seed, uint64_t i) {
 // elements [0, nrand) get std * normal(base + i), the rest `fill`.
 __global__ void init_tensor_kernel(float* p, long long base, long long n, long long nrand, double stdv, float fill,
                                    uint64_t seed) {
+  pdl_launch_dependents();
+  pdl_wait();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
     p[i] = i < nrand ? (float)(stdv * normal_at(seed, (uint64_t)(base + i))) : fill;
 }
@@ -40,6 +42,8 @@ __global__ void init_tensor_kernel(float* p, long long base, long long n, long l
 // Token ids must lie in [0, V).
 // ---------------------------------------------------------------------------
 __global__ void validate_tokens_kernel(const int* ids, const int* tgt, int n, int V, int* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     int a = ids[i];
     int b = tgt ? tgt[i] : 0;
@@ -54,6 +58,8 @@ __global__ void validate_tokens_kernel(const int* ids, const int* tgt, int n, in
 // ---------------------------------------------------------------------------
 __global__ void encoder_fwd_kernel(float* __restrict__ x, const int* __restrict__ ids, const float* __restrict__ wte,
                                    const float* __restrict__ wpe, int BT, int T, int C, int V) {
+  pdl_launch_dependents();
+  pdl_wait();
   int C4 = C >> 2;
   long long total = (long long)BT * C4;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
@@ -79,6 +85,8 @@ __global__ void encoder_fwd_kernel(float* __restrict__ x, const int* __restrict_
 
 __global__ void __launch_bounds__(1024) sort_tokens_kernel(const int* __restrict__ ids, int n, int V,
                                                           uint32_t* __restrict__ sorted) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ uint32_t keys[];
   int P = 1;
   while (P < n) P <<= 1;
@@ -109,6 +117,8 @@ __global__ void __launch_bounds__(1024) sort_tokens_kernel(const int* __restrict
 // grid: (n, ceil(C/128)); block: 32 threads, one float4 of channels each.
 __global__ void wte_grad_kernel(float* __restrict__ dwte, const float* __restrict__ dx,
                                 const uint32_t* __restrict__ sorted, int n, int C) {
+  pdl_launch_dependents();
+  pdl_wait();
   int i = blockIdx.x;
   uint32_t id = sorted[i] >> 14;
   if (i > 0 && (sorted[i - 1] >> 14) == id) return;
@@ -126,6 +136,8 @@ __global__ void wte_grad_kernel(float* __restrict__ dwte, const float* __restric
 }
 
 __global__ void wpe_grad_kernel(float* __restrict__ dwpe, const float* __restrict__ dx, int B, int T, int C) {
+  pdl_launch_dependents();
+  pdl_wait();
   int C4 = C >> 2;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T * C4; i += gridDim.x * blockDim.x) {
     int t = i / C4, c4 = i % C4;
@@ -147,6 +159,8 @@ __global__ void wpe_grad_kernel(float* __restrict__ dwpe, const float* __restric
 // ---------------------------------------------------------------------------
 __global__ void col_partial_kernel(const float* __restrict__ Y, int M, int N, long long ldy, int rows,
                                    float* __restrict__ partial) {
+  pdl_launch_dependents();
+  pdl_wait();
   int col = blockIdx.x * blockDim.x + threadIdx.x;
   if (col >= N) return;
   int r0 = blockIdx.y * rows, r1 = min(M, r0 + rows);
@@ -157,6 +171,8 @@ __global__ void col_partial_kernel(const float* __restrict__ Y, int M, int N, lo
 }
 
 __global__ void col_finish_kernel(const float* __restrict__ partial, int nchunks, int N, float* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   int col = blockIdx.x * blockDim.x + threadIdx.x;
   if (col >= N) return;
   float s = 0.f;
@@ -166,6 +182,8 @@ __global__ void col_finish_kernel(const float* __restrict__ partial, int nchunks
 
 // Mean of n values in a fixed order (one CTA of 1024 threads).
 __global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ x, int n, float* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ float sh[32];
   float s = 0.f;
   for (int i = threadIdx.x; i < n; i += blockDim.x) s += x[i];
@@ -187,6 +205,8 @@ __global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ x,
 __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
                              float* __restrict__ v, long long n4, const float* __restrict__ hp,
                              uint16_t* __restrict__ pbf16) {
+  pdl_launch_dependents();
+  pdl_wait();
   const float lr = hp[0], b1 = hp[1], b2 = hp[2], eps = hp[3], wd = hp[4], c1inv = hp[5], c2inv = hp[6];
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
     float4 pp = reinterpret_cast<float4*>(p)[i];
@@ -219,6 +239,8 @@ __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g,
 }
 
 __global__ void to_bf16_kernel(const float* __restrict__ x, uint16_t* __restrict__ y, long long n) {
+  pdl_launch_dependents();
+  pdl_wait();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
     y[i] = to_bf16_bits(x[i]);
 }

@@ -5,7 +5,8 @@
 // float4 slice of the V real columns; the CTA combines the pairs in a fixed
 // tree.  loss = log(sum) + max - logit[target].
 // Pass 2: dlogits[v] = (exp(logit[v] - max) / sum - [v == target]) * dloss
-// for v < V and 0 for the padded columns [V, Vp).  Vp % 4 == 0.
+// for v < V and 0 for the padded columns [V, Vp), stored in fp32 (dlogits,
+// may be NULL) and/or bf16 (dlogits_bf, may be NULL).  Vp % 4 == 0.
 #pragma once
 #include "common.cuh"
 
@@ -21,6 +22,8 @@ GPT2_DEV void online_merge(float& m, float& s, float m2, float s2) {
 __global__ void __launch_bounds__(XENT_THREADS) xent_fused_kernel(
     float* __restrict__ dlogits, uint16_t* __restrict__ dlogits_bf, float* __restrict__ losses,
     const float* __restrict__ logits, const int* __restrict__ targets, int V, int Vp, float dloss) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ float shm[XENT_THREADS / 32], shs[XENT_THREADS / 32];
   int row = blockIdx.x;
   const float* lr = logits + (size_t)row * Vp;
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(XENT_THREADS) xent_fused_kernel(
       int v = i * 4 + k;
       xv[k] = v < V ? (__expf(xv[k] - m) * inv - (v == tgt ? 1.f : 0.f)) * dloss : 0.f;
     }
-    reinterpret_cast<float4*>(dr)[i] = x;
+    if (dlogits) reinterpret_cast<float4*>(dr)[i] = x;
     if (dlogits_bf) {
       ushort4 hb;
       hb.x = to_bf16_bits(x.x);

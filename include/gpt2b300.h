@@ -212,6 +212,21 @@ size_t gpt2op_attention_workspace_bytes(int B, int T, int C);
 int gpt2op_attention_forward(float* y, float* lse, const float* qkv, int B, int T, int C, int NH, int precision,
                              void* workspace, void* stream);
 
+/* The per-layer causal attention backward of the page's item 1
+ * (attention_backward): dqkv (B, T, 3C) = the gradient of the loss through
+ * y = attention(qkv) for the upstream gradient dy (B, T, C), in the layout of
+ * qkv.  The call first runs the attention forward (for y and the row
+ * log-sum-exp), then D = rowsum(dy o y), P recomputed from the log-sum-exp,
+ * dS = P o (dy v^T - D), dq = dS k / sqrt(hs), dk = dS^T q / sqrt(hs),
+ * dv = P^T dy.  precision and requirements as gpt2op_attention_forward (bf16:
+ * qkv and dy rounded to bf16; with hs = 64 and T % 128 == 0 the tensor-core
+ * kernels, one CTA per output row tile, no atomics).  dqkv is overwritten.
+ * workspace: gpt2op_attention_backward_workspace_bytes(B, T, C, NH) device
+ * bytes.  Synchronises the stream. */
+size_t gpt2op_attention_backward_workspace_bytes(int B, int T, int C, int NH);
+int gpt2op_attention_backward(float* dqkv, const float* dy, const float* qkv, int B, int T, int C, int NH,
+                              int precision, void* workspace, void* stream);
+
 /* gpt2op_matmul_backward without a workspace argument: the same products
  * (dx = dy W; dW += dy^T x; dbias += column sums of dy, dbias may be NULL)
  * with the same arguments minus `workspace`.  The pages have no counterpart:

@@ -88,3 +88,55 @@ def test_attention_forward_bf16_other_head_size():
     ry, preatt, _ = OPS.attention_forward(bf16(qkv), NH)
     assert np.abs(y - ry).max() <= 1e-2 * np.abs(ry).max()
     assert np.abs(lse - oracle_lse(preatt)).max() <= 1e-3
+
+
+def run_gpu_backward(qkv, dy, NH, precision):
+    import torch
+    import gpt_train_step_02_b300 as g
+
+    dqkv = torch.full(qkv.shape, float("nan"), device="cuda")
+    g.attention_backward(dqkv, torch.tensor(dy, device="cuda"), torch.tensor(qkv, device="cuda"), NH,
+                         precision=precision)
+    return dqkv.cpu().numpy()
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return np.linalg.norm(a - b) / np.linalg.norm(b)
+
+
+@pytest.mark.parametrize("B,T,C,NH", [(2, 32, 64, 4), (1, 13, 64, 4), (2, 64, 768, 12)])
+def test_attention_backward_fp32(B, T, C, NH):
+    import gpt_train_step_02_b300 as g
+
+    qkv = synth.randn(311, (B, T, 3 * C))
+    dy = synth.randn(312, (B, T, C))
+    got = run_gpu_backward(qkv, dy, NH, g.GPT2_PREC_FP32)
+    _, _, att = OPS.attention_forward(qkv, NH)
+    ref_d = OPS.attention_backward(dy, qkv, att, NH)
+    assert np.abs(got - ref_d).max() <= 1e-4 * np.abs(ref_d).max()
+
+
+@pytest.mark.parametrize("B,T,C,NH", [(2, 128, 128, 2), (1, 384, 64, 1), (1, 1024, 768, 12)])
+def test_attention_backward_bf16_tensor_cores(B, T, C, NH):
+    """Tensor-core dK/dV and dQ kernels against the oracle fed the same
+    bf16-rounded qkv and dy.  P and dS are rounded to bf16 for the products
+    (relative 2^-9 each), so the bar is 1e-2 relative L2 per q, k, v block and
+    3e-2 of the largest gradient entrywise."""
+    import gpt_train_step_02_b300 as g
+
+    qkv = synth.randn(313, (B, T, 3 * C))
+    dy = synth.randn(314, (B, T, C))
+    got = run_gpu_backward(qkv, dy, NH, g.GPT2_PREC_BF16)
+    q, d = bf16(qkv), bf16(dy)
+    _, _, att = OPS.attention_forward(q, NH)
+    ref_d = OPS.attention_backward(d, q, att, NH)
+    assert np.isfinite(got).all()
+    for part in range(3):  # dq, dk, dv
+        gp, rp = got[..., part * C:(part + 1) * C], ref_d[..., part * C:(part + 1) * C]
+        assert rel_l2(gp, rp) <= 1e-2, (part, rel_l2(gp, rp))
+        assert np.abs(gp - rp).max() <= 3e-2 * np.abs(rp).max(), part
+    # the last key of each sequence is seen only by the last query
+    last_k = ref_d[:, -1, C:2 * C]
+    np.testing.assert_allclose(got[:, -1, C:2 * C], last_k, atol=3e-2 * np.abs(ref_d[..., C:2 * C]).max())

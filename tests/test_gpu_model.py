@@ -257,6 +257,24 @@ def test_bf16_operands_tiny():
     m.close()
 
 
+def test_bf16_tensor_core_attention_small():
+    """bf16 workload whose attention takes the tensor-core kernels (head
+    size 64, T a multiple of 128): the 10-step fixed-batch trajectory stays
+    within 2% per step of the fp32 oracle, as the bf16 bar requires."""
+    w = synth.Workload("small_bf16_hs64", 2, 128, 2, 512, 512, 256, 2, 256, "bf16", "uniform", 10)
+    p0 = synth.init_params(w)
+    inp, tgt = synth.batch(w)
+    m = gpu_model(w)
+    m.set_params(p0)
+    o = oracle_model(w, p0)
+    lg = [m.step(inp, tgt, t) for t in range(1, 11)]
+    lo = [o.step(inp, tgt, t) for t in range(1, 11)]
+    assert abs(lg[0] - lo[0]) <= 2e-2
+    np.testing.assert_allclose(lg, lo, rtol=0.02)
+    assert all(b < a for a, b in zip(lg, lg[1:]))
+    m.close()
+
+
 # ---------------------------------------------------------------------------
 # GPT-2 124M, fp32, B=4, T=64 (the workload of the pages' console log)
 # ---------------------------------------------------------------------------
