@@ -315,6 +315,39 @@ def run_ours(args, w):
     return 0
 
 
+# Sources of each kernel class: DRAM traffic recorded by ncu stays valid only
+# while these files are unchanged.
+KERNEL_SOURCES = {
+    "gemm": ["gemm_common.cuh", "k_gemm_tc.cuh", "k_gemm_bf16.cuh", "common.cuh"],
+    "adamw": ["k_misc.cuh", "common.cuh"],
+    "xent": ["k_xent.cuh", "common.cuh"],
+    "layernorm": ["k_layernorm.cuh", "k_misc.cuh", "common.cuh"],
+}
+
+
+def kernel_source_sha(kind):
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kind, []):
+        with open(os.path.join(ROOT, "gpt_train_step_02_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kind, w):
+    """DRAM bytes per launch of this kernel class from the committed ncu
+    capture (profiles/roofline_traffic.json), or None when there is none or
+    the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(w.name, {}).get(kind)
+    if not rec or rec.get("source_sha") != kernel_source_sha(kind):
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 def roofline_for(kind, k, peaks, w):
     if kind == "gemm":
         achieved = k["work_per_launch"] / (k["avg_launch_ms"] * 1e-3) / 1e12
@@ -328,10 +361,11 @@ def roofline_for(kind, k, peaks, w):
             peak = peaks["bf16_tflops"]
             src = f"{peaks['source']} bf16 dense burst"
         return {"kernel": "matmul (all tcgen05 launches of the step)", "bound": "tensor", "achieved": achieved,
-                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None, "peak_source": src}
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(kind, w),
+                "peak_source": src}
     achieved = k["work_per_launch"] / (k["avg_launch_ms"] * 1e-3) / 1e9
     return {"kernel": kind, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peaks["source"]}
+            "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(kind, w), "peak_source": peaks["source"]}
 
 
 def main():

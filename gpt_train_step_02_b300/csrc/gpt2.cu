@@ -42,7 +42,7 @@
 // op workspaces start with [error word, 256 B][tile counters, 1 KB]
 #define OP_HDR_BYTES 1280
 // smallest row chunk of the bias-gradient column sums
-#define BIAS_MIN_ROWS 16
+#define BIAS_MIN_ROWS 32
 
 enum {
   P_WTE, P_WPE, P_LN1W, P_LN1B, P_QKVW, P_QKVB, P_ATTPROJW, P_ATTPROJB,
@@ -82,7 +82,7 @@ static int config_ok(const gpt2_config* c) {
   if (c->channels % 64 || c->channels % c->num_heads) return 0;
   int hs = c->channels / c->num_heads;
   if (hs != 16 && hs != 32 && hs != 64 && hs != 128) return 0;
-  if (c->channels > 32 * 4 * LN_MAXV4) return 0;
+  if (c->channels > 32 * 4 * LN_MAXV4_LIMIT) return 0;
   if (c->vocab_size < 1 || c->vocab_size > c->padded_vocab_size || c->padded_vocab_size % 64) return 0;
   if (c->padded_vocab_size > 65536) return 0;
   if (c->gemm_precision != GPT2_PREC_FP32 && c->gemm_precision != GPT2_PREC_BF16) return 0;
@@ -191,6 +191,10 @@ struct gpt2_t {
       *datty_bf;
   float* hparams;
   int B, T, have_targets, fwd_done;
+  // 1: the backward adds into the gradients (gpt2_backward); 0: it stores
+  // them (the fused training step, whose gradients would otherwise be zeroed
+  // first -- every gradient element is written exactly once there)
+  int grad_accumulate;
   int poisoned;
   long long launches;
   // graph replay of whole steps
@@ -505,30 +509,36 @@ static void mm_dx(gpt2_t* m, float* dx, uint16_t* dxbf, Opnd dy, Opnd W, int N, 
   matmul(m, d);
 }
 
-// dW += dy^T x
+// dW += dy^T x  (dW = dy^T x in the fused step, whose gradients start from zero)
 static void mm_dw(gpt2_t* m, float* dW, Opnd dy, Opnd x, int N, int IC, int OC) {
-  MatmulDesc d = {OC, IC, N, dy.f, OC, 0, x.f, IC, 0, epi_args(dW, IC, EPI_ACCUM), dy.h, x.h};
+  MatmulDesc d = {OC, IC, N, dy.f, OC, 0, x.f, IC, 0, epi_args(dW, IC, m->grad_accumulate ? EPI_ACCUM : EPI_STORE),
+                  dy.h, x.h};
   matmul(m, d);
 }
 
-// db += column sums of dy (N, OC): row chunks of at least BIAS_MIN_ROWS rows,
-// as many as fill about two CTAs per SM, reduced in chunk order.
+// db += column sums of dy (N, OC): chunks of BIAS_MIN_ROWS rows summed by
+// one thread per column, then the chunk partials finished in a fixed order.
 static void bias_grad(gpt2_t* m, float* db, const float* dy, int N, int OC) {
-  int colb = ceil_div(OC, 256);
-  int want = ceil_div(2 * 148, colb);
-  int rows = ceil_div(N, want);
-  if (rows < BIAS_MIN_ROWS) rows = BIAS_MIN_ROWS;
-  int chunks = ceil_div(N, rows);
-  launch_k(col_partial_kernel, dim3(colb, chunks), 256, 0, m->stream, dy, N, OC, OC, rows, m->scratch);
-  launch_k(col_finish_kernel, colb, 256, 0, m->stream, m->scratch, chunks, OC, db);
+  const int rows = BIAS_MIN_ROWS, chunks = ceil_div(N, rows);
+  launch_k(col_partial_kernel, dim3(ceil_div(OC, 256), chunks), 256, 0, m->stream, dy, N, OC, OC, rows, m->scratch);
+  launch_k(col_finish_kernel, ceil_div(OC, 32), 256, 0, m->stream, db, db, OC, m->scratch, chunks, OC,
+           m->grad_accumulate);
   m->launches += 2;
+}
+
+template <typename K>
+static K ln_pick(int C, K k1, K k2, K k4, K k6, K k8, K k10) {
+  const int v = ceil_div(C, 128);
+  return v <= 1 ? k1 : v <= 2 ? k2 : v <= 4 ? k4 : v <= 6 ? k6 : v <= 8 ? k8 : k10;
 }
 
 static void ln_forward(gpt2_t* m, float* y, uint16_t* ybf, float* mean, float* rstd, const float* x, const float* w,
                        const float* b, int N) {
   int C = m->cfg.channels;
   timer_begin(m, TK_LAYERNORM, (8.0 * C + 8.0) * N);
-  launch_k(layernorm_fwd_kernel, ceil_div(N, 8), 256, 0, m->stream, y, ybf, mean, rstd, x, w, b, N, C);
+  auto k = ln_pick(C, layernorm_fwd_kernel<1>, layernorm_fwd_kernel<2>, layernorm_fwd_kernel<4>,
+                   layernorm_fwd_kernel<6>, layernorm_fwd_kernel<8>, layernorm_fwd_kernel<10>);
+  launch_k(k, ceil_div(N, 8), 256, 0, m->stream, y, ybf, mean, rstd, x, w, b, N, C);
   timer_end(m, TK_LAYERNORM);
   m->launches++;
 }
@@ -536,20 +546,22 @@ static void ln_forward(gpt2_t* m, float* y, uint16_t* ybf, float* mean, float* r
 static void ln_backward(gpt2_t* m, float* dx, uint16_t* dxbf, float* dw, float* db, const float* dy, const float* x,
                         const float* w, const float* mean, const float* rstd, int N) {
   int C = m->cfg.channels;
-  // rows per block: a multiple of the warp count, enough blocks for two per SM
-  int rows = ceil_div(ceil_div(N, 2 * 148), LNB_WARPS) * LNB_WARPS;
+  // rows per block: a multiple of the warp count, about two blocks per SM's worth of warps
+  int rows = ceil_div(ceil_div(N, 8 * 148), LNB_WARPS) * LNB_WARPS;
   if (rows < LNB_MIN_ROWS) rows = LNB_MIN_ROWS;
   int nb = ceil_div(N, rows);
   timer_begin(m, TK_LAYERNORM, (16.0 * C + 8.0) * N);
-  launch_k(layernorm_bwd_kernel, nb, LNB_WARPS * 32, 2 * C * sizeof(float), m->stream, dx, dxbf, m->scratch, dy, x, w,
-                                                                                    mean, rstd, N, C, rows);
-  launch_k(layernorm_param_grad_kernel, ceil_div(C, 256), 256, 0, m->stream, dw, db, m->scratch, nb, C);
+  auto k = ln_pick(C, layernorm_bwd_kernel<1>, layernorm_bwd_kernel<2>, layernorm_bwd_kernel<4>,
+                   layernorm_bwd_kernel<6>, layernorm_bwd_kernel<8>, layernorm_bwd_kernel<10>);
+  launch_k(k, nb, LNB_WARPS * 32, 2 * C * sizeof(float), m->stream, dx, dxbf, m->scratch, dy, x, w, mean, rstd, N, C,
+           rows);
+  // dw[c] += sum_b partial[b][c], db[c] += sum_b partial[b][C + c]
+  launch_k(col_finish_kernel, ceil_div(2 * C, 32), 256, 0, m->stream, dw, db, C, m->scratch, nb, 2 * C,
+           m->grad_accumulate);
   timer_end(m, TK_LAYERNORM);
   m->launches += 2;
 }
 
-// causal attention on CUDA cores; the template argument is the number of head
-// dimensions each lane holds (hs <= 32 * ND)
 // Causal attention forward: the tensor-core kernel for bf16 operands with
 // head size 64 and T % 128 == 0, else the CUDA-core kernel (the template
 // argument is the number of head dimensions each lane holds, hs <= 32 * ND).
@@ -567,10 +579,11 @@ static int launch_attn_fwd(float* atty, uint16_t* attybf, float* lse, const floa
     launch_k(tca::attn_fwd_tc_kernel, dim3(T / tca::BQ, NH, B), tca::THREADS, tca::fwd::SMEM_BYTES, s, tm, p);
     return 1;
   }
-  int grid = ceil_div((long long)B * NH * T * 32, 256);
-  if (hs <= 32) launch_k(attn_fwd_simt_kernel<1>, grid, 256, 0, s, atty, attybf, lse, qkv, B, T, C, NH, bf);
-  else if (hs <= 64) launch_k(attn_fwd_simt_kernel<2>, grid, 256, 0, s, atty, attybf, lse, qkv, B, T, C, NH, bf);
-  else launch_k(attn_fwd_simt_kernel<4>, grid, 256, 0, s, atty, attybf, lse, qkv, B, T, C, NH, bf);
+  const dim3 g(ceil_div(T, ATT_ROWS), NH, B);
+  const size_t sm = att_smem_fwd(hs);
+  if (hs <= 32) launch_k(attn_fwd_simt_kernel<1>, g, ATT_ROWS * 32, sm, s, atty, attybf, lse, qkv, B, T, C, NH, bf);
+  else if (hs <= 64) launch_k(attn_fwd_simt_kernel<2>, g, ATT_ROWS * 32, sm, s, atty, attybf, lse, qkv, B, T, C, NH, bf);
+  else launch_k(attn_fwd_simt_kernel<4>, g, ATT_ROWS * 32, sm, s, atty, attybf, lse, qkv, B, T, C, NH, bf);
   return 1;
 }
 
@@ -609,15 +622,17 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
     launch_k(tca::attn_bwd_dq_tc_kernel, g, tca::THREADS, tca::dqk::SMEM_BYTES, s, tq, td, p);
     return 3;
   }
+  const dim3 g(ceil_div(T, ATT_ROWS), NH, B);
+  const size_t sq = att_smem_fwd(hs), skv = att_smem_dkv(hs);
   if (hs <= 32) {
-    launch_k(attn_bwd_dq_kernel<1>, grid, 256, 0, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
-    launch_k(attn_bwd_dkv_kernel<1>, grid, 256, 0, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
+    launch_k(attn_bwd_dq_kernel<1>, g, ATT_ROWS * 32, sq, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
+    launch_k(attn_bwd_dkv_kernel<1>, g, ATT_ROWS * 32, skv, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
   } else if (hs <= 64) {
-    launch_k(attn_bwd_dq_kernel<2>, grid, 256, 0, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
-    launch_k(attn_bwd_dkv_kernel<2>, grid, 256, 0, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
+    launch_k(attn_bwd_dq_kernel<2>, g, ATT_ROWS * 32, sq, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
+    launch_k(attn_bwd_dkv_kernel<2>, g, ATT_ROWS * 32, skv, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
   } else {
-    launch_k(attn_bwd_dq_kernel<4>, grid, 256, 0, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
-    launch_k(attn_bwd_dkv_kernel<4>, grid, 256, 0, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
+    launch_k(attn_bwd_dq_kernel<4>, g, ATT_ROWS * 32, sq, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
+    launch_k(attn_bwd_dkv_kernel<4>, g, ATT_ROWS * 32, skv, s, dqkv, dqkv_bf, qkv, dy, lse, D, B, T, C, NH, bf);
   }
   return 3;
 }
@@ -661,6 +676,17 @@ static int set_kernel_attributes() {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tca::attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                tca::dqk::SMEM_BYTES);
+    // CUDA-core attention: up to head size 128
+    const int f = (int)att_smem_fwd(128), kv = (int)att_smem_dkv(128);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_fwd_simt_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, f);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_fwd_simt_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, f);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_fwd_simt_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, f);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_bwd_dq_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, f);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_bwd_dq_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, f);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_bwd_dq_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, f);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_bwd_dkv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_bwd_dkv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_bwd_dkv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv);
     if (e != cudaSuccess) {
       fprintf(stderr, "gpt2b300: cudaFuncSetAttribute failed: %s\n", cudaGetErrorString(e));
       cudaGetLastError();
@@ -819,7 +845,8 @@ static int enqueue_backward(gpt2_t* m) {
   while ((int)smem < N) smem <<= 1;
   launch_k(sort_tokens_kernel, 1, 1024, smem * sizeof(uint32_t), s, m->tokens, N, c.vocab_size, m->sorted);
   launch_k(wte_grad_kernel, dim3(N, ceil_div(C, 128)), 32, 0, s, G[P_WTE], m->dres, m->sorted, N, C);
-  launch_k(wpe_grad_kernel, grid_for((long long)T * C / 4, 256), 256, 0, s, G[P_WPE], m->dres, B, T, C);
+  launch_k(wpe_grad_kernel, grid_for((long long)T * C / 4, 256), 256, 0, s, G[P_WPE], m->dres, B, T, C,
+           m->grad_accumulate);
   m->launches += 3;
   KCHECK(m);
   return GPT2_OK;
@@ -933,6 +960,7 @@ EXPORT int gpt2_build(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, int m
   if (!shape_ok(cfg, maxB, maxT)) return GPT2_ERR_SHAPE;
   gpt2_t* m = (gpt2_t*)calloc(1, sizeof(gpt2_t));
   if (!m) return GPT2_ERR_ARG;
+  m->grad_accumulate = 1;
   m->cfg = *cfg;
   m->maxB = maxB;
   m->maxT = maxT;
@@ -1089,11 +1117,22 @@ EXPORT int gpt2_update(gpt2_t* m, float lr, float beta1, float beta2, float eps,
 
 // forward (device-side token check) -> zero_grad -> backward -> AdamW, all
 // reading the staged tokens and the device-resident hyper-parameters.
+// forward -> zero_grad -> backward -> update.  zero_grad followed by an
+// accumulating backward equals a backward that stores its gradients, so the
+// fused step skips the 4*Np-byte clear: every gradient is stored exactly once
+// (the LM-head weight gradient first, then the embedding rows added on top),
+// except the wpe rows at positions >= T, which are cleared.
 static int enqueue_step(gpt2_t* m, int B, int T) {
   int rc;
   if ((rc = enqueue_forward(m, m->tokens, m->targets, B, T, 1))) return rc;
-  CCHECK(m, cudaMemsetAsync(m->grads, 0, m->np * sizeof(float), m->stream));
-  if ((rc = enqueue_backward(m))) return rc;
+  const int C = m->cfg.channels;
+  if (m->cfg.max_seq_len > T)
+    CCHECK(m, cudaMemsetAsync(m->G[P_WPE] + (size_t)T * C, 0, (size_t)(m->cfg.max_seq_len - T) * C * sizeof(float),
+                              m->stream));
+  m->grad_accumulate = 0;
+  rc = enqueue_backward(m);
+  m->grad_accumulate = 1;
+  if (rc) return rc;
   return enqueue_update(m);
 }
 
@@ -1347,7 +1386,7 @@ static int op_backward(float* dx, float* dW, float* dbias, const float* dy, cons
   if (dbias) {
     int chunks = ceil_div(N, 64);
     launch_k(col_partial_kernel, dim3(ceil_div(OC, 256), chunks), 256, 0, s, dy, N, OC, OC, 64, w.bias_partial);
-    launch_k(col_finish_kernel, ceil_div(OC, 256), 256, 0, s, w.bias_partial, chunks, OC, dbias);
+    launch_k(col_finish_kernel, ceil_div(OC, 32), 256, 0, s, dbias, dbias, OC, w.bias_partial, chunks, OC, 1);
     if (cudaGetLastError() != cudaSuccess) return GPT2_ERR_CUDA;
   }
   return op_status(w, s);

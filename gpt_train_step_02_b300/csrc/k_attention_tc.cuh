@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     bool ok = true;
     uint8_t* prow = smem + OFF_P + r * 128;
     for (int j = 0; j < nkt; j++) {
-      if (!mbar_wait(s_full, j & 1, abort_flag, p.err)) {
+      if (!tc::epi_bar_and<128>(mbar_wait(s_full, j & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive(p_full);
-      if (!mbar_wait(pv_full, j & 1, abort_flag, p.err)) {
+      if (!tc::epi_bar_and<128>(mbar_wait(pv_full, j & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         for (int d = 0; d < 32; d++) o[hh * 32 + d] = o[hh * 32 + d] * corr + pv[d];
       }
     }
-    if (ok && !*abort_flag) {
+    if (tc::epi_bar_and<128>(ok && !*abort_flag)) {
       const float inv = 1.f / lrow;
       const size_t yo = (size_t)(row0 + r) * p.C + h * HS;
 #pragma unroll
@@ -479,11 +479,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < niter; i++) {
       const int qt = kt + i;
       // lse (pre-multiplied by log2 e) and D of this query tile, shared by the 128 rows
-      tc::epi_bar();
+      tc::epi_bar<128>();
       lse_s[t] = p.lse[bh + qt * BQ + t] * l2e;
       D_s[t] = p.D[bh + qt * BQ + t];
-      tc::epi_bar();
-      if (!mbar_wait(s_full, i & 1, abort_flag, p.err)) {
+      tc::epi_bar<128>();
+      if (!tc::epi_bar_and<128>(mbar_wait(s_full, i & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
@@ -516,7 +516,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(st_ready);
     }
     if (ok) ok = mbar_wait(mma_done, 0, abort_flag, p.err);
-    if (ok && !*abort_flag) {
+    // one decision for all 128 threads: the TMEM loads below are warp-collective
+    if (tc::epi_bar_and<128>(ok && !*abort_flag)) {
       tc_fence_after();
       float dv[64], dk[64];
       tmem_ld32(T_DV + lane_off, dv);
@@ -676,7 +677,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float L2 = p.lse[bh + t] * l2e, Dt = p.D[bh + t];
     bool ok = true;
     for (int j = 0; j < niter; j++) {
-      if (!mbar_wait(s_full, j & 1, abort_flag, p.err)) {
+      if (!tc::epi_bar_and<128>(mbar_wait(s_full, j & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
@@ -707,7 +708,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(ds_ready);
     }
     if (ok) ok = mbar_wait(mma_done, 0, abort_flag, p.err);
-    if (ok && !*abort_flag) {
+    // one decision for all 128 threads: the TMEM loads below are warp-collective
+    if (tc::epi_bar_and<128>(ok && !*abort_flag)) {
       tc_fence_after();
       float dq[64];
       tmem_ld32(T_DQ + lane_off, dq);

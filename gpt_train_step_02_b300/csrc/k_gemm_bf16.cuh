@@ -59,7 +59,8 @@ using tc::tmem_ld32;
 constexpr int BM = 128;
 constexpr int BK = 64;  // bf16 elements per K tile: 128 bytes, one swizzle row
 constexpr int UMMA_K = 16;
-constexpr int THREADS = 192;
+constexpr int EPI_THREADS = 128;  // four epilogue warps, one per TMEM lane quadrant
+constexpr int THREADS = 64 + EPI_THREADS;
 constexpr int MN_BOX = 64;                   // MN extent of one MN-major TMA box
 constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;  // 8 KB
 
@@ -269,9 +270,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = mbar_wait(&acc_full[buf], (lu >> 1) & 1, abort_flag, p.err);
       // one decision for all four warps (tcgen05.ld is warp-collective and
       // the split-K hand-off uses a barrier over these 128 threads)
-      tc::epi_bar();
+      tc::epi_bar<EPI_THREADS>();
       if (t == 0) *go_flag = (ok && !*abort_flag) ? 1 : 0;
-      tc::epi_bar();
+      tc::epi_bar<EPI_THREADS>();
       if (!*go_flag) break;
       tc_fence_after();
       const int i = m0 + row;
@@ -304,9 +305,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(&acc_empty[buf]);
       if (split) {
         __threadfence();
-        tc::epi_bar();
+        tc::epi_bar<EPI_THREADS>();
         if (t == 0) *last_flag = (atomicAdd(&p.tile_ctr[tile], 1) == p.splits - 1) ? 1 : 0;
-        tc::epi_bar();
+        tc::epi_bar<EPI_THREADS>();
         if (*last_flag) {
           __threadfence();
           const int ew = warp - 2;

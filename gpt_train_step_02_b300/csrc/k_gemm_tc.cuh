@@ -167,8 +167,29 @@ GPT2_DEV float4 ld_dsmem_f4(uint32_t addr) {
   return v;
 }
 
-// Barrier over the splitter / epilogue warps only (threads 64 ..).
-GPT2_DEV void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(SPLIT_THREADS) : "memory"); }
+// Named barrier 1 over the NT threads of a kernel's epilogue warps (threads
+// 64 .. 64+NT-1).  NT must equal the number of threads that reach it: each
+// kernel instantiates it with its own epilogue width.
+template <int NT>
+GPT2_DEV void epi_bar() {
+  static_assert(NT % 32 == 0, "whole warps");
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+
+// Named barrier 1 over NT epilogue threads that also ANDs a predicate across
+// them: every thread gets the same answer, so a CTA's epilogue threads take
+// one decision together (for instance after a bounded wait that may have
+// timed out for some of them).
+template <int NT>
+GPT2_DEV bool epi_bar_and(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.and.pred po, 1, %2, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(NT)
+      : "memory");
+  return r != 0;
+}
 
 GPT2_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 GPT2_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -413,9 +434,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     // One decision for all epilogue warps (tcgen05.ld is warp-collective and
     // the split-K hand-off below uses a barrier over these threads).
     // Every epilogue thread reaches this barrier: all of its waits are bounded.
-    epi_bar();
+    epi_bar<SPLIT_THREADS>();
     if (t == 0) *go_flag = (nk > 0 && !*abort_flag) ? 1 : 0;
-    epi_bar();
+    epi_bar<SPLIT_THREADS>();
     if (*go_flag) {
       tc_fence_after();
       const int q = warp & 3;  // TMEM lane quadrant this warp may access
@@ -461,11 +482,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int ii = m0 + r;
         if (ii >= p.M || j >= p.N) continue;
         const uint32_t off = stage + (uint32_t)(r * STAGE_PITCH + 4 * c4) * 4u;
-        float4 acc = ld_dsmem_f4(map_peer(off, 0));
-        for (int z = 1; z < S; z++) {
-          float4 b = ld_dsmem_f4(map_peer(off, (uint32_t)z));
-          acc.x += b.x; acc.y += b.y; acc.z += b.z; acc.w += b.w;
-        }
+        // every peer's partial is loaded before any is summed (the loads
+        // overlap instead of each waiting for the previous one's add)
+        float4 part[8];
+#pragma unroll
+        for (int z = 0; z < 8; z++)
+          if (z < S) part[z] = ld_dsmem_f4(map_peer(off, (uint32_t)z));
+        float4 acc = part[0];
+#pragma unroll
+        for (int z = 1; z < 8; z++)
+          if (z < S) {
+            acc.x += part[z].x; acc.y += part[z].y; acc.z += part[z].z; acc.w += part[z].w;
+          }
         if (j + 4 <= p.N) {
           epi_store4(p.epi, ii, j, acc);
         } else {

@@ -6,13 +6,16 @@
 //   dx += rstd * (g - mean(g) - n * mean(g * n))     (accumulated in place;
 //                                                    optional bf16 copy of dx)
 //   dw += sum_rows dy * n,  db += sum_rows dy         (two-stage, fixed order)
-// C must be a multiple of 4 and at most 32 * 4 * LN_MAXV4.
+// C must be a multiple of 4 and at most 32 * 4 * LN_MAXV4_LIMIT; the kernels
+// are instantiated for the per-lane float4 count ceil(C / 128) so that the
+// row lives in as few registers as it needs.
 #pragma once
 #include "common.cuh"
 
-#define LN_MAXV4 10  // up to C = 1280
+#define LN_MAXV4_LIMIT 10  // float4 elements per lane: C <= 32 * 4 * 10 = 1280
 #define LN_EPS 1e-5f
 
+template <int LN_MAXV4>
 __global__ void layernorm_fwd_kernel(float* __restrict__ y, uint16_t* __restrict__ ybf, float* __restrict__ mean,
                                      float* __restrict__ rstd, const float* __restrict__ x,
                                      const float* __restrict__ w, const float* __restrict__ b, int N, int C) {
@@ -79,6 +82,7 @@ __global__ void layernorm_fwd_kernel(float* __restrict__ y, uint16_t* __restrict
 #define LNB_WARPS 8
 #define LNB_MIN_ROWS 8
 
+template <int LN_MAXV4>
 __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
     float* __restrict__ dx, uint16_t* __restrict__ dxbf, float* __restrict__ partial, const float* __restrict__ dy,
     const float* __restrict__ x, const float* __restrict__ w, const float* __restrict__ mean,
@@ -159,18 +163,3 @@ __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
   for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) partial[(size_t)blockIdx.x * 2 * C + c] = sh[c];
 }
 
-// dw[c] += sum_k partial[k][c], db[c] += sum_k partial[k][C + c].
-__global__ void layernorm_param_grad_kernel(float* __restrict__ dw, float* __restrict__ db,
-                                            const float* __restrict__ partial, int nblocks, int C) {
-  pdl_launch_dependents();
-  pdl_wait();
-  int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= C) return;
-  float sw = 0.f, sb = 0.f;
-  for (int k = 0; k < nblocks; k++) {
-    sw += partial[(size_t)k * 2 * C + c];
-    sb += partial[(size_t)k * 2 * C + C + c];
-  }
-  dw[c] += sw;
-  db[c] += sb;
-}

@@ -135,7 +135,10 @@ __global__ void wte_grad_kernel(float* __restrict__ dwte, const float* __restric
   *d = make_float4(o.x + s.x, o.y + s.y, o.z + s.z, o.w + s.w);
 }
 
-__global__ void wpe_grad_kernel(float* __restrict__ dwpe, const float* __restrict__ dx, int B, int T, int C) {
+// accumulate = 0 stores the sums instead of adding them (the fused training
+// step, whose gradients start from zero).
+__global__ void wpe_grad_kernel(float* __restrict__ dwpe, const float* __restrict__ dx, int B, int T, int C,
+                                int accumulate) {
   pdl_launch_dependents();
   pdl_wait();
   int C4 = C >> 2;
@@ -147,8 +150,11 @@ __global__ void wpe_grad_kernel(float* __restrict__ dwpe, const float* __restric
       s.x += g.x; s.y += g.y; s.z += g.z; s.w += g.w;
     }
     float4* d = reinterpret_cast<float4*>(dwpe + (size_t)t * C) + c4;
-    float4 o = *d;
-    *d = make_float4(o.x + s.x, o.y + s.y, o.z + s.z, o.w + s.w);
+    if (accumulate) {
+      float4 o = *d;
+      s = make_float4(o.x + s.x, o.y + s.y, o.z + s.z, o.w + s.w);
+    }
+    *d = s;
   }
 }
 
@@ -170,14 +176,34 @@ __global__ void col_partial_kernel(const float* __restrict__ Y, int M, int N, lo
   partial[(size_t)blockIdx.y * N + col] = s;
 }
 
-__global__ void col_finish_kernel(const float* __restrict__ partial, int nchunks, int N, float* __restrict__ out) {
+// Column sums of partial rows, finished in a fixed order:
+//   out[c] += sum_{r < nrows} partial[r][c]   for c < split   (out0)
+//   out1[c - split] += ...                    for c >= split  (out1)
+// (= instead of += when accumulate == 0).
+// One CTA of 8 warps per 32 columns: warp w sums rows w, w+8, ... (lane =
+// column, coalesced), then the 8 warp sums are added in warp order.
+__global__ void __launch_bounds__(256) col_finish_kernel(float* __restrict__ out0, float* __restrict__ out1, int split,
+                                                         const float* __restrict__ partial, int nrows, int ncols,
+                                                         int accumulate) {
   pdl_launch_dependents();
   pdl_wait();
-  int col = blockIdx.x * blockDim.x + threadIdx.x;
-  if (col >= N) return;
+  __shared__ float sh[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * 32 + lane;
   float s = 0.f;
-  for (int k = 0; k < nchunks; k++) s += partial[(size_t)k * N + col];
-  out[col] += s;
+  if (c < ncols) {
+#pragma unroll 4
+    for (int r = warp; r < nrows; r += 8) s += partial[(size_t)r * ncols + c];
+  }
+  sh[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && c < ncols) {
+    float t = sh[0][lane];
+#pragma unroll
+    for (int w = 1; w < 8; w++) t += sh[w][lane];
+    float* o = c < split ? out0 + c : out1 + (c - split);
+    *o = accumulate ? *o + t : t;
+  }
 }
 
 // Mean of n values in a fixed order (one CTA of 1024 threads).

@@ -50,7 +50,12 @@ def run_gpu(qkv, NH, precision):
     return y.cpu().numpy(), lse.cpu().numpy()
 
 
-@pytest.mark.parametrize("B,T,C,NH", [(2, 32, 64, 4), (1, 13, 64, 4), (2, 64, 768, 12), (1, 1, 64, 4)])
+# CUDA-core shapes: several 64-row chunks with a ragged tail (T = 200), head
+# sizes 16, 64 and 128, a single position, a partial 8-row CTA (T = 13)
+FP32_SHAPES = [(2, 32, 64, 4), (1, 13, 64, 4), (2, 64, 768, 12), (1, 1, 64, 4), (1, 200, 128, 2), (1, 70, 256, 2)]
+
+
+@pytest.mark.parametrize("B,T,C,NH", FP32_SHAPES)
 def test_attention_forward_fp32(B, T, C, NH):
     import gpt_train_step_02_b300 as g
 
@@ -106,7 +111,7 @@ def rel_l2(a, b):
     return np.linalg.norm(a - b) / np.linalg.norm(b)
 
 
-@pytest.mark.parametrize("B,T,C,NH", [(2, 32, 64, 4), (1, 13, 64, 4), (2, 64, 768, 12)])
+@pytest.mark.parametrize("B,T,C,NH", FP32_SHAPES)
 def test_attention_backward_fp32(B, T, C, NH):
     import gpt_train_step_02_b300 as g
 

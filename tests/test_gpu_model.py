@@ -218,6 +218,31 @@ def test_device_step_matches_host_calls():
     b.close()
 
 
+def test_fused_step_gradients_equal_zero_grad_then_backward():
+    """The fused step stores each gradient once instead of clearing the
+    buffer and accumulating: its gradients must equal zero_grad + backward
+    exactly, also when a shorter sequence follows a longer one (the wpe rows
+    past T are cleared, not left from the previous step)."""
+    import torch
+
+    w = TINY
+    p0 = perturbed(w)
+    a = gpu_model(w)
+    b = gpu_model(w)
+    a.set_params(p0)
+    b.set_params(p0)
+    for t, (B, T) in enumerate([(2, 32), (2, 16), (1, 7)], start=1):
+        inp, tgt = synth.batch(w, B=B, T=T)
+        la = a.step(inp, tgt, t)
+        b.train_step_device(torch.tensor(inp, device="cuda"), torch.tensor(tgt, device="cuda"), t)
+        lb = b.sync()
+        assert la == lb, (t, la, lb)
+        assert np.array_equal(a.get_grads(), b.get_grads()), t
+        assert np.array_equal(a.get_params(), b.get_params()), t
+    a.close()
+    b.close()
+
+
 def test_checkpoint_resume_is_bitwise():
     w = TINY
     p0 = synth.init_params(w)
