@@ -55,61 +55,45 @@ GPT2_DEV void epi_store(const EpiArgs& e, int i, int j, float acc) {
 GPT2_DEV float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 GPT2_DEV void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 
-// Finishes 32 consecutive outputs (i, j0 .. j0+31) of one row, nvalid of
-// them inside the matrix.  With a full chunk and vec4 set, every global load
-// of the chunk (bias, R, C) is issued before any arithmetic or store, as
-// 16-byte accesses, so a thread waits about one memory latency per chunk.
-GPT2_DEV void epi_store_row32(const EpiArgs& e, int i, int j0, const float* v, int nvalid) {
-  if (nvalid < 32 || !e.vec4) {
-#pragma unroll
-    for (int q = 0; q < 32; q++)
-      if (q < nvalid) epi_store(e, i, j0 + q, v[q]);
-    return;
-  }
-  float4 in[8], bs[8];
-  float* crow = e.C + (size_t)i * e.ldc + j0;
-  const int op = e.epi;
-  if (op == EPI_BIAS || op == EPI_BIAS_RESID || op == EPI_BIAS_GELU) {
-#pragma unroll
-    for (int q = 0; q < 8; q++) bs[q] = ld4(e.bias + j0 + 4 * q);
-  }
-  if (op == EPI_BIAS_RESID || op == EPI_DGELU) {
-    const float* rrow = e.R + (size_t)i * e.ldr + j0;
-#pragma unroll
-    for (int q = 0; q < 8; q++) in[q] = ld4(rrow + 4 * q);
-  } else if (op == EPI_ACCUM) {
-#pragma unroll
-    for (int q = 0; q < 8; q++) in[q] = ld4(crow + 4 * q);
-  }
-#pragma unroll
-  for (int q = 0; q < 8; q++) {
-    float o[4];
-    const float* b4 = &bs[q].x;
-    const float* r4 = &in[q].x;
-#pragma unroll
-    for (int c = 0; c < 4; c++) {
-      float a = v[4 * q + c];
-      switch (op) {
-        case EPI_BIAS: o[c] = a + b4[c]; break;
-        case EPI_BIAS_RESID: o[c] = a + b4[c] + r4[c]; break;
-        case EPI_BIAS_GELU: o[c] = a + b4[c]; break;  // pre-activation; GELU below
-        case EPI_DGELU: o[c] = a * gelu_grad(r4[c]); break;
-        case EPI_ACCUM: o[c] = r4[c] + a; break;
-        default: o[c] = a;
-      }
+// Whether an epilogue reads a per-column bias / a per-element input (R, or C
+// for the accumulating product).
+GPT2_DEV bool epi_has_bias(int op) { return op == EPI_BIAS || op == EPI_BIAS_RESID || op == EPI_BIAS_GELU; }
+GPT2_DEV bool epi_has_input(int op) { return op == EPI_BIAS_RESID || op == EPI_DGELU || op == EPI_ACCUM; }
+
+// The input of element block (i, j .. j+3) an epilogue reads (R or C).
+GPT2_DEV float4 epi_load_input(const EpiArgs& e, int i, int j) {
+  return e.epi == EPI_ACCUM ? ld4(e.C + (size_t)i * e.ldc + j) : ld4(e.R + (size_t)i * e.ldr + j);
+}
+
+// Finishes (i, j .. j+3) from the accumulator, the column bias b and the
+// element input in (both already loaded when the epilogue needs them).
+// vec4 must hold.
+GPT2_DEV void epi_apply4(const EpiArgs& e, int i, int j, float4 acc, float4 b, float4 in) {
+  float4 o = acc;
+  switch (e.epi) {
+    case EPI_BIAS: o = make_float4(acc.x + b.x, acc.y + b.y, acc.z + b.z, acc.w + b.w); break;
+    case EPI_BIAS_RESID:
+      o = make_float4(acc.x + b.x + in.x, acc.y + b.y + in.y, acc.z + b.z + in.z, acc.w + b.w + in.w);
+      break;
+    case EPI_BIAS_GELU: {
+      float4 h = make_float4(acc.x + b.x, acc.y + b.y, acc.z + b.z, acc.w + b.w);
+      st4(e.pre + (size_t)i * e.ldpre + j, h);
+      o = make_float4(gelu_fwd(h.x), gelu_fwd(h.y), gelu_fwd(h.z), gelu_fwd(h.w));
+      break;
     }
-    if (op == EPI_BIAS_GELU) {
-      st4(e.pre + (size_t)i * e.ldpre + j0 + 4 * q, make_float4(o[0], o[1], o[2], o[3]));
-#pragma unroll
-      for (int c = 0; c < 4; c++) o[c] = gelu_fwd(o[c]);
-    }
-    if (e.C) st4(crow + 4 * q, make_float4(o[0], o[1], o[2], o[3]));
-    if (e.Cbf) {
-      uint2 h;
-      h.x = (uint32_t)to_bf16_bits(o[0]) | ((uint32_t)to_bf16_bits(o[1]) << 16);
-      h.y = (uint32_t)to_bf16_bits(o[2]) | ((uint32_t)to_bf16_bits(o[3]) << 16);
-      *reinterpret_cast<uint2*>(e.Cbf + (size_t)i * e.ldcbf + j0 + 4 * q) = h;
-    }
+    case EPI_DGELU:
+      o = make_float4(acc.x * gelu_grad(in.x), acc.y * gelu_grad(in.y), acc.z * gelu_grad(in.z),
+                      acc.w * gelu_grad(in.w));
+      break;
+    case EPI_ACCUM: o = make_float4(in.x + acc.x, in.y + acc.y, in.z + acc.z, in.w + acc.w); break;
+    default: break;
+  }
+  if (e.C) st4(e.C + (size_t)i * e.ldc + j, o);
+  if (e.Cbf) {
+    uint2 h;
+    h.x = (uint32_t)to_bf16_bits(o.x) | ((uint32_t)to_bf16_bits(o.y) << 16);
+    h.y = (uint32_t)to_bf16_bits(o.z) | ((uint32_t)to_bf16_bits(o.w) << 16);
+    *reinterpret_cast<uint2*>(e.Cbf + (size_t)i * e.ldcbf + j) = h;
   }
 }
 
@@ -122,43 +106,72 @@ GPT2_DEV void epi_store4(const EpiArgs& e, int i, int j, float4 acc) {
     epi_store(e, i, j + 3, acc.w);
     return;
   }
-  float* cp = e.C + (size_t)i * e.ldc + j;
-  float4 o = acc;
-  switch (e.epi) {
-    case EPI_BIAS: {
-      float4 b = ld4(e.bias + j);
-      o = make_float4(acc.x + b.x, acc.y + b.y, acc.z + b.z, acc.w + b.w);
-      break;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  epi_apply4(e, i, j, acc, epi_has_bias(e.epi) ? ld4(e.bias + j) : z, epi_has_input(e.epi) ? epi_load_input(e, i, j) : z);
+}
+
+// ---- coalesced epilogue of a warp's 32 x 32 sub-tile --------------------------
+// Thread `lane` holds row i0 + lane, columns j0 .. j0+31 (from tcgen05.ld).
+// The sub-tile is transposed through the warp's own staging area (32 rows of
+// EPI_STAGE_PITCH floats) so that one warp instruction then covers 4 rows of
+// 32 columns: lane l handles columns j0 + 4 (l % 8) .. +3 of rows
+// i0 + l / 8 + 4 k, k = 0 .. 7, every access a 16-byte piece of a full
+// 128-byte row segment.  All global loads of the sub-tile are issued before
+// any store.
+#define EPI_STAGE_PITCH 36  // floats; keeps rows 16-byte aligned and spreads the banks
+#define EPI_STAGE_FLOATS (32 * EPI_STAGE_PITCH)
+
+GPT2_DEV void warp32_stage(float* stage, const float* v, int lane) {
+#pragma unroll
+  for (int u = 0; u < 8; u++)
+    st4(stage + lane * EPI_STAGE_PITCH + 4 * u, make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]));
+  __syncwarp();
+}
+
+// Raw fp32 store of the staged sub-tile into P (row pitch ldp), rows < M, columns < N.
+GPT2_DEV void warp32_store_raw(float* P, long long ldp, const float* stage, int i0, int j0, int M, int N, int lane) {
+  const int c = 4 * (lane & 7), rs = lane >> 3, j = j0 + c;
+#pragma unroll
+  for (int k = 0; k < 8; k++) {
+    const int r = rs + 4 * k, i = i0 + r;
+    if (i < M && j < N) {
+      const float4 a = ld4(stage + r * EPI_STAGE_PITCH + c);
+      if (j + 4 <= N && (ldp & 3) == 0) {
+        st4(P + (size_t)i * ldp + j, a);
+      } else {
+        const float a4[4] = {a.x, a.y, a.z, a.w};
+        for (int q = 0; q < 4 && j + q < N; q++) P[(size_t)i * ldp + j + q] = a4[q];
+      }
     }
-    case EPI_BIAS_RESID: {
-      float4 b = ld4(e.bias + j), r = ld4(e.R + (size_t)i * e.ldr + j);
-      o = make_float4(acc.x + b.x + r.x, acc.y + b.y + r.y, acc.z + b.z + r.z, acc.w + b.w + r.w);
-      break;
-    }
-    case EPI_BIAS_GELU: {
-      float4 b = ld4(e.bias + j);
-      float4 h = make_float4(acc.x + b.x, acc.y + b.y, acc.z + b.z, acc.w + b.w);
-      st4(e.pre + (size_t)i * e.ldpre + j, h);
-      o = make_float4(gelu_fwd(h.x), gelu_fwd(h.y), gelu_fwd(h.z), gelu_fwd(h.w));
-      break;
-    }
-    case EPI_DGELU: {
-      float4 r = ld4(e.R + (size_t)i * e.ldr + j);
-      o = make_float4(acc.x * gelu_grad(r.x), acc.y * gelu_grad(r.y), acc.z * gelu_grad(r.z), acc.w * gelu_grad(r.w));
-      break;
-    }
-    case EPI_ACCUM: {
-      float4 c = ld4(cp);
-      o = make_float4(c.x + acc.x, c.y + acc.y, c.z + acc.z, c.w + acc.w);
-      break;
-    }
-    default: break;
   }
-  if (e.C) st4(cp, o);
-  if (e.Cbf) {
-    uint2 h;
-    h.x = (uint32_t)to_bf16_bits(o.x) | ((uint32_t)to_bf16_bits(o.y) << 16);
-    h.y = (uint32_t)to_bf16_bits(o.z) | ((uint32_t)to_bf16_bits(o.w) << 16);
-    *reinterpret_cast<uint2*>(e.Cbf + (size_t)i * e.ldcbf + j) = h;
+  __syncwarp();
+}
+
+// Fused epilogue of the staged sub-tile into the product's outputs.
+GPT2_DEV void warp32_epilogue(const EpiArgs& e, const float* stage, int i0, int j0, int M, int N, int lane) {
+  const int c = 4 * (lane & 7), rs = lane >> 3, j = j0 + c;
+  if (j < N) {
+    if (e.vec4 && j + 4 <= N) {
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 b = epi_has_bias(e.epi) ? ld4(e.bias + j) : z;
+      float4 in[8];
+#pragma unroll
+      for (int k = 0; k < 8; k++) {
+        const int i = i0 + rs + 4 * k;
+        in[k] = (epi_has_input(e.epi) && i < M) ? epi_load_input(e, i, j) : z;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; k++) {
+        const int r = rs + 4 * k, i = i0 + r;
+        if (i < M) epi_apply4(e, i, j, ld4(stage + r * EPI_STAGE_PITCH + c), b, in[k]);
+      }
+    } else {
+      for (int k = 0; k < 8; k++) {
+        const int r = rs + 4 * k, i = i0 + r;
+        if (i < M)
+          for (int q = 0; q < 4 && j + q < N; q++) epi_store(e, i, j + q, stage[r * EPI_STAGE_PITCH + c + q]);
+      }
+    }
   }
+  __syncwarp();
 }

@@ -137,9 +137,9 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->dfch = take(BT * 4 * C * F);
   p->attD = take(BT * NH * F);
   // scratch: column-sum partials (<= ceil(BT/BIAS_MIN_ROWS) x 4C) and
-  // layernorm partials (<= ceil(BT/LNB_MIN_ROWS) x 2C)
+  // layernorm partials (<= ceil(BT/LNB_MIN_ROWS) x 3C)
   size_t s1 = ((BT + BIAS_MIN_ROWS - 1) / BIAS_MIN_ROWS) * 4 * C;
-  size_t s2 = ((BT + LNB_MIN_ROWS - 1) / LNB_MIN_ROWS) * 2 * C;
+  size_t s2 = ((BT + LNB_MIN_ROWS - 1) / LNB_MIN_ROWS) * 3 * C;
   p->scratch_floats = s1 > s2 ? s1 : s2;
   p->scratch = take(p->scratch_floats * F);
   p->sorted = take(BT * sizeof(uint32_t));
@@ -521,8 +521,8 @@ static void mm_dw(gpt2_t* m, float* dW, Opnd dy, Opnd x, int N, int IC, int OC) 
 static void bias_grad(gpt2_t* m, float* db, const float* dy, int N, int OC) {
   const int rows = BIAS_MIN_ROWS, chunks = ceil_div(N, rows);
   launch_k(col_partial_kernel, dim3(ceil_div(OC, 256), chunks), 256, 0, m->stream, dy, N, OC, OC, rows, m->scratch);
-  launch_k(col_finish_kernel, ceil_div(OC, 32), 256, 0, m->stream, db, db, OC, m->scratch, chunks, OC,
-           m->grad_accumulate);
+  launch_k(col_finish_kernel, ceil_div(OC, 32), COLF_WARPS * 32, 0, m->stream, db, db, db, OC, m->scratch, chunks,
+           OC, m->grad_accumulate);
   m->launches += 2;
 }
 
@@ -543,21 +543,22 @@ static void ln_forward(gpt2_t* m, float* y, uint16_t* ybf, float* mean, float* r
   m->launches++;
 }
 
-static void ln_backward(gpt2_t* m, float* dx, uint16_t* dxbf, float* dw, float* db, const float* dy, const float* x,
-                        const float* w, const float* mean, const float* rstd, int N) {
+// layernorm backward: dx += ...; dw, db (+)= the parameter gradients; when
+// dxsum != NULL also dxsum (+)= the column sums of the updated dx -- the bias
+// gradient of the linear layer whose output gradient dx is.
+static void ln_backward(gpt2_t* m, float* dx, uint16_t* dxbf, float* dw, float* db, float* dxsum, const float* dy,
+                        const float* x, const float* w, const float* mean, const float* rstd, int N) {
   int C = m->cfg.channels;
-  // rows per block: a multiple of the warp count, about two blocks per SM's worth of warps
-  int rows = ceil_div(ceil_div(N, 8 * 148), LNB_WARPS) * LNB_WARPS;
-  if (rows < LNB_MIN_ROWS) rows = LNB_MIN_ROWS;
-  int nb = ceil_div(N, rows);
+  const int nb = ceil_div(N, LNB_WARPS);  // one row per warp
+  const int nout = dxsum ? 3 : 2;
   timer_begin(m, TK_LAYERNORM, (16.0 * C + 8.0) * N);
   auto k = ln_pick(C, layernorm_bwd_kernel<1>, layernorm_bwd_kernel<2>, layernorm_bwd_kernel<4>,
                    layernorm_bwd_kernel<6>, layernorm_bwd_kernel<8>, layernorm_bwd_kernel<10>);
-  launch_k(k, nb, LNB_WARPS * 32, 2 * C * sizeof(float), m->stream, dx, dxbf, m->scratch, dy, x, w, mean, rstd, N, C,
-           rows);
-  // dw[c] += sum_b partial[b][c], db[c] += sum_b partial[b][C + c]
-  launch_k(col_finish_kernel, ceil_div(2 * C, 32), 256, 0, m->stream, dw, db, C, m->scratch, nb, 2 * C,
-           m->grad_accumulate);
+  launch_k(k, nb, LNB_WARPS * 32, (size_t)LNB_WARPS * nout * C * sizeof(float), m->stream, dx, dxbf, m->scratch, dy, x,
+           w, mean, rstd, N, C, dxsum ? 1 : 0);
+  // dw[c] (+)= sum_b partial[b][c], db[c] (+)= sum_b partial[b][C + c], dxsum[c] (+)= ...[2C + c]
+  launch_k(col_finish_kernel, ceil_div(nout * C, 32), COLF_WARPS * 32, 0, m->stream, dw, db, dxsum, C, m->scratch, nb,
+           nout * C, m->grad_accumulate);
   timer_end(m, TK_LAYERNORM);
   m->launches += 2;
 }
@@ -676,6 +677,14 @@ static int set_kernel_attributes() {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tca::attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                tca::dqk::SMEM_BYTES);
+    // layernorm backward: 8 rows x 3C floats of shared memory (C <= 1280)
+    const int lnb = LNB_WARPS * 3 * 32 * 4 * LN_MAXV4_LIMIT * (int)sizeof(float);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<10>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
     // CUDA-core attention: up to head size 128
     const int f = (int)att_smem_fwd(128), kv = (int)att_smem_dkv(128);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_fwd_simt_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, f);
@@ -813,23 +822,23 @@ static int enqueue_backward(gpt2_t* m) {
   mm_dw(m, G[P_WTE], {m->dlogits, m->dlogits_bf}, {m->lnf, m->lnf_bf}, N, C, Vp);
   CCHECK(m, cudaMemsetAsync(m->dres, 0, (size_t)N * C * sizeof(float), s));
   LayerActs last = layer_acts(m, L - 1);
-  ln_backward(m, m->dres, m->dres_bf, G[P_LNFW], G[P_LNFB], m->dln, last.res3, P[P_LNFW], m->lnf_mean, m->lnf_rstd,
-              N);
+  // the column sums of this dres are the last layer's MLP output-projection bias gradient
+  ln_backward(m, m->dres, m->dres_bf, G[P_LNFW], G[P_LNFB], G[P_FCPROJB] + (size_t)(L - 1) * C, m->dln, last.res3,
+              P[P_LNFW], m->lnf_mean, m->lnf_rstd, N);
   for (int l = L - 1; l >= 0; l--) {
     LayerActs a = layer_acts(m, l);
     // MLP output projection: res3 = res2 + fchg fcprojw^T + fcprojb
     mm_dw(m, G[P_FCPROJW] + l * 4 * CC, dres, {a.fchg, a.fchg_bf}, N, 4 * C, C);
-    bias_grad(m, G[P_FCPROJB] + (size_t)l * C, m->dres, N, C);
+    // (its bias gradient came with the layernorm backward that produced dres)
     mm_dx(m, m->dfch, m->dfch_bf, dres, wparam(m, P_FCPROJW, l * 4 * CC), N, 4 * C, C, a.fch);  // x gelu'(fch)
     // MLP input projection: fch = ln2 fcw^T + fcb
     mm_dw(m, G[P_FCW] + l * 4 * CC, dfch, {a.ln2, a.ln2_bf}, N, C, 4 * C);
     bias_grad(m, G[P_FCB] + (size_t)l * 4 * C, m->dfch, N, 4 * C);
     mm_dx(m, m->dln, nullptr, dfch, wparam(m, P_FCW, l * 4 * CC), N, C, 4 * C, nullptr);
-    ln_backward(m, m->dres, m->dres_bf, G[P_LN2W] + (size_t)l * C, G[P_LN2B] + (size_t)l * C, m->dln, a.res2,
-                P[P_LN2W] + (size_t)l * C, a.ln2_mean, a.ln2_rstd, N);
+    ln_backward(m, m->dres, m->dres_bf, G[P_LN2W] + (size_t)l * C, G[P_LN2B] + (size_t)l * C,
+                G[P_ATTPROJB] + (size_t)l * C, m->dln, a.res2, P[P_LN2W] + (size_t)l * C, a.ln2_mean, a.ln2_rstd, N);
     // attention output projection: res2 = x + atty attprojw^T + attprojb
     mm_dw(m, G[P_ATTPROJW] + l * CC, dres, {a.atty, a.atty_bf}, N, C, C);
-    bias_grad(m, G[P_ATTPROJB] + (size_t)l * C, m->dres, N, C);
     mm_dx(m, m->datty, m->datty_bf, dres, wparam(m, P_ATTPROJW, l * CC), N, C, C, nullptr);
     // attention
     attn_backward(m, a.qkv, a.qkv_bf, a.atty, a.lse, B, T, bf);
@@ -837,8 +846,10 @@ static int enqueue_backward(gpt2_t* m) {
     mm_dw(m, G[P_QKVW] + l * 3 * CC, dqkv, {a.ln1, a.ln1_bf}, N, C, 3 * C);
     bias_grad(m, G[P_QKVB] + (size_t)l * 3 * C, m->dqkv, N, 3 * C);
     mm_dx(m, m->dln, nullptr, dqkv, wparam(m, P_QKVW, l * 3 * CC), N, C, 3 * C, nullptr);
-    ln_backward(m, m->dres, m->dres_bf, G[P_LN1W] + (size_t)l * C, G[P_LN1B] + (size_t)l * C, m->dln, a.x,
-                P[P_LN1W] + (size_t)l * C, a.ln1_mean, a.ln1_rstd, N);
+    // below layer 0 this dres is the previous layer's MLP output gradient
+    ln_backward(m, m->dres, m->dres_bf, G[P_LN1W] + (size_t)l * C, G[P_LN1B] + (size_t)l * C,
+                l > 0 ? G[P_FCPROJB] + (size_t)(l - 1) * C : nullptr, m->dln, a.x, P[P_LN1W] + (size_t)l * C,
+                a.ln1_mean, a.ln1_rstd, N);
   }
   // embeddings
   size_t smem = 1;
@@ -1386,7 +1397,8 @@ static int op_backward(float* dx, float* dW, float* dbias, const float* dy, cons
   if (dbias) {
     int chunks = ceil_div(N, 64);
     launch_k(col_partial_kernel, dim3(ceil_div(OC, 256), chunks), 256, 0, s, dy, N, OC, OC, 64, w.bias_partial);
-    launch_k(col_finish_kernel, ceil_div(OC, 32), 256, 0, s, dbias, dbias, OC, w.bias_partial, chunks, OC, 1);
+    launch_k(col_finish_kernel, ceil_div(OC, 32), COLF_WARPS * 32, 0, s, dbias, dbias, dbias, OC, w.bias_partial,
+             chunks, OC, 1);
     if (cudaGetLastError() != cudaSuccess) return GPT2_ERR_CUDA;
   }
   return op_status(w, s);

@@ -38,12 +38,33 @@ static inline size_t att_smem_dkv(int hs) {
 
 // Loads rows r0 .. r0+n-1 (n <= ATT_CHUNK; the rest of the chunk is zero) of
 // a head's hs columns into dst[ATT_CHUNK][pitch]; source row r at src + r*ld.
+// hs % 4 == 0 and the source rows are 16-byte aligned: each thread issues all
+// of its 16-byte loads before it stores any of them.
 GPT2_DEV void att_load_chunk(float* dst, int pitch, const float* src, long long ld, int r0, int n, int hs,
                              int bf16_ops) {
-  for (int e = threadIdx.x; e < ATT_CHUNK * hs; e += blockDim.x) {
-    int r = e / hs, d = e - r * hs;
-    float v = r < n ? src[(size_t)(r0 + r) * ld + d] : 0.f;
-    dst[r * pitch + d] = att_rnd(v, bf16_ops);
+  constexpr int MAXV = ATT_CHUNK * 128 / 4 / (ATT_ROWS * 32);  // float4 per thread for hs <= 128
+  const int hs4 = hs >> 2, total = ATT_CHUNK * hs4;
+  float4 v[MAXV];
+#pragma unroll
+  for (int u = 0; u < MAXV; u++) {
+    const int e = threadIdx.x + u * ATT_ROWS * 32;
+    v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e < total) {
+      const int r = e / hs4, d4 = e - r * hs4;
+      if (r < n) v[u] = *reinterpret_cast<const float4*>(src + (size_t)(r0 + r) * ld + 4 * d4);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < MAXV; u++) {
+    const int e = threadIdx.x + u * ATT_ROWS * 32;
+    if (e < total) {
+      const int r = e / hs4, d = 4 * (e - r * hs4);
+      float* o = dst + r * pitch + d;
+      o[0] = att_rnd(v[u].x, bf16_ops);
+      o[1] = att_rnd(v[u].y, bf16_ops);
+      o[2] = att_rnd(v[u].z, bf16_ops);
+      o[3] = att_rnd(v[u].w, bf16_ops);
+    }
   }
 }
 

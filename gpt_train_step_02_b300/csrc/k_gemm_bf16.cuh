@@ -74,7 +74,8 @@ struct Cfg {
   // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], mma_done
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+  static constexpr int OFF_EPI = (OFF_MISC + 64 + 15) / 16 * 16;  // four warps' epilogue staging
+  static constexpr int SMEM_BYTES = OFF_EPI + 4 * EPI_STAGE_FLOATS * 4 + 1024;  // + alignment slack
   static constexpr int TMEM_COLS = 2 * BN;                  // two accumulators
 };
 
@@ -260,7 +261,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- epilogue ----------------
     const int t = threadIdx.x - 64;  // 0..127
     const int q = warp & 3;          // TMEM lane quadrant this warp may access
-    const int row = q * 32 + lane;
     int lu = 0;
     for (int unit = blockIdx.x; unit < p.units; unit += gridDim.x, lu++) {
       int m0, tn, z, tile;
@@ -275,30 +275,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::epi_bar<EPI_THREADS>();
       if (!*go_flag) break;
       tc_fence_after();
-      const int i = m0 + row;
       const bool split = p.splits > 1;
+      float* stage = reinterpret_cast<float*>(smem + CF::OFF_EPI) + (warp - 2) * EPI_STAGE_FLOATS;
+      const int i0 = m0 + q * 32;  // this warp's 32 rows
       const uint32_t tbase = tmem + (uint32_t)(buf * BN) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
       for (int cc = 0; cc < BN / 32; cc++) {
         float v[32];
         tmem_ld32(tbase + (uint32_t)(cc * 32), v);
         const int j0 = n0 + cc * 32;
-        const int nvalid = min(32, p.N - j0);
-        if (i < p.M && nvalid > 0) {
-          if (split) {
-            float* dst = p.partial + (size_t)z * p.M * p.N + (size_t)i * p.N + j0;
-            if (nvalid == 32 && (p.N & 3) == 0) {
-#pragma unroll
-              for (int u = 0; u < 8; u++) st4(dst + 4 * u, make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]));
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; e++)
-                if (e < nvalid) dst[e] = v[e];
-            }
-          } else {
-            epi_store_row32(p.epi, i, j0, v, nvalid);
-          }
-        }
+        if (j0 >= p.N || i0 >= p.M) continue;  // warp-uniform
+        warp32_stage(stage, v, lane);
+        if (split)
+          warp32_store_raw(p.partial + (size_t)z * p.M * p.N, p.N, stage, i0, j0, p.M, p.N, lane);
+        else
+          warp32_epilogue(p.epi, stage, i0, j0, p.M, p.N, lane);
       }
       // the accumulator is in registers / global memory now: hand it back
       tc_fence_before();

@@ -58,6 +58,7 @@ constexpr int OFF_BAR = OFF_LO_B + COMP_STAGES * TILE_BYTES;
 constexpr int OFF_STAGE = OFF_HI_A;
 constexpr int STAGE_PITCH = BN + 4;  // floats per staged row (padding spreads the banks)
 static_assert(BM * STAGE_PITCH * 4 <= OFF_BAR - OFF_HI_A, "staged partial tile must fit the hi/lo region");
+static_assert(SPLIT_WARPS * EPI_STAGE_FLOATS * 4 <= OFF_BAR - OFF_HI_A, "epilogue staging must fit the hi/lo region");
 constexpr int NUM_BARS = 2 * RAW_STAGES + 2 * COMP_STAGES + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
@@ -441,7 +442,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int q = warp & 3;  // TMEM lane quadrant this warp may access
       const int row = q * 32 + lane;
-      const int i = m0 + row;
       const int half = (warp - 2) >> 2;  // which half of the 128 columns this warp finishes
       float* stage = reinterpret_cast<float*>(smem + OFF_STAGE);
 #pragma unroll 1
@@ -453,10 +453,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           float* dst = stage + row * STAGE_PITCH + cc * 32;
 #pragma unroll
           for (int u = 0; u < 8; u++) st4(dst + 4 * u, make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]));
-        } else if (i < p.M) {
-          int j0 = n0 + cc * 32;
-          int nvalid = min(32, p.N - j0);
-          if (nvalid > 0) epi_store_row32(p.epi, i, j0, v, nvalid);
+        } else {
+          // coalesced epilogue through this warp's staging area (the hi/lo
+          // region is free once the accumulator is complete)
+          const int j0 = n0 + cc * 32, i0 = m0 + q * 32;
+          if (j0 < p.N && i0 < p.M) {  // warp-uniform
+            float* ws = reinterpret_cast<float*>(smem + OFF_STAGE) + (warp - 2) * EPI_STAGE_FLOATS;
+            warp32_stage(ws, v, lane);
+            warp32_epilogue(p.epi, ws, i0, j0, p.M, p.N, lane);
+          }
         }
       }
     }

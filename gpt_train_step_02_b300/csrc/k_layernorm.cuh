@@ -75,54 +75,66 @@ __global__ void layernorm_fwd_kernel(float* __restrict__ y, uint16_t* __restrict
   }
 }
 
-// Block = LNB_WARPS warps covering `rows` consecutive rows (a multiple of
-// LNB_WARPS, at least LNB_MIN_ROWS; the host picks it so that the grid
-// covers the SMs).  Writes the block's dw/db partial sums (rows in order,
-// warps in order) to partial[blockIdx][0..C) and partial[blockIdx][C..2C).
+// Backward: one row per warp, LNB_WARPS rows per block.  Each warp writes its
+// row's contributions dy*n, dy (and, with with_dxsum, the updated dx) to its
+// own shared-memory slot; the block then sums the slots column by column in
+// warp order and writes partial[blockIdx][0..C) (dw), [C..2C) (db) and
+// [2C..3C) (column sums of dx: the bias gradient of the linear layer whose
+// output gradient dx is).  Only x and dy of one row live in registers, so
+// many warps fit an SM.
 #define LNB_WARPS 8
-#define LNB_MIN_ROWS 8
+#define LNB_MIN_ROWS LNB_WARPS  // rows per block
 
 template <int LN_MAXV4>
 __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
     float* __restrict__ dx, uint16_t* __restrict__ dxbf, float* __restrict__ partial, const float* __restrict__ dy,
     const float* __restrict__ x, const float* __restrict__ w, const float* __restrict__ mean,
-    const float* __restrict__ rstd, int N, int C, int rows) {
+    const float* __restrict__ rstd, int N, int C, int with_dxsum) {
   pdl_launch_dependents();
   pdl_wait();
-  extern __shared__ float sh[];  // [2C]
-  int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float4 aw[LN_MAXV4], ab[LN_MAXV4];
-#pragma unroll
-  for (int k = 0; k < LN_MAXV4; k++) aw[k] = ab[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  int r0 = blockIdx.x * rows;
-  for (int r = r0 + warp; r < min(N, r0 + rows); r += LNB_WARPS) {
-    float mu = mean[r], rs = rstd[r];
-    float4 n[LN_MAXV4], g[LN_MAXV4], d[LN_MAXV4];
+  extern __shared__ float sh[];  // [LNB_WARPS][nout * C]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nout = with_dxsum ? 3 : 2;
+  const int r = blockIdx.x * LNB_WARPS + warp;
+  float* my = sh + warp * nout * C;
+  if (r < N) {
+    const float mu = mean[r], rs = rstd[r];
+    float4 xv[LN_MAXV4], dv[LN_MAXV4];
     float sg = 0.f, sgn = 0.f;
 #pragma unroll
     for (int k = 0; k < LN_MAXV4; k++) {
-      int c = (lane + 32 * k) * 4;
+      const int c = (lane + 32 * k) * 4;
       if (c < C) {
-        float4 xx = *reinterpret_cast<const float4*>(x + (size_t)r * C + c);
-        d[k] = *reinterpret_cast<const float4*>(dy + (size_t)r * C + c);
-        float4 ww = *reinterpret_cast<const float4*>(w + c);
-        n[k] = make_float4((xx.x - mu) * rs, (xx.y - mu) * rs, (xx.z - mu) * rs, (xx.w - mu) * rs);
-        g[k] = make_float4(d[k].x * ww.x, d[k].y * ww.y, d[k].z * ww.z, d[k].w * ww.w);
-        sg += (g[k].x + g[k].y) + (g[k].z + g[k].w);
-        sgn += (g[k].x * n[k].x + g[k].y * n[k].y) + (g[k].z * n[k].z + g[k].w * n[k].w);
+        xv[k] = *reinterpret_cast<const float4*>(x + (size_t)r * C + c);
+        dv[k] = *reinterpret_cast<const float4*>(dy + (size_t)r * C + c);
       }
     }
-    float mg = warp_sum(sg) / (float)C, mgn = warp_sum(sgn) / (float)C;
 #pragma unroll
     for (int k = 0; k < LN_MAXV4; k++) {
-      int c = (lane + 32 * k) * 4;
+      const int c = (lane + 32 * k) * 4;
       if (c < C) {
+        const float4 ww = *reinterpret_cast<const float4*>(w + c);
+        const float n0 = (xv[k].x - mu) * rs, n1 = (xv[k].y - mu) * rs, n2 = (xv[k].z - mu) * rs,
+                    n3 = (xv[k].w - mu) * rs;
+        const float g0 = dv[k].x * ww.x, g1 = dv[k].y * ww.y, g2 = dv[k].z * ww.z, g3 = dv[k].w * ww.w;
+        sg += (g0 + g1) + (g2 + g3);
+        sgn += (g0 * n0 + g1 * n1) + (g2 * n2 + g3 * n3);
+      }
+    }
+    const float mg = warp_sum(sg) / (float)C, mgn = warp_sum(sgn) / (float)C;
+#pragma unroll
+    for (int k = 0; k < LN_MAXV4; k++) {
+      const int c = (lane + 32 * k) * 4;
+      if (c < C) {
+        const float4 ww = *reinterpret_cast<const float4*>(w + c);
+        const float4 n = make_float4((xv[k].x - mu) * rs, (xv[k].y - mu) * rs, (xv[k].z - mu) * rs,
+                                     (xv[k].w - mu) * rs);
         float4* o = reinterpret_cast<float4*>(dx + (size_t)r * C + c);
         float4 a = *o;
-        a.x += rs * (g[k].x - mg - n[k].x * mgn);
-        a.y += rs * (g[k].y - mg - n[k].y * mgn);
-        a.z += rs * (g[k].z - mg - n[k].z * mgn);
-        a.w += rs * (g[k].w - mg - n[k].w * mgn);
+        a.x += rs * (dv[k].x * ww.x - mg - n.x * mgn);
+        a.y += rs * (dv[k].y * ww.y - mg - n.y * mgn);
+        a.z += rs * (dv[k].z * ww.z - mg - n.z * mgn);
+        a.w += rs * (dv[k].w * ww.w - mg - n.w * mgn);
         *o = a;
         if (dxbf) {
           ushort4 hb;
@@ -132,34 +144,20 @@ __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
           hb.w = to_bf16_bits(a.w);
           *reinterpret_cast<ushort4*>(dxbf + (size_t)r * C + c) = hb;
         }
-        aw[k].x += d[k].x * n[k].x; aw[k].y += d[k].y * n[k].y;
-        aw[k].z += d[k].z * n[k].z; aw[k].w += d[k].w * n[k].w;
-        ab[k].x += d[k].x; ab[k].y += d[k].y; ab[k].z += d[k].z; ab[k].w += d[k].w;
+        *reinterpret_cast<float4*>(my + c) = make_float4(dv[k].x * n.x, dv[k].y * n.y, dv[k].z * n.z, dv[k].w * n.w);
+        *reinterpret_cast<float4*>(my + C + c) = dv[k];
+        if (with_dxsum) *reinterpret_cast<float4*>(my + 2 * C + c) = a;
       }
     }
+  } else {
+    for (int c = lane; c < nout * C; c += 32) my[c] = 0.f;
   }
-  // combine the warps' partials in warp order
-  for (int wv = 0; wv < LNB_WARPS; wv++) {
-    if (warp == wv) {
+  __syncthreads();
+  // column sums of the block's rows, in warp (= row) order
+  for (int c = threadIdx.x; c < nout * C; c += blockDim.x) {
+    float t = sh[c];
 #pragma unroll
-      for (int k = 0; k < LN_MAXV4; k++) {
-        int c = (lane + 32 * k) * 4;
-        if (c < C) {
-          float4* pw = reinterpret_cast<float4*>(sh + c);
-          float4* pb = reinterpret_cast<float4*>(sh + C + c);
-          if (wv == 0) {
-            *pw = aw[k];
-            *pb = ab[k];
-          } else {
-            float4 a = *pw, bb = *pb;
-            *pw = make_float4(a.x + aw[k].x, a.y + aw[k].y, a.z + aw[k].z, a.w + aw[k].w);
-            *pb = make_float4(bb.x + ab[k].x, bb.y + ab[k].y, bb.z + ab[k].z, bb.w + ab[k].w);
-          }
-        }
-      }
-    }
-    __syncthreads();
+    for (int wv = 1; wv < LNB_WARPS; wv++) t += sh[wv * nout * C + c];
+    partial[(size_t)blockIdx.x * nout * C + c] = t;
   }
-  for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) partial[(size_t)blockIdx.x * 2 * C + c] = sh[c];
 }
-

@@ -178,30 +178,33 @@ __global__ void col_partial_kernel(const float* __restrict__ Y, int M, int N, lo
 
 // Column sums of partial rows, finished in a fixed order:
 //   out[c] += sum_{r < nrows} partial[r][c]   for c < split   (out0)
-//   out1[c - split] += ...                    for c >= split  (out1)
-// (= instead of += when accumulate == 0).
-// One CTA of 8 warps per 32 columns: warp w sums rows w, w+8, ... (lane =
-// column, coalesced), then the 8 warp sums are added in warp order.
-__global__ void __launch_bounds__(256) col_finish_kernel(float* __restrict__ out0, float* __restrict__ out1, int split,
-                                                         const float* __restrict__ partial, int nrows, int ncols,
-                                                         int accumulate) {
+//   out1[c - split] += ...                    for split <= c < 2 split
+//   out2[c - 2 split] += ...                  for c >= 2 split
+// (= instead of += when accumulate == 0).  One CTA of 32 warps per 32
+// columns: warp w sums rows w, w+32, ... (lane = column, coalesced), then the
+// 32 warp sums are added in warp order.
+#define COLF_WARPS 32
+__global__ void __launch_bounds__(COLF_WARPS * 32) col_finish_kernel(float* __restrict__ out0, float* __restrict__ out1,
+                                                                     float* __restrict__ out2, int split,
+                                                                     const float* __restrict__ partial, int nrows,
+                                                                     int ncols, int accumulate) {
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ float sh[8][32];
+  __shared__ float sh[COLF_WARPS][33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * 32 + lane;
   float s = 0.f;
   if (c < ncols) {
 #pragma unroll 4
-    for (int r = warp; r < nrows; r += 8) s += partial[(size_t)r * ncols + c];
+    for (int r = warp; r < nrows; r += COLF_WARPS) s += partial[(size_t)r * ncols + c];
   }
   sh[warp][lane] = s;
   __syncthreads();
   if (warp == 0 && c < ncols) {
     float t = sh[0][lane];
 #pragma unroll
-    for (int w = 1; w < 8; w++) t += sh[w][lane];
-    float* o = c < split ? out0 + c : out1 + (c - split);
+    for (int w = 1; w < COLF_WARPS; w++) t += sh[w][lane];
+    float* o = c < split ? out0 + c : c < 2 * split ? out1 + (c - split) : out2 + (c - 2 * split);
     *o = accumulate ? *o + t : t;
   }
 }
