@@ -62,6 +62,25 @@ GPT2_DEV float gelu_fwd(float x) {
   return 0.5f * x * (1.0f + tanhf(u));
 }
 
+// The same with the hardware tanh approximation (tanh.approx.f32, relative
+// error about 2^-11): used where the result is rounded to bf16 anyway.
+GPT2_DEV float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+GPT2_DEV float gelu_fwd_fast(float x) {
+  float u = GELU_SQRT_2_OVER_PI * (x + GELU_COEF * x * x * x);
+  return 0.5f * x * (1.0f + tanh_fast(u));
+}
+
+GPT2_DEV float gelu_grad_fast(float x) {
+  float u = GELU_SQRT_2_OVER_PI * (x + GELU_COEF * x * x * x);
+  float th = tanh_fast(u);
+  return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * GELU_SQRT_2_OVER_PI * (1.0f + 3.0f * GELU_COEF * x * x);
+}
+
 GPT2_DEV float gelu_grad(float x) {
   float u = GELU_SQRT_2_OVER_PI * (x + GELU_COEF * x * x * x);
   float th = tanhf(u);

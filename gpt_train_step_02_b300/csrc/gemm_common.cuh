@@ -30,6 +30,7 @@ struct EpiArgs {
   int vec4;  // every pointer 16-byte aligned and every leading dimension a multiple of 4 (8 for Cbf)
   uint16_t* Cbf;  // optional bf16 copy of the output
   long long ldcbf;
+  int fast;       // GELU / GELU' through the hardware tanh approximation (bf16 products)
 };
 
 GPT2_DEV void epi_store(const EpiArgs& e, int i, int j, float acc) {
@@ -41,10 +42,14 @@ GPT2_DEV void epi_store(const EpiArgs& e, int i, int j, float acc) {
     case EPI_BIAS_GELU: {
       float h = acc + e.bias[j];
       e.pre[(size_t)i * e.ldpre + j] = h;
-      out = gelu_fwd(h);
+      out = e.fast ? gelu_fwd_fast(h) : gelu_fwd(h);
       break;
     }
-    case EPI_DGELU: out = acc * gelu_grad(e.R[(size_t)i * e.ldr + j]); break;
+    case EPI_DGELU: {
+      const float r = e.R[(size_t)i * e.ldr + j];
+      out = acc * (e.fast ? gelu_grad_fast(r) : gelu_grad(r));
+      break;
+    }
     case EPI_ACCUM: out = e.C[ci] + acc; break;
     default: out = acc;
   }
@@ -78,12 +83,19 @@ GPT2_DEV void epi_apply4(const EpiArgs& e, int i, int j, float4 acc, float4 b, f
     case EPI_BIAS_GELU: {
       float4 h = make_float4(acc.x + b.x, acc.y + b.y, acc.z + b.z, acc.w + b.w);
       st4(e.pre + (size_t)i * e.ldpre + j, h);
-      o = make_float4(gelu_fwd(h.x), gelu_fwd(h.y), gelu_fwd(h.z), gelu_fwd(h.w));
+      if (e.fast)
+        o = make_float4(gelu_fwd_fast(h.x), gelu_fwd_fast(h.y), gelu_fwd_fast(h.z), gelu_fwd_fast(h.w));
+      else
+        o = make_float4(gelu_fwd(h.x), gelu_fwd(h.y), gelu_fwd(h.z), gelu_fwd(h.w));
       break;
     }
     case EPI_DGELU:
-      o = make_float4(acc.x * gelu_grad(in.x), acc.y * gelu_grad(in.y), acc.z * gelu_grad(in.z),
-                      acc.w * gelu_grad(in.w));
+      if (e.fast)
+        o = make_float4(acc.x * gelu_grad_fast(in.x), acc.y * gelu_grad_fast(in.y), acc.z * gelu_grad_fast(in.z),
+                        acc.w * gelu_grad_fast(in.w));
+      else
+        o = make_float4(acc.x * gelu_grad(in.x), acc.y * gelu_grad(in.y), acc.z * gelu_grad(in.z),
+                        acc.w * gelu_grad(in.w));
       break;
     case EPI_ACCUM: o = make_float4(in.x + acc.x, in.y + acc.y, in.z + acc.z, in.w + acc.w); break;
     default: break;

@@ -433,12 +433,15 @@ static void launch_bf16_kernel(const CUtensorMap& ta, const CUtensorMap& tb, con
   launch_k(tcb::gemm_bf16_kernel<BN>, grid, tcb::THREADS, tcb::Cfg<BN>::SMEM_BYTES, s, ta, tb, p);
 }
 
-// Launches the persistent bf16 tensor-core matmul.  Output tiles are 128 x 256
-// (128 x 128 when N <= 128).  Returns 1, or -1 on a host-side failure.
+// Launches the persistent bf16 tensor-core matmul.  Returns 1, or -1 on a
+// host-side failure.
 static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int* err, cudaStream_t s,
                               long long ws_floats = SPLITK_WS_FLOATS) {
   if (!d.Abf || !d.Bbf) return -1;
-  const int BN = d.N > 128 ? 256 : 128;
+  // 128 x 256 tiles when they alone fill the SMs; otherwise 128 x 128 tiles,
+  // which halve the K splits (and their partial-tile traffic) needed to fill them
+  const long long tiles256 = (long long)ceil_div(d.M, tcb::BM) * ceil_div(d.N, 256);
+  const int BN = (d.N > 128 && tiles256 >= 148) ? 256 : 128;
   CUtensorMap ta, tb;
   if (!make_bf16_map(&ta, d.Abf, d.a_kmajor, d.a_kmajor ? d.M : d.K, d.a_kmajor ? d.K : d.M, d.lda, tcb::BM))
     return -1;
@@ -456,6 +459,7 @@ static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int
   p.tiles_n = ceil_div(d.N, BN);
   p.units = p.tiles_m * p.tiles_n * p.splits;
   p.epi = d.epi;
+  p.epi.fast = 1;  // bf16 outputs: GELU through the hardware tanh approximation
   p.partial = p.splits > 1 ? ws : nullptr;
   p.tile_ctr = tile_ctr;
   p.err = err;
@@ -483,7 +487,7 @@ static EpiArgs epi_args(float* C, long long ldc, int epi, const float* bias = nu
                         long long ldcbf = 0) {
   EpiArgs e;
   e.C = C; e.ldc = ldc; e.bias = bias; e.R = R; e.ldr = ldr; e.pre = pre; e.ldpre = ldpre; e.epi = epi;
-  e.Cbf = Cbf; e.ldcbf = ldcbf;
+  e.Cbf = Cbf; e.ldcbf = ldcbf; e.fast = 0;
   uintptr_t addr = (uintptr_t)C | (uintptr_t)bias | (uintptr_t)R | (uintptr_t)pre | (uintptr_t)Cbf;
   e.vec4 = (addr & 15) == 0 && (ldc & 3) == 0 && (ldr & 3) == 0 && (ldpre & 3) == 0 && (ldcbf & 7) == 0;
   return e;
@@ -855,7 +859,7 @@ static int enqueue_backward(gpt2_t* m) {
   size_t smem = 1;
   while ((int)smem < N) smem <<= 1;
   launch_k(sort_tokens_kernel, 1, 1024, smem * sizeof(uint32_t), s, m->tokens, N, c.vocab_size, m->sorted);
-  launch_k(wte_grad_kernel, dim3(N, ceil_div(C, 128)), 32, 0, s, G[P_WTE], m->dres, m->sorted, N, C);
+  launch_k(wte_grad_kernel, dim3(N, ceil_div(C, 128)), WTE_WARPS * 32, 0, s, G[P_WTE], m->dres, m->sorted, N, C);
   launch_k(wpe_grad_kernel, grid_for((long long)T * C / 4, 256), 256, 0, s, G[P_WPE], m->dres, B, T, C,
            m->grad_accumulate);
   m->launches += 3;

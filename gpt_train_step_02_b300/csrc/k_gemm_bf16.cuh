@@ -14,14 +14,16 @@
 // transpose bits).
 //
 // Work unit = (128 x BN output tile, K split); a CTA walks the units
-// blockIdx.x, blockIdx.x + gridDim.x, ...  Six warps:
+// blockIdx.x, blockIdx.x + gridDim.x, ...  Ten warps:
 //   warp 0      one lane issues the TMA loads into a STAGES-deep ring
 //   warp 1      allocates TMEM; one lane issues the MMAs (K = 16 per
 //               instruction, four per 64-wide K tile) into one of two TMEM
 //               accumulators, so the epilogue of unit u overlaps the MMAs of
 //               unit u + 1
-//   warps 2..5  epilogue: tcgen05.ld TMEM -> registers -> fused epilogue ->
-//               global; K-split units hand off through partial tiles and an
+//   warps 2..9  epilogue (two warps per TMEM lane quadrant, half the
+//               columns each): tcgen05.ld TMEM -> registers -> shared-memory
+//               transpose -> fused epilogue -> coalesced global stores; K-split
+//               units hand off through partial tiles and an
 //               arrival counter, the last unit to arrive reducing in split
 //               order (deterministic).
 // Shared-memory layouts (128-byte swizzle, as TMA writes them):
@@ -59,14 +61,15 @@ using tc::tmem_ld32;
 constexpr int BM = 128;
 constexpr int BK = 64;  // bf16 elements per K tile: 128 bytes, one swizzle row
 constexpr int UMMA_K = 16;
-constexpr int EPI_THREADS = 128;  // four epilogue warps, one per TMEM lane quadrant
+constexpr int EPI_WARPS = 8;  // epilogue warps: two per TMEM lane quadrant, each finishing half the columns
+constexpr int EPI_THREADS = 32 * EPI_WARPS;
 constexpr int THREADS = 64 + EPI_THREADS;
 constexpr int MN_BOX = 64;                   // MN extent of one MN-major TMA box
 constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;  // 8 KB
 
 template <int BN>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int STAGES = BN == 256 ? 3 : 5;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -74,8 +77,9 @@ struct Cfg {
   // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], mma_done
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int OFF_EPI = (OFF_MISC + 64 + 15) / 16 * 16;  // four warps' epilogue staging
-  static constexpr int SMEM_BYTES = OFF_EPI + 4 * EPI_STAGE_FLOATS * 4 + 1024;  // + alignment slack
+  static constexpr int OFF_EPI = (OFF_MISC + 64 + 15) / 16 * 16;  // the epilogue warps' staging
+  static constexpr int SMEM_BYTES = OFF_EPI + EPI_WARPS * EPI_STAGE_FLOATS * 4 + 1024;  // + alignment slack
+  static_assert(SMEM_BYTES <= 232448, "227 KB of shared memory per CTA");
   static constexpr int TMEM_COLS = 2 * BN;                  // two accumulators
 };
 
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 128);
+      mbar_init(&acc_empty[b], EPI_THREADS);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -259,8 +263,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ---------------- epilogue ----------------
-    const int t = threadIdx.x - 64;  // 0..127
-    const int q = warp & 3;          // TMEM lane quadrant this warp may access
+    const int t = threadIdx.x - 64;          // 0 .. EPI_THREADS-1
+    const int q = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) / 4;         // which half of the BN columns this warp finishes
     int lu = 0;
     for (int unit = blockIdx.x; unit < p.units; unit += gridDim.x, lu++) {
       int m0, tn, z, tile;
@@ -268,8 +273,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int n0 = tn * BN;
       const int buf = lu & 1;
       bool ok = mbar_wait(&acc_full[buf], (lu >> 1) & 1, abort_flag, p.err);
-      // one decision for all four warps (tcgen05.ld is warp-collective and
-      // the split-K hand-off uses a barrier over these 128 threads)
+      // one decision for all epilogue warps (tcgen05.ld is warp-collective
+      // and the split-K hand-off uses a barrier over these threads)
       tc::epi_bar<EPI_THREADS>();
       if (t == 0) *go_flag = (ok && !*abort_flag) ? 1 : 0;
       tc::epi_bar<EPI_THREADS>();
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int i0 = m0 + q * 32;  // this warp's 32 rows
       const uint32_t tbase = tmem + (uint32_t)(buf * BN) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int cc = 0; cc < BN / 32; cc++) {
+      for (int cc = half * (BN / 64); cc < (half + 1) * (BN / 64); cc++) {
         float v[32];
         tmem_ld32(tbase + (uint32_t)(cc * 32), v);
         const int j0 = n0 + cc * 32;
@@ -303,7 +308,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           __threadfence();
           const int ew = warp - 2;
           const size_t plane = (size_t)p.M * p.N;
-          for (int r = ew; r < BM && m0 + r < p.M; r += 4) {
+          for (int r = ew; r < BM && m0 + r < p.M; r += EPI_WARPS) {
             const int ii = m0 + r;
             for (int jj = 4 * lane; jj < BN; jj += 128) {
               const int j = n0 + jj;

@@ -77,7 +77,7 @@ __global__ void encoder_fwd_kernel(float* __restrict__ x, const int* __restrict_
 //  1. sort_tokens_kernel: one CTA bitonic-sorts the keys (id << 14 | pos),
 //     which groups positions by id and keeps them in position order.
 //  2. wte_grad_kernel: the CTA at the first key of each id sums that id's
-//     gradient rows in position order and adds the sum to dwte[id] once.
+//     gradient rows in a fixed order and adds the sum to dwte[id] once.
 //  3. wpe_grad_kernel: dwpe[t] += sum over b of dx[b,t].
 // Limits: B*T <= 16384 and V <= 65536 (keys fit 30 bits).
 // ---------------------------------------------------------------------------
@@ -114,25 +114,57 @@ __global__ void __launch_bounds__(1024) sort_tokens_kernel(const int* __restrict
   for (int i = threadIdx.x; i < n; i += blockDim.x) sorted[i] = keys[i];
 }
 
-// grid: (n, ceil(C/128)); block: 32 threads, one float4 of channels each.
-__global__ void wte_grad_kernel(float* __restrict__ dwte, const float* __restrict__ dx,
-                                const uint32_t* __restrict__ sorted, int n, int C) {
+// grid: (n, ceil(C/128)); block: WTE_WARPS warps; lane l owns channels
+// 4*(blockIdx.y*32 + l) .. +3.  The block at the first sorted key of an id
+// finds the end of that id's run (256 keys per step, the first key of another
+// id taken with atomicMin, which does not depend on order), then warp w sums
+// the run's rows w, w + WTE_WARPS, ... in order and the warp sums are added
+// in warp order: a fixed summation order for any run length.
+#define WTE_WARPS 8
+__global__ void __launch_bounds__(WTE_WARPS * 32) wte_grad_kernel(float* __restrict__ dwte, const float* __restrict__ dx,
+                                                                  const uint32_t* __restrict__ sorted, int n, int C) {
   pdl_launch_dependents();
   pdl_wait();
-  int i = blockIdx.x;
-  uint32_t id = sorted[i] >> 14;
-  if (i > 0 && (sorted[i - 1] >> 14) == id) return;
-  int c = (blockIdx.y * 32 + threadIdx.x) * 4;
-  if (c >= C) return;
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = i; j < n && (sorted[j] >> 14) == id; j++) {
-    int pos = (int)(sorted[j] & 0x3FFFu);
-    float4 g = *reinterpret_cast<const float4*>(dx + (size_t)pos * C + c);
-    s.x += g.x; s.y += g.y; s.z += g.z; s.w += g.w;
+  __shared__ int s_end;
+  __shared__ float4 s_part[WTE_WARPS][32];
+  const int i = blockIdx.x;
+  const uint32_t id = sorted[i] >> 14;
+  if (i > 0 && (sorted[i - 1] >> 14) == id) return;  // not the first key of its id (block-uniform)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) s_end = n;
+  __syncthreads();
+  for (int base = i;; base += WTE_WARPS * 32) {
+    const int j = base + threadIdx.x;
+    if (j < n && (sorted[j] >> 14) != id) atomicMin(&s_end, j);
+    __syncthreads();
+    const int e = s_end;
+    __syncthreads();
+    if (e < base + WTE_WARPS * 32 || base + WTE_WARPS * 32 >= n) break;
   }
-  float4* d = reinterpret_cast<float4*>(dwte + (size_t)id * C + c);
-  float4 o = *d;
-  *d = make_float4(o.x + s.x, o.y + s.y, o.z + s.z, o.w + s.w);
+  const int end = s_end;
+  const int c = (blockIdx.y * 32 + lane) * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (c < C) {
+#pragma unroll 4
+    for (int j = i + warp; j < end; j += WTE_WARPS) {
+      const int pos = (int)(sorted[j] & 0x3FFFu);
+      const float4 g = *reinterpret_cast<const float4*>(dx + (size_t)pos * C + c);
+      acc.x += g.x; acc.y += g.y; acc.z += g.z; acc.w += g.w;
+    }
+  }
+  s_part[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && c < C) {
+    float4 t = s_part[0][lane];
+#pragma unroll
+    for (int w = 1; w < WTE_WARPS; w++) {
+      const float4 u = s_part[w][lane];
+      t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+    }
+    float4* d = reinterpret_cast<float4*>(dwte + (size_t)id * C + c);
+    const float4 o = *d;
+    *d = make_float4(o.x + t.x, o.y + t.y, o.z + t.z, o.w + t.w);
+  }
 }
 
 // accumulate = 0 stores the sums instead of adding them (the fused training
