@@ -368,6 +368,50 @@ def roofline_for(kind, k, peaks, w):
             "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(kind, w), "peak_source": peaks["source"]}
 
 
+TRAFFIC_KERNELS = {"gemm": ("gemm_tf32x3_kernel", "gemm_bf16_kernel")}
+BYTE_UNITS = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+
+
+def record_traffic(csv_path, w, kind="gemm"):
+    """Average DRAM bytes (read + write) per launch of one kernel class, from
+    an ncu capture of the launches of whole steps of workload w
+    (``--metrics dram__bytes_read.sum,dram__bytes_write.sum --csv``), stored
+    in profiles/roofline_traffic.json with the hash of the kernel sources it
+    was taken on.  Every step launches the same sequence, so any run of one
+    step's launch count covers each launch of a step once."""
+    import csv as _csv
+
+    rows = list(_csv.DictReader(l for l in open(csv_path) if not l.startswith("==")))
+    launches = {}
+    for r in rows:
+        name = r["Kernel Name"]
+        if not any(k in name for k in TRAFFIC_KERNELS[kind]):
+            continue
+        m = r["Metric Name"]
+        if m not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        v = float(r["Metric Value"].replace(",", "")) * BYTE_UNITS[r["Metric Unit"]]
+        launches.setdefault(int(r["ID"]), {})[m] = v
+    full = [d for d in launches.values() if len(d) == 2]
+    if not full:
+        print(f"no {kind} launches with both DRAM metrics in {csv_path}", file=sys.stderr)
+        return 1
+    per_launch = sum(d["dram__bytes_read.sum"] + d["dram__bytes_write.sum"] for d in full) / len(full)
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    data = json.load(open(path)) if os.path.exists(path) else {}
+    data.setdefault(w.name, {})[kind] = {
+        "dram_bytes_per_launch": per_launch,
+        "launches_captured": len(full),
+        "source_sha": kernel_source_sha(kind),
+        "capture": os.path.basename(csv_path),
+    }
+    with open(path, "w") as fh:
+        json.dump(data, fh, indent=1, sort_keys=True)
+        fh.write("\n")
+    print(json.dumps({"workload": w.name, "kind": kind, "dram_bytes_per_launch": per_launch, "launches": len(full)}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -377,9 +421,13 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--record-traffic", metavar="NCU_CSV",
+                    help="store the DRAM bytes per matmul launch of an ncu capture of --workload and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     w = synth.WORKLOADS[args.workload]
+    if args.record_traffic:
+        return record_traffic(args.record_traffic, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -135,7 +135,7 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->datty = take(BT * C * F);
   p->dqkv = take(BT * 3 * C * F);
   p->dfch = take(BT * 4 * C * F);
-  p->attD = take(BT * NH * F);
+  p->attD = take(2 * BT * NH * F);  // D, or the (-lse log2 e, D) pairs of the tensor-core path
   // scratch: column-sum partials (<= ceil(BT/BIAS_MIN_ROWS) x 4C) and
   // layernorm partials (<= ceil(BT/LNB_MIN_ROWS) x 3C)
   size_t s1 = ((BT + BIAS_MIN_ROWS - 1) / BIAS_MIN_ROWS) * 4 * C;
@@ -613,18 +613,21 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
                            int C, int NH, int bf, int* err, cudaStream_t s) {
   const int hs = C / NH;
   const int grid = ceil_div((long long)B * NH * T * 32, 256);
-  launch_k(attn_bwd_D_kernel, grid, 256, 0, s, D, dy, atty, B, T, C, NH);
-  if (bf && qkv_bf && dy_bf && hs == tca::HS && T % tca::BQ == 0) {
+  const bool tc_path = bf && qkv_bf && dy_bf && hs == tca::HS && T % tca::BQ == 0;
+  // D holds 2 B NH T floats: the (-lse log2 e, D) pairs of the tensor-core path
+  launch_k(attn_bwd_D_kernel, grid, 256, 0, s, tc_path ? nullptr : D, tc_path ? (float2*)D : nullptr, lse, dy, atty,
+           B, T, C, NH);
+  if (tc_path) {
     CUtensorMap tq, td;
     if (!make_bf16_map(&tq, qkv_bf, 1, (long long)B * T, 3LL * C, 3LL * C, tca::BQ)) return -1;
     if (!make_bf16_map(&td, dy_bf, 1, (long long)B * T, C, C, tca::BQ)) return -1;
     tca::BwdParams p;
     p.B = B; p.T = T; p.C = C; p.NH = NH;
     p.scale = 1.0f / sqrtf((float)hs);
-    p.lse = lse; p.D = D; p.dqkv = dqkv; p.dqkv_bf = dqkv_bf; p.err = err;
+    p.LD = (const float2*)D; p.dqkv = dqkv; p.dqkv_bf = dqkv_bf; p.err = err;
     dim3 g(T / tca::BQ, NH, B);
-    launch_k(tca::attn_bwd_dkv_tc_kernel, g, tca::THREADS, tca::dkv::SMEM_BYTES, s, tq, td, p);
-    launch_k(tca::attn_bwd_dq_tc_kernel, g, tca::THREADS, tca::dqk::SMEM_BYTES, s, tq, td, p);
+    launch_k(tca::attn_bwd_dkv_tc_kernel, g, tca::BWD_THREADS, tca::dkv::SMEM_BYTES, s, tq, td, p);
+    launch_k(tca::attn_bwd_dq_tc_kernel, g, tca::BWD_THREADS, tca::dqk::SMEM_BYTES, s, tq, td, p);
     return 3;
   }
   const dim3 g(ceil_div(T, ATT_ROWS), NH, B);
@@ -1442,11 +1445,11 @@ EXPORT int gpt2op_attention_forward(float* y, float* lse, const float* qkv, int 
   return op_status(w, s);
 }
 
-// attention backward: workspace = [error word][bf16 qkv][bf16 dy][y][lse][D]
+// attention backward: workspace = [error word][bf16 qkv][bf16 dy][y][lse][D, or (-lse log2 e, D) pairs]
 EXPORT size_t gpt2op_attention_backward_workspace_bytes(int B, int T, int C, int NH) {
   if (B < 1 || T < 1 || C < 1 || NH < 1) return 0;
   size_t n = (size_t)B * T;
-  return 256 + al256(n * 3 * C * 2) + al256(n * C * 2) + al256(n * C * 4) + 2 * al256(n * NH * 4);
+  return 256 + al256(n * 3 * C * 2) + al256(n * C * 2) + al256(n * C * 4) + al256(n * NH * 4) + al256(n * NH * 8);
 }
 
 EXPORT int gpt2op_attention_backward(float* dqkv, const float* dy, const float* qkv, int B, int T, int C, int NH,

@@ -142,9 +142,11 @@ __global__ void __launch_bounds__(ATT_ROWS * 32)
   if (lane == 0) lse[((size_t)b * NH + h) * T + t] = m + logf(l);
 }
 
-// D[b,h,t] = sum_d dy[b,t,h,d] * y[b,t,h,d]
-__global__ void attn_bwd_D_kernel(float* __restrict__ D, const float* __restrict__ dy, const float* __restrict__ y,
-                                  int B, int T, int C, int NH) {
+// D[b,h,t] = sum_d dy[b,t,h,d] * y[b,t,h,d], into D and/or, for the tensor-core
+// kernels, as the pair LD[b,h,t] = (-lse[b,h,t] log2 e, D[b,h,t]).
+__global__ void attn_bwd_D_kernel(float* __restrict__ D, float2* __restrict__ LD, const float* __restrict__ lse,
+                                  const float* __restrict__ dy, const float* __restrict__ y, int B, int T, int C,
+                                  int NH) {
   pdl_launch_dependents();
   pdl_wait();
   int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -156,7 +158,11 @@ __global__ void attn_bwd_D_kernel(float* __restrict__ D, const float* __restrict
   float s = 0.f;
   for (int d = lane; d < hs; d += 32) s += dy[off + d] * y[off + d];
   s = warp_sum(s);
-  if (lane == 0) D[((size_t)b * NH + h) * T + t] = s;
+  if (lane == 0) {
+    const size_t i = ((size_t)b * NH + h) * T + t;
+    if (D) D[i] = s;
+    if (LD) LD[i] = make_float2(-lse[i] * 1.4426950408889634f, s);
+  }
 }
 
 // dq for 8 query rows per CTA; keys and values stream through shared memory.

@@ -44,6 +44,53 @@ using tc::tmem_ld32;
 using tcb::desc_sw128;
 using tcb::mma_bf16;
 
+// ---- softmax arithmetic, one PTX instruction each ----
+// 2^x on the special-function unit (relative error near 2^-22; 2^-inf = 0;
+// subnormal results flush to zero, far below what a bf16 weight resolves).
+GPT2_DEV float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// (a.x b.x + c.x, a.y b.y + c.y) as one paired fp32 fused multiply-add
+GPT2_DEV float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n mov.b64 rc, {%5, %6};\n"
+      " fma.rn.f32x2 %0, ra, rb, rc;\n}"
+      : "=l"(d)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+// lo and hi rounded to bf16 (nearest even) and packed, lo in the low half
+GPT2_DEV uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+GPT2_DEV float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// 64 consecutive fp32 TMEM columns of the warp's 32 lanes (one per thread)
+GPT2_DEV void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; i++) v[i] = __uint_as_float(r[i]);
+}
+// v[k] = -inf for every k > lim (the keys after the query on the diagonal tile)
+GPT2_DEV void mask_after(float* v, int lim) {
+#pragma unroll
+  for (int k = 0; k < 64; k++)
+    if (k > lim) v[k] = -INFINITY;
+}
+
 constexpr int BQ = 128;   // queries per CTA
 constexpr int BKV = 128;  // keys per tile
 constexpr int HS = 64;    // head size
@@ -157,15 +204,18 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // Order per key tile j: wait for P_j (the softmax warps have also read
+    // S_j out of TMEM by then), issue S_{j+1} = Q K_{j+1}^T into the freed S
+    // columns, then O_j = P_j V_j.  The softmax warps get S_{j+1} while
+    // P_j V_j is still running.
     if (lane == 0) {
-      const uint32_t sq = smem_u32(smem + OFF_Q), sp = smem_u32(smem + OFF_P);
+      const uint32_t sq = smem_u32(smem + OFF_Q), sp = smem_u32(smem + OFF_P), sv = smem_u32(smem + OFF_V);
       const uint32_t t_s = tmem, t_pv = tmem + 128;
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
-      for (int j = 0; j < nkt && ok; j++) {
+      auto issue_s = [&](int j) -> bool {
         const int s = j & 1;
-        if (!mbar_wait(&k_full[s], (j >> 1) & 1, abort_flag, p.err)) break;
+        if (!mbar_wait(&k_full[s], (j >> 1) & 1, abort_flag, p.err)) return false;
         tc_fence_after();
-        const uint32_t sk = smem_u32(smem + OFF_K + s * TILE_BYTES), sv = smem_u32(smem + OFF_V);
+        const uint32_t sk = smem_u32(smem + OFF_K + s * TILE_BYTES);
         // S = Q K^T over the 64 head dims (four K = 16 steps along the 128-byte rows)
 #pragma unroll
         for (int kk = 0; kk < HS / 16; kk++)
@@ -173,13 +223,19 @@ __global__ void __launch_bounds__(THREADS, 2)
                    kk > 0 ? 1u : 0u);
         mma_commit(s_full);
         mma_commit(&k_empty[s]);
-        // P (written by the softmax warps) times V over the 128 keys
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.err) && issue_s(0);
+      for (int j = 0; j < nkt && ok; j++) {
         if (!mbar_wait(p_full, j & 1, abort_flag, p.err)) break;
+        tc_fence_after();
+        if (j + 1 < nkt && !issue_s(j + 1)) break;
         if (!mbar_wait(v_full, j & 1, abort_flag, p.err)) break;
         tc_fence_after();
+        // P (two 64-key chunks, K-major) times V (MN-major) over the 128 keys
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; kk++) {
-          const uint32_t pa = sp + (kk >> 2) * TILE_BYTES + (kk & 3) * 32;  // two 64-key chunks
+          const uint32_t pa = sp + (kk >> 2) * TILE_BYTES + (kk & 3) * 32;
           mma_bf16(t_pv, desc_sw128(pa, 16, 1024), desc_sw128(sv + kk * 2048, 8192, 1024), IDESC_PV,
                    kk > 0 ? 1u : 0u);
         }
@@ -191,82 +247,97 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
   } else {
     // ---------------- softmax + output: one query row per thread ----------------
+    // Scores are kept in base 2: x = s * scale * log2(e), m = running max of x,
+    // P = 2^(x - m), l = running sum of the bf16-rounded P (the weights the
+    // P V product uses), O accumulated in registers in the basis of m.
+    // Tile j: (1) row max of S_j; (2) fold in P_{j-1} V_{j-1}, rescaled by the
+    // correction of tile j-1, which also frees the P buffer; (3) write P_j.
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;  // row within the tile = TMEM lane
-    const int t = qt * BQ + r;     // query position
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t t_s = tmem + lane_off, t_pv = tmem + 128 + lane_off;
     const float sl2 = p.scale * 1.4426950408889634f;  // scale * log2(e)
+    const float2 sl2v = make_float2(sl2, sl2);
     float o[HS];
 #pragma unroll
     for (int d = 0; d < HS; d++) o[d] = 0.f;
-    float mrow = -INFINITY, lrow = 0.f;  // running max (of scaled scores) and sum
+    float m2 = -INFINITY, lrow = 0.f, corr_prev = 0.f;
     bool ok = true;
     uint8_t* prow = smem + OFF_P + r * 128;
+    auto fold_pv = [&](float corr) {
+      float pv[HS];
+      tmem_ld64(t_pv, pv);
+#pragma unroll
+      for (int d = 0; d < HS; d += 2) {
+        const float2 u = fma2(make_float2(o[d], o[d + 1]), make_float2(corr, corr), make_float2(pv[d], pv[d + 1]));
+        o[d] = u.x;
+        o[d + 1] = u.y;
+      }
+    };
     for (int j = 0; j < nkt; j++) {
       if (!tc::epi_bar_and<128>(mbar_wait(s_full, j & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool diag = j == qt;
-      const int kbase = j * BKV - t;  // key k of this tile lies after the query when kbase + k > 0
-      // pass 1: row max of this tile's scores (TMEM read in 32-column chunks)
-      float mt = -INFINITY;
+      const bool diag = j == qt;  // keys k > r of the diagonal tile follow the query
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-      for (int c = 0; c < BKV / 32; c++) {
-        float sv[32];
-        tmem_ld32(tmem + lane_off + c * 32, sv);
+      for (int c = 0; c < BKV / 64; c++) {
+        float sv[64];
+        tmem_ld64(t_s + c * 64, sv);
+        if (diag) mask_after(sv, r - c * 64);
 #pragma unroll
-        for (int k = 0; k < 32; k++)
-          if (!diag || kbase + c * 32 + k <= 0) mt = fmaxf(mt, sv[k]);
+        for (int k = 0; k < 64; k += 8) {
+          mx[0] = max3(mx[0], sv[k], sv[k + 1]);
+          mx[1] = max3(mx[1], sv[k + 2], sv[k + 3]);
+          mx[2] = max3(mx[2], sv[k + 4], sv[k + 5]);
+          mx[3] = max3(mx[3], sv[k + 6], sv[k + 7]);
+        }
       }
-      const float mnew = fmaxf(mrow, mt * p.scale);
-      const float corr = exp2f((mrow - mnew) * 1.4426950408889634f);  // 0 on the first tile
-      const float mb = mnew * 1.4426950408889634f;
-      float lsum = 0.f;
-      // pass 2: P = exp(s*scale - mnew) as bf16 into the swizzled K-major P
-      // tile (two 64-key chunks of 16 KB; 16-byte groups XOR-swizzled by row)
+      const float mnew = fmaxf(m2, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
+      const float corr = ex2(m2 - mnew);  // 0 on the first tile (m2 = -inf)
+      if (j > 0) {
+        if (!tc::epi_bar_and<128>(mbar_wait(pv_full, (j - 1) & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        fold_pv(corr_prev);
+      }
+      const float2 nm = make_float2(-mnew, -mnew);
+      float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll 1
-      for (int c = 0; c < BKV / 32; c++) {
-        float sv[32];
-        tmem_ld32(tmem + lane_off + c * 32, sv);
+      for (int c = 0; c < BKV / 64; c++) {
+        float sv[64];
+        tmem_ld64(t_s + c * 64, sv);
+        if (diag) mask_after(sv, r - c * 64);
 #pragma unroll
-        for (int g = 0; g < 4; g++) {
+        for (int g = 0; g < 8; g++) {  // 8 keys = one 16-byte group of the swizzled row
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; e++) {
             const int k = g * 8 + 2 * e;
-            const bool m0 = diag && kbase + c * 32 + k > 0, m1 = diag && kbase + c * 32 + k + 1 > 0;
-            float p0 = m0 ? 0.f : exp2f(sv[k] * sl2 - mb), p1 = m1 ? 0.f : exp2f(sv[k + 1] * sl2 - mb);
-            uint16_t h0 = to_bf16_bits(p0), h1 = to_bf16_bits(p1);
-            // the row sum uses the bf16-rounded weights that the PV product uses
-            lsum += __uint_as_float((uint32_t)h0 << 16) + __uint_as_float((uint32_t)h1 << 16);
-            w[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+            const float2 x = fma2(make_float2(sv[k], sv[k + 1]), sl2v, nm);
+            w[e] = cvt_bf16x2(ex2(x.x), ex2(x.y));
+            ls0 += __uint_as_float(w[e] << 16);
+            ls1 += __uint_as_float(w[e] & 0xffff0000u);
           }
-          const int key16 = c * 4 + g;  // 16-byte group of 8 keys, 0..15
-          const int chunk = key16 >> 3, grp = key16 & 7;
-          *reinterpret_cast<uint4*>(prow + chunk * TILE_BYTES + ((grp ^ (r & 7)) << 4)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(prow + c * TILE_BYTES + ((g ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      lrow = lrow * corr + lsum;
-      mrow = mnew;
+      lrow = lrow * corr + (ls0 + ls1);
+      m2 = mnew;
+      corr_prev = corr;
       // make the generic-proxy P writes visible to the tensor core
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive(p_full);
-      if (!tc::epi_bar_and<128>(mbar_wait(pv_full, j & 1, abort_flag, p.err))) {
-        ok = false;
-        break;
-      }
+    }
+    ok = tc::epi_bar_and<128>(ok && mbar_wait(pv_full, (nkt - 1) & 1, abort_flag, p.err));
+    if (ok) {
       tc_fence_after();
-#pragma unroll
-      for (int hh = 0; hh < HS / 32; hh++) {
-        float pv[32];
-        tmem_ld32(tmem + 128 + lane_off + hh * 32, pv);
-#pragma unroll
-        for (int d = 0; d < 32; d++) o[hh * 32 + d] = o[hh * 32 + d] * corr + pv[d];
-      }
+      fold_pv(corr_prev);
     }
     if (tc::epi_bar_and<128>(ok && !*abort_flag)) {
       const float inv = 1.f / lrow;
@@ -276,16 +347,13 @@ __global__ void __launch_bounds__(THREADS, 2)
         *reinterpret_cast<float4*>(p.y + yo + d) = make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
       if (p.ybf) {
 #pragma unroll
-        for (int d = 0; d < HS; d += 8) {
-          uint4 w;
-          w.x = (uint32_t)to_bf16_bits(o[d] * inv) | ((uint32_t)to_bf16_bits(o[d + 1] * inv) << 16);
-          w.y = (uint32_t)to_bf16_bits(o[d + 2] * inv) | ((uint32_t)to_bf16_bits(o[d + 3] * inv) << 16);
-          w.z = (uint32_t)to_bf16_bits(o[d + 4] * inv) | ((uint32_t)to_bf16_bits(o[d + 5] * inv) << 16);
-          w.w = (uint32_t)to_bf16_bits(o[d + 6] * inv) | ((uint32_t)to_bf16_bits(o[d + 7] * inv) << 16);
-          *reinterpret_cast<uint4*>(p.ybf + yo + d) = w;
-        }
+        for (int d = 0; d < HS; d += 8)
+          *reinterpret_cast<uint4*>(p.ybf + yo + d) =
+              make_uint4(cvt_bf16x2(o[d] * inv, o[d + 1] * inv), cvt_bf16x2(o[d + 2] * inv, o[d + 3] * inv),
+                         cvt_bf16x2(o[d + 4] * inv, o[d + 5] * inv), cvt_bf16x2(o[d + 6] * inv, o[d + 7] * inv));
       }
-      p.lse[((size_t)b * p.NH + h) * p.T + t] = mrow + logf(lrow);
+      // log-sum-exp of the scaled scores: (m2 + log2 l) ln 2
+      p.lse[((size_t)b * p.NH + h) * p.T + qt * BQ + r] = m2 * 0.6931471805599453f + logf(lrow);
     }
   }
 
@@ -298,7 +366,75 @@ __global__ void __launch_bounds__(THREADS, 2)
 }
 
 
-// ---------------------------------------------------------------------------
+struct BwdParams {
+  int B, T, C, NH;
+  float scale;
+  const float2* LD;  // (B, NH, T) pairs (-lse * log2 e, D)
+  float* dqkv;       // (B, T, 3C) fp32
+  uint16_t* dqkv_bf; // (B, T, 3C) bf16 copy, or NULL
+  int* err;
+};
+
+constexpr int BWD_THREADS = 320;  // producer warp, MMA warp, 8 softmax warps
+constexpr int SUB = 64;           // queries (dK/dV) or keys (dQ) per sub-tile
+
+// (a.x + b.x, a.y + b.y) and (a.x b.x, a.y b.y), one paired instruction each
+GPT2_DEV float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n add.rn.f32x2 %0, ra, rb;\n}"
+      : "=l"(d)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+GPT2_DEV float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n mul.rn.f32x2 %0, ra, rb;\n}"
+      : "=l"(d)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+
+// 32 columns from each of two TMEM addresses, one wait for both loads
+GPT2_DEV void tmem_ld32x2(uint32_t a0, uint32_t a1, float* v0, float* v1) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(a0), "r"(a1)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; i++) {
+    v0[i] = __uint_as_float(r[i]);
+    v1[i] = __uint_as_float(r[32 + i]);
+  }
+}
+
+// Writes 32 bf16 values (16 packed words) at columns hf*32 .. hf*32+31 of row
+// r of a K-major, 128-byte-swizzled tile with 64-column (128-byte) rows.
+GPT2_DEV void st_half_row_sw128(uint8_t* tile, int r, int hf, const uint32_t (&w)[16]) {
+#pragma unroll
+  for (int g = 0; g < 4; g++)
+    *reinterpret_cast<uint4*>(tile + r * 128 + (((hf * 4 + g) ^ (r & 7)) << 4)) =
+        make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global to shared memory, completing on an mbarrier.
+GPT2_DEV void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 128 x 64 scores (M = 128 rows, N = 64 columns, both operands K-major)
+constexpr uint32_t IDESC_S64 =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(SUB >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+constexpr uint32_t IDESC_ACC = IDESC_PV;  // 128 x 64 accumulation, B MN-major
+
 // Backward (the page's attention_backward), bf16 operands, head size 64,
 // T % 128 == 0.  With P = exp(S*scale - lse) recomputed from the saved
 // log-sum-exp, dP = dO V^T, D = rowsum(dO o y) and dS = P o (dP - D):
@@ -306,67 +442,38 @@ __global__ void __launch_bounds__(THREADS, 2)
 // Two kernels, each output row produced by one CTA (no atomics, so the
 // result is deterministic):
 //   attn_bwd_dkv_tc_kernel  CTA per (key tile, head, batch); walks the query
-//       tiles at or after the key tile: S^T = K Q^T, dP^T = V dO^T in TMEM,
-//       P^T and dS^T (bf16) staged in shared memory, dV += P^T dO and
+//       tiles at or after the key tile in sub-tiles of 64 queries:
+//       S^T = K Q^T, dP^T = V dO^T into one of two TMEM buffers, P^T and
+//       dS^T (bf16) into one of two shared-memory buffers, dV += P^T dO and
 //       dK += dS^T Q accumulated in TMEM.
 //   attn_bwd_dq_tc_kernel   CTA per (query tile, head, batch); walks the key
-//       tiles at or before it: S = Q K^T, dP = dO V^T, dS staged,
-//       dQ += dS K in TMEM.
-// Operand tiles come from the bf16 copies of qkv and of dO (the gradient of
-// the attention output, (B*T, C)), each through a TMA map with 64 x 128
-// boxes.  Q, K, V, dO tiles are K-major for the score products and read
-// MN-major as the B operand of the accumulating products.
-// ---------------------------------------------------------------------------
-struct BwdParams {
-  int B, T, C, NH;
-  float scale;
-  const float* lse;  // (B, NH, T)
-  const float* D;    // (B, NH, T)
-  float* dqkv;       // (B, T, 3C) fp32
-  uint16_t* dqkv_bf; // (B, T, 3C) bf16 copy, or NULL
-  int* err;
-};
-
-// Writes 32 consecutive bf16 values (keys or queries c*32 .. c*32+31 of a
-// 128-wide row r) into a K-major, 128-byte-swizzled 128 x 128 tile made of
-// two 64-column chunks of 16 KB.
-GPT2_DEV void st_row32_sw128(uint8_t* tile, int r, int c, const uint32_t (&w)[16]) {
-#pragma unroll
-  for (int g = 0; g < 4; g++) {
-    const int key16 = c * 4 + g, chunk = key16 >> 3, grp = key16 & 7;
-    *reinterpret_cast<uint4*>(tile + chunk * TILE_BYTES + r * 128 + ((grp ^ (r & 7)) << 4)) =
-        make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
-  }
-}
-
-GPT2_DEV uint32_t pack_bf16x2(float a, float b) {
-  return (uint32_t)to_bf16_bits(a) | ((uint32_t)to_bf16_bits(b) << 16);
-}
-
-// 128 x 128 K-major A operand in two 64-column chunks: descriptor of K step kk
-GPT2_DEV uint64_t desc_a128(uint32_t base, int kk) {
-  return desc_sw128(base + (kk >> 2) * TILE_BYTES + (kk & 3) * 32, 16, 1024);
-}
-
-constexpr uint32_t IDESC_SS = IDESC_S;   // 128 x 128 scores, both K-major
-constexpr uint32_t IDESC_ACC = IDESC_PV; // 128 x 64 accumulation, B MN-major
-
+//       tiles at or before it in sub-tiles of 64 keys: S = Q K^T, dP = dO V^T,
+//       dS staged, dQ += dS K in TMEM.
+// The MMA warp issues the scores of sub-tile i+1 before the products of
+// sub-tile i, so the tensor core computes the next scores while the eight
+// softmax warps (two per TMEM lane quarter, 32 columns each) work on the
+// current ones.  Operand tiles come from the bf16 copies of qkv and of dO
+// (the gradient of the attention output, (B*T, C)) through TMA maps with
+// 64 x 128 boxes; a 64-row sub-tile starts 8 KB into its 128-row tile.
 namespace dkv {
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + TILE_BYTES;
-constexpr int OFF_Q = OFF_V + TILE_BYTES;        // 2 stages
-constexpr int OFF_DO = OFF_Q + 2 * TILE_BYTES;   // 2 stages
-constexpr int OFF_PT = OFF_DO + 2 * TILE_BYTES;  // P^T, 128 x 128 bf16
-constexpr int OFF_DST = OFF_PT + 2 * TILE_BYTES; // dS^T, 128 x 128 bf16
-constexpr int OFF_LD = OFF_DST + 2 * TILE_BYTES; // lse and D of one query tile (2 x 128 floats)
-constexpr int OFF_BAR = OFF_LD + 2 * 128 * 4;
-// kv_full, qd_full[2], qd_empty[2], s_full, st_ready, mma_done
-constexpr int NUM_BARS = 8;
+constexpr int OFF_Q = OFF_V + TILE_BYTES;          // 2 stages
+constexpr int OFF_DO = OFF_Q + 2 * TILE_BYTES;     // 2 stages
+constexpr int SUB_BYTES = 128 * SUB * 2;           // 16 KB: a 128 x 64 bf16 P^T or dS^T
+constexpr int OFF_PT = OFF_DO + 2 * TILE_BYTES;    // 2 buffers
+constexpr int OFF_DST = OFF_PT + 2 * SUB_BYTES;    // 2 buffers
+constexpr int LD_BYTES = 128 * 8;                  // (-lse log2 e, D) of one query tile
+constexpr int OFF_LD = OFF_DST + 2 * SUB_BYTES;    // 2 stages
+constexpr int OFF_BAR = OFF_LD + 2 * LD_BYTES;
+// kv_full, qd_full[2], qd_empty[2], s_full[2], st_ready[2], pt_free[2], mma_done
+constexpr int NUM_BARS = 12;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 }  // namespace dkv
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
                            const __grid_constant__ BwdParams p) {
   pdl_launch_dependents();
@@ -378,8 +485,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* qd_full = bars + 1;
   uint64_t* qd_empty = bars + 3;
   uint64_t* s_full = bars + 5;
-  uint64_t* st_ready = bars + 6;
-  uint64_t* mma_done = bars + 7;
+  uint64_t* st_ready = bars + 7;
+  uint64_t* pt_free = bars + 9;
+  uint64_t* mma_done = bars + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -387,16 +495,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nt = p.T / BKV;
   const int kt = (int)blockIdx.x;  // key tile; walks query tiles kt .. nt-1
   const int h = blockIdx.y, b = blockIdx.z;
-  const int niter = nt - kt;
+  const int niter = nt - kt;       // query tiles
+  const int nsub = 2 * niter;      // 64-query sub-tiles
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     for (int s = 0; s < 2; s++) {
       mbar_init(&qd_full[s], 1);
       mbar_init(&qd_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&st_ready[s], 256);
+      mbar_init(&pt_free[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(st_ready, 128);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -412,7 +522,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the first global-memory access comes after this
-  const uint32_t T_ST = tmem, T_DPT = tmem + 128, T_DV = tmem + 256, T_DK = tmem + 320;
+  // TMEM: buffer x in columns [128 x, 128 x + 128): S^T then dP^T (64 each); dV, dK
+  const uint32_t T_DV = tmem + 256, T_DK = tmem + 320;
+  const size_t bh = ((size_t)b * p.NH + h) * p.T;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -422,11 +534,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_load_2d(smem + OFF_V, &tmQKV, 2 * p.C + h * HS, krow, kv_full);
       int issued = 0;
       for (int i = 0; i < niter; i++) {
-        const int s = i & 1, qrow = b * p.T + (kt + i) * BQ;
+        const int s = i & 1, qt = kt + i, qrow = b * p.T + qt * BQ;
         if (!mbar_wait(&qd_empty[s], ((i >> 1) & 1) ^ 1, abort_flag, p.err)) break;
-        mbar_expect_tx(&qd_full[s], 2 * TILE_BYTES);
+        mbar_expect_tx(&qd_full[s], 2 * TILE_BYTES + LD_BYTES);
         tma_load_2d(smem + OFF_Q + s * TILE_BYTES, &tmQKV, h * HS, qrow, &qd_full[s]);
         tma_load_2d(smem + OFF_DO + s * TILE_BYTES, &tmDO, h * HS, qrow, &qd_full[s]);
+        bulk_load(smem + OFF_LD + s * LD_BYTES, p.LD + bh + qt * BQ, LD_BYTES, &qd_full[s]);
         issued = i + 1;
       }
       if (*abort_flag) {
@@ -437,114 +550,115 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t sk = smem_u32(smem + OFF_K), sv = smem_u32(smem + OFF_V);
-      const uint32_t spt = smem_u32(smem + OFF_PT), sdst = smem_u32(smem + OFF_DST);
-      bool ok = mbar_wait(kv_full, 0, abort_flag, p.err);
-      for (int i = 0; i < niter && ok; i++) {
-        const int s = i & 1;
-        if (!mbar_wait(&qd_full[s], (i >> 1) & 1, abort_flag, p.err)) break;
+      // scores of sub-tile i into TMEM buffer i & 1
+      auto issue_s = [&](int i) -> bool {
+        const int it = i >> 1, s = it & 1, u = i & 1;
+        if (u == 0 && !mbar_wait(&qd_full[s], (it >> 1) & 1, abort_flag, p.err)) return false;
         tc_fence_after();
-        const uint32_t sq = smem_u32(smem + OFF_Q + s * TILE_BYTES), sdo = smem_u32(smem + OFF_DO + s * TILE_BYTES);
+        const uint32_t sq = smem_u32(smem + OFF_Q + s * TILE_BYTES) + u * (TILE_BYTES / 2);
+        const uint32_t sdo = smem_u32(smem + OFF_DO + s * TILE_BYTES) + u * (TILE_BYTES / 2);
+        const uint32_t t_st = tmem + (i & 1) * 128, t_dpt = t_st + SUB;
 #pragma unroll
         for (int kk = 0; kk < HS / 16; kk++) {
-          mma_bf16(T_ST, desc_sw128(sk + kk * 32, 16, 1024), desc_sw128(sq + kk * 32, 16, 1024), IDESC_SS,
+          mma_bf16(t_st, desc_sw128(sk + kk * 32, 16, 1024), desc_sw128(sq + kk * 32, 16, 1024), IDESC_S64,
                    kk > 0 ? 1u : 0u);
-          mma_bf16(T_DPT, desc_sw128(sv + kk * 32, 16, 1024), desc_sw128(sdo + kk * 32, 16, 1024), IDESC_SS,
+          mma_bf16(t_dpt, desc_sw128(sv + kk * 32, 16, 1024), desc_sw128(sdo + kk * 32, 16, 1024), IDESC_S64,
                    kk > 0 ? 1u : 0u);
         }
-        mma_commit(s_full);
-        if (!mbar_wait(st_ready, i & 1, abort_flag, p.err)) break;
+        mma_commit(&s_full[i & 1]);
+        return true;
+      };
+      bool ok = mbar_wait(kv_full, 0, abort_flag, p.err) && issue_s(0);
+      for (int i = 0; i < nsub && ok; i++) {
+        // buffer (i+1) & 1 was read out by the softmax warps before st_ready(i-1)
+        if (i + 1 < nsub && !issue_s(i + 1)) break;
+        if (!mbar_wait(&st_ready[i & 1], (i >> 1) & 1, abort_flag, p.err)) break;
         tc_fence_after();
+        const int it = i >> 1, s = it & 1, u = i & 1;
+        const uint32_t sq = smem_u32(smem + OFF_Q + s * TILE_BYTES) + u * (TILE_BYTES / 2);
+        const uint32_t sdo = smem_u32(smem + OFF_DO + s * TILE_BYTES) + u * (TILE_BYTES / 2);
+        const uint32_t spt = smem_u32(smem + OFF_PT + (i & 1) * SUB_BYTES);
+        const uint32_t sdst = smem_u32(smem + OFF_DST + (i & 1) * SUB_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; kk++) {
+        for (int kk = 0; kk < SUB / 16; kk++) {
           const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          mma_bf16(T_DV, desc_a128(spt, kk), desc_sw128(sdo + kk * 2048, 8192, 1024), IDESC_ACC, acc);
-          mma_bf16(T_DK, desc_a128(sdst, kk), desc_sw128(sq + kk * 2048, 8192, 1024), IDESC_ACC, acc);
+          mma_bf16(T_DV, desc_sw128(spt + kk * 32, 16, 1024), desc_sw128(sdo + kk * 2048, 8192, 1024), IDESC_ACC,
+                   acc);
+          mma_bf16(T_DK, desc_sw128(sdst + kk * 32, 16, 1024), desc_sw128(sq + kk * 2048, 8192, 1024), IDESC_ACC,
+                   acc);
         }
-        mma_commit(&qd_empty[s]);
+        mma_commit(&pt_free[i & 1]);
+        if (u == 1) mma_commit(&qd_empty[s]);
       }
       mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0);
     }
   } else {
-    const int q4 = warp & 3;
+    const int q4 = warp & 3, hf = (warp - 2) >> 2;
     const int r = q4 * 32 + lane;  // key row within the tile = TMEM lane
-    const int t = threadIdx.x - 64;
     const int k = kt * BKV + r;    // key position
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const float l2e = 1.4426950408889634f, sl2 = p.scale * l2e;
-    float* lse_s = reinterpret_cast<float*>(smem + OFF_LD);
-    float* D_s = lse_s + 128;
-    const size_t bh = ((size_t)b * p.NH + h) * p.T;
+    const float sl2 = p.scale * 1.4426950408889634f;
+    const float2 sl2v = make_float2(sl2, sl2);
     bool ok = true;
-    for (int i = 0; i < niter; i++) {
-      const int qt = kt + i;
-      // lse (pre-multiplied by log2 e) and D of this query tile, shared by the 128 rows
-      tc::epi_bar<128>();
-      lse_s[t] = p.lse[bh + qt * BQ + t] * l2e;
-      D_s[t] = p.D[bh + qt * BQ + t];
-      tc::epi_bar<128>();
-      if (!tc::epi_bar_and<128>(mbar_wait(s_full, i & 1, abort_flag, p.err))) {
+    for (int i = 0; i < nsub; i++) {
+      const int it = i >> 1, s = it & 1, u = i & 1;
+      // one decision for all 256 threads: the TMEM loads below are warp-collective
+      const bool got = mbar_wait(&s_full[i & 1], (i >> 1) & 1, abort_flag, p.err) &&
+                       mbar_wait(&qd_full[s], (it >> 1) & 1, abort_flag, p.err) &&
+                       (i < 2 || mbar_wait(&pt_free[i & 1], ((i - 2) >> 1) & 1, abort_flag, p.err));
+      if (!tc::epi_bar_and<256>(got)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool diag = i == 0;  // queries before this key are masked
-#pragma unroll 1
-      for (int c = 0; c < BQ / 32; c++) {
-        float st[32], dpt[32];
-        tmem_ld32(T_ST + lane_off + c * 32, st);
-        tmem_ld32(T_DPT + lane_off + c * 32, dpt);
-        uint32_t wp[16], wd[16];
+      float st[32], dpt[32];
+      const uint32_t t_st = tmem + (i & 1) * 128 + lane_off + hf * 32;
+      tmem_ld32x2(t_st, t_st + SUB, st, dpt);
+      // queries u*64 + hf*32 + c of this query tile; before the key (masked) only in the first
+      const float4* ld = reinterpret_cast<const float4*>(smem + OFF_LD + s * LD_BYTES) + (u * SUB + hf * 32) / 2;
+      if (it == 0) {
+        const int lim = r - u * SUB - hf * 32;  // column c is masked when c < lim
 #pragma unroll
-        for (int e = 0; e < 16; e++) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; u++) {
-            const int qi = c * 32 + 2 * e + u;
-            const bool masked = diag && qt * BQ + qi < k;
-            pv[u] = masked ? 0.f : exp2f(st[2 * e + u] * sl2 - lse_s[qi]);
-            dv[u] = pv[u] * (dpt[2 * e + u] - D_s[qi]);
-          }
-          wp[e] = pack_bf16x2(pv[0], pv[1]);
-          wd[e] = pack_bf16x2(dv[0], dv[1]);
-        }
-        st_row32_sw128(smem + OFF_PT, r, c, wp);
-        st_row32_sw128(smem + OFF_DST, r, c, wd);
+        for (int c = 0; c < 32; c++)
+          if (c < lim) st[c] = -INFINITY;
       }
+      uint32_t wp[16], wd[16];
+#pragma unroll
+      for (int e = 0; e < 16; e++) {
+        const float4 v = ld[e];  // (-lse2, D) of queries 2e, 2e+1
+        const float2 x = fma2(make_float2(st[2 * e], st[2 * e + 1]), sl2v, make_float2(v.x, v.z));
+        const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+        const float2 ds = mul2(pp, add2(make_float2(dpt[2 * e], dpt[2 * e + 1]), make_float2(-v.y, -v.w)));
+        wp[e] = cvt_bf16x2(pp.x, pp.y);
+        wd[e] = cvt_bf16x2(ds.x, ds.y);
+      }
+      st_half_row_sw128(smem + OFF_PT + (i & 1) * SUB_BYTES, r, hf, wp);
+      st_half_row_sw128(smem + OFF_DST + (i & 1) * SUB_BYTES, r, hf, wd);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(st_ready);
+      mbar_arrive(&st_ready[i & 1]);
     }
-    if (ok) ok = mbar_wait(mma_done, 0, abort_flag, p.err);
-    // one decision for all 128 threads: the TMEM loads below are warp-collective
-    if (tc::epi_bar_and<128>(ok && !*abort_flag)) {
+    if (tc::epi_bar_and<256>(ok && mbar_wait(mma_done, 0, abort_flag, p.err) && !*abort_flag)) {
       tc_fence_after();
-      float dv[64], dk[64];
-      tmem_ld32(T_DV + lane_off, dv);
-      tmem_ld32(T_DV + lane_off + 32, dv + 32);
-      tmem_ld32(T_DK + lane_off, dk);
-      tmem_ld32(T_DK + lane_off + 32, dk + 32);
-      const size_t o = ((size_t)b * p.T + k) * 3 * p.C + h * HS;
+      float dv[32], dk[32];
+      tmem_ld32x2(T_DV + lane_off + hf * 32, T_DK + lane_off + hf * 32, dv, dk);
+      const size_t o = ((size_t)b * p.T + k) * 3 * p.C + h * HS + hf * 32;
 #pragma unroll
-      for (int d = 0; d < HS; d += 4) {
+      for (int d = 0; d < 32; d += 4) {
         *reinterpret_cast<float4*>(p.dqkv + o + p.C + d) =
             make_float4(dk[d] * p.scale, dk[d + 1] * p.scale, dk[d + 2] * p.scale, dk[d + 3] * p.scale);
         *reinterpret_cast<float4*>(p.dqkv + o + 2 * p.C + d) = make_float4(dv[d], dv[d + 1], dv[d + 2], dv[d + 3]);
       }
       if (p.dqkv_bf) {
 #pragma unroll
-        for (int d = 0; d < HS; d += 8) {
-          uint4 a, c;
-          a.x = pack_bf16x2(dk[d] * p.scale, dk[d + 1] * p.scale);
-          a.y = pack_bf16x2(dk[d + 2] * p.scale, dk[d + 3] * p.scale);
-          a.z = pack_bf16x2(dk[d + 4] * p.scale, dk[d + 5] * p.scale);
-          a.w = pack_bf16x2(dk[d + 6] * p.scale, dk[d + 7] * p.scale);
-          c.x = pack_bf16x2(dv[d], dv[d + 1]);
-          c.y = pack_bf16x2(dv[d + 2], dv[d + 3]);
-          c.z = pack_bf16x2(dv[d + 4], dv[d + 5]);
-          c.w = pack_bf16x2(dv[d + 6], dv[d + 7]);
-          *reinterpret_cast<uint4*>(p.dqkv_bf + o + p.C + d) = a;
-          *reinterpret_cast<uint4*>(p.dqkv_bf + o + 2 * p.C + d) = c;
+        for (int d = 0; d < 32; d += 8) {
+          *reinterpret_cast<uint4*>(p.dqkv_bf + o + p.C + d) =
+              make_uint4(cvt_bf16x2(dk[d] * p.scale, dk[d + 1] * p.scale), cvt_bf16x2(dk[d + 2] * p.scale, dk[d + 3] * p.scale),
+                         cvt_bf16x2(dk[d + 4] * p.scale, dk[d + 5] * p.scale), cvt_bf16x2(dk[d + 6] * p.scale, dk[d + 7] * p.scale));
+          *reinterpret_cast<uint4*>(p.dqkv_bf + o + 2 * p.C + d) =
+              make_uint4(cvt_bf16x2(dv[d], dv[d + 1]), cvt_bf16x2(dv[d + 2], dv[d + 3]), cvt_bf16x2(dv[d + 4], dv[d + 5]),
+                         cvt_bf16x2(dv[d + 6], dv[d + 7]));
         }
       }
     }
@@ -563,15 +677,17 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_DO = OFF_Q + TILE_BYTES;
 constexpr int OFF_K = OFF_DO + TILE_BYTES;      // 2 stages
 constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;   // 2 stages
-constexpr int OFF_DS = OFF_V + 2 * TILE_BYTES;  // dS, 128 x 128 bf16
-constexpr int OFF_BAR = OFF_DS + 2 * TILE_BYTES;
-// qd_full, kv_full[2], kv_empty[2], s_full, ds_ready, mma_done
-constexpr int NUM_BARS = 8;
+constexpr int SUB_BYTES = 128 * SUB * 2;
+constexpr int OFF_DS = OFF_V + 2 * TILE_BYTES;  // dS, 2 buffers of 128 x 64 bf16
+constexpr int OFF_BAR = OFF_DS + 2 * SUB_BYTES;
+// qd_full, kv_full[2], kv_empty[2], s_full[2], ds_ready[2], ds_free[2], mma_done
+constexpr int NUM_BARS = 12;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 }  // namespace dqk
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
                           const __grid_constant__ BwdParams p) {
   pdl_launch_dependents();
@@ -583,8 +699,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = bars + 3;
   uint64_t* s_full = bars + 5;
-  uint64_t* ds_ready = bars + 6;
-  uint64_t* mma_done = bars + 7;
+  uint64_t* ds_ready = bars + 7;
+  uint64_t* ds_free = bars + 9;
+  uint64_t* mma_done = bars + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -593,6 +710,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int qt = nt - 1 - (int)blockIdx.x;  // longest rows first
   const int h = blockIdx.y, b = blockIdx.z;
   const int niter = qt + 1;                 // key tiles 0 .. qt
+  const int nsub = 2 * niter;               // 64-key sub-tiles
   const int qrow = b * p.T + qt * BQ;
 
   if (threadIdx.x == 0) {
@@ -600,9 +718,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int s = 0; s < 2; s++) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&ds_ready[s], 256);
+      mbar_init(&ds_free[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(ds_ready, 128);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -618,7 +737,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the first global-memory access comes after this
-  const uint32_t T_S = tmem, T_DP = tmem + 128, T_DQ = tmem + 256;
+  // TMEM: buffer x in columns [128 x, 128 x + 128): S then dP (64 each); dQ
+  const uint32_t T_DQ = tmem + 256;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -641,94 +761,98 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t sq = smem_u32(smem + OFF_Q), sdo = smem_u32(smem + OFF_DO), sds = smem_u32(smem + OFF_DS);
-      bool ok = mbar_wait(qd_full, 0, abort_flag, p.err);
-      for (int j = 0; j < niter && ok; j++) {
-        const int s = j & 1;
-        if (!mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.err)) break;
+      const uint32_t sq = smem_u32(smem + OFF_Q), sdo = smem_u32(smem + OFF_DO);
+      // scores of sub-tile i (keys 64 u .. of key tile i >> 1) into TMEM buffer i & 1
+      auto issue_s = [&](int i) -> bool {
+        const int j = i >> 1, s = j & 1, u = i & 1;
+        if (u == 0 && !mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.err)) return false;
         tc_fence_after();
-        const uint32_t sk = smem_u32(smem + OFF_K + s * TILE_BYTES), sv = smem_u32(smem + OFF_V + s * TILE_BYTES);
+        const uint32_t sk = smem_u32(smem + OFF_K + s * TILE_BYTES) + u * (TILE_BYTES / 2);
+        const uint32_t sv = smem_u32(smem + OFF_V + s * TILE_BYTES) + u * (TILE_BYTES / 2);
+        const uint32_t t_s = tmem + (i & 1) * 128, t_dp = t_s + SUB;
 #pragma unroll
         for (int kk = 0; kk < HS / 16; kk++) {
-          mma_bf16(T_S, desc_sw128(sq + kk * 32, 16, 1024), desc_sw128(sk + kk * 32, 16, 1024), IDESC_SS,
+          mma_bf16(t_s, desc_sw128(sq + kk * 32, 16, 1024), desc_sw128(sk + kk * 32, 16, 1024), IDESC_S64,
                    kk > 0 ? 1u : 0u);
-          mma_bf16(T_DP, desc_sw128(sdo + kk * 32, 16, 1024), desc_sw128(sv + kk * 32, 16, 1024), IDESC_SS,
+          mma_bf16(t_dp, desc_sw128(sdo + kk * 32, 16, 1024), desc_sw128(sv + kk * 32, 16, 1024), IDESC_S64,
                    kk > 0 ? 1u : 0u);
         }
-        mma_commit(s_full);
-        if (!mbar_wait(ds_ready, j & 1, abort_flag, p.err)) break;
+        mma_commit(&s_full[i & 1]);
+        return true;
+      };
+      bool ok = mbar_wait(qd_full, 0, abort_flag, p.err) && issue_s(0);
+      for (int i = 0; i < nsub && ok; i++) {
+        if (i + 1 < nsub && !issue_s(i + 1)) break;
+        if (!mbar_wait(&ds_ready[i & 1], (i >> 1) & 1, abort_flag, p.err)) break;
         tc_fence_after();
+        const int j = i >> 1, s = j & 1, u = i & 1;
+        const uint32_t sk = smem_u32(smem + OFF_K + s * TILE_BYTES) + u * (TILE_BYTES / 2);
+        const uint32_t sds = smem_u32(smem + OFF_DS + (i & 1) * SUB_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; kk++)
-          mma_bf16(T_DQ, desc_a128(sds, kk), desc_sw128(sk + kk * 2048, 8192, 1024), IDESC_ACC,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&kv_empty[s]);
+        for (int kk = 0; kk < SUB / 16; kk++)
+          mma_bf16(T_DQ, desc_sw128(sds + kk * 32, 16, 1024), desc_sw128(sk + kk * 2048, 8192, 1024), IDESC_ACC,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&ds_free[i & 1]);
+        if (u == 1) mma_commit(&kv_empty[s]);
       }
       mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0);
     }
   } else {
-    const int q4 = warp & 3;
+    const int q4 = warp & 3, hf = (warp - 2) >> 2;
     const int r = q4 * 32 + lane;  // query row within the tile = TMEM lane
     const int t = qt * BQ + r;     // query position
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const float l2e = 1.4426950408889634f, sl2 = p.scale * l2e;
-    const size_t bh = ((size_t)b * p.NH + h) * p.T;
-    const float L2 = p.lse[bh + t] * l2e, Dt = p.D[bh + t];
+    const float sl2 = p.scale * 1.4426950408889634f;
+    const float2 ldr = p.LD[((size_t)b * p.NH + h) * p.T + t];  // (-lse2, D) of this query
+    const float2 sl2v = make_float2(sl2, sl2), nlv = make_float2(ldr.x, ldr.x), ndv = make_float2(-ldr.y, -ldr.y);
     bool ok = true;
-    for (int j = 0; j < niter; j++) {
-      if (!tc::epi_bar_and<128>(mbar_wait(s_full, j & 1, abort_flag, p.err))) {
+    for (int i = 0; i < nsub; i++) {
+      const int j = i >> 1, u = i & 1;
+      const bool got = mbar_wait(&s_full[i & 1], (i >> 1) & 1, abort_flag, p.err) &&
+                       (i < 2 || mbar_wait(&ds_free[i & 1], ((i - 2) >> 1) & 1, abort_flag, p.err));
+      if (!tc::epi_bar_and<256>(got)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool diag = j == qt;  // keys after this query are masked
-#pragma unroll 1
-      for (int c = 0; c < BKV / 32; c++) {
-        float sv[32], dp[32];
-        tmem_ld32(T_S + lane_off + c * 32, sv);
-        tmem_ld32(T_DP + lane_off + c * 32, dp);
-        uint32_t wd[16];
+      float sv[32], dp[32];
+      const uint32_t t_s = tmem + (i & 1) * 128 + lane_off + hf * 32;
+      tmem_ld32x2(t_s, t_s + SUB, sv, dp);
+      if (j == qt) {  // keys after the query are masked: column c when u*64 + hf*32 + c > r
+        const int lim = r - u * SUB - hf * 32;
 #pragma unroll
-        for (int e = 0; e < 16; e++) {
-          float dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; u++) {
-            const int ki = c * 32 + 2 * e + u;
-            const bool masked = diag && j * BKV + ki > t;
-            const float pv = masked ? 0.f : exp2f(sv[2 * e + u] * sl2 - L2);
-            dv[u] = pv * (dp[2 * e + u] - Dt);
-          }
-          wd[e] = pack_bf16x2(dv[0], dv[1]);
-        }
-        st_row32_sw128(smem + OFF_DS, r, c, wd);
+        for (int c = 0; c < 32; c++)
+          if (c > lim) sv[c] = -INFINITY;
       }
+      uint32_t wd[16];
+#pragma unroll
+      for (int e = 0; e < 16; e++) {
+        const float2 x = fma2(make_float2(sv[2 * e], sv[2 * e + 1]), sl2v, nlv);
+        const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+        const float2 ds = mul2(pp, add2(make_float2(dp[2 * e], dp[2 * e + 1]), ndv));
+        wd[e] = cvt_bf16x2(ds.x, ds.y);
+      }
+      st_half_row_sw128(smem + OFF_DS + (i & 1) * SUB_BYTES, r, hf, wd);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(ds_ready);
+      mbar_arrive(&ds_ready[i & 1]);
     }
-    if (ok) ok = mbar_wait(mma_done, 0, abort_flag, p.err);
-    // one decision for all 128 threads: the TMEM loads below are warp-collective
-    if (tc::epi_bar_and<128>(ok && !*abort_flag)) {
+    if (tc::epi_bar_and<256>(ok && mbar_wait(mma_done, 0, abort_flag, p.err) && !*abort_flag)) {
       tc_fence_after();
-      float dq[64];
-      tmem_ld32(T_DQ + lane_off, dq);
-      tmem_ld32(T_DQ + lane_off + 32, dq + 32);
-      const size_t o = ((size_t)b * p.T + t) * 3 * p.C + h * HS;
+      float dq[32];
+      tmem_ld32(T_DQ + lane_off + hf * 32, dq);
+      const size_t o = ((size_t)b * p.T + t) * 3 * p.C + h * HS + hf * 32;
 #pragma unroll
-      for (int d = 0; d < HS; d += 4)
+      for (int d = 0; d < 32; d += 4)
         *reinterpret_cast<float4*>(p.dqkv + o + d) =
             make_float4(dq[d] * p.scale, dq[d + 1] * p.scale, dq[d + 2] * p.scale, dq[d + 3] * p.scale);
       if (p.dqkv_bf) {
 #pragma unroll
-        for (int d = 0; d < HS; d += 8) {
-          uint4 a;
-          a.x = pack_bf16x2(dq[d] * p.scale, dq[d + 1] * p.scale);
-          a.y = pack_bf16x2(dq[d + 2] * p.scale, dq[d + 3] * p.scale);
-          a.z = pack_bf16x2(dq[d + 4] * p.scale, dq[d + 5] * p.scale);
-          a.w = pack_bf16x2(dq[d + 6] * p.scale, dq[d + 7] * p.scale);
-          *reinterpret_cast<uint4*>(p.dqkv_bf + o + d) = a;
-        }
+        for (int d = 0; d < 32; d += 8)
+          *reinterpret_cast<uint4*>(p.dqkv_bf + o + d) =
+              make_uint4(cvt_bf16x2(dq[d] * p.scale, dq[d + 1] * p.scale), cvt_bf16x2(dq[d + 2] * p.scale, dq[d + 3] * p.scale),
+                         cvt_bf16x2(dq[d + 4] * p.scale, dq[d + 5] * p.scale), cvt_bf16x2(dq[d + 6] * p.scale, dq[d + 7] * p.scale));
       }
     }
   }
