@@ -49,8 +49,27 @@ GPT2_DEV float round_bf16(float x) {
   return __uint_as_float(u & 0xffff0000u);
 }
 
+// x rounded to bf16 (nearest even; NaN stays NaN) by the conversion
+// instruction; the same value round_bf16 gives for every non-NaN x
 GPT2_DEV uint16_t to_bf16_bits(float x) {
-  return (uint16_t)(__float_as_uint(round_bf16(x)) >> 16);
+  uint16_t h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));
+  return h;
+}
+
+// 2^x on the special-function unit (relative error near 2^-22; subnormal
+// results flush to zero)
+GPT2_DEV float ex2f_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// lo and hi rounded to bf16 and packed into one word, lo in the low half
+GPT2_DEV uint32_t bf16x2_bits(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // tanh-form GELU used by GPT-2 and its derivative.

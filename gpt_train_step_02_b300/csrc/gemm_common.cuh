@@ -31,12 +31,27 @@ struct EpiArgs {
   uint16_t* Cbf;  // optional bf16 copy of the output
   long long ldcbf;
   int fast;       // GELU / GELU' through the hardware tanh approximation (bf16 products)
+  // Optional column sums of the fp32 outputs over each 32-row block:
+  // colsum[(i / 32) * ldcs + j] = sum of C(i', j) for i' in that block (the
+  // first stage of a bias gradient).  Only on the coalesced warp epilogue
+  // (vec4, N a multiple of 32); each block is written by exactly one warp.
+  float* colsum;
+  long long ldcs;
 };
 
+// The epilogue functions take the kind as a template argument OP when the
+// caller knows it at compile time (straight-line code per kernel
+// instantiation), or read e.epi at run time (OP = -1).
+template <int OP>
+GPT2_DEV int epi_kind(const EpiArgs& e) {
+  return OP >= 0 ? OP : e.epi;
+}
+
+template <int OP = -1>
 GPT2_DEV void epi_store(const EpiArgs& e, int i, int j, float acc) {
   size_t ci = (size_t)i * e.ldc + j;
   float out;
-  switch (e.epi) {
+  switch (epi_kind<OP>(e)) {
     case EPI_BIAS: out = acc + e.bias[j]; break;
     case EPI_BIAS_RESID: out = acc + e.bias[j] + e.R[(size_t)i * e.ldr + j]; break;
     case EPI_BIAS_GELU: {
@@ -66,16 +81,18 @@ GPT2_DEV bool epi_has_bias(int op) { return op == EPI_BIAS || op == EPI_BIAS_RES
 GPT2_DEV bool epi_has_input(int op) { return op == EPI_BIAS_RESID || op == EPI_DGELU || op == EPI_ACCUM; }
 
 // The input of element block (i, j .. j+3) an epilogue reads (R or C).
+template <int OP = -1>
 GPT2_DEV float4 epi_load_input(const EpiArgs& e, int i, int j) {
-  return e.epi == EPI_ACCUM ? ld4(e.C + (size_t)i * e.ldc + j) : ld4(e.R + (size_t)i * e.ldr + j);
+  return epi_kind<OP>(e) == EPI_ACCUM ? ld4(e.C + (size_t)i * e.ldc + j) : ld4(e.R + (size_t)i * e.ldr + j);
 }
 
 // Finishes (i, j .. j+3) from the accumulator, the column bias b and the
 // element input in (both already loaded when the epilogue needs them).
 // vec4 must hold.
-GPT2_DEV void epi_apply4(const EpiArgs& e, int i, int j, float4 acc, float4 b, float4 in) {
+template <int OP = -1>
+GPT2_DEV float4 epi_apply4(const EpiArgs& e, int i, int j, float4 acc, float4 b, float4 in) {
   float4 o = acc;
-  switch (e.epi) {
+  switch (epi_kind<OP>(e)) {
     case EPI_BIAS: o = make_float4(acc.x + b.x, acc.y + b.y, acc.z + b.z, acc.w + b.w); break;
     case EPI_BIAS_RESID:
       o = make_float4(acc.x + b.x + in.x, acc.y + b.y + in.y, acc.z + b.z + in.z, acc.w + b.w + in.w);
@@ -103,23 +120,26 @@ GPT2_DEV void epi_apply4(const EpiArgs& e, int i, int j, float4 acc, float4 b, f
   if (e.C) st4(e.C + (size_t)i * e.ldc + j, o);
   if (e.Cbf) {
     uint2 h;
-    h.x = (uint32_t)to_bf16_bits(o.x) | ((uint32_t)to_bf16_bits(o.y) << 16);
-    h.y = (uint32_t)to_bf16_bits(o.z) | ((uint32_t)to_bf16_bits(o.w) << 16);
+    h.x = bf16x2_bits(o.x, o.y);
+    h.y = bf16x2_bits(o.z, o.w);
     *reinterpret_cast<uint2*>(e.Cbf + (size_t)i * e.ldcbf + j) = h;
   }
+  return o;
 }
 
 // Finishes 4 consecutive outputs (i, j .. j+3), all inside the matrix.
+template <int OP = -1>
 GPT2_DEV void epi_store4(const EpiArgs& e, int i, int j, float4 acc) {
   if (!e.vec4) {
-    epi_store(e, i, j, acc.x);
-    epi_store(e, i, j + 1, acc.y);
-    epi_store(e, i, j + 2, acc.z);
-    epi_store(e, i, j + 3, acc.w);
+    epi_store<OP>(e, i, j, acc.x);
+    epi_store<OP>(e, i, j + 1, acc.y);
+    epi_store<OP>(e, i, j + 2, acc.z);
+    epi_store<OP>(e, i, j + 3, acc.w);
     return;
   }
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  epi_apply4(e, i, j, acc, epi_has_bias(e.epi) ? ld4(e.bias + j) : z, epi_has_input(e.epi) ? epi_load_input(e, i, j) : z);
+  const int op = epi_kind<OP>(e);
+  epi_apply4<OP>(e, i, j, acc, epi_has_bias(op) ? ld4(e.bias + j) : z, epi_has_input(op) ? epi_load_input<OP>(e, i, j) : z);
 }
 
 // ---- coalesced epilogue of a warp's 32 x 32 sub-tile --------------------------
@@ -160,28 +180,46 @@ GPT2_DEV void warp32_store_raw(float* P, long long ldp, const float* stage, int 
 }
 
 // Fused epilogue of the staged sub-tile into the product's outputs.
+template <int OP = -1>
 GPT2_DEV void warp32_epilogue(const EpiArgs& e, const float* stage, int i0, int j0, int M, int N, int lane) {
   const int c = 4 * (lane & 7), rs = lane >> 3, j = j0 + c;
+  const int op = epi_kind<OP>(e);
   if (j < N) {
     if (e.vec4 && j + 4 <= N) {
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 b = epi_has_bias(e.epi) ? ld4(e.bias + j) : z;
+      const float4 b = epi_has_bias(op) ? ld4(e.bias + j) : z;
       float4 in[8];
 #pragma unroll
       for (int k = 0; k < 8; k++) {
         const int i = i0 + rs + 4 * k;
-        in[k] = (epi_has_input(e.epi) && i < M) ? epi_load_input(e, i, j) : z;
+        in[k] = (epi_has_input(op) && i < M) ? epi_load_input<OP>(e, i, j) : z;
       }
+      float4 cs = z;
 #pragma unroll
       for (int k = 0; k < 8; k++) {
         const int r = rs + 4 * k, i = i0 + r;
-        if (i < M) epi_apply4(e, i, j, ld4(stage + r * EPI_STAGE_PITCH + c), b, in[k]);
+        if (i < M) {
+          const float4 o = epi_apply4<OP>(e, i, j, ld4(stage + r * EPI_STAGE_PITCH + c), b, in[k]);
+          cs = make_float4(cs.x + o.x, cs.y + o.y, cs.z + o.z, cs.w + o.w);
+        }
+      }
+      if (e.colsum) {
+        // lanes l, l^8, l^16, l^24 hold the same 4 columns for 8 rows each;
+        // the caller guarantees every lane of the warp is on this path
+#pragma unroll
+        for (int off = 8; off < 32; off <<= 1) {
+          cs.x += __shfl_xor_sync(0xffffffffu, cs.x, off);
+          cs.y += __shfl_xor_sync(0xffffffffu, cs.y, off);
+          cs.z += __shfl_xor_sync(0xffffffffu, cs.z, off);
+          cs.w += __shfl_xor_sync(0xffffffffu, cs.w, off);
+        }
+        if (lane < 8) st4(e.colsum + (size_t)(i0 >> 5) * e.ldcs + j, cs);
       }
     } else {
       for (int k = 0; k < 8; k++) {
         const int r = rs + 4 * k, i = i0 + r;
         if (i < M)
-          for (int q = 0; q < 4 && j + q < N; q++) epi_store(e, i, j + q, stage[r * EPI_STAGE_PITCH + c + q]);
+          for (int q = 0; q < 4 && j + q < N; q++) epi_store<OP>(e, i, j + q, stage[r * EPI_STAGE_PITCH + c + q]);
       }
     }
   }

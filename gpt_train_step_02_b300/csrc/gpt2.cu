@@ -135,7 +135,7 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->datty = take(BT * C * F);
   p->dqkv = take(BT * 3 * C * F);
   p->dfch = take(BT * 4 * C * F);
-  p->attD = take(2 * BT * NH * F);  // D, or the (-lse log2 e, D) pairs of the tensor-core path
+  p->attD = take(2 * BT * NH * F);  // D, or the (-lse log2 e, -D) pairs of the tensor-core path
   // scratch: column-sum partials (<= ceil(BT/BIAS_MIN_ROWS) x 4C) and
   // layernorm partials (<= ceil(BT/LNB_MIN_ROWS) x 3C)
   size_t s1 = ((BT + BIAS_MIN_ROWS - 1) / BIAS_MIN_ROWS) * 4 * C;
@@ -430,7 +430,29 @@ static int choose_splits_bf16(int M, int N, int K, int BN, long long ws_floats) 
 template <int BN>
 static void launch_bf16_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const tcb::Params& p, int grid,
                                cudaStream_t s) {
-  launch_k(tcb::gemm_bf16_kernel<BN>, grid, tcb::THREADS, tcb::Cfg<BN>::SMEM_BYTES, s, ta, tb, p);
+  const size_t sm = tcb::Cfg<BN>::SMEM_BYTES;
+  switch (p.epi.epi) {
+    case EPI_BIAS: launch_k(tcb::gemm_bf16_kernel<BN, EPI_BIAS>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
+    case EPI_BIAS_RESID: launch_k(tcb::gemm_bf16_kernel<BN, EPI_BIAS_RESID>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
+    case EPI_BIAS_GELU: launch_k(tcb::gemm_bf16_kernel<BN, EPI_BIAS_GELU>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
+    case EPI_DGELU: launch_k(tcb::gemm_bf16_kernel<BN, EPI_DGELU>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
+    case EPI_ACCUM: launch_k(tcb::gemm_bf16_kernel<BN, EPI_ACCUM>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
+    default: launch_k(tcb::gemm_bf16_kernel<BN, EPI_STORE>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
+  }
+}
+
+// Raises the dynamic shared-memory limit of every epilogue instantiation.
+template <int BN>
+static cudaError_t set_bf16_smem() {
+  const int sm = tcb::Cfg<BN>::SMEM_BYTES;
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_STORE>, a, sm);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_BIAS>, a, sm);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_BIAS_RESID>, a, sm);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_BIAS_GELU>, a, sm);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_DGELU>, a, sm);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_ACCUM>, a, sm);
+  return e;
 }
 
 // Launches the persistent bf16 tensor-core matmul.  Returns 1, or -1 on a
@@ -452,7 +474,9 @@ static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int
   p.K = d.K;
   p.a_kmajor = d.a_kmajor;
   p.b_kmajor = d.b_kmajor;
-  p.splits = choose_splits_bf16(d.M, d.N, d.K, BN, ws_floats);
+  // column sums are taken in the warp epilogue, which a K split bypasses
+  p.splits = d.epi.colsum ? 1 : choose_splits_bf16(d.M, d.N, d.K, BN, ws_floats);
+  if (d.epi.colsum && (!d.epi.vec4 || d.N % 32 || (d.epi.ldcs & 3) || ((uintptr_t)d.epi.colsum & 15))) return -1;
   p.k_tiles = ceil_div(d.K, tcb::BK);
   p.kt_per_split = ceil_div(p.k_tiles, p.splits);
   p.tiles_m = ceil_div(d.M, tcb::BM);
@@ -470,6 +494,10 @@ static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int
 }
 
 static int matmul(gpt2_t* m, const MatmulDesc& d) {
+  if (d.epi.colsum && m->cfg.gemm_precision != GPT2_PREC_BF16) {  // fused column sums: bf16 kernel only
+    m->poisoned = GPT2_ERR_CUDA;
+    return GPT2_ERR_CUDA;
+  }
   timer_begin(m, TK_GEMM, 2.0 * d.M * (double)d.N * d.K);
   int n = m->cfg.gemm_precision == GPT2_PREC_BF16 ? launch_matmul_bf16(d, m->splitk, m->tilectr, m->err, m->stream)
                                                   : launch_matmul(d, m->stream, m->err);
@@ -488,6 +516,7 @@ static EpiArgs epi_args(float* C, long long ldc, int epi, const float* bias = nu
   EpiArgs e;
   e.C = C; e.ldc = ldc; e.bias = bias; e.R = R; e.ldr = ldr; e.pre = pre; e.ldpre = ldpre; e.epi = epi;
   e.Cbf = Cbf; e.ldcbf = ldcbf; e.fast = 0;
+  e.colsum = nullptr; e.ldcs = 0;
   uintptr_t addr = (uintptr_t)C | (uintptr_t)bias | (uintptr_t)R | (uintptr_t)pre | (uintptr_t)Cbf;
   e.vec4 = (addr & 15) == 0 && (ldc & 3) == 0 && (ldr & 3) == 0 && (ldpre & 3) == 0 && (ldcbf & 7) == 0;
   return e;
@@ -506,10 +535,14 @@ static void mm_forward(gpt2_t* m, float* out, uint16_t* outbf, Opnd x, Opnd W, c
   matmul(m, d);
 }
 
-// dx = dy W (times gelu'(pre) when pre != NULL)
-static void mm_dx(gpt2_t* m, float* dx, uint16_t* dxbf, Opnd dy, Opnd W, int N, int IC, int OC, const float* pre) {
+// dx = dy W (times gelu'(pre) when pre != NULL); colsum: optional 32-row
+// column partial sums of dx (bf16 matmuls), leading dimension IC
+static void mm_dx(gpt2_t* m, float* dx, uint16_t* dxbf, Opnd dy, Opnd W, int N, int IC, int OC, const float* pre,
+                  float* colsum = nullptr) {
   MatmulDesc d = {N,    IC,   OC,   dy.f, OC, 1, W.f, IC, 0,
                   epi_args(dx, IC, pre ? EPI_DGELU : EPI_STORE, nullptr, pre, IC, nullptr, 0, dxbf, IC), dy.h, W.h};
+  d.epi.colsum = colsum;
+  d.epi.ldcs = IC;
   matmul(m, d);
 }
 
@@ -528,6 +561,15 @@ static void bias_grad(gpt2_t* m, float* db, const float* dy, int N, int OC) {
   launch_k(col_finish_kernel, ceil_div(OC, 32), COLF_WARPS * 32, 0, m->stream, db, db, db, OC, m->scratch, chunks,
            OC, m->grad_accumulate);
   m->launches += 2;
+}
+
+// db (+)= the sums of the nrows column-partial rows (OC columns) a matmul or
+// attention epilogue left in m->scratch
+static_assert(BIAS_MIN_ROWS == 32, "the scratch is sized in 32-row column-sum blocks");
+static void bias_finish(gpt2_t* m, float* db, int nrows, int OC) {
+  launch_k(col_finish_kernel, ceil_div(OC, 32), COLF_WARPS * 32, 0, m->stream, db, db, db, OC, m->scratch, nrows, OC,
+           m->grad_accumulate);
+  m->launches++;
 }
 
 template <typename K>
@@ -581,7 +623,10 @@ static int launch_attn_fwd(float* atty, uint16_t* attybf, float* lse, const floa
     p.B = B; p.T = T; p.C = C; p.NH = NH;
     p.scale = 1.0f / sqrtf((float)hs);
     p.y = atty; p.ybf = attybf; p.lse = lse; p.err = err;
-    launch_k(tca::attn_fwd_tc_kernel, dim3(T / tca::BQ, NH, B), tca::THREADS, tca::fwd::SMEM_BYTES, s, tm, p);
+    // persistent: two CTAs on each of the 148 SMs walk the (query tile, head, batch) items
+    const long long items = (long long)(T / tca::BQ) * NH * B;
+    launch_k(tca::attn_fwd_tc_kernel, (int)(items < 2 * 148 ? items : 2 * 148), tca::THREADS, tca::fwd::SMEM_BYTES, s,
+             tm, p);
     return 1;
   }
   const dim3 g(ceil_div(T, ATT_ROWS), NH, B);
@@ -610,13 +655,19 @@ static void attn_forward(gpt2_t* m, float* atty, uint16_t* attybf, float* lse, c
 // the CUDA-core kernels.  Returns the number of launches, or -1.
 static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float* dy, const uint16_t* dy_bf,
                            const float* qkv, const uint16_t* qkv_bf, const float* atty, const float* lse, int B, int T,
-                           int C, int NH, int bf, int* err, cudaStream_t s) {
+                           int C, int NH, int bf, int* err, cudaStream_t s, float* colsum = nullptr) {
   const int hs = C / NH;
   const int grid = ceil_div((long long)B * NH * T * 32, 256);
   const bool tc_path = bf && qkv_bf && dy_bf && hs == tca::HS && T % tca::BQ == 0;
-  // D holds 2 B NH T floats: the (-lse log2 e, D) pairs of the tensor-core path
-  launch_k(attn_bwd_D_kernel, grid, 256, 0, s, tc_path ? nullptr : D, tc_path ? (float2*)D : nullptr, lse, dy, atty,
-           B, T, C, NH);
+  // D holds 2 B NH T floats: the (-lse log2 e, -D) pairs of the tensor-core path
+  const int ldg = ceil_div((long long)B * T, tca::LD_WARPS);
+  if (tc_path && C <= 1024)
+    launch_k(tca::attn_bwd_ld_kernel<8>, ldg, tca::LD_WARPS * 32, 0, s, (float2*)D, lse, dy, atty, B, T, C);
+  else if (tc_path && C <= 2048)
+    launch_k(tca::attn_bwd_ld_kernel<16>, ldg, tca::LD_WARPS * 32, 0, s, (float2*)D, lse, dy, atty, B, T, C);
+  else
+    launch_k(attn_bwd_D_kernel, grid, 256, 0, s, tc_path ? nullptr : D, tc_path ? (float2*)D : nullptr, lse, dy, atty,
+             B, T, C, NH);
   if (tc_path) {
     CUtensorMap tq, td;
     if (!make_bf16_map(&tq, qkv_bf, 1, (long long)B * T, 3LL * C, 3LL * C, tca::BQ)) return -1;
@@ -624,12 +675,13 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
     tca::BwdParams p;
     p.B = B; p.T = T; p.C = C; p.NH = NH;
     p.scale = 1.0f / sqrtf((float)hs);
-    p.LD = (const float2*)D; p.dqkv = dqkv; p.dqkv_bf = dqkv_bf; p.err = err;
+    p.LD = (const float2*)D; p.dqkv = dqkv; p.dqkv_bf = dqkv_bf; p.colsum = colsum; p.err = err;
     dim3 g(T / tca::BQ, NH, B);
     launch_k(tca::attn_bwd_dkv_tc_kernel, g, tca::BWD_THREADS, tca::dkv::SMEM_BYTES, s, tq, td, p);
     launch_k(tca::attn_bwd_dq_tc_kernel, g, tca::BWD_THREADS, tca::dqk::SMEM_BYTES, s, tq, td, p);
     return 3;
   }
+  if (!dqkv || colsum) return -1;  // the CUDA-core kernels store fp32 dqkv only
   const dim3 g(ceil_div(T, ATT_ROWS), NH, B);
   const size_t sq = att_smem_fwd(hs), skv = att_smem_dkv(hs);
   if (hs <= 32) {
@@ -645,12 +697,15 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
   return 3;
 }
 
+// fuse_bias: the tensor-core kernels leave the 128-row column sums of dqkv in
+// m->scratch (the QKV bias gradient's first stage) and skip the fp32 dqkv,
+// which nothing else reads in bf16 precision
 static void attn_backward(gpt2_t* m, const float* qkv, const uint16_t* qkv_bf, const float* atty, const float* lse,
-                          int B, int T, int bf) {
+                          int B, int T, int bf, bool fuse_bias) {
   int C = m->cfg.channels, NH = m->cfg.num_heads, hs = C / NH;
   timer_begin(m, TK_ATTN_BWD, 8.0 * (double)B * NH * T * (T + 1) / 2.0 * hs);
-  int n = launch_attn_bwd(m->dqkv, m->dqkv_bf, m->attD, m->datty, m->datty_bf, qkv, qkv_bf, atty, lse, B, T, C, NH, bf,
-                          m->err, m->stream);
+  int n = launch_attn_bwd(fuse_bias ? nullptr : m->dqkv, m->dqkv_bf, m->attD, m->datty, m->datty_bf, qkv, qkv_bf, atty,
+                          lse, B, T, C, NH, bf, m->err, m->stream, fuse_bias ? m->scratch : nullptr);
   timer_end(m, TK_ATTN_BWD);
   if (n < 0) {
     m->poisoned = GPT2_ERR_CUDA;
@@ -669,12 +724,8 @@ static int set_kernel_attributes() {
                                          SORT_MAX * (int)sizeof(uint32_t));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc::gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               tcb::Cfg<256>::SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               tcb::Cfg<128>::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_bf16_smem<256>();
+    if (e == cudaSuccess) e = set_bf16_smem<128>();
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tca::attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                tca::fwd::SMEM_BYTES);
@@ -800,8 +851,7 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
   if (d_tgt) {
     timer_begin(m, TK_XENT, 8.0 * (double)N * Vp);
     launch_k(xent_fused_kernel, N, XENT_THREADS, 0, s, bf ? nullptr : m->dlogits, m->dlogits_bf, m->losses, m->logits,
-             d_tgt, V, Vp,
-                                                 1.0f / (float)N);
+             d_tgt, V, Vp, 1.0f / (float)N);
     timer_end(m, TK_XENT);
     launch_k(mean_kernel, 1, 1024, 0, s, m->losses, N, m->loss);
     m->launches += 2;
@@ -824,6 +874,10 @@ static int enqueue_backward(gpt2_t* m) {
   float** P = m->P;
   float** G = m->G;
   const Opnd dres = {m->dres, m->dres_bf}, dfch = {m->dfch, m->dfch_bf}, dqkv = {m->dqkv, m->dqkv_bf};
+  // the fused column sums need 32-column-aligned rows of 16-byte-aligned floats
+  const bool fuse_fcb = bf && (4 * C) % 32 == 0;
+  // the tensor-core attention backward (bf16, hs = 64, T % 128 == 0) takes the QKV bias column sums
+  const bool fuse_qkvb = bf && C / c.num_heads == tca::HS && T % tca::BQ == 0;
   // LM head (tied to wte): dlnf = dlogits wte; dwte += dlogits^T lnf
   mm_dx(m, m->dln, nullptr, {m->dlogits, m->dlogits_bf}, wparam(m, P_WTE, 0), N, C, Vp, nullptr);
   mm_dw(m, G[P_WTE], {m->dlogits, m->dlogits_bf}, {m->lnf, m->lnf_bf}, N, C, Vp);
@@ -837,10 +891,14 @@ static int enqueue_backward(gpt2_t* m) {
     // MLP output projection: res3 = res2 + fchg fcprojw^T + fcprojb
     mm_dw(m, G[P_FCPROJW] + l * 4 * CC, dres, {a.fchg, a.fchg_bf}, N, 4 * C, C);
     // (its bias gradient came with the layernorm backward that produced dres)
-    mm_dx(m, m->dfch, m->dfch_bf, dres, wparam(m, P_FCPROJW, l * 4 * CC), N, 4 * C, C, a.fch);  // x gelu'(fch)
+    // x gelu'(fch).  bf16: only the bf16 copy of dfch is stored; the MLP input
+    // bias gradient comes from column sums taken in the same epilogue
+    mm_dx(m, fuse_fcb ? nullptr : m->dfch, m->dfch_bf, dres, wparam(m, P_FCPROJW, l * 4 * CC), N, 4 * C, C, a.fch,
+          fuse_fcb ? m->scratch : nullptr);
     // MLP input projection: fch = ln2 fcw^T + fcb
     mm_dw(m, G[P_FCW] + l * 4 * CC, dfch, {a.ln2, a.ln2_bf}, N, C, 4 * C);
-    bias_grad(m, G[P_FCB] + (size_t)l * 4 * C, m->dfch, N, 4 * C);
+    if (fuse_fcb) bias_finish(m, G[P_FCB] + (size_t)l * 4 * C, ceil_div(N, 32), 4 * C);
+    else bias_grad(m, G[P_FCB] + (size_t)l * 4 * C, m->dfch, N, 4 * C);
     mm_dx(m, m->dln, nullptr, dfch, wparam(m, P_FCW, l * 4 * CC), N, C, 4 * C, nullptr);
     ln_backward(m, m->dres, m->dres_bf, G[P_LN2W] + (size_t)l * C, G[P_LN2B] + (size_t)l * C,
                 G[P_ATTPROJB] + (size_t)l * C, m->dln, a.res2, P[P_LN2W] + (size_t)l * C, a.ln2_mean, a.ln2_rstd, N);
@@ -848,10 +906,11 @@ static int enqueue_backward(gpt2_t* m) {
     mm_dw(m, G[P_ATTPROJW] + l * CC, dres, {a.atty, a.atty_bf}, N, C, C);
     mm_dx(m, m->datty, m->datty_bf, dres, wparam(m, P_ATTPROJW, l * CC), N, C, C, nullptr);
     // attention
-    attn_backward(m, a.qkv, a.qkv_bf, a.atty, a.lse, B, T, bf);
+    attn_backward(m, a.qkv, a.qkv_bf, a.atty, a.lse, B, T, bf, fuse_qkvb);
     // qkv projection: qkv = ln1 qkvw^T + qkvb
     mm_dw(m, G[P_QKVW] + l * 3 * CC, dqkv, {a.ln1, a.ln1_bf}, N, C, 3 * C);
-    bias_grad(m, G[P_QKVB] + (size_t)l * 3 * C, m->dqkv, N, 3 * C);
+    if (fuse_qkvb) bias_finish(m, G[P_QKVB] + (size_t)l * 3 * C, N / tca::BQ, 3 * C);
+    else bias_grad(m, G[P_QKVB] + (size_t)l * 3 * C, m->dqkv, N, 3 * C);
     mm_dx(m, m->dln, nullptr, dqkv, wparam(m, P_QKVW, l * 3 * CC), N, C, 3 * C, nullptr);
     // below layer 0 this dres is the previous layer's MLP output gradient
     ln_backward(m, m->dres, m->dres_bf, G[P_LN1W] + (size_t)l * C, G[P_LN1B] + (size_t)l * C,
@@ -1445,7 +1504,7 @@ EXPORT int gpt2op_attention_forward(float* y, float* lse, const float* qkv, int 
   return op_status(w, s);
 }
 
-// attention backward: workspace = [error word][bf16 qkv][bf16 dy][y][lse][D, or (-lse log2 e, D) pairs]
+// attention backward: workspace = [error word][bf16 qkv][bf16 dy][y][lse][D, or (-lse log2 e, -D) pairs]
 EXPORT size_t gpt2op_attention_backward_workspace_bytes(int B, int T, int C, int NH) {
   if (B < 1 || T < 1 || C < 1 || NH < 1) return 0;
   size_t n = (size_t)B * T;

@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(ATT_ROWS * 32)
 }
 
 // D[b,h,t] = sum_d dy[b,t,h,d] * y[b,t,h,d], into D and/or, for the tensor-core
-// kernels, as the pair LD[b,h,t] = (-lse[b,h,t] log2 e, D[b,h,t]).
+// kernels, as the pair LD[b,h,t] = (-lse[b,h,t] log2 e, -D[b,h,t]).
 __global__ void attn_bwd_D_kernel(float* __restrict__ D, float2* __restrict__ LD, const float* __restrict__ lse,
                                   const float* __restrict__ dy, const float* __restrict__ y, int B, int T, int C,
                                   int NH) {
@@ -161,7 +161,7 @@ __global__ void attn_bwd_D_kernel(float* __restrict__ D, float2* __restrict__ LD
   if (lane == 0) {
     const size_t i = ((size_t)b * NH + h) * T + t;
     if (D) D[i] = s;
-    if (LD) LD[i] = make_float2(-lse[i] * 1.4426950408889634f, s);
+    if (LD) LD[i] = make_float2(-lse[i] * 1.4426950408889634f, -s);
   }
 }
 

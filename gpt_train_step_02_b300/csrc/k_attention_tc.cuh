@@ -17,10 +17,10 @@
 // TMA map with 64 x 128 boxes (128-byte swizzle): Q and K tiles are K-major
 // (a row of 64 head dims per token); the V tile is read MN-major by the PV
 // product (rows of 64 head dims per key = the N dimension contiguous).
-// Six warps: warp 0 issues the TMA loads (Q once, K double-buffered, V
-// single-buffered so that two CTAs fit one SM);
-// warp 1 allocates TMEM and issues the MMAs; warps 2..5 own one query row
-// per thread (TMEM lane = row) for the softmax and the output.  Every
+// Six warps: warp 0 issues the TMA loads (Q once per item, K double-buffered,
+// V single-buffered so that two CTAs fit one SM); warp 1 allocates TMEM and
+// issues the MMAs; warps 2..5 own one query row per thread (TMEM lane = row)
+// for the softmax and the output.
 // mbarrier wait is bounded (1 s); on expiry the CTA records DEV_ERR_TIMEOUT,
 // drains its copies and MMAs and returns.
 #pragma once
@@ -61,6 +61,23 @@ GPT2_DEV float2 fma2(float2 a, float2 b, float2 c) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
 }
+// (a.x + b.x, a.y + b.y) and (a.x b.x, a.y b.y), one paired instruction each
+GPT2_DEV float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n add.rn.f32x2 %0, ra, rb;\n}"
+      : "=l"(d)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+GPT2_DEV float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n mul.rn.f32x2 %0, ra, rb;\n}"
+      : "=l"(d)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+
+// 32 columns from each of two TMEM addresses, one wait for both loads
 // lo and hi rounded to bf16 (nearest even) and packed, lo in the low half
 GPT2_DEV uint32_t cvt_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -94,7 +111,7 @@ GPT2_DEV void mask_after(float* v, int lim) {
 constexpr int BQ = 128;   // queries per CTA
 constexpr int BKV = 128;  // keys per tile
 constexpr int HS = 64;    // head size
-constexpr int THREADS = 192;
+constexpr int THREADS = 192;  // forward: TMA warp, MMA warp, 4 softmax warps
 constexpr int TILE_BYTES = 128 * HS * 2;  // 16 KB: a Q, K or V tile
 namespace fwd {
 constexpr int OFF_Q = 0;
@@ -102,8 +119,8 @@ constexpr int OFF_K = OFF_Q + TILE_BYTES;          // 2 stages
 constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;      // 1 stage (its load waits only on the previous P V)
 constexpr int OFF_P = OFF_V + TILE_BYTES;          // 128 x 128 bf16 = two 16 KB K chunks
 constexpr int OFF_BAR = OFF_P + 2 * TILE_BYTES;
-// q_full, k_full[2], k_empty[2], v_full, v_empty, s_full, p_full, pv_full, mma_done
-constexpr int NUM_BARS = 11;
+// q_full, q_empty, k_full[2], k_empty[2], v_full, v_empty, s_full, p_full, pv_full, mma_done
+constexpr int NUM_BARS = 12;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES + 1024 <= 233472 / 2, "two CTAs per SM");
@@ -125,6 +142,20 @@ constexpr uint32_t IDESC_S = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BK
 constexpr uint32_t IDESC_PV =
     (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(HS >> 3) << 17) | ((uint32_t)(BQ >> 4) << 24);
 
+// Work item w of B*NH*(T/128): query tile nqt-1 - w / (B*NH) (longest rows
+// first) of head/batch w % (B*NH).  The grid is persistent (two CTAs per SM);
+// CTA c of G takes item r*G + c in even rounds r and r*G + G-1-c in odd ones,
+// a snake order that evens out the causal lengths.
+GPT2_DEV bool fwd_item(const Params& p, int r, int& qt, int& h, int& b) {
+  const int BH = p.B * p.NH, nitems = (p.T / BQ) * BH, G = gridDim.x, c = blockIdx.x;
+  const int w = r * G + ((r & 1) ? G - 1 - c : c);
+  if (w >= nitems) return false;
+  qt = p.T / BQ - 1 - w / BH;
+  h = (w % BH) % p.NH;
+  b = (w % BH) / p.NH;
+  return true;
+}
+
 __global__ void __launch_bounds__(THREADS, 2)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ Params p) {
   pdl_launch_dependents();
@@ -133,26 +164,22 @@ __global__ void __launch_bounds__(THREADS, 2)
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = bars + 3;
-  uint64_t* v_full = bars + 5;
-  uint64_t* v_empty = bars + 6;
-  uint64_t* s_full = bars + 7;
-  uint64_t* p_full = bars + 8;
-  uint64_t* pv_full = bars + 9;
-  uint64_t* mma_done = bars + 10;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* k_empty = bars + 4;
+  uint64_t* v_full = bars + 6;
+  uint64_t* v_empty = bars + 7;
+  uint64_t* s_full = bars + 8;
+  uint64_t* p_full = bars + 9;
+  uint64_t* pv_full = bars + 10;
+  uint64_t* mma_done = bars + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nqt = p.T / BQ;
-  const int qt = nqt - 1 - (int)blockIdx.x;  // longest rows first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int nkt = qt + 1;                    // key tiles 0..qt
-  const int row0 = b * p.T + qt * BQ;        // first query row in (B*T)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < 2; s++) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -160,7 +187,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     mbar_init(v_full, 1);
     mbar_init(v_empty, 1);
     mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    mbar_init(p_full, 4);  // one arrival per softmax warp
     mbar_init(pv_full, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -178,42 +205,54 @@ __global__ void __launch_bounds__(THREADS, 2)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the first global-memory access comes after this
 
+  // Barrier phases run on across work items: item n of this CTA uses phase n
+  // of q_full/q_empty; its key tiles continue the running tile count g of the
+  // K ring (stage g & 1), the V buffer and s_full/p_full/pv_full.
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      mbar_expect_tx(q_full, TILE_BYTES);
-      tma_load_2d(smem + OFF_Q, &tmQKV, h * HS, row0, q_full);
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < nkt; j++) {
-        const int s = j & 1;
-        const int krow = b * p.T + j * BKV;
-        if (!mbar_wait(&k_empty[s], ((j >> 1) & 1) ^ 1, abort_flag, p.err)) break;
-        mbar_expect_tx(&k_full[s], TILE_BYTES);
-        tma_load_2d(smem + OFF_K + s * TILE_BYTES, &tmQKV, p.C + h * HS, krow, &k_full[s]);
-        k_issued = j + 1;
-        if (!mbar_wait(v_empty, (j & 1) ^ 1, abort_flag, p.err)) break;
-        mbar_expect_tx(v_full, TILE_BYTES);
-        tma_load_2d(smem + OFF_V, &tmQKV, 2 * p.C + h * HS, krow, v_full);
-        v_issued = j + 1;
+      int nq = 0, nk = 0, nv = 0;  // Q, K and V tiles issued (nk - nv is 0 or 1)
+      int qt, h, b;
+      bool ok = true;
+      for (int r = 0; ok && fwd_item(p, r, qt, h, b); r++) {
+        ok = mbar_wait(q_empty, (r & 1) ^ 1, abort_flag, p.err);
+        if (!ok) break;
+        mbar_expect_tx(q_full, TILE_BYTES);
+        tma_load_2d(smem + OFF_Q, &tmQKV, h * HS, b * p.T + qt * BQ, q_full);
+        nq++;
+        for (int j = 0; j <= qt; j++) {
+          const int krow = b * p.T + j * BKV;
+          ok = mbar_wait(&k_empty[nk & 1], ((nk >> 1) & 1) ^ 1, abort_flag, p.err);
+          if (!ok) break;
+          mbar_expect_tx(&k_full[nk & 1], TILE_BYTES);
+          tma_load_2d(smem + OFF_K + (nk & 1) * TILE_BYTES, &tmQKV, p.C + h * HS, krow, &k_full[nk & 1]);
+          nk++;
+          ok = mbar_wait(v_empty, (nv & 1) ^ 1, abort_flag, p.err);
+          if (!ok) break;
+          mbar_expect_tx(v_full, TILE_BYTES);
+          tma_load_2d(smem + OFF_V, &tmQKV, 2 * p.C + h * HS, krow, v_full);
+          nv++;
+        }
       }
       if (*abort_flag) {
-        mbar_wait_drain(q_full, 0);
-        for (int j = max(0, k_issued - 2); j < k_issued; j++) mbar_wait_drain(&k_full[j & 1], (j >> 1) & 1);
-        if (v_issued > 0) mbar_wait_drain(v_full, (v_issued - 1) & 1);
+        // wait for the copies still in flight before the CTA's memory goes away
+        if (nq > 0) mbar_wait_drain(q_full, (nq - 1) & 1);
+        for (int i = max(0, nk - 2); i < nk; i++) mbar_wait_drain(&k_full[i & 1], (i >> 1) & 1);
+        if (nv > 0) mbar_wait_drain(v_full, (nv - 1) & 1);
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    // Order per key tile j: wait for P_j (the softmax warps have also read
-    // S_j out of TMEM by then), issue S_{j+1} = Q K_{j+1}^T into the freed S
-    // columns, then O_j = P_j V_j.  The softmax warps get S_{j+1} while
-    // P_j V_j is still running.
+    // Per key tile j: wait for P_j (the softmax warps have also read S_j out
+    // of TMEM by then), issue S_{j+1} = Q K_{j+1}^T into the freed S columns,
+    // then O_j = P_j V_j.  The softmax warps get S_{j+1} while P_j V_j runs;
+    // the first S of the next item follows the last P V of this one.
     if (lane == 0) {
       const uint32_t sq = smem_u32(smem + OFF_Q), sp = smem_u32(smem + OFF_P), sv = smem_u32(smem + OFF_V);
       const uint32_t t_s = tmem, t_pv = tmem + 128;
-      auto issue_s = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!mbar_wait(&k_full[s], (j >> 1) & 1, abort_flag, p.err)) return false;
+      auto issue_s = [&](int g) -> bool {
+        const int s = g & 1;
+        if (!mbar_wait(&k_full[s], (g >> 1) & 1, abort_flag, p.err)) return false;
         tc_fence_after();
         const uint32_t sk = smem_u32(smem + OFF_K + s * TILE_BYTES);
         // S = Q K^T over the 64 head dims (four K = 16 steps along the 128-byte rows)
@@ -225,22 +264,35 @@ __global__ void __launch_bounds__(THREADS, 2)
         mma_commit(&k_empty[s]);
         return true;
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.err) && issue_s(0);
-      for (int j = 0; j < nkt && ok; j++) {
-        if (!mbar_wait(p_full, j & 1, abort_flag, p.err)) break;
-        tc_fence_after();
-        if (j + 1 < nkt && !issue_s(j + 1)) break;
-        if (!mbar_wait(v_full, j & 1, abort_flag, p.err)) break;
-        tc_fence_after();
-        // P (two 64-key chunks, K-major) times V (MN-major) over the 128 keys
+      int g = 0;
+      bool ok = true;
+      int qt, h, b;
+      for (int r = 0; ok && fwd_item(p, r, qt, h, b); r++) {
+        const int nkt = qt + 1;
+        ok = mbar_wait(q_full, r & 1, abort_flag, p.err) && issue_s(g);
+        if (ok && nkt == 1) mma_commit(q_empty);  // the item's last S reads Q
+        for (int j = 0; j < nkt && ok; j++, g++) {
+          ok = mbar_wait(p_full, g & 1, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          if (j + 1 < nkt) {
+            ok = issue_s(g + 1);
+            if (!ok) break;
+            if (j + 2 == nkt) mma_commit(q_empty);
+          }
+          ok = mbar_wait(v_full, g & 1, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          // P (two 64-key chunks, K-major) times V (MN-major) over the 128 keys
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; kk++) {
-          const uint32_t pa = sp + (kk >> 2) * TILE_BYTES + (kk & 3) * 32;
-          mma_bf16(t_pv, desc_sw128(pa, 16, 1024), desc_sw128(sv + kk * 2048, 8192, 1024), IDESC_PV,
-                   kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < BKV / 16; kk++) {
+            const uint32_t pa = sp + (kk >> 2) * TILE_BYTES + (kk & 3) * 32;
+            mma_bf16(t_pv, desc_sw128(pa, 16, 1024), desc_sw128(sv + kk * 2048, 8192, 1024), IDESC_PV,
+                     kk > 0 ? 1u : 0u);
+          }
+          mma_commit(pv_full);
+          mma_commit(v_empty);
         }
-        mma_commit(pv_full);
-        mma_commit(v_empty);
       }
       mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0);
@@ -248,22 +300,20 @@ __global__ void __launch_bounds__(THREADS, 2)
   } else {
     // ---------------- softmax + output: one query row per thread ----------------
     // Scores are kept in base 2: x = s * scale * log2(e), m = running max of x,
-    // P = 2^(x - m), l = running sum of the bf16-rounded P (the weights the
-    // P V product uses), O accumulated in registers in the basis of m.
-    // Tile j: (1) row max of S_j; (2) fold in P_{j-1} V_{j-1}, rescaled by the
-    // correction of tile j-1, which also frees the P buffer; (3) write P_j.
+    // P = 2^(x - m) rounded to bf16 for the P V product, l = running fp32 sum
+    // of P, O accumulated in registers in the basis of m.  Tile j: (1) row max
+    // of S_j; (2) fold in P_{j-1} V_{j-1}, rescaled by the correction of tile
+    // j-1, which also frees the P buffer; (3) write P_j.  Waits are decided
+    // per warp (the TMEM loads are warp-collective); the warps meet only at
+    // the end of the kernel, so a timeout cannot split a barrier.
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;  // row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const uint32_t t_s = tmem + lane_off, t_pv = tmem + 128 + lane_off;
     const float sl2 = p.scale * 1.4426950408889634f;  // scale * log2(e)
     const float2 sl2v = make_float2(sl2, sl2);
-    float o[HS];
-#pragma unroll
-    for (int d = 0; d < HS; d++) o[d] = 0.f;
-    float m2 = -INFINITY, lrow = 0.f, corr_prev = 0.f;
-    bool ok = true;
     uint8_t* prow = smem + OFF_P + r * 128;
+    float o[HS];
     auto fold_pv = [&](float corr) {
       float pv[HS];
       tmem_ld64(t_pv, pv);
@@ -274,74 +324,82 @@ __global__ void __launch_bounds__(THREADS, 2)
         o[d + 1] = u.y;
       }
     };
-    for (int j = 0; j < nkt; j++) {
-      if (!tc::epi_bar_and<128>(mbar_wait(s_full, j & 1, abort_flag, p.err))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const bool diag = j == qt;  // keys k > r of the diagonal tile follow the query
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int c = 0; c < BKV / 64; c++) {
-        float sv[64];
-        tmem_ld64(t_s + c * 64, sv);
-        if (diag) mask_after(sv, r - c * 64);
+    int g = 0;
+    bool ok = true;
+    int qt, h, b;
+    for (int it = 0; ok && fwd_item(p, it, qt, h, b); it++) {
+      const int nkt = qt + 1;
 #pragma unroll
-        for (int k = 0; k < 64; k += 8) {
-          mx[0] = max3(mx[0], sv[k], sv[k + 1]);
-          mx[1] = max3(mx[1], sv[k + 2], sv[k + 3]);
-          mx[2] = max3(mx[2], sv[k + 4], sv[k + 5]);
-          mx[3] = max3(mx[3], sv[k + 6], sv[k + 7]);
-        }
-      }
-      const float mnew = fmaxf(m2, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
-      const float corr = ex2(m2 - mnew);  // 0 on the first tile (m2 = -inf)
-      if (j > 0) {
-        if (!tc::epi_bar_and<128>(mbar_wait(pv_full, (j - 1) & 1, abort_flag, p.err))) {
+      for (int d = 0; d < HS; d++) o[d] = 0.f;
+      float m2 = -INFINITY, lrow = 0.f, corr_prev = 0.f;
+      for (int j = 0; j < nkt; j++, g++) {
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full, g & 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        fold_pv(corr_prev);
-      }
-      const float2 nm = make_float2(-mnew, -mnew);
-      float ls0 = 0.f, ls1 = 0.f;
+        const bool diag = j == qt;  // keys k > r of the diagonal tile follow the query
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-      for (int c = 0; c < BKV / 64; c++) {
-        float sv[64];
-        tmem_ld64(t_s + c * 64, sv);
-        if (diag) mask_after(sv, r - c * 64);
+        for (int c = 0; c < BKV / 64; c++) {
+          float sv[64];
+          tmem_ld64(t_s + c * 64, sv);
+          if (diag) mask_after(sv, r - c * 64);
 #pragma unroll
-        for (int g = 0; g < 8; g++) {  // 8 keys = one 16-byte group of the swizzled row
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; e++) {
-            const int k = g * 8 + 2 * e;
-            const float2 x = fma2(make_float2(sv[k], sv[k + 1]), sl2v, nm);
-            w[e] = cvt_bf16x2(ex2(x.x), ex2(x.y));
-            ls0 += __uint_as_float(w[e] << 16);
-            ls1 += __uint_as_float(w[e] & 0xffff0000u);
+          for (int k = 0; k < 64; k += 8) {
+            mx[0] = max3(mx[0], sv[k], sv[k + 1]);
+            mx[1] = max3(mx[1], sv[k + 2], sv[k + 3]);
+            mx[2] = max3(mx[2], sv[k + 4], sv[k + 5]);
+            mx[3] = max3(mx[3], sv[k + 6], sv[k + 7]);
           }
-          *reinterpret_cast<uint4*>(prow + c * TILE_BYTES + ((g ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        const float mnew = fmaxf(m2, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
+        const float corr = ex2(m2 - mnew);  // 0 on the first tile (m2 = -inf)
+        if (j > 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait(pv_full, (g - 1) & 1, abort_flag, p.err))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          fold_pv(corr_prev);
+        }
+        const float2 nm = make_float2(-mnew, -mnew);
+        float2 ls = make_float2(0.f, 0.f);
+#pragma unroll 1
+        for (int c = 0; c < BKV / 64; c++) {
+          float sv[64];
+          tmem_ld64(t_s + c * 64, sv);
+          if (diag) mask_after(sv, r - c * 64);
+#pragma unroll
+          for (int gg = 0; gg < 8; gg++) {  // 8 keys = one 16-byte group of the swizzled row
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+              const int k = gg * 8 + 2 * e;
+              const float2 x = fma2(make_float2(sv[k], sv[k + 1]), sl2v, nm);
+              const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+              w[e] = cvt_bf16x2(pp.x, pp.y);
+              ls = add2(ls, pp);
+            }
+            *reinterpret_cast<uint4*>(prow + c * TILE_BYTES + ((gg ^ (r & 7)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        lrow = lrow * corr + (ls.x + ls.y);
+        m2 = mnew;
+        corr_prev = corr;
+        // make the generic-proxy P writes visible to the tensor core
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        tc::mbar_arrive_warp(p_full);
       }
-      lrow = lrow * corr + (ls0 + ls1);
-      m2 = mnew;
-      corr_prev = corr;
-      // make the generic-proxy P writes visible to the tensor core
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc_fence_before();
-      mbar_arrive(p_full);
-    }
-    ok = tc::epi_bar_and<128>(ok && mbar_wait(pv_full, (nkt - 1) & 1, abort_flag, p.err));
-    if (ok) {
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(pv_full, (g - 1) & 1, abort_flag, p.err));
+      if (!ok) break;
       tc_fence_after();
       fold_pv(corr_prev);
-    }
-    if (tc::epi_bar_and<128>(ok && !*abort_flag)) {
       const float inv = 1.f / lrow;
-      const size_t yo = (size_t)(row0 + r) * p.C + h * HS;
+      const size_t yo = (size_t)(b * p.T + qt * BQ + r) * p.C + h * HS;
 #pragma unroll
       for (int d = 0; d < HS; d += 4)
         *reinterpret_cast<float4*>(p.y + yo + d) = make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
@@ -365,36 +423,96 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
 }
 
-
 struct BwdParams {
   int B, T, C, NH;
   float scale;
-  const float2* LD;  // (B, NH, T) pairs (-lse * log2 e, D)
-  float* dqkv;       // (B, T, 3C) fp32
+  const float2* LD;  // (B, NH, T) pairs (-lse * log2 e, -D)
+  float* dqkv;       // (B, T, 3C) fp32, or NULL
   uint16_t* dqkv_bf; // (B, T, 3C) bf16 copy, or NULL
+  // or NULL: colsum[(b T/128 + tile) 3C + c] = the sum of dqkv(b, t, c) over
+  // the 128 positions t of that tile (the first stage of the QKV bias gradient)
+  float* colsum;
   int* err;
 };
 
-constexpr int BWD_THREADS = 320;  // producer warp, MMA warp, 8 softmax warps
+// Column sums of v[0..31] over the 32 lanes of the warp (lane = row): on
+// return lane l holds the sum of column l.  Five halving exchange steps,
+// 31 shuffles, a fixed order.  v is overwritten.
+GPT2_DEV float warp_colsum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool hi = (lane & w) != 0;
+#pragma unroll
+    for (int k = 0; k < w; k++) {
+      const float send = hi ? v[k] : v[k + w];
+      const float keep = hi ? v[k + w] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+
+constexpr int BWD_SOFTMAX_WARPS = 16;  // four per TMEM lane quarter, 16 columns each
+constexpr int BWD_THREADS = 64 + 32 * BWD_SOFTMAX_WARPS;  // + producer warp, MMA warp
+constexpr int BWD_CW = 16;  // sub-tile columns per softmax warp
 constexpr int SUB = 64;           // queries (dK/dV) or keys (dQ) per sub-tile
 
-// (a.x + b.x, a.y + b.y) and (a.x b.x, a.y b.y), one paired instruction each
-GPT2_DEV float2 add2(float2 a, float2 b) {
-  uint64_t d;
-  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n add.rn.f32x2 %0, ra, rb;\n}"
-      : "=l"(d)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
-}
-GPT2_DEV float2 mul2(float2 a, float2 b) {
-  uint64_t d;
-  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n mul.rn.f32x2 %0, ra, rb;\n}"
-      : "=l"(d)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+// 16 consecutive fp32 TMEM columns of the warp's 32 lanes
+GPT2_DEV void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
 
-// 32 columns from each of two TMEM addresses, one wait for both loads
+// 16 columns from each of two TMEM addresses, one wait for both loads
+GPT2_DEV void tmem_ld16x2(uint32_t a0, uint32_t a1, float* v0, float* v1) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(a0), "r"(a1)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; i++) {
+    v0[i] = __uint_as_float(r[i]);
+    v1[i] = __uint_as_float(r[16 + i]);
+  }
+}
+
+// Column sums of v[0..15] over the 32 lanes of the warp (lane = row): on
+// return lane l holds the sum of column l % 16.  Four halving exchange steps
+// within each 16-lane half, then the two halves; 16 shuffles, a fixed order.
+GPT2_DEV float warp_colsum16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+    const bool hi = (lane & w) != 0;
+#pragma unroll
+    for (int k = 0; k < w; k++) {
+      const float send = hi ? v[k] : v[k + w];
+      const float keep = hi ? v[k + w] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
+// Writes 16 bf16 values (8 packed words) at columns 16 qs .. 16 qs + 15 of row
+// r of a K-major, 128-byte-swizzled tile with 64-column (128-byte) rows.
+GPT2_DEV void st_quarter_row_sw128(uint8_t* tile, int r, int qs, const uint32_t (&w)[8]) {
+#pragma unroll
+  for (int g = 0; g < 2; g++)
+    *reinterpret_cast<uint4*>(tile + r * 128 + (((qs * 2 + g) ^ (r & 7)) << 4)) =
+        make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+}
+
 GPT2_DEV void tmem_ld32x2(uint32_t a0, uint32_t a1, float* v0, float* v1) {
   uint32_t r[64];
   asm volatile(
@@ -450,11 +568,55 @@ constexpr uint32_t IDESC_ACC = IDESC_PV;  // 128 x 64 accumulation, B MN-major
 //       tiles at or before it in sub-tiles of 64 keys: S = Q K^T, dP = dO V^T,
 //       dS staged, dQ += dS K in TMEM.
 // The MMA warp issues the scores of sub-tile i+1 before the products of
-// sub-tile i, so the tensor core computes the next scores while the eight
-// softmax warps (two per TMEM lane quarter, 32 columns each) work on the
+// sub-tile i, so the tensor core computes the next scores while the sixteen
+// softmax warps (four per TMEM lane quarter, 16 columns each) work on the
 // current ones.  Operand tiles come from the bf16 copies of qkv and of dO
 // (the gradient of the attention output, (B*T, C)) through TMA maps with
 // 64 x 128 boxes; a 64-row sub-tile starts 8 KB into its 128-row tile.
+// The per-query pairs LD[b,h,t] = (-lse log2 e, -D) with D = sum_d dO y over
+// the head's 64 dims (the rowsum the backward subtracts from dP).  One warp
+// per token: lane l reads dims 128 k + 4 l .. +3 of dO and y (all loads
+// issued before any sum), so each 128-dim chunk holds two heads, summed over
+// 16 lanes each.
+constexpr int LD_WARPS = 8;
+template <int MAXK>  // C <= 128 MAXK
+__global__ void __launch_bounds__(LD_WARPS * 32)
+    attn_bwd_ld_kernel(float2* __restrict__ LD, const float* __restrict__ lse, const float* __restrict__ dy,
+                       const float* __restrict__ y, int B, int T, int C) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * LD_WARPS + (threadIdx.x >> 5);  // token b*T + t
+  if (row >= (long long)B * T) return;
+  const int b = (int)(row / T), t = (int)(row % T), NH = C / HS;
+  const float* dr = dy + row * C;
+  const float* yr = y + row * C;
+  float sum[MAXK];
+#pragma unroll
+  for (int k = 0; k < MAXK; k++) {
+    const int d = 128 * k + 4 * lane;
+    sum[k] = 0.f;
+    if (d < C) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(dr + d));
+      const float4 c = __ldg(reinterpret_cast<const float4*>(yr + d));
+      sum[k] = a.x * c.x + a.y * c.y + a.z * c.z + a.w * c.w;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < MAXK; k++) {
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) sum[k] += __shfl_xor_sync(0xffffffffu, sum[k], o);
+  }
+#pragma unroll
+  for (int k = 0; k < MAXK; k++) {
+    const int d = 128 * k + 4 * lane, h = 2 * k + (lane >> 4);
+    if ((lane & 15) == 0 && d < C) {
+      const size_t i = ((size_t)b * NH + h) * T + t;
+      LD[i] = make_float2(-lse[i] * 1.4426950408889634f, -sum[k]);
+    }
+  }
+}
+
 namespace dkv {
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + TILE_BYTES;
@@ -463,7 +625,7 @@ constexpr int OFF_DO = OFF_Q + 2 * TILE_BYTES;     // 2 stages
 constexpr int SUB_BYTES = 128 * SUB * 2;           // 16 KB: a 128 x 64 bf16 P^T or dS^T
 constexpr int OFF_PT = OFF_DO + 2 * TILE_BYTES;    // 2 buffers
 constexpr int OFF_DST = OFF_PT + 2 * SUB_BYTES;    // 2 buffers
-constexpr int LD_BYTES = 128 * 8;                  // (-lse log2 e, D) of one query tile
+constexpr int LD_BYTES = 128 * 8;                  // (-lse log2 e, -D) of one query tile
 constexpr int OFF_LD = OFF_DST + 2 * SUB_BYTES;    // 2 stages
 constexpr int OFF_BAR = OFF_LD + 2 * LD_BYTES;
 // kv_full, qd_full[2], qd_empty[2], s_full[2], st_ready[2], pt_free[2], mma_done
@@ -504,7 +666,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_init(&qd_full[s], 1);
       mbar_init(&qd_empty[s], 1);
       mbar_init(&s_full[s], 1);
-      mbar_init(&st_ready[s], 256);
+      mbar_init(&st_ready[s], BWD_SOFTMAX_WARPS);  // one arrival per softmax warp
       mbar_init(&pt_free[s], 1);
     }
     mbar_init(mma_done, 1);
@@ -594,7 +756,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_wait_drain(mma_done, 0);
     }
   } else {
-    const int q4 = warp & 3, hf = (warp - 2) >> 2;
+    const int q4 = warp & 3, qs = (warp - 2) >> 2;  // TMEM lane quarter; 16-column slice
     const int r = q4 * 32 + lane;  // key row within the tile = TMEM lane
     const int k = kt * BKV + r;    // key position
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -603,62 +765,82 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     bool ok = true;
     for (int i = 0; i < nsub; i++) {
       const int it = i >> 1, s = it & 1, u = i & 1;
-      // one decision for all 256 threads: the TMEM loads below are warp-collective
+      // one decision per warp: the TMEM loads below are warp-collective
       const bool got = mbar_wait(&s_full[i & 1], (i >> 1) & 1, abort_flag, p.err) &&
                        mbar_wait(&qd_full[s], (it >> 1) & 1, abort_flag, p.err) &&
                        (i < 2 || mbar_wait(&pt_free[i & 1], ((i - 2) >> 1) & 1, abort_flag, p.err));
-      if (!tc::epi_bar_and<256>(got)) {
+      if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float st[32], dpt[32];
-      const uint32_t t_st = tmem + (i & 1) * 128 + lane_off + hf * 32;
-      tmem_ld32x2(t_st, t_st + SUB, st, dpt);
-      // queries u*64 + hf*32 + c of this query tile; before the key (masked) only in the first
-      const float4* ld = reinterpret_cast<const float4*>(smem + OFF_LD + s * LD_BYTES) + (u * SUB + hf * 32) / 2;
+      float st[BWD_CW], dpt[BWD_CW];
+      const uint32_t t_st = tmem + (i & 1) * 128 + lane_off + qs * BWD_CW;
+      tmem_ld16x2(t_st, t_st + SUB, st, dpt);
+      // queries u*64 + qs*16 + c of this query tile; before the key (masked) only in the first
+      const float4* ld = reinterpret_cast<const float4*>(smem + OFF_LD + s * LD_BYTES) + (u * SUB + qs * BWD_CW) / 2;
       if (it == 0) {
-        const int lim = r - u * SUB - hf * 32;  // column c is masked when c < lim
+        const int lim = r - u * SUB - qs * BWD_CW;  // column c is masked when c < lim
 #pragma unroll
-        for (int c = 0; c < 32; c++)
+        for (int c = 0; c < BWD_CW; c++)
           if (c < lim) st[c] = -INFINITY;
       }
-      uint32_t wp[16], wd[16];
+      uint32_t wp[BWD_CW / 2], wd[BWD_CW / 2];
 #pragma unroll
-      for (int e = 0; e < 16; e++) {
-        const float4 v = ld[e];  // (-lse2, D) of queries 2e, 2e+1
+      for (int e = 0; e < BWD_CW / 2; e++) {
+        const float4 v = ld[e];  // (-lse2, -D) of queries 2e, 2e+1
         const float2 x = fma2(make_float2(st[2 * e], st[2 * e + 1]), sl2v, make_float2(v.x, v.z));
         const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-        const float2 ds = mul2(pp, add2(make_float2(dpt[2 * e], dpt[2 * e + 1]), make_float2(-v.y, -v.w)));
+        const float2 ds = mul2(pp, add2(make_float2(dpt[2 * e], dpt[2 * e + 1]), make_float2(v.y, v.w)));
         wp[e] = cvt_bf16x2(pp.x, pp.y);
         wd[e] = cvt_bf16x2(ds.x, ds.y);
       }
-      st_half_row_sw128(smem + OFF_PT + (i & 1) * SUB_BYTES, r, hf, wp);
-      st_half_row_sw128(smem + OFF_DST + (i & 1) * SUB_BYTES, r, hf, wd);
+      st_quarter_row_sw128(smem + OFF_PT + (i & 1) * SUB_BYTES, r, qs, wp);
+      st_quarter_row_sw128(smem + OFF_DST + (i & 1) * SUB_BYTES, r, qs, wd);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(&st_ready[i & 1]);
+      tc::mbar_arrive_warp(&st_ready[i & 1]);
     }
-    if (tc::epi_bar_and<256>(ok && mbar_wait(mma_done, 0, abort_flag, p.err) && !*abort_flag)) {
+    if (tc::epi_bar_and<32 * BWD_SOFTMAX_WARPS>(ok && mbar_wait(mma_done, 0, abort_flag, p.err) && !*abort_flag)) {
       tc_fence_after();
-      float dv[32], dk[32];
-      tmem_ld32x2(T_DV + lane_off + hf * 32, T_DK + lane_off + hf * 32, dv, dk);
-      const size_t o = ((size_t)b * p.T + k) * 3 * p.C + h * HS + hf * 32;
+      float dv[BWD_CW], dk[BWD_CW];
+      tmem_ld16x2(T_DV + lane_off + qs * BWD_CW, T_DK + lane_off + qs * BWD_CW, dv, dk);
 #pragma unroll
-      for (int d = 0; d < 32; d += 4) {
-        *reinterpret_cast<float4*>(p.dqkv + o + p.C + d) =
-            make_float4(dk[d] * p.scale, dk[d + 1] * p.scale, dk[d + 2] * p.scale, dk[d + 3] * p.scale);
-        *reinterpret_cast<float4*>(p.dqkv + o + 2 * p.C + d) = make_float4(dv[d], dv[d + 1], dv[d + 2], dv[d + 3]);
+      for (int d = 0; d < BWD_CW; d++) dk[d] *= p.scale;
+      const size_t o = ((size_t)b * p.T + k) * 3 * p.C + h * HS + qs * BWD_CW;
+      if (p.dqkv) {
+#pragma unroll
+        for (int d = 0; d < BWD_CW; d += 4) {
+          *reinterpret_cast<float4*>(p.dqkv + o + p.C + d) = make_float4(dk[d], dk[d + 1], dk[d + 2], dk[d + 3]);
+          *reinterpret_cast<float4*>(p.dqkv + o + 2 * p.C + d) = make_float4(dv[d], dv[d + 1], dv[d + 2], dv[d + 3]);
+        }
       }
       if (p.dqkv_bf) {
 #pragma unroll
-        for (int d = 0; d < 32; d += 8) {
+        for (int d = 0; d < BWD_CW; d += 8) {
           *reinterpret_cast<uint4*>(p.dqkv_bf + o + p.C + d) =
-              make_uint4(cvt_bf16x2(dk[d] * p.scale, dk[d + 1] * p.scale), cvt_bf16x2(dk[d + 2] * p.scale, dk[d + 3] * p.scale),
-                         cvt_bf16x2(dk[d + 4] * p.scale, dk[d + 5] * p.scale), cvt_bf16x2(dk[d + 6] * p.scale, dk[d + 7] * p.scale));
+              make_uint4(cvt_bf16x2(dk[d], dk[d + 1]), cvt_bf16x2(dk[d + 2], dk[d + 3]), cvt_bf16x2(dk[d + 4], dk[d + 5]),
+                         cvt_bf16x2(dk[d + 6], dk[d + 7]));
           *reinterpret_cast<uint4*>(p.dqkv_bf + o + 2 * p.C + d) =
               make_uint4(cvt_bf16x2(dv[d], dv[d + 1]), cvt_bf16x2(dv[d + 2], dv[d + 3]), cvt_bf16x2(dv[d + 4], dv[d + 5]),
                          cvt_bf16x2(dv[d + 6], dv[d + 7]));
+        }
+      }
+      if (p.colsum) {
+        // the 128 key rows' column sums: warp butterflies, then the four lane
+        // quarters in order, through the (-lse, -D) staging area (free now)
+        float* red = reinterpret_cast<float*>(smem + OFF_LD);  // [dK, dV][qs][q4][16]
+        const float sk = warp_colsum16(dk, lane), sv = warp_colsum16(dv, lane);
+        if (lane < 16) {
+          red[((0 * 4 + qs) * 4 + q4) * 16 + lane] = sk;
+          red[((1 * 4 + qs) * 4 + q4) * 16 + lane] = sv;
+        }
+        tc::epi_bar<32 * BWD_SOFTMAX_WARPS>();
+        const int t2 = threadIdx.x - 64;
+        if (t2 < 128) {
+          const int arr = t2 >> 6, col = t2 & 63, base = (arr * 4 + (col >> 4)) * 4 * 16 + (col & 15);
+          const float sum = ((red[base] + red[base + 16]) + red[base + 32]) + red[base + 48];
+          p.colsum[((size_t)b * nt + kt) * 3 * p.C + (1 + arr) * p.C + h * HS + col] = sum;
         }
       }
     }
@@ -719,7 +901,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
       mbar_init(&s_full[s], 1);
-      mbar_init(&ds_ready[s], 256);
+      mbar_init(&ds_ready[s], BWD_SOFTMAX_WARPS);  // one arrival per softmax warp
       mbar_init(&ds_free[s], 1);
     }
     mbar_init(mma_done, 1);
@@ -799,60 +981,76 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_wait_drain(mma_done, 0);
     }
   } else {
-    const int q4 = warp & 3, hf = (warp - 2) >> 2;
+    const int q4 = warp & 3, qs = (warp - 2) >> 2;  // TMEM lane quarter; 16-column slice
     const int r = q4 * 32 + lane;  // query row within the tile = TMEM lane
     const int t = qt * BQ + r;     // query position
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const float sl2 = p.scale * 1.4426950408889634f;
-    const float2 ldr = p.LD[((size_t)b * p.NH + h) * p.T + t];  // (-lse2, D) of this query
-    const float2 sl2v = make_float2(sl2, sl2), nlv = make_float2(ldr.x, ldr.x), ndv = make_float2(-ldr.y, -ldr.y);
+    const float2 ldr = p.LD[((size_t)b * p.NH + h) * p.T + t];  // (-lse2, -D) of this query
+    const float2 sl2v = make_float2(sl2, sl2), nlv = make_float2(ldr.x, ldr.x), ndv = make_float2(ldr.y, ldr.y);
     bool ok = true;
     for (int i = 0; i < nsub; i++) {
       const int j = i >> 1, u = i & 1;
       const bool got = mbar_wait(&s_full[i & 1], (i >> 1) & 1, abort_flag, p.err) &&
                        (i < 2 || mbar_wait(&ds_free[i & 1], ((i - 2) >> 1) & 1, abort_flag, p.err));
-      if (!tc::epi_bar_and<256>(got)) {
+      if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float sv[32], dp[32];
-      const uint32_t t_s = tmem + (i & 1) * 128 + lane_off + hf * 32;
-      tmem_ld32x2(t_s, t_s + SUB, sv, dp);
-      if (j == qt) {  // keys after the query are masked: column c when u*64 + hf*32 + c > r
-        const int lim = r - u * SUB - hf * 32;
+      float sv[BWD_CW], dp[BWD_CW];
+      const uint32_t t_s = tmem + (i & 1) * 128 + lane_off + qs * BWD_CW;
+      tmem_ld16x2(t_s, t_s + SUB, sv, dp);
+      if (j == qt) {  // keys after the query are masked: column c when u*64 + qs*16 + c > r
+        const int lim = r - u * SUB - qs * BWD_CW;
 #pragma unroll
-        for (int c = 0; c < 32; c++)
+        for (int c = 0; c < BWD_CW; c++)
           if (c > lim) sv[c] = -INFINITY;
       }
-      uint32_t wd[16];
+      uint32_t wd[BWD_CW / 2];
 #pragma unroll
-      for (int e = 0; e < 16; e++) {
+      for (int e = 0; e < BWD_CW / 2; e++) {
         const float2 x = fma2(make_float2(sv[2 * e], sv[2 * e + 1]), sl2v, nlv);
         const float2 pp = make_float2(ex2(x.x), ex2(x.y));
         const float2 ds = mul2(pp, add2(make_float2(dp[2 * e], dp[2 * e + 1]), ndv));
         wd[e] = cvt_bf16x2(ds.x, ds.y);
       }
-      st_half_row_sw128(smem + OFF_DS + (i & 1) * SUB_BYTES, r, hf, wd);
+      st_quarter_row_sw128(smem + OFF_DS + (i & 1) * SUB_BYTES, r, qs, wd);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(&ds_ready[i & 1]);
+      tc::mbar_arrive_warp(&ds_ready[i & 1]);
     }
-    if (tc::epi_bar_and<256>(ok && mbar_wait(mma_done, 0, abort_flag, p.err) && !*abort_flag)) {
+    if (tc::epi_bar_and<32 * BWD_SOFTMAX_WARPS>(ok && mbar_wait(mma_done, 0, abort_flag, p.err) && !*abort_flag)) {
       tc_fence_after();
-      float dq[32];
-      tmem_ld32(T_DQ + lane_off + hf * 32, dq);
-      const size_t o = ((size_t)b * p.T + t) * 3 * p.C + h * HS + hf * 32;
+      float dq[BWD_CW];
+      tmem_ld16(T_DQ + lane_off + qs * BWD_CW, dq);
 #pragma unroll
-      for (int d = 0; d < 32; d += 4)
-        *reinterpret_cast<float4*>(p.dqkv + o + d) =
-            make_float4(dq[d] * p.scale, dq[d + 1] * p.scale, dq[d + 2] * p.scale, dq[d + 3] * p.scale);
+      for (int d = 0; d < BWD_CW; d++) dq[d] *= p.scale;
+      const size_t o = ((size_t)b * p.T + t) * 3 * p.C + h * HS + qs * BWD_CW;
+      if (p.dqkv) {
+#pragma unroll
+        for (int d = 0; d < BWD_CW; d += 4)
+          *reinterpret_cast<float4*>(p.dqkv + o + d) = make_float4(dq[d], dq[d + 1], dq[d + 2], dq[d + 3]);
+      }
       if (p.dqkv_bf) {
 #pragma unroll
-        for (int d = 0; d < 32; d += 8)
+        for (int d = 0; d < BWD_CW; d += 8)
           *reinterpret_cast<uint4*>(p.dqkv_bf + o + d) =
-              make_uint4(cvt_bf16x2(dq[d] * p.scale, dq[d + 1] * p.scale), cvt_bf16x2(dq[d + 2] * p.scale, dq[d + 3] * p.scale),
-                         cvt_bf16x2(dq[d + 4] * p.scale, dq[d + 5] * p.scale), cvt_bf16x2(dq[d + 6] * p.scale, dq[d + 7] * p.scale));
+              make_uint4(cvt_bf16x2(dq[d], dq[d + 1]), cvt_bf16x2(dq[d + 2], dq[d + 3]), cvt_bf16x2(dq[d + 4], dq[d + 5]),
+                         cvt_bf16x2(dq[d + 6], dq[d + 7]));
+      }
+      if (p.colsum) {
+        // the 128 query rows' column sums, through the dS buffers (free now)
+        float* red = reinterpret_cast<float*>(smem + OFF_DS);  // [qs][q4][16]
+        const float sq = warp_colsum16(dq, lane);
+        if (lane < 16) red[(qs * 4 + q4) * 16 + lane] = sq;
+        tc::epi_bar<32 * BWD_SOFTMAX_WARPS>();
+        const int t2 = threadIdx.x - 64;
+        if (t2 < 64) {
+          const int base = (t2 >> 4) * 4 * 16 + (t2 & 15);
+          const float sum = ((red[base] + red[base + 16]) + red[base + 32]) + red[base + 48];
+          p.colsum[((size_t)b * nt + qt) * 3 * p.C + h * HS + t2] = sum;
+        }
       }
     }
   }

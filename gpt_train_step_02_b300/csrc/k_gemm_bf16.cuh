@@ -132,7 +132,8 @@ GPT2_DEV void unit_coords(const Params& p, int unit, int& m0, int& tn, int& z, i
   tn = tile / p.tiles_m;
 }
 
-template <int BN>
+// OP: the epilogue kind (a GemmEpi value), fixed per instantiation
+template <int BN, int OP>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ Params p) {
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], EPI_THREADS);
+      mbar_init(&acc_empty[b], EPI_WARPS);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -294,11 +295,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (split)
           warp32_store_raw(p.partial + (size_t)z * p.M * p.N, p.N, stage, i0, j0, p.M, p.N, lane);
         else
-          warp32_epilogue(p.epi, stage, i0, j0, p.M, p.N, lane);
+          warp32_epilogue<OP>(p.epi, stage, i0, j0, p.M, p.N, lane);
       }
       // the accumulator is in registers / global memory now: hand it back
       tc_fence_before();
-      mbar_arrive(&acc_empty[buf]);
+      tc::mbar_arrive_warp(&acc_empty[buf]);
       if (split) {
         __threadfence();
         tc::epi_bar<EPI_THREADS>();
@@ -320,12 +321,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                   float4 b = __ldcg(reinterpret_cast<const float4*>(src + zz * plane));
                   acc.x += b.x; acc.y += b.y; acc.z += b.z; acc.w += b.w;
                 }
-                epi_store4(p.epi, ii, j, acc);
+                epi_store4<OP>(p.epi, ii, j, acc);
               } else {
                 for (int c = 0; c < 4 && j + c < p.N; c++) {
                   float a = __ldcg(src + c);
                   for (int zz = 1; zz < p.splits; zz++) a += __ldcg(src + c + zz * plane);
-                  epi_store(p.epi, ii, j + c, a);
+                  epi_store<OP>(p.epi, ii, j + c, a);
                 }
               }
             }

@@ -87,6 +87,17 @@ GPT2_DEV void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One arrival per warp (barriers initialised with a count of warps).  Each
+// lane makes its own writes visible first (fence.proxy.async for shared
+// memory the tensor core or TMA will read, tcgen05.fence::before_thread_sync
+// after TMEM reads); the warp barrier then orders them before lane 0's
+// release-arrive.  A per-thread arrive would be 32 serialised atomics on one
+// shared-memory word per warp.
+GPT2_DEV void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 GPT2_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -304,10 +315,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < RAW_STAGES; s++) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], SPLIT_THREADS);
+      mbar_init(&raw_empty[s], SPLIT_WARPS);
     }
     for (int s = 0; s < COMP_STAGES; s++) {
-      mbar_init(&comp_full[s], SPLIT_THREADS);
+      mbar_init(&comp_full[s], SPLIT_WARPS);
       mbar_init(&comp_empty[s], 1);
     }
     mbar_init(acc_full, 1);
@@ -404,11 +415,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int i = 0; i < nk; i++) {
       int s = i % RAW_STAGES, c = i % COMP_STAGES;
-      if (!mbar_wait(&raw_full[s], (i / RAW_STAGES) & 1, abort_flag, p.err)) {
-        ok = false;
-        break;
-      }
-      if (!mbar_wait(&comp_empty[c], ((i / COMP_STAGES) & 1) ^ 1, abort_flag, p.err)) {
+      // one decision per warp: its lanes arrive together below
+      if (!__all_sync(0xffffffffu, mbar_wait(&raw_full[s], (i / RAW_STAGES) & 1, abort_flag, p.err) &&
+                                       mbar_wait(&comp_empty[c], ((i / COMP_STAGES) & 1) ^ 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
@@ -428,8 +437,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         split_mnmajor(reinterpret_cast<const float*>(rb), hb, lb, t);
       // make the generic-proxy smem writes visible to the tensor core (async proxy)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&raw_empty[s]);
-      mbar_arrive(&comp_full[c]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&raw_empty[s]);
+        mbar_arrive(&comp_full[c]);
+      }
     }
     if (ok && nk > 0) ok = mbar_wait(acc_full, 0, abort_flag, p.err);
     // One decision for all epilogue warps (tcgen05.ld is warp-collective and
@@ -507,6 +519,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
+  }
+
     cluster_sync();  // peers keep their shared memory until every CTA has read it
   }
 

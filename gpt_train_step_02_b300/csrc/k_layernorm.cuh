@@ -60,12 +60,7 @@ __global__ void layernorm_fwd_kernel(float* __restrict__ y, uint16_t* __restrict
       o.w = (v[k].w - mu) * rs * ww.w + bb.w;
       if (y) *reinterpret_cast<float4*>(y + (size_t)warp * C + c) = o;
       if (ybf) {
-        ushort4 h;
-        h.x = to_bf16_bits(o.x);
-        h.y = to_bf16_bits(o.y);
-        h.z = to_bf16_bits(o.z);
-        h.w = to_bf16_bits(o.w);
-        *reinterpret_cast<ushort4*>(ybf + (size_t)warp * C + c) = h;
+        *reinterpret_cast<uint2*>(ybf + (size_t)warp * C + c) = make_uint2(bf16x2_bits(o.x, o.y), bf16x2_bits(o.z, o.w));
       }
     }
   }
@@ -99,7 +94,9 @@ __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
   float* my = sh + warp * nout * C;
   if (r < N) {
     const float mu = mean[r], rs = rstd[r];
-    float4 xv[LN_MAXV4], dv[LN_MAXV4];
+    // every load of the row (x, dy and the dx being accumulated into) is
+    // issued before the row reductions
+    float4 xv[LN_MAXV4], dv[LN_MAXV4], av[LN_MAXV4];
     float sg = 0.f, sgn = 0.f;
 #pragma unroll
     for (int k = 0; k < LN_MAXV4; k++) {
@@ -107,6 +104,7 @@ __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
       if (c < C) {
         xv[k] = *reinterpret_cast<const float4*>(x + (size_t)r * C + c);
         dv[k] = *reinterpret_cast<const float4*>(dy + (size_t)r * C + c);
+        av[k] = *reinterpret_cast<const float4*>(dx + (size_t)r * C + c);
       }
     }
 #pragma unroll
@@ -130,19 +128,14 @@ __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
         const float4 n = make_float4((xv[k].x - mu) * rs, (xv[k].y - mu) * rs, (xv[k].z - mu) * rs,
                                      (xv[k].w - mu) * rs);
         float4* o = reinterpret_cast<float4*>(dx + (size_t)r * C + c);
-        float4 a = *o;
+        float4 a = av[k];
         a.x += rs * (dv[k].x * ww.x - mg - n.x * mgn);
         a.y += rs * (dv[k].y * ww.y - mg - n.y * mgn);
         a.z += rs * (dv[k].z * ww.z - mg - n.z * mgn);
         a.w += rs * (dv[k].w * ww.w - mg - n.w * mgn);
         *o = a;
         if (dxbf) {
-          ushort4 hb;
-          hb.x = to_bf16_bits(a.x);
-          hb.y = to_bf16_bits(a.y);
-          hb.z = to_bf16_bits(a.z);
-          hb.w = to_bf16_bits(a.w);
-          *reinterpret_cast<ushort4*>(dxbf + (size_t)r * C + c) = hb;
+          *reinterpret_cast<uint2*>(dxbf + (size_t)r * C + c) = make_uint2(bf16x2_bits(a.x, a.y), bf16x2_bits(a.z, a.w));
         }
         *reinterpret_cast<float4*>(my + c) = make_float4(dv[k].x * n.x, dv[k].y * n.y, dv[k].z * n.z, dv[k].w * n.w);
         *reinterpret_cast<float4*>(my + C + c) = dv[k];

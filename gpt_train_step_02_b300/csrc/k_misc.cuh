@@ -288,14 +288,7 @@ __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g,
     reinterpret_cast<float4*>(p)[i] = pp;
     reinterpret_cast<float4*>(m)[i] = mm;
     reinterpret_cast<float4*>(v)[i] = vv;
-    if (pbf16) {
-      ushort4 o;
-      o.x = to_bf16_bits(pp.x);
-      o.y = to_bf16_bits(pp.y);
-      o.z = to_bf16_bits(pp.z);
-      o.w = to_bf16_bits(pp.w);
-      reinterpret_cast<ushort4*>(pbf16)[i] = o;
-    }
+    if (pbf16) reinterpret_cast<uint2*>(pbf16)[i] = make_uint2(bf16x2_bits(pp.x, pp.y), bf16x2_bits(pp.z, pp.w));
   }
 }
 

@@ -10,7 +10,11 @@
 #pragma once
 #include "common.cuh"
 
-#define XENT_THREADS 512
+// 1024 threads: at most two CTAs per SM, so the rows being processed
+// (2 x 148 x Vp x 4 bytes, 60 MB for GPT-2) stay in the 126 MB L2 and pass 2
+// re-reads them from there.  Each thread keeps four float4 loads in flight.
+#define XENT_THREADS 1024
+#define XENT_UNROLL 4
 
 GPT2_DEV void online_merge(float& m, float& s, float m2, float s2) {
   float mn = fmaxf(m, m2);
@@ -25,24 +29,32 @@ __global__ void __launch_bounds__(XENT_THREADS) xent_fused_kernel(
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float shm[XENT_THREADS / 32], shs[XENT_THREADS / 32];
-  int row = blockIdx.x;
+  const int row = blockIdx.x;
   const float* lr = logits + (size_t)row * Vp;
+  const float4* lr4 = reinterpret_cast<const float4*>(lr);
   float m = -INFINITY, s = 0.f;
-  int V4 = Vp >> 2;
-  for (int i = threadIdx.x; i < V4; i += XENT_THREADS) {
-    float4 x = reinterpret_cast<const float4*>(lr)[i];
-    const float* xv = &x.x;
+  const int V4 = Vp >> 2;
+  for (int i0 = threadIdx.x; i0 < V4; i0 += XENT_UNROLL * XENT_THREADS) {
+    float4 x[XENT_UNROLL];
 #pragma unroll
-    for (int k = 0; k < 4; k++) {
-      int v = i * 4 + k;
-      if (v < V) {
-        if (xv[k] > m) {
-          s = s * __expf(m - xv[k]) + 1.f;
-          m = xv[k];
-        } else {
-          s += __expf(xv[k] - m);
-        }
+    for (int u = 0; u < XENT_UNROLL; u++) {
+      const int i = i0 + u * XENT_THREADS;
+      x[u] = i < V4 ? lr4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+#pragma unroll
+    for (int u = 0; u < XENT_UNROLL; u++) {
+      const int v0 = 4 * (i0 + u * XENT_THREADS);
+      float a[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; k++)
+        if (v0 + k >= V) a[k] = -INFINITY;  // padded vocabulary columns
+      const float mx = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
+      if (mx == -INFINITY) continue;
+      if (mx > m) {
+        s *= __expf(m - mx);  // 0 while m = -inf
+        m = mx;
       }
+      s += __expf(a[0] - m) + __expf(a[1] - m) + __expf(a[2] - m) + __expf(a[3] - m);
     }
   }
   // warp combine
@@ -73,26 +85,37 @@ __global__ void __launch_bounds__(XENT_THREADS) xent_fused_kernel(
   __syncthreads();
   m = shm[0];
   s = shs[0];
-  int tgt = min(max(targets[row], 0), V - 1);
+  const int tgt = min(max(targets[row], 0), V - 1);
   if (threadIdx.x == 0) losses[row] = logf(s) + m - lr[tgt];
-  float inv = 1.f / s;
+  // pass 2: dlogits[v] = (exp(x_v - m) / s - [v == tgt]) dloss, in base 2:
+  // 2^(x_v log2 e - m log2 e) * (dloss / s); 0 for the padded columns
+  const float L2E = 1.4426950408889634f, mb = m * L2E, scale = dloss / s;
+  const int tgt4 = tgt >> 2, full4 = V >> 2;  // float4 i holds only real columns when i < full4
   float* dr = dlogits + (size_t)row * Vp;
-  for (int i = threadIdx.x; i < V4; i += XENT_THREADS) {
-    float4 x = reinterpret_cast<const float4*>(lr)[i];
-    float* xv = &x.x;
+  for (int i0 = threadIdx.x; i0 < V4; i0 += XENT_UNROLL * XENT_THREADS) {
+    float4 x[XENT_UNROLL];
 #pragma unroll
-    for (int k = 0; k < 4; k++) {
-      int v = i * 4 + k;
-      xv[k] = v < V ? (__expf(xv[k] - m) * inv - (v == tgt ? 1.f : 0.f)) * dloss : 0.f;
+    for (int u = 0; u < XENT_UNROLL; u++) {
+      const int i = i0 + u * XENT_THREADS;
+      if (i < V4) x[u] = lr4[i];
     }
-    if (dlogits) reinterpret_cast<float4*>(dr)[i] = x;
-    if (dlogits_bf) {
-      ushort4 hb;
-      hb.x = to_bf16_bits(x.x);
-      hb.y = to_bf16_bits(x.y);
-      hb.z = to_bf16_bits(x.z);
-      hb.w = to_bf16_bits(x.w);
-      reinterpret_cast<ushort4*>(dlogits_bf + (size_t)row * Vp)[i] = hb;
+#pragma unroll
+    for (int u = 0; u < XENT_UNROLL; u++) {
+      const int i = i0 + u * XENT_THREADS;
+      if (i >= V4) continue;
+      float* xv = &x[u].x;
+#pragma unroll
+      for (int k = 0; k < 4; k++) xv[k] = ex2f_fast(fmaf(xv[k], L2E, -mb)) * scale;
+      if (i >= full4) {  // the float4 that straddles V, and the padding
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          if (4 * i + k >= V) xv[k] = 0.f;
+      }
+      if (i == tgt4) xv[tgt & 3] -= dloss;
+      if (dlogits) reinterpret_cast<float4*>(dr)[i] = x[u];
+      if (dlogits_bf)
+        reinterpret_cast<uint2*>(dlogits_bf + (size_t)row * Vp)[i] =
+            make_uint2(bf16x2_bits(x[u].x, x[u].y), bf16x2_bits(x[u].z, x[u].w));
     }
   }
 }

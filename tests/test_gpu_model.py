@@ -300,6 +300,32 @@ def test_bf16_tensor_core_attention_small():
     m.close()
 
 
+def test_bf16_tensor_core_gradients():
+    """Every parameter gradient of one bf16 step on a workload that takes the
+    tensor-core attention (head size 64, T % 128 == 0), whose MLP input and
+    QKV bias gradients come from column sums taken in the matmul and
+    attention epilogues, against the fp32 oracle.  bf16 operand rounding
+    (u = 2^-9) through a few chained products gives about 1e-2 relative L2
+    per tensor; the bar is 3e-2."""
+    w = synth.Workload("grad_bf16_hs64", 2, 128, 2, 512, 512, 256, 2, 256, "bf16", "uniform", 1)
+    p0 = perturbed(w)
+    inp, tgt = synth.batch(w)
+    m = gpu_model(w)
+    m.set_params(p0)
+    o = oracle_model(w, p0)
+    lg = m.forward(inp, tgt)
+    lo = o.forward(inp, tgt)
+    assert abs(lg - lo) <= 2e-2, (lg, lo)
+    m.zero_grad()
+    m.backward()
+    o.zero_grad()
+    o.backward()
+    worst = check_grads(w, m.get_grads(), o.grads, tol=3e-2)
+    assert max(worst.values()) > 0.0  # bf16 rounding is visible, so the bf16 path really ran
+    m.close()
+    o.close()
+
+
 # ---------------------------------------------------------------------------
 # GPT-2 124M, fp32, B=4, T=64 (the workload of the pages' console log)
 # ---------------------------------------------------------------------------
