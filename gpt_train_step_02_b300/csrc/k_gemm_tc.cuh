@@ -519,8 +519,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-  }
-
     cluster_sync();  // peers keep their shared memory until every CTA has read it
   }
 
