@@ -35,7 +35,8 @@ GPT2_PREC_BF16 = 1
 
 # every symbol the header declares
 EXPORTS = [
-    "gpt2_arena_bytes", "gpt2_build", "gpt2_forward", "gpt2_forward_device", "gpt2_sync", "gpt2_zero_grad",
+    "gpt2_arena_bytes", "gpt2_build", "gpt2_forward", "gpt2_forward_device", "gpt2_sample", "gpt2_sync",
+    "gpt2_zero_grad",
     "gpt2_backward", "gpt2_update", "gpt2_train_step_device", "gpt2_free", "gpt2_num_parameters",
     "gpt2_get_params", "gpt2_set_params", "gpt2_get_grads", "gpt2_get_opt_state", "gpt2_set_opt_state",
     "gpt2_get_logits", "gpt2_last_launch_count", "gpt2_status_string", "gpt2_train_step", "gpt2_kernel_timer",
@@ -73,6 +74,7 @@ def lib() -> ct.CDLL:
             "gpt2_build": (I, [ct.POINTER(P), CFG, ct.c_uint64, I, I, P, SZ, P]),
             "gpt2_forward": (I, [P, P, P, I, I, P]),
             "gpt2_forward_device": (I, [P, P, P, I, I]),
+            "gpt2_sample": (I, [P, P, I, I, P]),
             "gpt2_sync": (I, [P, P]),
             "gpt2_zero_grad": (I, [P]),
             "gpt2_backward": (I, [P]),
@@ -158,6 +160,19 @@ def gpt2_forward(h, inputs: np.ndarray, targets: np.ndarray | None, want_loss: b
 
 def gpt2_forward_device(h, d_inputs: int, d_targets: int | None, B: int, T: int) -> None:
     _check(lib().gpt2_forward_device(h, d_inputs, d_targets, B, T), "gpt2_forward_device")
+
+
+def gpt2_sample(h, prompt: np.ndarray, n_total: int, coins: np.ndarray) -> np.ndarray:
+    """Generate tokens n_prompt .. n_total-1 after the prompt; coins: one
+    uniform draw in [0, 1) per generated token.  Returns all n_total ids."""
+    prompt = np.ascontiguousarray(prompt, dtype=np.int32).ravel()
+    coins = np.ascontiguousarray(coins, dtype=np.float32).ravel()
+    n_prompt = prompt.size
+    assert coins.size == n_total - n_prompt
+    tokens = np.zeros(n_total, np.int32)
+    tokens[:n_prompt] = prompt
+    _check(lib().gpt2_sample(h, _hptr(tokens), n_prompt, n_total, _hptr(coins)), "gpt2_sample")
+    return tokens
 
 
 def gpt2_sync(h) -> float:
@@ -264,6 +279,10 @@ class GPT2:
         B, T = d_inputs.shape
         self._order_after_torch()
         gpt2_forward_device(self.h, d_inputs.data_ptr(), None if d_targets is None else d_targets.data_ptr(), B, T)
+
+    def sample(self, prompt, n_total: int, coins) -> np.ndarray:
+        """The pages' generation loop; see gpt2_sample."""
+        return gpt2_sample(self.h, prompt, n_total, coins)
 
     def sync(self) -> float:
         return gpt2_sync(self.h)

@@ -11,6 +11,7 @@
 // activation arena never stores the (T,T) attention matrices: the attention
 // kernels keep only the per-row log-sum-exp and recompute probabilities in
 // the backward pass.
+#include <vector>
 #include <math.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -31,6 +32,7 @@
 #include "k_gemm_tc.cuh"
 #include "k_layernorm.cuh"
 #include "k_misc.cuh"
+#include "k_sample.cuh"
 #include "k_xent.cuh"
 
 #define EXPORT extern "C" __attribute__((visibility("default")))
@@ -555,7 +557,16 @@ static void mm_dw(gpt2_t* m, float* dW, Opnd dy, Opnd x, int N, int IC, int OC) 
 
 // db += column sums of dy (N, OC): chunks of BIAS_MIN_ROWS rows summed by
 // one thread per column, then the chunk partials finished in a fixed order.
+// Up to BIAS_DIRECT_ROWS rows the finishing kernel sums dy's rows itself
+// (32 warps, each striding over the rows): one launch instead of two.
+#define BIAS_DIRECT_ROWS 2048
 static void bias_grad(gpt2_t* m, float* db, const float* dy, int N, int OC) {
+  if (N <= BIAS_DIRECT_ROWS) {
+    launch_k(col_finish_kernel, ceil_div(OC, 32), COLF_WARPS * 32, 0, m->stream, db, db, db, OC, dy, N, OC,
+             m->grad_accumulate);
+    m->launches++;
+    return;
+  }
   const int rows = BIAS_MIN_ROWS, chunks = ceil_div(N, rows);
   launch_k(col_partial_kernel, dim3(ceil_div(OC, 256), chunks), 256, 0, m->stream, dy, N, OC, OC, rows, m->scratch);
   launch_k(col_finish_kernel, ceil_div(OC, 32), COLF_WARPS * 32, 0, m->stream, db, db, db, OC, m->scratch, chunks,
@@ -1151,6 +1162,41 @@ EXPORT int gpt2_forward(gpt2_t* m, const int32_t* inputs, const int32_t* targets
   if (rc) return rc;
   if (loss_out) return gpt2_sync(m, loss_out);
   return GPT2_OK;
+}
+
+// Generation (the pages' sample_mult loop): for t = n_prompt .. n_total-1, a
+// forward of batch row 0 over all n_total positions, then one draw from the
+// softmax of logits row t-1 with coin t - n_prompt, written to position t of
+// the device token buffer, where the next forward reads it.  Positions not
+// yet sampled hold the first prompt token; causal attention keeps them out of
+// the logits that are read.  The coins are staged in the per-row loss buffer,
+// which a forward without targets does not use.
+EXPORT int gpt2_sample(gpt2_t* m, int32_t* tokens, int n_prompt, int n_total, const float* coins) {
+  if (!m || !tokens || !coins) return GPT2_ERR_ARG;
+  if (m->poisoned) return m->poisoned;
+  if (n_prompt < 1 || n_total <= n_prompt) return GPT2_ERR_ARG;
+  int rc = check_shape(m, 1, n_total);
+  if (rc) return rc;
+  const int V = m->cfg.vocab_size, Vp = m->cfg.padded_vocab_size, ncoins = n_total - n_prompt;
+  for (int i = 0; i < n_prompt; i++)
+    if (tokens[i] < 0 || tokens[i] >= V) return GPT2_ERR_TOKEN_RANGE;
+  for (int i = 0; i < ncoins; i++)
+    if (!(coins[i] >= 0.f && coins[i] < 1.f)) return GPT2_ERR_ARG;
+  m->launches = 0;
+  std::vector<int32_t> init(tokens, tokens + n_total);
+  for (int i = n_prompt; i < n_total; i++) init[i] = tokens[0];
+  CCHECK(m, cudaMemcpyAsync(m->tokens, init.data(), (size_t)n_total * sizeof(int32_t), cudaMemcpyHostToDevice,
+                            m->stream));
+  CCHECK(m, cudaMemcpyAsync(m->losses, coins, (size_t)ncoins * sizeof(float), cudaMemcpyHostToDevice, m->stream));
+  for (int t = n_prompt; t < n_total; t++) {
+    rc = enqueue_forward(m, m->tokens, nullptr, 1, n_total, 0);
+    if (rc) return rc;
+    launch_k(sample_kernel, 1, SAMPLE_THREADS, 0, m->stream, m->tokens, t, m->logits + (size_t)(t - 1) * Vp, V,
+             (const float*)m->losses, t - n_prompt);
+    m->launches++;
+  }
+  CCHECK(m, cudaMemcpyAsync(tokens, m->tokens, (size_t)n_total * sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
+  return read_device_status(m);
 }
 
 EXPORT int gpt2_forward_device(gpt2_t* m, const int32_t* d_inputs, const int32_t* d_targets, int B, int T) {

@@ -495,9 +495,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int c4 = t & 31;  // float4 column group of the 128-wide tile
       const int j = n0 + 4 * c4;
       const uint32_t stage = smem_u32(smem + OFF_STAGE);
+      // the bias of this thread's four columns, once; per row, the epilogue's
+      // global input is requested before the peers' partials, so its latency
+      // overlaps theirs instead of following them
+      const bool vec = p.epi.vec4 && j + 4 <= p.N;
+      const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 bias4 = (vec && epi_has_bias(p.epi.epi)) ? ld4(p.epi.bias + j) : zero;
       for (int r = r0 + (t >> 5); r < r1; r += SPLIT_WARPS) {
         const int ii = m0 + r;
         if (ii >= p.M || j >= p.N) continue;
+        const float4 in4 = (vec && epi_has_input(p.epi.epi)) ? epi_load_input(p.epi, ii, j) : zero;
         const uint32_t off = stage + (uint32_t)(r * STAGE_PITCH + 4 * c4) * 4u;
         // every peer's partial is loaded before any is summed (the loads
         // overlap instead of each waiting for the previous one's add)
@@ -511,7 +518,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (z < S) {
             acc.x += part[z].x; acc.y += part[z].y; acc.z += part[z].z; acc.w += part[z].w;
           }
-        if (j + 4 <= p.N) {
+        if (vec) {
+          epi_apply4(p.epi, ii, j, acc, bias4, in4);
+        } else if (j + 4 <= p.N) {
           epi_store4(p.epi, ii, j, acc);
         } else {
           const float a4[4] = {acc.x, acc.y, acc.z, acc.w};

@@ -108,6 +108,27 @@ int gpt2_forward(gpt2_t* m, const int32_t* inputs, const int32_t* targets, int B
  * gpt2_sync() returns GPT2_ERR_TOKEN_RANGE. */
 int gpt2_forward_device(gpt2_t* m, const int32_t* d_inputs, const int32_t* d_targets, int B, int T);
 
+/* Text generation: the page «llm.c：Andrej Karpathy带你从零复现LLM», section
+ * «核心代码解读：train_gpt2.c», item 5 (sample_mult draws an index from a
+ * probability distribution; the main loop generates a sequence with it).
+ * For t = n_prompt .. n_total-1: one forward without targets over batch row
+ * 0 and all n_total positions (positions not yet generated hold tokens[0];
+ * causal attention keeps them out of the row that is read), then
+ * tokens[t] = the first index i < vocab_size whose cumulative softmax
+ * probability of logits row t-1 exceeds coins[t - n_prompt] (inverse-CDF
+ * sampling; the last index with nonzero weight if rounding leaves the coin
+ * above every prefix).
+ *  tokens  : host int32[n_total]; in: the prompt in [0, n_prompt), ids in
+ *            [0, vocab_size); out: prompt followed by the generated ids.
+ *  coins   : host float[n_total - n_prompt], each in [0, 1), e.g. uniform
+ *            draws of the caller's generator (the library draws none).
+ *  1 <= n_prompt < n_total <= min(maxT, max_seq_len); the handle needs maxB >= 1.
+ * Synchronises the stream.  Returns GPT2_ERR_ARG for a bad count or a coin
+ * outside [0, 1), GPT2_ERR_TOKEN_RANGE for a bad prompt id, GPT2_ERR_SHAPE when
+ * n_total does not fit the handle.  Overwrites the logits, so a following
+ * gpt2_backward() fails with GPT2_ERR_STATE. */
+int gpt2_sample(gpt2_t* m, int32_t* tokens, int n_prompt, int n_total, const float* coins);
+
 /* Synchronises the handle's stream; reports device-side errors recorded since
  * the previous sync and, when loss_out != NULL, stores the last mean loss. */
 int gpt2_sync(gpt2_t* m, float* loss_out);

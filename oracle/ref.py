@@ -7,7 +7,8 @@ and by bench.py's CPU-baseline leg.  The CUDA package never imports it.
 «llm.c：Andrej Karpathy带你从零复现LLM», section «核心代码解读：train_gpt2.c»,
 item 3 (build, forward, zero_grad, backward, update), with numpy views onto
 the oracle's flat parameter, gradient, optimizer-state and activation
-buffers.  ``ops(dtype)`` exposes the per-layer functions of item 1.
+buffers.  ``ops(dtype)`` exposes the per-layer functions of item 1;
+``sample_mult`` and ``generate`` follow item 5 (sampling generation).
 """
 from __future__ import annotations
 
@@ -351,3 +352,59 @@ class Ops:
 
 def ops(dtype=np.float64) -> Ops:
     return Ops(dtype)
+
+
+# ---------------------------------------------------------------------------
+# Generation: the page «llm.c：Andrej Karpathy带你从零复现LLM», section
+# «核心代码解读：train_gpt2.c», item 5 -- sample_mult draws an index from a
+# probability distribution and the main loop generates a sequence with it.
+# The pages do not print the function; the reading here is inverse-CDF
+# sampling with the uniform draw passed in.
+# ---------------------------------------------------------------------------
+def softmax64(logits) -> np.ndarray:
+    """softmax of a 1-D logits vector in float64 (max-subtracted)."""
+    x = np.asarray(logits, dtype=np.float64).ravel()
+    e = np.exp(x - x.max())
+    return e / e.sum()
+
+
+def sample_mult(probs, coin: float) -> int:
+    """The first index whose cumulative probability exceeds coin (a uniform
+    draw in [0, 1)); when rounding leaves coin at or above every prefix, the
+    last index with a nonzero probability.  Prefix sums in float64, in index
+    order."""
+    p = np.asarray(probs, dtype=np.float64).ravel()
+    cdf = np.cumsum(p)
+    i = int(np.searchsorted(cdf, coin, side="right"))  # first i with cdf[i] > coin
+    if i >= p.size:
+        nz = np.nonzero(p > 0)[0]
+        i = int(nz[-1]) if nz.size else p.size - 1
+    return i
+
+
+def sample_is_valid(probs, coin: float, index: int, tol: float) -> bool:
+    """Whether index is the inverse-CDF draw for coin up to a tolerance tol on
+    the cumulative probabilities: cdf[index-1] - tol <= coin < cdf[index] + tol
+    and probs[index] > 0 (several indices qualify when coin lies within tol of
+    a boundary)."""
+    p = np.asarray(probs, dtype=np.float64).ravel()
+    if not 0 <= index < p.size or p[index] <= 0:
+        return False
+    cdf = np.cumsum(p)
+    lo = cdf[index - 1] if index > 0 else 0.0
+    return lo - tol <= coin < cdf[index] + tol
+
+
+def generate(model: RefModel, prompt, n_total: int, coins, vocab_size: int) -> np.ndarray:
+    """The generation loop on the oracle: for t = len(prompt) .. n_total-1, a
+    forward without targets over the n_total positions (positions not yet
+    generated hold prompt[0]), then tokens[t] = sample_mult(softmax of logits
+    row t-1 over the real vocabulary, coins[t - len(prompt)])."""
+    prompt = np.asarray(prompt, dtype=np.int32).ravel()
+    tokens = np.full(n_total, prompt[0], np.int32)
+    tokens[:prompt.size] = prompt
+    for t in range(prompt.size, n_total):
+        model.forward(tokens[None, :], None)
+        logits = model.act("logits").reshape(n_total, -1)[t - 1, :vocab_size]
+        tokens[t] = sample_mult(softmax64(logits), float(coins[t - prompt.size]))
+    return tokens

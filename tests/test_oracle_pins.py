@@ -352,3 +352,46 @@ def test_P12_oracle_bit_identical_across_thread_counts():
                            check=True)
         outs.append(r.stdout.strip())
     assert outs[0] == outs[1] == outs[2]
+
+
+# ---------------------------------------------------------------------------
+# Sampling (the page's item 5, sample_mult): inverse-CDF draws with the
+# uniform coin passed in.  Pins: the definition at exact binary boundaries,
+# zero-probability entries, the rounding tail, and the closed-form counts of
+# stratified coins.
+# ---------------------------------------------------------------------------
+def test_sample_mult_boundaries():
+    p = [0.125, 0.25, 0.625]  # cumulative 0.125, 0.375, 1.0, exact in binary
+    cases = [(0.0, 0), (0.124, 0), (0.125, 1), (0.374, 1), (0.375, 2), (0.999, 2)]
+    for coin, want in cases:
+        assert ref.sample_mult(p, coin) == want, (coin, want)
+
+
+def test_sample_mult_skips_zero_probabilities():
+    p = [0.0, 0.5, 0.0, 0.5, 0.0]
+    draws = {ref.sample_mult(p, c) for c in np.linspace(0.0, 0.999, 101)}
+    assert draws == {1, 3}
+    assert ref.sample_mult(p, 0.0) == 1
+
+
+def test_sample_mult_rounding_tail_takes_last_nonzero():
+    # probabilities summing below the coin (as rounding can leave them)
+    assert ref.sample_mult([0.25, 0.25, 0.0], 0.75) == 1
+
+
+def test_sample_mult_stratified_counts():
+    p = [0.2, 0.5, 0.3]
+    n = 1000
+    counts = np.bincount([ref.sample_mult(p, (i + 0.5) / n) for i in range(n)], minlength=3)
+    assert counts.tolist() == [200, 500, 300]
+
+
+def test_softmax64_closed_form():
+    np.testing.assert_allclose(ref.softmax64([0.0, np.log(3.0)]), [0.25, 0.75], rtol=1e-15)
+
+
+def test_sample_is_valid():
+    p = [0.125, 0.25, 0.625]
+    assert ref.sample_is_valid(p, 0.2, 1, 0.0)
+    assert not ref.sample_is_valid(p, 0.2, 2, 0.0)
+    assert ref.sample_is_valid(p, 0.3749999, 2, 1e-6)  # within tol of the 0.375 boundary
