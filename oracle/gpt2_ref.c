@@ -30,6 +30,11 @@
  *          with every weight and activation pointing into it; the list of
  *          components (encoder, matmul, self-attention, GELU, residual,
  *          softmax, cross-entropy).
+ *   [LL]   page «千行C代码训完GPT-2» (新智元): the plans for Llama2/Gemma-style
+ *          models -- RMSNorm in place of layernorm, new layers such as RoPE.
+ *          With cfg.llama set the model follows them: RMSNorm (no bias), RoPE
+ *          on q and k (base 10000, interleaved pairs), no learned position
+ *          table and no linear biases; the MLP stays GELU.
  * Readings where the pages are silent (GELU tanh form, layernorm eps 1e-5,
  * 1/sqrt(hs) attention scale, tied LM head without bias, (out,in) weight
  * orientation, padded vocab columns excluded from the softmax, AdamW with
@@ -62,9 +67,13 @@ EXPORT void encoder_forward(real* x, const int* ids, const real* wte, const real
   for (int b = 0; b < B; b++)
     for (int t = 0; t < T; t++) {
       const real* e = wte + (size_t)ids[b * T + t] * C;
-      const real* p = wpe + (size_t)t * C;
       real* o = x + ((size_t)b * T + t) * C;
-      for (int c = 0; c < C; c++) o[c] = e[c] + p[c];
+      if (wpe) {
+        const real* p = wpe + (size_t)t * C;
+        for (int c = 0; c < C; c++) o[c] = e[c] + p[c];
+      } else {
+        for (int c = 0; c < C; c++) o[c] = e[c];  /* no learned position table */
+      }
     }
 }
 
@@ -75,7 +84,7 @@ EXPORT void encoder_backward(real* dwte, real* dwpe, const real* dx, const int* 
                              int B, int T, int C) {
   int N = B * T;
   double* acc = (double*)malloc(sizeof(double) * (size_t)C);
-  for (int t = 0; t < T; t++) {
+  for (int t = 0; t < T && dwpe; t++) {
     for (int c = 0; c < C; c++) acc[c] = 0.0;
     for (int b = 0; b < B; b++)
       for (int c = 0; c < C; c++) acc[c] += dx[((size_t)b * T + t) * C + c];
@@ -150,6 +159,66 @@ EXPORT void layernorm_backward(real* dx, real* dw, real* db, const real* dy, con
     dw[c] += (real)sw;
     db[c] += (real)sb;
   }
+}
+
+/* [LL] RMSNorm: per row, rstd = 1/sqrt(mean_c(x^2) + 1e-5), y = x * rstd * w. */
+EXPORT void rmsnorm_forward(real* y, real* rstd, const real* x, const real* w, int N, int C) {
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < N; r++) {
+    const real* xr = x + (size_t)r * C;
+    double ms = 0.0;
+    for (int c = 0; c < C; c++) ms += (double)xr[c] * xr[c];
+    ms /= C;
+    double rs = 1.0 / sqrt(ms + LN_EPS);
+    for (int c = 0; c < C; c++) y[(size_t)r * C + c] = (real)(xr[c] * rs * w[c]);
+    rstd[r] = (real)rs;
+  }
+}
+
+/* [LL] RMSNorm backward.  With n = x * rstd and g = dy * w, y = n*w gives
+ *   dx = rstd * (g - n * mean_c(g * n)),   dw = sum_rows dy * n
+ * (the layernorm formula without the mean(g) term: nothing is subtracted). */
+EXPORT void rmsnorm_backward(real* dx, real* dw, const real* dy, const real* x, const real* w, const real* rstd,
+                             int N, int C) {
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < N; r++) {
+    const real* xr = x + (size_t)r * C;
+    const real* dyr = dy + (size_t)r * C;
+    double rs = rstd[r], mgn = 0.0;
+    for (int c = 0; c < C; c++) mgn += (double)dyr[c] * w[c] * (xr[c] * rs);
+    mgn /= C;
+    for (int c = 0; c < C; c++) {
+      double n = xr[c] * rs, g = (double)dyr[c] * w[c];
+      dx[(size_t)r * C + c] += (real)(rs * (g - n * mgn));
+    }
+  }
+  for (int c = 0; c < C; c++) {
+    double a = 0.0;
+    for (int r = 0; r < N; r++) a += (double)dy[(size_t)r * C + c] * (x[(size_t)r * C + c] * (double)rstd[r]);
+    dw[c] += (real)a;
+  }
+}
+
+/* [LL] rotary position embedding of q and k, in place in qkv (B,T,3C):
+ * head h, pair i < hs/2 of token t is rotated by theta = t * 10000^(-2i/hs),
+ *   (a, b) -> (a cos theta - b sin theta, a sin theta + b cos theta),
+ * on the channels h*hs + 2i, h*hs + 2i + 1 of the q block and of the k block.
+ * inverse != 0 rotates by -theta (the transpose: the backward of the map). */
+EXPORT void rope_apply(real* qkv, int B, int T, int C, int NH, int inverse) {
+  int hs = C / NH;
+  for (int b = 0; b < B; b++)
+    for (int t = 0; t < T; t++)
+      for (int h = 0; h < NH; h++)
+        for (int i = 0; i < hs / 2; i++) {
+          double theta = t * pow(10000.0, -2.0 * i / hs);
+          double cs = cos(theta), sn = inverse ? -sin(theta) : sin(theta);
+          for (int part = 0; part < 2; part++) { /* q, then k */
+            real* v = qkv + ((size_t)b * T + t) * 3 * C + part * C + h * hs + 2 * i;
+            double a = v[0], bb = v[1];
+            v[0] = (real)(a * cs - bb * sn);
+            v[1] = (real)(a * sn + bb * cs);
+          }
+        }
 }
 
 /* [HX-1 matmul_forward]: out[r,o] = sum_i x[r,i] * W[o,i] + bias[o]
@@ -407,6 +476,7 @@ EXPORT void adamw_update(real* p, const real* g, real* m, real* v, long long n, 
 
 typedef struct {
   int max_seq_len, vocab_size, padded_vocab_size, num_layers, num_heads, channels;
+  int llama; /* [LL]: RMSNorm, RoPE, no position table, no biases */
 } ref_config;
 
 enum {
@@ -440,6 +510,8 @@ static void param_sizes(const ref_config* c, long long vocab_rows, long long s[N
   s[P_FCPROJB] = L * C;
   s[P_LNFW] = C;
   s[P_LNFB] = C;
+  if (c->llama) /* no position table, no biases (RMSNorm has no shift either) */
+    s[P_WPE] = s[P_LN1B] = s[P_QKVB] = s[P_ATTPROJB] = s[P_LN2B] = s[P_FCB] = s[P_FCPROJB] = s[P_LNFB] = 0;
 }
 
 /* Element counts of the 23 activation tensors for a (B,T) batch; vocab_cols
@@ -586,7 +658,9 @@ EXPORT double ref_forward(ref_model* M, const int* inputs, const int* targets, i
   real** P = M->P;
   real** A = M->A;
   size_t NC = (size_t)N * C, TT = (size_t)B * NH * T * T;
-  encoder_forward(A[A_ENCODED], inputs, P[P_WTE], P[P_WPE], B, T, C);
+  const int ll = c->llama;
+#define BIAS(t, off) (ll ? (const real*)NULL : P[t] + (off))
+  encoder_forward(A[A_ENCODED], inputs, P[P_WTE], ll ? NULL : P[P_WPE], B, T, C);
   for (int l = 0; l < L; l++) {
     const real* x = l == 0 ? A[A_ENCODED] : A[A_RESIDUAL3] + (size_t)(l - 1) * NC;
     real* ln1 = A[A_LN1] + l * NC;
@@ -601,21 +675,32 @@ EXPORT double ref_forward(ref_model* M, const int* inputs, const int* targets, i
     real* fchg = A[A_FCH_GELU] + l * 4 * NC;
     real* fcproj = A[A_FCPROJ] + l * NC;
     real* res3 = A[A_RESIDUAL3] + l * NC;
-    layernorm_forward(ln1, A[A_LN1_MEAN] + (size_t)l * N, A[A_LN1_RSTD] + (size_t)l * N, x,
-                      P[P_LN1W] + (size_t)l * C, P[P_LN1B] + (size_t)l * C, N, C);
-    matmul_forward(qkv, ln1, P[P_QKVW] + (size_t)l * 3 * C * C, P[P_QKVB] + (size_t)l * 3 * C, N, C, 3 * C);
+    if (ll)
+      rmsnorm_forward(ln1, A[A_LN1_RSTD] + (size_t)l * N, x, P[P_LN1W] + (size_t)l * C, N, C);
+    else
+      layernorm_forward(ln1, A[A_LN1_MEAN] + (size_t)l * N, A[A_LN1_RSTD] + (size_t)l * N, x,
+                        P[P_LN1W] + (size_t)l * C, P[P_LN1B] + (size_t)l * C, N, C);
+    matmul_forward(qkv, ln1, P[P_QKVW] + (size_t)l * 3 * C * C, BIAS(P_QKVB, (size_t)l * 3 * C), N, C, 3 * C);
+    if (ll) rope_apply(qkv, B, T, C, NH, 0);
     attention_forward(atty, preatt, att, qkv, B, T, C, NH);
-    matmul_forward(attproj, atty, P[P_ATTPROJW] + (size_t)l * C * C, P[P_ATTPROJB] + (size_t)l * C, N, C, C);
+    matmul_forward(attproj, atty, P[P_ATTPROJW] + (size_t)l * C * C, BIAS(P_ATTPROJB, (size_t)l * C), N, C, C);
     residual_forward(res2, x, attproj, (long long)NC);
-    layernorm_forward(ln2, A[A_LN2_MEAN] + (size_t)l * N, A[A_LN2_RSTD] + (size_t)l * N, res2,
-                      P[P_LN2W] + (size_t)l * C, P[P_LN2B] + (size_t)l * C, N, C);
-    matmul_forward(fch, ln2, P[P_FCW] + (size_t)l * 4 * C * C, P[P_FCB] + (size_t)l * 4 * C, N, C, 4 * C);
+    if (ll)
+      rmsnorm_forward(ln2, A[A_LN2_RSTD] + (size_t)l * N, res2, P[P_LN2W] + (size_t)l * C, N, C);
+    else
+      layernorm_forward(ln2, A[A_LN2_MEAN] + (size_t)l * N, A[A_LN2_RSTD] + (size_t)l * N, res2,
+                        P[P_LN2W] + (size_t)l * C, P[P_LN2B] + (size_t)l * C, N, C);
+    matmul_forward(fch, ln2, P[P_FCW] + (size_t)l * 4 * C * C, BIAS(P_FCB, (size_t)l * 4 * C), N, C, 4 * C);
     gelu_forward(fchg, fch, (long long)(4 * NC));
-    matmul_forward(fcproj, fchg, P[P_FCPROJW] + (size_t)l * 4 * C * C, P[P_FCPROJB] + (size_t)l * C, N, 4 * C, C);
+    matmul_forward(fcproj, fchg, P[P_FCPROJW] + (size_t)l * 4 * C * C, BIAS(P_FCPROJB, (size_t)l * C), N, 4 * C, C);
     residual_forward(res3, res2, fcproj, (long long)NC);
   }
-  layernorm_forward(A[A_LNF], A[A_LNF_MEAN], A[A_LNF_RSTD], A[A_RESIDUAL3] + (size_t)(L - 1) * NC,
-                    P[P_LNFW], P[P_LNFB], N, C);
+  if (ll)
+    rmsnorm_forward(A[A_LNF], A[A_LNF_RSTD], A[A_RESIDUAL3] + (size_t)(L - 1) * NC, P[P_LNFW], N, C);
+  else
+    layernorm_forward(A[A_LNF], A[A_LNF_MEAN], A[A_LNF_RSTD], A[A_RESIDUAL3] + (size_t)(L - 1) * NC,
+                      P[P_LNFW], P[P_LNFB], N, C);
+#undef BIAS
   /* LM head tied to wte, no bias; all Vp columns are computed. */
   matmul_forward(A[A_LOGITS], A[A_LNF], P[P_WTE], NULL, N, C, Vp);
   softmax_forward(A[A_PROBS], A[A_LOGITS], N, V, Vp);
@@ -660,8 +745,13 @@ EXPORT int ref_backward(ref_model* M) {
   matmul_backward(dA[A_LNF], G[P_WTE], NULL, dA[A_LOGITS], A[A_LNF], P[P_WTE], N, C, Vp);
   real* resL = A[A_RESIDUAL3] + (size_t)(L - 1) * NC;
   real* dresL = dA[A_RESIDUAL3] + (size_t)(L - 1) * NC;
-  layernorm_backward(dresL, G[P_LNFW], G[P_LNFB], dA[A_LNF], resL, P[P_LNFW], A[A_LNF_MEAN],
-                     A[A_LNF_RSTD], N, C);
+  const int ll = c->llama;
+#define DBIAS(t, off) (ll ? (real*)NULL : G[t] + (off))
+  if (ll)
+    rmsnorm_backward(dresL, G[P_LNFW], dA[A_LNF], resL, P[P_LNFW], A[A_LNF_RSTD], N, C);
+  else
+    layernorm_backward(dresL, G[P_LNFW], G[P_LNFB], dA[A_LNF], resL, P[P_LNFW], A[A_LNF_MEAN],
+                       A[A_LNF_RSTD], N, C);
   for (int l = L - 1; l >= 0; l--) {
     const real* x = l == 0 ? A[A_ENCODED] : A[A_RESIDUAL3] + (size_t)(l - 1) * NC;
     real* dx = l == 0 ? dA[A_ENCODED] : dA[A_RESIDUAL3] + (size_t)(l - 1) * NC;
@@ -671,28 +761,39 @@ EXPORT int ref_backward(ref_model* M) {
     /* res3 = res2 + fcproj */
     residual_backward(dres2, dA[A_FCPROJ] + l * NC, dres3, (long long)NC);
     matmul_backward(dA[A_FCH_GELU] + l * 4 * NC, G[P_FCPROJW] + (size_t)l * 4 * C * C,
-                    G[P_FCPROJB] + (size_t)l * C, dA[A_FCPROJ] + l * NC, A[A_FCH_GELU] + l * 4 * NC,
+                    DBIAS(P_FCPROJB, (size_t)l * C), dA[A_FCPROJ] + l * NC, A[A_FCH_GELU] + l * 4 * NC,
                     P[P_FCPROJW] + (size_t)l * 4 * C * C, N, 4 * C, C);
     gelu_backward(dA[A_FCH] + l * 4 * NC, A[A_FCH] + l * 4 * NC, dA[A_FCH_GELU] + l * 4 * NC,
                   (long long)(4 * NC));
-    matmul_backward(dA[A_LN2] + l * NC, G[P_FCW] + (size_t)l * 4 * C * C, G[P_FCB] + (size_t)l * 4 * C,
+    matmul_backward(dA[A_LN2] + l * NC, G[P_FCW] + (size_t)l * 4 * C * C, DBIAS(P_FCB, (size_t)l * 4 * C),
                     dA[A_FCH] + l * 4 * NC, A[A_LN2] + l * NC, P[P_FCW] + (size_t)l * 4 * C * C, N, C, 4 * C);
-    layernorm_backward(dres2, G[P_LN2W] + (size_t)l * C, G[P_LN2B] + (size_t)l * C, dA[A_LN2] + l * NC,
-                       A[A_RESIDUAL2] + l * NC, P[P_LN2W] + (size_t)l * C, A[A_LN2_MEAN] + (size_t)l * N,
-                       A[A_LN2_RSTD] + (size_t)l * N, N, C);
+    if (ll)
+      rmsnorm_backward(dres2, G[P_LN2W] + (size_t)l * C, dA[A_LN2] + l * NC, A[A_RESIDUAL2] + l * NC,
+                       P[P_LN2W] + (size_t)l * C, A[A_LN2_RSTD] + (size_t)l * N, N, C);
+    else
+      layernorm_backward(dres2, G[P_LN2W] + (size_t)l * C, G[P_LN2B] + (size_t)l * C, dA[A_LN2] + l * NC,
+                         A[A_RESIDUAL2] + l * NC, P[P_LN2W] + (size_t)l * C, A[A_LN2_MEAN] + (size_t)l * N,
+                         A[A_LN2_RSTD] + (size_t)l * N, N, C);
     /* res2 = x + attproj */
     residual_backward(dx, dA[A_ATTPROJ] + l * NC, dres2, (long long)NC);
-    matmul_backward(dA[A_ATTY] + l * NC, G[P_ATTPROJW] + (size_t)l * C * C, G[P_ATTPROJB] + (size_t)l * C,
+    matmul_backward(dA[A_ATTY] + l * NC, G[P_ATTPROJW] + (size_t)l * C * C, DBIAS(P_ATTPROJB, (size_t)l * C),
                     dA[A_ATTPROJ] + l * NC, A[A_ATTY] + l * NC, P[P_ATTPROJW] + (size_t)l * C * C, N, C, C);
     attention_backward(dA[A_QKV] + l * 3 * NC, dA[A_ATTY] + l * NC, A[A_QKV] + l * 3 * NC,
                        A[A_ATT] + l * TT, B, T, C, NH);
-    matmul_backward(dA[A_LN1] + l * NC, G[P_QKVW] + (size_t)l * 3 * C * C, G[P_QKVB] + (size_t)l * 3 * C,
+    /* q and k were rotated after the matmul: carry their gradients back through the rotation */
+    if (ll) rope_apply(dA[A_QKV] + l * 3 * NC, B, T, C, NH, 1);
+    matmul_backward(dA[A_LN1] + l * NC, G[P_QKVW] + (size_t)l * 3 * C * C, DBIAS(P_QKVB, (size_t)l * 3 * C),
                     dA[A_QKV] + l * 3 * NC, A[A_LN1] + l * NC, P[P_QKVW] + (size_t)l * 3 * C * C, N, C, 3 * C);
-    layernorm_backward(dx, G[P_LN1W] + (size_t)l * C, G[P_LN1B] + (size_t)l * C, dA[A_LN1] + l * NC, x,
-                       P[P_LN1W] + (size_t)l * C, A[A_LN1_MEAN] + (size_t)l * N, A[A_LN1_RSTD] + (size_t)l * N,
-                       N, C);
+    if (ll)
+      rmsnorm_backward(dx, G[P_LN1W] + (size_t)l * C, dA[A_LN1] + l * NC, x, P[P_LN1W] + (size_t)l * C,
+                       A[A_LN1_RSTD] + (size_t)l * N, N, C);
+    else
+      layernorm_backward(dx, G[P_LN1W] + (size_t)l * C, G[P_LN1B] + (size_t)l * C, dA[A_LN1] + l * NC, x,
+                         P[P_LN1W] + (size_t)l * C, A[A_LN1_MEAN] + (size_t)l * N, A[A_LN1_RSTD] + (size_t)l * N,
+                         N, C);
   }
-  encoder_backward(G[P_WTE], G[P_WPE], dA[A_ENCODED], M->inputs, B, T, C);
+#undef DBIAS
+  encoder_backward(G[P_WTE], ll ? NULL : G[P_WPE], dA[A_ENCODED], M->inputs, B, T, C);
   return 0;
 }
 

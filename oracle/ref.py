@@ -32,7 +32,7 @@ ACT_NAMES = [
 
 class RefConfig(ct.Structure):
     _fields_ = [(n, ct.c_int) for n in
-                ("max_seq_len", "vocab_size", "padded_vocab_size", "num_layers", "num_heads", "channels")]
+                ("max_seq_len", "vocab_size", "padded_vocab_size", "num_layers", "num_heads", "channels", "llama")]
 
 
 _LIBS: dict = {}
@@ -69,13 +69,16 @@ def _lib(dtype) -> ct.CDLL:
     return _LIBS[key]
 
 
-def make_config(max_seq_len, vocab_size, padded_vocab_size, num_layers, num_heads, channels) -> RefConfig:
-    return RefConfig(max_seq_len, vocab_size, padded_vocab_size, num_layers, num_heads, channels)
+def make_config(max_seq_len, vocab_size, padded_vocab_size, num_layers, num_heads, channels,
+                llama: int = 0) -> RefConfig:
+    return RefConfig(max_seq_len, vocab_size, padded_vocab_size, num_layers, num_heads, channels, int(llama))
 
 
 def config_from(w) -> RefConfig:
-    """Build a RefConfig from any object with the GPT-2 shape fields."""
-    return make_config(w.max_seq_len, w.vocab_size, w.padded_vocab_size, w.num_layers, w.num_heads, w.channels)
+    """Build a RefConfig from any object with the GPT-2 shape fields (and an
+    optional ``llama`` flag: RMSNorm, RoPE, no position table, no biases)."""
+    return make_config(w.max_seq_len, w.vocab_size, w.padded_vocab_size, w.num_layers, w.num_heads, w.channels,
+                       getattr(w, "llama", 0))
 
 
 def num_parameters(cfg: RefConfig, padded: bool = True) -> int:
@@ -249,6 +252,32 @@ class Ops:
         self.lib.layernorm_backward(_ptr(dx), _ptr(dw), _ptr(db), _ptr(dy), _ptr(x), _ptr(w),
                                     _ptr(mean), _ptr(rstd), N, C)
         return dx, dw, db
+
+    def rmsnorm_forward(self, x, w):
+        """y = x * rstd * w, rstd = 1/sqrt(mean(x^2) + 1e-5) per row."""
+        x, w = self._a(x), self._a(w)
+        C = x.shape[-1]
+        N = x.size // C
+        y = np.zeros_like(x)
+        rstd = np.zeros(N, self.dtype)
+        self.lib.rmsnorm_forward(_ptr(y), _ptr(rstd), _ptr(x), _ptr(w), N, C)
+        return y, rstd
+
+    def rmsnorm_backward(self, dy, x, w, rstd):
+        dy, x, w, rstd = map(self._a, (dy, x, w, rstd))
+        C = x.shape[-1]
+        N = x.size // C
+        dx = np.zeros_like(x)
+        dw = np.zeros(C, self.dtype)
+        self.lib.rmsnorm_backward(_ptr(dx), _ptr(dw), _ptr(dy), _ptr(x), _ptr(w), _ptr(rstd), N, C)
+        return dx, dw
+
+    def rope_apply(self, qkv, NH, inverse=False):
+        """Rotary position embedding of the q and k blocks of qkv (B,T,3C) (a copy)."""
+        qkv = self._a(qkv).copy()
+        B, T, C3 = qkv.shape
+        self.lib.rope_apply(_ptr(qkv), B, T, C3 // 3, NH, int(bool(inverse)))
+        return qkv
 
     def matmul_forward(self, x, W, bias=None):
         x, W = self._a(x), self._a(W)

@@ -60,6 +60,7 @@ class Workload:
     beta2: float = 0.999
     eps: float = 1e-8
     weight_decay: float = 0.0
+    llama: int = 0  # 1: RMSNorm, RoPE, no position table, no biases
 
     @property
     def BT(self) -> int:
@@ -147,7 +148,7 @@ PARAM_NAMES = [
 def param_shapes(w: Workload, padded: bool = True) -> dict:
     L, C = w.num_layers, w.channels
     Vr = w.padded_vocab_size if padded else w.vocab_size
-    return {
+    shapes = {
         "wte": (Vr, C), "wpe": (w.max_seq_len, C),
         "ln1w": (L, C), "ln1b": (L, C),
         "qkvw": (L, 3 * C, C), "qkvb": (L, 3 * C),
@@ -157,6 +158,10 @@ def param_shapes(w: Workload, padded: bool = True) -> dict:
         "fcprojw": (L, C, 4 * C), "fcprojb": (L, C),
         "lnfw": (C,), "lnfb": (C,),
     }
+    if w.llama:  # the tensors keep their places with no elements
+        for name in ("wpe", "ln1b", "qkvb", "attprojb", "ln2b", "fcb", "fcprojb", "lnfb"):
+            shapes[name] = (0,)
+    return shapes
 
 
 def param_offsets(w: Workload) -> dict:

@@ -395,3 +395,132 @@ def test_sample_is_valid():
     assert ref.sample_is_valid(p, 0.2, 1, 0.0)
     assert not ref.sample_is_valid(p, 0.2, 2, 0.0)
     assert ref.sample_is_valid(p, 0.3749999, 2, 1e-6)  # within tol of the 0.375 boundary
+
+
+# ---------------------------------------------------------------------------
+# Llama-style variant ([LL]: RMSNorm in place of layernorm, RoPE on q and k,
+# no position table, no biases).  Pins: closed forms, the invariances that
+# define the two layers (scale invariance; rotation, identity at t = 0 and
+# dependence of q.k on the position difference only), the transpose used by
+# the backward, the parameter count, and whole-model finite differences.
+# ---------------------------------------------------------------------------
+LL_OPS = ref.ops(np.float64)
+
+
+def test_LL_rmsnorm_closed_form_and_scale_invariance():
+    x = np.array([[3.0, 4.0], [-1.0, 2.0]])
+    w = np.array([2.0, 0.5])
+    y, rstd = LL_OPS.rmsnorm_forward(x, w)
+    np.testing.assert_allclose(y[0], [6.0 / np.sqrt(12.5 + 1e-5), 2.0 / np.sqrt(12.5 + 1e-5)], rtol=1e-14)
+    np.testing.assert_allclose(rstd, 1.0 / np.sqrt((x * x).mean(1) + 1e-5), rtol=1e-14)
+    xr = np.random.default_rng(0).standard_normal((4, 32))
+    y1, _ = LL_OPS.rmsnorm_forward(xr, np.ones(32))
+    y5, _ = LL_OPS.rmsnorm_forward(5.0 * xr, np.ones(32))
+    np.testing.assert_allclose(y5, y1, rtol=1e-5)  # eps 1e-5 is the only scale-dependent term
+    np.testing.assert_allclose(np.sqrt((y1 * y1).mean(1)), 1.0, rtol=1e-4)
+
+
+def test_LL_rmsnorm_backward_finite_differences():
+    rng = np.random.default_rng(1)
+    x, w, dy = rng.standard_normal((3, 8)), rng.standard_normal(8), rng.standard_normal((3, 8))
+    _, rstd = LL_OPS.rmsnorm_forward(x, w)
+    dx, dw = LL_OPS.rmsnorm_backward(dy, x, w, rstd)
+    h = 1e-6
+    f = lambda xx, ww: float((LL_OPS.rmsnorm_forward(xx, ww)[0] * dy).sum())
+    for i in range(3):
+        for j in range(8):
+            xp, xm = x.copy(), x.copy()
+            xp[i, j] += h
+            xm[i, j] -= h
+            assert abs((f(xp, w) - f(xm, w)) / (2 * h) - dx[i, j]) <= 1e-7 * (1 + abs(dx[i, j]))
+    for j in range(8):
+        wp, wm = w.copy(), w.copy()
+        wp[j] += h
+        wm[j] -= h
+        assert abs((f(x, wp) - f(x, wm)) / (2 * h) - dw[j]) <= 1e-7 * (1 + abs(dw[j]))
+
+
+def test_LL_rope_closed_form_identity_and_v_untouched():
+    # one head of size 2: the single pair turns by t radians (frequency 10000^0)
+    qkv = np.zeros((1, 3, 6))
+    qkv[0, :, 0] = 1.0  # q = (1, 0) at every position
+    qkv[0, :, 4] = 7.0  # v
+    r = LL_OPS.rope_apply(qkv, 1)
+    for t in range(3):
+        np.testing.assert_allclose(r[0, t, 0:2], [np.cos(t), np.sin(t)], rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(r[0, :, 4:6], qkv[0, :, 4:6])
+    x = np.random.default_rng(2).standard_normal((2, 1, 3 * 16))  # position 0 only
+    np.testing.assert_array_equal(LL_OPS.rope_apply(x, 2), x)
+
+
+def test_LL_rope_scores_depend_on_position_difference_only():
+    rng = np.random.default_rng(3)
+    C, NH, T = 16, 2, 9
+    hs = C // NH
+    q, k = rng.standard_normal(hs), rng.standard_normal(hs)
+
+    def score(tq, tk):
+        x = np.zeros((1, T, 3 * C))
+        x[0, tq, 0:hs] = q  # head 0 query at position tq
+        x[0, tk, C:C + hs] = k  # head 0 key at position tk
+        r = LL_OPS.rope_apply(x, NH)
+        return float(r[0, tq, 0:hs] @ r[0, tk, C:C + hs])
+
+    for tq, tk, d in [(2, 0, 5), (4, 4, 3), (0, 3, 2), (6, 1, 2)]:
+        assert abs(score(tq, tk) - score(tq + d, tk + d)) <= 1e-12 * (1 + abs(score(tq, tk)))
+    assert abs(score(2, 0) - score(3, 0)) > 1e-6  # and it does depend on the difference
+
+
+def test_LL_rope_inverse_is_the_transpose():
+    rng = np.random.default_rng(4)
+    x, y = rng.standard_normal((2, 7, 3 * 24)), rng.standard_normal((2, 7, 3 * 24))
+    rx = LL_OPS.rope_apply(x, 3)
+    np.testing.assert_allclose(LL_OPS.rope_apply(rx, 3, inverse=True), x, atol=1e-14)
+    lhs = float((rx * y).sum())
+    rhs = float((x * LL_OPS.rope_apply(y, 3, inverse=True)).sum())
+    assert abs(lhs - rhs) <= 1e-12 * abs(lhs)
+
+
+LLAMA_FD = synth.Workload("llama_fd", 2, 32, 4, 64, 64, 16, 2, 12, "fp32", "uniform", 1, llama=1)
+
+
+def test_LL_parameter_count():
+    w = LLAMA_FD
+    L, C, Vp = w.num_layers, w.channels, w.padded_vocab_size
+    want = Vp * C + L * (C + 3 * C * C + C * C + C + 4 * C * C + 4 * C * C) + C
+    assert ref.num_parameters(ref.config_from(w)) == want == synth.num_params(w)
+    offs = ref.param_offsets(ref.config_from(w))
+    assert offs == synth.param_offsets(w)
+
+
+def test_LL_finite_difference_gradients():
+    w = LLAMA_FD
+    p0 = perturbed_params(w, seed=17)
+    inp, tgt = synth.batch(w)
+    m = ref.RefModel(ref.config_from(w), w.B, w.T, np.float64)
+    m.set_params(p0)
+    m.forward(inp, tgt)
+    m.zero_grad()
+    assert m.backward() == 0
+    g = m.grads.copy()
+
+    def loss_at(p):
+        m.set_params(p)
+        return m.forward(inp, tgt)
+
+    h = 1e-5
+    rng = np.random.default_rng(5)
+    for name, (o, n) in synth.param_offsets(w).items():
+        if n == 0:
+            continue
+        for i in o + rng.choice(n, size=min(n, 10), replace=False):
+            pp = p0.copy(); pp[i] += h
+            pm = p0.copy(); pm[i] -= h
+            fd = (loss_at(pp) - loss_at(pm)) / (2 * h)
+            assert abs(fd - g[i]) <= 1e-6 * abs(g[i]) + 2e-9, (name, i, fd, g[i])
+        d = np.zeros_like(p0)
+        d[o:o + n] = rng.standard_normal(n)
+        fd = (loss_at(p0 + h * d) - loss_at(p0 - h * d)) / (2 * h)
+        gd = float(g[o:o + n] @ d[o:o + n])
+        assert abs(fd - gd) <= 1e-6 * abs(gd) + 1e-8, (name, fd, gd)
+    m.close()
