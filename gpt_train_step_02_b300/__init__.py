@@ -48,7 +48,7 @@ EXPORTS = [
 
 class gpt2_config(ct.Structure):
     _fields_ = [(n, ct.c_int) for n in ("max_seq_len", "vocab_size", "padded_vocab_size", "num_layers",
-                                        "num_heads", "channels", "gemm_precision")]
+                                        "num_heads", "channels", "gemm_precision", "llama")]
 
 
 class GPT2Error(RuntimeError):
@@ -124,7 +124,7 @@ def make_config(w) -> gpt2_config:
     """gpt2_config from any object with the GPT-2 shape fields."""
     prec = getattr(w, "gemm_precision", GPT2_PREC_FP32)
     return gpt2_config(w.max_seq_len, w.vocab_size, w.padded_vocab_size, w.num_layers, w.num_heads, w.channels,
-                       prec)
+                       prec, int(getattr(w, "llama", 0)))
 
 
 def _hptr(a: np.ndarray) -> ct.c_void_p:

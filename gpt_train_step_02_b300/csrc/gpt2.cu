@@ -32,6 +32,7 @@
 #include "k_gemm_tc.cuh"
 #include "k_layernorm.cuh"
 #include "k_misc.cuh"
+#include "k_rope.cuh"
 #include "k_sample.cuh"
 #include "k_xent.cuh"
 
@@ -62,6 +63,9 @@ struct Plan {
   size_t dres, dln, datty, dqkv, dfch, attD, scratch, sorted, tokens, targets, err, hparams, splitk, tilectr;
   // bf16 operand copies (bf16 matmuls only)
   size_t ln1_bf, qkv_bf, atty_bf, ln2_bf, fchg_bf, lnf_bf, dlogits_bf, dres_bf, dfch_bf, dqkv_bf, datty_bf;
+  // Llama-style variant: (cos, sin) per position and pair, and a zero vector
+  // standing in for the biases the variant does not have
+  size_t rope, zero_bias;
   size_t scratch_floats;
 };
 
@@ -70,6 +74,8 @@ static long long param_count(const gpt2_config* c, long long sizes[NUM_PARAMS]) 
   long long s[NUM_PARAMS] = {(long long)c->padded_vocab_size * C, (long long)c->max_seq_len * C, L * C, L * C,
                              L * 3 * C * C, L * 3 * C, L * C * C, L * C, L * C, L * C, L * 4 * C * C, L * 4 * C,
                              L * C * 4 * C, L * C, C, C};
+  if (c->llama)  // no position table, no biases, no layernorm shifts: the tensors stay, empty
+    s[P_WPE] = s[P_LN1B] = s[P_QKVB] = s[P_ATTPROJB] = s[P_LN2B] = s[P_FCB] = s[P_FCPROJB] = s[P_LNFB] = 0;
   long long n = 0;
   for (int i = 0; i < NUM_PARAMS; i++) {
     if (sizes) sizes[i] = s[i];
@@ -88,6 +94,7 @@ static int config_ok(const gpt2_config* c) {
   if (c->vocab_size < 1 || c->vocab_size > c->padded_vocab_size || c->padded_vocab_size % 64) return 0;
   if (c->padded_vocab_size > 65536) return 0;
   if (c->gemm_precision != GPT2_PREC_FP32 && c->gemm_precision != GPT2_PREC_BF16) return 0;
+  if (c->llama != 0 && c->llama != 1) return 0;
   return 1;
 }
 
@@ -163,6 +170,9 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->dfch_bf = take(BT * 4 * C * H);
   p->dqkv_bf = take(BT * 3 * C * H);
   p->datty_bf = take(BT * C * H);
+  const size_t ll = c->llama ? 1 : 0;
+  p->rope = take(ll * (size_t)maxT * (C / NH / 2) * 2 * F);
+  p->zero_bias = take(ll * 4 * C * F);
   p->total = off;
   return off;
 }
@@ -192,6 +202,8 @@ struct gpt2_t {
   uint16_t *ln1_bf, *qkv_bf, *atty_bf, *ln2_bf, *fchg_bf, *lnf_bf, *dlogits_bf, *dres_bf, *dfch_bf, *dqkv_bf,
       *datty_bf;
   float* hparams;
+  float2* rope;       // [maxT][hs/2] (cos, sin) of t * 10000^(-2i/hs) (Llama-style variant)
+  float* zero_bias;   // 4C zeros: the bias operand of the variant's linear layers
   int B, T, have_targets, fwd_done;
   // 1: the backward adds into the gradients (gpt2_backward); 0: it stores
   // them (the fused training step, whose gradients would otherwise be zeroed
@@ -593,9 +605,15 @@ static void ln_forward(gpt2_t* m, float* y, uint16_t* ybf, float* mean, float* r
                        const float* b, int N) {
   int C = m->cfg.channels;
   timer_begin(m, TK_LAYERNORM, (8.0 * C + 8.0) * N);
-  auto k = ln_pick(C, layernorm_fwd_kernel<1>, layernorm_fwd_kernel<2>, layernorm_fwd_kernel<4>,
-                   layernorm_fwd_kernel<6>, layernorm_fwd_kernel<8>, layernorm_fwd_kernel<10>);
-  launch_k(k, ceil_div(N, 8), 256, 0, m->stream, y, ybf, mean, rstd, x, w, b, N, C);
+  if (m->cfg.llama) {  // RMSNorm: no mean, no shift
+    auto k = ln_pick(C, layernorm_fwd_kernel<1, true>, layernorm_fwd_kernel<2, true>, layernorm_fwd_kernel<4, true>,
+                     layernorm_fwd_kernel<6, true>, layernorm_fwd_kernel<8, true>, layernorm_fwd_kernel<10, true>);
+    launch_k(k, ceil_div(N, 8), 256, 0, m->stream, y, ybf, mean, rstd, x, w, (const float*)nullptr, N, C);
+  } else {
+    auto k = ln_pick(C, layernorm_fwd_kernel<1, false>, layernorm_fwd_kernel<2, false>, layernorm_fwd_kernel<4, false>,
+                     layernorm_fwd_kernel<6, false>, layernorm_fwd_kernel<8, false>, layernorm_fwd_kernel<10, false>);
+    launch_k(k, ceil_div(N, 8), 256, 0, m->stream, y, ybf, mean, rstd, x, w, b, N, C);
+  }
   timer_end(m, TK_LAYERNORM);
   m->launches++;
 }
@@ -607,12 +625,19 @@ static void ln_backward(gpt2_t* m, float* dx, uint16_t* dxbf, float* dw, float* 
                         const float* x, const float* w, const float* mean, const float* rstd, int N) {
   int C = m->cfg.channels;
   const int nb = ceil_div(N, LNB_WARPS);  // one row per warp
-  const int nout = dxsum ? 3 : 2;
+  const bool rms = m->cfg.llama != 0;        // RMSNorm: dw only (no shift, no linear biases)
+  const int nout = rms ? 1 : (dxsum ? 3 : 2);
   timer_begin(m, TK_LAYERNORM, (16.0 * C + 8.0) * N);
-  auto k = ln_pick(C, layernorm_bwd_kernel<1>, layernorm_bwd_kernel<2>, layernorm_bwd_kernel<4>,
-                   layernorm_bwd_kernel<6>, layernorm_bwd_kernel<8>, layernorm_bwd_kernel<10>);
-  launch_k(k, nb, LNB_WARPS * 32, (size_t)LNB_WARPS * nout * C * sizeof(float), m->stream, dx, dxbf, m->scratch, dy, x,
-           w, mean, rstd, N, C, dxsum ? 1 : 0);
+  const size_t smem = (size_t)LNB_WARPS * nout * C * sizeof(float);
+  if (rms) {
+    auto k = ln_pick(C, layernorm_bwd_kernel<1, true>, layernorm_bwd_kernel<2, true>, layernorm_bwd_kernel<4, true>,
+                     layernorm_bwd_kernel<6, true>, layernorm_bwd_kernel<8, true>, layernorm_bwd_kernel<10, true>);
+    launch_k(k, nb, LNB_WARPS * 32, smem, m->stream, dx, dxbf, m->scratch, dy, x, w, mean, rstd, N, C, 0);
+  } else {
+    auto k = ln_pick(C, layernorm_bwd_kernel<1, false>, layernorm_bwd_kernel<2, false>, layernorm_bwd_kernel<4, false>,
+                     layernorm_bwd_kernel<6, false>, layernorm_bwd_kernel<8, false>, layernorm_bwd_kernel<10, false>);
+    launch_k(k, nb, LNB_WARPS * 32, smem, m->stream, dx, dxbf, m->scratch, dy, x, w, mean, rstd, N, C, dxsum ? 1 : 0);
+  }
   // dw[c] (+)= sum_b partial[b][c], db[c] (+)= sum_b partial[b][C + c], dxsum[c] (+)= ...[2C + c]
   launch_k(col_finish_kernel, ceil_div(nout * C, 32), COLF_WARPS * 32, 0, m->stream, dw, db, dxsum, C, m->scratch, nb,
            nout * C, m->grad_accumulate);
@@ -748,12 +773,18 @@ static int set_kernel_attributes() {
                                tca::dqk::SMEM_BYTES);
     // layernorm backward: 8 rows x 3C floats of shared memory (C <= 1280)
     const int lnb = LNB_WARPS * 3 * 32 * 4 * LN_MAXV4_LIMIT * (int)sizeof(float);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<10>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<6, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<6, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<10, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<10, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
     // CUDA-core attention: up to head size 128
     const int f = (int)att_smem_fwd(128), kv = (int)att_smem_dkv(128);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_fwd_simt_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, f);
@@ -832,28 +863,37 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
     launch_k(validate_tokens_kernel, grid_for(N, 256, 64), 256, 0, s, d_in, d_tgt, N, V, m->err);
     m->launches++;
   }
-  launch_k(encoder_fwd_kernel, grid_for((long long)N * C / 4, 256), 256, 0, s, m->encoded, d_in, m->P[P_WTE], m->P[P_WPE],
+  launch_k(encoder_fwd_kernel, grid_for((long long)N * C / 4, 256), 256, 0, s, m->encoded, d_in, m->P[P_WTE],
+           c.llama ? (const float*)nullptr : m->P[P_WPE],
                                                                           N, T, C, V);
   m->launches++;
   // bf16 matmuls read only the bf16 copies: the fp32 layernorm outputs, the
   // fp32 GELU output and (with the tensor-core attention) the fp32 qkv are
   // then not written at all
   const bool tc_attn = bf && C / c.num_heads == tca::HS && T % tca::BQ == 0;
+  // the Llama-style variant has no linear biases: its matmuls add a zero vector
+  auto bias = [&](int which, size_t off) -> const float* { return c.llama ? m->zero_bias : m->P[which] + off; };
   for (int l = 0; l < L; l++) {
     LayerActs a = layer_acts(m, l);
     ln_forward(m, bf ? nullptr : a.ln1, a.ln1_bf, a.ln1_mean, a.ln1_rstd, a.x, m->P[P_LN1W] + (size_t)l * C,
                m->P[P_LN1B] + (size_t)l * C, N);
-    mm_forward(m, tc_attn ? nullptr : a.qkv, a.qkv_bf, {a.ln1, a.ln1_bf}, wparam(m, P_QKVW, l * 3 * CC),
-               m->P[P_QKVB] + (size_t)l * 3 * C, N, C, 3 * C, EPI_BIAS, nullptr, nullptr);
+    // the rotary embedding reads and rewrites the fp32 q and k, so the variant keeps fp32 qkv
+    mm_forward(m, tc_attn && !c.llama ? nullptr : a.qkv, a.qkv_bf, {a.ln1, a.ln1_bf}, wparam(m, P_QKVW, l * 3 * CC),
+               bias(P_QKVB, (size_t)l * 3 * C), N, C, 3 * C, EPI_BIAS, nullptr, nullptr);
+    if (c.llama) {
+      launch_k(rope_kernel, grid_for((long long)N * C / 2, 256), 256, 0, s, a.qkv, a.qkv_bf, (const float2*)m->rope, B,
+               T, C, c.num_heads, 0);
+      m->launches++;
+    }
     attn_forward(m, a.atty, a.atty_bf, a.lse, a.qkv, a.qkv_bf, B, T, bf);
-    mm_forward(m, a.res2, nullptr, {a.atty, a.atty_bf}, wparam(m, P_ATTPROJW, l * CC), m->P[P_ATTPROJB] + (size_t)l * C,
+    mm_forward(m, a.res2, nullptr, {a.atty, a.atty_bf}, wparam(m, P_ATTPROJW, l * CC), bias(P_ATTPROJB, (size_t)l * C),
                N, C, C, EPI_BIAS_RESID, a.x, nullptr);
     ln_forward(m, bf ? nullptr : a.ln2, a.ln2_bf, a.ln2_mean, a.ln2_rstd, a.res2, m->P[P_LN2W] + (size_t)l * C,
                m->P[P_LN2B] + (size_t)l * C, N);
     mm_forward(m, bf ? nullptr : a.fchg, a.fchg_bf, {a.ln2, a.ln2_bf}, wparam(m, P_FCW, l * 4 * CC),
-               m->P[P_FCB] + (size_t)l * 4 * C, N, C, 4 * C, EPI_BIAS_GELU, nullptr, a.fch);
+               bias(P_FCB, (size_t)l * 4 * C), N, C, 4 * C, EPI_BIAS_GELU, nullptr, a.fch);
     mm_forward(m, a.res3, nullptr, {a.fchg, a.fchg_bf}, wparam(m, P_FCPROJW, l * 4 * CC),
-               m->P[P_FCPROJB] + (size_t)l * C, N, 4 * C, C, EPI_BIAS_RESID, a.res2, nullptr);
+               bias(P_FCPROJB, (size_t)l * C), N, 4 * C, C, EPI_BIAS_RESID, a.res2, nullptr);
   }
   LayerActs last = layer_acts(m, L - 1);
   ln_forward(m, bf ? nullptr : m->lnf, m->lnf_bf, m->lnf_mean, m->lnf_rstd, last.res3, m->P[P_LNFW], m->P[P_LNFB], N);
@@ -885,17 +925,20 @@ static int enqueue_backward(gpt2_t* m) {
   float** P = m->P;
   float** G = m->G;
   const Opnd dres = {m->dres, m->dres_bf}, dfch = {m->dfch, m->dfch_bf}, dqkv = {m->dqkv, m->dqkv_bf};
+  // the Llama-style variant has no biases (and no bias gradients) and no position table
+  const bool ll = c.llama != 0;
   // the fused column sums need 32-column-aligned rows of 16-byte-aligned floats
-  const bool fuse_fcb = bf && (4 * C) % 32 == 0;
+  const bool fuse_fcb = bf && !ll && (4 * C) % 32 == 0;
   // the tensor-core attention backward (bf16, hs = 64, T % 128 == 0) takes the QKV bias column sums
-  const bool fuse_qkvb = bf && C / c.num_heads == tca::HS && T % tca::BQ == 0;
+  const bool fuse_qkvb = bf && !ll && C / c.num_heads == tca::HS && T % tca::BQ == 0;
+  auto gbias = [&](int which, size_t off) -> float* { return ll ? nullptr : G[which] + off; };
   // LM head (tied to wte): dlnf = dlogits wte; dwte += dlogits^T lnf
   mm_dx(m, m->dln, nullptr, {m->dlogits, m->dlogits_bf}, wparam(m, P_WTE, 0), N, C, Vp, nullptr);
   mm_dw(m, G[P_WTE], {m->dlogits, m->dlogits_bf}, {m->lnf, m->lnf_bf}, N, C, Vp);
   CCHECK(m, cudaMemsetAsync(m->dres, 0, (size_t)N * C * sizeof(float), s));
   LayerActs last = layer_acts(m, L - 1);
   // the column sums of this dres are the last layer's MLP output-projection bias gradient
-  ln_backward(m, m->dres, m->dres_bf, G[P_LNFW], G[P_LNFB], G[P_FCPROJB] + (size_t)(L - 1) * C, m->dln, last.res3,
+  ln_backward(m, m->dres, m->dres_bf, G[P_LNFW], G[P_LNFB], gbias(P_FCPROJB, (size_t)(L - 1) * C), m->dln, last.res3,
               P[P_LNFW], m->lnf_mean, m->lnf_rstd, N);
   for (int l = L - 1; l >= 0; l--) {
     LayerActs a = layer_acts(m, l);
@@ -904,28 +947,33 @@ static int enqueue_backward(gpt2_t* m) {
     // (its bias gradient came with the layernorm backward that produced dres)
     // x gelu'(fch).  bf16: only the bf16 copy of dfch is stored; the MLP input
     // bias gradient comes from column sums taken in the same epilogue
-    mm_dx(m, fuse_fcb ? nullptr : m->dfch, m->dfch_bf, dres, wparam(m, P_FCPROJW, l * 4 * CC), N, 4 * C, C, a.fch,
-          fuse_fcb ? m->scratch : nullptr);
+    mm_dx(m, bf && (fuse_fcb || ll) ? nullptr : m->dfch, m->dfch_bf, dres, wparam(m, P_FCPROJW, l * 4 * CC), N, 4 * C, C,
+          a.fch, fuse_fcb ? m->scratch : nullptr);
     // MLP input projection: fch = ln2 fcw^T + fcb
     mm_dw(m, G[P_FCW] + l * 4 * CC, dfch, {a.ln2, a.ln2_bf}, N, C, 4 * C);
     if (fuse_fcb) bias_finish(m, G[P_FCB] + (size_t)l * 4 * C, ceil_div(N, 32), 4 * C);
-    else bias_grad(m, G[P_FCB] + (size_t)l * 4 * C, m->dfch, N, 4 * C);
+    else if (!ll) bias_grad(m, G[P_FCB] + (size_t)l * 4 * C, m->dfch, N, 4 * C);
     mm_dx(m, m->dln, nullptr, dfch, wparam(m, P_FCW, l * 4 * CC), N, C, 4 * C, nullptr);
     ln_backward(m, m->dres, m->dres_bf, G[P_LN2W] + (size_t)l * C, G[P_LN2B] + (size_t)l * C,
-                G[P_ATTPROJB] + (size_t)l * C, m->dln, a.res2, P[P_LN2W] + (size_t)l * C, a.ln2_mean, a.ln2_rstd, N);
+                gbias(P_ATTPROJB, (size_t)l * C), m->dln, a.res2, P[P_LN2W] + (size_t)l * C, a.ln2_mean, a.ln2_rstd, N);
     // attention output projection: res2 = x + atty attprojw^T + attprojb
     mm_dw(m, G[P_ATTPROJW] + l * CC, dres, {a.atty, a.atty_bf}, N, C, C);
     mm_dx(m, m->datty, m->datty_bf, dres, wparam(m, P_ATTPROJW, l * CC), N, C, C, nullptr);
     // attention
     attn_backward(m, a.qkv, a.qkv_bf, a.atty, a.lse, B, T, bf, fuse_qkvb);
+    if (ll) {  // q and k were rotated after the matmul: turn their gradients back (the transpose)
+      launch_k(rope_kernel, grid_for((long long)N * C / 2, 256), 256, 0, s, m->dqkv, m->dqkv_bf, (const float2*)m->rope,
+               B, T, C, c.num_heads, 1);
+      m->launches++;
+    }
     // qkv projection: qkv = ln1 qkvw^T + qkvb
     mm_dw(m, G[P_QKVW] + l * 3 * CC, dqkv, {a.ln1, a.ln1_bf}, N, C, 3 * C);
     if (fuse_qkvb) bias_finish(m, G[P_QKVB] + (size_t)l * 3 * C, N / tca::BQ, 3 * C);
-    else bias_grad(m, G[P_QKVB] + (size_t)l * 3 * C, m->dqkv, N, 3 * C);
+    else if (!ll) bias_grad(m, G[P_QKVB] + (size_t)l * 3 * C, m->dqkv, N, 3 * C);
     mm_dx(m, m->dln, nullptr, dqkv, wparam(m, P_QKVW, l * 3 * CC), N, C, 3 * C, nullptr);
     // below layer 0 this dres is the previous layer's MLP output gradient
     ln_backward(m, m->dres, m->dres_bf, G[P_LN1W] + (size_t)l * C, G[P_LN1B] + (size_t)l * C,
-                l > 0 ? G[P_FCPROJB] + (size_t)(l - 1) * C : nullptr, m->dln, a.x, P[P_LN1W] + (size_t)l * C,
+                l > 0 ? gbias(P_FCPROJB, (size_t)(l - 1) * C) : nullptr, m->dln, a.x, P[P_LN1W] + (size_t)l * C,
                 a.ln1_mean, a.ln1_rstd, N);
   }
   // embeddings
@@ -933,9 +981,12 @@ static int enqueue_backward(gpt2_t* m) {
   while ((int)smem < N) smem <<= 1;
   launch_k(sort_tokens_kernel, 1, 1024, smem * sizeof(uint32_t), s, m->tokens, N, c.vocab_size, m->sorted);
   launch_k(wte_grad_kernel, dim3(N, ceil_div(C, 128)), WTE_WARPS * 32, 0, s, G[P_WTE], m->dres, m->sorted, N, C);
-  launch_k(wpe_grad_kernel, grid_for((long long)T * C / 4, 256), 256, 0, s, G[P_WPE], m->dres, B, T, C,
-           m->grad_accumulate);
-  m->launches += 3;
+  m->launches += 2;
+  if (!ll) {
+    launch_k(wpe_grad_kernel, grid_for((long long)T * C / 4, 256), 256, 0, s, G[P_WPE], m->dres, B, T, C,
+             m->grad_accumulate);
+    m->launches++;
+  }
   KCHECK(m);
   return GPT2_OK;
 }
@@ -1009,6 +1060,8 @@ static void carve(gpt2_t* m) {
 #define CARVE_BF(f) m->f = m->params_bf ? (uint16_t*)(a + p.f) : nullptr
   CARVE_BF(ln1_bf); CARVE_BF(qkv_bf); CARVE_BF(atty_bf); CARVE_BF(ln2_bf); CARVE_BF(fchg_bf); CARVE_BF(lnf_bf); CARVE_BF(dlogits_bf);
   CARVE_BF(dres_bf); CARVE_BF(dfch_bf); CARVE_BF(dqkv_bf); CARVE_BF(datty_bf);
+  m->rope = m->cfg.llama ? (float2*)(a + p.rope) : nullptr;
+  m->zero_bias = m->cfg.llama ? (float*)(a + p.zero_bias) : nullptr;
 #undef CARVE_BF
 }
 
@@ -1083,6 +1136,23 @@ EXPORT int gpt2_build(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, int m
   if ((e = cudaMemsetAsync(m->tilectr, 0, TILE_CTRS * sizeof(int), m->stream)) != cudaSuccess) goto cuda_fail;
   if ((rc = init_params(m, seed)) != GPT2_OK) goto fail;
   if ((rc = refresh_bf16(m)) != GPT2_OK) goto fail;
+  if (m->cfg.llama) {
+    // rotary angles t * 10000^(-2i/hs) in double, stored as (cos, sin) floats:
+    // accurate to float rounding even where t * frequency is ~1000 radians
+    const int half = cfg->channels / cfg->num_heads / 2;
+    std::vector<float2> tab((size_t)maxT * half);
+    for (int t = 0; t < maxT; t++)
+      for (int i = 0; i < half; i++) {
+        const double theta = t * pow(10000.0, -2.0 * i / (2.0 * half));
+        tab[(size_t)t * half + i] = make_float2((float)cos(theta), (float)sin(theta));
+      }
+    if ((e = cudaMemcpyAsync(m->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice, m->stream)) !=
+        cudaSuccess)
+      goto cuda_fail;
+    if ((e = cudaMemsetAsync(m->zero_bias, 0, 4 * (size_t)cfg->channels * sizeof(float), m->stream)) != cudaSuccess)
+      goto cuda_fail;
+    if ((e = cudaStreamSynchronize(m->stream)) != cudaSuccess) goto cuda_fail;  // tab is released on return
+  }
   if ((e = cudaStreamSynchronize(m->stream)) != cudaSuccess) goto cuda_fail;
   *out = m;
   return GPT2_OK;
@@ -1249,7 +1319,7 @@ static int enqueue_step(gpt2_t* m, int B, int T) {
   int rc;
   if ((rc = enqueue_forward(m, m->tokens, m->targets, B, T, 1))) return rc;
   const int C = m->cfg.channels;
-  if (m->cfg.max_seq_len > T)
+  if (m->cfg.max_seq_len > T && !m->cfg.llama)  // (the Llama-style variant has no position table)
     CCHECK(m, cudaMemsetAsync(m->G[P_WPE] + (size_t)T * C, 0, (size_t)(m->cfg.max_seq_len - T) * C * sizeof(float),
                               m->stream));
   m->grad_accumulate = 0;

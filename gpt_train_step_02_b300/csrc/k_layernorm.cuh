@@ -6,6 +6,9 @@
 //   dx += rstd * (g - mean(g) - n * mean(g * n))     (accumulated in place;
 //                                                    optional bf16 copy of dx)
 //   dw += sum_rows dy * n,  db += sum_rows dy         (two-stage, fixed order)
+// RMS = true gives RMSNorm (the Llama-style variant): no mean is subtracted
+// (mean = 0 is stored), rstd = 1/sqrt(mean(x^2) + 1e-5), y = x * rstd * w with
+// no shift, and the backward drops the mean(g) term and produces dw only.
 // C must be a multiple of 4 and at most 32 * 4 * LN_MAXV4_LIMIT; the kernels
 // are instantiated for the per-lane float4 count ceil(C / 128) so that the
 // row lives in as few registers as it needs.
@@ -15,7 +18,7 @@
 #define LN_MAXV4_LIMIT 10  // float4 elements per lane: C <= 32 * 4 * 10 = 1280
 #define LN_EPS 1e-5f
 
-template <int LN_MAXV4>
+template <int LN_MAXV4, bool RMS>
 __global__ void layernorm_fwd_kernel(float* __restrict__ y, uint16_t* __restrict__ ybf, float* __restrict__ mean,
                                      float* __restrict__ rstd, const float* __restrict__ x,
                                      const float* __restrict__ w, const float* __restrict__ b, int N, int C) {
@@ -35,7 +38,7 @@ __global__ void layernorm_fwd_kernel(float* __restrict__ y, uint16_t* __restrict
       s += (v[k].x + v[k].y) + (v[k].z + v[k].w);
     }
   }
-  float mu = warp_sum(s) / (float)C;
+  float mu = RMS ? 0.f : warp_sum(s) / (float)C;
   float q = 0.f;
 #pragma unroll
   for (int k = 0; k < LN_MAXV4; k++) {
@@ -52,7 +55,7 @@ __global__ void layernorm_fwd_kernel(float* __restrict__ y, uint16_t* __restrict
     int c = (lane + 32 * k) * 4;
     if (c < C) {
       float4 ww = *reinterpret_cast<const float4*>(w + c);
-      float4 bb = *reinterpret_cast<const float4*>(b + c);
+      const float4 bb = RMS ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(b + c);
       float4 o;
       o.x = (v[k].x - mu) * rs * ww.x + bb.x;
       o.y = (v[k].y - mu) * rs * ww.y + bb.y;
@@ -80,7 +83,7 @@ __global__ void layernorm_fwd_kernel(float* __restrict__ y, uint16_t* __restrict
 #define LNB_WARPS 8
 #define LNB_MIN_ROWS LNB_WARPS  // rows per block
 
-template <int LN_MAXV4>
+template <int LN_MAXV4, bool RMS>
 __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
     float* __restrict__ dx, uint16_t* __restrict__ dxbf, float* __restrict__ partial, const float* __restrict__ dy,
     const float* __restrict__ x, const float* __restrict__ w, const float* __restrict__ mean,
@@ -89,7 +92,7 @@ __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
   pdl_wait();
   extern __shared__ float sh[];  // [LNB_WARPS][nout * C]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nout = with_dxsum ? 3 : 2;
+  const int nout = RMS ? 1 : (with_dxsum ? 3 : 2);  // partial columns: dw [, db [, dx sums]]
   const int r = blockIdx.x * LNB_WARPS + warp;
   float* my = sh + warp * nout * C;
   if (r < N) {
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
         sgn += (g0 * n0 + g1 * n1) + (g2 * n2 + g3 * n3);
       }
     }
-    const float mg = warp_sum(sg) / (float)C, mgn = warp_sum(sgn) / (float)C;
+    const float mg = RMS ? 0.f : warp_sum(sg) / (float)C, mgn = warp_sum(sgn) / (float)C;
 #pragma unroll
     for (int k = 0; k < LN_MAXV4; k++) {
       const int c = (lane + 32 * k) * 4;
@@ -138,8 +141,10 @@ __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
           *reinterpret_cast<uint2*>(dxbf + (size_t)r * C + c) = make_uint2(bf16x2_bits(a.x, a.y), bf16x2_bits(a.z, a.w));
         }
         *reinterpret_cast<float4*>(my + c) = make_float4(dv[k].x * n.x, dv[k].y * n.y, dv[k].z * n.z, dv[k].w * n.w);
-        *reinterpret_cast<float4*>(my + C + c) = dv[k];
-        if (with_dxsum) *reinterpret_cast<float4*>(my + 2 * C + c) = a;
+        if (!RMS) {
+          *reinterpret_cast<float4*>(my + C + c) = dv[k];
+          if (with_dxsum) *reinterpret_cast<float4*>(my + 2 * C + c) = a;
+        }
       }
     }
   } else {

@@ -67,7 +67,8 @@ __global__ void encoder_fwd_kernel(float* __restrict__ x, const int* __restrict_
     int id = min(max(ids[bt], 0), V - 1);
     int t = bt % T;
     float4 e = reinterpret_cast<const float4*>(wte + (size_t)id * C)[c4];
-    float4 p = reinterpret_cast<const float4*>(wpe + (size_t)t * C)[c4];
+    // wpe == NULL: no learned position table (the Llama-style variant)
+    float4 p = wpe ? reinterpret_cast<const float4*>(wpe + (size_t)t * C)[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
     reinterpret_cast<float4*>(x + (size_t)bt * C)[c4] = make_float4(e.x + p.x, e.y + p.y, e.z + p.z, e.w + p.w);
   }
 }

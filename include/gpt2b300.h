@@ -52,10 +52,20 @@ extern "C" {
 #define GPT2_PREC_FP32 0 /* fp32 operands (3xTF32 split products), fp32 everything */
 #define GPT2_PREC_BF16 1 /* bf16 matmul/attention operands, fp32 accumulate, fp32 master/AdamW */
 
-/* GPT2Config (item 2 of the page above) plus the padded vocabulary and the
- * matmul operand precision.  Requirements: channels % num_heads == 0,
- * channels % 64 == 0, head size (channels/num_heads) in {16, 32, 64, 128},
- * vocab_size <= padded_vocab_size, padded_vocab_size % 64 == 0. */
+/* GPT2Config (item 2 of the page above) plus the padded vocabulary, the
+ * matmul operand precision and the architecture variant.  Requirements:
+ * channels % num_heads == 0, channels % 64 == 0, head size
+ * (channels/num_heads) in {16, 32, 64, 128}, vocab_size <= padded_vocab_size,
+ * padded_vocab_size % 64 == 0, llama in {0, 1}.
+ * llama = 1 selects the Llama-style variant that the page «千行C代码训完GPT-2»
+ * (新智元) names as llm.c's next architectures (RMSNorm in place of layernorm,
+ * new layers such as RoPE): every layernorm becomes RMSNorm (y = x rstd w,
+ * rstd = 1/sqrt(mean(x^2) + 1e-5), no shift), q and k get rotary position
+ * embeddings after the QKV matmul (pair (2i, 2i+1) of each head turned by
+ * t * 10000^(-2i/hs) radians), there is no learned position table and no
+ * linear bias.  Those tensors keep their places in the flat parameter layout
+ * with zero elements, so the layout is GPT-2's minus wpe, every bias and every
+ * layernorm shift. */
 typedef struct {
   int max_seq_len;
   int vocab_size;
@@ -64,6 +74,7 @@ typedef struct {
   int num_heads;
   int channels;
   int gemm_precision;
+  int llama;
 } gpt2_config;
 
 typedef struct gpt2_t gpt2_t;
