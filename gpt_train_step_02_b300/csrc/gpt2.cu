@@ -356,19 +356,63 @@ struct MatmulDesc {
   const uint16_t* Bbf;
 };
 
-// Split K so that small-M products still fill the 148 SMs.  The splits of a
-// tile form one thread-block cluster (at most 8 CTAs, the portable cluster
-// size) and are reduced through distributed shared memory in split order.
+// Clusters of s CTAs of the fp32 matmul (one CTA per SM: its shared memory
+// fills the SM) that the GPU holds at once, s = 1..8, and the SM count; filled
+// once per process after the kernel's shared-memory limit is set.  A cluster
+// sits inside one GPC, so the SMs of a GPC beyond a multiple of s stay idle:
+// at s = 3 a 148-SM B300 holds 45 clusters (135 CTAs), not 49.
+static int g_num_sms = 148;
+static int g_max_clusters[9] = {0, 148, 0, 0, 0, 0, 0, 0, 0};
+
+static cudaError_t query_cluster_limits() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+  g_max_clusters[1] = g_num_sms;
+  for (int s = 2; s <= 8 && e == cudaSuccess; s++) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, s);
+    cfg.blockDim = dim3(tc::THREADS);
+    cfg.dynamicSmemBytes = tc::SMEM_BYTES;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 1;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = s;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, tc::gemm_tf32x3_kernel, &cfg);
+    g_max_clusters[s] = n;
+  }
+  return e;
+}
+
+// Split K so that small-M products still fill the SMs.  The splits of a tile
+// form one thread-block cluster (at most 8 CTAs, the portable cluster size)
+// and are reduced through distributed shared memory in split order.  Cost of
+// s splits in units of one K tile of the main loop: waves x (K tiles per
+// split + pipeline fill and epilogue) + the cluster reduction, a wave being
+// as many clusters as the GPU holds at once.  A tile beyond the first wave
+// doubles the time, so s is chosen against the cluster limit above.
 static int choose_splits(int M, int N, int K) {
-  long long tiles = (long long)ceil_div(M, tc::BM) * ceil_div(N, tc::BN);
-  int kt = ceil_div(K, tc::BK);
-  if (tiles >= 148 || kt < 4) return 1;
-  int s = (int)(148 / tiles);
-  s = s < kt / 2 ? s : kt / 2;
-  s = s < 8 ? s : 8;
-  if (s < 1) s = 1;
-  int per = ceil_div(kt, s);
-  return ceil_div(kt, per);
+  const long long tiles = (long long)ceil_div(M, tc::BM) * ceil_div(N, tc::BN);
+  const int kt = ceil_div(K, tc::BK);
+  if (kt < 4) return 1;
+  const int FILL = 4, REDUCE = 3;
+  int best = 1;
+  long long best_cost = ((tiles + g_num_sms - 1) / g_num_sms) * (long long)(kt + FILL);
+  for (int s = 2; s <= 8 && s <= kt / 2; s++) {
+    const int per = ceil_div(kt, s);
+    if (ceil_div(kt, per) != s || g_max_clusters[s] <= 0) continue;  // same split as a smaller s, or no fit
+    const long long waves = (tiles + g_max_clusters[s] - 1) / g_max_clusters[s];
+    const long long cost = waves * (per + FILL) + REDUCE;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
 }
 
 // Launches the 3xTF32 tensor-core matmul (one launch; K splits reduced in
@@ -760,6 +804,7 @@ static int set_kernel_attributes() {
                                          SORT_MAX * (int)sizeof(uint32_t));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc::gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+    if (e == cudaSuccess) e = query_cluster_limits();
     if (e == cudaSuccess) e = set_bf16_smem<256>();
     if (e == cudaSuccess) e = set_bf16_smem<128>();
     if (e == cudaSuccess)
