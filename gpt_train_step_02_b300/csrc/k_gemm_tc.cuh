@@ -20,10 +20,16 @@
 // through distributed shared memory (below).
 //   warp 0      one lane issues the TMA loads of raw fp32 tiles (raw ring)
 //   warp 1      allocates TMEM; one lane issues tcgen05.mma and commits
-//   warps 2..9  split each raw tile into hi/lo tiles laid out K-major with
-//               the 128-byte swizzle (transposing MN-major tiles), then run
+//   warps 2..9  split each raw tile into hi/lo halves: A's go to tensor
+//               memory (row i in TMEM lane i, one K value per column), B's
+//               to shared memory laid out K-major with the 128-byte swizzle
+//               (MN-major tiles are transposed on the way); then they run
 //               the epilogue: tcgen05.ld TMEM -> registers -> global (two
 //               warps per TMEM lane quadrant, 64 columns each).
+// The MMAs read A from tensor memory and only B from shared memory, so a K
+// tile costs the splitters' raw reads and B writes plus three B reads: about
+// half the shared-memory traffic of staging both operands there, which is
+// what bounds the main loop.
 // Every mbarrier wait is bounded; on expiry the CTA records DEV_ERR_TIMEOUT
 // in the error word, stops issuing work, frees its TMEM and returns.
 #pragma once
@@ -37,28 +43,31 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int BK = 32;  // fp32 elements = 128 bytes: one swizzle row
-constexpr int RAW_STAGES = 3;
+constexpr int RAW_STAGES = 4;
 constexpr int COMP_STAGES = 2;
 constexpr int TILE_BYTES = BM * BK * 4;  // 16 KB (A or B tile)
 constexpr int SPLIT_WARPS = 8;           // splitter / epilogue warps (two per TMEM lane quadrant)
 constexpr int SPLIT_THREADS = 32 * SPLIT_WARPS;
 constexpr int THREADS = 64 + SPLIT_THREADS;
-constexpr int TMEM_COLS = 128;
+// TMEM columns: the 128 x 128 fp32 accumulator in 0..127, then per hi/lo
+// stage c the A halves: hi at TM_A + 64c, lo at TM_A + 64c + 32.
+constexpr int TM_A = 128;
+constexpr int TMEM_COLS = 256;
+static_assert(TM_A + COMP_STAGES * 2 * BK <= TMEM_COLS, "A stages must fit the TMEM allocation");
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s of wall time per wait before giving up
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int OFF_RAW_A = 0;
 constexpr int OFF_RAW_B = OFF_RAW_A + RAW_STAGES * TILE_BYTES;
-constexpr int OFF_HI_A = OFF_RAW_B + RAW_STAGES * TILE_BYTES;
-constexpr int OFF_LO_A = OFF_HI_A + COMP_STAGES * TILE_BYTES;
-constexpr int OFF_HI_B = OFF_LO_A + COMP_STAGES * TILE_BYTES;
+constexpr int OFF_HI_B = OFF_RAW_B + RAW_STAGES * TILE_BYTES;
 constexpr int OFF_LO_B = OFF_HI_B + COMP_STAGES * TILE_BYTES;
 constexpr int OFF_BAR = OFF_LO_B + COMP_STAGES * TILE_BYTES;
-// after the main loop the hi/lo region holds this CTA's split-K partial tile
-constexpr int OFF_STAGE = OFF_HI_A;
+// after the main loop (every raw tile consumed) the raw ring holds this CTA's
+// split-K partial tile or the epilogue's staging
+constexpr int OFF_STAGE = OFF_RAW_A;
 constexpr int STAGE_PITCH = BN + 4;  // floats per staged row (padding spreads the banks)
-static_assert(BM * STAGE_PITCH * 4 <= OFF_BAR - OFF_HI_A, "staged partial tile must fit the hi/lo region");
-static_assert(SPLIT_WARPS * EPI_STAGE_FLOATS * 4 <= OFF_BAR - OFF_HI_A, "epilogue staging must fit the hi/lo region");
+static_assert(BM * STAGE_PITCH * 4 <= OFF_HI_B - OFF_RAW_A, "staged partial tile must fit the raw ring");
+static_assert(SPLIT_WARPS * EPI_STAGE_FLOATS * 4 <= OFF_HI_B - OFF_RAW_A, "epilogue staging must fit the raw ring");
 constexpr int NUM_BARS = 2 * RAW_STAGES + 2 * COMP_STAGES + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
@@ -229,6 +238,16 @@ GPT2_DEV void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t
       : "memory");
 }
 
+// The same MMA with A read from tensor memory (M rows in TMEM lanes 0..127,
+// the instruction's 8 K values in 8 consecutive columns from a_tmem).
+GPT2_DEV void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(IDESC_TF32), "r"(accumulate)
+      : "memory");
+}
+
 GPT2_DEV void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -257,6 +276,52 @@ GPT2_DEV float tf32_hi(float x) { return __uint_as_float((__float_as_uint(x) + 0
 GPT2_DEV void split4(float4 x, float4& h, float4& l) {
   h = make_float4(tf32_hi(x.x), tf32_hi(x.y), tf32_hi(x.z), tf32_hi(x.w));
   l = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+}
+
+// 16 consecutive TMEM columns of this warp's 32 lanes from v[] (lane i -> TMEM
+// lane (taddr >> 16) + i).  Asynchronous: tcgen05.wait::st before the values
+// are handed to the tensor core.
+GPT2_DEV void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+// A operand into TMEM: this lane holds tile row m (its TMEM lane) and the 16
+// K values [16h, 16h + 16); their hi halves go to columns t_hi .. t_hi + 15
+// and the lo halves to t_hi + 32 .. (t_hi is this warp's lane base, the
+// stage's hi column and 16h).  K-major raw tiles are as TMA wrote them with
+// the 128-byte swizzle: the 16-byte chunk c of row m sits at chunk c ^ (m & 7).
+GPT2_DEV void split_a_kmajor_tmem(const float* raw, uint32_t t_hi, int m, int h) {
+  float hv[16], lv[16];
+#pragma unroll
+  for (int cc = 0; cc < 4; cc++) {
+    const int c = 4 * h + cc;
+    float4 hh, ll;
+    split4(*reinterpret_cast<const float4*>(raw + m * BK + ((c ^ (m & 7)) << 2)), hh, ll);
+    hv[4 * cc] = hh.x; hv[4 * cc + 1] = hh.y; hv[4 * cc + 2] = hh.z; hv[4 * cc + 3] = hh.w;
+    lv[4 * cc] = ll.x; lv[4 * cc + 1] = ll.y; lv[4 * cc + 2] = ll.z; lv[4 * cc + 3] = ll.w;
+  }
+  tmem_st16(t_hi, hv);
+  tmem_st16(t_hi + BK, lv);
+}
+
+// The same from an MN-major raw tile (unswizzled [BK rows of k][128 of m]).
+GPT2_DEV void split_a_mnmajor_tmem(const float* raw, uint32_t t_hi, int m, int h) {
+  float hv[16], lv[16];
+#pragma unroll
+  for (int k = 0; k < 16; k++) {
+    const float x = raw[(16 * h + k) * BM + m];
+    hv[k] = tf32_hi(x);
+    lv[k] = x - hv[k];
+  }
+  tmem_st16(t_hi, hv);
+  tmem_st16(t_hi + BK, lv);
 }
 
 // raw tile already K-major SW128 (as TMA wrote it): split in place order.
@@ -376,16 +441,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        uint32_t ah = smem_u32(smem + OFF_HI_A + c * TILE_BYTES), al = smem_u32(smem + OFF_LO_A + c * TILE_BYTES);
-        uint32_t bh = smem_u32(smem + OFF_HI_B + c * TILE_BYTES), bl = smem_u32(smem + OFF_LO_B + c * TILE_BYTES);
+        const uint32_t ah = tmem + (uint32_t)(TM_A + c * 2 * BK), al = ah + BK;
+        const uint32_t bh = smem_u32(smem + OFF_HI_B + c * TILE_BYTES), bl = smem_u32(smem + OFF_LO_B + c * TILE_BYTES);
 #pragma unroll
-        for (int j = 0; j < BK / 8; j++) {  // kind::tf32 consumes K = 8 (32 bytes) per instruction
-          uint32_t kb = j * 32;
-          uint64_t dah = smem_desc_kmajor_sw128(ah + kb), dal = smem_desc_kmajor_sw128(al + kb);
-          uint64_t dbh = smem_desc_kmajor_sw128(bh + kb), dbl = smem_desc_kmajor_sw128(bl + kb);
-          mma_tf32(tmem, dah, dbh, (i > 0 || j > 0) ? 1u : 0u);
-          mma_tf32(tmem, dah, dbl, 1u);
-          mma_tf32(tmem, dal, dbh, 1u);
+        for (int j = 0; j < BK / 8; j++) {  // kind::tf32 consumes K = 8 (32 bytes, 8 TMEM columns) per instruction
+          const uint64_t dbh = smem_desc_kmajor_sw128(bh + j * 32), dbl = smem_desc_kmajor_sw128(bl + j * 32);
+          mma_tf32_ta(tmem, ah + 8 * j, dbh, (i > 0 || j > 0) ? 1u : 0u);
+          mma_tf32_ta(tmem, ah + 8 * j, dbl, 1u);
+          mma_tf32_ta(tmem, al + 8 * j, dbh, 1u);
         }
         mma_commit(&comp_empty[c]);  // frees the hi/lo stage once these MMAs have read it
       }
@@ -412,6 +475,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (n0 + c * 32 < p.N) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + n0 + c * 32));
       }
     }
+    const int a_quad = warp & 3, a_half = (warp - 2) >> 2;  // TMEM lanes this warp may access; its K half
     bool ok = true;
     for (int i = 0; i < nk; i++) {
       int s = i % RAW_STAGES, c = i % COMP_STAGES;
@@ -421,22 +485,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         ok = false;
         break;
       }
-      const uint8_t* ra = smem + OFF_RAW_A + s * TILE_BYTES;
+      tc_fence_after();  // the MMAs that read this stage's TMEM columns have completed
+      const float* ra = reinterpret_cast<const float*>(smem + OFF_RAW_A + s * TILE_BYTES);
       const uint8_t* rb = smem + OFF_RAW_B + s * TILE_BYTES;
-      float* ha = reinterpret_cast<float*>(smem + OFF_HI_A + c * TILE_BYTES);
-      float* la = reinterpret_cast<float*>(smem + OFF_LO_A + c * TILE_BYTES);
       float* hb = reinterpret_cast<float*>(smem + OFF_HI_B + c * TILE_BYTES);
       float* lb = reinterpret_cast<float*>(smem + OFF_LO_B + c * TILE_BYTES);
-      if (p.a_kmajor)
-        split_kmajor(reinterpret_cast<const float4*>(ra), reinterpret_cast<float4*>(ha), reinterpret_cast<float4*>(la), t);
-      else
-        split_mnmajor(reinterpret_cast<const float*>(ra), ha, la, t);
+      // A: this warp's TMEM lane quadrant, half of the K columns
+      const uint32_t t_hi = tmem + ((uint32_t)(a_quad * 32) << 16) + (uint32_t)(TM_A + c * 2 * BK + 16 * a_half);
+      if (p.a_kmajor) split_a_kmajor_tmem(ra, t_hi, a_quad * 32 + lane, a_half);
+      else split_a_mnmajor_tmem(ra, t_hi, a_quad * 32 + lane, a_half);
       if (p.b_kmajor)
         split_kmajor(reinterpret_cast<const float4*>(rb), reinterpret_cast<float4*>(hb), reinterpret_cast<float4*>(lb), t);
       else
         split_mnmajor(reinterpret_cast<const float*>(rb), hb, lb, t);
-      // make the generic-proxy smem writes visible to the tensor core (async proxy)
+      // make the TMEM stores complete and the generic-proxy smem writes
+      // visible to the tensor core (async proxy) before the hand-off
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&raw_empty[s]);
