@@ -27,6 +27,7 @@
 #include "../../include/gpt2b300.h"
 #include "common.cuh"
 #include "k_attention_simt.cuh"
+#include "k_attention_small.cuh"
 #include "k_attention_tc.cuh"
 #include "k_gemm_bf16.cuh"
 #include "k_gemm_tc.cuh"
@@ -709,6 +710,11 @@ static int launch_attn_fwd(float* atty, uint16_t* attybf, float* lse, const floa
              tm, p);
     return 1;
   }
+  if (T <= atts::T_MAX && hs == atts::HS) {  // short sequences: one CTA per (batch, head)
+    launch_k(atts::attn_fwd_small_kernel, dim3(NH, B), atts::THREADS, atts::FWD_SMEM, s, atty, attybf, lse, qkv, B, T,
+             C, NH, bf);
+    return 1;
+  }
   const dim3 g(ceil_div(T, ATT_ROWS), NH, B);
   const size_t sm = att_smem_fwd(hs);
   if (hs <= 32) launch_k(attn_fwd_simt_kernel<1>, g, ATT_ROWS * 32, sm, s, atty, attybf, lse, qkv, B, T, C, NH, bf);
@@ -739,6 +745,12 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
   const int hs = C / NH;
   const int grid = ceil_div((long long)B * NH * T * 32, 256);
   const bool tc_path = bf && qkv_bf && dy_bf && hs == tca::HS && T % tca::BQ == 0;
+  if (!tc_path && T <= atts::T_MAX && hs == atts::HS) {  // short sequences: one launch, D formed in the kernel
+    if (!dqkv || colsum) return -1;
+    launch_k(atts::attn_bwd_small_kernel, dim3(NH, B), atts::THREADS, atts::BWD_SMEM, s, dqkv, dqkv_bf, qkv, dy, atty,
+             lse, B, T, C, NH, bf);
+    return 1;
+  }
   // D holds 2 B NH T floats: the (-lse log2 e, -D) pairs of the tensor-core path
   const int ldg = ceil_div((long long)B * T, tca::LD_WARPS);
   if (tc_path && C <= 1024)
@@ -830,6 +842,12 @@ static int set_kernel_attributes() {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<10, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<10, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(atts::attn_fwd_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)atts::FWD_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(atts::attn_bwd_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)atts::BWD_SMEM);
     // CUDA-core attention: up to head size 128
     const int f = (int)att_smem_fwd(128), kv = (int)att_smem_dkv(128);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_fwd_simt_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, f);

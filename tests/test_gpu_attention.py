@@ -2,14 +2,17 @@
 attention_forward (the page «llm.c：Andrej Karpathy带你从零复现LLM», section
 «核心代码解读：train_gpt2.c», item 1), through the C ABI.
 
-* fp32: the CUDA-core kernel, against the fp32 oracle, 1e-5 relative.
+* fp32: the CUDA-core kernels, against the fp32 oracle, 1e-5 relative: the
+  streaming ones, and for head size 64 with T <= 64 the one-CTA-per-head ones
+  (register-tiled products, causal blocks skipped, one backward launch).
 * bf16 with head size 64 and T % 128 == 0: the tensor-core kernel, against
   the oracle fed the same bf16-rounded qkv.  The kernel also rounds the
   softmax weights P to bf16 for the P V product (relative 2^-9 each) while
   the row sums take the fp32 weights, so y is a combination of the v rows
   with weights off by at most 2^-9 relative.  Tolerance: max |dy| <= 1e-2
   max |v|, |d lse| <= 1e-2.
-* bf16 with another head size: the CUDA-core kernel with rounded operands.
+* bf16 with another head size, or T <= 64: the CUDA-core kernels with
+  rounded operands.
 Inputs come from ``synth``; expected values from ``oracle/`` only."""
 import numpy as np
 import pytest
@@ -52,8 +55,11 @@ def run_gpu(qkv, NH, precision):
 
 
 # CUDA-core shapes: several 64-row chunks with a ragged tail (T = 200), head
-# sizes 16, 64 and 128, a single position, a partial 8-row CTA (T = 13)
-FP32_SHAPES = [(2, 32, 64, 4), (1, 13, 64, 4), (2, 64, 768, 12), (1, 1, 64, 4), (1, 200, 128, 2), (1, 70, 256, 2)]
+# sizes 16, 64 and 128, a single position, a partial 8-row CTA (T = 13); the
+# short-sequence kernels (head size 64, T <= 64) at the GPT-2 124M shape of
+# the B=4, T=64 step, with ragged T (37, 61: partial 4-row blocks) and T = 1
+FP32_SHAPES = [(2, 32, 64, 4), (1, 13, 64, 4), (2, 64, 768, 12), (1, 1, 64, 4), (1, 200, 128, 2), (1, 70, 256, 2),
+               (4, 64, 768, 12), (2, 37, 128, 2), (3, 61, 192, 3), (1, 1, 128, 2)]
 
 
 @pytest.mark.parametrize("B,T,C,NH", FP32_SHAPES)
@@ -97,6 +103,21 @@ def test_attention_forward_bf16_other_head_size():
     ry, preatt, _ = OPS.attention_forward(bf16(qkv), NH)
     assert np.abs(y - ry).max() <= 1e-2 * np.abs(ry).max()
     assert np.abs(lse - oracle_lse(preatt)).max() <= 1e-3
+
+
+@pytest.mark.parametrize("B,T,C,NH", [(2, 48, 128, 2), (1, 64, 768, 12)])
+def test_attention_forward_bf16_short_sequences(B, T, C, NH):
+    """Head size 64, T <= 64: the one-CTA-per-head kernel with operands and
+    the P entering P V rounded to bf16, against the oracle fed the rounded qkv."""
+    import gpt_train_step_02_b300 as g
+
+    qkv = synth.randn(304, (B, T, 3 * C))
+    y, lse = run_gpu(qkv, NH, g.GPT2_PREC_BF16)
+    q = bf16(qkv)
+    ry, preatt, _ = OPS.attention_forward(q, NH)
+    assert np.abs(y - ry).max() <= 1e-2 * np.abs(ry).max()
+    assert np.abs(lse - oracle_lse(preatt)).max() <= 1e-3
+    np.testing.assert_allclose(y[:, 0, :], q[:, 0, 2 * C:], rtol=0, atol=0)
 
 
 def run_gpu_backward(qkv, dy, NH, precision):
@@ -149,3 +170,23 @@ def test_attention_backward_bf16_tensor_cores(B, T, C, NH):
     # the last key of each sequence is seen only by the last query
     last_k = ref_d[:, -1, C:2 * C]
     np.testing.assert_allclose(got[:, -1, C:2 * C], last_k, atol=3e-2 * np.abs(ref_d[..., C:2 * C]).max())
+
+
+@pytest.mark.parametrize("B,T,C,NH", [(2, 48, 128, 2), (1, 64, 768, 12)])
+def test_attention_backward_bf16_short_sequences(B, T, C, NH):
+    """Head size 64, T <= 64 with bf16 operands: the one-launch backward with
+    q, k, v, dy, P (for dV) and dS rounded to bf16, against the oracle fed the
+    rounded qkv and dy; bars as for the tensor-core backward."""
+    import gpt_train_step_02_b300 as g
+
+    qkv = synth.randn(315, (B, T, 3 * C))
+    dy = synth.randn(316, (B, T, C))
+    got = run_gpu_backward(qkv, dy, NH, g.GPT2_PREC_BF16)
+    q, d = bf16(qkv), bf16(dy)
+    _, _, att = OPS.attention_forward(q, NH)
+    ref_d = OPS.attention_backward(d, q, att, NH)
+    assert np.isfinite(got).all()
+    for part in range(3):
+        gp, rp = got[..., part * C:(part + 1) * C], ref_d[..., part * C:(part + 1) * C]
+        assert rel_l2(gp, rp) <= 1e-2, (part, rel_l2(gp, rp))
+        assert np.abs(gp - rp).max() <= 3e-2 * np.abs(rp).max(), part
