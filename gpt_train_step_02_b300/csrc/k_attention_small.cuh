@@ -63,26 +63,48 @@ GPT2_DEV void zero4x4(float (&acc)[4][4]) {
     for (int j = 0; j < 4; j++) acc[i][j] = 0.f;
 }
 
-// Rows 0 .. T-1 of one head's 64 columns (source row r at src + r * ld) into
-// shared memory, row-major (dst[r * P + d]) and/or transposed (dT[d * P + r]);
-// rows T .. 63 are zero.  Lanes take consecutive rows, so the transposing
-// stores hit consecutive words.
-GPT2_DEV void load_head(float* dst, float* dT, const float* src, long long ld, int T, int bf16_ops) {
+// One head's 64 columns of rows 0 .. T-1 of a source (row r at src + r * ld),
+// to be stored in shared memory row-major (dst[r * P + d]) and/or transposed
+// (dT[d * P + r]); rows T .. 63 are stored as zero.
+struct HeadCopy {
+  const float* src;
+  long long ld;
+  float* dst;
+  float* dT;
+};
+
+// All NS copies, every global load issued before the first shared-memory
+// store (one round trip to L2 / HBM instead of NS).  Lanes take consecutive
+// rows, so the transposing stores hit consecutive words.
+template <int NS>
+GPT2_DEV void load_heads(const HeadCopy (&cp)[NS], int T, int bf16_ops) {
+  constexpr int U = T_MAX * HS / 4 / THREADS;
+  float4 v[NS][U];
 #pragma unroll
-  for (int u = 0; u < T_MAX * HS / 4 / THREADS; u++) {
-    const int e = threadIdx.x + u * THREADS;
-    const int r = e & (T_MAX - 1), c = (e >> 6) * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < T) v = *reinterpret_cast<const float4*>(src + (size_t)r * ld + c);
-    v = make_float4(att_rnd(v.x, bf16_ops), att_rnd(v.y, bf16_ops), att_rnd(v.z, bf16_ops), att_rnd(v.w, bf16_ops));
-    if (dst) *reinterpret_cast<float4*>(dst + r * P + c) = v;
-    if (dT) {
-      dT[(c + 0) * P + r] = v.x;
-      dT[(c + 1) * P + r] = v.y;
-      dT[(c + 2) * P + r] = v.z;
-      dT[(c + 3) * P + r] = v.w;
+  for (int q = 0; q < NS; q++)
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      const int e = threadIdx.x + u * THREADS;
+      const int r = e & (T_MAX - 1), c = (e >> 6) * 4;
+      v[q][u] = r < T ? *reinterpret_cast<const float4*>(cp[q].src + (size_t)r * cp[q].ld + c)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-  }
+#pragma unroll
+  for (int q = 0; q < NS; q++)
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      const int e = threadIdx.x + u * THREADS;
+      const int r = e & (T_MAX - 1), c = (e >> 6) * 4;
+      const float4 x = make_float4(att_rnd(v[q][u].x, bf16_ops), att_rnd(v[q][u].y, bf16_ops),
+                                   att_rnd(v[q][u].z, bf16_ops), att_rnd(v[q][u].w, bf16_ops));
+      if (cp[q].dst) *reinterpret_cast<float4*>(cp[q].dst + r * P + c) = x;
+      if (cp[q].dT) {
+        cp[q].dT[(c + 0) * P + r] = x.x;
+        cp[q].dT[(c + 1) * P + r] = x.y;
+        cp[q].dT[(c + 2) * P + r] = x.z;
+        cp[q].dT[(c + 3) * P + r] = x.w;
+      }
+    }
 }
 
 // max / sum over the 16 threads of a row block (lanes differing in bits 0..3)
@@ -111,9 +133,8 @@ __global__ void __launch_bounds__(THREADS)
   float* PT = V + MAT;
   const int h = blockIdx.x, b = blockIdx.y;
   const float* base = qkv + (size_t)b * T * 3 * C + (size_t)h * HS;
-  load_head(nullptr, QT, base, 3LL * C, T, bf16_ops);
-  load_head(nullptr, KT, base + C, 3LL * C, T, bf16_ops);
-  load_head(V, nullptr, base + 2 * C, 3LL * C, T, bf16_ops);
+  const HeadCopy cp[3] = {{base, 3LL * C, nullptr, QT}, {base + C, 3LL * C, nullptr, KT}, {base + 2 * C, 3LL * C, V, nullptr}};
+  load_heads(cp, T, bf16_ops);
   __syncthreads();
 
   const int t0 = 4 * row_block(), j0 = 4 * col_block();
@@ -196,23 +217,30 @@ __global__ void __launch_bounds__(THREADS)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* base = qkv + (size_t)b * T * 3 * C + (size_t)h * HS;
   const float* gbase = dy + (size_t)b * T * C + (size_t)h * HS;
-  load_head(Qr, QT, base, 3LL * C, T, bf16_ops);
-  load_head(Kr, KT, base + C, 3LL * C, T, bf16_ops);
-  load_head(nullptr, VT, base + 2 * C, 3LL * C, T, bf16_ops);
-  load_head(Gr, GT, gbase, C, T, bf16_ops);
-  // D_t = dy_t . y_t in fp32 (unrounded), and lse, one warp per row
-  for (int t = warp; t < T_MAX; t += THREADS / 32) {
-    float d = 0.f;
-    if (t < T) {
-      const size_t off = ((size_t)b * T + t) * C + (size_t)h * HS;
-      d = dy[off + lane] * y[off + lane] + dy[off + lane + 32] * y[off + lane + 32];
-    }
-    d = warp_sum(d);
-    if (lane == 0) {
-      Ds[t] = d;
-      Ls[t] = t < T ? lse[((size_t)b * NH + h) * T + t] : 0.f;
-    }
+  // D_t = dy_t . y_t in fp32 (unrounded; warp w takes rows w + 8u, lane the
+  // columns lane and lane + 32) and lse: their loads go out with the head
+  // copies' below, so the whole CTA waits for memory once
+  constexpr int DR = T_MAX / (THREADS / 32);
+  float dyv[DR][2], yv[DR][2];
+#pragma unroll
+  for (int u = 0; u < DR; u++) {
+    const int t = warp + u * (THREADS / 32);
+    const size_t off = ((size_t)b * T + t) * C + (size_t)h * HS;
+    dyv[u][0] = t < T ? dy[off + lane] : 0.f;
+    dyv[u][1] = t < T ? dy[off + lane + 32] : 0.f;
+    yv[u][0] = t < T ? y[off + lane] : 0.f;
+    yv[u][1] = t < T ? y[off + lane + 32] : 0.f;
   }
+  const float lsev = (int)threadIdx.x < T ? lse[((size_t)b * NH + h) * T + threadIdx.x] : 0.f;
+  const HeadCopy cp[4] = {{base, 3LL * C, Qr, QT}, {base + C, 3LL * C, Kr, KT}, {base + 2 * C, 3LL * C, nullptr, VT},
+                          {gbase, C, Gr, GT}};
+  load_heads(cp, T, bf16_ops);
+#pragma unroll
+  for (int u = 0; u < DR; u++) {
+    const float d = warp_sum(dyv[u][0] * yv[u][0] + dyv[u][1] * yv[u][1]);
+    if (lane == 0) Ds[warp + u * (THREADS / 32)] = d;
+  }
+  if (threadIdx.x < T_MAX) Ls[threadIdx.x] = lsev;
   __syncthreads();
 
   const int t0 = 4 * row_block(), j0 = 4 * col_block();
