@@ -435,6 +435,22 @@ static int launch_matmul(const MatmulDesc& d, cudaStream_t s, int* err) {
   p.epi = d.epi;
   p.splits = splits;
   p.err = err;
+  const long long tiles = (long long)ceil_div(d.M, tc::BM) * ceil_div(d.N, tc::BN);
+  if (splits == 1 && tiles > g_num_sms) {
+    // more tiles than SMs: one persistent CTA per SM walks them
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g_num_sms);
+    cfg.blockDim = dim3(tc::pers::THREADS);
+    cfg.dynamicSmemBytes = tc::pers::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = g_pdl ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, tc::gemm_tf32x3_persistent_kernel, ta, tb, p) != cudaSuccess) return -1;
+    return 1;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ceil_div(d.N, tc::BN), ceil_div(d.M, tc::BM), splits);
   cfg.blockDim = dim3(tc::THREADS);
@@ -816,6 +832,9 @@ static int set_kernel_attributes() {
                                          SORT_MAX * (int)sizeof(uint32_t));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc::gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc::gemm_tf32x3_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               tc::pers::SMEM_BYTES);
     if (e == cudaSuccess) e = query_cluster_limits();
     if (e == cudaSuccess) e = set_bf16_smem<256>();
     if (e == cudaSuccess) e = set_bf16_smem<128>();

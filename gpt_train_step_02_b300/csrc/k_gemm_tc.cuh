@@ -154,6 +154,12 @@ GPT2_DEV void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Pull a tensor map (a kernel parameter written by the host) into the
+// descriptor cache while the CTA sets up, ahead of its first TMA copy.
+GPT2_DEV void prefetch_tmap(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tm) : "memory");
+}
+
 GPT2_DEV void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
@@ -602,6 +608,244 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// ---- the persistent variant ---------------------------------------------------
+// For products with more 128 x 128 output tiles than SMs and no K split (the
+// LM head forward and its weight gradient): one CTA per SM walks the tiles
+// (stride gridDim.x), so a tile's TMEM set-up, first copies and epilogue
+// overlap the neighbouring tiles' main loops instead of being paid once per
+// tile.  The roles are those above plus four epilogue warps; the MMAs
+// alternate between two TMEM accumulators (columns 0..127 and 128..255), the
+// epilogue warps drain one while the other fills, and A's hi/lo stages sit in
+// columns 256..383.  Tiles are numbered with the operand that is reused
+// varying fastest: when there are fewer row tiles than column tiles,
+// consecutive tiles share a column block of B (read from HBM about once),
+// otherwise they share a row block of A.
+namespace pers {
+constexpr int EPI_WARPS = 4;
+constexpr int THREADS = 64 + SPLIT_THREADS + 32 * EPI_WARPS;
+constexpr int TMEM_COLS = 512;
+constexpr int TM_ACC = 0;    // accumulator b at columns b * BN
+constexpr int TM_A = 2 * BN;  // A stage c: hi at TM_A + 64c, lo at TM_A + 64c + 32
+static_assert(TM_A + COMP_STAGES * 2 * BK <= TMEM_COLS, "A stages must fit the TMEM allocation");
+constexpr int OFF_RAW_A = 0;
+constexpr int OFF_RAW_B = OFF_RAW_A + RAW_STAGES * TILE_BYTES;
+constexpr int OFF_HI_B = OFF_RAW_B + RAW_STAGES * TILE_BYTES;
+constexpr int OFF_LO_B = OFF_HI_B + COMP_STAGES * TILE_BYTES;
+constexpr int OFF_EPI = OFF_LO_B + COMP_STAGES * TILE_BYTES;
+constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_STAGE_FLOATS * 4;
+constexpr int NUM_BARS = 2 * RAW_STAGES + 2 * COMP_STAGES + 4 + 1;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
+
+GPT2_DEV void tile_coords(int tile, int tiles_m, int tiles_n, int& m0, int& n0) {
+  int tm, tn;
+  if (tiles_m <= tiles_n) {
+    tm = tile % tiles_m;
+    tn = tile / tiles_m;
+  } else {
+    tn = tile % tiles_n;
+    tm = tile / tiles_n;
+  }
+  m0 = tm * BM;
+  n0 = tn * BN;
+}
+}  // namespace pers
+
+__global__ void __launch_bounds__(pers::THREADS, 1)
+    gemm_tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                                  const __grid_constant__ Params p) {
+  using namespace pers;
+  pdl_launch_dependents();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pers::OFF_BAR);
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = bars + RAW_STAGES;
+  uint64_t* comp_full = bars + 2 * RAW_STAGES;
+  uint64_t* comp_empty = bars + 2 * RAW_STAGES + COMP_STAGES;
+  uint64_t* acc_full = bars + 2 * RAW_STAGES + 2 * COMP_STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;                            // [2]
+  uint64_t* mma_done = acc_full + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pers::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + pers::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
+  const int tiles = tiles_m * tiles_n;
+  const int nk = p.k_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RAW_STAGES; s++) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], SPLIT_WARPS);
+    }
+    for (int s = 0; s < COMP_STAGES; s++) {
+      mbar_init(&comp_full[s], SPLIT_WARPS);
+      mbar_init(&comp_empty[s], 1);
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(pers::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the first global-memory access comes after this
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        int m0, n0;
+        tile_coords(tile, tiles_m, tiles_n, m0, n0);
+        for (int kt = 0; kt < nk; kt++, it++) {
+          const int s = it % RAW_STAGES;
+          if (!mbar_wait(&raw_empty[s], ((it / RAW_STAGES) & 1) ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const int k = kt * BK;
+          mbar_expect_tx(&raw_full[s], 2 * TILE_BYTES);
+          uint8_t* ra = smem + pers::OFF_RAW_A + s * TILE_BYTES;
+          uint8_t* rb = smem + pers::OFF_RAW_B + s * TILE_BYTES;
+          if (p.a_kmajor) tma_load_2d(ra, &tmA, k, m0, &raw_full[s]);
+          else tma_load_2d(ra, &tmA, m0, k, &raw_full[s]);
+          if (p.b_kmajor) tma_load_2d(rb, &tmB, k, n0, &raw_full[s]);
+          else tma_load_2d(rb, &tmB, n0, k, &raw_full[s]);
+        }
+      }
+      if (!ok) {  // let the copies already in flight land before the CTA exits
+        for (int j = max(0, it - RAW_STAGES); j < it; j++) mbar_wait_drain(&raw_full[j % RAW_STAGES], (j / RAW_STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int it = 0, lt = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, lt++) {
+        const int buf = lt & 1;
+        if (!mbar_wait(&acc_empty[buf], ((lt >> 1) & 1) ^ 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(TM_ACC + buf * BN);
+        for (int kt = 0; kt < nk; kt++, it++) {
+          const int c = it % COMP_STAGES;
+          if (!mbar_wait(&comp_full[c], (it / COMP_STAGES) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ah = tmem + (uint32_t)(pers::TM_A + c * 2 * BK), al = ah + BK;
+          const uint32_t bh = smem_u32(smem + pers::OFF_HI_B + c * TILE_BYTES);
+          const uint32_t bl = smem_u32(smem + pers::OFF_LO_B + c * TILE_BYTES);
+#pragma unroll
+          for (int j = 0; j < BK / 8; j++) {
+            const uint64_t dbh = smem_desc_kmajor_sw128(bh + j * 32), dbl = smem_desc_kmajor_sw128(bl + j * 32);
+            mma_tf32_ta(d_tmem, ah + 8 * j, dbh, (kt > 0 || j > 0) ? 1u : 0u);
+            mma_tf32_ta(d_tmem, ah + 8 * j, dbl, 1u);
+            mma_tf32_ta(d_tmem, al + 8 * j, dbh, 1u);
+          }
+          mma_commit(&comp_empty[c]);  // frees the hi/lo stage once these MMAs have read it
+        }
+        if (ok) mma_commit(&acc_full[buf]);
+      }
+      // every MMA this thread issued has completed once mma_done fires
+      mma_commit(mma_done);
+      mbar_wait_drain(mma_done, 0);
+    }
+  } else if (warp < 2 + SPLIT_WARPS) {
+    // ---------------- splitters ----------------
+    const int t = threadIdx.x - 64;
+    const int a_quad = warp & 3, a_half = (warp - 2) >> 2;
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      for (int kt = 0; kt < nk; kt++, it++) {
+        const int s = it % RAW_STAGES, c = it % COMP_STAGES;
+        if (!__all_sync(0xffffffffu, mbar_wait(&raw_full[s], (it / RAW_STAGES) & 1, abort_flag, p.err) &&
+                                         mbar_wait(&comp_empty[c], ((it / COMP_STAGES) & 1) ^ 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();  // the MMAs that read this stage's TMEM columns have completed
+        const float* ra = reinterpret_cast<const float*>(smem + pers::OFF_RAW_A + s * TILE_BYTES);
+        const uint8_t* rb = smem + pers::OFF_RAW_B + s * TILE_BYTES;
+        float* hb = reinterpret_cast<float*>(smem + pers::OFF_HI_B + c * TILE_BYTES);
+        float* lb = reinterpret_cast<float*>(smem + pers::OFF_LO_B + c * TILE_BYTES);
+        const uint32_t t_hi = tmem + ((uint32_t)(a_quad * 32) << 16) + (uint32_t)(pers::TM_A + c * 2 * BK + 16 * a_half);
+        if (p.a_kmajor) split_a_kmajor_tmem(ra, t_hi, a_quad * 32 + lane, a_half);
+        else split_a_mnmajor_tmem(ra, t_hi, a_quad * 32 + lane, a_half);
+        if (p.b_kmajor)
+          split_kmajor(reinterpret_cast<const float4*>(rb), reinterpret_cast<float4*>(hb), reinterpret_cast<float4*>(lb), t);
+        else
+          split_mnmajor(reinterpret_cast<const float*>(rb), hb, lb, t);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&raw_empty[s]);
+          mbar_arrive(&comp_full[c]);
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    float* stage = reinterpret_cast<float*>(smem + pers::OFF_EPI) + (warp - 2 - SPLIT_WARPS) * EPI_STAGE_FLOATS;
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, lt++) {
+      int m0, n0;
+      tile_coords(tile, tiles_m, tiles_n, m0, n0);
+      const int buf = lt & 1;
+      // one decision per warp (tcgen05.ld is warp-collective)
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (lt >> 1) & 1, abort_flag, p.err))) break;
+      tc_fence_after();
+      const int i0 = m0 + q * 32;
+      const uint32_t tbase = tmem + (uint32_t)(TM_ACC + buf * BN) + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 32; cc++) {
+        float v[32];
+        tmem_ld32(tbase + (uint32_t)(cc * 32), v);
+        const int j0 = n0 + cc * 32;
+        if (j0 < p.N && i0 < p.M) {  // warp-uniform
+          warp32_stage(stage, v, lane);
+          warp32_epilogue(p.epi, stage, i0, j0, p.M, p.N, lane);
+        }
+      }
+      // the accumulator is in global memory now: hand it back to the MMAs
+      tc_fence_before();
+      mbar_arrive_warp(&acc_empty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(pers::TMEM_COLS) : "memory");
   }
 }
 

@@ -2,7 +2,9 @@
 oracle's matmul_forward / matmul_backward (the page «llm.c：Andrej Karpathy
 带你从零复现LLM», section «核心代码解读：train_gpt2.c», item 1).  Shapes cover
 ragged M, N and K (partial 128x128 tiles and partial 32-wide K tiles),
-split-K (small N with long K) and both operand layouts of each product."""
+split-K (small N with long K), products with more tiles than SMs (the
+persistent kernel, one CTA per SM walking the tiles) and both operand
+layouts of each product."""
 import numpy as np
 import pytest
 
@@ -20,7 +22,9 @@ SHAPES = [  # (N rows, IC, OC)
     (300, 96, 260),     # M spans 3 tiles with a tail
     (256, 768, 2304),   # 124M QKV at B*T=256: split-K
     (256, 3072, 768),   # 124M MLP output projection: split-K over 3072
-    (256, 768, 50304),  # LM head (tied wte), 393 column tiles
+    (256, 768, 50304),  # LM head (tied wte), 393 column tiles: forward and weight gradient persistent
+    (1000, 200, 2500),  # forward with 160 tiles (> 148 SMs, persistent), ragged M, N and K
+    (300, 1100, 2100),  # weight gradient with 153 tiles (persistent, both operands MN-major), ragged K = 300
 ]
 
 
