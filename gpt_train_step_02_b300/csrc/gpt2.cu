@@ -41,6 +41,8 @@
 
 // split-K workspace (fp32 partial tiles), 32 MB
 #define SPLITK_WS_FLOATS ((long long)8 << 20)
+// events of the backward's side stream (two per side launch, ~50 launches per backward)
+#define SIDE_EVENTS 256
 // split-K arrival counters: K is split only when there are fewer than 148 tiles
 #define TILE_CTRS 256
 // op workspaces start with [error word, 256 B][tile counters, 1 KB]
@@ -217,6 +219,15 @@ struct gpt2_t {
   int gB, gT;
   long long g_launches;
   int capturing;
+  // Side stream for the backward's column-sum finishes (bias, layernorm gain
+  // and shift gradients): nothing but AdamW reads their outputs, so they run
+  // beside the main stream instead of between two dependent matmuls.  sev is
+  // a ring of events; rd_* is the event after which the side stream no
+  // longer reads that buffer (-1: no pending reader), side_last the last
+  // side event (the join before the update).
+  cudaStream_t side;
+  cudaEvent_t sev[SIDE_EVENTS];
+  int sev_next, side_last, rd_scratch, rd_dfch, rd_dqkv;
   // kernel timer: event pairs around every launch of one kernel class
   int timer_kind;
   cudaEvent_t* tev;
@@ -612,12 +623,56 @@ static void mm_forward(gpt2_t* m, float* out, uint16_t* outbf, Opnd x, Opnd W, c
 
 // dx = dy W (times gelu'(pre) when pre != NULL); colsum: optional 32-row
 // column partial sums of dx (bf16 matmuls), leading dimension IC
+// ---- the backward's side stream -------------------------------------------
+// side_fork: the side stream continues after everything enqueued so far on
+// the main stream; returns the event side_done records at the end of the side
+// work.  side_wait: the main stream waits for a pending side reader of a
+// buffer before overwriting it.  side_join: the main stream waits for all side
+// work.  The kernel timer brackets launches on the main stream only, so under
+// it (and on a handle without a side stream) everything stays on the main
+// stream.
+static bool side_on(const gpt2_t* m) { return m->side && m->timer_kind == TK_NONE; }
+
+static int side_fork(gpt2_t* m, cudaStream_t* st) {
+  if (!side_on(m)) {
+    *st = m->stream;
+    return -1;
+  }
+  const int f = m->sev_next, d = (m->sev_next + 1) % SIDE_EVENTS;
+  m->sev_next = (m->sev_next + 2) % SIDE_EVENTS;
+  CCHECK(m, cudaEventRecord(m->sev[f], m->stream));
+  CCHECK(m, cudaStreamWaitEvent(m->side, m->sev[f], 0));
+  *st = m->side;
+  return d;
+}
+
+static int side_done(gpt2_t* m, int d, int* reader) {
+  if (d < 0) return GPT2_OK;
+  CCHECK(m, cudaEventRecord(m->sev[d], m->side));
+  m->side_last = d;
+  if (reader) *reader = d;
+  return GPT2_OK;
+}
+
+static int side_wait(gpt2_t* m, int* reader) {
+  if (*reader >= 0) CCHECK(m, cudaStreamWaitEvent(m->stream, m->sev[*reader], 0));
+  *reader = -1;
+  return GPT2_OK;
+}
+
+static int side_join(gpt2_t* m) {
+  if (m->side_last >= 0) CCHECK(m, cudaStreamWaitEvent(m->stream, m->sev[m->side_last], 0));
+  m->side_last = m->rd_scratch = m->rd_dfch = m->rd_dqkv = -1;
+  return GPT2_OK;
+}
+
 static void mm_dx(gpt2_t* m, float* dx, uint16_t* dxbf, Opnd dy, Opnd W, int N, int IC, int OC, const float* pre,
                   float* colsum = nullptr) {
   MatmulDesc d = {N,    IC,   OC,   dy.f, OC, 1, W.f, IC, 0,
                   epi_args(dx, IC, pre ? EPI_DGELU : EPI_STORE, nullptr, pre, IC, nullptr, 0, dxbf, IC), dy.h, W.h};
   d.epi.colsum = colsum;
   d.epi.ldcs = IC;
+  if (colsum == m->scratch) side_wait(m, &m->rd_scratch);
   matmul(m, d);
 }
 
@@ -633,13 +688,19 @@ static void mm_dw(gpt2_t* m, float* dW, Opnd dy, Opnd x, int N, int IC, int OC) 
 // Up to BIAS_DIRECT_ROWS rows the finishing kernel sums dy's rows itself
 // (32 warps, each striding over the rows): one launch instead of two.
 #define BIAS_DIRECT_ROWS 2048
-static void bias_grad(gpt2_t* m, float* db, const float* dy, int N, int OC) {
+// The direct form runs on the side stream; *reader records when it has
+// finished reading dy.
+static void bias_grad(gpt2_t* m, float* db, const float* dy, int N, int OC, int* reader) {
   if (N <= BIAS_DIRECT_ROWS) {
-    launch_k(col_finish_kernel, ceil_div(OC, 32), COLF_WARPS * 32, 0, m->stream, db, db, db, OC, dy, N, OC,
+    cudaStream_t st;
+    const int d = side_fork(m, &st);
+    launch_k(col_finish_kernel, ceil_div(OC, 32), COLF_WARPS * 32, 0, st, db, db, db, OC, dy, N, OC,
              m->grad_accumulate);
+    side_done(m, d, reader);
     m->launches++;
     return;
   }
+  side_wait(m, &m->rd_scratch);
   const int rows = BIAS_MIN_ROWS, chunks = ceil_div(N, rows);
   launch_k(col_partial_kernel, dim3(ceil_div(OC, 256), chunks), 256, 0, m->stream, dy, N, OC, OC, rows, m->scratch);
   launch_k(col_finish_kernel, ceil_div(OC, 32), COLF_WARPS * 32, 0, m->stream, db, db, db, OC, m->scratch, chunks,
@@ -651,8 +712,11 @@ static void bias_grad(gpt2_t* m, float* db, const float* dy, int N, int OC) {
 // attention epilogue left in m->scratch
 static_assert(BIAS_MIN_ROWS == 32, "the scratch is sized in 32-row column-sum blocks");
 static void bias_finish(gpt2_t* m, float* db, int nrows, int OC) {
-  launch_k(col_finish_kernel, ceil_div(OC, 32), COLF_WARPS * 32, 0, m->stream, db, db, db, OC, m->scratch, nrows, OC,
+  cudaStream_t st;
+  const int d = side_fork(m, &st);
+  launch_k(col_finish_kernel, ceil_div(OC, 32), COLF_WARPS * 32, 0, st, db, db, db, OC, m->scratch, nrows, OC,
            m->grad_accumulate);
+  side_done(m, d, &m->rd_scratch);
   m->launches++;
 }
 
@@ -689,6 +753,7 @@ static void ln_backward(gpt2_t* m, float* dx, uint16_t* dxbf, float* dw, float* 
   const bool rms = m->cfg.llama != 0;        // RMSNorm: dw only (no shift, no linear biases)
   const int nout = rms ? 1 : (dxsum ? 3 : 2);
   timer_begin(m, TK_LAYERNORM, (16.0 * C + 8.0) * N);
+  side_wait(m, &m->rd_scratch);  // the partials below overwrite the scratch
   const size_t smem = (size_t)LNB_WARPS * nout * C * sizeof(float);
   if (rms) {
     auto k = ln_pick(C, layernorm_bwd_kernel<1, true>, layernorm_bwd_kernel<2, true>, layernorm_bwd_kernel<4, true>,
@@ -700,8 +765,11 @@ static void ln_backward(gpt2_t* m, float* dx, uint16_t* dxbf, float* dw, float* 
     launch_k(k, nb, LNB_WARPS * 32, smem, m->stream, dx, dxbf, m->scratch, dy, x, w, mean, rstd, N, C, dxsum ? 1 : 0);
   }
   // dw[c] (+)= sum_b partial[b][c], db[c] (+)= sum_b partial[b][C + c], dxsum[c] (+)= ...[2C + c]
-  launch_k(col_finish_kernel, ceil_div(nout * C, 32), COLF_WARPS * 32, 0, m->stream, dw, db, dxsum, C, m->scratch, nb,
+  cudaStream_t st;
+  const int d = side_fork(m, &st);
+  launch_k(col_finish_kernel, ceil_div(nout * C, 32), COLF_WARPS * 32, 0, st, dw, db, dxsum, C, m->scratch, nb,
            nout * C, m->grad_accumulate);
+  side_done(m, d, &m->rd_scratch);
   timer_end(m, TK_LAYERNORM);
   m->launches += 2;
 }
@@ -811,6 +879,8 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
 static void attn_backward(gpt2_t* m, const float* qkv, const uint16_t* qkv_bf, const float* atty, const float* lse,
                           int B, int T, int bf, bool fuse_bias) {
   int C = m->cfg.channels, NH = m->cfg.num_heads, hs = C / NH;
+  side_wait(m, &m->rd_dqkv);
+  if (fuse_bias) side_wait(m, &m->rd_scratch);
   timer_begin(m, TK_ATTN_BWD, 8.0 * (double)B * NH * T * (T + 1) / 2.0 * hs);
   int n = launch_attn_bwd(fuse_bias ? nullptr : m->dqkv, m->dqkv_bf, m->attD, m->datty, m->datty_bf, qkv, qkv_bf, atty,
                           lse, B, T, C, NH, bf, m->err, m->stream, fuse_bias ? m->scratch : nullptr);
@@ -1029,12 +1099,13 @@ static int enqueue_backward(gpt2_t* m) {
     // (its bias gradient came with the layernorm backward that produced dres)
     // x gelu'(fch).  bf16: only the bf16 copy of dfch is stored; the MLP input
     // bias gradient comes from column sums taken in the same epilogue
+    side_wait(m, &m->rd_dfch);  // dfch is overwritten here
     mm_dx(m, bf && (fuse_fcb || ll) ? nullptr : m->dfch, m->dfch_bf, dres, wparam(m, P_FCPROJW, l * 4 * CC), N, 4 * C, C,
           a.fch, fuse_fcb ? m->scratch : nullptr);
     // MLP input projection: fch = ln2 fcw^T + fcb
     mm_dw(m, G[P_FCW] + l * 4 * CC, dfch, {a.ln2, a.ln2_bf}, N, C, 4 * C);
     if (fuse_fcb) bias_finish(m, G[P_FCB] + (size_t)l * 4 * C, ceil_div(N, 32), 4 * C);
-    else if (!ll) bias_grad(m, G[P_FCB] + (size_t)l * 4 * C, m->dfch, N, 4 * C);
+    else if (!ll) bias_grad(m, G[P_FCB] + (size_t)l * 4 * C, m->dfch, N, 4 * C, &m->rd_dfch);
     mm_dx(m, m->dln, nullptr, dfch, wparam(m, P_FCW, l * 4 * CC), N, C, 4 * C, nullptr);
     ln_backward(m, m->dres, m->dres_bf, G[P_LN2W] + (size_t)l * C, G[P_LN2B] + (size_t)l * C,
                 gbias(P_ATTPROJB, (size_t)l * C), m->dln, a.res2, P[P_LN2W] + (size_t)l * C, a.ln2_mean, a.ln2_rstd, N);
@@ -1051,7 +1122,7 @@ static int enqueue_backward(gpt2_t* m) {
     // qkv projection: qkv = ln1 qkvw^T + qkvb
     mm_dw(m, G[P_QKVW] + l * 3 * CC, dqkv, {a.ln1, a.ln1_bf}, N, C, 3 * C);
     if (fuse_qkvb) bias_finish(m, G[P_QKVB] + (size_t)l * 3 * C, N / tca::BQ, 3 * C);
-    else if (!ll) bias_grad(m, G[P_QKVB] + (size_t)l * 3 * C, m->dqkv, N, 3 * C);
+    else if (!ll) bias_grad(m, G[P_QKVB] + (size_t)l * 3 * C, m->dqkv, N, 3 * C, &m->rd_dqkv);
     mm_dx(m, m->dln, nullptr, dqkv, wparam(m, P_QKVW, l * 3 * CC), N, C, 3 * C, nullptr);
     // below layer 0 this dres is the previous layer's MLP output gradient
     ln_backward(m, m->dres, m->dres_bf, G[P_LN1W] + (size_t)l * C, G[P_LN1B] + (size_t)l * C,
@@ -1070,7 +1141,7 @@ static int enqueue_backward(gpt2_t* m) {
     m->launches++;
   }
   KCHECK(m);
-  return GPT2_OK;
+  return side_join(m);  // every gradient is complete on the main stream from here on
 }
 
 // AdamW hyper-parameters live in device memory so that a captured step can
@@ -1207,10 +1278,17 @@ EXPORT int gpt2_build(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, int m
   carve(m);
   int rc;
   cudaError_t e;
+  m->side_last = m->rd_scratch = m->rd_dfch = m->rd_dqkv = -1;
   if (set_kernel_attributes() != GPT2_OK) {
     rc = GPT2_ERR_CUDA;
     goto fail;
   }
+  if ((e = cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking)) != cudaSuccess) {
+    m->side = nullptr;
+    goto cuda_fail;
+  }
+  for (int i = 0; i < SIDE_EVENTS; i++)
+    if ((e = cudaEventCreateWithFlags(&m->sev[i], cudaEventDisableTiming)) != cudaSuccess) goto cuda_fail;
   if ((e = cudaMemsetAsync(m->grads, 0, m->np * sizeof(float), m->stream)) != cudaSuccess) goto cuda_fail;
   if ((e = cudaMemsetAsync(m->m, 0, m->np * sizeof(float), m->stream)) != cudaSuccess) goto cuda_fail;
   if ((e = cudaMemsetAsync(m->v, 0, m->np * sizeof(float), m->stream)) != cudaSuccess) goto cuda_fail;
@@ -1243,6 +1321,9 @@ cuda_fail:
   cudaGetLastError();
   rc = GPT2_ERR_CUDA;
 fail:
+  for (int i = 0; i < SIDE_EVENTS; i++)
+    if (m->sev[i]) cudaEventDestroy(m->sev[i]);
+  if (m->side) cudaStreamDestroy(m->side);
   if (m->own_arena) cudaFree(m->arena);
   free(m);
   return rc;
@@ -1251,6 +1332,12 @@ fail:
 EXPORT int gpt2_free(gpt2_t* m) {
   if (!m) return GPT2_ERR_ARG;
   cudaStreamSynchronize(m->stream);
+  if (m->side) {
+    cudaStreamSynchronize(m->side);
+    cudaStreamDestroy(m->side);
+  }
+  for (int i = 0; i < SIDE_EVENTS; i++)
+    if (m->sev[i]) cudaEventDestroy(m->sev[i]);
   if (m->gexec) cudaGraphExecDestroy(m->gexec);
   if (m->tev) {
     for (int i = 0; i < 2 * m->tcap; i++) cudaEventDestroy(m->tev[i]);
