@@ -228,6 +228,11 @@ struct gpt2_t {
   cudaStream_t side;
   cudaEvent_t sev[SIDE_EVENTS];
   int sev_next, side_last, rd_scratch, rd_dfch, rd_dqkv;
+  // A second, lower-priority side stream for the per-layer weight-gradient
+  // matmuls of the fp32 path (their split-K reduction needs no workspace, so
+  // they can run beside the input-gradient chain); wd_* as rd_* for it.
+  cudaStream_t side_w;
+  int side_w_last, wd_dres, wd_dfch, wd_dqkv;
   // kernel timer: event pairs around every launch of one kernel class
   int timer_kind;
   cudaEvent_t* tev;
@@ -579,14 +584,15 @@ static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int
   return 1;
 }
 
-static int matmul(gpt2_t* m, const MatmulDesc& d) {
+static int matmul(gpt2_t* m, const MatmulDesc& d, cudaStream_t st = nullptr) {
   if (d.epi.colsum && m->cfg.gemm_precision != GPT2_PREC_BF16) {  // fused column sums: bf16 kernel only
     m->poisoned = GPT2_ERR_CUDA;
     return GPT2_ERR_CUDA;
   }
+  if (!st) st = m->stream;
   timer_begin(m, TK_GEMM, 2.0 * d.M * (double)d.N * d.K);
-  int n = m->cfg.gemm_precision == GPT2_PREC_BF16 ? launch_matmul_bf16(d, m->splitk, m->tilectr, m->err, m->stream)
-                                                  : launch_matmul(d, m->stream, m->err);
+  int n = m->cfg.gemm_precision == GPT2_PREC_BF16 ? launch_matmul_bf16(d, m->splitk, m->tilectr, m->err, st)
+                                                  : launch_matmul(d, st, m->err);
   timer_end(m, TK_GEMM);
   if (n < 0) {
     m->poisoned = GPT2_ERR_CUDA;
@@ -662,7 +668,9 @@ static int side_wait(gpt2_t* m, int* reader) {
 
 static int side_join(gpt2_t* m) {
   if (m->side_last >= 0) CCHECK(m, cudaStreamWaitEvent(m->stream, m->sev[m->side_last], 0));
+  if (m->side_w_last >= 0) CCHECK(m, cudaStreamWaitEvent(m->stream, m->sev[m->side_w_last], 0));
   m->side_last = m->rd_scratch = m->rd_dfch = m->rd_dqkv = -1;
+  m->side_w_last = m->wd_dres = m->wd_dfch = m->wd_dqkv = -1;
   return GPT2_OK;
 }
 
@@ -681,6 +689,32 @@ static void mm_dw(gpt2_t* m, float* dW, Opnd dy, Opnd x, int N, int IC, int OC) 
   MatmulDesc d = {OC, IC, N, dy.f, OC, 0, x.f, IC, 0, epi_args(dW, IC, m->grad_accumulate ? EPI_ACCUM : EPI_STORE),
                   dy.h, x.h};
   matmul(m, d);
+}
+
+// The same on the weight-gradient side stream (fp32 path): it starts after
+// everything enqueued so far on the main stream, and *reader records when it
+// has finished reading dy (x is a per-layer activation nothing overwrites
+// during the backward).
+static void mm_dw_side(gpt2_t* m, float* dW, Opnd dy, Opnd x, int N, int IC, int OC, int* reader) {
+  if (!side_on(m) || !m->side_w || m->cfg.gemm_precision != GPT2_PREC_FP32) {
+    mm_dw(m, dW, dy, x, N, IC, OC);
+    return;
+  }
+  const int f = m->sev_next, d = (m->sev_next + 1) % SIDE_EVENTS;
+  m->sev_next = (m->sev_next + 2) % SIDE_EVENTS;
+  if (cudaEventRecord(m->sev[f], m->stream) != cudaSuccess || cudaStreamWaitEvent(m->side_w, m->sev[f], 0) != cudaSuccess) {
+    m->poisoned = GPT2_ERR_CUDA;
+    return;
+  }
+  MatmulDesc md = {OC, IC, N, dy.f, OC, 0, x.f, IC, 0, epi_args(dW, IC, m->grad_accumulate ? EPI_ACCUM : EPI_STORE),
+                   dy.h, x.h};
+  matmul(m, md, m->side_w);
+  if (cudaEventRecord(m->sev[d], m->side_w) != cudaSuccess) {
+    m->poisoned = GPT2_ERR_CUDA;
+    return;
+  }
+  m->side_w_last = d;
+  *reader = d;
 }
 
 // db += column sums of dy (N, OC): chunks of BIAS_MIN_ROWS rows summed by
@@ -754,6 +788,7 @@ static void ln_backward(gpt2_t* m, float* dx, uint16_t* dxbf, float* dw, float* 
   const int nout = rms ? 1 : (dxsum ? 3 : 2);
   timer_begin(m, TK_LAYERNORM, (16.0 * C + 8.0) * N);
   side_wait(m, &m->rd_scratch);  // the partials below overwrite the scratch
+  if (dx == m->dres) side_wait(m, &m->wd_dres);
   const size_t smem = (size_t)LNB_WARPS * nout * C * sizeof(float);
   if (rms) {
     auto k = ln_pick(C, layernorm_bwd_kernel<1, true>, layernorm_bwd_kernel<2, true>, layernorm_bwd_kernel<4, true>,
@@ -880,6 +915,7 @@ static void attn_backward(gpt2_t* m, const float* qkv, const uint16_t* qkv_bf, c
                           int B, int T, int bf, bool fuse_bias) {
   int C = m->cfg.channels, NH = m->cfg.num_heads, hs = C / NH;
   side_wait(m, &m->rd_dqkv);
+  side_wait(m, &m->wd_dqkv);
   if (fuse_bias) side_wait(m, &m->rd_scratch);
   timer_begin(m, TK_ATTN_BWD, 8.0 * (double)B * NH * T * (T + 1) / 2.0 * hs);
   int n = launch_attn_bwd(fuse_bias ? nullptr : m->dqkv, m->dqkv_bf, m->attD, m->datty, m->datty_bf, qkv, qkv_bf, atty,
@@ -1095,22 +1131,23 @@ static int enqueue_backward(gpt2_t* m) {
   for (int l = L - 1; l >= 0; l--) {
     LayerActs a = layer_acts(m, l);
     // MLP output projection: res3 = res2 + fchg fcprojw^T + fcprojb
-    mm_dw(m, G[P_FCPROJW] + l * 4 * CC, dres, {a.fchg, a.fchg_bf}, N, 4 * C, C);
+    mm_dw_side(m, G[P_FCPROJW] + l * 4 * CC, dres, {a.fchg, a.fchg_bf}, N, 4 * C, C, &m->wd_dres);
     // (its bias gradient came with the layernorm backward that produced dres)
     // x gelu'(fch).  bf16: only the bf16 copy of dfch is stored; the MLP input
     // bias gradient comes from column sums taken in the same epilogue
     side_wait(m, &m->rd_dfch);  // dfch is overwritten here
+    side_wait(m, &m->wd_dfch);
     mm_dx(m, bf && (fuse_fcb || ll) ? nullptr : m->dfch, m->dfch_bf, dres, wparam(m, P_FCPROJW, l * 4 * CC), N, 4 * C, C,
           a.fch, fuse_fcb ? m->scratch : nullptr);
     // MLP input projection: fch = ln2 fcw^T + fcb
-    mm_dw(m, G[P_FCW] + l * 4 * CC, dfch, {a.ln2, a.ln2_bf}, N, C, 4 * C);
+    mm_dw_side(m, G[P_FCW] + l * 4 * CC, dfch, {a.ln2, a.ln2_bf}, N, C, 4 * C, &m->wd_dfch);
     if (fuse_fcb) bias_finish(m, G[P_FCB] + (size_t)l * 4 * C, ceil_div(N, 32), 4 * C);
     else if (!ll) bias_grad(m, G[P_FCB] + (size_t)l * 4 * C, m->dfch, N, 4 * C, &m->rd_dfch);
     mm_dx(m, m->dln, nullptr, dfch, wparam(m, P_FCW, l * 4 * CC), N, C, 4 * C, nullptr);
     ln_backward(m, m->dres, m->dres_bf, G[P_LN2W] + (size_t)l * C, G[P_LN2B] + (size_t)l * C,
                 gbias(P_ATTPROJB, (size_t)l * C), m->dln, a.res2, P[P_LN2W] + (size_t)l * C, a.ln2_mean, a.ln2_rstd, N);
     // attention output projection: res2 = x + atty attprojw^T + attprojb
-    mm_dw(m, G[P_ATTPROJW] + l * CC, dres, {a.atty, a.atty_bf}, N, C, C);
+    mm_dw_side(m, G[P_ATTPROJW] + l * CC, dres, {a.atty, a.atty_bf}, N, C, C, &m->wd_dres);
     mm_dx(m, m->datty, m->datty_bf, dres, wparam(m, P_ATTPROJW, l * CC), N, C, C, nullptr);
     // attention
     attn_backward(m, a.qkv, a.qkv_bf, a.atty, a.lse, B, T, bf, fuse_qkvb);
@@ -1120,7 +1157,7 @@ static int enqueue_backward(gpt2_t* m) {
       m->launches++;
     }
     // qkv projection: qkv = ln1 qkvw^T + qkvb
-    mm_dw(m, G[P_QKVW] + l * 3 * CC, dqkv, {a.ln1, a.ln1_bf}, N, C, 3 * C);
+    mm_dw_side(m, G[P_QKVW] + l * 3 * CC, dqkv, {a.ln1, a.ln1_bf}, N, C, 3 * C, &m->wd_dqkv);
     if (fuse_qkvb) bias_finish(m, G[P_QKVB] + (size_t)l * 3 * C, N / tca::BQ, 3 * C);
     else if (!ll) bias_grad(m, G[P_QKVB] + (size_t)l * 3 * C, m->dqkv, N, 3 * C, &m->rd_dqkv);
     mm_dx(m, m->dln, nullptr, dqkv, wparam(m, P_QKVW, l * 3 * CC), N, C, 3 * C, nullptr);
@@ -1279,6 +1316,7 @@ EXPORT int gpt2_build(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, int m
   int rc;
   cudaError_t e;
   m->side_last = m->rd_scratch = m->rd_dfch = m->rd_dqkv = -1;
+  m->side_w_last = m->wd_dres = m->wd_dfch = m->wd_dqkv = -1;
   if (set_kernel_attributes() != GPT2_OK) {
     rc = GPT2_ERR_CUDA;
     goto fail;
@@ -1286,6 +1324,14 @@ EXPORT int gpt2_build(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, int m
   if ((e = cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking)) != cudaSuccess) {
     m->side = nullptr;
     goto cuda_fail;
+  }
+  {
+    int lo = 0, hi = 0;  // the weight-gradient side stream at the lowest priority
+    if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) goto cuda_fail;
+    if ((e = cudaStreamCreateWithPriority(&m->side_w, cudaStreamNonBlocking, lo)) != cudaSuccess) {
+      m->side_w = nullptr;
+      goto cuda_fail;
+    }
   }
   for (int i = 0; i < SIDE_EVENTS; i++)
     if ((e = cudaEventCreateWithFlags(&m->sev[i], cudaEventDisableTiming)) != cudaSuccess) goto cuda_fail;
@@ -1324,6 +1370,7 @@ fail:
   for (int i = 0; i < SIDE_EVENTS; i++)
     if (m->sev[i]) cudaEventDestroy(m->sev[i]);
   if (m->side) cudaStreamDestroy(m->side);
+  if (m->side_w) cudaStreamDestroy(m->side_w);
   if (m->own_arena) cudaFree(m->arena);
   free(m);
   return rc;
@@ -1335,6 +1382,10 @@ EXPORT int gpt2_free(gpt2_t* m) {
   if (m->side) {
     cudaStreamSynchronize(m->side);
     cudaStreamDestroy(m->side);
+  }
+  if (m->side_w) {
+    cudaStreamSynchronize(m->side_w);
+    cudaStreamDestroy(m->side_w);
   }
   for (int i = 0; i < SIDE_EVENTS; i++)
     if (m->sev[i]) cudaEventDestroy(m->sev[i]);
