@@ -368,7 +368,7 @@ def roofline_for(kind, k, peaks, w):
             "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(kind, w), "peak_source": peaks["source"]}
 
 
-TRAFFIC_KERNELS = {"gemm": ("gemm_tf32x3_kernel", "gemm_bf16_kernel")}
+TRAFFIC_KERNELS = {"gemm": ("gemm_tf32x3", "gemm_bf16")}
 BYTE_UNITS = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
 
 
