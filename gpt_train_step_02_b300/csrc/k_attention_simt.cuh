@@ -1,6 +1,6 @@
 // k_attention_simt.cuh -- causal multi-head attention on CUDA cores, for the
-// shapes the tensor-core kernels do not take (head size other than 64, T not
-// a multiple of 128, fp32 operands).
+// shapes neither the tensor-core kernels (bf16, head size 64, T a multiple of
+// 128) nor the one-CTA-per-head kernels (head size 64, T <= 64) take.
 //
 // Forward (online softmax over keys t2 <= t, scale 1/sqrt(hs)) writes the
 // output y (B,T,C) and the log-sum-exp lse (B,NH,T) of each score row.

@@ -14,8 +14,11 @@
  *  - Every function returns a status code (GPT2_OK = 0, negative = error,
  *    positive = warning) unless stated otherwise; gpt2_status_string() names it.
  *  - A handle orders all of its device work on the CUDA stream given to
- *    gpt2_build().  Calls on one handle must not run concurrently (the handle
- *    is not thread-safe); different handles are independent.
+ *    gpt2_build().  Inside a backward pass some gradient work runs on two
+ *    streams the handle owns; they fork from that stream and are joined back
+ *    into it before the call returns, so to the caller every call is ordered
+ *    on the given stream.  Calls on one handle must not run concurrently (the
+ *    handle is not thread-safe); different handles are independent.
  *  - Host pointers are read or written during the call only and never kept.
  *  - After GPT2_ERR_DEVICE_TIMEOUT or GPT2_ERR_CUDA the handle is poisoned:
  *    every later call except gpt2_free() returns the same error.
