@@ -64,6 +64,8 @@ struct Plan {
   size_t encoded, ln1, ln1_mean, ln1_rstd, qkv, atty, lse, res2, ln2, ln2_mean, ln2_rstd, fch, fchg, res3;
   size_t lnf, lnf_mean, lnf_rstd, logits, dlogits, losses, loss;
   size_t dres, dln, datty, dqkv, dfch, attD, scratch, sorted, tokens, targets, err, hparams, splitk, tilectr;
+  // the split-K workspace and tile counters of the weight-gradient side stream (bf16 matmuls only)
+  size_t splitk_w, tilectr_w;
   // bf16 operand copies (bf16 matmuls only)
   size_t ln1_bf, qkv_bf, atty_bf, ln2_bf, fchg_bf, lnf_bf, dlogits_bf, dres_bf, dfch_bf, dqkv_bf, datty_bf;
   // Llama-style variant: (cos, sin) per position and pair, and a zero vector
@@ -161,6 +163,9 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->hparams = take(16 * F);
   p->splitk = take(SPLITK_WS_FLOATS * F);
   p->tilectr = take(TILE_CTRS * sizeof(int));
+  const bool bf16_gemm = c->gemm_precision == GPT2_PREC_BF16;
+  p->splitk_w = take(bf16_gemm ? SPLITK_WS_FLOATS * F : 0);
+  p->tilectr_w = take(bf16_gemm ? TILE_CTRS * sizeof(int) : 0);
   const size_t H = c->gemm_precision == GPT2_PREC_BF16 ? 2 : 0;  // bytes per bf16 copy element (0: none)
   p->ln1_bf = take(L * BT * C * H);
   p->qkv_bf = take(L * BT * 3 * C * H);
@@ -199,9 +204,9 @@ struct gpt2_t {
   float *encoded, *ln1, *ln1_mean, *ln1_rstd, *qkv, *atty, *lse, *res2, *ln2, *ln2_mean, *ln2_rstd, *fch, *fchg,
       *res3;
   float *lnf, *lnf_mean, *lnf_rstd, *logits, *dlogits, *losses, *loss;
-  float *dres, *dln, *datty, *dqkv, *dfch, *attD, *scratch, *splitk;
+  float *dres, *dln, *datty, *dqkv, *dfch, *attD, *scratch, *splitk, *splitk_w;
   uint32_t* sorted;
-  int *tokens, *targets, *err, *tilectr;
+  int *tokens, *targets, *err, *tilectr, *tilectr_w;
   uint16_t *ln1_bf, *qkv_bf, *atty_bf, *ln2_bf, *fchg_bf, *lnf_bf, *dlogits_bf, *dres_bf, *dfch_bf, *dqkv_bf,
       *datty_bf;
   float* hparams;
@@ -229,8 +234,9 @@ struct gpt2_t {
   cudaEvent_t sev[SIDE_EVENTS];
   int sev_next, side_last, rd_scratch, rd_dfch, rd_dqkv;
   // A second, lower-priority side stream for the per-layer weight-gradient
-  // matmuls of the fp32 path (their split-K reduction needs no workspace, so
-  // they can run beside the input-gradient chain); wd_* as rd_* for it.
+  // matmuls, beside the input-gradient chain (bf16 matmuls there use their own
+  // split-K workspace and tile counters, splitk_w and tilectr_w); wd_* as
+  // rd_* for it.
   cudaStream_t side_w;
   int side_w_last, wd_dres, wd_dfch, wd_dqkv;
   // kernel timer: event pairs around every launch of one kernel class
@@ -591,7 +597,10 @@ static int matmul(gpt2_t* m, const MatmulDesc& d, cudaStream_t st = nullptr) {
   }
   if (!st) st = m->stream;
   timer_begin(m, TK_GEMM, 2.0 * d.M * (double)d.N * d.K);
-  int n = m->cfg.gemm_precision == GPT2_PREC_BF16 ? launch_matmul_bf16(d, m->splitk, m->tilectr, m->err, st)
+  // the weight-gradient side stream has a split-K workspace of its own
+  const bool on_w = st == m->side_w && m->splitk_w;
+  int n = m->cfg.gemm_precision == GPT2_PREC_BF16
+              ? launch_matmul_bf16(d, on_w ? m->splitk_w : m->splitk, on_w ? m->tilectr_w : m->tilectr, m->err, st)
                                                   : launch_matmul(d, st, m->err);
   timer_end(m, TK_GEMM);
   if (n < 0) {
@@ -691,12 +700,13 @@ static void mm_dw(gpt2_t* m, float* dW, Opnd dy, Opnd x, int N, int IC, int OC) 
   matmul(m, d);
 }
 
-// The same on the weight-gradient side stream (fp32 path): it starts after
+// The same on the weight-gradient side stream: it starts after
 // everything enqueued so far on the main stream, and *reader records when it
 // has finished reading dy (x is a per-layer activation nothing overwrites
 // during the backward).
 static void mm_dw_side(gpt2_t* m, float* dW, Opnd dy, Opnd x, int N, int IC, int OC, int* reader) {
-  if (!side_on(m) || !m->side_w || m->cfg.gemm_precision != GPT2_PREC_FP32) {
+  // fp32 reduces K splits inside a cluster; bf16 needs the side stream's own workspace
+  if (!side_on(m) || !m->side_w || (m->cfg.gemm_precision != GPT2_PREC_FP32 && !m->splitk_w)) {
     mm_dw(m, dW, dy, x, N, IC, OC);
     return;
   }
@@ -1246,6 +1256,8 @@ static void carve(gpt2_t* m) {
   CARVE(lnf); CARVE(lnf_mean); CARVE(lnf_rstd); CARVE(logits); CARVE(dlogits); CARVE(losses); CARVE(loss);
   CARVE(dres); CARVE(dln); CARVE(datty); CARVE(dqkv); CARVE(dfch); CARVE(attD); CARVE(scratch); CARVE(sorted);
   CARVE(tokens); CARVE(targets); CARVE(err); CARVE(hparams); CARVE(splitk); CARVE(tilectr);
+  CARVE(splitk_w); CARVE(tilectr_w);
+  if (m->cfg.gemm_precision != GPT2_PREC_BF16) m->splitk_w = nullptr, m->tilectr_w = nullptr;
 #undef CARVE
 #define CARVE_BF(f) m->f = m->params_bf ? (uint16_t*)(a + p.f) : nullptr
   CARVE_BF(ln1_bf); CARVE_BF(qkv_bf); CARVE_BF(atty_bf); CARVE_BF(ln2_bf); CARVE_BF(fchg_bf); CARVE_BF(lnf_bf); CARVE_BF(dlogits_bf);
@@ -1340,6 +1352,8 @@ EXPORT int gpt2_build(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, int m
   if ((e = cudaMemsetAsync(m->v, 0, m->np * sizeof(float), m->stream)) != cudaSuccess) goto cuda_fail;
   if ((e = cudaMemsetAsync(m->err, 0, sizeof(int), m->stream)) != cudaSuccess) goto cuda_fail;
   if ((e = cudaMemsetAsync(m->tilectr, 0, TILE_CTRS * sizeof(int), m->stream)) != cudaSuccess) goto cuda_fail;
+  if (m->tilectr_w && (e = cudaMemsetAsync(m->tilectr_w, 0, TILE_CTRS * sizeof(int), m->stream)) != cudaSuccess)
+    goto cuda_fail;
   if ((rc = init_params(m, seed)) != GPT2_OK) goto fail;
   if ((rc = refresh_bf16(m)) != GPT2_OK) goto fail;
   if (m->cfg.llama) {
