@@ -649,14 +649,17 @@ static void mm_forward(gpt2_t* m, float* out, uint16_t* outbf, Opnd x, Opnd W, c
 static bool side_on(const gpt2_t* m) { return m->side && m->timer_kind == TK_NONE; }
 
 static int side_fork(gpt2_t* m, cudaStream_t* st) {
-  if (!side_on(m)) {
-    *st = m->stream;
-    return -1;
-  }
+  *st = m->stream;  // also the stream of the failure path below
+  if (!side_on(m)) return -1;
   const int f = m->sev_next, d = (m->sev_next + 1) % SIDE_EVENTS;
   m->sev_next = (m->sev_next + 2) % SIDE_EVENTS;
-  CCHECK(m, cudaEventRecord(m->sev[f], m->stream));
-  CCHECK(m, cudaStreamWaitEvent(m->side, m->sev[f], 0));
+  cudaError_t e = cudaEventRecord(m->sev[f], m->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(m->side, m->sev[f], 0);
+  if (e != cudaSuccess) {
+    fprintf(stderr, "gpt2b300: %s (side stream fork)\n", cudaGetErrorString(e));
+    m->poisoned = GPT2_ERR_CUDA;
+    return -1;
+  }
   *st = m->side;
   return d;
 }
