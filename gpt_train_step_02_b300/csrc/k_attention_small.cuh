@@ -4,8 +4,9 @@
 // The same arithmetic as the streaming CUDA-core kernels (scale 1/sqrt(hs),
 // keys t2 <= t; lse = max + log sum exp; backward through P = exp(S - lse),
 // D_t = dy_t . y_t, dS = P (dP - D_t)), organised for short sequences: one CTA
-// of 256 threads owns a whole (batch, head), loads its q, k, v (and dy, y)
-// into shared memory once, and forms every product as a register-tiled
+// of 256 threads owns a whole (batch, head), loads its q, k, v (and dy) into
+// shared memory once -- every global load of the CTA, y's for D included,
+// issued before the first store -- and forms every product as a register-tiled
 // 64 x 64 matrix product -- each thread a 4 x 4 output block, one 16-byte
 // shared-memory load of each operand per 16 FMAs -- instead of one scalar
 // load per FMA.  Blocks that lie wholly above the causal diagonal are
