@@ -384,14 +384,37 @@ struct MatmulDesc {
 // once per process after the kernel's shared-memory limit is set.  A cluster
 // sits inside one GPC, so the SMs of a GPC beyond a multiple of s stay idle:
 // at s = 3 a 148-SM B300 holds 45 clusters (135 CTAs), not 49.
-static int g_num_sms = 148;
-static int g_max_clusters[9] = {0, 148, 0, 0, 0, 0, 0, 0, 0};
+// Per device: the SM count and the clusters of s CTAs of the fp32 matmul that
+// the GPU holds at once (s = 1..8), queried with that device current once its
+// kernels' shared-memory limits are set (kernel attributes apply per device);
+// attr: 0 not yet set, 1 set, -1 failed.
+#define MAX_DEVICES 64
+struct DevInfo {
+  int num_sms;
+  int max_clusters[9];
+  int attr;
+};
+static DevInfo g_dev[MAX_DEVICES];
+static std::mutex g_dev_mu;
 
-static cudaError_t query_cluster_limits() {
+static int current_device() {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-  g_max_clusters[1] = g_num_sms;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+    cudaGetLastError();
+    return -1;
+  }
+  return dev;
+}
+
+// the current device's entry (device 0's when the lookup fails)
+static const DevInfo& dev_info() {
+  const int d = current_device();
+  return g_dev[d < 0 ? 0 : d];
+}
+
+static cudaError_t query_cluster_limits(int dev, DevInfo* di) {
+  cudaError_t e = cudaDeviceGetAttribute(&di->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  di->max_clusters[1] = di->num_sms;
   for (int s = 2; s <= 8 && e == cudaSuccess; s++) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, s);
@@ -406,7 +429,7 @@ static cudaError_t query_cluster_limits() {
     cfg.numAttrs = 1;
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, tc::gemm_tf32x3_kernel, &cfg);
-    g_max_clusters[s] = n;
+    di->max_clusters[s] = n;
   }
   return e;
 }
@@ -419,16 +442,19 @@ static cudaError_t query_cluster_limits() {
 // as many clusters as the GPU holds at once.  A tile beyond the first wave
 // doubles the time, so s is chosen against the cluster limit above.
 static int choose_splits(int M, int N, int K) {
+  const DevInfo& di = dev_info();
+  const int num_sms = di.num_sms;
+  const int* max_clusters = di.max_clusters;
   const long long tiles = (long long)ceil_div(M, tc::BM) * ceil_div(N, tc::BN);
   const int kt = ceil_div(K, tc::BK);
   if (kt < 4) return 1;
   const int FILL = 4, REDUCE = 3;
   int best = 1;
-  long long best_cost = ((tiles + g_num_sms - 1) / g_num_sms) * (long long)(kt + FILL);
+  long long best_cost = ((tiles + num_sms - 1) / num_sms) * (long long)(kt + FILL);
   for (int s = 2; s <= 8 && s <= kt / 2; s++) {
     const int per = ceil_div(kt, s);
-    if (ceil_div(kt, per) != s || g_max_clusters[s] <= 0) continue;  // same split as a smaller s, or no fit
-    const long long waves = (tiles + g_max_clusters[s] - 1) / g_max_clusters[s];
+    if (ceil_div(kt, per) != s || max_clusters[s] <= 0) continue;  // same split as a smaller s, or no fit
+    const long long waves = (tiles + max_clusters[s] - 1) / max_clusters[s];
     const long long cost = waves * (per + FILL) + REDUCE;
     if (cost < best_cost) {
       best_cost = cost;
@@ -458,10 +484,11 @@ static int launch_matmul(const MatmulDesc& d, cudaStream_t s, int* err) {
   p.splits = splits;
   p.err = err;
   const long long tiles = (long long)ceil_div(d.M, tc::BM) * ceil_div(d.N, tc::BN);
-  if (splits == 1 && tiles > g_num_sms) {
+  const int num_sms = dev_info().num_sms;
+  if (splits == 1 && tiles > num_sms) {
     // more tiles than SMs: one persistent CTA per SM walks them
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(g_num_sms);
+    cfg.gridDim = dim3(num_sms);
     cfg.blockDim = dim3(tc::pers::THREADS);
     cfg.dynamicSmemBytes = tc::pers::SMEM_BYTES;
     cfg.stream = s;
@@ -941,12 +968,16 @@ static void attn_backward(gpt2_t* m, const float* qkv, const uint16_t* qkv_bf, c
   m->launches += n;
 }
 
-// Dynamic shared memory limits of the large-smem kernels, set once per process.
-static std::once_flag g_attr_once;
-static int g_attr_status = GPT2_ERR_CUDA;
-
+// Dynamic shared memory limits of the large-smem kernels.  They apply per
+// device, so they are set once for each device the library is used on, with
+// that device current.
 static int set_kernel_attributes() {
-  std::call_once(g_attr_once, [] {
+  const int dev = current_device();
+  if (dev < 0) return GPT2_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DevInfo* di = &g_dev[dev];
+  if (di->attr) return di->attr > 0 ? GPT2_OK : GPT2_ERR_CUDA;
+  {
     cudaError_t e = cudaFuncSetAttribute(sort_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SORT_MAX * (int)sizeof(uint32_t));
     if (e == cudaSuccess)
@@ -954,7 +985,7 @@ static int set_kernel_attributes() {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tc::gemm_tf32x3_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                tc::pers::SMEM_BYTES);
-    if (e == cudaSuccess) e = query_cluster_limits();
+    if (e == cudaSuccess) e = query_cluster_limits(dev, di);
     if (e == cudaSuccess) e = set_bf16_smem<256>();
     if (e == cudaSuccess) e = set_bf16_smem<128>();
     if (e == cudaSuccess)
@@ -998,13 +1029,14 @@ static int set_kernel_attributes() {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_bwd_dkv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_bwd_dkv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv);
     if (e != cudaSuccess) {
-      fprintf(stderr, "gpt2b300: cudaFuncSetAttribute failed: %s\n", cudaGetErrorString(e));
+      fprintf(stderr, "gpt2b300: cudaFuncSetAttribute failed on device %d: %s\n", dev, cudaGetErrorString(e));
       cudaGetLastError();
+      di->attr = -1;
     } else {
-      g_attr_status = GPT2_OK;
+      di->attr = 1;
     }
-  });
-  return g_attr_status;
+  }
+  return di->attr > 0 ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------------------
@@ -1814,8 +1846,12 @@ static int op_backward(float* dx, float* dW, float* dbias, const float* dy, cons
   MatmulDesc ddw = {OC, IC, N, dy, OC, 0, x, IC, 0, epi_args(dW, IC, EPI_ACCUM), w.dybf, w.xbf};
   if ((rc = op_matmul(ddw, precision, w, s))) return rc;
   if (dbias) {
-    int chunks = ceil_div(N, 64);
-    launch_k(col_partial_kernel, dim3(ceil_div(OC, 256), chunks), 256, 0, s, dy, N, OC, OC, 64, w.bias_partial);
+    // 64-row chunks, doubled while the chunks would exceed the grid's y limit:
+    // never more partial rows than ceil(N/64), which the scratch is sized for
+    int rows = 64;
+    while (ceil_div(N, rows) > 65535) rows *= 2;
+    const int chunks = ceil_div(N, rows);
+    launch_k(col_partial_kernel, dim3(ceil_div(OC, 256), chunks), 256, 0, s, dy, N, OC, OC, rows, w.bias_partial);
     launch_k(col_finish_kernel, ceil_div(OC, 32), COLF_WARPS * 32, 0, s, dbias, dbias, dbias, OC, w.bias_partial,
              chunks, OC, 1);
     if (cudaGetLastError() != cudaSuccess) return GPT2_ERR_CUDA;
@@ -1895,14 +1931,14 @@ EXPORT int gpt2op_attention_backward(float* dqkv, const float* dy, const float* 
 // ---------------------------------------------------------------------------
 // matmul backward with library-owned scratch (no allocation by anyone)
 // ---------------------------------------------------------------------------
-// The scratch of gpt2op_matmul_backward (error word, column-sum partials of
-// the bias gradient, split-K partials) is taken from one fixed array in the
-// library's device memory.  Every GPU that loads the library holds it until
-// the process exits.  Layout: [error word, 256 B][split-K tile counters]
-// [column-sum partials, NOALLOC_BIAS_FLOATS][split-K partials, the rest].
-#define NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
-#define NOALLOC_BIAS_FLOATS ((long long)1 << 20)
-#define NOALLOC_SPLITK_OFFSET ((size_t)OP_HDR_BYTES + (size_t)NOALLOC_BIAS_FLOATS * sizeof(float))
+// The scratch of gpt2op_matmul_backward (error word, split-K tile counters,
+// column-sum partials of the bias gradient) is taken from one fixed array in
+// the library's device memory.  Every GPU that loads the library holds it
+// until the process exits.  Layout: [error word, 256 B][tile counters]
+// [column-sum partials, NOALLOC_BIAS_FLOATS floats].  The fp32 matmul reduces
+// its K splits inside a thread-block cluster, so it needs no split-K partials.
+#define NOALLOC_BIAS_FLOATS ((long long)1 << 21)
+#define NOALLOC_SCRATCH_BYTES ((size_t)OP_HDR_BYTES + (size_t)NOALLOC_BIAS_FLOATS * sizeof(float))
 #define NOALLOC_MAX_DEVICES 64
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
@@ -1955,7 +1991,7 @@ EXPORT int gpt2op_matmul_backward_noalloc(float* dx, float* dW, float* dbias, co
   w.err = (int*)base;
   w.tile_ctr = (int*)((char*)base + 256);
   w.bias_partial = (float*)((char*)base + OP_HDR_BYTES);
-  w.splitk = (float*)((char*)base + NOALLOC_SPLITK_OFFSET);
-  w.splitk_floats = (long long)((NOALLOC_SCRATCH_BYTES - NOALLOC_SPLITK_OFFSET) / sizeof(float));
+  w.splitk = nullptr;  // read only by the bf16 kernel
+  w.splitk_floats = 0;
   return op_backward(dx, dW, dbias, dy, x, W, N, IC, OC, precision, w, s);
 }

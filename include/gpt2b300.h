@@ -270,20 +270,21 @@ int gpt2op_attention_backward(float* dqkv, const float* dy, const float* qkv, in
  * owns the device's memory, or a loop that must not call cudaMalloc because
  * it can synchronise the device.  It allocates nothing and calls no
  * allocating routine.
- * Scratch: one fixed 8 MiB array in the library's device memory, which every
- * GPU that loads the library holds until the process exits.  The first call
- * on a device looks up that array's device address (cudaGetSymbolAddress,
- * with the device current) and caches it; make that first call before any
- * stream capture.  Every call on a device shares the array, and each call
- * clears the part that must start at zero: calls that overlap on the GPU
- * (different streams, or different host threads on one device) race and
- * give wrong results.
- * Limit: with dbias != NULL, ceil(N/64) * OC must be <= 1,048,576 (for
- * example N = 16384 with OC <= 4096); larger shapes return GPT2_ERR_SHAPE
- * before any device work.  precision must be GPT2_PREC_FP32 (bf16 operand
- * copies would need scratch that grows with the inputs): GPT2_ERR_ARG
- * otherwise.  The split-K partials use the rest of the array,
- * which only lowers how far K is split.  Synchronises the stream. */
+ * Scratch: one fixed array of 8 MiB + 1280 bytes in the library's device
+ * memory, which every GPU that loads the library holds until the process
+ * exits.  The first call on a device looks up that array's device address
+ * (cudaGetSymbolAddress, with the device current) and caches it; make that
+ * first call before any stream capture.  Every call on a device shares the
+ * array, and each call clears the part that must start at zero: calls that
+ * overlap on the GPU (different streams, or different host threads on one
+ * device) race and give wrong results.
+ * Limit: with dbias != NULL, ceil(N/64) * OC must be <= 2,097,152 (for
+ * example N = 16384 with OC <= 8192): the column-sum partials of the bias
+ * gradient fill the array; larger shapes return GPT2_ERR_SHAPE before any
+ * device work.  precision must be GPT2_PREC_FP32 (bf16 operand copies would
+ * need scratch that grows with the inputs): GPT2_ERR_ARG otherwise.  The fp32
+ * products reduce their K splits on chip and use no other scratch.
+ * Synchronises the stream. */
 int gpt2op_matmul_backward_noalloc(float* dx, float* dW, float* dbias, const float* dy, const float* x,
                                    const float* W, int N, int IC, int OC, int precision, void* stream);
 
