@@ -149,8 +149,10 @@ def run_reference(args, w):
 
     m = ref.RefModel(ref.config_from(w), B_sample, w.T, np.float32)
     m.set_params(synth.init_params(w))
-    steps = min(args.steps, 8)
-    warm = min(args.warmup, 1)
+    # exactly the K timed and W warm-up steps asked for; each is one full
+    # oracle training step on a bounded sample of the batch
+    steps = args.steps
+    warm = args.warmup
     batches = [synth.batch(w, step=s) for s in range(warm + steps)]
     for s in range(warm):
         m.step(batches[s][0][:B_sample], batches[s][1][:B_sample], s + 1, lr=w.lr)
@@ -184,27 +186,47 @@ def workload_config(w, n_gpus):
             "l2": "no flush: each step streams params+grads+AdamW moments (> 126 MB L2)"}
 
 
-def run_ours(args, w):
+def measure_tf32_peak():
+    """Dense TF32 tensor-core rate of this GPU, measured the way the bf16 peak
+    is: torch.matmul (cuBLAS) of two 8192 x 8192 fp32 matrices with TF32
+    allowed, 2 * 8192^3 FLOPs, best of 10 (CUDA events).  TFLOP/s."""
     import torch
 
-    import gpt_train_step_02_b300 as g
+    n = 8192
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.randn(n, n, device="cuda")
+        b = torch.randn(n, n, device="cuda")
+        c = torch.empty(n, n, device="cuda")
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        best = float("inf")
+        for _ in range(10):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            torch.matmul(a, b, out=c)
+            e.record()
+            e.synchronize()
+            best = min(best, s.elapsed_time(e))
+        del a, b, c
+        torch.cuda.empty_cache()
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    return 2.0 * n ** 3 / (best * 1e-3) / 1e12
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
 
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+KERNEL_CLASSES = ("gemm", "adamw", "xent", "layernorm", "attn_fwd", "attn_bwd", "encoder")
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
 
-    K, W = args.steps, args.warmup
-    peaks = load_peaks()
+def measure(w, K, W, peaks, g, rank=0, world=1, barrier=lambda: None, reduce_max=lambda x: x, with_e2e=True):
+    """Times K graph-replayed training steps of workload w (after W warm-up
+    steps) with CUDA events on the handle's stream, samples the SM clocks
+    during them, times every kernel class with events around each launch,
+    and (with_e2e) times K steps through gpt2_train_step from pinned host
+    tokens with the loss read back every step."""
+    import torch
+
     model = g.GPT2(w, seed=synth.INIT_SEED)
     stream = model.stream
     # token batches for every step, resident in HBM before timing (distinct per rank)
@@ -224,6 +246,7 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     barrier()
 
+    local = torch.cuda.current_device()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.25)
@@ -238,20 +261,16 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms = start.elapsed_time(end)
+    ms = reduce_max(start.elapsed_time(end))
     launches_per_step = model.last_launch_count()
     last_loss = model.sync()
-    if dist is not None:
-        x = torch.tensor([ms], device="cuda")
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        ms = float(x.item())
     ms_per_step = ms / K
     value = world * w.BT * K / (ms / 1000.0)
 
     # per-kernel-class timing (events around each launch, direct launches)
     kinds = {}
     ksteps = min(K, 5)
-    for kind in ("gemm", "adamw", "xent", "layernorm", "attn_fwd", "attn_bwd"):
+    for kind in KERNEL_CLASSES:
         g.gpt2_kernel_timer(model.h, kind)
         for s in range(ksteps):
             t += 1
@@ -265,25 +284,85 @@ def run_ours(args, w):
     # every timed class against its own bound (the dominant one is `roofline`)
     rooflines = {kd: roofline_for(kd, kinds[kd], peaks, w) for kd in kinds if kinds[kd]["launches_per_step"] > 0}
 
-    # end to end: pinned host tokens, H2D every step, loss read back every step
-    pin_in = torch.from_numpy(host_in).pin_memory().numpy()
-    pin_tg = torch.from_numpy(host_tg).pin_memory().numpy()
-    for s in range(min(W, 3)):
-        t += 1
-        model.train_step(pin_in[s], pin_tg[s], t, lr=w.lr)
-    barrier()
-    t0 = time.perf_counter()
-    for s in range(K):
-        t += 1
-        model.train_step(pin_in[W + s], pin_tg[W + s], t, lr=w.lr)
-    e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        x = torch.tensor([e2e_s], device="cuda")
+    e2e = None
+    if with_e2e:
+        # end to end: pinned host tokens, H2D every step, loss read back every step
+        pin_in = torch.from_numpy(host_in).pin_memory().numpy()
+        pin_tg = torch.from_numpy(host_tg).pin_memory().numpy()
+        for s in range(min(W, 3)):
+            t += 1
+            model.train_step(pin_in[s], pin_tg[s], t, lr=w.lr)
+        barrier()
+        t0 = time.perf_counter()
+        for s in range(K):
+            t += 1
+            model.train_step(pin_in[W + s], pin_tg[W + s], t, lr=w.lr)
+        e2e_s = reduce_max(time.perf_counter() - t0)
+        barrier()
+        e2e = {"value": world * w.BT * K / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 2 * w.BT * 4,
+               "d2h_bytes_per_step": 4, "api": "gpt2_train_step (host tokens, loss returned every step)"}
+    model.close()
+    del d_in, d_tg
+    torch.cuda.empty_cache()
+    f_tok = flops_per_token(w)
+    return {
+        "value": value, "ms_per_step": ms_per_step, "launches_per_step": launches_per_step, "clocks": clk,
+        "roofline": roof, "rooflines": rooflines, "kernels": kinds, "e2e": e2e, "last_loss": last_loss,
+        "mfu": {"vs_bf16_dense_measured": value * f_tok / (peaks["bf16_tflops"] * 1e12 * world),
+                "vs_bf16_dense_sustained_measured": (value * f_tok / (peaks["bf16_tflops_sustained"] * 1e12 * world)
+                                                     if peaks.get("bf16_tflops_sustained") else None),
+                "vs_tf32_dense_measured": value * f_tok / (peaks["tf32_tflops"] * 1e12 * world),
+                "flops_per_token": f_tok},
+    }
+
+
+# the T = 1024 bf16 workloads, timed after the headline in a default single-GPU run
+EXTRA_WORKLOADS = ("gpt2_124m_B16_T1024_bf16", "gpt2_350m_B8_T1024_bf16", "gpt2_774m_B4_T1024_bf16")
+
+
+def run_ours(args, w):
+    import torch
+
+    import gpt_train_step_02_b300 as g
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def reduce_max(v):
+        if dist is None:
+            return v
+        x = torch.tensor([v], device="cuda", dtype=torch.float64)
         dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        e2e_s = float(x.item())
-    barrier()
-    e2e = {"value": world * w.BT * K / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 2 * w.BT * 4,
-           "d2h_bytes_per_step": 4, "api": "gpt2_train_step (host tokens, loss returned every step)"}
+        return float(x.item())
+
+    peaks = load_peaks()
+    peaks["tf32_tflops"] = measure_tf32_peak()
+    peaks["tf32_source"] = "measured in this run: torch.matmul fp32 8192^3 with TF32 allowed, best of 10"
+    res = measure(w, args.steps, args.warmup, peaks, g, rank, world, barrier, reduce_max)
+    extra = {}
+    if world == 1 and not args.no_extra:
+        for name in EXTRA_WORKLOADS:
+            if name == w.name:
+                continue
+            xw = synth.WORKLOADS[name]
+            r = measure(xw, args.extra_steps, 3, peaks, g, with_e2e=False)
+            extra[name] = {
+                "config": workload_config(xw, 1), "tokens_per_s": r["value"], "ms_per_step": r["ms_per_step"],
+                "steps": args.extra_steps, "warmup": 3, "mfu": r["mfu"], "roofline": r["roofline"],
+                "rooflines": r["rooflines"], "clocks": r["clocks"], "gpu_launches_per_step": r["launches_per_step"],
+                "last_loss": r["last_loss"],
+            }
 
     if rank != 0:
         if dist is not None:
@@ -295,22 +374,23 @@ def run_ours(args, w):
         cpu = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{steps} full oracle training step(s) of the same workload ({tok} tokens each), "
                          f"{el:.1f} s of CPU time"}
-    f_tok = flops_per_token(w)
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if w.precision == "fp32" else "bf16", "data": "synthetic",
+        "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if w.precision == "fp32" else "bf16", "data": "synthetic",
         "config": workload_config(w, world),
-        "mfu": {"vs_bf16_dense_measured": value * f_tok / (peaks["bf16_tflops"] * 1e12 * world),
-                "flops_per_token": f_tok},
-        "roofline": roof,
-        "rooflines": rooflines,
+        "mfu": res["mfu"],
+        "roofline": res["roofline"],
+        "rooflines": res["rooflines"],
         "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": int(launches_per_step * K),
-        "clocks": clk,
-        "kernels": kinds,
-        "last_loss": last_loss,
+        "e2e": res["e2e"],
+        "gpu_launches": int(res["launches_per_step"] * args.steps),
+        "clocks": res["clocks"],
+        "kernels": res["kernels"],
+        "last_loss": res["last_loss"],
+        "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "tf32_tflops", "source",
+                                        "tf32_source")},
+        "workloads_t1024": extra,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:
@@ -325,6 +405,7 @@ KERNEL_SOURCES = {
     "adamw": ["k_misc.cuh", "common.cuh"],
     "xent": ["k_xent.cuh", "common.cuh"],
     "layernorm": ["k_layernorm.cuh", "k_misc.cuh", "common.cuh"],
+    "encoder": ["k_misc.cuh", "common.cuh"],
 }
 
 
@@ -355,17 +436,25 @@ def roofline_for(kind, k, peaks, w):
     if kind == "gemm":
         achieved = k["work_per_launch"] / (k["avg_launch_ms"] * 1e-3) / 1e12
         if w.precision == "fp32":
-            # fp32 matmuls run as 3xTF32 on tcgen05 kind::tf32: dense TF32 peak =
-            # measured bf16 dense x the nominal TF32/bf16 ratio (1.1 / 2.25 PFLOP/s).
-            # Each product takes three MMAs, so 1/3 of this peak is the ceiling.
-            peak = peaks["bf16_tflops"] * 1.1 / 2.25
-            src = f"{peaks['source']} bf16 dense burst x nominal tf32/bf16 ratio 1.1/2.25; 3 MMAs per product"
-        else:
-            peak = peaks["bf16_tflops"]
-            src = f"{peaks['source']} bf16 dense burst"
-        return {"kernel": "matmul (all tcgen05 launches of the step)", "bound": "tensor", "achieved": achieved,
-                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(kind, w),
-                "peak_source": src}
+            # fp32 matmuls run as 3xTF32 on tcgen05 kind::tf32 against the
+            # measured dense TF32 rate (nominal ratio to bf16 when it is absent);
+            # each product takes three MMAs, so 1/3 of this peak is the ceiling
+            if peaks.get("tf32_tflops"):
+                peak, src = peaks["tf32_tflops"], peaks["tf32_source"]
+            else:
+                peak = peaks["bf16_tflops"] * 1.1 / 2.25
+                src = f"{peaks['source']} bf16 dense burst x nominal tf32/bf16 ratio 1.1/2.25"
+            return {"kernel": "matmul (all tcgen05 launches of the step)", "bound": "tensor", "achieved": achieved,
+                    "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                    "frac_of_3xtf32_ceiling": 3.0 * achieved / peak, "traffic": recorded_traffic(kind, w),
+                    "peak_source": src + "; 3 MMAs per product"}
+        peak = peaks["bf16_tflops"]
+        out = {"kernel": "matmul (all tcgen05 launches of the step)", "bound": "tensor", "achieved": achieved,
+               "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(kind, w),
+               "peak_source": f"{peaks['source']} bf16 dense burst"}
+        if peaks.get("bf16_tflops_sustained"):
+            out["frac_of_sustained"] = achieved / peaks["bf16_tflops_sustained"]
+        return out
     if kind in ("attn_fwd", "attn_bwd"):
         # the timer's work figure is FLOPs: 4 (forward) or 8 (backward) x B NH hs T(T+1)/2
         achieved = k["work_per_launch"] / (k["avg_launch_ms"] * 1e-3) / 1e12
@@ -384,7 +473,9 @@ def roofline_for(kind, k, peaks, w):
             "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(kind, w), "peak_source": peaks["source"]}
 
 
-TRAFFIC_KERNELS = {"gemm": ("gemm_tf32x3", "gemm_bf16")}
+# kernel-name fragments of each class in an ncu capture
+TRAFFIC_KERNELS = {"gemm": ("gemm_tf32x3", "gemm_bf16"), "adamw": ("adamw_kernel",), "xent": ("xent_fused_kernel",),
+                   "layernorm": ("layernorm_fwd_kernel", "layernorm_bwd_kernel"), "encoder": ("encoder_fwd_kernel",)}
 BYTE_UNITS = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
 
 
@@ -437,13 +528,17 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-extra", action="store_true", help="skip the T = 1024 bf16 workloads after the headline")
+    ap.add_argument("--extra-steps", type=int, default=10)
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
-                    help="store the DRAM bytes per matmul launch of an ncu capture of --workload and exit")
+                    help="store the DRAM bytes per launch of one kernel class (--traffic-kind) from an ncu capture "
+                         "of --workload and exit")
+    ap.add_argument("--traffic-kind", default="gemm", choices=sorted(TRAFFIC_KERNELS))
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     w = synth.WORKLOADS[args.workload]
     if args.record_traffic:
-        return record_traffic(args.record_traffic, w)
+        return record_traffic(args.record_traffic, w, args.traffic_kind)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

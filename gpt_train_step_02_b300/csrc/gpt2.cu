@@ -1096,9 +1096,11 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
     launch_k(validate_tokens_kernel, grid_for(N, 256, 64), 256, 0, s, d_in, d_tgt, N, V, m->err);
     m->launches++;
   }
+  // reads a wte row and a wpe row, writes one row per token
+  timer_begin(m, TK_ENCODER, (c.llama ? 8.0 : 12.0) * C * N);
   launch_k(encoder_fwd_kernel, grid_for((long long)N * C / 4, 256), 256, 0, s, m->encoded, d_in, m->P[P_WTE],
-           c.llama ? (const float*)nullptr : m->P[P_WPE],
-                                                                          N, T, C, V);
+           c.llama ? (const float*)nullptr : m->P[P_WPE], N, T, C, V);
+  timer_end(m, TK_ENCODER);
   m->launches++;
   // bf16 matmuls read only the bf16 copies: the fp32 layernorm outputs, the
   // fp32 GELU output and (with the tensor-core attention) the fp32 qkv are

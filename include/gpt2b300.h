@@ -180,7 +180,7 @@ int gpt2_train_step(gpt2_t* m, const int32_t* inputs, const int32_t* targets, in
 
 /* Kernel timer for roofline measurement.  kind selects one kernel class
  * (0 off, 1 matmuls, 2 AdamW, 3 fused cross-entropy, 4 attention forward,
- * 5 attention backward, 6 layernorm, 7 embedding); while it is on, every
+ * 5 attention backward, 6 layernorm, 7 embedding forward); while it is on, every
  * launch of that class is bracketed by CUDA events on the handle's stream
  * and steps run without graph replay.  gpt2_kernel_timer() resets the
  * totals; gpt2_kernel_timer_read() synchronises and returns the summed

@@ -46,6 +46,16 @@ def test_fp32_matmul_peak_is_tf32_from_bf16(bench):
     assert r["peak"] == pytest.approx(1800.0 * 1.1 / 2.25)
 
 
+def test_fp32_matmul_peak_is_the_measured_tf32_rate_when_present(bench):
+    w = synth.WORKLOADS["gpt2_124m_B4_T64_fp32"]
+    peaks = dict(PEAKS, tf32_tflops=900.0, tf32_source="test")
+    r = bench.roofline_for("gemm", k(2.0e12, 10.0), peaks, w)  # 200 TFLOP/s
+    assert r["peak"] == 900.0
+    assert r["frac"] == pytest.approx(200.0 / 900.0)
+    # three MMAs per 3xTF32 product: the ceiling is a third of the peak
+    assert r["frac_of_3xtf32_ceiling"] == pytest.approx(600.0 / 900.0)
+
+
 def test_bf16_matmul_peak_is_measured_bf16(bench):
     w = synth.WORKLOADS["gpt2_124m_B16_T1024_bf16"]
     r = bench.roofline_for("gemm", k(1.8e12, 1.0), PEAKS, w)
