@@ -25,6 +25,10 @@ SHAPES = [  # (N rows, IC, OC)
     (256, 768, 50304),  # LM head (tied wte), 393 column tiles: forward and weight gradient persistent
     (1000, 200, 2500),  # forward with 160 tiles (> 148 SMs, persistent), ragged M, N and K
     (300, 1100, 2100),  # weight gradient with 153 tiles (persistent, both operands MN-major), ragged K = 300
+    (256, 1024, 3072),  # 350M QKV (K = 1024)
+    (256, 4096, 1024),  # 350M MLP output projection (K = 4096)
+    (256, 1280, 3840),  # 774M QKV (K = 1280)
+    (256, 5120, 1280),  # 774M MLP output projection (K = 5120)
 ]
 
 
@@ -87,6 +91,10 @@ SHAPES_BF16 = [  # (N rows, IC, OC); IC and OC multiples of 8 (16-byte bf16 rows
     (256, 3072, 768),   # MLP output projection: K split for the weight gradient
     (1024, 768, 768),   # attention projection at B*T=1024: K-split weight gradient
     (256, 768, 50304),  # LM head (tied wte), 197 column tiles
+    (2048, 1024, 3072),  # 350M QKV at B*T = 2048 (K = 1024)
+    (1024, 4096, 1024),  # 350M MLP output projection (K = 4096)
+    (1024, 1280, 3840),  # 774M QKV (K = 1280)
+    (1024, 5120, 1280),  # 774M MLP output projection (K = 5120)
 ]
 
 
