@@ -16,6 +16,7 @@ enum GemmEpi : int {
   EPI_BIAS_GELU = 3,   // pre(i,j) = acc + bias[j]; C = gelu(pre) (MLP input projection)
   EPI_DGELU = 4,       // C = acc * gelu'(R(i,j))                (input gradient through GELU)
   EPI_ACCUM = 5,       // C += acc                               (weight gradient accumulation)
+  EPI_LOGITS = 6,      // C = acc, plus the row softmax statistics below (LM head with targets; bf16 kernel)
 };
 
 struct EpiArgs {
@@ -37,6 +38,15 @@ struct EpiArgs {
   // (vec4, N a multiple of 32); each block is written by exactly one warp.
   float* colsum;
   long long ldcs;
+  // EPI_LOGITS: for row i and column block b (the BN/2 columns one epilogue
+  // warp finishes), xstats[i * ldxs + b] = (m, s) with m the largest acc(i, j)
+  // and s the sum of exp(acc(i, j) - m) over the block's columns j < V
+  // (m = -inf, s = 0 when it has none); tlogit[i] = acc(i, targets[i]), in fp32.
+  const int* targets;
+  int V;
+  float2* xstats;
+  int ldxs;
+  float* tlogit;
 };
 
 // The epilogue functions take the kind as a template argument OP when the

@@ -68,6 +68,9 @@ struct Plan {
   size_t splitk_w, tilectr_w;
   // bf16 operand copies (bf16 matmuls only)
   size_t ln1_bf, qkv_bf, atty_bf, ln2_bf, fchg_bf, lnf_bf, dlogits_bf, dres_bf, dfch_bf, dqkv_bf, datty_bf;
+  // bf16 logits, their per-block softmax statistics and the targets' fp32
+  // logits (forward with targets, bf16 matmuls)
+  size_t logits_bf, xstats, tlogit;
   // Llama-style variant: (cos, sin) per position and pair, and a zero vector
   // standing in for the biases the variant does not have
   size_t rope, zero_bias;
@@ -106,6 +109,10 @@ static int config_ok(const gpt2_config* c) {
 static int shape_ok(const gpt2_config* c, int maxB, int maxT) {
   return maxB >= 1 && maxT >= 1 && maxT <= c->max_seq_len && (long long)maxB * maxT <= SORT_MAX;
 }
+
+// Softmax-statistics blocks per row of the bf16 logits: one per BN/2 columns
+// of the LM-head tiles, at most Vp/64 (BN = 128).
+static size_t xstats_pitch(size_t Vp) { return (Vp + 63) / 64; }
 
 static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   size_t off = 0;
@@ -178,6 +185,9 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->dfch_bf = take(BT * 4 * C * H);
   p->dqkv_bf = take(BT * 3 * C * H);
   p->datty_bf = take(BT * C * H);
+  p->logits_bf = take(BT * Vp * H);
+  p->xstats = take(H ? BT * xstats_pitch(Vp) * sizeof(float2) : 0);
+  p->tlogit = take(H ? BT * F : 0);
   const size_t ll = c->llama ? 1 : 0;
   p->rope = take(ll * (size_t)maxT * (C / NH / 2) * 2 * F);
   p->zero_bias = take(ll * 4 * C * F);
@@ -209,6 +219,10 @@ struct gpt2_t {
   int *tokens, *targets, *err, *tilectr, *tilectr_w;
   uint16_t *ln1_bf, *qkv_bf, *atty_bf, *ln2_bf, *fchg_bf, *lnf_bf, *dlogits_bf, *dres_bf, *dfch_bf, *dqkv_bf,
       *datty_bf;
+  uint16_t* logits_bf;  // the LM head's output of a bf16 forward with targets
+  float2* xstats;       // its per-block softmax statistics, xstats_pitch(Vp) per row
+  float* tlogit;        // the targets' fp32 logits
+  int logits_in_bf;     // 1: the last forward's logits are in logits_bf (bf16), 0: in logits (fp32)
   float* hparams;
   float2* rope;       // [maxT][hs/2] (cos, sin) of t * 10000^(-2i/hs) (Llama-style variant)
   float* zero_bias;   // 4C zeros: the bias operand of the variant's linear layers
@@ -561,6 +575,7 @@ static void launch_bf16_kernel(const CUtensorMap& ta, const CUtensorMap& tb, con
     case EPI_BIAS_GELU: launch_k(tcb::gemm_bf16_kernel<BN, EPI_BIAS_GELU>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
     case EPI_DGELU: launch_k(tcb::gemm_bf16_kernel<BN, EPI_DGELU>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
     case EPI_ACCUM: launch_k(tcb::gemm_bf16_kernel<BN, EPI_ACCUM>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
+    case EPI_LOGITS: launch_k(tcb::gemm_bf16_kernel<BN, EPI_LOGITS>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
     default: launch_k(tcb::gemm_bf16_kernel<BN, EPI_STORE>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
   }
 }
@@ -576,7 +591,16 @@ static cudaError_t set_bf16_smem() {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_BIAS_GELU>, a, sm);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_DGELU>, a, sm);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_ACCUM>, a, sm);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_LOGITS>, a, sm);
   return e;
+}
+
+// Column width of the bf16 matmul's output tiles: 128 x 256 tiles when they
+// alone fill the SMs; otherwise 128 x 128 tiles, which halve the K splits (and
+// their partial-tile traffic) needed to fill them.
+static int bf16_tile_n(int M, int N) {
+  const long long tiles256 = (long long)ceil_div(M, tcb::BM) * ceil_div(N, 256);
+  return (N > 128 && tiles256 >= 148) ? 256 : 128;
 }
 
 // Launches the persistent bf16 tensor-core matmul.  Returns 1, or -1 on a
@@ -584,10 +608,7 @@ static cudaError_t set_bf16_smem() {
 static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int* err, cudaStream_t s,
                               long long ws_floats = SPLITK_WS_FLOATS) {
   if (!d.Abf || !d.Bbf) return -1;
-  // 128 x 256 tiles when they alone fill the SMs; otherwise 128 x 128 tiles,
-  // which halve the K splits (and their partial-tile traffic) needed to fill them
-  const long long tiles256 = (long long)ceil_div(d.M, tcb::BM) * ceil_div(d.N, 256);
-  const int BN = (d.N > 128 && tiles256 >= 148) ? 256 : 128;
+  const int BN = bf16_tile_n(d.M, d.N);
   CUtensorMap ta, tb;
   if (!make_bf16_map(&ta, d.Abf, d.a_kmajor, d.a_kmajor ? d.M : d.K, d.a_kmajor ? d.K : d.M, d.lda, tcb::BM))
     return -1;
@@ -599,7 +620,9 @@ static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int
   p.a_kmajor = d.a_kmajor;
   p.b_kmajor = d.b_kmajor;
   // column sums are taken in the warp epilogue, which a K split bypasses
-  p.splits = d.epi.colsum ? 1 : choose_splits_bf16(d.M, d.N, d.K, BN, ws_floats);
+  // (and so do the softmax statistics of the LM head)
+  p.splits = (d.epi.colsum || d.epi.epi == EPI_LOGITS) ? 1 : choose_splits_bf16(d.M, d.N, d.K, BN, ws_floats);
+  if (d.epi.epi == EPI_LOGITS && (!d.epi.vec4 || !d.epi.Cbf || d.epi.C)) return -1;
   if (d.epi.colsum && (!d.epi.vec4 || d.N % 32 || (d.epi.ldcs & 3) || ((uintptr_t)d.epi.colsum & 15))) return -1;
   p.k_tiles = ceil_div(d.K, tcb::BK);
   p.kt_per_split = ceil_div(p.k_tiles, p.splits);
@@ -645,6 +668,7 @@ static EpiArgs epi_args(float* C, long long ldc, int epi, const float* bias = nu
   e.C = C; e.ldc = ldc; e.bias = bias; e.R = R; e.ldr = ldr; e.pre = pre; e.ldpre = ldpre; e.epi = epi;
   e.Cbf = Cbf; e.ldcbf = ldcbf; e.fast = 0;
   e.colsum = nullptr; e.ldcs = 0;
+  e.targets = nullptr; e.V = 0; e.xstats = nullptr; e.ldxs = 0; e.tlogit = nullptr;
   uintptr_t addr = (uintptr_t)C | (uintptr_t)bias | (uintptr_t)R | (uintptr_t)pre | (uintptr_t)Cbf;
   e.vec4 = (addr & 15) == 0 && (ldc & 3) == 0 && (ldr & 3) == 0 && (ldpre & 3) == 0 && (ldcbf & 7) == 0;
   return e;
@@ -1132,12 +1156,39 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
   }
   LayerActs last = layer_acts(m, L - 1);
   ln_forward(m, bf ? nullptr : m->lnf, m->lnf_bf, m->lnf_mean, m->lnf_rstd, last.res3, m->P[P_LNFW], m->P[P_LNFB], N);
-  mm_forward(m, m->logits, nullptr, {m->lnf, m->lnf_bf}, wparam(m, P_WTE, 0), nullptr, N, C, Vp, EPI_STORE, nullptr,
-             nullptr);
-  if (d_tgt) {
+  // bf16 matmuls with targets: the LM head stores its logits in bf16 and
+  // leaves the rows' softmax statistics and the targets' fp32 logits, so the
+  // cross-entropy reads the logits once (bf16) instead of twice (fp32)
+  const bool xbf = bf && d_tgt;
+  if (xbf) {
+    const Opnd wte = wparam(m, P_WTE, 0);
+    MatmulDesc d = {N, Vp, C, m->lnf, C, 1, wte.f, C, 1,
+                    epi_args(nullptr, Vp, EPI_LOGITS, nullptr, nullptr, 0, nullptr, 0, m->logits_bf, Vp), m->lnf_bf,
+                    wte.h};
+    d.epi.targets = d_tgt;
+    d.epi.V = V;
+    d.epi.xstats = m->xstats;
+    d.epi.ldxs = (int)xstats_pitch(Vp);
+    d.epi.tlogit = m->tlogit;
+    matmul(m, d);
+  } else {
+    mm_forward(m, m->logits, nullptr, {m->lnf, m->lnf_bf}, wparam(m, P_WTE, 0), nullptr, N, C, Vp, EPI_STORE, nullptr,
+               nullptr);
+  }
+  m->logits_in_bf = xbf ? 1 : 0;
+  if (xbf) {
+    const int nblk = ceil_div(Vp, bf16_tile_n(N, Vp) / 2), ldxs = (int)xstats_pitch(Vp);
+    // reads the bf16 logits and the statistics, writes the bf16 dlogits
+    timer_begin(m, TK_XENT, (double)N * (4.0 * Vp + 8.0 * nblk + 8.0));
+    launch_k(xent_bf16_kernel, N, XENT_BF_THREADS, 0, s, m->dlogits_bf, m->losses, (const uint16_t*)m->logits_bf,
+             (const float2*)m->xstats, nblk, ldxs, (const float*)m->tlogit, d_tgt, V, Vp, 1.0f / (float)N);
+    timer_end(m, TK_XENT);
+    launch_k(mean_kernel, 1, 1024, 0, s, m->losses, N, m->loss);
+    m->launches += 2;
+  } else if (d_tgt) {
     timer_begin(m, TK_XENT, 8.0 * (double)N * Vp);
-    launch_k(xent_fused_kernel, N, XENT_THREADS, 0, s, bf ? nullptr : m->dlogits, m->dlogits_bf, m->losses, m->logits,
-             d_tgt, V, Vp, 1.0f / (float)N);
+    launch_k(xent_fused_kernel, N, XENT_THREADS, 0, s, m->dlogits, (uint16_t*)nullptr, m->losses, m->logits, d_tgt, V,
+             Vp, 1.0f / (float)N);
     timer_end(m, TK_XENT);
     launch_k(mean_kernel, 1, 1024, 0, s, m->losses, N, m->loss);
     m->launches += 2;
@@ -1298,7 +1349,9 @@ static void carve(gpt2_t* m) {
 #undef CARVE
 #define CARVE_BF(f) m->f = m->params_bf ? (uint16_t*)(a + p.f) : nullptr
   CARVE_BF(ln1_bf); CARVE_BF(qkv_bf); CARVE_BF(atty_bf); CARVE_BF(ln2_bf); CARVE_BF(fchg_bf); CARVE_BF(lnf_bf); CARVE_BF(dlogits_bf);
-  CARVE_BF(dres_bf); CARVE_BF(dfch_bf); CARVE_BF(dqkv_bf); CARVE_BF(datty_bf);
+  CARVE_BF(dres_bf); CARVE_BF(dfch_bf); CARVE_BF(dqkv_bf); CARVE_BF(datty_bf); CARVE_BF(logits_bf);
+  m->xstats = m->params_bf ? (float2*)(a + p.xstats) : nullptr;
+  m->tlogit = m->params_bf ? (float*)(a + p.tlogit) : nullptr;
   m->rope = m->cfg.llama ? (float2*)(a + p.rope) : nullptr;
   m->zero_bias = m->cfg.llama ? (float*)(a + p.zero_bias) : nullptr;
 #undef CARVE_BF
@@ -1741,7 +1794,17 @@ EXPORT int gpt2_get_logits(gpt2_t* m, float* host, long long n) {
   if (!m->fwd_done) return GPT2_ERR_STATE;
   if (n != (long long)m->B * m->T * m->cfg.padded_vocab_size) return GPT2_ERR_ARG;
   CCHECK(m, cudaStreamSynchronize(m->stream));
-  CCHECK(m, cudaMemcpy(host, m->logits, n * sizeof(float), cudaMemcpyDeviceToHost));
+  if (!m->logits_in_bf) {
+    CCHECK(m, cudaMemcpy(host, m->logits, n * sizeof(float), cudaMemcpyDeviceToHost));
+    return GPT2_OK;
+  }
+  // bf16 logits: widened to fp32 exactly (a bf16 value is the top half of an fp32 one)
+  std::vector<uint16_t> tmp((size_t)n);
+  CCHECK(m, cudaMemcpy(tmp.data(), m->logits_bf, n * sizeof(uint16_t), cudaMemcpyDeviceToHost));
+  for (long long i = 0; i < n; i++) {
+    const uint32_t u = (uint32_t)tmp[(size_t)i] << 16;
+    memcpy(&host[i], &u, sizeof(float));
+  }
   return GPT2_OK;
 }
 

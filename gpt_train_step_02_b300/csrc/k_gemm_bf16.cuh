@@ -132,6 +132,29 @@ GPT2_DEV void unit_coords(const Params& p, int unit, int& m0, int& tn, int& z, i
   tn = tile / p.tiles_m;
 }
 
+// Softmax statistics of one row's 32 logits v (columns j0 .. j0+31) merged
+// into the running (m, s): m the largest logit of a real column (j < V), s the
+// sum of exp(logit - m) over them.  The target column's logit goes to *tl.
+GPT2_DEV void logits_row_stats(const float* v, int j0, int V, int tgt, float& m, float& s, float* tl) {
+  float cm = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 32; k++)
+    if (j0 + k < V) cm = fmaxf(cm, v[k]);
+  if (cm != -INFINITY) {
+    const float L2E = 1.4426950408889634f;
+    const float nm = fmaxf(m, cm), nmb = nm * L2E;
+    float cs = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; k++)
+      if (j0 + k < V) cs += ex2f_fast(fmaf(v[k], L2E, -nmb));
+    s = s * ex2f_fast((m - nm) * L2E) + cs;  // 0 * 0 while m = -inf
+    m = nm;
+  }
+#pragma unroll
+  for (int k = 0; k < 32; k++)
+    if (j0 + k == tgt) *tl = v[k];
+}
+
 // OP: the epilogue kind (a GemmEpi value), fixed per instantiation
 template <int BN, int OP>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -285,17 +308,28 @@ __global__ void __launch_bounds__(THREADS, 1)
       float* stage = reinterpret_cast<float*>(smem + CF::OFF_EPI) + (warp - 2) * EPI_STAGE_FLOATS;
       const int i0 = m0 + q * 32;  // this warp's 32 rows
       const uint32_t tbase = tmem + (uint32_t)(buf * BN) + ((uint32_t)(q * 32) << 16);
+      // EPI_LOGITS: row i0 + lane's running (max, sum of exp) over this warp's
+      // half of the tile, and its target column
+      float xm = -INFINITY, xs = 0.f;
+      int xt = -1;
+      if constexpr (OP == EPI_LOGITS) xt = (i0 + lane < p.M) ? p.epi.targets[i0 + lane] : -1;
 #pragma unroll 1
       for (int cc = half * (BN / 64); cc < (half + 1) * (BN / 64); cc++) {
         float v[32];
         tmem_ld32(tbase + (uint32_t)(cc * 32), v);
         const int j0 = n0 + cc * 32;
         if (j0 >= p.N || i0 >= p.M) continue;  // warp-uniform
+        if constexpr (OP == EPI_LOGITS) logits_row_stats(v, j0, p.epi.V, xt, xm, xs, p.epi.tlogit + i0 + lane);
         warp32_stage(stage, v, lane);
         if (split)
           warp32_store_raw(p.partial + (size_t)z * p.M * p.N, p.N, stage, i0, j0, p.M, p.N, lane);
         else
           warp32_epilogue<OP>(p.epi, stage, i0, j0, p.M, p.N, lane);
+      }
+      if constexpr (OP == EPI_LOGITS) {
+        const int blk = tn * 2 + half;  // this warp's BN/2 columns
+        if (i0 + lane < p.M && blk * (BN / 2) < p.N)
+          p.epi.xstats[(size_t)(i0 + lane) * p.epi.ldxs + blk] = make_float2(xm, xs);
       }
       // the accumulator is in registers / global memory now: hand it back
       tc_fence_before();

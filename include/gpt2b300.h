@@ -203,7 +203,10 @@ int gpt2_get_grads(gpt2_t* m, float* host, long long n);
 int gpt2_get_opt_state(gpt2_t* m, float* host_m, float* host_v, long long n);
 int gpt2_set_opt_state(gpt2_t* m, const float* host_m, const float* host_v, long long n);
 
-/* Logits of the last forward, (B, T, Vp) fp32, n = B*T*Vp elements. */
+/* Logits of the last forward, (B, T, Vp) fp32, n = B*T*Vp elements.  With
+ * GPT2_PREC_BF16 and targets, the forward keeps its logits in bf16 (the
+ * cross-entropy reads them once, with row statistics the LM-head matmul
+ * computed from the fp32 accumulators); they come back widened to fp32. */
 int gpt2_get_logits(gpt2_t* m, float* host, long long n);
 
 /* Number of kernels the last gpt2_forward/backward/update/train_step call

@@ -326,6 +326,42 @@ def test_bf16_tensor_core_gradients():
     o.close()
 
 
+def bf16_round(a):
+    """Round to the nearest bf16 (ties to even), returned as float32."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+@pytest.mark.parametrize("V,Vp,T,tokens", [(500, 512, 64, "uniform"), (50257, 50304, 128, "zipf")])
+def test_bf16_logits_row_statistics_and_loss(V, Vp, T, tokens):
+    """bf16 forward with targets: the LM-head matmul stores the logits in bf16
+    and the rows' softmax statistics and the targets' logits in fp32; the
+    cross-entropy merges the statistics.  The stored logits must be exactly
+    the bf16 rounding of the same matmul's fp32 logits (a forward without
+    targets), and the loss must equal the softmax cross-entropy of those fp32
+    logits over the V real columns, evaluated here in float64 (the
+    statistics are exact up to fp32 rounding).  The two vocabularies take
+    128- and 256-column tiles (64- and 128-column statistic blocks), with
+    padded columns in the last tile."""
+    w = synth.Workload(f"xent_bf16_V{V}", 1, 64, 4, V, Vp, T, 2, T, "bf16", tokens, 1)
+    p0 = perturbed(w)
+    inp, tgt = synth.batch(w)
+    m = gpu_model(w)
+    m.set_params(p0)
+    assert m.forward(inp, None) == -1.0
+    l32 = m.get_logits(w.B, w.T).astype(np.float32)
+    loss = m.forward(inp, tgt)
+    l16 = m.get_logits(w.B, w.T)
+    m.close()
+    assert np.array_equal(l16, bf16_round(l32))
+    x = l32.reshape(-1, Vp)[:, :V].astype(np.float64)
+    mx = x.max(axis=1, keepdims=True)
+    lse = mx[:, 0] + np.log(np.exp(x - mx).sum(axis=1))
+    ref_loss = float(np.mean(lse - x[np.arange(x.shape[0]), tgt.reshape(-1)]))
+    assert abs(loss - ref_loss) <= 2e-6 * abs(ref_loss), (loss, ref_loss)
+
+
 # ---------------------------------------------------------------------------
 # GPT-2 124M, fp32, B=4, T=64 (the workload of the pages' console log)
 # ---------------------------------------------------------------------------
