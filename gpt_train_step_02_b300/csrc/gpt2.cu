@@ -253,6 +253,13 @@ struct gpt2_t {
   // rd_* for it.
   cudaStream_t side_w;
   int side_w_last, wd_dres, wd_dfch, wd_dqkv;
+  // A third side stream, also at the lowest priority, for the AdamW updates of
+  // the fused step: layer l's parameters are updated there as soon as the
+  // backward has finished their gradients, beside the backward of the layers
+  // below (upd_layers: 1 while the fused step enqueues its backward;
+  // side_u_last: the event after its last update, -1 for none).
+  cudaStream_t side_u;
+  int upd_layers, side_u_last;
   // kernel timer: event pairs around every launch of one kernel class
   int timer_kind;
   cudaEvent_t* tev;
@@ -1201,6 +1208,8 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
   return GPT2_OK;
 }
 
+static int update_layer(gpt2_t* m, int l);
+
 static int enqueue_backward(gpt2_t* m) {
   const gpt2_config& c = m->cfg;
   int L = c.num_layers, C = c.channels, Vp = c.padded_vocab_size;
@@ -1263,6 +1272,11 @@ static int enqueue_backward(gpt2_t* m) {
     ln_backward(m, m->dres, m->dres_bf, G[P_LN1W] + (size_t)l * C, G[P_LN1B] + (size_t)l * C,
                 l > 0 ? gbias(P_FCPROJB, (size_t)(l - 1) * C) : nullptr, m->dln, a.x, P[P_LN1W] + (size_t)l * C,
                 a.ln1_mean, a.ln1_rstd, N);
+    // every gradient of layer l is complete once the work enqueued so far is
+    if (m->upd_layers) {
+      int rc = update_layer(m, l);
+      if (rc) return rc;
+    }
   }
   // embeddings
   size_t smem = 1;
@@ -1289,15 +1303,75 @@ static int write_hparams(gpt2_t* m, float lr, float b1, float b2, float eps, flo
   return GPT2_OK;
 }
 
-static int enqueue_update(gpt2_t* m) {
-  long long n4 = m->np / 4;
-  timer_begin(m, TK_ADAMW, 28.0 * (double)m->np + (m->params_bf ? 2.0 * (double)m->np : 0.0));
-  launch_k(adamw_kernel, grid_for(n4, 256, 148 * 8), 256, 0, m->stream, m->params, m->grads, m->m, m->v, n4, m->hparams,
-                                                                   m->params_bf);
-  timer_end(m, TK_ADAMW);
+// AdamW over k pieces (element offset into the flat buffers, element count) in
+// one launch, on stream st.
+static int launch_adamw(gpt2_t* m, const long long* off, const long long* cnt, int k, cudaStream_t st) {
+  AdamSegs sg = {};
+  long long tot = 0;
+  for (int i = 0; i < k; i++) {
+    if (cnt[i] <= 0) continue;  // the Llama-style variant's empty tensors
+    if (sg.n == ADAMW_MAX_SEGS || (off[i] & 3) || (cnt[i] & 3)) {
+      m->poisoned = GPT2_ERR_CUDA;
+      return GPT2_ERR_CUDA;
+    }
+    sg.off4[sg.n] = off[i] / 4;
+    tot += cnt[i] / 4;
+    sg.end4[sg.n++] = tot;
+  }
+  if (!sg.n) return GPT2_OK;
+  const bool on_main = st == m->stream;
+  if (on_main) timer_begin(m, TK_ADAMW, 4.0 * tot * (28.0 + (m->params_bf ? 2.0 : 0.0)));
+  launch_k(adamw_kernel, grid_for(tot, 256, 148 * 8), 256, 0, st, m->params, (const float*)m->grads, m->m, m->v, sg,
+           (const float*)m->hparams, m->params_bf);
+  if (on_main) timer_end(m, TK_ADAMW);
   m->launches++;
   KCHECK(m);
   return GPT2_OK;
+}
+
+static long long poff(const gpt2_t* m, int i) { return (long long)(m->P[i] - m->params); }
+
+// AdamW of every parameter (gpt2_update)
+static int enqueue_update(gpt2_t* m) {
+  const long long off = 0, cnt = m->np;
+  return launch_adamw(m, &off, &cnt, 1, m->stream);
+}
+
+// AdamW of layer l's twelve tensors, once their gradients are complete: on
+// the update side stream after everything enqueued so far on the main stream
+// and both gradient side streams (on the main stream when side streams are
+// off).  Called by the fused step's backward after layer l's last kernel.
+static int update_layer(gpt2_t* m, int l) {
+  static const int T[12] = {P_LN1W, P_LN1B, P_QKVW, P_QKVB, P_ATTPROJW, P_ATTPROJB,
+                            P_LN2W, P_LN2B, P_FCW,  P_FCB,  P_FCPROJW,  P_FCPROJB};
+  const long long L = m->cfg.num_layers;
+  long long off[12], cnt[12];
+  for (int i = 0; i < 12; i++) {
+    cnt[i] = m->psize[T[i]] / L;
+    off[i] = poff(m, T[i]) + l * cnt[i];
+  }
+  if (!side_on(m) || !m->side_u) return launch_adamw(m, off, cnt, 12, m->stream);
+  const int f = m->sev_next, d = (m->sev_next + 1) % SIDE_EVENTS;
+  m->sev_next = (m->sev_next + 2) % SIDE_EVENTS;
+  CCHECK(m, cudaEventRecord(m->sev[f], m->stream));
+  CCHECK(m, cudaStreamWaitEvent(m->side_u, m->sev[f], 0));
+  if (m->side_last >= 0) CCHECK(m, cudaStreamWaitEvent(m->side_u, m->sev[m->side_last], 0));
+  if (m->side_w_last >= 0) CCHECK(m, cudaStreamWaitEvent(m->side_u, m->sev[m->side_w_last], 0));
+  int rc = launch_adamw(m, off, cnt, 12, m->side_u);
+  if (rc) return rc;
+  CCHECK(m, cudaEventRecord(m->sev[d], m->side_u));
+  m->side_u_last = d;
+  return GPT2_OK;
+}
+
+// The rest of the fused step's AdamW (the tensors outside the layers: wte,
+// wpe, the final layernorm), after joining the per-layer updates.
+static int update_rest(gpt2_t* m) {
+  if (m->side_u_last >= 0) CCHECK(m, cudaStreamWaitEvent(m->stream, m->sev[m->side_u_last], 0));
+  m->side_u_last = -1;
+  const long long off[4] = {poff(m, P_WTE), poff(m, P_WPE), poff(m, P_LNFW), poff(m, P_LNFB)};
+  const long long cnt[4] = {m->psize[P_WTE], m->psize[P_WPE], m->psize[P_LNFW], m->psize[P_LNFB]};
+  return launch_adamw(m, off, cnt, 4, m->stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -1419,6 +1493,7 @@ EXPORT int gpt2_build(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, int m
   cudaError_t e;
   m->side_last = m->rd_scratch = m->rd_dfch = m->rd_dqkv = -1;
   m->side_w_last = m->wd_dres = m->wd_dfch = m->wd_dqkv = -1;
+  m->side_u_last = -1;
   if (set_kernel_attributes() != GPT2_OK) {
     rc = GPT2_ERR_CUDA;
     goto fail;
@@ -1432,6 +1507,10 @@ EXPORT int gpt2_build(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, int m
     if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) goto cuda_fail;
     if ((e = cudaStreamCreateWithPriority(&m->side_w, cudaStreamNonBlocking, lo)) != cudaSuccess) {
       m->side_w = nullptr;
+      goto cuda_fail;
+    }
+    if ((e = cudaStreamCreateWithPriority(&m->side_u, cudaStreamNonBlocking, lo)) != cudaSuccess) {
+      m->side_u = nullptr;
       goto cuda_fail;
     }
   }
@@ -1475,6 +1554,7 @@ fail:
     if (m->sev[i]) cudaEventDestroy(m->sev[i]);
   if (m->side) cudaStreamDestroy(m->side);
   if (m->side_w) cudaStreamDestroy(m->side_w);
+  if (m->side_u) cudaStreamDestroy(m->side_u);
   if (m->own_arena) cudaFree(m->arena);
   free(m);
   return rc;
@@ -1490,6 +1570,10 @@ EXPORT int gpt2_free(gpt2_t* m) {
   if (m->side_w) {
     cudaStreamSynchronize(m->side_w);
     cudaStreamDestroy(m->side_w);
+  }
+  if (m->side_u) {
+    cudaStreamSynchronize(m->side_u);
+    cudaStreamDestroy(m->side_u);
   }
   for (int i = 0; i < SIDE_EVENTS; i++)
     if (m->sev[i]) cudaEventDestroy(m->sev[i]);
@@ -1647,10 +1731,12 @@ static int enqueue_step(gpt2_t* m, int B, int T) {
     CCHECK(m, cudaMemsetAsync(m->G[P_WPE] + (size_t)T * C, 0, (size_t)(m->cfg.max_seq_len - T) * C * sizeof(float),
                               m->stream));
   m->grad_accumulate = 0;
+  m->upd_layers = 1;  // each layer's AdamW starts once its gradients are complete
   rc = enqueue_backward(m);
+  m->upd_layers = 0;
   m->grad_accumulate = 1;
   if (rc) return rc;
-  return enqueue_update(m);
+  return update_rest(m);
 }
 
 static int run_step(gpt2_t* m, int B, int T, int use_graph) {

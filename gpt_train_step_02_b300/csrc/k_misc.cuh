@@ -260,17 +260,31 @@ __global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ x,
 }
 
 // ---------------------------------------------------------------------------
-// AdamW over the flat buffers (float4 granularity; n % 4 == 0).  hp holds
-// {lr, beta1, beta2, eps, weight_decay, 1/(1-beta1^t), 1/(1-beta2^t)}.  When pbf16 != NULL the bf16
-// copy of the updated parameters is written too.
+// AdamW over segments of the flat buffers (float4 granularity).  Segment k
+// covers float4 elements [off4[k], off4[k] + (end4[k] - end4[k-1])), end4 the
+// running total (end4[-1] = 0); one launch updates one segment list, e.g. the
+// whole buffer or the twelve tensors of one layer.  hp holds {lr, beta1,
+// beta2, eps, weight_decay, 1/(1-beta1^t), 1/(1-beta2^t)}.  When pbf16 !=
+// NULL the bf16 copy of the updated parameters is written too.
 // ---------------------------------------------------------------------------
+#define ADAMW_MAX_SEGS 16
+struct AdamSegs {
+  long long off4[ADAMW_MAX_SEGS];
+  long long end4[ADAMW_MAX_SEGS];
+  int n;
+};
+
 __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
-                             float* __restrict__ v, long long n4, const float* __restrict__ hp,
-                             uint16_t* __restrict__ pbf16) {
+                             float* __restrict__ v, const __grid_constant__ AdamSegs segs,
+                             const float* __restrict__ hp, uint16_t* __restrict__ pbf16) {
   pdl_launch_dependents();
   pdl_wait();
   const float lr = hp[0], b1 = hp[1], b2 = hp[2], eps = hp[3], wd = hp[4], c1inv = hp[5], c2inv = hp[6];
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+  const long long total = segs.end4[segs.n - 1];
+  int sg = 0;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
+    while (e >= segs.end4[sg]) sg++;  // e only grows
+    const long long i = segs.off4[sg] + e - (sg ? segs.end4[sg - 1] : 0);
     float4 pp = reinterpret_cast<float4*>(p)[i];
     float4 gg = reinterpret_cast<const float4*>(g)[i];
     float4 mm = reinterpret_cast<float4*>(m)[i];
