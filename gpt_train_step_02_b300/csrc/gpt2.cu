@@ -29,6 +29,7 @@
 #include "k_attention_simt.cuh"
 #include "k_attention_small.cuh"
 #include "k_attention_tc.cuh"
+#include "k_attention_tf32.cuh"
 #include "k_gemm_bf16.cuh"
 #include "k_gemm_tc.cuh"
 #include "k_layernorm.cuh"
@@ -880,6 +881,24 @@ static void ln_backward(gpt2_t* m, float* dx, uint16_t* dxbf, float* dw, float* 
   m->launches += 2;
 }
 
+// Tensor map of an fp32 matrix stored as `outer` rows of pitch `ld` elements
+// with `inner` valid columns: 32 x 64 boxes (128-byte rows) with the 128-byte
+// swizzle, the tile format of the short-sequence fp32 attention.
+static int make_f32_box64_map(CUtensorMap* tm, const float* base, long long outer, long long inner, long long ld) {
+  if (!get_encoder()) return 0;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * sizeof(float)};
+  cuuint32_t box[2] = {32, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode_tiled(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, (void*)base, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// fp32 operands, head size 64, T <= 64: the 3xTF32 tensor-core kernels
+static bool attn_tf32_path(int bf, int hs, int T) { return !bf && hs == atf::HS && T <= atf::T_MAX; }
+
 // Causal attention forward: the tensor-core kernel for bf16 operands with
 // head size 64 and T % 128 == 0, else the CUDA-core kernel (the template
 // argument is the number of head dimensions each lane holds, hs <= 32 * ND).
@@ -898,6 +917,16 @@ static int launch_attn_fwd(float* atty, uint16_t* attybf, float* lse, const floa
     const long long items = (long long)(T / tca::BQ) * NH * B;
     launch_k(tca::attn_fwd_tc_kernel, (int)(items < 2 * 148 ? items : 2 * 148), tca::THREADS, tca::fwd::SMEM_BYTES, s,
              tm, p);
+    return 1;
+  }
+  if (attn_tf32_path(bf, hs, T)) {  // fp32, short sequences: one CTA per (head, batch), 3xTF32 products
+    CUtensorMap tm;
+    if (!make_f32_box64_map(&tm, qkv, (long long)B * T, 3LL * C, 3LL * C)) return -1;
+    atf::Params p = {};
+    p.B = B; p.T = T; p.C = C; p.NH = NH;
+    p.scale = 1.0f / sqrtf((float)hs);
+    p.qkv = qkv; p.out = atty; p.out_bf = attybf; p.lse = lse; p.err = err;
+    launch_k(atf::attn_fwd_tf32_kernel, dim3(NH, B), atf::THREADS, atf::FWD_SMEM, s, tm, p);
     return 1;
   }
   if (T <= atts::T_MAX && hs == atts::HS) {  // short sequences: one CTA per (batch, head)
@@ -935,6 +964,19 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
   const int hs = C / NH;
   const int grid = ceil_div((long long)B * NH * T * 32, 256);
   const bool tc_path = bf && qkv_bf && dy_bf && hs == tca::HS && T % tca::BQ == 0;
+  if (!tc_path && attn_tf32_path(bf, hs, T)) {  // fp32, short sequences: dQ and dK/dV kernels, 3xTF32 products
+    if (!dqkv || colsum) return -1;
+    CUtensorMap tq, td;
+    if (!make_f32_box64_map(&tq, qkv, (long long)B * T, 3LL * C, 3LL * C)) return -1;
+    if (!make_f32_box64_map(&td, dy, (long long)B * T, C, C)) return -1;
+    atf::Params p = {};
+    p.B = B; p.T = T; p.C = C; p.NH = NH;
+    p.scale = 1.0f / sqrtf((float)hs);
+    p.qkv = qkv; p.dy = dy; p.y = atty; p.out = dqkv; p.out_bf = dqkv_bf; p.lse = (float*)lse; p.err = err;
+    launch_k(atf::attn_bwd_dq_tf32_kernel, dim3(NH, B), atf::THREADS, atf::DQ_SMEM, s, tq, p);
+    launch_k(atf::attn_bwd_dkv_tf32_kernel, dim3(NH, B), atf::THREADS, atf::DKV_SMEM, s, tq, td, p);
+    return 2;
+  }
   if (!tc_path && T <= atts::T_MAX && hs == atts::HS) {  // short sequences: one launch, D formed in the kernel
     if (!dqkv || colsum) return -1;
     launch_k(atts::attn_bwd_small_kernel, dim3(NH, B), atts::THREADS, atts::BWD_SMEM, s, dqkv, dqkv_bf, qkv, dy, atty,
@@ -1042,6 +1084,15 @@ static int set_kernel_attributes() {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<10, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<10, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(atf::attn_fwd_tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)atf::FWD_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(atf::attn_bwd_dq_tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)atf::DQ_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(atf::attn_bwd_dkv_tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)atf::DKV_SMEM);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(atts::attn_fwd_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)atts::FWD_SMEM);

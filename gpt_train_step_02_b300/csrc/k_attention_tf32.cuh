@@ -1,0 +1,557 @@
+// k_attention_tf32.cuh -- causal multi-head attention for short sequences
+// (T <= 64) with head size 64 and fp32 operands, its products on the
+// 5th-generation tensor cores (tcgen05.mma kind::tf32, accumulators in TMEM)
+// at fp32 accuracy: every operand value is split x = hi + lo (hi = x rounded
+// to TF32, lo = x - hi) and each product is ah*bh + ah*bl + al*bh, three MMAs
+// into one fp32 accumulator (the 3xTF32 scheme of Ootomo & Yokota, 2022),
+// as in the fp32 matmul.
+//
+// Arithmetic (the page «llm.c：Andrej Karpathy带你从零复现LLM», section
+// «核心代码解读：train_gpt2.c», item 1: attention_forward / attention_backward):
+// scale 1/sqrt(hs), keys t2 <= t; S = q k^T scale, P = softmax(S), y = P v,
+// lse = max + log(sum exp); backward through P = exp(S - lse),
+// D_t = dy_t . y_t, dS = P o (dy v^T - D), dq = dS k scale, dk = dS^T q scale,
+// dv = P^T dy.  Exponentials use expf (the fp32 workloads are compared step
+// by step with the oracle).
+//
+// One CTA of 128 threads per (head, batch); thread r owns TMEM lane r, i.e.
+// row r of every 128-row accumulator (rows >= T are padding).  Operands:
+//  - A operands (the rows the CTA's threads own) go from registers to TMEM
+//    (tcgen05.st; row in the lane, one K value per column);
+//  - B operands sit in shared memory as 64 x 64 fp32 tiles, K-major with the
+//    128-byte swizzle: K values [32c, 32c + 32) of row n at
+//    8 KB * c + 128 n + 16 ((k/4 % 8) ^ (n % 8)) + 4 (k % 4) bytes.  Tiles
+//    whose rows are rows of qkv (or dy) come in by TMA in exactly that layout
+//    and are split in place (hi) plus a lo copy; transposed tiles are written
+//    from the split ones.
+// One thread issues the MMAs; completion is signalled through an mbarrier.
+// Every wait is bounded (tc::mbar_wait) and every stop-or-continue decision
+// is taken by the whole CTA at once (__syncthreads_and), so a wait that gives
+// up leaves no thread behind at a barrier.
+#pragma once
+#include <cuda.h>
+
+#include "common.cuh"
+#include "k_gemm_tc.cuh"
+
+namespace atf {
+using tc::mbar_expect_tx;
+using tc::mbar_init;
+using tc::mbar_wait;
+using tc::mbar_wait_drain;
+using tc::mma_commit;
+using tc::smem_u32;
+using tc::tc_fence_after;
+using tc::tc_fence_before;
+using tc::tf32_hi;
+using tc::tma_load_2d;
+using tc::tmem_ld32;
+using tc::tmem_st16;
+
+constexpr int T_MAX = 64;                 // longest sequence
+constexpr int HS = 64;                    // head size
+constexpr int THREADS = 128;              // one thread per TMEM lane
+constexpr int TILE_FLOATS = 64 * 64;      // one 64 x 64 fp32 B tile
+constexpr int TILE_BYTES = TILE_FLOATS * 4;  // 16 KB
+constexpr int BOX_BYTES = TILE_BYTES / 2;    // one 32-column TMA box: 64 rows x 128 B
+
+// float offset of K value k of row n in a swizzled 64 x 64 K-major tile
+GPT2_DEV int sw(int n, int k) { return (k >> 5) * 2048 + n * 32 + ((((k & 31) >> 2) ^ (n & 7)) << 2) + (k & 3); }
+
+// Shared-memory descriptor of the 8 K values [8 kc, 8 kc + 8) of a swizzled tile.
+GPT2_DEV uint64_t bdesc(const float* tile, int kc) {
+  return tc::smem_desc_kmajor_sw128(smem_u32(tile) + (uint32_t)((kc >> 2) * BOX_BYTES + (kc & 3) * 32));
+}
+
+// Instruction descriptor: D fp32, A and B tf32 K-major, M = 128, N = n.
+GPT2_DEV uint32_t idesc(int n) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+GPT2_DEV void mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
+      : "memory");
+}
+
+// acc (TMEM columns d_col ..) = A B^T over K = 8 ksteps values, 3xTF32: A's
+// hi and lo halves in TMEM columns a_hi / a_lo (K value k in column + k), B's
+// in swizzled tiles b_hi / b_lo; N = n rows of B.
+GPT2_DEV void mma3(uint32_t tmem, int d_col, int a_hi, int a_lo, const float* b_hi, const float* b_lo, int ksteps,
+                   int n) {
+  const uint32_t id = idesc(n);
+  for (int kc = 0; kc < ksteps; kc++) {
+    const uint64_t bh = bdesc(b_hi, kc), bl = bdesc(b_lo, kc);
+    mma_ta(tmem + d_col, tmem + a_hi + 8 * kc, bh, id, kc > 0 ? 1u : 0u);
+    mma_ta(tmem + d_col, tmem + a_hi + 8 * kc, bl, id, 1u);
+    mma_ta(tmem + d_col, tmem + a_lo + 8 * kc, bh, id, 1u);
+  }
+}
+
+// 64 values of this thread's row into TMEM columns col .. col+63 (hi) and
+// col + 64 .. col + 127 (lo) of its lane.
+GPT2_DEV void st_row_split(uint32_t tlane, int col, const float* v) {
+#pragma unroll
+  for (int g = 0; g < 4; g++) {
+    float hv[16], lv[16];
+#pragma unroll
+    for (int k = 0; k < 16; k++) {
+      hv[k] = tf32_hi(v[16 * g + k]);
+      lv[k] = v[16 * g + k] - hv[k];
+    }
+    tmem_st16(tlane + (uint32_t)(col + 16 * g), hv);
+    tmem_st16(tlane + (uint32_t)(col + 64 + 16 * g), lv);
+  }
+}
+
+// 64 floats of row src (16-byte aligned) into v, or zeros when !valid.
+GPT2_DEV void ld_row64(const float* src, bool valid, float* v) {
+#pragma unroll
+  for (int q = 0; q < 16; q++) {
+    const float4 x = valid ? __ldg(reinterpret_cast<const float4*>(src) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[4 * q] = x.x;
+    v[4 * q + 1] = x.y;
+    v[4 * q + 2] = x.z;
+    v[4 * q + 3] = x.w;
+  }
+}
+
+GPT2_DEV void ld_row64_tmem(uint32_t taddr, float* v) {
+  tmem_ld32(taddr, v);
+  tmem_ld32(taddr + 32, v + 32);
+}
+
+// In-place split of a TMA-written tile: hi stays, lo goes to lo.
+GPT2_DEV void split_tile(float* t, float* lo) {
+  float4* t4 = reinterpret_cast<float4*>(t);
+  float4* l4 = reinterpret_cast<float4*>(lo);
+  for (int i = threadIdx.x; i < TILE_FLOATS / 4; i += THREADS) {
+    float4 h, l;
+    tc::split4(t4[i], h, l);
+    t4[i] = h;
+    l4[i] = l;
+  }
+}
+
+// dst(n, k) = src(k, n) for the 64 x 64 tiles (already split halves are copied).
+GPT2_DEV void transpose_tile(const float* src, float* dst) {
+  for (int e = threadIdx.x; e < TILE_FLOATS; e += THREADS) {
+    const int n = e >> 6, k = e & 63;  // a warp writes 32 consecutive k of one row n
+    dst[sw(n, k)] = src[sw(k, n)];
+  }
+}
+
+// Generic-proxy shared-memory writes and TMEM stores made visible to the
+// tensor core, then a CTA barrier.
+GPT2_DEV void publish_operands() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+struct Params {
+  int B, T, C, NH;
+  float scale;
+  const float* qkv;    // (B, T, 3C)
+  const float* dy;     // (B, T, C) upstream gradient (backward)
+  const float* y;      // (B, T, C) attention output (backward: D = dy . y)
+  float* out;          // forward: y (B, T, C); backward: dqkv (B, T, 3C)
+  uint16_t* out_bf;    // optional bf16 copy of out
+  float* lse;          // (B, NH, T): written by the forward, read by the backward
+  int* err;
+};
+
+// Shared-memory layout (from a 1024-byte aligned base) of each kernel: NT
+// tiles, then two mbarriers and the TMEM slot; + 1 KB alignment slack.
+template <int NT>
+struct Smem {
+  static constexpr int OFF_BAR = NT * TILE_BYTES;
+  static constexpr int OFF_VEC = OFF_BAR + 64;  // two 64-float vectors (lse, D) for the dK/dV kernel
+  static constexpr int BYTES = OFF_VEC + 2 * 64 * 4 + 1024;
+};
+constexpr int FWD_TILES = 5;  // K (hi, lo), V raw, V^T (hi, lo)
+constexpr int DQ_TILES = 6;   // K (hi, lo), V (hi, lo), K^T (hi, lo)
+constexpr int DKV_TILES = 8;  // Q (hi, lo), dY (hi, lo), Q^T (hi, lo), dY^T (hi, lo)
+constexpr size_t FWD_SMEM = Smem<FWD_TILES>::BYTES;
+constexpr size_t DQ_SMEM = Smem<DQ_TILES>::BYTES;
+constexpr size_t DKV_SMEM = Smem<DKV_TILES>::BYTES;
+
+// Common prologue: barriers, TMEM allocation (ncols), PDL wait.
+template <int NT>
+GPT2_DEV uint32_t prologue(uint8_t* smem, int ncols) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<NT>::OFF_BAR);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + Smem<NT>::OFF_BAR + 16);
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);  // TMA
+    mbar_init(&bars[1], 1);  // MMA completion
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (threadIdx.x < 32) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  return *slot;
+}
+
+template <int NT>
+GPT2_DEV void epilogue_free(uint8_t* smem, uint32_t tmem, int ncols) {
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+  }
+}
+
+// Thread 0 issues the four TMA box loads of two tiles (rows y0 .. y0+63 of
+// map tm, columns x0 .. x0+63 and x1 .. x1+63) onto bar.
+GPT2_DEV void tma_two_tiles(const CUtensorMap* tm, float* t0, int x0, float* t1, int x1, int y0, uint64_t* bar) {
+  mbar_expect_tx(bar, 2 * TILE_BYTES);
+  tma_load_2d(t0, tm, x0, y0, bar);
+  tma_load_2d(reinterpret_cast<uint8_t*>(t0) + BOX_BYTES, tm, x0 + 32, y0, bar);
+  tma_load_2d(t1, tm, x1, y0, bar);
+  tma_load_2d(reinterpret_cast<uint8_t*>(t1) + BOX_BYTES, tm, x1 + 32, y0, bar);
+}
+
+// The abort path: the TMA copies and the last committed MMA batch (phase
+// mma_phase of the MMA barrier, -1 for none) land before the CTA releases its
+// memory.
+GPT2_DEV void drain(uint64_t* bars, int mma_phase) {
+  if (threadIdx.x == 0) {
+    mbar_wait_drain(&bars[0], 0);
+    if (mma_phase >= 0) mbar_wait_drain(&bars[1], (uint32_t)(mma_phase & 1));
+  }
+}
+
+// A bounded wait on bar (phase) by every thread, decided collectively.
+GPT2_DEV bool wait_all(uint64_t* bar, uint32_t phase, volatile int* abort_flag, int* err) {
+  const bool ok = mbar_wait(bar, phase, abort_flag, err);
+  return __syncthreads_and(ok) != 0;
+}
+
+// ---------------------------------------------------------------------------
+// forward.  TMEM: S accumulator [0, 64) -> later O; Q hi/lo [64, 192) ->
+// later P hi/lo.  tmQKV: qkv as (B*T rows, 3C columns), 32 x 64 boxes, SW128.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_constant__ CUtensorMap tmQKV,
+                                                                const __grid_constant__ Params p) {
+  pdl_launch_dependents();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  float* k_hi = reinterpret_cast<float*>(smem);
+  float* k_lo = k_hi + TILE_FLOATS;
+  float* v_raw = k_lo + TILE_FLOATS;
+  float* vt_hi = v_raw + TILE_FLOATS;
+  float* vt_lo = vt_hi + TILE_FLOATS;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<FWD_TILES>::OFF_BAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<FWD_TILES>::OFF_BAR + 24);
+  if (threadIdx.x == 0) *abort_flag = 0;
+  const uint32_t tmem = prologue<FWD_TILES>(smem, 256);
+  pdl_wait();
+
+  const int h = blockIdx.x, b = blockIdx.y, T = p.T, C = p.C, r = threadIdx.x;
+  const int Tp = (T + 15) & ~15;  // keys padded to the MMA's N granularity
+  const uint32_t tlane = tmem + ((uint32_t)(r & ~31) << 16);
+  const size_t row0 = (size_t)b * T;
+  if (r == 0) tma_two_tiles(&tmQKV, k_hi, C + h * HS, v_raw, 2 * C + h * HS, b * T, &bars[0]);
+  {
+    float q[64];
+    ld_row64(p.qkv + (row0 + r) * 3 * C + h * HS, r < T, q);
+    st_row_split(tlane, 64, q);
+  }
+  int mma_phase = -1;
+  bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
+  if (ok) {
+    split_tile(k_hi, k_lo);
+    // V^T halves: rows d, K values = keys
+    for (int e = threadIdx.x; e < TILE_FLOATS; e += THREADS) {
+      const int d = e >> 6, key = e & 63;
+      const float x = v_raw[sw(key, d)], hi = tf32_hi(x);
+      vt_hi[sw(d, key)] = hi;
+      vt_lo[sw(d, key)] = x - hi;
+    }
+    publish_operands();
+    if (r == 0) {
+      mma3(tmem, 0, 64, 128, k_hi, k_lo, HS / 8, Tp);  // S = Q K^T
+      mma_commit(&bars[1]);
+    }
+    mma_phase = 0;
+    ok = wait_all(&bars[1], 0, abort_flag, p.err);
+  }
+  if (ok) {
+    tc_fence_after();
+    float s[64];
+    ld_row64_tmem(tlane + 0, s);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 64; j++) {
+      s[j] = (j <= r && j < T) ? s[j] * p.scale : -INFINITY;
+      mx = fmaxf(mx, s[j]);
+    }
+    float l = 0.f;
+#pragma unroll
+    for (int j = 0; j < 64; j++) {
+      s[j] = s[j] == -INFINITY ? 0.f : expf(s[j] - mx);
+      l += s[j];
+    }
+    const bool valid = r < T;
+    const float inv = valid ? 1.0f / l : 0.f;
+#pragma unroll
+    for (int j = 0; j < 64; j++) s[j] *= inv;
+    if (valid) p.lse[((size_t)b * p.NH + h) * T + r] = mx + logf(l);
+    st_row_split(tlane, 64, s);  // P over Q's columns: the S MMAs have completed
+    publish_operands();
+    if (r == 0) {
+      mma3(tmem, 0, 64, 128, vt_hi, vt_lo, Tp / 8, HS);  // O = P V, over S's columns
+      mma_commit(&bars[1]);
+    }
+    mma_phase = 1;
+    ok = wait_all(&bars[1], 1, abort_flag, p.err);
+  }
+  if (ok) {
+    tc_fence_after();
+    float o[64];
+    ld_row64_tmem(tlane + 0, o);
+    if (r < T) {
+      float* yr = p.out + (row0 + r) * C + h * HS;
+#pragma unroll
+      for (int q = 0; q < 16; q++)
+        reinterpret_cast<float4*>(yr)[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      if (p.out_bf) {
+        uint16_t* yb = p.out_bf + (row0 + r) * C + h * HS;
+#pragma unroll
+        for (int q = 0; q < 16; q++)
+          reinterpret_cast<uint2*>(yb)[q] =
+              make_uint2(bf16x2_bits(o[4 * q], o[4 * q + 1]), bf16x2_bits(o[4 * q + 2], o[4 * q + 3]));
+      }
+    }
+  } else {
+    drain(bars, mma_phase);  // a copy or MMA still in flight lands before the CTA's memory is released
+  }
+  epilogue_free<FWD_TILES>(smem, tmem, 256);
+}
+
+// Stores this thread's 64 fp32 gradient values into dqkv (and its bf16 copy).
+GPT2_DEV void store_grad_row(const Params& p, size_t row, int col, const float* g) {
+  float* dst = p.out + row * 3 * p.C + col;
+#pragma unroll
+  for (int q = 0; q < 16; q++)
+    reinterpret_cast<float4*>(dst)[q] = make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
+  if (p.out_bf) {
+    uint16_t* db = p.out_bf + row * 3 * p.C + col;
+#pragma unroll
+    for (int q = 0; q < 16; q++)
+      reinterpret_cast<uint2*>(db)[q] =
+          make_uint2(bf16x2_bits(g[4 * q], g[4 * q + 1]), bf16x2_bits(g[4 * q + 2], g[4 * q + 3]));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// backward, query rows: dq.  TMEM: S [0, 64) -> later dQ; dP [64, 128);
+// Q hi/lo [128, 256) -> later dS hi/lo; dY hi/lo [256, 384).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(THREADS) attn_bwd_dq_tf32_kernel(const __grid_constant__ CUtensorMap tmQKV,
+                                                                   const __grid_constant__ Params p) {
+  pdl_launch_dependents();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  float* k_hi = reinterpret_cast<float*>(smem);
+  float* k_lo = k_hi + TILE_FLOATS;
+  float* v_hi = k_lo + TILE_FLOATS;
+  float* v_lo = v_hi + TILE_FLOATS;
+  float* kt_hi = v_lo + TILE_FLOATS;
+  float* kt_lo = kt_hi + TILE_FLOATS;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<DQ_TILES>::OFF_BAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<DQ_TILES>::OFF_BAR + 24);
+  if (threadIdx.x == 0) *abort_flag = 0;
+  const uint32_t tmem = prologue<DQ_TILES>(smem, 512);
+  pdl_wait();
+
+  const int h = blockIdx.x, b = blockIdx.y, T = p.T, C = p.C, r = threadIdx.x;
+  const int Tp = (T + 15) & ~15;
+  const uint32_t tlane = tmem + ((uint32_t)(r & ~31) << 16);
+  const size_t row0 = (size_t)b * T;
+  const bool valid = r < T;
+  if (r == 0) tma_two_tiles(&tmQKV, k_hi, C + h * HS, v_hi, 2 * C + h * HS, b * T, &bars[0]);
+  float Dr, lse_r;
+  {
+    float a[64], c[64];
+    ld_row64(p.dy + (row0 + r) * C + h * HS, valid, a);
+    ld_row64(p.y + (row0 + r) * C + h * HS, valid, c);
+    Dr = 0.f;
+#pragma unroll
+    for (int d = 0; d < 64; d++) Dr = fmaf(a[d], c[d], Dr);
+    st_row_split(tlane, 256, a);  // dY
+    ld_row64(p.qkv + (row0 + r) * 3 * C + h * HS, valid, c);
+    st_row_split(tlane, 128, c);  // Q
+    lse_r = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
+  }
+  int mma_phase = -1;
+  bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
+  if (ok) {
+    split_tile(k_hi, k_lo);
+    split_tile(v_hi, v_lo);
+    __syncthreads();
+    transpose_tile(k_hi, kt_hi);
+    transpose_tile(k_lo, kt_lo);
+    publish_operands();
+    if (r == 0) {
+      mma3(tmem, 0, 128, 192, k_hi, k_lo, HS / 8, Tp);   // S = Q K^T
+      mma3(tmem, 64, 256, 320, v_hi, v_lo, HS / 8, Tp);  // dP = dY V^T
+      mma_commit(&bars[1]);
+    }
+    mma_phase = 0;
+    ok = wait_all(&bars[1], 0, abort_flag, p.err);
+  }
+  if (ok) {
+    tc_fence_after();
+    float s[64], dp[64];
+    ld_row64_tmem(tlane + 0, s);
+    ld_row64_tmem(tlane + 64, dp);
+#pragma unroll
+    for (int j = 0; j < 64; j++) {
+      // dS, with the scale of S folded in; columns past the MMA's N hold no data
+      s[j] = (valid && j <= r) ? expf(s[j] * p.scale - lse_r) * (dp[j] - Dr) * p.scale : 0.f;
+    }
+    st_row_split(tlane, 128, s);  // dS over Q's columns
+    publish_operands();
+    if (r == 0) {
+      mma3(tmem, 0, 128, 192, kt_hi, kt_lo, Tp / 8, HS);  // dQ = dS K, over S's columns
+      mma_commit(&bars[1]);
+    }
+    mma_phase = 1;
+    ok = wait_all(&bars[1], 1, abort_flag, p.err);
+  }
+  if (ok) {
+    tc_fence_after();
+    float g[64];
+    ld_row64_tmem(tlane + 0, g);
+    if (valid) store_grad_row(p, row0 + r, h * HS, g);
+  } else {
+    drain(bars, mma_phase);
+  }
+  epilogue_free<DQ_TILES>(smem, tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// backward, key rows: dk and dv.  TMEM: S^T [0, 64) -> later dV;
+// dP^T [64, 128) -> later dK; K hi/lo [128, 256) -> later P^T hi/lo;
+// V hi/lo [256, 384) -> later dS^T hi/lo.  tmDY: dy as (B*T rows, C columns).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(THREADS) attn_bwd_dkv_tf32_kernel(const __grid_constant__ CUtensorMap tmQKV,
+                                                                    const __grid_constant__ CUtensorMap tmDY,
+                                                                    const __grid_constant__ Params p) {
+  pdl_launch_dependents();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  float* q_hi = reinterpret_cast<float*>(smem);
+  float* q_lo = q_hi + TILE_FLOATS;
+  float* dy_hi = q_lo + TILE_FLOATS;
+  float* dy_lo = dy_hi + TILE_FLOATS;
+  float* qt_hi = dy_lo + TILE_FLOATS;
+  float* qt_lo = qt_hi + TILE_FLOATS;
+  float* dyt_hi = qt_lo + TILE_FLOATS;
+  float* dyt_lo = dyt_hi + TILE_FLOATS;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<DKV_TILES>::OFF_BAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<DKV_TILES>::OFF_BAR + 24);
+  float* lse_s = reinterpret_cast<float*>(smem + Smem<DKV_TILES>::OFF_VEC);
+  float* D_s = lse_s + 64;
+  if (threadIdx.x == 0) *abort_flag = 0;
+  const uint32_t tmem = prologue<DKV_TILES>(smem, 512);
+  pdl_wait();
+
+  const int h = blockIdx.x, b = blockIdx.y, T = p.T, C = p.C, r = threadIdx.x;
+  const int Tp = (T + 15) & ~15;
+  const uint32_t tlane = tmem + ((uint32_t)(r & ~31) << 16);
+  const size_t row0 = (size_t)b * T;
+  const bool valid = r < T;
+  if (r == 0) {
+    mbar_expect_tx(&bars[0], 2 * TILE_BYTES);
+    tma_load_2d(q_hi, &tmQKV, h * HS, b * T, &bars[0]);
+    tma_load_2d(reinterpret_cast<uint8_t*>(q_hi) + BOX_BYTES, &tmQKV, h * HS + 32, b * T, &bars[0]);
+    tma_load_2d(dy_hi, &tmDY, h * HS, b * T, &bars[0]);
+    tma_load_2d(reinterpret_cast<uint8_t*>(dy_hi) + BOX_BYTES, &tmDY, h * HS + 32, b * T, &bars[0]);
+  }
+  {
+    float a[64], c[64];
+    // row r as a query: D_r = dy_r . y_r and lse_r, shared with every key row
+    ld_row64(p.dy + (row0 + r) * C + h * HS, valid, a);
+    ld_row64(p.y + (row0 + r) * C + h * HS, valid, c);
+    float D = 0.f;
+#pragma unroll
+    for (int d = 0; d < 64; d++) D = fmaf(a[d], c[d], D);
+    if (r < 64) {
+      D_s[r] = D;
+      lse_s[r] = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
+    }
+    // row r as a key: K and V into TMEM
+    ld_row64(p.qkv + (row0 + r) * 3 * C + C + h * HS, valid, a);
+    st_row_split(tlane, 128, a);
+    ld_row64(p.qkv + (row0 + r) * 3 * C + 2 * C + h * HS, valid, c);
+    st_row_split(tlane, 256, c);
+  }
+  int mma_phase = -1;
+  bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
+  if (ok) {
+    split_tile(q_hi, q_lo);
+    split_tile(dy_hi, dy_lo);
+    __syncthreads();
+    transpose_tile(q_hi, qt_hi);
+    transpose_tile(q_lo, qt_lo);
+    transpose_tile(dy_hi, dyt_hi);
+    transpose_tile(dy_lo, dyt_lo);
+    publish_operands();
+    if (r == 0) {
+      mma3(tmem, 0, 128, 192, q_hi, q_lo, HS / 8, Tp);     // S^T = K Q^T
+      mma3(tmem, 64, 256, 320, dy_hi, dy_lo, HS / 8, Tp);  // dP^T = V dY^T
+      mma_commit(&bars[1]);
+    }
+    mma_phase = 0;
+    ok = wait_all(&bars[1], 0, abort_flag, p.err);
+  }
+  if (ok) {
+    tc_fence_after();
+    float pt[64], dst[64];
+    ld_row64_tmem(tlane + 0, pt);
+    ld_row64_tmem(tlane + 64, dst);
+#pragma unroll
+    for (int t = 0; t < 64; t++) {
+      // columns past the MMA's N hold no data
+      const bool live = valid && t >= r && t < T;
+      const float pv = live ? expf(pt[t] * p.scale - lse_s[t]) : 0.f;
+      pt[t] = pv;
+      dst[t] = live ? pv * (dst[t] - D_s[t]) * p.scale : 0.f;  // dS^T, with the scale folded in
+    }
+    st_row_split(tlane, 128, pt);   // P^T over K's columns
+    st_row_split(tlane, 256, dst);  // dS^T over V's columns
+    publish_operands();
+    if (r == 0) {
+      mma3(tmem, 0, 128, 192, dyt_hi, dyt_lo, Tp / 8, HS);  // dV = P^T dY
+      mma3(tmem, 64, 256, 320, qt_hi, qt_lo, Tp / 8, HS);   // dK = dS^T Q
+      mma_commit(&bars[1]);
+    }
+    mma_phase = 1;
+    ok = wait_all(&bars[1], 1, abort_flag, p.err);
+  }
+  if (ok) {
+    tc_fence_after();
+    float g[64];
+    ld_row64_tmem(tlane + 64, g);
+    if (valid) store_grad_row(p, row0 + r, C + h * HS, g);
+    ld_row64_tmem(tlane + 0, g);
+    if (valid) store_grad_row(p, row0 + r, 2 * C + h * HS, g);
+  } else {
+    drain(bars, mma_phase);
+  }
+  epilogue_free<DKV_TILES>(smem, tmem, 512);
+}
+
+}  // namespace atf
