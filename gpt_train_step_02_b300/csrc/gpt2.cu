@@ -72,6 +72,8 @@ struct Plan {
   // bf16 logits, their per-block softmax statistics and the targets' fp32
   // logits (forward with targets, bf16 matmuls)
   size_t logits_bf, xstats, tlogit;
+  // one byte per wte row: 1 when the batch's tokens touch it (fused step)
+  size_t rowmask;
   // Llama-style variant: (cos, sin) per position and pair, and a zero vector
   // standing in for the biases the variant does not have
   size_t rope, zero_bias;
@@ -189,6 +191,7 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->logits_bf = take(BT * Vp * H);
   p->xstats = take(H ? BT * xstats_pitch(Vp) * sizeof(float2) : 0);
   p->tlogit = take(H ? BT * F : 0);
+  p->rowmask = take(Vp);
   const size_t ll = c->llama ? 1 : 0;
   p->rope = take(ll * (size_t)maxT * (C / NH / 2) * 2 * F);
   p->zero_bias = take(ll * 4 * C * F);
@@ -224,6 +227,7 @@ struct gpt2_t {
   float2* xstats;       // its per-block softmax statistics, xstats_pitch(Vp) per row
   float* tlogit;        // the targets' fp32 logits
   int logits_in_bf;     // 1: the last forward's logits are in logits_bf (bf16), 0: in logits (fp32)
+  uint8_t* rowmask;     // per wte row: touched by the batch's tokens (fused step)
   float* hparams;
   float2* rope;       // [maxT][hs/2] (cos, sin) of t * 10000^(-2i/hs) (Llama-style variant)
   float* zero_bias;   // 4C zeros: the bias operand of the variant's linear layers
@@ -973,9 +977,8 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
     p.B = B; p.T = T; p.C = C; p.NH = NH;
     p.scale = 1.0f / sqrtf((float)hs);
     p.qkv = qkv; p.dy = dy; p.y = atty; p.out = dqkv; p.out_bf = dqkv_bf; p.lse = (float*)lse; p.err = err;
-    launch_k(atf::attn_bwd_dq_tf32_kernel, dim3(NH, B), atf::THREADS, atf::DQ_SMEM, s, tq, p);
-    launch_k(atf::attn_bwd_dkv_tf32_kernel, dim3(NH, B), atf::THREADS, atf::DKV_SMEM, s, tq, td, p);
-    return 2;
+    launch_k(atf::attn_bwd_tf32_kernel, dim3(NH, B, 2), atf::THREADS, atf::BWD_SMEM, s, tq, td, p);
+    return 1;
   }
   if (!tc_path && T <= atts::T_MAX && hs == atts::HS) {  // short sequences: one launch, D formed in the kernel
     if (!dqkv || colsum) return -1;
@@ -1088,11 +1091,8 @@ static int set_kernel_attributes() {
       e = cudaFuncSetAttribute(atf::attn_fwd_tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)atf::FWD_SMEM);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(atf::attn_bwd_dq_tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)atf::DQ_SMEM);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(atf::attn_bwd_dkv_tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)atf::DKV_SMEM);
+      e = cudaFuncSetAttribute(atf::attn_bwd_tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)atf::BWD_SMEM);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(atts::attn_fwd_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)atts::FWD_SMEM);
@@ -1260,6 +1260,8 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
 }
 
 static int update_layer(gpt2_t* m, int l);
+static int mark_touched_rows(gpt2_t* m, int N);
+static int update_wte_untouched(gpt2_t* m);
 
 static int enqueue_backward(gpt2_t* m) {
   const gpt2_config& c = m->cfg;
@@ -1278,9 +1280,17 @@ static int enqueue_backward(gpt2_t* m) {
   // the tensor-core attention backward (bf16, hs = 64, T % 128 == 0) takes the QKV bias column sums
   const bool fuse_qkvb = bf && !ll && C / c.num_heads == tca::HS && T % tca::BQ == 0;
   auto gbias = [&](int which, size_t off) -> float* { return ll ? nullptr : G[which] + off; };
+  if (m->upd_layers) {
+    int rc = mark_touched_rows(m, N);
+    if (rc) return rc;
+  }
   // LM head (tied to wte): dlnf = dlogits wte; dwte += dlogits^T lnf
   mm_dx(m, m->dln, nullptr, {m->dlogits, m->dlogits_bf}, wparam(m, P_WTE, 0), N, C, Vp, nullptr);
   mm_dw(m, G[P_WTE], {m->dlogits, m->dlogits_bf}, {m->lnf, m->lnf_bf}, N, C, Vp);
+  if (m->upd_layers) {  // nothing later reads wte, and the untouched rows' gradients are final
+    int rc = update_wte_untouched(m);
+    if (rc) return rc;
+  }
   CCHECK(m, cudaMemsetAsync(m->dres, 0, (size_t)N * C * sizeof(float), s));
   LayerActs last = layer_acts(m, L - 1);
   // the column sums of this dres are the last layer's MLP output-projection bias gradient
@@ -1388,10 +1398,33 @@ static int enqueue_update(gpt2_t* m) {
   return launch_adamw(m, &off, &cnt, 1, m->stream);
 }
 
-// AdamW of layer l's twelve tensors, once their gradients are complete: on
-// the update side stream after everything enqueued so far on the main stream
-// and both gradient side streams (on the main stream when side streams are
-// off).  Called by the fused step's backward after layer l's last kernel.
+// The update side stream continues after everything enqueued so far on the
+// main stream and both gradient side streams; returns the stream to launch
+// on (the main stream when side streams are off).
+static cudaStream_t upd_fork(gpt2_t* m) {
+  if (!side_on(m) || !m->side_u) return m->stream;
+  const int f = m->sev_next;
+  m->sev_next = (m->sev_next + 1) % SIDE_EVENTS;
+  if (cudaEventRecord(m->sev[f], m->stream) != cudaSuccess || cudaStreamWaitEvent(m->side_u, m->sev[f], 0) != cudaSuccess ||
+      (m->side_last >= 0 && cudaStreamWaitEvent(m->side_u, m->sev[m->side_last], 0) != cudaSuccess) ||
+      (m->side_w_last >= 0 && cudaStreamWaitEvent(m->side_u, m->sev[m->side_w_last], 0) != cudaSuccess)) {
+    m->poisoned = GPT2_ERR_CUDA;
+    return m->stream;
+  }
+  return m->side_u;
+}
+
+static int upd_done(gpt2_t* m, cudaStream_t st) {
+  if (st == m->stream) return m->poisoned ? m->poisoned : GPT2_OK;
+  const int d = m->sev_next;
+  m->sev_next = (m->sev_next + 1) % SIDE_EVENTS;
+  CCHECK(m, cudaEventRecord(m->sev[d], st));
+  m->side_u_last = d;
+  return GPT2_OK;
+}
+
+// AdamW of layer l's twelve tensors, once their gradients are complete.
+// Called by the fused step's backward after layer l's last kernel.
 static int update_layer(gpt2_t* m, int l) {
   static const int T[12] = {P_LN1W, P_LN1B, P_QKVW, P_QKVB, P_ATTPROJW, P_ATTPROJB,
                             P_LN2W, P_LN2B, P_FCW,  P_FCB,  P_FCPROJW,  P_FCPROJB};
@@ -1401,28 +1434,55 @@ static int update_layer(gpt2_t* m, int l) {
     cnt[i] = m->psize[T[i]] / L;
     off[i] = poff(m, T[i]) + l * cnt[i];
   }
-  if (!side_on(m) || !m->side_u) return launch_adamw(m, off, cnt, 12, m->stream);
-  const int f = m->sev_next, d = (m->sev_next + 1) % SIDE_EVENTS;
-  m->sev_next = (m->sev_next + 2) % SIDE_EVENTS;
-  CCHECK(m, cudaEventRecord(m->sev[f], m->stream));
-  CCHECK(m, cudaStreamWaitEvent(m->side_u, m->sev[f], 0));
-  if (m->side_last >= 0) CCHECK(m, cudaStreamWaitEvent(m->side_u, m->sev[m->side_last], 0));
-  if (m->side_w_last >= 0) CCHECK(m, cudaStreamWaitEvent(m->side_u, m->sev[m->side_w_last], 0));
-  int rc = launch_adamw(m, off, cnt, 12, m->side_u);
-  if (rc) return rc;
-  CCHECK(m, cudaEventRecord(m->sev[d], m->side_u));
-  m->side_u_last = d;
+  cudaStream_t st = upd_fork(m);
+  int rc = launch_adamw(m, off, cnt, 12, st);
+  return rc ? rc : upd_done(m, st);
+}
+
+// The fused step's wte rows: those no token of the batch touches have their
+// final gradient once the LM head's weight gradient is done, so they are
+// updated right after it (part 1); the rows the tokens touch also get the
+// embedding gradient, at the end of the backward (part 2, update_rest).
+static int mark_touched_rows(gpt2_t* m, int N) {
+  CCHECK(m, cudaMemsetAsync(m->rowmask, 0, (size_t)m->cfg.padded_vocab_size, m->stream));
+  launch_k(mark_rows_kernel, grid_for(N, 256, 64), 256, 0, m->stream, (const int*)m->tokens, N, m->cfg.vocab_size,
+           m->rowmask);
+  m->launches++;
+  KCHECK(m);
   return GPT2_OK;
 }
 
-// The rest of the fused step's AdamW (the tensors outside the layers: wte,
-// wpe, the final layernorm), after joining the per-layer updates.
-static int update_rest(gpt2_t* m) {
+static int update_wte_untouched(gpt2_t* m) {
+  cudaStream_t st = upd_fork(m);
+  const int C = m->cfg.channels, Vp = m->cfg.padded_vocab_size;
+  const bool on_main = st == m->stream;
+  if (on_main) timer_begin(m, TK_ADAMW, 4.0 * (double)Vp * C * (7.0 + (m->params_bf ? 0.5 : 0.0)));
+  launch_k(adamw_rows_kernel, grid_for((long long)Vp * C / 4, 256, 148 * 8), 256, 0, st, m->params,
+           (const float*)m->grads, m->m, m->v, poff(m, P_WTE), Vp, C, (const uint8_t*)m->rowmask, 0,
+           (const float*)m->hparams, m->params_bf);
+  if (on_main) timer_end(m, TK_ADAMW);
+  m->launches++;
+  KCHECK(m);
+  return upd_done(m, st);
+}
+
+// The rest of the fused step's AdamW, after joining the earlier updates: the
+// wte rows the batch's tokens touch (one CTA per sorted token key; the CTA at
+// the first key of each id updates its row), then wpe and the final
+// layernorm.
+static int update_rest(gpt2_t* m, int N) {
   if (m->side_u_last >= 0) CCHECK(m, cudaStreamWaitEvent(m->stream, m->sev[m->side_u_last], 0));
   m->side_u_last = -1;
-  const long long off[4] = {poff(m, P_WTE), poff(m, P_WPE), poff(m, P_LNFW), poff(m, P_LNFB)};
-  const long long cnt[4] = {m->psize[P_WTE], m->psize[P_WPE], m->psize[P_LNFW], m->psize[P_LNFB]};
-  return launch_adamw(m, off, cnt, 4, m->stream);
+  const int C = m->cfg.channels;
+  timer_begin(m, TK_ADAMW, 0.0);  // the touched rows' bytes are not known on the host: counted as 0
+  launch_k(adamw_sorted_rows_kernel, N, 256, 0, m->stream, m->params, (const float*)m->grads, m->m, m->v,
+           poff(m, P_WTE), C, (const uint32_t*)m->sorted, (const float*)m->hparams, m->params_bf);
+  timer_end(m, TK_ADAMW);
+  m->launches++;
+  KCHECK(m);
+  const long long off[3] = {poff(m, P_WPE), poff(m, P_LNFW), poff(m, P_LNFB)};
+  const long long cnt[3] = {m->psize[P_WPE], m->psize[P_LNFW], m->psize[P_LNFB]};
+  return launch_adamw(m, off, cnt, 3, m->stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -1477,6 +1537,7 @@ static void carve(gpt2_t* m) {
   CARVE_BF(dres_bf); CARVE_BF(dfch_bf); CARVE_BF(dqkv_bf); CARVE_BF(datty_bf); CARVE_BF(logits_bf);
   m->xstats = m->params_bf ? (float2*)(a + p.xstats) : nullptr;
   m->tlogit = m->params_bf ? (float*)(a + p.tlogit) : nullptr;
+  m->rowmask = (uint8_t*)(a + p.rowmask);
   m->rope = m->cfg.llama ? (float2*)(a + p.rope) : nullptr;
   m->zero_bias = m->cfg.llama ? (float*)(a + p.zero_bias) : nullptr;
 #undef CARVE_BF
@@ -1787,7 +1848,7 @@ static int enqueue_step(gpt2_t* m, int B, int T) {
   m->upd_layers = 0;
   m->grad_accumulate = 1;
   if (rc) return rc;
-  return update_rest(m);
+  return update_rest(m, B * T);
 }
 
 static int run_step(gpt2_t* m, int B, int T, int use_graph) {

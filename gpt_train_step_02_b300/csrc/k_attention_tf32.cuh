@@ -14,8 +14,10 @@
 // dv = P^T dy.  Exponentials use expf (the fp32 workloads are compared step
 // by step with the oracle).
 //
-// One CTA of 128 threads per (head, batch); thread r owns TMEM lane r, i.e.
-// row r of every 128-row accumulator (rows >= T are padding).  Operands:
+// One CTA of 256 threads per (head, batch).  Thread r < 64 (warps 0-1) owns
+// TMEM lane r, i.e. row r of every 128-row accumulator (rows >= T are
+// padding; lanes 64..127 are never written or read); all eight warps share
+// the shared-memory passes (splits, transposes).  Operands:
 //  - A operands (the rows the CTA's threads own) go from registers to TMEM
 //    (tcgen05.st; row in the lane, one K value per column);
 //  - B operands sit in shared memory as 64 x 64 fp32 tiles, K-major with the
@@ -50,7 +52,8 @@ using tc::tmem_st16;
 
 constexpr int T_MAX = 64;                 // longest sequence
 constexpr int HS = 64;                    // head size
-constexpr int THREADS = 128;              // one thread per TMEM lane
+constexpr int THREADS = 256;              // 8 warps share the shared-memory passes
+constexpr int ROW_THREADS = 64;           // warps 0-1 own rows 0..63 (TMEM lanes 0..63)
 constexpr int TILE_FLOATS = 64 * 64;      // one 64 x 64 fp32 B tile
 constexpr int TILE_BYTES = TILE_FLOATS * 4;  // 16 KB
 constexpr int BOX_BYTES = TILE_BYTES / 2;    // one 32-column TMA box: 64 rows x 128 B
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   const uint32_t tlane = tmem + ((uint32_t)(r & ~31) << 16);
   const size_t row0 = (size_t)b * T;
   if (r == 0) tma_two_tiles(&tmQKV, k_hi, C + h * HS, v_raw, 2 * C + h * HS, b * T, &bars[0]);
-  {
+  if (r < ROW_THREADS) {
     float q[64];
     ld_row64(p.qkv + (row0 + r) * 3 * C + h * HS, r < T, q);
     st_row_split(tlane, 64, q);
@@ -288,6 +291,7 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   }
   if (ok) {
     tc_fence_after();
+    if (r < ROW_THREADS) {
     float s[64];
     ld_row64_tmem(tlane + 0, s);
     float mx = -INFINITY;
@@ -308,6 +312,7 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
     for (int j = 0; j < 64; j++) s[j] *= inv;
     if (valid) p.lse[((size_t)b * p.NH + h) * T + r] = mx + logf(l);
     st_row_split(tlane, 64, s);  // P over Q's columns: the S MMAs have completed
+    }
     publish_operands();
     if (r == 0) {
       mma3(tmem, 0, 64, 128, vt_hi, vt_lo, Tp / 8, HS);  // O = P V, over S's columns
@@ -318,6 +323,7 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   }
   if (ok) {
     tc_fence_after();
+    if (r < ROW_THREADS) {
     float o[64];
     ld_row64_tmem(tlane + 0, o);
     if (r < T) {
@@ -332,6 +338,7 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
           reinterpret_cast<uint2*>(yb)[q] =
               make_uint2(bf16x2_bits(o[4 * q], o[4 * q + 1]), bf16x2_bits(o[4 * q + 2], o[4 * q + 3]));
       }
+    }
     }
   } else {
     drain(bars, mma_phase);  // a copy or MMA still in flight lands before the CTA's memory is released
@@ -355,14 +362,11 @@ GPT2_DEV void store_grad_row(const Params& p, size_t row, int col, const float* 
 }
 
 // ---------------------------------------------------------------------------
-// backward, query rows: dq.  TMEM: S [0, 64) -> later dQ; dP [64, 128);
+// backward, query rows (blockIdx.z == 0 of the backward kernel): dq.  TMEM: S [0, 64) -> later dQ; dP [64, 128);
 // Q hi/lo [128, 256) -> later dS hi/lo; dY hi/lo [256, 384).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(THREADS) attn_bwd_dq_tf32_kernel(const __grid_constant__ CUtensorMap tmQKV,
-                                                                   const __grid_constant__ Params p) {
-  pdl_launch_dependents();
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV_, const Params& p, uint8_t* smem) {
+  const CUtensorMap& tmQKV = *tmQKV_;
   float* k_hi = reinterpret_cast<float*>(smem);
   float* k_lo = k_hi + TILE_FLOATS;
   float* v_hi = k_lo + TILE_FLOATS;
@@ -381,8 +385,8 @@ __global__ void __launch_bounds__(THREADS) attn_bwd_dq_tf32_kernel(const __grid_
   const size_t row0 = (size_t)b * T;
   const bool valid = r < T;
   if (r == 0) tma_two_tiles(&tmQKV, k_hi, C + h * HS, v_hi, 2 * C + h * HS, b * T, &bars[0]);
-  float Dr, lse_r;
-  {
+  float Dr = 0.f, lse_r = 0.f;
+  if (r < ROW_THREADS) {
     float a[64], c[64];
     ld_row64(p.dy + (row0 + r) * C + h * HS, valid, a);
     ld_row64(p.y + (row0 + r) * C + h * HS, valid, c);
@@ -413,6 +417,7 @@ __global__ void __launch_bounds__(THREADS) attn_bwd_dq_tf32_kernel(const __grid_
   }
   if (ok) {
     tc_fence_after();
+    if (r < ROW_THREADS) {
     float s[64], dp[64];
     ld_row64_tmem(tlane + 0, s);
     ld_row64_tmem(tlane + 64, dp);
@@ -422,6 +427,7 @@ __global__ void __launch_bounds__(THREADS) attn_bwd_dq_tf32_kernel(const __grid_
       s[j] = (valid && j <= r) ? expf(s[j] * p.scale - lse_r) * (dp[j] - Dr) * p.scale : 0.f;
     }
     st_row_split(tlane, 128, s);  // dS over Q's columns
+    }
     publish_operands();
     if (r == 0) {
       mma3(tmem, 0, 128, 192, kt_hi, kt_lo, Tp / 8, HS);  // dQ = dS K, over S's columns
@@ -432,9 +438,11 @@ __global__ void __launch_bounds__(THREADS) attn_bwd_dq_tf32_kernel(const __grid_
   }
   if (ok) {
     tc_fence_after();
-    float g[64];
-    ld_row64_tmem(tlane + 0, g);
-    if (valid) store_grad_row(p, row0 + r, h * HS, g);
+    if (r < ROW_THREADS) {
+      float g[64];
+      ld_row64_tmem(tlane + 0, g);
+      if (valid) store_grad_row(p, row0 + r, h * HS, g);
+    }
   } else {
     drain(bars, mma_phase);
   }
@@ -442,16 +450,13 @@ __global__ void __launch_bounds__(THREADS) attn_bwd_dq_tf32_kernel(const __grid_
 }
 
 // ---------------------------------------------------------------------------
-// backward, key rows: dk and dv.  TMEM: S^T [0, 64) -> later dV;
+// backward, key rows (blockIdx.z == 1): dk and dv.  TMEM: S^T [0, 64) -> later dV;
 // dP^T [64, 128) -> later dK; K hi/lo [128, 256) -> later P^T hi/lo;
 // V hi/lo [256, 384) -> later dS^T hi/lo.  tmDY: dy as (B*T rows, C columns).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(THREADS) attn_bwd_dkv_tf32_kernel(const __grid_constant__ CUtensorMap tmQKV,
-                                                                    const __grid_constant__ CUtensorMap tmDY,
-                                                                    const __grid_constant__ Params p) {
-  pdl_launch_dependents();
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV_, const CUtensorMap* tmDY_, const Params& p, uint8_t* smem) {
+  const CUtensorMap& tmQKV = *tmQKV_;
+  const CUtensorMap& tmDY = *tmDY_;
   float* q_hi = reinterpret_cast<float*>(smem);
   float* q_lo = q_hi + TILE_FLOATS;
   float* dy_hi = q_lo + TILE_FLOATS;
@@ -480,7 +485,7 @@ __global__ void __launch_bounds__(THREADS) attn_bwd_dkv_tf32_kernel(const __grid
     tma_load_2d(dy_hi, &tmDY, h * HS, b * T, &bars[0]);
     tma_load_2d(reinterpret_cast<uint8_t*>(dy_hi) + BOX_BYTES, &tmDY, h * HS + 32, b * T, &bars[0]);
   }
-  {
+  if (r < ROW_THREADS) {
     float a[64], c[64];
     // row r as a query: D_r = dy_r . y_r and lse_r, shared with every key row
     ld_row64(p.dy + (row0 + r) * C + h * HS, valid, a);
@@ -488,10 +493,8 @@ __global__ void __launch_bounds__(THREADS) attn_bwd_dkv_tf32_kernel(const __grid
     float D = 0.f;
 #pragma unroll
     for (int d = 0; d < 64; d++) D = fmaf(a[d], c[d], D);
-    if (r < 64) {
-      D_s[r] = D;
-      lse_s[r] = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
-    }
+    D_s[r] = D;
+    lse_s[r] = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
     // row r as a key: K and V into TMEM
     ld_row64(p.qkv + (row0 + r) * 3 * C + C + h * HS, valid, a);
     st_row_split(tlane, 128, a);
@@ -519,6 +522,7 @@ __global__ void __launch_bounds__(THREADS) attn_bwd_dkv_tf32_kernel(const __grid
   }
   if (ok) {
     tc_fence_after();
+    if (r < ROW_THREADS) {
     float pt[64], dst[64];
     ld_row64_tmem(tlane + 0, pt);
     ld_row64_tmem(tlane + 64, dst);
@@ -532,6 +536,7 @@ __global__ void __launch_bounds__(THREADS) attn_bwd_dkv_tf32_kernel(const __grid
     }
     st_row_split(tlane, 128, pt);   // P^T over K's columns
     st_row_split(tlane, 256, dst);  // dS^T over V's columns
+    }
     publish_operands();
     if (r == 0) {
       mma3(tmem, 0, 128, 192, dyt_hi, dyt_lo, Tp / 8, HS);  // dV = P^T dY
@@ -543,15 +548,33 @@ __global__ void __launch_bounds__(THREADS) attn_bwd_dkv_tf32_kernel(const __grid
   }
   if (ok) {
     tc_fence_after();
-    float g[64];
-    ld_row64_tmem(tlane + 64, g);
-    if (valid) store_grad_row(p, row0 + r, C + h * HS, g);
-    ld_row64_tmem(tlane + 0, g);
-    if (valid) store_grad_row(p, row0 + r, 2 * C + h * HS, g);
+    if (r < ROW_THREADS) {
+      float g[64];
+      ld_row64_tmem(tlane + 64, g);
+      if (valid) store_grad_row(p, row0 + r, C + h * HS, g);
+      ld_row64_tmem(tlane + 0, g);
+      if (valid) store_grad_row(p, row0 + r, 2 * C + h * HS, g);
+    }
   } else {
     drain(bars, mma_phase);
   }
   epilogue_free<DKV_TILES>(smem, tmem, 512);
+}
+
+// The backward: grid (NH, B, 2); the query-row CTAs (z = 0) and the key-row
+// CTAs (z = 1) of every head run side by side.
+constexpr size_t BWD_SMEM = DQ_SMEM > DKV_SMEM ? DQ_SMEM : DKV_SMEM;
+
+__global__ void __launch_bounds__(THREADS) attn_bwd_tf32_kernel(const __grid_constant__ CUtensorMap tmQKV,
+                                                                const __grid_constant__ CUtensorMap tmDY,
+                                                                const __grid_constant__ Params p) {
+  pdl_launch_dependents();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  if (blockIdx.z == 0)
+    bwd_dq(&tmQKV, p, smem);
+  else
+    bwd_dkv(&tmQKV, &tmDY, p, smem);
 }
 
 }  // namespace atf

@@ -274,37 +274,82 @@ struct AdamSegs {
   int n;
 };
 
+// One float4 of AdamW at float4 index i.
+GPT2_DEV void adamw_f4(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
+                       float* __restrict__ v, long long i, const float* __restrict__ hp, uint16_t* __restrict__ pbf16) {
+  const float lr = hp[0], b1 = hp[1], b2 = hp[2], eps = hp[3], wd = hp[4], c1inv = hp[5], c2inv = hp[6];
+  float4 pp = reinterpret_cast<float4*>(p)[i];
+  float4 gg = reinterpret_cast<const float4*>(g)[i];
+  float4 mm = reinterpret_cast<float4*>(m)[i];
+  float4 vv = reinterpret_cast<float4*>(v)[i];
+  float* P = &pp.x;
+  const float* G = &gg.x;
+  float* Mm = &mm.x;
+  float* Vv = &vv.x;
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    Mm[k] = b1 * Mm[k] + (1.0f - b1) * G[k];
+    Vv[k] = b2 * Vv[k] + (1.0f - b2) * G[k] * G[k];
+    float mh = Mm[k] * c1inv, vh = Vv[k] * c2inv;
+    P[k] = P[k] - lr * (mh / (sqrtf(vh) + eps) + wd * P[k]);
+  }
+  reinterpret_cast<float4*>(p)[i] = pp;
+  reinterpret_cast<float4*>(m)[i] = mm;
+  reinterpret_cast<float4*>(v)[i] = vv;
+  if (pbf16) reinterpret_cast<uint2*>(pbf16)[i] = make_uint2(bf16x2_bits(pp.x, pp.y), bf16x2_bits(pp.z, pp.w));
+}
+
 __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
                              float* __restrict__ v, const __grid_constant__ AdamSegs segs,
                              const float* __restrict__ hp, uint16_t* __restrict__ pbf16) {
   pdl_launch_dependents();
   pdl_wait();
-  const float lr = hp[0], b1 = hp[1], b2 = hp[2], eps = hp[3], wd = hp[4], c1inv = hp[5], c2inv = hp[6];
   const long long total = segs.end4[segs.n - 1];
   int sg = 0;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
     while (e >= segs.end4[sg]) sg++;  // e only grows
-    const long long i = segs.off4[sg] + e - (sg ? segs.end4[sg - 1] : 0);
-    float4 pp = reinterpret_cast<float4*>(p)[i];
-    float4 gg = reinterpret_cast<const float4*>(g)[i];
-    float4 mm = reinterpret_cast<float4*>(m)[i];
-    float4 vv = reinterpret_cast<float4*>(v)[i];
-    float* P = &pp.x;
-    const float* G = &gg.x;
-    float* Mm = &mm.x;
-    float* Vv = &vv.x;
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-      Mm[k] = b1 * Mm[k] + (1.0f - b1) * G[k];
-      Vv[k] = b2 * Vv[k] + (1.0f - b2) * G[k] * G[k];
-      float mh = Mm[k] * c1inv, vh = Vv[k] * c2inv;
-      P[k] = P[k] - lr * (mh / (sqrtf(vh) + eps) + wd * P[k]);
-    }
-    reinterpret_cast<float4*>(p)[i] = pp;
-    reinterpret_cast<float4*>(m)[i] = mm;
-    reinterpret_cast<float4*>(v)[i] = vv;
-    if (pbf16) reinterpret_cast<uint2*>(pbf16)[i] = make_uint2(bf16x2_bits(pp.x, pp.y), bf16x2_bits(pp.z, pp.w));
+    adamw_f4(p, g, m, v, segs.off4[sg] + e - (sg ? segs.end4[sg - 1] : 0), hp, pbf16);
   }
+}
+
+// AdamW of the rows r < nrows of a row-major (nrows, C) tensor at element
+// offset off whose mask byte mask[r] equals want (C % 4 == 0, off % 4 == 0).
+__global__ void adamw_rows_kernel(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
+                                  float* __restrict__ v, long long off, int nrows, int C,
+                                  const uint8_t* __restrict__ mask, int want, const float* __restrict__ hp,
+                                  uint16_t* __restrict__ pbf16) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int C4 = C >> 2;
+  const long long total = (long long)nrows * C4;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
+    if (mask[e / C4] != want) continue;
+    adamw_f4(p, g, m, v, off / 4 + e, hp, pbf16);
+  }
+}
+
+// AdamW of the rows of a (rows, C) tensor at element offset off named by the
+// sorted token keys of the embedding backward (id << 14 | pos):
+// one CTA per key; the CTA at the first key of each id updates that row.
+__global__ void adamw_sorted_rows_kernel(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
+                                         float* __restrict__ v, long long off, int C,
+                                         const uint32_t* __restrict__ sorted, const float* __restrict__ hp,
+                                         uint16_t* __restrict__ pbf16) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int i = blockIdx.x;
+  const uint32_t id = sorted[i] >> 14;
+  if (i > 0 && (sorted[i - 1] >> 14) == id) return;
+  const int C4 = C >> 2;
+  for (int c4 = threadIdx.x; c4 < C4; c4 += blockDim.x) adamw_f4(p, g, m, v, off / 4 + (long long)id * C4 + c4, hp, pbf16);
+}
+
+// mask[ids[i]] = 1 for every i < n (the rows of wte a batch touches)
+__global__ void mark_rows_kernel(const int* __restrict__ ids, int n, int V, uint8_t* __restrict__ mask) {
+  pdl_launch_dependents();
+  pdl_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    mask[min(max(ids[i], 0), V - 1)] = 1;
 }
 
 __global__ void to_bf16_kernel(const float* __restrict__ x, uint16_t* __restrict__ y, long long n) {
