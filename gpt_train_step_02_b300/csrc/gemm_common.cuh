@@ -47,7 +47,14 @@ struct EpiArgs {
   float2* xstats;
   int ldxs;
   float* tlogit;
+  // bf16 in place of the fp32 pre-activation: EPI_BIAS_GELU stores pre(i,j)
+  // at pre_bf (pitch ldpre) instead of (or besides) pre; EPI_DGELU reads R
+  // from Rbf (pitch ldr) when it is set.
+  uint16_t* pre_bf;
+  const uint16_t* Rbf;
 };
+
+GPT2_DEV float bf16_bits_to_float(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
 // The epilogue functions take the kind as a template argument OP when the
 // caller knows it at compile time (straight-line code per kernel
@@ -66,12 +73,13 @@ GPT2_DEV void epi_store(const EpiArgs& e, int i, int j, float acc) {
     case EPI_BIAS_RESID: out = acc + e.bias[j] + e.R[(size_t)i * e.ldr + j]; break;
     case EPI_BIAS_GELU: {
       float h = acc + e.bias[j];
-      e.pre[(size_t)i * e.ldpre + j] = h;
+      if (e.pre) e.pre[(size_t)i * e.ldpre + j] = h;
+      if (e.pre_bf) e.pre_bf[(size_t)i * e.ldpre + j] = to_bf16_bits(h);
       out = e.fast ? gelu_fwd_fast(h) : gelu_fwd(h);
       break;
     }
     case EPI_DGELU: {
-      const float r = e.R[(size_t)i * e.ldr + j];
+      const float r = e.Rbf ? bf16_bits_to_float(e.Rbf[(size_t)i * e.ldr + j]) : e.R[(size_t)i * e.ldr + j];
       out = acc * (e.fast ? gelu_grad_fast(r) : gelu_grad(r));
       break;
     }
@@ -93,7 +101,13 @@ GPT2_DEV bool epi_has_input(int op) { return op == EPI_BIAS_RESID || op == EPI_D
 // The input of element block (i, j .. j+3) an epilogue reads (R or C).
 template <int OP = -1>
 GPT2_DEV float4 epi_load_input(const EpiArgs& e, int i, int j) {
-  return epi_kind<OP>(e) == EPI_ACCUM ? ld4(e.C + (size_t)i * e.ldc + j) : ld4(e.R + (size_t)i * e.ldr + j);
+  if (epi_kind<OP>(e) == EPI_ACCUM) return ld4(e.C + (size_t)i * e.ldc + j);
+  if (e.Rbf) {
+    const uint2 h = *reinterpret_cast<const uint2*>(e.Rbf + (size_t)i * e.ldr + j);
+    return make_float4(__uint_as_float(h.x << 16), __uint_as_float(h.x & 0xffff0000u), __uint_as_float(h.y << 16),
+                       __uint_as_float(h.y & 0xffff0000u));
+  }
+  return ld4(e.R + (size_t)i * e.ldr + j);
 }
 
 // Finishes (i, j .. j+3) from the accumulator, the column bias b and the
@@ -109,7 +123,9 @@ GPT2_DEV float4 epi_apply4(const EpiArgs& e, int i, int j, float4 acc, float4 b,
       break;
     case EPI_BIAS_GELU: {
       float4 h = make_float4(acc.x + b.x, acc.y + b.y, acc.z + b.z, acc.w + b.w);
-      st4(e.pre + (size_t)i * e.ldpre + j, h);
+      if (e.pre) st4(e.pre + (size_t)i * e.ldpre + j, h);
+      if (e.pre_bf)
+        *reinterpret_cast<uint2*>(e.pre_bf + (size_t)i * e.ldpre + j) = make_uint2(bf16x2_bits(h.x, h.y), bf16x2_bits(h.z, h.w));
       if (e.fast)
         o = make_float4(gelu_fwd_fast(h.x), gelu_fwd_fast(h.y), gelu_fwd_fast(h.z), gelu_fwd_fast(h.w));
       else

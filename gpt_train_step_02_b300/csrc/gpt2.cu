@@ -144,7 +144,8 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->ln2 = take(L * BT * C * F);
   p->ln2_mean = take(L * BT * F);
   p->ln2_rstd = take(L * BT * F);
-  p->fch = take(L * BT * 4 * C * F);
+  // the MLP pre-activation: fp32, or bf16 with bf16 matmuls (only gelu' reads it)
+  p->fch = take(L * BT * 4 * C * (c->gemm_precision == GPT2_PREC_BF16 ? 2 : F));
   p->fchg = take(L * BT * 4 * C * F);
   p->res3 = take(L * BT * C * F);
   p->lnf = take(BT * C * F);
@@ -681,6 +682,7 @@ static EpiArgs epi_args(float* C, long long ldc, int epi, const float* bias = nu
   e.Cbf = Cbf; e.ldcbf = ldcbf; e.fast = 0;
   e.colsum = nullptr; e.ldcs = 0;
   e.targets = nullptr; e.V = 0; e.xstats = nullptr; e.ldxs = 0; e.tlogit = nullptr;
+  e.pre_bf = nullptr; e.Rbf = nullptr;
   uintptr_t addr = (uintptr_t)C | (uintptr_t)bias | (uintptr_t)R | (uintptr_t)pre | (uintptr_t)Cbf;
   e.vec4 = (addr & 15) == 0 && (ldc & 3) == 0 && (ldr & 3) == 0 && (ldpre & 3) == 0 && (ldcbf & 7) == 0;
   return e;
@@ -694,8 +696,10 @@ struct Opnd {
 
 // linear layer y = x W^T + b with x (N, IC), W (OC, IC); ybf: optional bf16 copy of y
 static void mm_forward(gpt2_t* m, float* out, uint16_t* outbf, Opnd x, Opnd W, const float* bias, int N, int IC,
-                       int OC, int epi, const float* R, float* pre) {
+                       int OC, int epi, const float* R, float* pre, uint16_t* pre_bf = nullptr) {
   MatmulDesc d = {N, OC, IC, x.f, IC, 1, W.f, IC, 1, epi_args(out, OC, epi, bias, R, OC, pre, OC, outbf, OC), x.h, W.h};
+  d.epi.pre_bf = pre_bf;
+  if ((uintptr_t)pre_bf & 7) d.epi.vec4 = 0;
   matmul(m, d);
 }
 
@@ -750,9 +754,13 @@ static int side_join(gpt2_t* m) {
 }
 
 static void mm_dx(gpt2_t* m, float* dx, uint16_t* dxbf, Opnd dy, Opnd W, int N, int IC, int OC, const float* pre,
-                  float* colsum = nullptr) {
+                  float* colsum = nullptr, const uint16_t* pre_bf = nullptr) {
   MatmulDesc d = {N,    IC,   OC,   dy.f, OC, 1, W.f, IC, 0,
-                  epi_args(dx, IC, pre ? EPI_DGELU : EPI_STORE, nullptr, pre, IC, nullptr, 0, dxbf, IC), dy.h, W.h};
+                  epi_args(dx, IC, (pre || pre_bf) ? EPI_DGELU : EPI_STORE, nullptr, pre, IC, nullptr, 0, dxbf, IC),
+                  dy.h, W.h};
+  d.epi.Rbf = pre_bf;
+  if (pre_bf) d.epi.ldr = IC;
+  if ((uintptr_t)pre_bf & 7) d.epi.vec4 = 0;
   d.epi.colsum = colsum;
   d.epi.ldcs = IC;
   if (colsum == m->scratch) side_wait(m, &m->rd_scratch);
@@ -1131,6 +1139,7 @@ struct LayerActs {
   float *ln1, *qkv, *atty, *lse, *res2, *ln2, *fch, *fchg, *res3;
   float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd;
   uint16_t *ln1_bf, *qkv_bf, *atty_bf, *ln2_bf, *fchg_bf;
+  uint16_t* fch_bf;  // the pre-activation in bf16 (bf16 matmuls; fch is then NULL)
 };
 
 static LayerActs layer_acts(gpt2_t* m, int l) {
@@ -1156,6 +1165,8 @@ static LayerActs layer_acts(gpt2_t* m, int l) {
   a.atty_bf = bf ? m->atty_bf + l * cap * C : nullptr;
   a.ln2_bf = bf ? m->ln2_bf + l * cap * C : nullptr;
   a.fchg_bf = bf ? m->fchg_bf + l * cap * 4 * C : nullptr;
+  a.fch_bf = bf ? (uint16_t*)m->fch + l * cap * 4 * C : nullptr;
+  if (bf) a.fch = nullptr;
   return a;
 }
 
@@ -1208,7 +1219,7 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
     ln_forward(m, bf ? nullptr : a.ln2, a.ln2_bf, a.ln2_mean, a.ln2_rstd, a.res2, m->P[P_LN2W] + (size_t)l * C,
                m->P[P_LN2B] + (size_t)l * C, N);
     mm_forward(m, bf ? nullptr : a.fchg, a.fchg_bf, {a.ln2, a.ln2_bf}, wparam(m, P_FCW, l * 4 * CC),
-               bias(P_FCB, (size_t)l * 4 * C), N, C, 4 * C, EPI_BIAS_GELU, nullptr, a.fch);
+               bias(P_FCB, (size_t)l * 4 * C), N, C, 4 * C, EPI_BIAS_GELU, nullptr, a.fch, a.fch_bf);
     mm_forward(m, a.res3, nullptr, {a.fchg, a.fchg_bf}, wparam(m, P_FCPROJW, l * 4 * CC),
                bias(P_FCPROJB, (size_t)l * C), N, 4 * C, C, EPI_BIAS_RESID, a.res2, nullptr);
   }
@@ -1306,7 +1317,7 @@ static int enqueue_backward(gpt2_t* m) {
     side_wait(m, &m->rd_dfch);  // dfch is overwritten here
     side_wait(m, &m->wd_dfch);
     mm_dx(m, bf && (fuse_fcb || ll) ? nullptr : m->dfch, m->dfch_bf, dres, wparam(m, P_FCPROJW, l * 4 * CC), N, 4 * C, C,
-          a.fch, fuse_fcb ? m->scratch : nullptr);
+          a.fch, fuse_fcb ? m->scratch : nullptr, a.fch_bf);
     // MLP input projection: fch = ln2 fcw^T + fcb
     mm_dw_side(m, G[P_FCW] + l * 4 * CC, dfch, {a.ln2, a.ln2_bf}, N, C, 4 * C, &m->wd_dfch);
     if (fuse_fcb) bias_finish(m, G[P_FCB] + (size_t)l * 4 * C, ceil_div(N, 32), 4 * C);

@@ -53,10 +53,16 @@ using tc::tmem_st16;
 constexpr int T_MAX = 64;                 // longest sequence
 constexpr int HS = 64;                    // head size
 constexpr int THREADS = 256;              // 8 warps share the shared-memory passes
-constexpr int ROW_THREADS = 64;           // warps 0-1 own rows 0..63 (TMEM lanes 0..63)
 constexpr int TILE_FLOATS = 64 * 64;      // one 64 x 64 fp32 B tile
 constexpr int TILE_BYTES = TILE_FLOATS * 4;  // 16 KB
 constexpr int BOX_BYTES = TILE_BYTES / 2;    // one 32-column TMA box: 64 rows x 128 B
+
+// Row ownership: warps 0, 1, 4 and 5 (the ones that may access TMEM lanes
+// 0..63) own the 64 rows, two threads per row: row 32 (warp % 2) + lane,
+// half warp / 4 = columns [32 half, 32 half + 32) of every 64-wide row.
+GPT2_DEV bool row_owner() { return ((threadIdx.x >> 5) & 2) == 0; }
+GPT2_DEV int own_row() { return 32 * ((threadIdx.x >> 5) & 1) + (threadIdx.x & 31); }
+GPT2_DEV int own_half() { return threadIdx.x >> 7; }
 
 // float offset of K value k of row n in a swizzled 64 x 64 K-major tile
 GPT2_DEV int sw(int n, int k) { return (k >> 5) * 2048 + n * 32 + ((((k & 31) >> 2) ^ (n & 7)) << 2) + (k & 3); }
@@ -93,26 +99,27 @@ GPT2_DEV void mma3(uint32_t tmem, int d_col, int a_hi, int a_lo, const float* b_
   }
 }
 
-// 64 values of this thread's row into TMEM columns col .. col+63 (hi) and
-// col + 64 .. col + 127 (lo) of its lane.
-GPT2_DEV void st_row_split(uint32_t tlane, int col, const float* v) {
+// This thread's 32 values of its row (columns [32 half, +32) of a 64-wide
+// operand) into TMEM: hi halves at columns col + 32 half .., lo halves at
+// col + 64 + 32 half ..
+GPT2_DEV void st_half_split(uint32_t tlane, int col, int half, const float* v) {
 #pragma unroll
-  for (int g = 0; g < 4; g++) {
+  for (int g = 0; g < 2; g++) {
     float hv[16], lv[16];
 #pragma unroll
     for (int k = 0; k < 16; k++) {
       hv[k] = tf32_hi(v[16 * g + k]);
       lv[k] = v[16 * g + k] - hv[k];
     }
-    tmem_st16(tlane + (uint32_t)(col + 16 * g), hv);
-    tmem_st16(tlane + (uint32_t)(col + 64 + 16 * g), lv);
+    tmem_st16(tlane + (uint32_t)(col + 32 * half + 16 * g), hv);
+    tmem_st16(tlane + (uint32_t)(col + 64 + 32 * half + 16 * g), lv);
   }
 }
 
-// 64 floats of row src (16-byte aligned) into v, or zeros when !valid.
-GPT2_DEV void ld_row64(const float* src, bool valid, float* v) {
+// 32 floats at src (16-byte aligned) into v, or zeros when !valid.
+GPT2_DEV void ld_half32(const float* src, bool valid, float* v) {
 #pragma unroll
-  for (int q = 0; q < 16; q++) {
+  for (int q = 0; q < 8; q++) {
     const float4 x = valid ? __ldg(reinterpret_cast<const float4*>(src) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
     v[4 * q] = x.x;
     v[4 * q + 1] = x.y;
@@ -121,9 +128,17 @@ GPT2_DEV void ld_row64(const float* src, bool valid, float* v) {
   }
 }
 
-GPT2_DEV void ld_row64_tmem(uint32_t taddr, float* v) {
-  tmem_ld32(taddr, v);
-  tmem_ld32(taddr + 32, v + 32);
+// 32 floats to dst (16-byte aligned), plus their bf16 copy at dbf when set.
+GPT2_DEV void st_half32(float* dst, uint16_t* dbf, const float* v) {
+#pragma unroll
+  for (int q = 0; q < 8; q++)
+    reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  if (dbf) {
+#pragma unroll
+    for (int q = 0; q < 8; q++)
+      reinterpret_cast<uint2*>(dbf)[q] =
+          make_uint2(bf16x2_bits(v[4 * q], v[4 * q + 1]), bf16x2_bits(v[4 * q + 2], v[4 * q + 3]));
+  }
 }
 
 // In-place split of a TMA-written tile: hi stays, lo goes to lo.
@@ -156,6 +171,23 @@ GPT2_DEV void publish_operands() {
   tc_fence_after();
 }
 
+// Shared-memory layout (from a 1024-byte aligned base) of each kernel: NT
+// tiles, two mbarriers, the TMEM slot and the abort flag, then the row
+// exchange area: xa[2][64], xb[2][64] (per-half partial results of each row)
+// and lse_s[64]; + 1 KB alignment slack.
+template <int NT>
+struct Smem {
+  static constexpr int OFF_BAR = NT * TILE_BYTES;
+  static constexpr int OFF_VEC = OFF_BAR + 64;
+  static constexpr int BYTES = OFF_VEC + 5 * 64 * 4 + 1024;
+};
+constexpr int FWD_TILES = 5;  // K (hi, lo), V raw, V^T (hi, lo)
+constexpr int DQ_TILES = 6;   // K (hi, lo), V (hi, lo), K^T (hi, lo)
+constexpr int DKV_TILES = 8;  // Q (hi, lo), dY (hi, lo), Q^T (hi, lo), dY^T (hi, lo)
+constexpr size_t FWD_SMEM = Smem<FWD_TILES>::BYTES;
+constexpr size_t DQ_SMEM = Smem<DQ_TILES>::BYTES;
+constexpr size_t DKV_SMEM = Smem<DKV_TILES>::BYTES;
+
 struct Params {
   int B, T, C, NH;
   float scale;
@@ -168,21 +200,6 @@ struct Params {
   int* err;
 };
 
-// Shared-memory layout (from a 1024-byte aligned base) of each kernel: NT
-// tiles, then two mbarriers and the TMEM slot; + 1 KB alignment slack.
-template <int NT>
-struct Smem {
-  static constexpr int OFF_BAR = NT * TILE_BYTES;
-  static constexpr int OFF_VEC = OFF_BAR + 64;  // two 64-float vectors (lse, D) for the dK/dV kernel
-  static constexpr int BYTES = OFF_VEC + 2 * 64 * 4 + 1024;
-};
-constexpr int FWD_TILES = 5;  // K (hi, lo), V raw, V^T (hi, lo)
-constexpr int DQ_TILES = 6;   // K (hi, lo), V (hi, lo), K^T (hi, lo)
-constexpr int DKV_TILES = 8;  // Q (hi, lo), dY (hi, lo), Q^T (hi, lo), dY^T (hi, lo)
-constexpr size_t FWD_SMEM = Smem<FWD_TILES>::BYTES;
-constexpr size_t DQ_SMEM = Smem<DQ_TILES>::BYTES;
-constexpr size_t DKV_SMEM = Smem<DKV_TILES>::BYTES;
-
 // Common prologue: barriers, TMEM allocation (ncols), PDL wait.
 template <int NT>
 GPT2_DEV uint32_t prologue(uint8_t* smem, int ncols) {
@@ -191,6 +208,7 @@ GPT2_DEV uint32_t prologue(uint8_t* smem, int ncols) {
   if (threadIdx.x == 0) {
     mbar_init(&bars[0], 1);  // TMA
     mbar_init(&bars[1], 1);  // MMA completion
+    *reinterpret_cast<volatile int*>(smem + Smem<NT>::OFF_BAR + 24) = 0;  // abort flag
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (threadIdx.x < 32) {
@@ -201,11 +219,12 @@ GPT2_DEV uint32_t prologue(uint8_t* smem, int ncols) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  return *slot;
+  const uint32_t t = *slot;
+  pdl_wait();
+  return t;
 }
 
-template <int NT>
-GPT2_DEV void epilogue_free(uint8_t* smem, uint32_t tmem, int ncols) {
+GPT2_DEV void epilogue_free(uint32_t tmem, int ncols) {
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) {
@@ -215,13 +234,14 @@ GPT2_DEV void epilogue_free(uint8_t* smem, uint32_t tmem, int ncols) {
 }
 
 // Thread 0 issues the four TMA box loads of two tiles (rows y0 .. y0+63 of
-// map tm, columns x0 .. x0+63 and x1 .. x1+63) onto bar.
-GPT2_DEV void tma_two_tiles(const CUtensorMap* tm, float* t0, int x0, float* t1, int x1, int y0, uint64_t* bar) {
+// maps ta / tb, columns x0 .. x0+63 and x1 .. x1+63) onto bar.
+GPT2_DEV void tma_two_tiles(const CUtensorMap* ta, float* t0, int x0, const CUtensorMap* tb, float* t1, int x1, int y0,
+                            uint64_t* bar) {
   mbar_expect_tx(bar, 2 * TILE_BYTES);
-  tma_load_2d(t0, tm, x0, y0, bar);
-  tma_load_2d(reinterpret_cast<uint8_t*>(t0) + BOX_BYTES, tm, x0 + 32, y0, bar);
-  tma_load_2d(t1, tm, x1, y0, bar);
-  tma_load_2d(reinterpret_cast<uint8_t*>(t1) + BOX_BYTES, tm, x1 + 32, y0, bar);
+  tma_load_2d(t0, ta, x0, y0, bar);
+  tma_load_2d(reinterpret_cast<uint8_t*>(t0) + BOX_BYTES, ta, x0 + 32, y0, bar);
+  tma_load_2d(t1, tb, x1, y0, bar);
+  tma_load_2d(reinterpret_cast<uint8_t*>(t1) + BOX_BYTES, tb, x1 + 32, y0, bar);
 }
 
 // The abort path: the TMA copies and the last committed MMA batch (phase
@@ -234,9 +254,10 @@ GPT2_DEV void drain(uint64_t* bars, int mma_phase) {
   }
 }
 
-// A bounded wait on bar (phase) by every thread, decided collectively.
+// A bounded wait on bar (phase) by thread 0; the CTA takes the result
+// together at the barrier.
 GPT2_DEV bool wait_all(uint64_t* bar, uint32_t phase, volatile int* abort_flag, int* err) {
-  const bool ok = mbar_wait(bar, phase, abort_flag, err);
+  const bool ok = threadIdx.x == 0 ? mbar_wait(bar, phase, abort_flag, err) : true;
   return __syncthreads_and(ok) != 0;
 }
 
@@ -256,19 +277,22 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   float* vt_lo = vt_hi + TILE_FLOATS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<FWD_TILES>::OFF_BAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<FWD_TILES>::OFF_BAR + 24);
-  if (threadIdx.x == 0) *abort_flag = 0;
+  float* xa = reinterpret_cast<float*>(smem + Smem<FWD_TILES>::OFF_VEC);  // [2][64] half-row maxima
+  float* xb = xa + 128;                                                      // [2][64] half-row sums
   const uint32_t tmem = prologue<FWD_TILES>(smem, 256);
-  pdl_wait();
 
-  const int h = blockIdx.x, b = blockIdx.y, T = p.T, C = p.C, r = threadIdx.x;
+  const int h = blockIdx.x, b = blockIdx.y, T = p.T, C = p.C;
   const int Tp = (T + 15) & ~15;  // keys padded to the MMA's N granularity
-  const uint32_t tlane = tmem + ((uint32_t)(r & ~31) << 16);
+  const bool owner = row_owner();
+  const int r = own_row(), hf = own_half();
+  const uint32_t tlane = tmem + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16);
   const size_t row0 = (size_t)b * T;
-  if (r == 0) tma_two_tiles(&tmQKV, k_hi, C + h * HS, v_raw, 2 * C + h * HS, b * T, &bars[0]);
-  if (r < ROW_THREADS) {
-    float q[64];
-    ld_row64(p.qkv + (row0 + r) * 3 * C + h * HS, r < T, q);
-    st_row_split(tlane, 64, q);
+  const bool valid = owner && r < T;
+  if (threadIdx.x == 0) tma_two_tiles(&tmQKV, k_hi, C + h * HS, &tmQKV, v_raw, 2 * C + h * HS, b * T, &bars[0]);
+  if (owner) {
+    float q[32];
+    ld_half32(p.qkv + (row0 + r) * 3 * C + h * HS + 32 * hf, valid, q);
+    st_half_split(tlane, 64, hf, q);
   }
   int mma_phase = -1;
   bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
@@ -282,7 +306,7 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
       vt_lo[sw(d, key)] = x - hi;
     }
     publish_operands();
-    if (r == 0) {
+    if (threadIdx.x == 0) {
       mma3(tmem, 0, 64, 128, k_hi, k_lo, HS / 8, Tp);  // S = Q K^T
       mma_commit(&bars[1]);
     }
@@ -291,30 +315,40 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   }
   if (ok) {
     tc_fence_after();
-    if (r < ROW_THREADS) {
-    float s[64];
-    ld_row64_tmem(tlane + 0, s);
+    float s[32];
     float mx = -INFINITY;
+    if (owner) {
+      tmem_ld32(tlane + (uint32_t)(32 * hf), s);
 #pragma unroll
-    for (int j = 0; j < 64; j++) {
-      s[j] = (j <= r && j < T) ? s[j] * p.scale : -INFINITY;
-      mx = fmaxf(mx, s[j]);
+      for (int k = 0; k < 32; k++) {
+        const int j = 32 * hf + k;
+        s[k] = (j <= r && j < T) ? s[k] * p.scale : -INFINITY;
+        mx = fmaxf(mx, s[k]);
+      }
+      xa[hf * 64 + r] = mx;
     }
+    __syncthreads();
     float l = 0.f;
+    if (owner) {
+      mx = fmaxf(xa[r], xa[64 + r]);
 #pragma unroll
-    for (int j = 0; j < 64; j++) {
-      s[j] = s[j] == -INFINITY ? 0.f : expf(s[j] - mx);
-      l += s[j];
+      for (int k = 0; k < 32; k++) {
+        s[k] = s[k] == -INFINITY ? 0.f : expf(s[k] - mx);
+        l += s[k];
+      }
+      xb[hf * 64 + r] = l;
     }
-    const bool valid = r < T;
-    const float inv = valid ? 1.0f / l : 0.f;
+    __syncthreads();
+    if (owner) {
+      l = xb[r] + xb[64 + r];
+      const float inv = valid ? 1.0f / l : 0.f;
 #pragma unroll
-    for (int j = 0; j < 64; j++) s[j] *= inv;
-    if (valid) p.lse[((size_t)b * p.NH + h) * T + r] = mx + logf(l);
-    st_row_split(tlane, 64, s);  // P over Q's columns: the S MMAs have completed
+      for (int k = 0; k < 32; k++) s[k] *= inv;
+      if (valid && hf == 0) p.lse[((size_t)b * p.NH + h) * T + r] = mx + logf(l);
+      st_half_split(tlane, 64, hf, s);  // P over Q's columns: the S MMAs have completed
     }
     publish_operands();
-    if (r == 0) {
+    if (threadIdx.x == 0) {
       mma3(tmem, 0, 64, 128, vt_hi, vt_lo, Tp / 8, HS);  // O = P V, over S's columns
       mma_commit(&bars[1]);
     }
@@ -323,79 +357,56 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   }
   if (ok) {
     tc_fence_after();
-    if (r < ROW_THREADS) {
-    float o[64];
-    ld_row64_tmem(tlane + 0, o);
-    if (r < T) {
-      float* yr = p.out + (row0 + r) * C + h * HS;
-#pragma unroll
-      for (int q = 0; q < 16; q++)
-        reinterpret_cast<float4*>(yr)[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-      if (p.out_bf) {
-        uint16_t* yb = p.out_bf + (row0 + r) * C + h * HS;
-#pragma unroll
-        for (int q = 0; q < 16; q++)
-          reinterpret_cast<uint2*>(yb)[q] =
-              make_uint2(bf16x2_bits(o[4 * q], o[4 * q + 1]), bf16x2_bits(o[4 * q + 2], o[4 * q + 3]));
-      }
-    }
+    if (owner) {
+      float o[32];
+      tmem_ld32(tlane + (uint32_t)(32 * hf), o);
+      if (valid)
+        st_half32(p.out + (row0 + r) * C + h * HS + 32 * hf,
+                  p.out_bf ? p.out_bf + (row0 + r) * C + h * HS + 32 * hf : nullptr, o);
     }
   } else {
     drain(bars, mma_phase);  // a copy or MMA still in flight lands before the CTA's memory is released
   }
-  epilogue_free<FWD_TILES>(smem, tmem, 256);
-}
-
-// Stores this thread's 64 fp32 gradient values into dqkv (and its bf16 copy).
-GPT2_DEV void store_grad_row(const Params& p, size_t row, int col, const float* g) {
-  float* dst = p.out + row * 3 * p.C + col;
-#pragma unroll
-  for (int q = 0; q < 16; q++)
-    reinterpret_cast<float4*>(dst)[q] = make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
-  if (p.out_bf) {
-    uint16_t* db = p.out_bf + row * 3 * p.C + col;
-#pragma unroll
-    for (int q = 0; q < 16; q++)
-      reinterpret_cast<uint2*>(db)[q] =
-          make_uint2(bf16x2_bits(g[4 * q], g[4 * q + 1]), bf16x2_bits(g[4 * q + 2], g[4 * q + 3]));
-  }
+  epilogue_free(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
-// backward, query rows (blockIdx.z == 0 of the backward kernel): dq.  TMEM: S [0, 64) -> later dQ; dP [64, 128);
-// Q hi/lo [128, 256) -> later dS hi/lo; dY hi/lo [256, 384).
+// backward, query rows (blockIdx.z == 0 of the backward kernel): dq.  TMEM:
+// S [0, 64) -> later dQ; dP [64, 128); Q hi/lo [128, 256) -> later dS hi/lo;
+// dY hi/lo [256, 384).
 // ---------------------------------------------------------------------------
-GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV_, const Params& p, uint8_t* smem) {
-  const CUtensorMap& tmQKV = *tmQKV_;
+GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV, const Params& p, uint8_t* smem) {
   float* k_hi = reinterpret_cast<float*>(smem);
   float* k_lo = k_hi + TILE_FLOATS;
   float* v_hi = k_lo + TILE_FLOATS;
   float* v_lo = v_hi + TILE_FLOATS;
   float* kt_hi = v_lo + TILE_FLOATS;
   float* kt_lo = kt_hi + TILE_FLOATS;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<DQ_TILES>::OFF_BAR);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<DQ_TILES>::OFF_BAR + 24);
-  if (threadIdx.x == 0) *abort_flag = 0;
-  const uint32_t tmem = prologue<DQ_TILES>(smem, 512);
-  pdl_wait();
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<DKV_TILES>::OFF_BAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<DKV_TILES>::OFF_BAR + 24);
+  float* xa = reinterpret_cast<float*>(smem + Smem<DKV_TILES>::OFF_VEC);  // [2][64] half-row D partials
+  const uint32_t tmem = prologue<DKV_TILES>(smem, 512);
 
-  const int h = blockIdx.x, b = blockIdx.y, T = p.T, C = p.C, r = threadIdx.x;
+  const int h = blockIdx.x, b = blockIdx.y, T = p.T, C = p.C;
   const int Tp = (T + 15) & ~15;
-  const uint32_t tlane = tmem + ((uint32_t)(r & ~31) << 16);
+  const bool owner = row_owner();
+  const int r = own_row(), hf = own_half();
+  const uint32_t tlane = tmem + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16);
   const size_t row0 = (size_t)b * T;
-  const bool valid = r < T;
-  if (r == 0) tma_two_tiles(&tmQKV, k_hi, C + h * HS, v_hi, 2 * C + h * HS, b * T, &bars[0]);
-  float Dr = 0.f, lse_r = 0.f;
-  if (r < ROW_THREADS) {
-    float a[64], c[64];
-    ld_row64(p.dy + (row0 + r) * C + h * HS, valid, a);
-    ld_row64(p.y + (row0 + r) * C + h * HS, valid, c);
-    Dr = 0.f;
+  const bool valid = owner && r < T;
+  if (threadIdx.x == 0) tma_two_tiles(tmQKV, k_hi, C + h * HS, tmQKV, v_hi, 2 * C + h * HS, b * T, &bars[0]);
+  float lse_r = 0.f;
+  if (owner) {
+    float a[32], c[32];
+    ld_half32(p.dy + (row0 + r) * C + h * HS + 32 * hf, valid, a);
+    ld_half32(p.y + (row0 + r) * C + h * HS + 32 * hf, valid, c);
+    float D = 0.f;
 #pragma unroll
-    for (int d = 0; d < 64; d++) Dr = fmaf(a[d], c[d], Dr);
-    st_row_split(tlane, 256, a);  // dY
-    ld_row64(p.qkv + (row0 + r) * 3 * C + h * HS, valid, c);
-    st_row_split(tlane, 128, c);  // Q
+    for (int d = 0; d < 32; d++) D = fmaf(a[d], c[d], D);
+    xa[hf * 64 + r] = D;
+    st_half_split(tlane, 256, hf, a);  // dY
+    ld_half32(p.qkv + (row0 + r) * 3 * C + h * HS + 32 * hf, valid, c);
+    st_half_split(tlane, 128, hf, c);  // Q
     lse_r = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
   }
   int mma_phase = -1;
@@ -407,7 +418,7 @@ GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV_, const Params& p, uint8_t* smem) 
     transpose_tile(k_hi, kt_hi);
     transpose_tile(k_lo, kt_lo);
     publish_operands();
-    if (r == 0) {
+    if (threadIdx.x == 0) {
       mma3(tmem, 0, 128, 192, k_hi, k_lo, HS / 8, Tp);   // S = Q K^T
       mma3(tmem, 64, 256, 320, v_hi, v_lo, HS / 8, Tp);  // dP = dY V^T
       mma_commit(&bars[1]);
@@ -417,19 +428,21 @@ GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV_, const Params& p, uint8_t* smem) 
   }
   if (ok) {
     tc_fence_after();
-    if (r < ROW_THREADS) {
-    float s[64], dp[64];
-    ld_row64_tmem(tlane + 0, s);
-    ld_row64_tmem(tlane + 64, dp);
+    if (owner) {
+      const float Dr = xa[r] + xa[64 + r];
+      float s[32], dp[32];
+      tmem_ld32(tlane + (uint32_t)(32 * hf), s);
+      tmem_ld32(tlane + (uint32_t)(64 + 32 * hf), dp);
 #pragma unroll
-    for (int j = 0; j < 64; j++) {
-      // dS, with the scale of S folded in; columns past the MMA's N hold no data
-      s[j] = (valid && j <= r) ? expf(s[j] * p.scale - lse_r) * (dp[j] - Dr) * p.scale : 0.f;
-    }
-    st_row_split(tlane, 128, s);  // dS over Q's columns
+      for (int k = 0; k < 32; k++) {
+        const int j = 32 * hf + k;
+        // dS, with the scale of S folded in; columns past the MMA's N hold no data
+        s[k] = (valid && j <= r) ? expf(s[k] * p.scale - lse_r) * (dp[k] - Dr) * p.scale : 0.f;
+      }
+      st_half_split(tlane, 128, hf, s);  // dS over Q's columns
     }
     publish_operands();
-    if (r == 0) {
+    if (threadIdx.x == 0) {
       mma3(tmem, 0, 128, 192, kt_hi, kt_lo, Tp / 8, HS);  // dQ = dS K, over S's columns
       mma_commit(&bars[1]);
     }
@@ -438,25 +451,26 @@ GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV_, const Params& p, uint8_t* smem) 
   }
   if (ok) {
     tc_fence_after();
-    if (r < ROW_THREADS) {
-      float g[64];
-      ld_row64_tmem(tlane + 0, g);
-      if (valid) store_grad_row(p, row0 + r, h * HS, g);
+    if (owner) {
+      float g[32];
+      tmem_ld32(tlane + (uint32_t)(32 * hf), g);
+      const size_t o = (row0 + r) * 3 * C + h * HS + 32 * hf;
+      if (valid) st_half32(p.out + o, p.out_bf ? p.out_bf + o : nullptr, g);
     }
   } else {
     drain(bars, mma_phase);
   }
-  epilogue_free<DQ_TILES>(smem, tmem, 512);
+  epilogue_free(tmem, 512);
 }
 
 // ---------------------------------------------------------------------------
-// backward, key rows (blockIdx.z == 1): dk and dv.  TMEM: S^T [0, 64) -> later dV;
-// dP^T [64, 128) -> later dK; K hi/lo [128, 256) -> later P^T hi/lo;
-// V hi/lo [256, 384) -> later dS^T hi/lo.  tmDY: dy as (B*T rows, C columns).
+// backward, key rows (blockIdx.z == 1): dk and dv.  TMEM: S^T [0, 64) ->
+// later dV; dP^T [64, 128) -> later dK; K hi/lo [128, 256) -> later P^T
+// hi/lo; V hi/lo [256, 384) -> later dS^T hi/lo.  tmDY: dy as (B*T rows, C
+// columns).  Row r also stands for query r: its D_r partials and lse_r are
+// shared through shared memory with every key row.
 // ---------------------------------------------------------------------------
-GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV_, const CUtensorMap* tmDY_, const Params& p, uint8_t* smem) {
-  const CUtensorMap& tmQKV = *tmQKV_;
-  const CUtensorMap& tmDY = *tmDY_;
+GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const Params& p, uint8_t* smem) {
   float* q_hi = reinterpret_cast<float*>(smem);
   float* q_lo = q_hi + TILE_FLOATS;
   float* dy_hi = q_lo + TILE_FLOATS;
@@ -467,39 +481,32 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV_, const CUtensorMap* tmDY_, const
   float* dyt_lo = dyt_hi + TILE_FLOATS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<DKV_TILES>::OFF_BAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<DKV_TILES>::OFF_BAR + 24);
-  float* lse_s = reinterpret_cast<float*>(smem + Smem<DKV_TILES>::OFF_VEC);
-  float* D_s = lse_s + 64;
-  if (threadIdx.x == 0) *abort_flag = 0;
+  float* xa = reinterpret_cast<float*>(smem + Smem<DKV_TILES>::OFF_VEC);  // [2][64] D partials per query
+  float* lse_s = xa + 256;                                                  // [64]
   const uint32_t tmem = prologue<DKV_TILES>(smem, 512);
-  pdl_wait();
 
-  const int h = blockIdx.x, b = blockIdx.y, T = p.T, C = p.C, r = threadIdx.x;
+  const int h = blockIdx.x, b = blockIdx.y, T = p.T, C = p.C;
   const int Tp = (T + 15) & ~15;
-  const uint32_t tlane = tmem + ((uint32_t)(r & ~31) << 16);
+  const bool owner = row_owner();
+  const int r = own_row(), hf = own_half();
+  const uint32_t tlane = tmem + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16);
   const size_t row0 = (size_t)b * T;
-  const bool valid = r < T;
-  if (r == 0) {
-    mbar_expect_tx(&bars[0], 2 * TILE_BYTES);
-    tma_load_2d(q_hi, &tmQKV, h * HS, b * T, &bars[0]);
-    tma_load_2d(reinterpret_cast<uint8_t*>(q_hi) + BOX_BYTES, &tmQKV, h * HS + 32, b * T, &bars[0]);
-    tma_load_2d(dy_hi, &tmDY, h * HS, b * T, &bars[0]);
-    tma_load_2d(reinterpret_cast<uint8_t*>(dy_hi) + BOX_BYTES, &tmDY, h * HS + 32, b * T, &bars[0]);
-  }
-  if (r < ROW_THREADS) {
-    float a[64], c[64];
-    // row r as a query: D_r = dy_r . y_r and lse_r, shared with every key row
-    ld_row64(p.dy + (row0 + r) * C + h * HS, valid, a);
-    ld_row64(p.y + (row0 + r) * C + h * HS, valid, c);
+  const bool valid = owner && r < T;
+  if (threadIdx.x == 0) tma_two_tiles(tmQKV, q_hi, h * HS, tmDY, dy_hi, h * HS, b * T, &bars[0]);
+  if (owner) {
+    float a[32], c[32];
+    ld_half32(p.dy + (row0 + r) * C + h * HS + 32 * hf, valid, a);
+    ld_half32(p.y + (row0 + r) * C + h * HS + 32 * hf, valid, c);
     float D = 0.f;
 #pragma unroll
-    for (int d = 0; d < 64; d++) D = fmaf(a[d], c[d], D);
-    D_s[r] = D;
-    lse_s[r] = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
+    for (int d = 0; d < 32; d++) D = fmaf(a[d], c[d], D);
+    xa[hf * 64 + r] = D;
+    if (hf == 0) lse_s[r] = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
     // row r as a key: K and V into TMEM
-    ld_row64(p.qkv + (row0 + r) * 3 * C + C + h * HS, valid, a);
-    st_row_split(tlane, 128, a);
-    ld_row64(p.qkv + (row0 + r) * 3 * C + 2 * C + h * HS, valid, c);
-    st_row_split(tlane, 256, c);
+    ld_half32(p.qkv + (row0 + r) * 3 * C + C + h * HS + 32 * hf, valid, a);
+    st_half_split(tlane, 128, hf, a);
+    ld_half32(p.qkv + (row0 + r) * 3 * C + 2 * C + h * HS + 32 * hf, valid, c);
+    st_half_split(tlane, 256, hf, c);
   }
   int mma_phase = -1;
   bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
@@ -512,7 +519,7 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV_, const CUtensorMap* tmDY_, const
     transpose_tile(dy_hi, dyt_hi);
     transpose_tile(dy_lo, dyt_lo);
     publish_operands();
-    if (r == 0) {
+    if (threadIdx.x == 0) {
       mma3(tmem, 0, 128, 192, q_hi, q_lo, HS / 8, Tp);     // S^T = K Q^T
       mma3(tmem, 64, 256, 320, dy_hi, dy_lo, HS / 8, Tp);  // dP^T = V dY^T
       mma_commit(&bars[1]);
@@ -522,23 +529,24 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV_, const CUtensorMap* tmDY_, const
   }
   if (ok) {
     tc_fence_after();
-    if (r < ROW_THREADS) {
-    float pt[64], dst[64];
-    ld_row64_tmem(tlane + 0, pt);
-    ld_row64_tmem(tlane + 64, dst);
+    if (owner) {
+      float pt[32], dst[32];
+      tmem_ld32(tlane + (uint32_t)(32 * hf), pt);
+      tmem_ld32(tlane + (uint32_t)(64 + 32 * hf), dst);
 #pragma unroll
-    for (int t = 0; t < 64; t++) {
-      // columns past the MMA's N hold no data
-      const bool live = valid && t >= r && t < T;
-      const float pv = live ? expf(pt[t] * p.scale - lse_s[t]) : 0.f;
-      pt[t] = pv;
-      dst[t] = live ? pv * (dst[t] - D_s[t]) * p.scale : 0.f;  // dS^T, with the scale folded in
-    }
-    st_row_split(tlane, 128, pt);   // P^T over K's columns
-    st_row_split(tlane, 256, dst);  // dS^T over V's columns
+      for (int k = 0; k < 32; k++) {
+        const int t = 32 * hf + k;
+        // columns past the MMA's N hold no data
+        const bool live = valid && t >= r && t < T;
+        const float pv = live ? expf(pt[k] * p.scale - lse_s[t]) : 0.f;
+        pt[k] = pv;
+        dst[k] = live ? pv * (dst[k] - (xa[t] + xa[64 + t])) * p.scale : 0.f;  // dS^T, with the scale folded in
+      }
+      st_half_split(tlane, 128, hf, pt);   // P^T over K's columns
+      st_half_split(tlane, 256, hf, dst);  // dS^T over V's columns
     }
     publish_operands();
-    if (r == 0) {
+    if (threadIdx.x == 0) {
       mma3(tmem, 0, 128, 192, dyt_hi, dyt_lo, Tp / 8, HS);  // dV = P^T dY
       mma3(tmem, 64, 256, 320, qt_hi, qt_lo, Tp / 8, HS);   // dK = dS^T Q
       mma_commit(&bars[1]);
@@ -548,22 +556,23 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV_, const CUtensorMap* tmDY_, const
   }
   if (ok) {
     tc_fence_after();
-    if (r < ROW_THREADS) {
-      float g[64];
-      ld_row64_tmem(tlane + 64, g);
-      if (valid) store_grad_row(p, row0 + r, C + h * HS, g);
-      ld_row64_tmem(tlane + 0, g);
-      if (valid) store_grad_row(p, row0 + r, 2 * C + h * HS, g);
+    if (owner) {
+      float g[32];
+      const size_t o = (row0 + r) * 3 * C + h * HS + 32 * hf;
+      tmem_ld32(tlane + (uint32_t)(64 + 32 * hf), g);
+      if (valid) st_half32(p.out + o + C, p.out_bf ? p.out_bf + o + C : nullptr, g);
+      tmem_ld32(tlane + (uint32_t)(32 * hf), g);
+      if (valid) st_half32(p.out + o + 2 * C, p.out_bf ? p.out_bf + o + 2 * C : nullptr, g);
     }
   } else {
     drain(bars, mma_phase);
   }
-  epilogue_free<DKV_TILES>(smem, tmem, 512);
+  epilogue_free(tmem, 512);
 }
 
 // The backward: grid (NH, B, 2); the query-row CTAs (z = 0) and the key-row
-// CTAs (z = 1) of every head run side by side.
-constexpr size_t BWD_SMEM = DQ_SMEM > DKV_SMEM ? DQ_SMEM : DKV_SMEM;
+// CTAs (z = 1) of every head run side by side.  Both use the larger layout.
+constexpr size_t BWD_SMEM = DKV_SMEM;
 
 __global__ void __launch_bounds__(THREADS) attn_bwd_tf32_kernel(const __grid_constant__ CUtensorMap tmQKV,
                                                                 const __grid_constant__ CUtensorMap tmDY,
