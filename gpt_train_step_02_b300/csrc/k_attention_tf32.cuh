@@ -24,8 +24,9 @@
 //    128-byte swizzle: K values [32c, 32c + 32) of row n at
 //    8 KB * c + 128 n + 16 ((k/4 % 8) ^ (n % 8)) + 4 (k % 4) bytes.  Tiles
 //    whose rows are rows of qkv (or dy) come in by TMA in exactly that layout
-//    and are split in place (hi) plus a lo copy; transposed tiles are written
-//    from the split ones.
+//    and are split in place (hi) plus a lo copy; transposed tiles (rows =
+//    head dimensions) are written by the threads that hold the rows in
+//    registers, each thread filling one K position of every tile row.
 // One thread issues the MMAs; completion is signalled through an mbarrier.
 // Every wait is bounded (tc::mbar_wait) and every stop-or-continue decision
 // is taken by the whole CTA at once (__syncthreads_and), so a wait that gives
@@ -141,6 +142,20 @@ GPT2_DEV void st_half32(float* dst, uint16_t* dbf, const float* v) {
   }
 }
 
+// This thread's 32 values (columns [32 half, +32) of row `row`), split, into
+// the transposed tiles: value d goes to row d, K position `row`.  The 32 lanes
+// of a warp hold 32 consecutive rows, so each store covers 32 consecutive K
+// positions of one tile row: no bank conflicts.
+GPT2_DEV void st_half_transposed(float* t_hi, float* t_lo, int row, int half, const float* v) {
+#pragma unroll
+  for (int k = 0; k < 32; k++) {
+    const int d = 32 * half + k;
+    const float hi = tf32_hi(v[k]);
+    t_hi[sw(d, row)] = hi;
+    t_lo[sw(d, row)] = v[k] - hi;
+  }
+}
+
 // In-place split of a TMA-written tile: hi stays, lo goes to lo.
 GPT2_DEV void split_tile(float* t, float* lo) {
   float4* t4 = reinterpret_cast<float4*>(t);
@@ -150,14 +165,6 @@ GPT2_DEV void split_tile(float* t, float* lo) {
     tc::split4(t4[i], h, l);
     t4[i] = h;
     l4[i] = l;
-  }
-}
-
-// dst(n, k) = src(k, n) for the 64 x 64 tiles (already split halves are copied).
-GPT2_DEV void transpose_tile(const float* src, float* dst) {
-  for (int e = threadIdx.x; e < TILE_FLOATS; e += THREADS) {
-    const int n = e >> 6, k = e & 63;  // a warp writes 32 consecutive k of one row n
-    dst[sw(n, k)] = src[sw(k, n)];
   }
 }
 
@@ -181,7 +188,7 @@ struct Smem {
   static constexpr int OFF_VEC = OFF_BAR + 64;
   static constexpr int BYTES = OFF_VEC + 5 * 64 * 4 + 1024;
 };
-constexpr int FWD_TILES = 5;  // K (hi, lo), V raw, V^T (hi, lo)
+constexpr int FWD_TILES = 4;  // K (hi, lo), V^T (hi, lo)
 constexpr int DQ_TILES = 6;   // K (hi, lo), V (hi, lo), K^T (hi, lo)
 constexpr int DKV_TILES = 8;  // Q (hi, lo), dY (hi, lo), Q^T (hi, lo), dY^T (hi, lo)
 constexpr size_t FWD_SMEM = Smem<FWD_TILES>::BYTES;
@@ -272,8 +279,7 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   float* k_hi = reinterpret_cast<float*>(smem);
   float* k_lo = k_hi + TILE_FLOATS;
-  float* v_raw = k_lo + TILE_FLOATS;
-  float* vt_hi = v_raw + TILE_FLOATS;
+  float* vt_hi = k_lo + TILE_FLOATS;
   float* vt_lo = vt_hi + TILE_FLOATS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<FWD_TILES>::OFF_BAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<FWD_TILES>::OFF_BAR + 24);
@@ -288,23 +294,22 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   const uint32_t tlane = tmem + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16);
   const size_t row0 = (size_t)b * T;
   const bool valid = owner && r < T;
-  if (threadIdx.x == 0) tma_two_tiles(&tmQKV, k_hi, C + h * HS, &tmQKV, v_raw, 2 * C + h * HS, b * T, &bars[0]);
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(&bars[0], TILE_BYTES);
+    tma_load_2d(k_hi, &tmQKV, C + h * HS, b * T, &bars[0]);
+    tma_load_2d(reinterpret_cast<uint8_t*>(k_hi) + BOX_BYTES, &tmQKV, C + h * HS + 32, b * T, &bars[0]);
+  }
   if (owner) {
-    float q[32];
+    float q[32], v[32];
     ld_half32(p.qkv + (row0 + r) * 3 * C + h * HS + 32 * hf, valid, q);
+    ld_half32(p.qkv + (row0 + r) * 3 * C + 2 * C + h * HS + 32 * hf, valid, v);
     st_half_split(tlane, 64, hf, q);
+    st_half_transposed(vt_hi, vt_lo, r, hf, v);  // V^T: rows d, K values = keys
   }
   int mma_phase = -1;
   bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
   if (ok) {
     split_tile(k_hi, k_lo);
-    // V^T halves: rows d, K values = keys
-    for (int e = threadIdx.x; e < TILE_FLOATS; e += THREADS) {
-      const int d = e >> 6, key = e & 63;
-      const float x = v_raw[sw(key, d)], hi = tf32_hi(x);
-      vt_hi[sw(d, key)] = hi;
-      vt_lo[sw(d, key)] = x - hi;
-    }
     publish_operands();
     if (threadIdx.x == 0) {
       mma3(tmem, 0, 64, 128, k_hi, k_lo, HS / 8, Tp);  // S = Q K^T
@@ -397,26 +402,27 @@ GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV, const Params& p, uint8_t* smem) {
   if (threadIdx.x == 0) tma_two_tiles(tmQKV, k_hi, C + h * HS, tmQKV, v_hi, 2 * C + h * HS, b * T, &bars[0]);
   float lse_r = 0.f;
   if (owner) {
-    float a[32], c[32];
-    ld_half32(p.dy + (row0 + r) * C + h * HS + 32 * hf, valid, a);
-    ld_half32(p.y + (row0 + r) * C + h * HS + 32 * hf, valid, c);
+    // every global load first (the TMEM stores below order the code after them)
+    float dyv[32], yv[32], qv[32], kv[32];
+    const float* qkv_r = p.qkv + (row0 + r) * 3 * C + h * HS + 32 * hf;
+    ld_half32(p.dy + (row0 + r) * C + h * HS + 32 * hf, valid, dyv);
+    ld_half32(p.y + (row0 + r) * C + h * HS + 32 * hf, valid, yv);
+    ld_half32(qkv_r, valid, qv);
+    ld_half32(qkv_r + C, valid, kv);
+    lse_r = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
     float D = 0.f;
 #pragma unroll
-    for (int d = 0; d < 32; d++) D = fmaf(a[d], c[d], D);
+    for (int d = 0; d < 32; d++) D = fmaf(dyv[d], yv[d], D);
     xa[hf * 64 + r] = D;
-    st_half_split(tlane, 256, hf, a);  // dY
-    ld_half32(p.qkv + (row0 + r) * 3 * C + h * HS + 32 * hf, valid, c);
-    st_half_split(tlane, 128, hf, c);  // Q
-    lse_r = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
+    st_half_transposed(kt_hi, kt_lo, r, hf, kv);  // K^T: row r as a key
+    st_half_split(tlane, 256, hf, dyv);           // dY
+    st_half_split(tlane, 128, hf, qv);            // Q
   }
   int mma_phase = -1;
   bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
   if (ok) {
     split_tile(k_hi, k_lo);
     split_tile(v_hi, v_lo);
-    __syncthreads();
-    transpose_tile(k_hi, kt_hi);
-    transpose_tile(k_lo, kt_lo);
     publish_operands();
     if (threadIdx.x == 0) {
       mma3(tmem, 0, 128, 192, k_hi, k_lo, HS / 8, Tp);   // S = Q K^T
@@ -494,30 +500,32 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const P
   const bool valid = owner && r < T;
   if (threadIdx.x == 0) tma_two_tiles(tmQKV, q_hi, h * HS, tmDY, dy_hi, h * HS, b * T, &bars[0]);
   if (owner) {
-    float a[32], c[32];
-    ld_half32(p.dy + (row0 + r) * C + h * HS + 32 * hf, valid, a);
-    ld_half32(p.y + (row0 + r) * C + h * HS + 32 * hf, valid, c);
+    // every global load first (the TMEM stores below order the code after them)
+    float dyv[32], yv[32], qv[32], kv[32], vv[32];
+    const float* qkv_r = p.qkv + (row0 + r) * 3 * C + h * HS + 32 * hf;
+    ld_half32(p.dy + (row0 + r) * C + h * HS + 32 * hf, valid, dyv);
+    ld_half32(p.y + (row0 + r) * C + h * HS + 32 * hf, valid, yv);
+    ld_half32(qkv_r, valid, qv);
+    ld_half32(qkv_r + C, valid, kv);
+    ld_half32(qkv_r + 2 * C, valid, vv);
+    const float lse_r = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
+    // row r as a query: D_r partial, lse_r, its dY and Q values for the transposed tiles
     float D = 0.f;
 #pragma unroll
-    for (int d = 0; d < 32; d++) D = fmaf(a[d], c[d], D);
+    for (int d = 0; d < 32; d++) D = fmaf(dyv[d], yv[d], D);
     xa[hf * 64 + r] = D;
-    if (hf == 0) lse_s[r] = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
+    if (hf == 0) lse_s[r] = lse_r;
+    st_half_transposed(dyt_hi, dyt_lo, r, hf, dyv);  // dY^T
+    st_half_transposed(qt_hi, qt_lo, r, hf, qv);     // Q^T
     // row r as a key: K and V into TMEM
-    ld_half32(p.qkv + (row0 + r) * 3 * C + C + h * HS + 32 * hf, valid, a);
-    st_half_split(tlane, 128, hf, a);
-    ld_half32(p.qkv + (row0 + r) * 3 * C + 2 * C + h * HS + 32 * hf, valid, c);
-    st_half_split(tlane, 256, hf, c);
+    st_half_split(tlane, 128, hf, kv);
+    st_half_split(tlane, 256, hf, vv);
   }
   int mma_phase = -1;
   bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
   if (ok) {
     split_tile(q_hi, q_lo);
     split_tile(dy_hi, dy_lo);
-    __syncthreads();
-    transpose_tile(q_hi, qt_hi);
-    transpose_tile(q_lo, qt_lo);
-    transpose_tile(dy_hi, dyt_hi);
-    transpose_tile(dy_lo, dyt_lo);
     publish_operands();
     if (threadIdx.x == 0) {
       mma3(tmem, 0, 128, 192, q_hi, q_lo, HS / 8, Tp);     // S^T = K Q^T
