@@ -42,7 +42,7 @@ EXPORTS = [
     "gpt2_get_logits", "gpt2_last_launch_count", "gpt2_status_string", "gpt2_train_step", "gpt2_kernel_timer",
     "gpt2_kernel_timer_read", "gpt2op_matmul_workspace_bytes", "gpt2op_matmul_forward", "gpt2op_matmul_backward",
     "gpt2op_matmul_backward_noalloc", "gpt2op_attention_workspace_bytes", "gpt2op_attention_forward",
-    "gpt2op_attention_backward_workspace_bytes", "gpt2op_attention_backward",
+    "gpt2op_attention_backward_workspace_bytes", "gpt2op_attention_backward", "gpt2_set_wait_limit_ns",
 ]
 
 
@@ -92,6 +92,7 @@ def lib() -> ct.CDLL:
             "gpt2_status_string": (ct.c_char_p, [I]),
             "gpt2_train_step": (I, [P, P, P, I, I, F, F, F, F, F, I, P]),
             "gpt2_kernel_timer": (I, [P, I]),
+            "gpt2_set_wait_limit_ns": (I, [ct.c_ulonglong]),
             "gpt2op_matmul_workspace_bytes": (SZ, [I, I, I]),
             "gpt2op_matmul_forward": (I, [P, P, P, P, I, I, I, I, P, P]),
             "gpt2op_matmul_backward": (I, [P, P, P, P, P, P, I, I, I, I, P, P]),
@@ -220,6 +221,11 @@ def gpt2_kernel_timer_read(h):
     ms, n, work = ct.c_double(0), ct.c_longlong(0), ct.c_double(0)
     _check(lib().gpt2_kernel_timer_read(h, ct.byref(ms), ct.byref(n), ct.byref(work)), "gpt2_kernel_timer_read")
     return float(ms.value), int(n.value), float(work.value)
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of the device-side pipeline waits (0 restores the 1 s default)."""
+    _check(lib().gpt2_set_wait_limit_ns(int(ns)), "gpt2_set_wait_limit_ns")
 
 
 def gpt2_free(h) -> None:

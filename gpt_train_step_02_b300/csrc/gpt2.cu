@@ -1957,6 +1957,15 @@ EXPORT int gpt2_kernel_timer_read(gpt2_t* m, double* total_ms, long long* launch
   return GPT2_OK;
 }
 
+EXPORT int gpt2_set_wait_limit_ns(unsigned long long ns) {
+  const unsigned long long v = ns ? ns : (unsigned long long)tc::WAIT_LIMIT_NS;
+  if (cudaMemcpyToSymbol(tc::g_wait_limit_ns, &v, sizeof(v)) != cudaSuccess) {
+    cudaGetLastError();
+    return GPT2_ERR_CUDA;
+  }
+  return cudaDeviceSynchronize() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
 EXPORT long long gpt2_num_parameters(const gpt2_t* m) { return m ? m->np : -1; }
 
 EXPORT long long gpt2_last_launch_count(const gpt2_t* m) { return m ? m->launches : -1; }

@@ -56,6 +56,11 @@ constexpr int TMEM_COLS = 256;
 static_assert(TM_A + COMP_STAGES * 2 * BK <= TMEM_COLS, "A stages must fit the TMEM allocation");
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s of wall time per wait before giving up
 
+// The limit of the pipeline waits (mbar_wait), per device: WAIT_LIMIT_NS
+// unless a test lowers it to make them give up (gpt2_set_wait_limit_ns).  The
+// drain waits of the abort path always allow WAIT_LIMIT_NS.
+__device__ unsigned long long g_wait_limit_ns = WAIT_LIMIT_NS;
+
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int OFF_RAW_A = 0;
 constexpr int OFF_RAW_B = OFF_RAW_A + RAW_STAGES * TILE_BYTES;
@@ -124,19 +129,24 @@ GPT2_DEV uint64_t globaltimer_ns() {
 }
 
 // Bounded wait: returns false (and raises the CTA's abort flag and the
-// device error word) if the phase does not complete within WAIT_LIMIT_NS of
-// wall time or another role of the CTA has aborted.  try_wait may suspend
+// device error word) if the phase does not complete within g_wait_limit_ns
+// of wall time or another role of the CTA has aborted.  try_wait may suspend
 // the thread for a hardware-defined interval, so the bound is taken on the
-// global timer rather than on a poll count.
+// global timer rather than on a poll count; the clock is read after the first
+// four failed polls and every 256th after that.
 GPT2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
-  uint64_t t0 = 0;
+  uint64_t t0 = 0, limit = WAIT_LIMIT_NS;
   for (uint32_t i = 0;; i++) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255) == 0) {
+    if ((i & 255) == 0 || i < 4) {
       if (*abort_flag) return false;
       uint64_t now = globaltimer_ns();
-      if (i == 0) t0 = now;
-      else if (now - t0 > WAIT_LIMIT_NS) break;
+      if (i == 0) {
+        t0 = now;
+        limit = *(volatile unsigned long long*)&g_wait_limit_ns;
+      } else if (now - t0 > limit) {
+        break;
+      }
     }
   }
   *abort_flag = 1;

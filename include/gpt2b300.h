@@ -189,6 +189,18 @@ int gpt2_train_step(gpt2_t* m, const int32_t* inputs, const int32_t* targets, in
 int gpt2_kernel_timer(gpt2_t* m, int kind);
 int gpt2_kernel_timer_read(gpt2_t* m, double* total_ms, long long* launches, double* total_work);
 
+/* Test and diagnosis knob for the bounded device-side waits.  Every
+ * tensor-core kernel waits on its pipeline barriers for at most this long
+ * (wall time) before it records a timeout, lets its copies and MMAs in
+ * flight land, frees its tensor memory and returns; the next synchronising
+ * call then reports GPT2_ERR_DEVICE_TIMEOUT and poisons the handle (the
+ * per-layer gpt2op_* calls return it directly).  Default 1 s; ns = 0
+ * restores it.  Applies to the current device and to every handle and call
+ * on it; synchronises the device.  A limit far below a kernel's normal wait
+ * times (a few ns) makes such waits give up: tests use that to exercise the
+ * timeout path without a fault. */
+int gpt2_set_wait_limit_ns(unsigned long long ns);
+
 /* Frees the handle (and the arena if the library allocated it). */
 int gpt2_free(gpt2_t* m);
 
