@@ -59,7 +59,7 @@ constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s of wall time per wait 
 // The limit of the pipeline waits (mbar_wait), per device: WAIT_LIMIT_NS
 // unless a test lowers it to make them give up (gpt2_set_wait_limit_ns).  The
 // drain waits of the abort path always allow WAIT_LIMIT_NS.
-__device__ unsigned long long g_wait_limit_ns = WAIT_LIMIT_NS;
+__constant__ unsigned long long g_wait_limit_ns = WAIT_LIMIT_NS;
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int OFF_RAW_A = 0;
@@ -128,24 +128,37 @@ GPT2_DEV uint64_t globaltimer_ns() {
   return t;
 }
 
+// Non-blocking probe of a phase (mbarrier.test_wait).
+GPT2_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: returns false (and raises the CTA's abort flag and the
 // device error word) if the phase does not complete within g_wait_limit_ns
 // of wall time or another role of the CTA has aborted.  try_wait may suspend
 // the thread for a hardware-defined interval, so the bound is taken on the
-// global timer rather than on a poll count; the clock is read after the first
-// four failed polls and every 256th after that.
+// global timer rather than on a poll count (read every 256th failed poll).
+// The limit comes from the constant cache.  A limit below 1 us means
+// "do not wait": a phase that is not complete at the first probe times out
+// at once (the global timer's ticks are too coarse to time a few ns).
 GPT2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
-  uint64_t t0 = 0, limit = WAIT_LIMIT_NS;
-  for (uint32_t i = 0;; i++) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255) == 0 || i < 4) {
-      if (*abort_flag) return false;
-      uint64_t now = globaltimer_ns();
-      if (i == 0) {
-        t0 = now;
-        limit = *(volatile unsigned long long*)&g_wait_limit_ns;
-      } else if (now - t0 > limit) {
-        break;
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t limit = g_wait_limit_ns;
+  if (limit >= 1000) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; i++) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((i & 255) == 0) {
+        if (*abort_flag) return false;
+        uint64_t now = globaltimer_ns();
+        if (i == 0) t0 = now;
+        else if (now - t0 > limit) break;
       }
     }
   }
