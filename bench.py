@@ -360,7 +360,8 @@ def run_ours(args, w):
             extra[name] = {
                 "config": workload_config(xw, 1), "tokens_per_s": r["value"], "ms_per_step": r["ms_per_step"],
                 "steps": args.extra_steps, "warmup": 3, "mfu": r["mfu"], "roofline": r["roofline"],
-                "rooflines": r["rooflines"], "clocks": r["clocks"], "gpu_launches_per_step": r["launches_per_step"],
+                "rooflines": r["rooflines"], "kernels": r["kernels"], "clocks": r["clocks"],
+                "gpu_launches_per_step": r["launches_per_step"],
                 "last_loss": r["last_loss"],
             }
 

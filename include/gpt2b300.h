@@ -195,10 +195,10 @@ int gpt2_kernel_timer_read(gpt2_t* m, double* total_ms, long long* launches, dou
  * flight land, frees its tensor memory and returns; the next synchronising
  * call then reports GPT2_ERR_DEVICE_TIMEOUT and poisons the handle (the
  * per-layer gpt2op_* calls return it directly).  Default 1 s; ns = 0
- * restores it.  A limit below 1000 ns means "do not wait": a barrier phase
- * not complete at the first probe times out at once -- tests use that to
- * drive the timeout path without a fault.  Applies to the current device and
- * to every handle and call on it; synchronises the device. */
+ * restores it.  A limit below 1000 ns makes every such wait give up at its
+ * first call -- tests use that to drive the timeout path, the same way every
+ * time and without a fault.  Applies to the current device and to every
+ * handle and call on it; synchronises the device. */
 int gpt2_set_wait_limit_ns(unsigned long long ns);
 
 /* Frees the handle (and the arena if the library allocated it). */

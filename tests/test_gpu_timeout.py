@@ -5,8 +5,8 @@ copies and MMAs): past the limit it records a timeout in the error word,
 stops issuing work, lets the copies and MMAs it already issued land (those
 drain waits keep the full 1 s), frees its tensor memory and returns, and
 every CTA of a split-K cluster still reaches both cluster barriers.  The
-tests lower the limit to 1 ns through ``gpt2_set_wait_limit_ns`` -- so every
-wait that does not succeed at its first polls gives up -- and check that:
+tests lower the limit to 1 ns through ``gpt2_set_wait_limit_ns`` -- below
+1 us every wait gives up at its first call -- and check that:
 
 * the per-layer calls (a split-K 3xTF32 matmul, the fp32 tensor-core
   attention) return GPT2_ERR_DEVICE_TIMEOUT;
