@@ -401,22 +401,47 @@ def run_ours(args, w):
 
 # Sources of each kernel class: DRAM traffic recorded by ncu stays valid only
 # while these files are unchanged.
+# Sources of each kernel class: DRAM traffic recorded by ncu stays valid only
+# while these are unchanged -- whole files for the matmuls, the named
+# functions (their full definitions) for the others, so that an edit to an
+# unrelated kernel in the same file does not invalidate a record.
 KERNEL_SOURCES = {
-    "gemm": ["gemm_common.cuh", "k_gemm_tc.cuh", "k_gemm_bf16.cuh", "common.cuh"],
-    "adamw": ["k_misc.cuh", "common.cuh"],
-    "xent": ["k_xent.cuh", "common.cuh"],
-    "layernorm": ["k_layernorm.cuh", "k_misc.cuh", "common.cuh"],
-    "encoder": ["k_misc.cuh", "common.cuh"],
+    "gemm": ["gemm_common.cuh", "k_gemm_tc.cuh", "k_gemm_bf16.cuh"],
+    "adamw": [("k_misc.cuh", "adamw_f4"), ("k_misc.cuh", "adamw_kernel"), ("k_misc.cuh", "adamw_rows_kernel"),
+              ("k_misc.cuh", "adamw_sorted_rows_kernel")],
+    "xent": [("k_xent.cuh", "online_merge"), ("k_xent.cuh", "xent_fused_kernel"), ("k_xent.cuh", "xent_bf16_kernel")],
+    "layernorm": [("k_layernorm.cuh", "layernorm_fwd_kernel"), ("k_layernorm.cuh", "layernorm_bwd_kernel"),
+                  ("k_misc.cuh", "col_finish_kernel")],
+    "encoder": [("k_misc.cuh", "encoder_fwd_kernel")],
 }
+
+
+def function_source(text, name):
+    """The definition of function `name` in a CUDA source: from the line that
+    declares it to the brace closing its body."""
+    import re
+
+    m = re.search(r"^[^\n]*\b" + re.escape(name) + r"\(", text, re.M)
+    if not m:
+        raise KeyError(name)
+    i = text.index("{", m.end())
+    depth = 0
+    for j in range(i, len(text)):
+        depth += {"{": 1, "}": -1}.get(text[j], 0)
+        if depth == 0:
+            return text[m.start():j + 1]
+    raise ValueError(name)
 
 
 def kernel_source_sha(kind):
     import hashlib
 
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES.get(kind, []):
-        with open(os.path.join(ROOT, "gpt_train_step_02_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for src in KERNEL_SOURCES.get(kind, []):
+        f, fn = (src, None) if isinstance(src, str) else src
+        with open(os.path.join(ROOT, "gpt_train_step_02_b300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        h.update((text if fn is None else function_source(text, fn)).encode())
     return h.hexdigest()[:16]
 
 

@@ -65,6 +65,7 @@ struct Plan {
   size_t encoded, ln1, ln1_mean, ln1_rstd, qkv, atty, lse, res2, ln2, ln2_mean, ln2_rstd, fch, fchg, res3;
   size_t lnf, lnf_mean, lnf_rstd, logits, dlogits, losses, loss;
   size_t dres, dln, datty, dqkv, dfch, attD, scratch, sorted, tokens, targets, err, hparams, splitk, tilectr;
+  size_t sort_tmp, radix_hist;  // the embedding backward's radix sort (more than SORT_MAX tokens)
   // the split-K workspace and tile counters of the weight-gradient side stream (bf16 matmuls only)
   size_t splitk_w, tilectr_w;
   // bf16 operand copies (bf16 matmuls only)
@@ -109,8 +110,12 @@ static int config_ok(const gpt2_config* c) {
   return 1;
 }
 
+// Tokens per batch a handle may hold (the embedding backward's radix sort
+// scans its chunk table in one CTA; 4M tokens is far beyond any workload).
+#define MAX_TOKENS ((long long)1 << 22)
+
 static int shape_ok(const gpt2_config* c, int maxB, int maxT) {
-  return maxB >= 1 && maxT >= 1 && maxT <= c->max_seq_len && (long long)maxB * maxT <= SORT_MAX;
+  return maxB >= 1 && maxT >= 1 && maxT <= c->max_seq_len && (long long)maxB * maxT <= MAX_TOKENS;
 }
 
 // Softmax-statistics blocks per row of the bf16 logits: one per BN/2 columns
@@ -168,6 +173,8 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->scratch_floats = s1 > s2 ? s1 : s2;
   p->scratch = take(p->scratch_floats * F);
   p->sorted = take(BT * sizeof(uint32_t));
+  p->sort_tmp = take(BT * sizeof(uint32_t));
+  p->radix_hist = take(256 * ((BT + RADIX_CHUNK - 1) / RADIX_CHUNK) * sizeof(int));
   p->tokens = take(BT * sizeof(int));
   p->targets = take(BT * sizeof(int));
   p->err = take(sizeof(int));
@@ -220,7 +227,8 @@ struct gpt2_t {
       *res3;
   float *lnf, *lnf_mean, *lnf_rstd, *logits, *dlogits, *losses, *loss;
   float *dres, *dln, *datty, *dqkv, *dfch, *attD, *scratch, *splitk, *splitk_w;
-  uint32_t* sorted;
+  uint32_t *sorted, *sort_tmp;
+  int* radix_hist;
   int *tokens, *targets, *err, *tilectr, *tilectr_w;
   uint16_t *ln1_bf, *qkv_bf, *atty_bf, *ln2_bf, *fchg_bf, *lnf_bf, *dlogits_bf, *dres_bf, *dfch_bf, *dqkv_bf,
       *datty_bf;
@@ -1350,12 +1358,28 @@ static int enqueue_backward(gpt2_t* m) {
       if (rc) return rc;
     }
   }
-  // embeddings
-  size_t smem = 1;
-  while ((int)smem < N) smem <<= 1;
-  launch_k(sort_tokens_kernel, 1, 1024, smem * sizeof(uint32_t), s, m->tokens, N, c.vocab_size, m->sorted);
-  launch_k(wte_grad_kernel, dim3(N, ceil_div(C, 128)), WTE_WARPS * 32, 0, s, G[P_WTE], m->dres, m->sorted, N, C);
-  m->launches += 2;
+  // embeddings: positions sorted by (id, position), then one CTA per id's run
+  const int V = c.vocab_size;
+  if (N <= SORT_MAX) {
+    size_t smem = 1;
+    while ((int)smem < N) smem <<= 1;
+    launch_k(sort_tokens_kernel, 1, 1024, smem * sizeof(uint32_t), s, (const int*)m->tokens, N, V, m->sorted);
+    m->launches++;
+  } else {  // stable radix sort by the id's low byte, then its high byte
+    const int nch = ceil_div(N, RADIX_CHUNK);
+    for (int pass = 0; pass < 2; pass++) {
+      const uint32_t* src = pass ? m->sort_tmp : nullptr;
+      uint32_t* dst = pass ? m->sorted : m->sort_tmp;
+      launch_k(radix_hist_kernel, nch, RADIX_THREADS, 0, s, (const int*)m->tokens, V, src, N, 8 * pass, m->radix_hist);
+      launch_k(radix_scan_kernel, 1, 1024, 0, s, m->radix_hist, 256 * nch);
+      launch_k(radix_scatter_kernel, nch, RADIX_THREADS, 0, s, (const int*)m->tokens, V, src, N, 8 * pass,
+               (const int*)m->radix_hist, dst);
+      m->launches += 3;
+    }
+  }
+  launch_k(wte_grad_kernel, dim3(N, ceil_div(C, 128)), WTE_WARPS * 32, 0, s, G[P_WTE], m->dres,
+           (const uint32_t*)m->sorted, (const int*)m->tokens, V, N, C);
+  m->launches++;
   if (!ll) {
     launch_k(wpe_grad_kernel, grid_for((long long)T * C / 4, 256), 256, 0, s, G[P_WPE], m->dres, B, T, C,
              m->grad_accumulate);
@@ -1487,7 +1511,8 @@ static int update_rest(gpt2_t* m, int N) {
   const int C = m->cfg.channels;
   timer_begin(m, TK_ADAMW, 0.0);  // the touched rows' bytes are not known on the host: counted as 0
   launch_k(adamw_sorted_rows_kernel, N, 256, 0, m->stream, m->params, (const float*)m->grads, m->m, m->v,
-           poff(m, P_WTE), C, (const uint32_t*)m->sorted, (const float*)m->hparams, m->params_bf);
+           poff(m, P_WTE), C, (const uint32_t*)m->sorted, (const int*)m->tokens, m->cfg.vocab_size,
+           (const float*)m->hparams, m->params_bf);
   timer_end(m, TK_ADAMW);
   m->launches++;
   KCHECK(m);
@@ -1539,6 +1564,7 @@ static void carve(gpt2_t* m) {
   CARVE(res2); CARVE(ln2); CARVE(ln2_mean); CARVE(ln2_rstd); CARVE(fch); CARVE(fchg); CARVE(res3);
   CARVE(lnf); CARVE(lnf_mean); CARVE(lnf_rstd); CARVE(logits); CARVE(dlogits); CARVE(losses); CARVE(loss);
   CARVE(dres); CARVE(dln); CARVE(datty); CARVE(dqkv); CARVE(dfch); CARVE(attD); CARVE(scratch); CARVE(sorted);
+  CARVE(sort_tmp); CARVE(radix_hist);
   CARVE(tokens); CARVE(targets); CARVE(err); CARVE(hparams); CARVE(splitk); CARVE(tilectr);
   CARVE(splitk_w); CARVE(tilectr_w);
   if (m->cfg.gemm_precision != GPT2_PREC_BF16) m->splitk_w = nullptr, m->tilectr_w = nullptr;

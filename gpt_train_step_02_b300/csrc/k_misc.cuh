@@ -75,12 +75,16 @@ __global__ void encoder_fwd_kernel(float* __restrict__ x, const int* __restrict_
 
 // ---------------------------------------------------------------------------
 // Embedding backward, deterministic under skewed token frequencies.
-//  1. sort_tokens_kernel: one CTA bitonic-sorts the keys (id << 14 | pos),
-//     which groups positions by id and keeps them in position order.
-//  2. wte_grad_kernel: the CTA at the first key of each id sums that id's
-//     gradient rows in a fixed order and adds the sum to dwte[id] once.
+//  1. Sort the positions 0..n-1 by (token id, position): sorted[i] is the
+//     i-th position of that order, so the positions of one id form a run, in
+//     increasing order.  Up to SORT_MAX positions one CTA bitonic-sorts the
+//     keys (id << 14 | pos) in shared memory (sort_tokens_kernel); beyond it a
+//     stable least-significant-digit radix sort by the id, two passes of 8
+//     bits (radix_hist_kernel, radix_scan_kernel, radix_scatter_kernel).
+//  2. wte_grad_kernel: the CTA at the first position of each id's run sums
+//     that id's gradient rows in a fixed order and adds the sum to dwte[id].
 //  3. wpe_grad_kernel: dwpe[t] += sum over b of dx[b,t].
-// Limits: B*T <= 16384 and V <= 65536 (keys fit 30 bits).
+// Limits: V <= 65536.
 // ---------------------------------------------------------------------------
 #define SORT_MAX 16384
 
@@ -112,7 +116,103 @@ __global__ void __launch_bounds__(1024) sort_tokens_kernel(const int* __restrict
       __syncthreads();
     }
   }
-  for (int i = threadIdx.x; i < n; i += blockDim.x) sorted[i] = keys[i];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) sorted[i] = keys[i] & 0x3FFFu;  // the position
+}
+
+// ---- stable radix sort of positions by token id (n > SORT_MAX) ------------
+// A pass sorts by digit (id >> shift) & 255 of the positions src[0..n)
+// (identity when src == NULL), keeping the order of equal digits.  Chunks of
+// RADIX_CHUNK positions: radix_hist_kernel counts each chunk's digits into
+// hist[digit * nchunks + chunk]; radix_scan_kernel turns that table, in that
+// (digit-major) order, into exclusive offsets; radix_scatter_kernel walks
+// its chunk in rounds of 256 positions (position order), ranking each
+// position among the equal digits before it (warp match, then warp counts in
+// warp order, then the counts of earlier rounds), and writes it to
+// dst[offset + rank].  Every count is an integer, so the result does not
+// depend on execution order.
+#define RADIX_THREADS 256
+#define RADIX_ROUNDS 16
+#define RADIX_CHUNK (RADIX_THREADS * RADIX_ROUNDS)
+
+GPT2_DEV uint32_t radix_digit(const int* ids, int V, uint32_t pos, int shift) {
+  return ((uint32_t)min(max(ids[pos], 0), V - 1) >> shift) & 255u;
+}
+
+__global__ void __launch_bounds__(RADIX_THREADS) radix_hist_kernel(const int* __restrict__ ids, int V,
+                                                                    const uint32_t* __restrict__ src, int n, int shift,
+                                                                    int* __restrict__ hist) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ int cnt[256];
+  cnt[threadIdx.x] = 0;
+  __syncthreads();
+  const int c0 = blockIdx.x * RADIX_CHUNK;
+  for (int i = c0 + threadIdx.x; i < min(n, c0 + RADIX_CHUNK); i += RADIX_THREADS)
+    atomicAdd(&cnt[radix_digit(ids, V, src ? src[i] : (uint32_t)i, shift)], 1);
+  __syncthreads();
+  hist[threadIdx.x * gridDim.x + blockIdx.x] = cnt[threadIdx.x];
+}
+
+// One CTA: exclusive prefix sum of hist[0..len) in index order.
+__global__ void __launch_bounds__(1024) radix_scan_kernel(int* __restrict__ hist, int len) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ int part[1024];
+  const int per = (len + 1023) / 1024, i0 = threadIdx.x * per, i1 = min(len, i0 + per);
+  int s = 0;
+  for (int i = i0; i < i1; i++) s += hist[i];
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {  // inclusive scan of the per-thread sums
+    const int v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int run = threadIdx.x ? part[threadIdx.x - 1] : 0;
+  for (int i = i0; i < i1; i++) {
+    const int c = hist[i];
+    hist[i] = run;
+    run += c;
+  }
+}
+
+__global__ void __launch_bounds__(RADIX_THREADS) radix_scatter_kernel(const int* __restrict__ ids, int V,
+                                                                       const uint32_t* __restrict__ src, int n,
+                                                                       int shift, const int* __restrict__ offs,
+                                                                       uint32_t* __restrict__ dst) {
+  pdl_launch_dependents();
+  pdl_wait();
+  constexpr int W = RADIX_THREADS / 32;
+  __shared__ int run[256];     // positions of each digit placed by earlier rounds
+  __shared__ int wcnt[W][256]; // this round's count of each digit per warp
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  run[threadIdx.x] = offs[threadIdx.x * gridDim.x + blockIdx.x];
+  const int c0 = blockIdx.x * RADIX_CHUNK;
+  for (int r = 0; r < RADIX_ROUNDS; r++) {
+    const int i = c0 + r * RADIX_THREADS + threadIdx.x;
+    const bool live = i < n;
+    const uint32_t pos = live ? (src ? src[i] : (uint32_t)i) : 0u;
+    const uint32_t d = live ? radix_digit(ids, V, pos, shift) : 256u;  // 256: no digit
+    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    const int before = __popc(peers & ((1u << lane) - 1u));
+    for (int k = threadIdx.x; k < W * 256; k += RADIX_THREADS) (&wcnt[0][0])[k] = 0;
+    __syncthreads();
+    if (live && before == 0) wcnt[warp][d] = __popc(peers);  // the warp's count of d, by its first lane
+    __syncthreads();
+    if (live) {
+      int rank = run[d] + before;
+      for (int w = 0; w < warp; w++) rank += wcnt[w][d];
+      dst[rank] = pos;
+    }
+    __syncthreads();
+    {  // digit threadIdx.x: add this round's counts
+      int add = 0;
+      for (int w = 0; w < W; w++) add += wcnt[w][threadIdx.x];
+      run[threadIdx.x] += add;
+    }
+    __syncthreads();
+  }
 }
 
 // grid: (n, ceil(C/128)); block: WTE_WARPS warps; lane l owns channels
@@ -123,20 +223,21 @@ __global__ void __launch_bounds__(1024) sort_tokens_kernel(const int* __restrict
 // in warp order: a fixed summation order for any run length.
 #define WTE_WARPS 8
 __global__ void __launch_bounds__(WTE_WARPS * 32) wte_grad_kernel(float* __restrict__ dwte, const float* __restrict__ dx,
-                                                                  const uint32_t* __restrict__ sorted, int n, int C) {
+                                                                  const uint32_t* __restrict__ sorted,
+                                                                  const int* __restrict__ ids, int V, int n, int C) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ int s_end;
   __shared__ float4 s_part[WTE_WARPS][32];
   const int i = blockIdx.x;
-  const uint32_t id = sorted[i] >> 14;
-  if (i > 0 && (sorted[i - 1] >> 14) == id) return;  // not the first key of its id (block-uniform)
+  const int id = min(max(ids[sorted[i]], 0), V - 1);
+  if (i > 0 && min(max(ids[sorted[i - 1]], 0), V - 1) == id) return;  // not the first of its id (block-uniform)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) s_end = n;
   __syncthreads();
   for (int base = i;; base += WTE_WARPS * 32) {
     const int j = base + threadIdx.x;
-    if (j < n && (sorted[j] >> 14) != id) atomicMin(&s_end, j);
+    if (j < n && min(max(ids[sorted[j]], 0), V - 1) != id) atomicMin(&s_end, j);
     __syncthreads();
     const int e = s_end;
     __syncthreads();
@@ -148,7 +249,7 @@ __global__ void __launch_bounds__(WTE_WARPS * 32) wte_grad_kernel(float* __restr
   if (c < C) {
 #pragma unroll 4
     for (int j = i + warp; j < end; j += WTE_WARPS) {
-      const int pos = (int)(sorted[j] & 0x3FFFu);
+      const int pos = (int)sorted[j];
       const float4 g = *reinterpret_cast<const float4*>(dx + (size_t)pos * C + c);
       acc.x += g.x; acc.y += g.y; acc.z += g.z; acc.w += g.w;
     }
@@ -328,18 +429,19 @@ __global__ void adamw_rows_kernel(float* __restrict__ p, const float* __restrict
   }
 }
 
-// AdamW of the rows of a (rows, C) tensor at element offset off named by the
-// sorted token keys of the embedding backward (id << 14 | pos):
-// one CTA per key; the CTA at the first key of each id updates that row.
+// AdamW of the rows of a (rows, C) tensor at element offset off that the
+// batch's tokens name, through the embedding backward's positions sorted by
+// id: one CTA per position; the CTA at the first position of each id updates
+// that row.
 __global__ void adamw_sorted_rows_kernel(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
                                          float* __restrict__ v, long long off, int C,
-                                         const uint32_t* __restrict__ sorted, const float* __restrict__ hp,
-                                         uint16_t* __restrict__ pbf16) {
+                                         const uint32_t* __restrict__ sorted, const int* __restrict__ ids, int V,
+                                         const float* __restrict__ hp, uint16_t* __restrict__ pbf16) {
   pdl_launch_dependents();
   pdl_wait();
   const int i = blockIdx.x;
-  const uint32_t id = sorted[i] >> 14;
-  if (i > 0 && (sorted[i - 1] >> 14) == id) return;
+  const int id = min(max(ids[sorted[i]], 0), V - 1);
+  if (i > 0 && min(max(ids[sorted[i - 1]], 0), V - 1) == id) return;
   const int C4 = C >> 2;
   for (int c4 = threadIdx.x; c4 < C4; c4 += blockDim.x) adamw_f4(p, g, m, v, off / 4 + (long long)id * C4 + c4, hp, pbf16);
 }

@@ -84,7 +84,8 @@ typedef struct gpt2_t gpt2_t;
 
 /* Device bytes one handle needs for batches up to (maxB, maxT): parameters,
  * gradients, AdamW m and v, activations, activation gradients and scratch.
- * Returns 0 for an invalid config or shape. */
+ * Returns 0 for an invalid config or shape (maxT > max_seq_len, or more than
+ * 4,194,304 tokens maxB * maxT). */
 size_t gpt2_arena_bytes(const gpt2_config* cfg, int maxB, int maxT);
 
 /* Creates a handle and initialises the parameters from `seed`: matrices
