@@ -500,7 +500,9 @@ def roofline_for(kind, k, peaks, w):
 
 
 # kernel-name fragments of each class in an ncu capture
-TRAFFIC_KERNELS = {"gemm": ("gemm_tf32x3", "gemm_bf16"), "adamw": ("adamw_kernel",), "xent": ("xent_fused_kernel",),
+TRAFFIC_KERNELS = {"gemm": ("gemm_tf32x3", "gemm_bf16"),
+                   "adamw": ("adamw_kernel", "adamw_rows_kernel", "adamw_sorted_rows_kernel"),
+                   "xent": ("xent_fused_kernel", "xent_bf16_kernel"),
                    "layernorm": ("layernorm_fwd_kernel", "layernorm_bwd_kernel"), "encoder": ("encoder_fwd_kernel",)}
 BYTE_UNITS = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
 
