@@ -65,7 +65,8 @@ struct Plan {
   size_t encoded, ln1, ln1_mean, ln1_rstd, qkv, atty, lse, res2, ln2, ln2_mean, ln2_rstd, fch, fchg, res3;
   size_t lnf, lnf_mean, lnf_rstd, logits, dlogits, losses, loss;
   size_t dres, dln, datty, dqkv, dfch, attD, scratch, sorted, tokens, targets, err, hparams, splitk, tilectr;
-  size_t sort_tmp, radix_hist;  // the embedding backward's radix sort (more than SORT_MAX tokens)
+  size_t sort_tmp, radix_hist;  // the embedding backward's radix sort (more than SORT_BITONIC_MAX tokens)
+  size_t runs;                  // where each id's run of sorted positions starts, and the run count
   // the split-K workspace and tile counters of the weight-gradient side stream (bf16 matmuls only)
   size_t splitk_w, tilectr_w;
   // bf16 operand copies (bf16 matmuls only)
@@ -175,6 +176,7 @@ static size_t plan_arena(const gpt2_config* c, int maxB, int maxT, Plan* p) {
   p->sorted = take(BT * sizeof(uint32_t));
   p->sort_tmp = take(BT * sizeof(uint32_t));
   p->radix_hist = take(256 * ((BT + RADIX_CHUNK - 1) / RADIX_CHUNK) * sizeof(int));
+  p->runs = take((BT + 1) * sizeof(int));  // the run starts, then their count
   p->tokens = take(BT * sizeof(int));
   p->targets = take(BT * sizeof(int));
   p->err = take(sizeof(int));
@@ -228,7 +230,7 @@ struct gpt2_t {
   float *lnf, *lnf_mean, *lnf_rstd, *logits, *dlogits, *losses, *loss;
   float *dres, *dln, *datty, *dqkv, *dfch, *attD, *scratch, *splitk, *splitk_w;
   uint32_t *sorted, *sort_tmp;
-  int* radix_hist;
+  int *radix_hist, *runs, *nruns;
   int *tokens, *targets, *err, *tilectr, *tilectr_w;
   uint16_t *ln1_bf, *qkv_bf, *atty_bf, *ln2_bf, *fchg_bf, *lnf_bf, *dlogits_bf, *dres_bf, *dfch_bf, *dqkv_bf,
       *datty_bf;
@@ -1360,7 +1362,7 @@ static int enqueue_backward(gpt2_t* m) {
   }
   // embeddings: positions sorted by (id, position), then one CTA per id's run
   const int V = c.vocab_size;
-  if (N <= SORT_MAX) {
+  if (N <= SORT_BITONIC_MAX) {
     size_t smem = 1;
     while ((int)smem < N) smem <<= 1;
     launch_k(sort_tokens_kernel, 1, 1024, smem * sizeof(uint32_t), s, (const int*)m->tokens, N, V, m->sorted);
@@ -1377,9 +1379,11 @@ static int enqueue_backward(gpt2_t* m) {
       m->launches += 3;
     }
   }
-  launch_k(wte_grad_kernel, dim3(N, ceil_div(C, 128)), WTE_WARPS * 32, 0, s, G[P_WTE], m->dres,
-           (const uint32_t*)m->sorted, (const int*)m->tokens, V, N, C);
-  m->launches++;
+  launch_k(run_starts_kernel, 1, 1024, 0, s, (const uint32_t*)m->sorted, (const int*)m->tokens, V, N, m->runs,
+           m->nruns);
+  launch_k(wte_grad_kernel, dim3(grid_for(N, 1, 4 * 148), ceil_div(C, 128)), WTE_WARPS * 32, 0, s, G[P_WTE], m->dres,
+           (const uint32_t*)m->sorted, (const int*)m->tokens, V, (const int*)m->runs, (const int*)m->nruns, N, C);
+  m->launches += 2;
   if (!ll) {
     launch_k(wpe_grad_kernel, grid_for((long long)T * C / 4, 256), 256, 0, s, G[P_WPE], m->dres, B, T, C,
              m->grad_accumulate);
@@ -1510,9 +1514,9 @@ static int update_rest(gpt2_t* m, int N) {
   m->side_u_last = -1;
   const int C = m->cfg.channels;
   timer_begin(m, TK_ADAMW, 0.0);  // the touched rows' bytes are not known on the host: counted as 0
-  launch_k(adamw_sorted_rows_kernel, N, 256, 0, m->stream, m->params, (const float*)m->grads, m->m, m->v,
-           poff(m, P_WTE), C, (const uint32_t*)m->sorted, (const int*)m->tokens, m->cfg.vocab_size,
-           (const float*)m->hparams, m->params_bf);
+  launch_k(adamw_sorted_rows_kernel, grid_for(N, 1, 4 * 148), 256, 0, m->stream, m->params, (const float*)m->grads,
+           m->m, m->v, poff(m, P_WTE), C, (const uint32_t*)m->sorted, (const int*)m->tokens, m->cfg.vocab_size,
+           (const int*)m->runs, (const int*)m->nruns, (const float*)m->hparams, m->params_bf);
   timer_end(m, TK_ADAMW);
   m->launches++;
   KCHECK(m);
@@ -1564,7 +1568,8 @@ static void carve(gpt2_t* m) {
   CARVE(res2); CARVE(ln2); CARVE(ln2_mean); CARVE(ln2_rstd); CARVE(fch); CARVE(fchg); CARVE(res3);
   CARVE(lnf); CARVE(lnf_mean); CARVE(lnf_rstd); CARVE(logits); CARVE(dlogits); CARVE(losses); CARVE(loss);
   CARVE(dres); CARVE(dln); CARVE(datty); CARVE(dqkv); CARVE(dfch); CARVE(attD); CARVE(scratch); CARVE(sorted);
-  CARVE(sort_tmp); CARVE(radix_hist);
+  CARVE(sort_tmp); CARVE(radix_hist); CARVE(runs);
+  m->nruns = m->runs + (size_t)m->maxB * m->maxT;
   CARVE(tokens); CARVE(targets); CARVE(err); CARVE(hparams); CARVE(splitk); CARVE(tilectr);
   CARVE(splitk_w); CARVE(tilectr_w);
   if (m->cfg.gemm_precision != GPT2_PREC_BF16) m->splitk_w = nullptr, m->tilectr_w = nullptr;

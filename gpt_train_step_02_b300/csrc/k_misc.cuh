@@ -77,16 +77,18 @@ __global__ void encoder_fwd_kernel(float* __restrict__ x, const int* __restrict_
 // Embedding backward, deterministic under skewed token frequencies.
 //  1. Sort the positions 0..n-1 by (token id, position): sorted[i] is the
 //     i-th position of that order, so the positions of one id form a run, in
-//     increasing order.  Up to SORT_MAX positions one CTA bitonic-sorts the
+//     increasing order.  Up to SORT_BITONIC_MAX positions one CTA bitonic-sorts the
 //     keys (id << 14 | pos) in shared memory (sort_tokens_kernel); beyond it a
 //     stable least-significant-digit radix sort by the id, two passes of 8
 //     bits (radix_hist_kernel, radix_scan_kernel, radix_scatter_kernel).
-//  2. wte_grad_kernel: the CTA at the first position of each id's run sums
-//     that id's gradient rows in a fixed order and adds the sum to dwte[id].
+//  2. run_starts_kernel lists where each id's run starts; wte_grad_kernel
+//     sums each run's gradient rows in a fixed order and adds the sum to
+//     dwte[id] once.
 //  3. wpe_grad_kernel: dwpe[t] += sum over b of dx[b,t].
 // Limits: V <= 65536.
 // ---------------------------------------------------------------------------
-#define SORT_MAX 16384
+#define SORT_MAX 16384         // the bitonic sort's capacity (its keys hold 14 position bits)
+#define SORT_BITONIC_MAX 2048  // up to this many positions the bitonic sort (one launch) is the faster
 
 __global__ void __launch_bounds__(1024) sort_tokens_kernel(const int* __restrict__ ids, int n, int V,
                                                           uint32_t* __restrict__ sorted) {
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(1024) sort_tokens_kernel(const int* __restrict
   for (int i = threadIdx.x; i < n; i += blockDim.x) sorted[i] = keys[i] & 0x3FFFu;  // the position
 }
 
-// ---- stable radix sort of positions by token id (n > SORT_MAX) ------------
+// ---- stable radix sort of positions by token id (n > SORT_BITONIC_MAX) ----
 // A pass sorts by digit (id >> shift) & 255 of the positions src[0..n)
 // (identity when src == NULL), keeping the order of equal digits.  Chunks of
 // RADIX_CHUNK positions: radix_hist_kernel counts each chunk's digits into
@@ -215,57 +217,77 @@ __global__ void __launch_bounds__(RADIX_THREADS) radix_scatter_kernel(const int*
   }
 }
 
-// grid: (n, ceil(C/128)); block: WTE_WARPS warps; lane l owns channels
-// 4*(blockIdx.y*32 + l) .. +3.  The block at the first sorted key of an id
-// finds the end of that id's run (256 keys per step, the first key of another
-// id taken with atomicMin, which does not depend on order), then warp w sums
-// the run's rows w, w + WTE_WARPS, ... in order and the warp sums are added
-// in warp order: a fixed summation order for any run length.
+// The runs of the sorted positions: runs[k] = the first index i of the k-th
+// run of equal ids (i == 0 or id(sorted[i]) != id(sorted[i-1])), in order;
+// *count = the number of runs.  One CTA: thread t scans the contiguous slice
+// [t per, (t+1) per), the slices' counts are scanned in thread order.
+__global__ void __launch_bounds__(1024) run_starts_kernel(const uint32_t* __restrict__ sorted,
+                                                          const int* __restrict__ ids, int V, int n,
+                                                          int* __restrict__ runs, int* __restrict__ count) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ int part[1024];
+  const int per = (n + 1023) / 1024, i0 = threadIdx.x * per, i1 = min(n, i0 + per);
+  auto id_at = [&](int i) { return min(max(ids[sorted[i]], 0), V - 1); };
+  int c = 0;
+  for (int i = i0; i < i1; i++) c += (i == 0 || id_at(i) != id_at(i - 1)) ? 1 : 0;
+  part[threadIdx.x] = c;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {
+    const int v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int k = threadIdx.x ? part[threadIdx.x - 1] : 0;
+  for (int i = i0; i < i1; i++)
+    if (i == 0 || id_at(i) != id_at(i - 1)) runs[k++] = i;
+  if (threadIdx.x == 1023) *count = part[1023];
+}
+
+// grid: (G, ceil(C/128)); block: WTE_WARPS warps; lane l owns channels
+// 4*(blockIdx.y*32 + l) .. +3.  CTA x walks the runs x, x + G, ...; for a run
+// (one id's positions, from runs[k] up to runs[k+1] or n), warp w sums the
+// run's rows w, w + WTE_WARPS, ... in order and the warp sums are added in
+// warp order: a fixed summation order for any run length.
 #define WTE_WARPS 8
 __global__ void __launch_bounds__(WTE_WARPS * 32) wte_grad_kernel(float* __restrict__ dwte, const float* __restrict__ dx,
                                                                   const uint32_t* __restrict__ sorted,
-                                                                  const int* __restrict__ ids, int V, int n, int C) {
+                                                                  const int* __restrict__ ids, int V,
+                                                                  const int* __restrict__ runs,
+                                                                  const int* __restrict__ nruns, int n, int C) {
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ int s_end;
   __shared__ float4 s_part[WTE_WARPS][32];
-  const int i = blockIdx.x;
-  const int id = min(max(ids[sorted[i]], 0), V - 1);
-  if (i > 0 && min(max(ids[sorted[i - 1]], 0), V - 1) == id) return;  // not the first of its id (block-uniform)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) s_end = n;
-  __syncthreads();
-  for (int base = i;; base += WTE_WARPS * 32) {
-    const int j = base + threadIdx.x;
-    if (j < n && min(max(ids[sorted[j]], 0), V - 1) != id) atomicMin(&s_end, j);
-    __syncthreads();
-    const int e = s_end;
-    __syncthreads();
-    if (e < base + WTE_WARPS * 32 || base + WTE_WARPS * 32 >= n) break;
-  }
-  const int end = s_end;
   const int c = (blockIdx.y * 32 + lane) * 4;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (c < C) {
+  const int count = *nruns;
+  for (int k = blockIdx.x; k < count; k += gridDim.x) {
+    const int i = runs[k], end = k + 1 < count ? runs[k + 1] : n;
+    const int id = min(max(ids[sorted[i]], 0), V - 1);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < C) {
 #pragma unroll 4
-    for (int j = i + warp; j < end; j += WTE_WARPS) {
-      const int pos = (int)sorted[j];
-      const float4 g = *reinterpret_cast<const float4*>(dx + (size_t)pos * C + c);
-      acc.x += g.x; acc.y += g.y; acc.z += g.z; acc.w += g.w;
+      for (int j = i + warp; j < end; j += WTE_WARPS) {
+        const int pos = (int)sorted[j];
+        const float4 g = *reinterpret_cast<const float4*>(dx + (size_t)pos * C + c);
+        acc.x += g.x; acc.y += g.y; acc.z += g.z; acc.w += g.w;
+      }
     }
-  }
-  s_part[warp][lane] = acc;
-  __syncthreads();
-  if (warp == 0 && c < C) {
-    float4 t = s_part[0][lane];
+    s_part[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0 && c < C) {
+      float4 t = s_part[0][lane];
 #pragma unroll
-    for (int w = 1; w < WTE_WARPS; w++) {
-      const float4 u = s_part[w][lane];
-      t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+      for (int w = 1; w < WTE_WARPS; w++) {
+        const float4 u = s_part[w][lane];
+        t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+      }
+      float4* d = reinterpret_cast<float4*>(dwte + (size_t)id * C + c);
+      const float4 o = *d;
+      *d = make_float4(o.x + t.x, o.y + t.y, o.z + t.z, o.w + t.w);
     }
-    float4* d = reinterpret_cast<float4*>(dwte + (size_t)id * C + c);
-    const float4 o = *d;
-    *d = make_float4(o.x + t.x, o.y + t.y, o.z + t.z, o.w + t.w);
+    __syncthreads();
   }
 }
 
@@ -430,20 +452,20 @@ __global__ void adamw_rows_kernel(float* __restrict__ p, const float* __restrict
 }
 
 // AdamW of the rows of a (rows, C) tensor at element offset off that the
-// batch's tokens name, through the embedding backward's positions sorted by
-// id: one CTA per position; the CTA at the first position of each id updates
-// that row.
+// batch's tokens name: the ids of the runs of the embedding backward's sorted
+// positions.  CTA x updates the rows of runs x, x + gridDim.x, ...
 __global__ void adamw_sorted_rows_kernel(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
                                          float* __restrict__ v, long long off, int C,
                                          const uint32_t* __restrict__ sorted, const int* __restrict__ ids, int V,
+                                         const int* __restrict__ runs, const int* __restrict__ nruns,
                                          const float* __restrict__ hp, uint16_t* __restrict__ pbf16) {
   pdl_launch_dependents();
   pdl_wait();
-  const int i = blockIdx.x;
-  const int id = min(max(ids[sorted[i]], 0), V - 1);
-  if (i > 0 && min(max(ids[sorted[i - 1]], 0), V - 1) == id) return;
-  const int C4 = C >> 2;
-  for (int c4 = threadIdx.x; c4 < C4; c4 += blockDim.x) adamw_f4(p, g, m, v, off / 4 + (long long)id * C4 + c4, hp, pbf16);
+  const int C4 = C >> 2, count = *nruns;
+  for (int k = blockIdx.x; k < count; k += gridDim.x) {
+    const int id = min(max(ids[sorted[runs[k]]], 0), V - 1);
+    for (int c4 = threadIdx.x; c4 < C4; c4 += blockDim.x) adamw_f4(p, g, m, v, off / 4 + (long long)id * C4 + c4, hp, pbf16);
+  }
 }
 
 // mask[ids[i]] = 1 for every i < n (the rows of wte a batch touches)
