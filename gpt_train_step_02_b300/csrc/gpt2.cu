@@ -574,19 +574,6 @@ static int make_bf16_map(CUtensorMap* tm, const uint16_t* base, int kmajor, long
   return r == CUDA_SUCCESS;
 }
 
-// K splits for the persistent bf16 kernel: only when there are fewer output
-// tiles than SMs, keeping at least four 64-wide K tiles per split.
-static int choose_splits_bf16(int M, int N, int K, int BN, long long ws_floats) {
-  long long tiles = (long long)ceil_div(M, tcb::BM) * ceil_div(N, BN);
-  int kt = ceil_div(K, tcb::BK);
-  if (tiles >= 148 || kt < 8) return 1;
-  int s = (int)(148 / tiles);
-  s = s < kt / 4 ? s : kt / 4;
-  while (s > 1 && (long long)s * M * N > ws_floats) s--;
-  if (s < 1) s = 1;
-  int per = ceil_div(kt, s);
-  return ceil_div(kt, per);
-}
 
 template <int BN>
 static void launch_bf16_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const tcb::Params& p, int grid,
@@ -618,20 +605,41 @@ static cudaError_t set_bf16_smem() {
   return e;
 }
 
-// Column width of the bf16 matmul's output tiles: 128 x 256 tiles when they
-// alone fill the SMs; otherwise 128 x 128 tiles, which halve the K splits (and
-// their partial-tile traffic) needed to fill them.
-static int bf16_tile_n(int M, int N) {
+// Output tiles and K splits of the persistent bf16 matmul.  128 x 256 tiles
+// when they come within two thirds of a full wave of the SMs (the rest of
+// that wave idles, but a 128 x 256 tile does its work at a higher rate than
+// two 128 x 128 ones, which also read A twice); otherwise 128 x 128 tiles,
+// which halve the K splits (and their partial-tile traffic) needed to fill
+// the SMs.  K is split only when the tiles do not fill the SMs, keeping at
+// least four 64-wide K tiles per split; never for the epilogues that take
+// column sums or row statistics (no_split).
+struct Bf16Plan {
+  int BN, splits;
+};
+
+static Bf16Plan plan_bf16(int M, int N, int K, bool no_split, long long ws_floats, int num_sms) {
   const long long tiles256 = (long long)ceil_div(M, tcb::BM) * ceil_div(N, 256);
-  return (N > 128 && tiles256 >= 148) ? 256 : 128;
+  const int BN = (N > 128 && 3 * tiles256 >= 2 * num_sms) ? 256 : 128;
+  const long long tiles = (long long)ceil_div(M, tcb::BM) * ceil_div(N, BN);
+  const int kt = ceil_div(K, tcb::BK);
+  if (no_split || tiles >= num_sms || kt < 8) return {BN, 1};
+  int s = (int)(num_sms / tiles);
+  s = s < kt / 4 ? s : kt / 4;
+  while (s > 1 && (long long)s * M * N > ws_floats) s--;
+  if (s < 1) s = 1;
+  const int per = ceil_div(kt, s);
+  return {BN, ceil_div(kt, per)};
 }
 
-// Launches the persistent bf16 tensor-core matmul.  Returns 1, or -1 on a
+// Launches the persistent bf16 tensor-core matmul.// Launches the persistent bf16 tensor-core matmul.  Returns 1, or -1 on a
 // host-side failure.
 static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int* err, cudaStream_t s,
                               long long ws_floats = SPLITK_WS_FLOATS) {
   if (!d.Abf || !d.Bbf) return -1;
-  const int BN = bf16_tile_n(d.M, d.N);
+  // column sums and the row statistics are taken in the warp epilogue, which a K split bypasses
+  const bool no_split = d.epi.colsum || d.epi.epi == EPI_LOGITS;
+  const Bf16Plan plan = plan_bf16(d.M, d.N, d.K, no_split, ws_floats, dev_info().num_sms);
+  const int BN = plan.BN;
   CUtensorMap ta, tb;
   if (!make_bf16_map(&ta, d.Abf, d.a_kmajor, d.a_kmajor ? d.M : d.K, d.a_kmajor ? d.K : d.M, d.lda, tcb::BM))
     return -1;
@@ -642,9 +650,7 @@ static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int
   p.K = d.K;
   p.a_kmajor = d.a_kmajor;
   p.b_kmajor = d.b_kmajor;
-  // column sums are taken in the warp epilogue, which a K split bypasses
-  // (and so do the softmax statistics of the LM head)
-  p.splits = (d.epi.colsum || d.epi.epi == EPI_LOGITS) ? 1 : choose_splits_bf16(d.M, d.N, d.K, BN, ws_floats);
+  p.splits = plan.splits;
   if (d.epi.epi == EPI_LOGITS && (!d.epi.vec4 || !d.epi.Cbf || d.epi.C)) return -1;
   if (d.epi.colsum && (!d.epi.vec4 || d.N % 32 || (d.epi.ldcs & 3) || ((uintptr_t)d.epi.colsum & 15))) return -1;
   p.k_tiles = ceil_div(d.K, tcb::BK);
@@ -657,7 +663,8 @@ static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int
   p.partial = p.splits > 1 ? ws : nullptr;
   p.tile_ctr = tile_ctr;
   p.err = err;
-  int grid = p.units < 148 ? p.units : 148;
+  const int nsm = dev_info().num_sms;
+  int grid = p.units < nsm ? p.units : nsm;
   if (BN == 256) launch_bf16_kernel<256>(ta, tb, p, grid, s);
   else launch_bf16_kernel<128>(ta, tb, p, grid, s);
   return 1;
@@ -1256,7 +1263,9 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
   }
   m->logits_in_bf = xbf ? 1 : 0;
   if (xbf) {
-    const int nblk = ceil_div(Vp, bf16_tile_n(N, Vp) / 2), ldxs = (int)xstats_pitch(Vp);
+    // the LM head's tile width, as its launch chose it (EPI_LOGITS: no split)
+    const int bn = plan_bf16(N, Vp, C, true, SPLITK_WS_FLOATS, dev_info().num_sms).BN;
+    const int nblk = ceil_div(Vp, bn / 2), ldxs = (int)xstats_pitch(Vp);
     // reads the bf16 logits and the statistics, writes the bf16 dlogits
     timer_begin(m, TK_XENT, (double)N * (4.0 * Vp + 8.0 * nblk + 8.0));
     launch_k(xent_bf16_kernel, N, XENT_BF_THREADS, 0, s, m->dlogits_bf, m->losses, (const uint16_t*)m->logits_bf,
