@@ -458,37 +458,52 @@ def recorded_traffic(kind, w):
     return rec["dram_bytes_per_launch"]
 
 
+def tf32_peak(peaks):
+    """Dense TF32 rate for the 3xTF32 kernels: the rate measured in this run
+    (cuBLAS, TF32 allowed), else the bf16 burst figure x the nominal ratio."""
+    if peaks.get("tf32_tflops"):
+        return peaks["tf32_tflops"], peaks["tf32_source"]
+    return (peaks["bf16_tflops"] * 1.1 / 2.25,
+            f"{peaks['source']} bf16 dense burst x nominal tf32/bf16 ratio 1.1/2.25")
+
+
+def bf16_peak(peaks):
+    """Dense bf16 rate for kernels timed inside a long graph-replayed step at
+    the power cap: the sustained figure when it was measured, else the burst."""
+    if peaks.get("bf16_tflops_sustained"):
+        return peaks["bf16_tflops_sustained"], f"{peaks['source']} bf16 dense sustained"
+    return peaks["bf16_tflops"], f"{peaks['source']} bf16 dense burst"
+
+
+def tensor_line(kernel, achieved, peaks, w, three_mmas, traffic=None):
+    """A tensor-bound roofline entry: 3xTF32 kernels against the TF32 rate
+    (three MMAs per product, so a third of it is their ceiling), bf16 kernels
+    against the sustained bf16 rate (the burst fraction alongside)."""
+    if three_mmas:
+        peak, src = tf32_peak(peaks)
+        return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "frac_of_3xtf32_ceiling": 3.0 * achieved / peak, "traffic": traffic,
+                "peak_source": src + "; 3 MMAs per product"}
+    peak, src = bf16_peak(peaks)
+    return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "frac_of_burst": achieved / peaks["bf16_tflops"], "traffic": traffic,
+            "peak_source": src}
+
+
 def roofline_for(kind, k, peaks, w):
     if kind == "gemm":
+        # fp32 matmuls run as 3xTF32 on tcgen05 kind::tf32, bf16 ones on kind::f16
         achieved = k["work_per_launch"] / (k["avg_launch_ms"] * 1e-3) / 1e12
-        if w.precision == "fp32":
-            # fp32 matmuls run as 3xTF32 on tcgen05 kind::tf32 against the
-            # measured dense TF32 rate (nominal ratio to bf16 when it is absent);
-            # each product takes three MMAs, so 1/3 of this peak is the ceiling
-            if peaks.get("tf32_tflops"):
-                peak, src = peaks["tf32_tflops"], peaks["tf32_source"]
-            else:
-                peak = peaks["bf16_tflops"] * 1.1 / 2.25
-                src = f"{peaks['source']} bf16 dense burst x nominal tf32/bf16 ratio 1.1/2.25"
-            return {"kernel": "matmul (all tcgen05 launches of the step)", "bound": "tensor", "achieved": achieved,
-                    "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                    "frac_of_3xtf32_ceiling": 3.0 * achieved / peak, "traffic": recorded_traffic(kind, w),
-                    "peak_source": src + "; 3 MMAs per product"}
-        peak = peaks["bf16_tflops"]
-        out = {"kernel": "matmul (all tcgen05 launches of the step)", "bound": "tensor", "achieved": achieved,
-               "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(kind, w),
-               "peak_source": f"{peaks['source']} bf16 dense burst"}
-        if peaks.get("bf16_tflops_sustained"):
-            out["frac_of_sustained"] = achieved / peaks["bf16_tflops_sustained"]
-        return out
+        return tensor_line("matmul (all tcgen05 launches of the step)", achieved, peaks, w, w.precision == "fp32",
+                           recorded_traffic(kind, w))
     if kind in ("attn_fwd", "attn_bwd"):
         # the timer's work figure is FLOPs: 4 (forward) or 8 (backward) x B NH hs T(T+1)/2
         achieved = k["work_per_launch"] / (k["avg_launch_ms"] * 1e-3) / 1e12
         hs = w.channels // w.num_heads
         if w.precision == "bf16" and hs == 64 and w.T % 128 == 0:  # tcgen05 kind::f16 products
-            return {"kernel": kind, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
-                    "peak_source": f"{peaks['source']} bf16 dense burst"}
+            return tensor_line(kind, achieved, peaks, w, False)
+        if w.precision == "fp32" and hs == 64 and w.T <= 64:  # tcgen05 kind::tf32, 3xTF32 products
+            return tensor_line(kind, achieved, peaks, w, True)
         # CUDA-core fp32: 148 SMs x 128 FMA lanes x 2 FLOPs x the maximum SM clock
         peak = 148 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
         return {"kernel": kind, "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

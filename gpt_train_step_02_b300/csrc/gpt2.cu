@@ -864,7 +864,8 @@ static K ln_pick(int C, K k1, K k2, K k4, K k6, K k8, K k10) {
 static void ln_forward(gpt2_t* m, float* y, uint16_t* ybf, float* mean, float* rstd, const float* x, const float* w,
                        const float* b, int N) {
   int C = m->cfg.channels;
-  timer_begin(m, TK_LAYERNORM, (8.0 * C + 8.0) * N);
+  // read x; write y (fp32) and/or its bf16 copy; mean and rstd
+  timer_begin(m, TK_LAYERNORM, (4.0 * C + (y ? 4.0 * C : 0.0) + (ybf ? 2.0 * C : 0.0) + 8.0) * N);
   if (m->cfg.llama) {  // RMSNorm: no mean, no shift
     auto k = ln_pick(C, layernorm_fwd_kernel<1, true>, layernorm_fwd_kernel<2, true>, layernorm_fwd_kernel<4, true>,
                      layernorm_fwd_kernel<6, true>, layernorm_fwd_kernel<8, true>, layernorm_fwd_kernel<10, true>);
@@ -887,23 +888,46 @@ static void ln_backward(gpt2_t* m, float* dx, uint16_t* dxbf, float* dw, float* 
   const int nb = ceil_div(N, LNB_WARPS);  // one row per warp
   const bool rms = m->cfg.llama != 0;        // RMSNorm: dw only (no shift, no linear biases)
   const int nout = rms ? 1 : (dxsum ? 3 : 2);
-  timer_begin(m, TK_LAYERNORM, (16.0 * C + 8.0) * N);
+  // read dy, x, mean, rstd and dx; write dx (and its bf16 copy)
+  timer_begin(m, TK_LAYERNORM, (16.0 * C + 8.0 + (dxbf ? 2.0 * C : 0.0)) * N);
   side_wait(m, &m->rd_scratch);  // the partials below overwrite the scratch
   if (dx == m->dres) side_wait(m, &m->wd_dres);
-  const size_t smem = (size_t)LNB_WARPS * nout * C * sizeof(float);
-  if (rms) {
-    auto k = ln_pick(C, layernorm_bwd_kernel<1, true>, layernorm_bwd_kernel<2, true>, layernorm_bwd_kernel<4, true>,
-                     layernorm_bwd_kernel<6, true>, layernorm_bwd_kernel<8, true>, layernorm_bwd_kernel<10, true>);
-    launch_k(k, nb, LNB_WARPS * 32, smem, m->stream, dx, dxbf, m->scratch, dy, x, w, mean, rstd, N, C, 0);
+  const int wds = dxsum ? 1 : 0;
+  int nparts = nb;  // partial rows the column finish sums
+  const int nsm = dev_info().num_sms;
+  if (nb > 2 * nsm) {
+    // many rows: one block per SM walking the rows, one partial row per block
+    const int W = ln_pick(C, LnbStride<1>::WARPS, LnbStride<2>::WARPS, LnbStride<4>::WARPS, LnbStride<6>::WARPS,
+                          LnbStride<8>::WARPS, LnbStride<10>::WARPS);
+    const size_t smem = (size_t)W * nout * C * sizeof(float);
+    nparts = nsm;
+    if (rms) {
+      auto k = ln_pick(C, layernorm_bwd_stride_kernel<1, true>, layernorm_bwd_stride_kernel<2, true>,
+                       layernorm_bwd_stride_kernel<4, true>, layernorm_bwd_stride_kernel<6, true>,
+                       layernorm_bwd_stride_kernel<8, true>, layernorm_bwd_stride_kernel<10, true>);
+      launch_k(k, nsm, W * 32, smem, m->stream, dx, dxbf, m->scratch, dy, x, w, mean, rstd, N, C, 0);
+    } else {
+      auto k = ln_pick(C, layernorm_bwd_stride_kernel<1, false>, layernorm_bwd_stride_kernel<2, false>,
+                       layernorm_bwd_stride_kernel<4, false>, layernorm_bwd_stride_kernel<6, false>,
+                       layernorm_bwd_stride_kernel<8, false>, layernorm_bwd_stride_kernel<10, false>);
+      launch_k(k, nsm, W * 32, smem, m->stream, dx, dxbf, m->scratch, dy, x, w, mean, rstd, N, C, wds);
+    }
   } else {
-    auto k = ln_pick(C, layernorm_bwd_kernel<1, false>, layernorm_bwd_kernel<2, false>, layernorm_bwd_kernel<4, false>,
-                     layernorm_bwd_kernel<6, false>, layernorm_bwd_kernel<8, false>, layernorm_bwd_kernel<10, false>);
-    launch_k(k, nb, LNB_WARPS * 32, smem, m->stream, dx, dxbf, m->scratch, dy, x, w, mean, rstd, N, C, dxsum ? 1 : 0);
+    const size_t smem = (size_t)LNB_WARPS * nout * C * sizeof(float);
+    if (rms) {
+      auto k = ln_pick(C, layernorm_bwd_kernel<1, true>, layernorm_bwd_kernel<2, true>, layernorm_bwd_kernel<4, true>,
+                       layernorm_bwd_kernel<6, true>, layernorm_bwd_kernel<8, true>, layernorm_bwd_kernel<10, true>);
+      launch_k(k, nb, LNB_WARPS * 32, smem, m->stream, dx, dxbf, m->scratch, dy, x, w, mean, rstd, N, C, 0);
+    } else {
+      auto k = ln_pick(C, layernorm_bwd_kernel<1, false>, layernorm_bwd_kernel<2, false>, layernorm_bwd_kernel<4, false>,
+                       layernorm_bwd_kernel<6, false>, layernorm_bwd_kernel<8, false>, layernorm_bwd_kernel<10, false>);
+      launch_k(k, nb, LNB_WARPS * 32, smem, m->stream, dx, dxbf, m->scratch, dy, x, w, mean, rstd, N, C, wds);
+    }
   }
   // dw[c] (+)= sum_b partial[b][c], db[c] (+)= sum_b partial[b][C + c], dxsum[c] (+)= ...[2C + c]
   cudaStream_t st;
   const int d = side_fork(m, &st);
-  launch_k(col_finish_kernel, ceil_div(nout * C, 32), COLF_WARPS * 32, 0, st, dw, db, dxsum, C, m->scratch, nb,
+  launch_k(col_finish_kernel, ceil_div(nout * C, 32), COLF_WARPS * 32, 0, st, dw, db, dxsum, C, m->scratch, nparts,
            nout * C, m->grad_accumulate);
   side_done(m, d, &m->rd_scratch);
   timer_end(m, TK_LAYERNORM);
@@ -1112,6 +1136,16 @@ static int set_kernel_attributes() {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<10, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(layernorm_bwd_kernel<10, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lnb);
+    // the row-walking variant: LnbStride::WARPS slots of 3 x 128 V4 floats
+#define LNB_STRIDE_ATTR(V4)                                                                                   \
+  if (e == cudaSuccess)                                                                                       \
+    e = cudaFuncSetAttribute(layernorm_bwd_stride_kernel<V4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             LnbStride<V4>::WARPS * 3 * 128 * V4 * (int)sizeof(float));                       \
+  if (e == cudaSuccess)                                                                                       \
+    e = cudaFuncSetAttribute(layernorm_bwd_stride_kernel<V4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
+                             LnbStride<V4>::WARPS * 3 * 128 * V4 * (int)sizeof(float));
+    LNB_STRIDE_ATTR(1) LNB_STRIDE_ATTR(2) LNB_STRIDE_ATTR(4) LNB_STRIDE_ATTR(6) LNB_STRIDE_ATTR(8) LNB_STRIDE_ATTR(10)
+#undef LNB_STRIDE_ATTR
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(atf::attn_fwd_tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)atf::FWD_SMEM);

@@ -159,3 +159,101 @@ __global__ void __launch_bounds__(LNB_WARPS * 32) layernorm_bwd_kernel(
     partial[(size_t)blockIdx.x * nout * C + c] = t;
   }
 }
+
+// Backward for many rows (the host takes it when there are more row groups
+// than twice the SM count): one block per SM, LnbStride::WARPS warps, and
+// warp w of block b takes rows b W + w, b W + w + G W, ... (G blocks).  Each
+// warp adds its rows' contributions, in row order, into its own
+// shared-memory slot; the block then sums its slots in warp order into
+// partial[blockIdx][...] (the same three column groups as above), so the
+// column finish reads G rows instead of one per eight rows.  The row arithmetic is that of
+// layernorm_bwd_kernel.  The warp count fills the register file (x, dy and
+// dx of a row live in registers: each of the four schedulers of an SM holds
+// a quarter of the warps in its 16K registers) within the shared memory of
+// one block.
+template <int LN_MAXV4>
+struct LnbStride {
+  static constexpr int WARPS = LN_MAXV4 >= 8 ? 12 : (LN_MAXV4 >= 6 ? 16 : 20);
+};
+
+template <int LN_MAXV4, bool RMS>
+__global__ void __launch_bounds__(LnbStride<LN_MAXV4>::WARPS * 32, 1) layernorm_bwd_stride_kernel(
+    float* __restrict__ dx, uint16_t* __restrict__ dxbf, float* __restrict__ partial, const float* __restrict__ dy,
+    const float* __restrict__ x, const float* __restrict__ w, const float* __restrict__ mean,
+    const float* __restrict__ rstd, int N, int C, int with_dxsum) {
+  pdl_launch_dependents();
+  pdl_wait();
+  constexpr int W = LnbStride<LN_MAXV4>::WARPS;
+  extern __shared__ float sh[];  // [W][nout * C]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nout = RMS ? 1 : (with_dxsum ? 3 : 2);
+  float* my = sh + warp * nout * C;
+  for (int c = lane; c < nout * C; c += 32) my[c] = 0.f;
+  __syncwarp();
+  for (int r = blockIdx.x * W + warp; r < N; r += gridDim.x * W) {
+    const float mu = mean[r], rs = rstd[r];
+    float4 xv[LN_MAXV4], dv[LN_MAXV4], av[LN_MAXV4];
+    float sg = 0.f, sgn = 0.f;
+#pragma unroll
+    for (int k = 0; k < LN_MAXV4; k++) {
+      const int c = (lane + 32 * k) * 4;
+      if (c < C) {
+        xv[k] = *reinterpret_cast<const float4*>(x + (size_t)r * C + c);
+        dv[k] = *reinterpret_cast<const float4*>(dy + (size_t)r * C + c);
+        av[k] = *reinterpret_cast<const float4*>(dx + (size_t)r * C + c);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < LN_MAXV4; k++) {
+      const int c = (lane + 32 * k) * 4;
+      if (c < C) {
+        const float4 ww = *reinterpret_cast<const float4*>(w + c);
+        const float n0 = (xv[k].x - mu) * rs, n1 = (xv[k].y - mu) * rs, n2 = (xv[k].z - mu) * rs,
+                    n3 = (xv[k].w - mu) * rs;
+        const float g0 = dv[k].x * ww.x, g1 = dv[k].y * ww.y, g2 = dv[k].z * ww.z, g3 = dv[k].w * ww.w;
+        sg += (g0 + g1) + (g2 + g3);
+        sgn += (g0 * n0 + g1 * n1) + (g2 * n2 + g3 * n3);
+      }
+    }
+    const float mg = RMS ? 0.f : warp_sum(sg) / (float)C, mgn = warp_sum(sgn) / (float)C;
+#pragma unroll
+    for (int k = 0; k < LN_MAXV4; k++) {
+      const int c = (lane + 32 * k) * 4;
+      if (c < C) {
+        const float4 ww = *reinterpret_cast<const float4*>(w + c);
+        const float4 n = make_float4((xv[k].x - mu) * rs, (xv[k].y - mu) * rs, (xv[k].z - mu) * rs,
+                                     (xv[k].w - mu) * rs);
+        float4* o = reinterpret_cast<float4*>(dx + (size_t)r * C + c);
+        float4 a = av[k];
+        a.x += rs * (dv[k].x * ww.x - mg - n.x * mgn);
+        a.y += rs * (dv[k].y * ww.y - mg - n.y * mgn);
+        a.z += rs * (dv[k].z * ww.z - mg - n.z * mgn);
+        a.w += rs * (dv[k].w * ww.w - mg - n.w * mgn);
+        *o = a;
+        if (dxbf) {
+          *reinterpret_cast<uint2*>(dxbf + (size_t)r * C + c) = make_uint2(bf16x2_bits(a.x, a.y), bf16x2_bits(a.z, a.w));
+        }
+        float4* s0 = reinterpret_cast<float4*>(my + c);
+        float4 u = *s0;
+        *s0 = make_float4(u.x + dv[k].x * n.x, u.y + dv[k].y * n.y, u.z + dv[k].z * n.z, u.w + dv[k].w * n.w);
+        if (!RMS) {
+          float4* s1 = reinterpret_cast<float4*>(my + C + c);
+          u = *s1;
+          *s1 = make_float4(u.x + dv[k].x, u.y + dv[k].y, u.z + dv[k].z, u.w + dv[k].w);
+          if (with_dxsum) {
+            float4* s2 = reinterpret_cast<float4*>(my + 2 * C + c);
+            u = *s2;
+            *s2 = make_float4(u.x + a.x, u.y + a.y, u.z + a.z, u.w + a.w);
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < nout * C; c += blockDim.x) {
+    float t = sh[c];
+#pragma unroll 4
+    for (int wv = 1; wv < W; wv++) t += sh[wv * nout * C + c];
+    partial[(size_t)blockIdx.x * nout * C + c] = t;
+  }
+}

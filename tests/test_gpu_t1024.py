@@ -171,3 +171,43 @@ def test_wide_channel_layer_parity(C, NH, T, prec):
     for name, (off, n) in synth.param_offsets(w).items():
         e = rel_l2(gg[off:off + n], go[off:off + n])
         assert e <= (1e-3 if fp32 else 3e-2), (name, e)
+
+
+@pytest.mark.parametrize("C,NH,llama", [(768, 12, 0), (1024, 16, 0), (1280, 20, 0), (1024, 16, 1)])
+def test_layernorm_backward_many_rows(C, NH, llama):
+    """2560 rows (B = 40, T = 64): more row groups of eight than twice the SM
+    count, so the layernorm backward takes its row-walking form (one block per
+    SM, each warp summing its rows' gain and shift gradients in its own slot).
+    One fp32 layer at the 124M / 350M / 774M channel counts, and RMSNorm at
+    1024: loss 1e-5 relative, every gradient 1e-3 relative L2."""
+    import gpt_train_step_02_b300 as g
+
+    w = synth.Workload(f"ln_rows_C{C}_ll{llama}", 1, C, NH, 512, 512, 64, 40, 64, "fp32", "uniform", 1,
+                       llama=llama)
+    p0 = synth.init_params(w)
+    rng = np.random.default_rng(12)
+    for name, (o, n) in synth.param_offsets(w).items():
+        if name in ("ln1w", "ln2w", "lnfw"):
+            p0[o:o + n] += (0.1 * rng.standard_normal(n)).astype(np.float32)
+        elif not llama and name in ("ln1b", "ln2b", "lnfb", "qkvb", "attprojb", "fcb", "fcprojb"):
+            p0[o:o + n] = (0.02 * rng.standard_normal(n)).astype(np.float32)
+    inp, tgt = synth.batch(w)
+    m = g.GPT2(w)
+    m.set_params(p0)
+    o = ref.RefModel(ref.config_from(w), w.B, w.T, np.float32)
+    o.set_params(p0)
+    lg = m.forward(inp, tgt)
+    lo = o.forward(inp, tgt)
+    assert abs(lg - lo) <= 1e-5 * abs(lo), (lg, lo)
+    m.zero_grad()
+    m.backward()
+    o.zero_grad()
+    o.backward()
+    gg, go = m.get_grads(), o.grads.copy()
+    m.close()
+    o.close()
+    for name, (off, n) in synth.param_offsets(w).items():
+        if n == 0:
+            continue
+        e = rel_l2(gg[off:off + n], go[off:off + n])
+        assert e <= 1e-3, (name, e)
