@@ -1019,14 +1019,15 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
   const bool tc_path = bf && qkv_bf && dy_bf && hs == tca::HS && T % tca::BQ == 0;
   if (!tc_path && attn_tf32_path(bf, hs, T)) {  // fp32, short sequences: dQ and dK/dV kernels, 3xTF32 products
     if (!dqkv || colsum) return -1;
-    CUtensorMap tq, td;
+    CUtensorMap tq, td, ty;
     if (!make_f32_box64_map(&tq, qkv, (long long)B * T, 3LL * C, 3LL * C)) return -1;
     if (!make_f32_box64_map(&td, dy, (long long)B * T, C, C)) return -1;
+    if (!make_f32_box64_map(&ty, atty, (long long)B * T, C, C)) return -1;
     atf::Params p = {};
     p.B = B; p.T = T; p.C = C; p.NH = NH;
     p.scale = 1.0f / sqrtf((float)hs);
     p.qkv = qkv; p.dy = dy; p.y = atty; p.out = dqkv; p.out_bf = dqkv_bf; p.lse = (float*)lse; p.err = err;
-    launch_k(atf::attn_bwd_tf32_kernel, dim3(NH, B, 2), atf::THREADS, atf::BWD_SMEM, s, tq, td, p);
+    launch_k(atf::attn_bwd_tf32_kernel, dim3(NH, B, 2), atf::THREADS, atf::BWD_SMEM, s, tq, td, ty, p);
     return 1;
   }
   if (!tc_path && T <= atts::T_MAX && hs == atts::HS) {  // short sequences: one launch, D formed in the kernel

@@ -117,11 +117,14 @@ GPT2_DEV void st_half_split(uint32_t tlane, int col, int half, const float* v) {
   }
 }
 
-// 32 floats at src (16-byte aligned) into v, or zeros when !valid.
-GPT2_DEV void ld_half32(const float* src, bool valid, float* v) {
+// This thread's 32 values of row r (columns [32 half, +32)) of a TMA-written
+// swizzled tile, or zeros when !valid.  The 32 lanes of a warp read 32
+// consecutive rows: each 16-byte load touches every bank once per 8 lanes.
+GPT2_DEV void ld_tile_half(const float* tile, int r, int half, bool valid, float* v) {
 #pragma unroll
   for (int q = 0; q < 8; q++) {
-    const float4 x = valid ? __ldg(reinterpret_cast<const float4*>(src) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 x = valid ? *reinterpret_cast<const float4*>(tile + sw(r, 32 * half + 4 * q))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
     v[4 * q] = x.x;
     v[4 * q + 1] = x.y;
     v[4 * q + 2] = x.z;
@@ -188,9 +191,11 @@ struct Smem {
   static constexpr int OFF_VEC = OFF_BAR + 64;
   static constexpr int BYTES = OFF_VEC + 5 * 64 * 4 + 1024;
 };
-constexpr int FWD_TILES = 4;  // K (hi, lo), V^T (hi, lo)
-constexpr int DQ_TILES = 6;   // K (hi, lo), V (hi, lo), K^T (hi, lo)
-constexpr int DKV_TILES = 8;  // Q (hi, lo), dY (hi, lo), Q^T (hi, lo), dY^T (hi, lo)
+// Every tile of the head's rows comes in by TMA; the threads read their rows
+// out of the raw tiles (Q, V, Y, ... below) instead of from global memory.
+constexpr int FWD_TILES = 6;   // K (hi, lo), V^T (hi, lo), raw Q, raw V
+constexpr int DQ_TILES = 9;    // K (hi, lo), V (hi, lo), K^T (hi, lo), raw Q, dY, Y
+constexpr int DKV_TILES = 11;  // Q (hi, lo), dY (hi, lo), Q^T (hi, lo), dY^T (hi, lo), raw K, V, Y
 constexpr size_t FWD_SMEM = Smem<FWD_TILES>::BYTES;
 constexpr size_t DQ_SMEM = Smem<DQ_TILES>::BYTES;
 constexpr size_t DKV_SMEM = Smem<DKV_TILES>::BYTES;
@@ -240,15 +245,11 @@ GPT2_DEV void epilogue_free(uint32_t tmem, int ncols) {
   }
 }
 
-// Thread 0 issues the four TMA box loads of two tiles (rows y0 .. y0+63 of
-// maps ta / tb, columns x0 .. x0+63 and x1 .. x1+63) onto bar.
-GPT2_DEV void tma_two_tiles(const CUtensorMap* ta, float* t0, int x0, const CUtensorMap* tb, float* t1, int x1, int y0,
-                            uint64_t* bar) {
-  mbar_expect_tx(bar, 2 * TILE_BYTES);
-  tma_load_2d(t0, ta, x0, y0, bar);
-  tma_load_2d(reinterpret_cast<uint8_t*>(t0) + BOX_BYTES, ta, x0 + 32, y0, bar);
-  tma_load_2d(t1, tb, x1, y0, bar);
-  tma_load_2d(reinterpret_cast<uint8_t*>(t1) + BOX_BYTES, tb, x1 + 32, y0, bar);
+// The two TMA box loads of one tile (rows y0 .. y0+63, columns x0 .. x0+63 of
+// map m) onto bar; the caller has set the barrier's expected bytes.
+GPT2_DEV void tma_tile(const CUtensorMap* m, float* t, int x0, int y0, uint64_t* bar) {
+  tma_load_2d(t, m, x0, y0, bar);
+  tma_load_2d(reinterpret_cast<uint8_t*>(t) + BOX_BYTES, m, x0 + 32, y0, bar);
 }
 
 // The abort path: the TMA copies and the last committed MMA batch (phase
@@ -281,6 +282,8 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   float* k_lo = k_hi + TILE_FLOATS;
   float* vt_hi = k_lo + TILE_FLOATS;
   float* vt_lo = vt_hi + TILE_FLOATS;
+  float* q_raw = vt_lo + TILE_FLOATS;
+  float* v_raw = q_raw + TILE_FLOATS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<FWD_TILES>::OFF_BAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<FWD_TILES>::OFF_BAR + 24);
   float* xa = reinterpret_cast<float*>(smem + Smem<FWD_TILES>::OFF_VEC);  // [2][64] half-row maxima
@@ -295,20 +298,21 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   const size_t row0 = (size_t)b * T;
   const bool valid = owner && r < T;
   if (threadIdx.x == 0) {
-    mbar_expect_tx(&bars[0], TILE_BYTES);
-    tma_load_2d(k_hi, &tmQKV, C + h * HS, b * T, &bars[0]);
-    tma_load_2d(reinterpret_cast<uint8_t*>(k_hi) + BOX_BYTES, &tmQKV, C + h * HS + 32, b * T, &bars[0]);
-  }
-  if (owner) {
-    float q[32], v[32];
-    ld_half32(p.qkv + (row0 + r) * 3 * C + h * HS + 32 * hf, valid, q);
-    ld_half32(p.qkv + (row0 + r) * 3 * C + 2 * C + h * HS + 32 * hf, valid, v);
-    st_half_split(tlane, 64, hf, q);
-    st_half_transposed(vt_hi, vt_lo, r, hf, v);  // V^T: rows d, K values = keys
+    mbar_expect_tx(&bars[0], 3 * TILE_BYTES);
+    tma_tile(&tmQKV, k_hi, C + h * HS, b * T, &bars[0]);
+    tma_tile(&tmQKV, q_raw, h * HS, b * T, &bars[0]);
+    tma_tile(&tmQKV, v_raw, 2 * C + h * HS, b * T, &bars[0]);
   }
   int mma_phase = -1;
   bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
   if (ok) {
+    if (owner) {
+      float q[32], v[32];
+      ld_tile_half(q_raw, r, hf, valid, q);
+      ld_tile_half(v_raw, r, hf, valid, v);
+      st_half_split(tlane, 64, hf, q);
+      st_half_transposed(vt_hi, vt_lo, r, hf, v);  // V^T: rows d, K values = keys
+    }
     split_tile(k_hi, k_lo);
     publish_operands();
     if (threadIdx.x == 0) {
@@ -380,13 +384,17 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
 // S [0, 64) -> later dQ; dP [64, 128); Q hi/lo [128, 256) -> later dS hi/lo;
 // dY hi/lo [256, 384).
 // ---------------------------------------------------------------------------
-GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV, const Params& p, uint8_t* smem) {
+GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const CUtensorMap* tmY, const Params& p,
+                     uint8_t* smem) {
   float* k_hi = reinterpret_cast<float*>(smem);
   float* k_lo = k_hi + TILE_FLOATS;
   float* v_hi = k_lo + TILE_FLOATS;
   float* v_lo = v_hi + TILE_FLOATS;
   float* kt_hi = v_lo + TILE_FLOATS;
   float* kt_lo = kt_hi + TILE_FLOATS;
+  float* q_raw = kt_lo + TILE_FLOATS;
+  float* dy_raw = q_raw + TILE_FLOATS;
+  float* y_raw = dy_raw + TILE_FLOATS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<DKV_TILES>::OFF_BAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<DKV_TILES>::OFF_BAR + 24);
   float* xa = reinterpret_cast<float*>(smem + Smem<DKV_TILES>::OFF_VEC);  // [2][64] half-row D partials
@@ -399,28 +407,33 @@ GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV, const Params& p, uint8_t* smem) {
   const uint32_t tlane = tmem + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16);
   const size_t row0 = (size_t)b * T;
   const bool valid = owner && r < T;
-  if (threadIdx.x == 0) tma_two_tiles(tmQKV, k_hi, C + h * HS, tmQKV, v_hi, 2 * C + h * HS, b * T, &bars[0]);
-  float lse_r = 0.f;
-  if (owner) {
-    // every global load first (the TMEM stores below order the code after them)
-    float dyv[32], yv[32], qv[32], kv[32];
-    const float* qkv_r = p.qkv + (row0 + r) * 3 * C + h * HS + 32 * hf;
-    ld_half32(p.dy + (row0 + r) * C + h * HS + 32 * hf, valid, dyv);
-    ld_half32(p.y + (row0 + r) * C + h * HS + 32 * hf, valid, yv);
-    ld_half32(qkv_r, valid, qv);
-    ld_half32(qkv_r + C, valid, kv);
-    lse_r = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
-    float D = 0.f;
-#pragma unroll
-    for (int d = 0; d < 32; d++) D = fmaf(dyv[d], yv[d], D);
-    xa[hf * 64 + r] = D;
-    st_half_transposed(kt_hi, kt_lo, r, hf, kv);  // K^T: row r as a key
-    st_half_split(tlane, 256, hf, dyv);           // dY
-    st_half_split(tlane, 128, hf, qv);            // Q
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(&bars[0], 5 * TILE_BYTES);
+    tma_tile(tmQKV, k_hi, C + h * HS, b * T, &bars[0]);
+    tma_tile(tmQKV, v_hi, 2 * C + h * HS, b * T, &bars[0]);
+    tma_tile(tmQKV, q_raw, h * HS, b * T, &bars[0]);
+    tma_tile(tmDY, dy_raw, h * HS, b * T, &bars[0]);
+    tma_tile(tmY, y_raw, h * HS, b * T, &bars[0]);
   }
+  const float lse_r = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
   int mma_phase = -1;
   bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
   if (ok) {
+    if (owner) {
+      float dyv[32], yv[32], qv[32], kv[32];
+      ld_tile_half(dy_raw, r, hf, valid, dyv);
+      ld_tile_half(y_raw, r, hf, valid, yv);
+      ld_tile_half(q_raw, r, hf, valid, qv);
+      ld_tile_half(k_hi, r, hf, valid, kv);  // before the tile is split in place
+      float D = 0.f;
+#pragma unroll
+      for (int d = 0; d < 32; d++) D = fmaf(dyv[d], yv[d], D);
+      xa[hf * 64 + r] = D;
+      st_half_transposed(kt_hi, kt_lo, r, hf, kv);  // K^T: row r as a key
+      st_half_split(tlane, 256, hf, dyv);           // dY
+      st_half_split(tlane, 128, hf, qv);            // Q
+    }
+    __syncthreads();  // the K rows are read before the split below rewrites them
     split_tile(k_hi, k_lo);
     split_tile(v_hi, v_lo);
     publish_operands();
@@ -476,7 +489,8 @@ GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV, const Params& p, uint8_t* smem) {
 // columns).  Row r also stands for query r: its D_r partials and lse_r are
 // shared through shared memory with every key row.
 // ---------------------------------------------------------------------------
-GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const Params& p, uint8_t* smem) {
+GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const CUtensorMap* tmY, const Params& p,
+                      uint8_t* smem) {
   float* q_hi = reinterpret_cast<float*>(smem);
   float* q_lo = q_hi + TILE_FLOATS;
   float* dy_hi = q_lo + TILE_FLOATS;
@@ -485,6 +499,9 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const P
   float* qt_lo = qt_hi + TILE_FLOATS;
   float* dyt_hi = qt_lo + TILE_FLOATS;
   float* dyt_lo = dyt_hi + TILE_FLOATS;
+  float* k_raw = dyt_lo + TILE_FLOATS;
+  float* v_raw = k_raw + TILE_FLOATS;
+  float* y_raw = v_raw + TILE_FLOATS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<DKV_TILES>::OFF_BAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<DKV_TILES>::OFF_BAR + 24);
   float* xa = reinterpret_cast<float*>(smem + Smem<DKV_TILES>::OFF_VEC);  // [2][64] D partials per query
@@ -498,32 +515,38 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const P
   const uint32_t tlane = tmem + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16);
   const size_t row0 = (size_t)b * T;
   const bool valid = owner && r < T;
-  if (threadIdx.x == 0) tma_two_tiles(tmQKV, q_hi, h * HS, tmDY, dy_hi, h * HS, b * T, &bars[0]);
-  if (owner) {
-    // every global load first (the TMEM stores below order the code after them)
-    float dyv[32], yv[32], qv[32], kv[32], vv[32];
-    const float* qkv_r = p.qkv + (row0 + r) * 3 * C + h * HS + 32 * hf;
-    ld_half32(p.dy + (row0 + r) * C + h * HS + 32 * hf, valid, dyv);
-    ld_half32(p.y + (row0 + r) * C + h * HS + 32 * hf, valid, yv);
-    ld_half32(qkv_r, valid, qv);
-    ld_half32(qkv_r + C, valid, kv);
-    ld_half32(qkv_r + 2 * C, valid, vv);
-    const float lse_r = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
-    // row r as a query: D_r partial, lse_r, its dY and Q values for the transposed tiles
-    float D = 0.f;
-#pragma unroll
-    for (int d = 0; d < 32; d++) D = fmaf(dyv[d], yv[d], D);
-    xa[hf * 64 + r] = D;
-    if (hf == 0) lse_s[r] = lse_r;
-    st_half_transposed(dyt_hi, dyt_lo, r, hf, dyv);  // dY^T
-    st_half_transposed(qt_hi, qt_lo, r, hf, qv);     // Q^T
-    // row r as a key: K and V into TMEM
-    st_half_split(tlane, 128, hf, kv);
-    st_half_split(tlane, 256, hf, vv);
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(&bars[0], 5 * TILE_BYTES);
+    tma_tile(tmQKV, q_hi, h * HS, b * T, &bars[0]);
+    tma_tile(tmDY, dy_hi, h * HS, b * T, &bars[0]);
+    tma_tile(tmQKV, k_raw, C + h * HS, b * T, &bars[0]);
+    tma_tile(tmQKV, v_raw, 2 * C + h * HS, b * T, &bars[0]);
+    tma_tile(tmY, y_raw, h * HS, b * T, &bars[0]);
   }
+  const float lse_r = valid ? p.lse[((size_t)b * p.NH + h) * T + r] : 0.f;
   int mma_phase = -1;
   bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
   if (ok) {
+    if (owner) {
+      float dyv[32], yv[32], qv[32], kv[32], vv[32];
+      ld_tile_half(dy_hi, r, hf, valid, dyv);  // dY and Q before their tiles are split in place
+      ld_tile_half(y_raw, r, hf, valid, yv);
+      ld_tile_half(q_hi, r, hf, valid, qv);
+      ld_tile_half(k_raw, r, hf, valid, kv);
+      ld_tile_half(v_raw, r, hf, valid, vv);
+      // row r as a query: D_r partial, lse_r, its dY and Q values for the transposed tiles
+      float D = 0.f;
+#pragma unroll
+      for (int d = 0; d < 32; d++) D = fmaf(dyv[d], yv[d], D);
+      xa[hf * 64 + r] = D;
+      if (hf == 0) lse_s[r] = lse_r;
+      st_half_transposed(dyt_hi, dyt_lo, r, hf, dyv);  // dY^T
+      st_half_transposed(qt_hi, qt_lo, r, hf, qv);     // Q^T
+      // row r as a key: K and V into TMEM
+      st_half_split(tlane, 128, hf, kv);
+      st_half_split(tlane, 256, hf, vv);
+    }
+    __syncthreads();  // the Q and dY rows are read before the splits below rewrite them
     split_tile(q_hi, q_lo);
     split_tile(dy_hi, dy_lo);
     publish_operands();
@@ -584,14 +607,15 @@ constexpr size_t BWD_SMEM = DKV_SMEM;
 
 __global__ void __launch_bounds__(THREADS) attn_bwd_tf32_kernel(const __grid_constant__ CUtensorMap tmQKV,
                                                                 const __grid_constant__ CUtensorMap tmDY,
+                                                                const __grid_constant__ CUtensorMap tmY,
                                                                 const __grid_constant__ Params p) {
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   if (blockIdx.z == 0)
-    bwd_dq(&tmQKV, p, smem);
+    bwd_dq(&tmQKV, &tmDY, &tmY, p, smem);
   else
-    bwd_dkv(&tmQKV, &tmDY, p, smem);
+    bwd_dkv(&tmQKV, &tmDY, &tmY, p, smem);
 }
 
 }  // namespace atf
