@@ -60,7 +60,9 @@ constexpr int BOX_BYTES = TILE_BYTES / 2;    // one 32-column TMA box: 64 rows x
 
 // Row ownership: warps 0, 1, 4 and 5 (the ones that may access TMEM lanes
 // 0..63) own the 64 rows, two threads per row: row 32 (warp % 2) + lane,
-// half warp / 4 = columns [32 half, 32 half + 32) of every 64-wide row.
+// half warp / 4 = columns [32 half, 32 half + 32) of every 64-wide row.  The
+// other four warps map onto the rows the same way and, while the owners move
+// their rows into TMEM, write the transposed tiles and the hi/lo splits.
 GPT2_DEV bool row_owner() { return ((threadIdx.x >> 5) & 2) == 0; }
 GPT2_DEV int own_row() { return 32 * ((threadIdx.x >> 5) & 1) + (threadIdx.x & 31); }
 GPT2_DEV int own_half() { return threadIdx.x >> 7; }
@@ -159,17 +161,23 @@ GPT2_DEV void st_half_transposed(float* t_hi, float* t_lo, int row, int half, co
   }
 }
 
-// In-place split of a TMA-written tile: hi stays, lo goes to lo.
-GPT2_DEV void split_tile(float* t, float* lo) {
-  float4* t4 = reinterpret_cast<float4*>(t);
+// Split of a raw TMA-written tile into hi and lo tiles of the same layout,
+// by the 128 threads of the warps that own no TMEM lanes (index nid).
+GPT2_DEV void split_tile_to(const float* raw, float* hi, float* lo, int nid) {
+  const float4* r4 = reinterpret_cast<const float4*>(raw);
+  float4* h4 = reinterpret_cast<float4*>(hi);
   float4* l4 = reinterpret_cast<float4*>(lo);
-  for (int i = threadIdx.x; i < TILE_FLOATS / 4; i += THREADS) {
+#pragma unroll 4
+  for (int i = nid; i < TILE_FLOATS / 4; i += THREADS / 2) {
     float4 h, l;
-    tc::split4(t4[i], h, l);
-    t4[i] = h;
+    tc::split4(r4[i], h, l);
+    h4[i] = h;
     l4[i] = l;
   }
 }
+
+// Index of a thread among the warps that own no TMEM lanes (2, 3, 6, 7).
+GPT2_DEV int helper_index() { return (threadIdx.x & 63) | ((threadIdx.x >> 7) << 6); }
 
 // Generic-proxy shared-memory writes and TMEM stores made visible to the
 // tensor core, then a CTA barrier.
@@ -191,11 +199,11 @@ struct Smem {
   static constexpr int OFF_VEC = OFF_BAR + 64;
   static constexpr int BYTES = OFF_VEC + 5 * 64 * 4 + 1024;
 };
-// Every tile of the head's rows comes in by TMA; the threads read their rows
-// out of the raw tiles (Q, V, Y, ... below) instead of from global memory.
-constexpr int FWD_TILES = 6;   // K (hi, lo), V^T (hi, lo), raw Q, raw V
-constexpr int DQ_TILES = 9;    // K (hi, lo), V (hi, lo), K^T (hi, lo), raw Q, dY, Y
-constexpr int DKV_TILES = 11;  // Q (hi, lo), dY (hi, lo), Q^T (hi, lo), dY^T (hi, lo), raw K, V, Y
+// Every tile of the head's rows comes in raw by TMA; the threads read their
+// rows out of the raw tiles, and the B operands are split into hi/lo tiles.
+constexpr int FWD_TILES = 7;   // K (hi, lo), V^T (hi, lo), raw K, Q, V
+constexpr int DQ_TILES = 11;   // K (hi, lo), V (hi, lo), K^T (hi, lo), raw K, V, Q, dY, Y
+constexpr int DKV_TILES = 13;  // Q (hi, lo), dY (hi, lo), Q^T (hi, lo), dY^T (hi, lo), raw Q, dY, K, V, Y
 constexpr size_t FWD_SMEM = Smem<FWD_TILES>::BYTES;
 constexpr size_t DQ_SMEM = Smem<DQ_TILES>::BYTES;
 constexpr size_t DKV_SMEM = Smem<DKV_TILES>::BYTES;
@@ -284,6 +292,7 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   float* vt_lo = vt_hi + TILE_FLOATS;
   float* q_raw = vt_lo + TILE_FLOATS;
   float* v_raw = q_raw + TILE_FLOATS;
+  float* k_raw = v_raw + TILE_FLOATS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<FWD_TILES>::OFF_BAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<FWD_TILES>::OFF_BAR + 24);
   float* xa = reinterpret_cast<float*>(smem + Smem<FWD_TILES>::OFF_VEC);  // [2][64] half-row maxima
@@ -296,10 +305,10 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   const int r = own_row(), hf = own_half();
   const uint32_t tlane = tmem + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16);
   const size_t row0 = (size_t)b * T;
-  const bool valid = owner && r < T;
+  const bool row_ok = r < T, valid = owner && row_ok;
   if (threadIdx.x == 0) {
     mbar_expect_tx(&bars[0], 3 * TILE_BYTES);
-    tma_tile(&tmQKV, k_hi, C + h * HS, b * T, &bars[0]);
+    tma_tile(&tmQKV, k_raw, C + h * HS, b * T, &bars[0]);
     tma_tile(&tmQKV, q_raw, h * HS, b * T, &bars[0]);
     tma_tile(&tmQKV, v_raw, 2 * C + h * HS, b * T, &bars[0]);
   }
@@ -307,13 +316,15 @@ __global__ void __launch_bounds__(THREADS) attn_fwd_tf32_kernel(const __grid_con
   bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
   if (ok) {
     if (owner) {
-      float q[32], v[32];
+      float q[32];
       ld_tile_half(q_raw, r, hf, valid, q);
-      ld_tile_half(v_raw, r, hf, valid, v);
       st_half_split(tlane, 64, hf, q);
+    } else {
+      float v[32];
+      ld_tile_half(v_raw, r, hf, row_ok, v);
       st_half_transposed(vt_hi, vt_lo, r, hf, v);  // V^T: rows d, K values = keys
+      split_tile_to(k_raw, k_hi, k_lo, helper_index());
     }
-    split_tile(k_hi, k_lo);
     publish_operands();
     if (threadIdx.x == 0) {
       mma3(tmem, 0, 64, 128, k_hi, k_lo, HS / 8, Tp);  // S = Q K^T
@@ -395,6 +406,8 @@ GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const CU
   float* q_raw = kt_lo + TILE_FLOATS;
   float* dy_raw = q_raw + TILE_FLOATS;
   float* y_raw = dy_raw + TILE_FLOATS;
+  float* k_raw = y_raw + TILE_FLOATS;
+  float* v_raw = k_raw + TILE_FLOATS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<DKV_TILES>::OFF_BAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<DKV_TILES>::OFF_BAR + 24);
   float* xa = reinterpret_cast<float*>(smem + Smem<DKV_TILES>::OFF_VEC);  // [2][64] half-row D partials
@@ -406,11 +419,11 @@ GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const CU
   const int r = own_row(), hf = own_half();
   const uint32_t tlane = tmem + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16);
   const size_t row0 = (size_t)b * T;
-  const bool valid = owner && r < T;
+  const bool row_ok = r < T, valid = owner && row_ok;
   if (threadIdx.x == 0) {
     mbar_expect_tx(&bars[0], 5 * TILE_BYTES);
-    tma_tile(tmQKV, k_hi, C + h * HS, b * T, &bars[0]);
-    tma_tile(tmQKV, v_hi, 2 * C + h * HS, b * T, &bars[0]);
+    tma_tile(tmQKV, k_raw, C + h * HS, b * T, &bars[0]);
+    tma_tile(tmQKV, v_raw, 2 * C + h * HS, b * T, &bars[0]);
     tma_tile(tmQKV, q_raw, h * HS, b * T, &bars[0]);
     tma_tile(tmDY, dy_raw, h * HS, b * T, &bars[0]);
     tma_tile(tmY, y_raw, h * HS, b * T, &bars[0]);
@@ -420,22 +433,23 @@ GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const CU
   bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
   if (ok) {
     if (owner) {
-      float dyv[32], yv[32], qv[32], kv[32];
+      float dyv[32], yv[32], qv[32];
       ld_tile_half(dy_raw, r, hf, valid, dyv);
       ld_tile_half(y_raw, r, hf, valid, yv);
       ld_tile_half(q_raw, r, hf, valid, qv);
-      ld_tile_half(k_hi, r, hf, valid, kv);  // before the tile is split in place
       float D = 0.f;
 #pragma unroll
       for (int d = 0; d < 32; d++) D = fmaf(dyv[d], yv[d], D);
       xa[hf * 64 + r] = D;
+      st_half_split(tlane, 256, hf, dyv);  // dY
+      st_half_split(tlane, 128, hf, qv);   // Q
+    } else {
+      float kv[32];
+      ld_tile_half(k_raw, r, hf, row_ok, kv);
       st_half_transposed(kt_hi, kt_lo, r, hf, kv);  // K^T: row r as a key
-      st_half_split(tlane, 256, hf, dyv);           // dY
-      st_half_split(tlane, 128, hf, qv);            // Q
+      split_tile_to(k_raw, k_hi, k_lo, helper_index());
+      split_tile_to(v_raw, v_hi, v_lo, helper_index());
     }
-    __syncthreads();  // the K rows are read before the split below rewrites them
-    split_tile(k_hi, k_lo);
-    split_tile(v_hi, v_lo);
     publish_operands();
     if (threadIdx.x == 0) {
       mma3(tmem, 0, 128, 192, k_hi, k_lo, HS / 8, Tp);   // S = Q K^T
@@ -502,6 +516,8 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const C
   float* k_raw = dyt_lo + TILE_FLOATS;
   float* v_raw = k_raw + TILE_FLOATS;
   float* y_raw = v_raw + TILE_FLOATS;
+  float* q_raw = y_raw + TILE_FLOATS;
+  float* dy_raw = q_raw + TILE_FLOATS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<DKV_TILES>::OFF_BAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<DKV_TILES>::OFF_BAR + 24);
   float* xa = reinterpret_cast<float*>(smem + Smem<DKV_TILES>::OFF_VEC);  // [2][64] D partials per query
@@ -514,11 +530,11 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const C
   const int r = own_row(), hf = own_half();
   const uint32_t tlane = tmem + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16);
   const size_t row0 = (size_t)b * T;
-  const bool valid = owner && r < T;
+  const bool row_ok = r < T, valid = owner && row_ok;
   if (threadIdx.x == 0) {
     mbar_expect_tx(&bars[0], 5 * TILE_BYTES);
-    tma_tile(tmQKV, q_hi, h * HS, b * T, &bars[0]);
-    tma_tile(tmDY, dy_hi, h * HS, b * T, &bars[0]);
+    tma_tile(tmQKV, q_raw, h * HS, b * T, &bars[0]);
+    tma_tile(tmDY, dy_raw, h * HS, b * T, &bars[0]);
     tma_tile(tmQKV, k_raw, C + h * HS, b * T, &bars[0]);
     tma_tile(tmQKV, v_raw, 2 * C + h * HS, b * T, &bars[0]);
     tma_tile(tmY, y_raw, h * HS, b * T, &bars[0]);
@@ -528,27 +544,28 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const C
   bool ok = wait_all(&bars[0], 0, abort_flag, p.err);
   if (ok) {
     if (owner) {
-      float dyv[32], yv[32], qv[32], kv[32], vv[32];
-      ld_tile_half(dy_hi, r, hf, valid, dyv);  // dY and Q before their tiles are split in place
+      float dyv[32], yv[32], kv[32], vv[32];
+      ld_tile_half(dy_raw, r, hf, valid, dyv);
       ld_tile_half(y_raw, r, hf, valid, yv);
-      ld_tile_half(q_hi, r, hf, valid, qv);
       ld_tile_half(k_raw, r, hf, valid, kv);
       ld_tile_half(v_raw, r, hf, valid, vv);
-      // row r as a query: D_r partial, lse_r, its dY and Q values for the transposed tiles
+      // row r as a query: D_r partial, lse_r, its dY values for the transposed tile
       float D = 0.f;
 #pragma unroll
       for (int d = 0; d < 32; d++) D = fmaf(dyv[d], yv[d], D);
       xa[hf * 64 + r] = D;
       if (hf == 0) lse_s[r] = lse_r;
       st_half_transposed(dyt_hi, dyt_lo, r, hf, dyv);  // dY^T
-      st_half_transposed(qt_hi, qt_lo, r, hf, qv);     // Q^T
       // row r as a key: K and V into TMEM
       st_half_split(tlane, 128, hf, kv);
       st_half_split(tlane, 256, hf, vv);
+    } else {
+      float qv[32];
+      ld_tile_half(q_raw, r, hf, row_ok, qv);
+      st_half_transposed(qt_hi, qt_lo, r, hf, qv);  // Q^T
+      split_tile_to(q_raw, q_hi, q_lo, helper_index());
+      split_tile_to(dy_raw, dy_hi, dy_lo, helper_index());
     }
-    __syncthreads();  // the Q and dY rows are read before the splits below rewrite them
-    split_tile(q_hi, q_lo);
-    split_tile(dy_hi, dy_lo);
     publish_operands();
     if (threadIdx.x == 0) {
       mma3(tmem, 0, 128, 192, q_hi, q_lo, HS / 8, Tp);     // S^T = K Q^T
