@@ -411,7 +411,7 @@ KERNEL_SOURCES = {
               ("k_misc.cuh", "adamw_sorted_rows_kernel")],
     "xent": [("k_xent.cuh", "online_merge"), ("k_xent.cuh", "xent_fused_kernel"), ("k_xent.cuh", "xent_bf16_kernel")],
     "layernorm": [("k_layernorm.cuh", "layernorm_fwd_kernel"), ("k_layernorm.cuh", "layernorm_bwd_kernel"),
-                  ("k_misc.cuh", "col_finish_kernel")],
+                  ("k_layernorm.cuh", "layernorm_bwd_stride_kernel"), ("k_misc.cuh", "col_finish_kernel")],
     "encoder": [("k_misc.cuh", "encoder_fwd_kernel")],
 }
 
@@ -518,7 +518,8 @@ def roofline_for(kind, k, peaks, w):
 TRAFFIC_KERNELS = {"gemm": ("gemm_tf32x3", "gemm_bf16"),
                    "adamw": ("adamw_kernel", "adamw_rows_kernel", "adamw_sorted_rows_kernel"),
                    "xent": ("xent_fused_kernel", "xent_bf16_kernel"),
-                   "layernorm": ("layernorm_fwd_kernel", "layernorm_bwd_kernel"), "encoder": ("encoder_fwd_kernel",)}
+                   "layernorm": ("layernorm_fwd_kernel", "layernorm_bwd_kernel", "layernorm_bwd_stride_kernel"),
+                   "encoder": ("encoder_fwd_kernel",)}
 BYTE_UNITS = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
 
 

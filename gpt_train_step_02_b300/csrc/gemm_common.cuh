@@ -170,19 +170,23 @@ GPT2_DEV void epi_store4(const EpiArgs& e, int i, int j, float4 acc) {
 
 // ---- coalesced epilogue of a warp's 32 x 32 sub-tile --------------------------
 // Thread `lane` holds row i0 + lane, columns j0 .. j0+31 (from tcgen05.ld).
-// The sub-tile is transposed through the warp's own staging area (32 rows of
-// EPI_STAGE_PITCH floats) so that one warp instruction then covers 4 rows of
-// 32 columns: lane l handles columns j0 + 4 (l % 8) .. +3 of rows
-// i0 + l / 8 + 4 k, k = 0 .. 7, every access a 16-byte piece of a full
-// 128-byte row segment.  All global loads of the sub-tile are issued before
-// any store.
-#define EPI_STAGE_PITCH 36  // floats; keeps rows 16-byte aligned and spreads the banks
-#define EPI_STAGE_FLOATS (32 * EPI_STAGE_PITCH)
+// The sub-tile is transposed through the warp's own staging area so that one
+// warp instruction then covers 4 rows of 32 columns: lane l handles columns
+// j0 + 4 (l % 8) .. +3 of rows i0 + l / 8 + 4 k, k = 0 .. 7, every access a
+// 16-byte piece of a full 128-byte row segment.  All global loads of the
+// sub-tile are issued before any store.  The staging area is 32 rows of 32
+// floats with the row's 16-byte groups permuted (group u of row r at
+// position u ^ (r % 8)), so that the row writes and the column reads each
+// touch every bank once per 8 lanes without padding.
+#define EPI_STAGE_FLOATS (32 * 32)
+
+// float offset of column c of row r in the staging area
+GPT2_DEV int stage_off(int r, int c) { return r * 32 + ((((c >> 2) ^ (r & 7))) << 2) + (c & 3); }
 
 GPT2_DEV void warp32_stage(float* stage, const float* v, int lane) {
 #pragma unroll
   for (int u = 0; u < 8; u++)
-    st4(stage + lane * EPI_STAGE_PITCH + 4 * u, make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]));
+    st4(stage + stage_off(lane, 4 * u), make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]));
   __syncwarp();
 }
 
@@ -193,7 +197,7 @@ GPT2_DEV void warp32_store_raw(float* P, long long ldp, const float* stage, int 
   for (int k = 0; k < 8; k++) {
     const int r = rs + 4 * k, i = i0 + r;
     if (i < M && j < N) {
-      const float4 a = ld4(stage + r * EPI_STAGE_PITCH + c);
+      const float4 a = ld4(stage + stage_off(r, c));
       if (j + 4 <= N && (ldp & 3) == 0) {
         st4(P + (size_t)i * ldp + j, a);
       } else {
@@ -225,7 +229,7 @@ GPT2_DEV void warp32_epilogue(const EpiArgs& e, const float* stage, int i0, int 
       for (int k = 0; k < 8; k++) {
         const int r = rs + 4 * k, i = i0 + r;
         if (i < M) {
-          const float4 o = epi_apply4<OP>(e, i, j, ld4(stage + r * EPI_STAGE_PITCH + c), b, in[k]);
+          const float4 o = epi_apply4<OP>(e, i, j, ld4(stage + stage_off(r, c)), b, in[k]);
           cs = make_float4(cs.x + o.x, cs.y + o.y, cs.z + o.z, cs.w + o.w);
         }
       }
@@ -245,7 +249,7 @@ GPT2_DEV void warp32_epilogue(const EpiArgs& e, const float* stage, int i0, int 
       for (int k = 0; k < 8; k++) {
         const int r = rs + 4 * k, i = i0 + r;
         if (i < M)
-          for (int q = 0; q < 4 && j + q < N; q++) epi_store<OP>(e, i, j + q, stage[r * EPI_STAGE_PITCH + c + q]);
+          for (int q = 0; q < 4 && j + q < N; q++) epi_store<OP>(e, i, j + q, stage[stage_off(r, c + q)]);
       }
     }
   }

@@ -631,7 +631,7 @@ static Bf16Plan plan_bf16(int M, int N, int K, bool no_split, long long ws_float
   return {BN, ceil_div(kt, per)};
 }
 
-// Launches the persistent bf16 tensor-core matmul.// Launches the persistent bf16 tensor-core matmul.  Returns 1, or -1 on a
+// Launches the persistent bf16 tensor-core matmul.  Returns 1, or -1 on a
 // host-side failure.
 static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int* err, cudaStream_t s,
                               long long ws_floats = SPLITK_WS_FLOATS) {

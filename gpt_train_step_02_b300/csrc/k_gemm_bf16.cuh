@@ -69,7 +69,7 @@ constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;  // 8 KB
 
 template <int BN>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 3 : 5;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;  // as many 64-wide K tiles in flight as fit 227 KB
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
