@@ -605,30 +605,69 @@ static cudaError_t set_bf16_smem() {
   return e;
 }
 
-// Output tiles and K splits of the persistent bf16 matmul.  128 x 256 tiles
-// when they come within two thirds of a full wave of the SMs (the rest of
-// that wave idles, but a 128 x 256 tile does its work at a higher rate than
-// two 128 x 128 ones, which also read A twice); otherwise 128 x 128 tiles,
-// which halve the K splits (and their partial-tile traffic) needed to fill
-// the SMs.  K is split only when the tiles do not fill the SMs, keeping at
-// least four 64-wide K tiles per split; never for the epilogues that take
-// column sums or row statistics (no_split).
+// Output tiles and K splits of the persistent bf16 matmul.  A 128 x 256
+// tile does its work at a higher rate than two 128 x 128 ones (which also
+// read A twice); 128 x 128 tiles halve the K splits (and their partial-tile
+// traffic) needed to fill the SMs.  K is split only when the tiles do not fill
+// the SMs, keeping at least four 64-wide K tiles per split; never for the
+// epilogues that take column sums or row statistics (no_split).
 struct Bf16Plan {
   int BN, splits;
 };
 
-static Bf16Plan plan_bf16(int M, int N, int K, bool no_split, long long ws_floats, int num_sms) {
-  const long long tiles256 = (long long)ceil_div(M, tcb::BM) * ceil_div(N, 256);
-  const int BN = (N > 128 && 3 * tiles256 >= 2 * num_sms) ? 256 : 128;
+// Relative time of a plan: the waves of (tile, split) units times the K tiles
+// each unit walks, a 128-wide tile's K tile costing 0.625 of a 256-wide one
+// (half the MMA work at about 0.8 of the rate), plus the last arrival's
+// reduction of the fp32 partials (3 or 1.5 K-tile times per split).  The
+// constants are fitted to the kernel timed alone on the GPT-2 product shapes.
+static double bf16_plan_cost(int M, int N, int K, int BN, int splits, int num_sms) {
+  const long long tiles = (long long)ceil_div(M, tcb::BM) * ceil_div(N, BN);
+  const int kt = ceil_div(K, tcb::BK), per = ceil_div(kt, splits);
+  const long long waves = (tiles * splits + num_sms - 1) / num_sms;
+  const double c = BN == 256 ? 1.0 : 0.625, r = BN == 256 ? 3.0 : 1.5;
+  return (double)waves * per * c + (splits > 1 ? splits * r : 0.0);
+}
+
+// The K split of a BN-wide plan: s = min(SMs / tiles, K tiles / 4) for grids
+// below one wave with at least 8 K tiles, lowered until the fp32 partials fit
+// the workspace, then rounded to equal K ranges.
+static int bf16_splits(int M, int N, int K, int BN, bool no_split, long long ws_floats, int num_sms) {
   const long long tiles = (long long)ceil_div(M, tcb::BM) * ceil_div(N, BN);
   const int kt = ceil_div(K, tcb::BK);
-  if (no_split || tiles >= num_sms || kt < 8) return {BN, 1};
+  if (no_split || tiles >= num_sms || kt < 8) return 1;
   int s = (int)(num_sms / tiles);
   s = s < kt / 4 ? s : kt / 4;
   while (s > 1 && (long long)s * M * N > ws_floats) s--;
   if (s < 1) s = 1;
-  const int per = ceil_div(kt, s);
-  return {BN, ceil_div(kt, per)};
+  return ceil_div(kt, ceil_div(kt, s));
+}
+
+// 256-wide tiles when they fill at least two thirds of a wave, else 128-wide,
+// with the K split above.  The other width (or a smaller split) replaces
+// that plan only when its modelled time is at least 10% lower: on the GPT-2
+// shapes this turns the 124M weight gradients into 256-wide tiles split in
+// two (one wave of 256-wide tiles instead of one of 128-wide tiles).
+static Bf16Plan plan_bf16(int M, int N, int K, bool no_split, long long ws_floats, int num_sms) {
+  const long long tiles256 = (long long)ceil_div(M, tcb::BM) * ceil_div(N, 256);
+  const int BN = (N > 128 && 3 * tiles256 >= 2 * num_sms) ? 256 : 128;
+  const Bf16Plan plan = {BN, bf16_splits(M, N, K, BN, no_split, ws_floats, num_sms)};
+  const double base = bf16_plan_cost(M, N, K, plan.BN, plan.splits, num_sms);
+  const int kt = ceil_div(K, tcb::BK);
+  double best = base;
+  Bf16Plan alt = plan;
+  for (int bn = 128; bn <= 256; bn *= 2) {
+    if (bn == 256 && N <= 128) break;
+    const int smax = bf16_splits(M, N, K, bn, no_split, ws_floats, num_sms);
+    for (int s = 1; s <= smax; s++) {
+      const int sp = ceil_div(kt, ceil_div(kt, s));
+      const double c = bf16_plan_cost(M, N, K, bn, sp, num_sms);
+      if (c < best) {
+        best = c;
+        alt = {bn, sp};
+      }
+    }
+  }
+  return best <= 0.9 * base ? alt : plan;
 }
 
 // Launches the persistent bf16 tensor-core matmul.  Returns 1, or -1 on a
