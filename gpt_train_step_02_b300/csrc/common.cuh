@@ -89,6 +89,58 @@ GPT2_DEV float tanh_fast(float x) {
   return y;
 }
 
+// ---- paired fp32 arithmetic (f32x2), one instruction for two elements, rounded as
+// the scalar forms ----
+// (a.x b.x + c.x, a.y b.y + c.y) as one paired fp32 fused multiply-add
+GPT2_DEV float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n mov.b64 rc, {%5, %6};\n"
+      " fma.rn.f32x2 %0, ra, rb, rc;\n}"
+      : "=l"(d)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+// (a.x + b.x, a.y + b.y) and (a.x b.x, a.y b.y), one paired instruction each
+GPT2_DEV float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n add.rn.f32x2 %0, ra, rb;\n}"
+      : "=l"(d)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+GPT2_DEV float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n mul.rn.f32x2 %0, ra, rb;\n}"
+      : "=l"(d)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+
+// The GELU and its derivative on two elements with the hardware tanh, for the
+// bf16 products.  With u = x (c + c k x^2) (c = sqrt(2/pi), k = 0.044715) and
+// t = tanh(u): gelu = x/2 + (x/2) t and
+// gelu' = (1 + t)/2 + x (1 - t^2) (c/2 + (3/2) c k x^2).
+GPT2_DEV float2 gelu_fwd_fast2(float2 x) {
+  const float c = GELU_SQRT_2_OVER_PI, ck = GELU_SQRT_2_OVER_PI * GELU_COEF;
+  const float2 x2 = mul2(x, x);
+  const float2 u = mul2(x, fma2(x2, make_float2(ck, ck), make_float2(c, c)));
+  const float2 t = make_float2(tanh_fast(u.x), tanh_fast(u.y));
+  const float2 hx = mul2(x, make_float2(0.5f, 0.5f));
+  return fma2(hx, t, hx);
+}
+
+GPT2_DEV float2 gelu_grad_fast2(float2 x) {
+  const float c = GELU_SQRT_2_OVER_PI, ck = GELU_SQRT_2_OVER_PI * GELU_COEF;
+  const float d0 = 0.5f * GELU_SQRT_2_OVER_PI, d1 = 1.5f * GELU_SQRT_2_OVER_PI * GELU_COEF;
+  const float2 x2 = mul2(x, x);
+  const float2 u = mul2(x, fma2(x2, make_float2(ck, ck), make_float2(c, c)));
+  const float2 t = make_float2(tanh_fast(u.x), tanh_fast(u.y));
+  const float2 a = fma2(t, make_float2(0.5f, 0.5f), make_float2(0.5f, 0.5f));  // (1 + t) / 2
+  const float2 s = fma2(make_float2(-t.x, -t.y), t, make_float2(1.f, 1.f));     // 1 - t^2
+  const float2 d = fma2(x2, make_float2(d1, d1), make_float2(d0, d0));
+  return fma2(mul2(x, s), d, a);
+}
+
 GPT2_DEV float gelu_fwd_fast(float x) {
   float u = GELU_SQRT_2_OVER_PI * (x + GELU_COEF * x * x * x);
   return 0.5f * x * (1.0f + tanh_fast(u));

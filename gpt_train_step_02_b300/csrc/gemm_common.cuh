@@ -116,27 +116,40 @@ GPT2_DEV float4 epi_load_input(const EpiArgs& e, int i, int j) {
 template <int OP = -1>
 GPT2_DEV float4 epi_apply4(const EpiArgs& e, int i, int j, float4 acc, float4 b, float4 in) {
   float4 o = acc;
+  // paired adds in the order of the scalar expressions (acc + b) + in: the same roundings
+  const float2 a01 = make_float2(acc.x, acc.y), a23 = make_float2(acc.z, acc.w);
   switch (epi_kind<OP>(e)) {
-    case EPI_BIAS: o = make_float4(acc.x + b.x, acc.y + b.y, acc.z + b.z, acc.w + b.w); break;
-    case EPI_BIAS_RESID:
-      o = make_float4(acc.x + b.x + in.x, acc.y + b.y + in.y, acc.z + b.z + in.z, acc.w + b.w + in.w);
+    case EPI_BIAS: {
+      const float2 o01 = add2(a01, make_float2(b.x, b.y)), o23 = add2(a23, make_float2(b.z, b.w));
+      o = make_float4(o01.x, o01.y, o23.x, o23.y);
       break;
+    }
+    case EPI_BIAS_RESID: {
+      const float2 o01 = add2(add2(a01, make_float2(b.x, b.y)), make_float2(in.x, in.y));
+      const float2 o23 = add2(add2(a23, make_float2(b.z, b.w)), make_float2(in.z, in.w));
+      o = make_float4(o01.x, o01.y, o23.x, o23.y);
+      break;
+    }
     case EPI_BIAS_GELU: {
-      float4 h = make_float4(acc.x + b.x, acc.y + b.y, acc.z + b.z, acc.w + b.w);
+      const float2 h01 = add2(a01, make_float2(b.x, b.y)), h23 = add2(a23, make_float2(b.z, b.w));
+      const float4 h = make_float4(h01.x, h01.y, h23.x, h23.y);
       if (e.pre) st4(e.pre + (size_t)i * e.ldpre + j, h);
       if (e.pre_bf)
         *reinterpret_cast<uint2*>(e.pre_bf + (size_t)i * e.ldpre + j) = make_uint2(bf16x2_bits(h.x, h.y), bf16x2_bits(h.z, h.w));
-      if (e.fast)
-        o = make_float4(gelu_fwd_fast(h.x), gelu_fwd_fast(h.y), gelu_fwd_fast(h.z), gelu_fwd_fast(h.w));
-      else
+      if (e.fast) {
+        const float2 g01 = gelu_fwd_fast2(h01), g23 = gelu_fwd_fast2(h23);
+        o = make_float4(g01.x, g01.y, g23.x, g23.y);
+      } else {
         o = make_float4(gelu_fwd(h.x), gelu_fwd(h.y), gelu_fwd(h.z), gelu_fwd(h.w));
+      }
       break;
     }
     case EPI_DGELU:
-      if (e.fast)
-        o = make_float4(acc.x * gelu_grad_fast(in.x), acc.y * gelu_grad_fast(in.y), acc.z * gelu_grad_fast(in.z),
-                        acc.w * gelu_grad_fast(in.w));
-      else
+      if (e.fast) {
+        const float2 o01 = mul2(a01, gelu_grad_fast2(make_float2(in.x, in.y)));
+        const float2 o23 = mul2(a23, gelu_grad_fast2(make_float2(in.z, in.w)));
+        o = make_float4(o01.x, o01.y, o23.x, o23.y);
+      } else
         o = make_float4(acc.x * gelu_grad(in.x), acc.y * gelu_grad(in.y), acc.z * gelu_grad(in.z),
                         acc.w * gelu_grad(in.w));
       break;

@@ -52,31 +52,6 @@ GPT2_DEV float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// (a.x b.x + c.x, a.y b.y + c.y) as one paired fp32 fused multiply-add
-GPT2_DEV float2 fma2(float2 a, float2 b, float2 c) {
-  uint64_t d;
-  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n mov.b64 rc, {%5, %6};\n"
-      " fma.rn.f32x2 %0, ra, rb, rc;\n}"
-      : "=l"(d)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
-}
-// (a.x + b.x, a.y + b.y) and (a.x b.x, a.y b.y), one paired instruction each
-GPT2_DEV float2 add2(float2 a, float2 b) {
-  uint64_t d;
-  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n add.rn.f32x2 %0, ra, rb;\n}"
-      : "=l"(d)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
-}
-GPT2_DEV float2 mul2(float2 a, float2 b) {
-  uint64_t d;
-  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n mul.rn.f32x2 %0, ra, rb;\n}"
-      : "=l"(d)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
-}
-
 // 32 columns from each of two TMEM addresses, one wait for both loads
 // lo and hi rounded to bf16 (nearest even) and packed, lo in the low half
 GPT2_DEV uint32_t cvt_bf16x2(float lo, float hi) {
