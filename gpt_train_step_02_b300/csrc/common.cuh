@@ -90,31 +90,11 @@ GPT2_DEV float tanh_fast(float x) {
 }
 
 // ---- paired fp32 arithmetic (f32x2), one instruction for two elements, rounded as
-// the scalar forms ----
-// (a.x b.x + c.x, a.y b.y + c.y) as one paired fp32 fused multiply-add
-GPT2_DEV float2 fma2(float2 a, float2 b, float2 c) {
-  uint64_t d;
-  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n mov.b64 rc, {%5, %6};\n"
-      " fma.rn.f32x2 %0, ra, rb, rc;\n}"
-      : "=l"(d)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
-}
-// (a.x + b.x, a.y + b.y) and (a.x b.x, a.y b.y), one paired instruction each
-GPT2_DEV float2 add2(float2 a, float2 b) {
-  uint64_t d;
-  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n add.rn.f32x2 %0, ra, rb;\n}"
-      : "=l"(d)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
-}
-GPT2_DEV float2 mul2(float2 a, float2 b) {
-  uint64_t d;
-  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n mul.rn.f32x2 %0, ra, rb;\n}"
-      : "=l"(d)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
-}
+// the scalar forms (round to nearest even); the compiler's own pair builtins, so
+// that operands stay in register pairs without packing moves ----
+GPT2_DEV float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }  // (a.x b.x + c.x, a.y b.y + c.y)
+GPT2_DEV float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+GPT2_DEV float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
 // The GELU and its derivative on two elements with the hardware tanh, for the
 // bf16 products.  With u = x (c + c k x^2) (c = sqrt(2/pi), k = 0.044715) and
