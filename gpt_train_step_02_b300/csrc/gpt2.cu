@@ -575,33 +575,63 @@ static int make_bf16_map(CUtensorMap* tm, const uint16_t* base, int kmajor, long
 }
 
 
+// More epilogue warps for the GELU, GELU' and residual epilogues when the
+// product has at most 20 K tiles (K <= 1280: the K = C products of the GPT-2
+// shapes), where the epilogue, not the main loop, sets the pace.
+constexpr int HEAVY_EPI_MAX_KTILES = 20;
+
+template <int BN, int OP, int EG>
+static void launch_bf16_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const tcb::Params& p, int grid, cudaStream_t s) {
+  using CF = tcb::Cfg<BN, OP, EG>;
+  launch_k(tcb::gemm_bf16_kernel<BN, OP, EG>, grid, CF::THREADS, (size_t)CF::SMEM_BYTES, s, ta, tb, p);
+}
+
+template <int BN, int OP>
+static void launch_bf16_op(const CUtensorMap& ta, const CUtensorMap& tb, const tcb::Params& p, int grid, cudaStream_t s) {
+  if constexpr (tcb::heavy_epilogue(OP)) {
+    if (p.k_tiles <= HEAVY_EPI_MAX_KTILES) {
+      launch_bf16_cfg<BN, OP, tcb::heavy_epilogue_groups(OP)>(ta, tb, p, grid, s);
+      return;
+    }
+  }
+  launch_bf16_cfg<BN, OP, 2>(ta, tb, p, grid, s);
+}
+
 template <int BN>
 static void launch_bf16_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const tcb::Params& p, int grid,
                                cudaStream_t s) {
-  const size_t sm = tcb::Cfg<BN>::SMEM_BYTES;
   switch (p.epi.epi) {
-    case EPI_BIAS: launch_k(tcb::gemm_bf16_kernel<BN, EPI_BIAS>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
-    case EPI_BIAS_RESID: launch_k(tcb::gemm_bf16_kernel<BN, EPI_BIAS_RESID>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
-    case EPI_BIAS_GELU: launch_k(tcb::gemm_bf16_kernel<BN, EPI_BIAS_GELU>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
-    case EPI_DGELU: launch_k(tcb::gemm_bf16_kernel<BN, EPI_DGELU>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
-    case EPI_ACCUM: launch_k(tcb::gemm_bf16_kernel<BN, EPI_ACCUM>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
-    case EPI_LOGITS: launch_k(tcb::gemm_bf16_kernel<BN, EPI_LOGITS>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
-    default: launch_k(tcb::gemm_bf16_kernel<BN, EPI_STORE>, grid, tcb::THREADS, sm, s, ta, tb, p); break;
+    case EPI_BIAS: launch_bf16_op<BN, EPI_BIAS>(ta, tb, p, grid, s); break;
+    case EPI_BIAS_RESID: launch_bf16_op<BN, EPI_BIAS_RESID>(ta, tb, p, grid, s); break;
+    case EPI_BIAS_GELU: launch_bf16_op<BN, EPI_BIAS_GELU>(ta, tb, p, grid, s); break;
+    case EPI_DGELU: launch_bf16_op<BN, EPI_DGELU>(ta, tb, p, grid, s); break;
+    case EPI_ACCUM: launch_bf16_op<BN, EPI_ACCUM>(ta, tb, p, grid, s); break;
+    case EPI_LOGITS: launch_bf16_op<BN, EPI_LOGITS>(ta, tb, p, grid, s); break;
+    default: launch_bf16_op<BN, EPI_STORE>(ta, tb, p, grid, s); break;
   }
 }
 
 // Raises the dynamic shared-memory limit of every epilogue instantiation.
+template <int BN, int OP>
+static cudaError_t set_bf16_smem_op() {
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, OP, 2>, a, tcb::Cfg<BN, OP, 2>::SMEM_BYTES);
+  if constexpr (tcb::heavy_epilogue(OP)) {
+    constexpr int EG = tcb::heavy_epilogue_groups(OP);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, OP, EG>, a, tcb::Cfg<BN, OP, EG>::SMEM_BYTES);
+  }
+  return e;
+}
+
 template <int BN>
 static cudaError_t set_bf16_smem() {
-  const int sm = tcb::Cfg<BN>::SMEM_BYTES;
-  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  cudaError_t e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_STORE>, a, sm);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_BIAS>, a, sm);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_BIAS_RESID>, a, sm);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_BIAS_GELU>, a, sm);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_DGELU>, a, sm);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_ACCUM>, a, sm);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(tcb::gemm_bf16_kernel<BN, EPI_LOGITS>, a, sm);
+  cudaError_t e = set_bf16_smem_op<BN, EPI_STORE>();
+  if (e == cudaSuccess) e = set_bf16_smem_op<BN, EPI_BIAS>();
+  if (e == cudaSuccess) e = set_bf16_smem_op<BN, EPI_BIAS_RESID>();
+  if (e == cudaSuccess) e = set_bf16_smem_op<BN, EPI_BIAS_GELU>();
+  if (e == cudaSuccess) e = set_bf16_smem_op<BN, EPI_DGELU>();
+  if (e == cudaSuccess) e = set_bf16_smem_op<BN, EPI_ACCUM>();
+  if (e == cudaSuccess) e = set_bf16_smem_op<BN, EPI_LOGITS>();
   return e;
 }
 

@@ -14,14 +14,14 @@
 // transpose bits).
 //
 // Work unit = (128 x BN output tile, K split); a CTA walks the units
-// blockIdx.x, blockIdx.x + gridDim.x, ...  Ten warps:
+// blockIdx.x, blockIdx.x + gridDim.x, ...  Ten or fourteen warps:
 //   warp 0      one lane issues the TMA loads into a STAGES-deep ring
 //   warp 1      allocates TMEM; one lane issues the MMAs (K = 16 per
 //               instruction, four per 64-wide K tile) into one of two TMEM
 //               accumulators, so the epilogue of unit u overlaps the MMAs of
 //               unit u + 1
-//   warps 2..9  epilogue (two warps per TMEM lane quadrant, half the
-//               columns each): tcgen05.ld TMEM -> registers -> shared-memory
+//   warps 2..    epilogue (two or three warps per TMEM lane quadrant, a
+//               share of the columns each): tcgen05.ld TMEM -> registers -> shared-memory
 //               transpose -> fused epilogue -> coalesced global stores; K-split
 //               units hand off through partial tiles and an
 //               arrival counter, the last unit to arrive reducing in split
@@ -61,15 +61,28 @@ using tc::tmem_ld32;
 constexpr int BM = 128;
 constexpr int BK = 64;  // bf16 elements per K tile: 128 bytes, one swizzle row
 constexpr int UMMA_K = 16;
-constexpr int EPI_WARPS = 8;  // epilogue warps: two per TMEM lane quadrant, each finishing half the columns
-constexpr int EPI_THREADS = 32 * EPI_WARPS;
-constexpr int THREADS = 64 + EPI_THREADS;
 constexpr int MN_BOX = 64;                   // MN extent of one MN-major TMA box
 constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;  // 8 KB
 
-template <int BN>
+// The epilogues with per-element arithmetic or inputs (GELU, GELU', bias +
+// residual) are bound by their instruction issue on the products with few K
+// tiles (K = C): there they run with EG = 4 (GELU, GELU') or 3 (residual)
+// epilogue warps per TMEM lane quadrant instead of 2, at the cost of one
+// operand stage of shared memory (the host picks EG per launch).
+__host__ __device__ constexpr bool heavy_epilogue(int op) {
+  return op == EPI_BIAS_GELU || op == EPI_DGELU || op == EPI_BIAS_RESID;
+}
+__host__ __device__ constexpr int heavy_epilogue_groups(int op) { return op == EPI_BIAS_RESID ? 3 : 4; }
+
+template <int BN, int OP = EPI_STORE, int EG = 2>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 6;  // as many 64-wide K tiles in flight as fit 227 KB
+  static constexpr int EPI_GROUPS = EG;            // epilogue warps per TMEM lane quadrant
+  static constexpr bool STRIDED = EG != 2;         // chunks dealt round-robin instead of by half tile
+  static constexpr int EPI_WARPS = 4 * EPI_GROUPS;
+  static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+  static constexpr int THREADS = 64 + EPI_THREADS;
+  // as many 64-wide K tiles in flight as fit 227 KB beside the epilogue's staging
+  static constexpr int STAGES = BN == 256 ? (EG > 2 ? 3 : 4) : (EG > 2 ? 5 : 6);
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -156,12 +169,12 @@ GPT2_DEV void logits_row_stats(const float* v, int j0, int V, int tgt, float& m,
 }
 
 // OP: the epilogue kind (a GemmEpi value), fixed per instantiation
-template <int BN, int OP>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int BN, int OP, int EG>
+__global__ void __launch_bounds__(Cfg<BN, OP, EG>::THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ Params p) {
   pdl_launch_dependents();
-  using CF = Cfg<BN>;
+  using CF = Cfg<BN, OP, EG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::OFF_BAR);
@@ -184,7 +197,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], EPI_WARPS);
+      mbar_init(&acc_empty[b], CF::EPI_WARPS);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -289,7 +302,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- epilogue ----------------
     const int t = threadIdx.x - 64;          // 0 .. EPI_THREADS-1
     const int q = warp & 3;                  // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) / 4;         // which half of the BN columns this warp finishes
+    const int grp = (warp - 2) / 4;          // which of the quadrant's EPI_GROUPS warps this is
+    // its 32-column chunks: with two warps per quadrant the first or second
+    // half of the tile (the LM head's row statistics are per half tile); with
+    // more, every EG-th chunk
+    constexpr int NCH = BN / 32;
+    const int cc_first = CF::STRIDED ? grp : grp * (NCH / 2);
+    const int cc_end = CF::STRIDED ? NCH : (grp + 1) * (NCH / 2);
+    const int cc_step = CF::STRIDED ? CF::EPI_GROUPS : 1;
     int lu = 0;
     for (int unit = blockIdx.x; unit < p.units; unit += gridDim.x, lu++) {
       int m0, tn, z, tile;
@@ -299,9 +319,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = mbar_wait(&acc_full[buf], (lu >> 1) & 1, abort_flag, p.err);
       // one decision for all epilogue warps (tcgen05.ld is warp-collective
       // and the split-K hand-off uses a barrier over these threads)
-      tc::epi_bar<EPI_THREADS>();
+      tc::epi_bar<CF::EPI_THREADS>();
       if (t == 0) *go_flag = (ok && !*abort_flag) ? 1 : 0;
-      tc::epi_bar<EPI_THREADS>();
+      tc::epi_bar<CF::EPI_THREADS>();
       if (!*go_flag) break;
       tc_fence_after();
       const bool split = p.splits > 1;
@@ -314,7 +334,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int xt = -1;
       if constexpr (OP == EPI_LOGITS) xt = (i0 + lane < p.M) ? p.epi.targets[i0 + lane] : -1;
 #pragma unroll 1
-      for (int cc = half * (BN / 64); cc < (half + 1) * (BN / 64); cc++) {
+      for (int cc = cc_first; cc < cc_end; cc += cc_step) {
         float v[32];
         tmem_ld32(tbase + (uint32_t)(cc * 32), v);
         const int j0 = n0 + cc * 32;
@@ -327,7 +347,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           warp32_epilogue<OP>(p.epi, stage, i0, j0, p.M, p.N, lane);
       }
       if constexpr (OP == EPI_LOGITS) {
-        const int blk = tn * 2 + half;  // this warp's BN/2 columns
+        const int blk = tn * 2 + grp;  // this warp's BN/2 columns
         if (i0 + lane < p.M && blk * (BN / 2) < p.N)
           p.epi.xstats[(size_t)(i0 + lane) * p.epi.ldxs + blk] = make_float2(xm, xs);
       }
@@ -336,14 +356,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::mbar_arrive_warp(&acc_empty[buf]);
       if (split) {
         __threadfence();
-        tc::epi_bar<EPI_THREADS>();
+        tc::epi_bar<CF::EPI_THREADS>();
         if (t == 0) *last_flag = (atomicAdd(&p.tile_ctr[tile], 1) == p.splits - 1) ? 1 : 0;
-        tc::epi_bar<EPI_THREADS>();
+        tc::epi_bar<CF::EPI_THREADS>();
         if (*last_flag) {
           __threadfence();
           const int ew = warp - 2;
           const size_t plane = (size_t)p.M * p.N;
-          for (int r = ew; r < BM && m0 + r < p.M; r += EPI_WARPS) {
+          for (int r = ew; r < BM && m0 + r < p.M; r += CF::EPI_WARPS) {
             const int ii = m0 + r;
             for (int jj = 4 * lane; jj < BN; jj += 128) {
               const int j = n0 + jj;
