@@ -603,14 +603,21 @@ constexpr int OFF_DST = OFF_PT + 2 * SUB_BYTES;    // 2 buffers
 constexpr int LD_BYTES = 128 * 8;                  // (-lse log2 e, -D) of one query tile
 constexpr int OFF_LD = OFF_DST + 2 * SUB_BYTES;    // 2 stages
 constexpr int OFF_BAR = OFF_LD + 2 * LD_BYTES;
-// kv_full, qd_full[2], qd_empty[2], s_full[2], st_ready[2], pt_free[2], mma_done
-constexpr int NUM_BARS = 12;
+// kv_full, qd_full[2], qd_empty[2], s_full[2], st_ready[2], pt_free[2], mma_done, s_done
+constexpr int NUM_BARS = 13;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 }  // namespace dkv
 
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+// dK/dV: the scores (S^T, dP^T) and the products (dV, dK) are issued by two
+// threads in different warps (warp 1 and a last warp after the softmax
+// warps), so that the issue time of one set overlaps the other's: a 128 x 64
+// x 16 MMA takes about as long to issue as a 256-wide one.
+constexpr int DKV_THREADS = BWD_THREADS + 32;
+constexpr int DKV_PRODUCTS_WARP = DKV_THREADS / 32 - 1;
+
+__global__ void __launch_bounds__(DKV_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
                            const __grid_constant__ BwdParams p) {
   pdl_launch_dependents();
@@ -625,6 +632,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint64_t* st_ready = bars + 7;
   uint64_t* pt_free = bars + 9;
   uint64_t* mma_done = bars + 11;
+  uint64_t* s_done = bars + 12;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -645,6 +653,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_init(&pt_free[s], 1);
     }
     mbar_init(mma_done, 1);
+    mbar_init(s_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -685,6 +694,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
     }
   } else if (warp == 1) {
+    // ---------------- scores issuer ----------------
     if (lane == 0) {
       const uint32_t sk = smem_u32(smem + OFF_K), sv = smem_u32(smem + OFF_V);
       // scores of sub-tile i into TMEM buffer i & 1
@@ -706,9 +716,22 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         return true;
       };
       bool ok = mbar_wait(kv_full, 0, abort_flag, p.err) && issue_s(0);
-      for (int i = 0; i < nsub && ok; i++) {
-        // buffer (i+1) & 1 was read out by the softmax warps before st_ready(i-1)
-        if (i + 1 < nsub && !issue_s(i + 1)) break;
+      for (int j = 1; j < nsub && ok; j++) {
+        // TMEM buffer j & 1 was read out by the softmax warps before st_ready(j - 2)
+        if (j >= 2 && !mbar_wait(&st_ready[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err)) break;
+        tc_fence_after();
+        ok = issue_s(j);
+      }
+      // the scores this thread issued land before the CTA's resources go
+      mma_commit(s_done);
+      mbar_wait_drain(s_done, 0);
+    }
+  } else if (warp == DKV_PRODUCTS_WARP) {
+    // ---------------- products issuer ----------------
+    // (a sub-tile's scores have completed by the time its st_ready fires: the
+    // softmax warps waited for them, so these commits cover the tile's Q/dO)
+    if (lane == 0) {
+      for (int i = 0; i < nsub; i++) {
         if (!mbar_wait(&st_ready[i & 1], (i >> 1) & 1, abort_flag, p.err)) break;
         tc_fence_after();
         const int it = i >> 1, s = it & 1, u = i & 1;
