@@ -1124,7 +1124,7 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
     p.LD = (const float2*)D; p.dqkv = dqkv; p.dqkv_bf = dqkv_bf; p.colsum = colsum; p.err = err;
     dim3 g(T / tca::BQ, NH, B);
     launch_k(tca::attn_bwd_dkv_tc_kernel, g, tca::DKV_THREADS, tca::dkv::SMEM_BYTES, s, tq, td, p);
-    launch_k(tca::attn_bwd_dq_tc_kernel, g, tca::BWD_THREADS, tca::dqk::SMEM_BYTES, s, tq, td, p);
+    launch_k(tca::attn_bwd_dq_tc_kernel, g, tca::DQ_THREADS, tca::dqk::SMEM_BYTES, s, tq, td, p);
     return 3;
   }
   if (!dqkv || colsum) return -1;  // the CUDA-core kernels store fp32 dqkv only

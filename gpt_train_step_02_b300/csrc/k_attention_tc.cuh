@@ -860,14 +860,19 @@ constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;   // 2 stages
 constexpr int SUB_BYTES = 128 * SUB * 2;
 constexpr int OFF_DS = OFF_V + 2 * TILE_BYTES;  // dS, 2 buffers of 128 x 64 bf16
 constexpr int OFF_BAR = OFF_DS + 2 * SUB_BYTES;
-// qd_full, kv_full[2], kv_empty[2], s_full[2], ds_ready[2], ds_free[2], mma_done
-constexpr int NUM_BARS = 12;
+// qd_full, kv_full[2], kv_empty[2], s_full[2], ds_ready[2], ds_free[2], mma_done, s_done
+constexpr int NUM_BARS = 13;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 }  // namespace dqk
 
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+// dQ: the scores (S, dP) and the dQ products issued by two threads in
+// different warps, as in the dK/dV kernel.
+constexpr int DQ_THREADS = BWD_THREADS + 32;
+constexpr int DQ_PRODUCTS_WARP = DQ_THREADS / 32 - 1;
+
+__global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
                           const __grid_constant__ BwdParams p) {
   pdl_launch_dependents();
@@ -882,6 +887,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint64_t* ds_ready = bars + 7;
   uint64_t* ds_free = bars + 9;
   uint64_t* mma_done = bars + 11;
+  uint64_t* s_done = bars + 12;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -903,6 +909,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_init(&ds_free[s], 1);
     }
     mbar_init(mma_done, 1);
+    mbar_init(s_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -940,6 +947,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
     }
   } else if (warp == 1) {
+    // ---------------- scores issuer ----------------
     if (lane == 0) {
       const uint32_t sq = smem_u32(smem + OFF_Q), sdo = smem_u32(smem + OFF_DO);
       // scores of sub-tile i (keys 64 u .. of key tile i >> 1) into TMEM buffer i & 1
@@ -961,8 +969,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         return true;
       };
       bool ok = mbar_wait(qd_full, 0, abort_flag, p.err) && issue_s(0);
-      for (int i = 0; i < nsub && ok; i++) {
-        if (i + 1 < nsub && !issue_s(i + 1)) break;
+      for (int j = 1; j < nsub && ok; j++) {
+        // TMEM buffer j & 1 was read out by the softmax warps before ds_ready(j - 2)
+        if (j >= 2 && !mbar_wait(&ds_ready[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err)) break;
+        tc_fence_after();
+        ok = issue_s(j);
+      }
+      mma_commit(s_done);
+      mbar_wait_drain(s_done, 0);
+    }
+  } else if (warp == DQ_PRODUCTS_WARP) {
+    // ---------------- dQ products issuer ----------------
+    // (a sub-tile's scores have completed by the time its ds_ready fires, so
+    // these commits cover the key tile's K and V)
+    if (lane == 0) {
+      for (int i = 0; i < nsub; i++) {
         if (!mbar_wait(&ds_ready[i & 1], (i >> 1) & 1, abort_flag, p.err)) break;
         tc_fence_after();
         const int j = i >> 1, s = j & 1, u = i & 1;
