@@ -610,12 +610,16 @@ constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 }  // namespace dkv
 
-// dK/dV: the scores (S^T, dP^T) and the products (dV, dK) are issued by two
-// threads in different warps (warp 1 and a last warp after the softmax
-// warps), so that the issue time of one set overlaps the other's: a 128 x 64
-// x 16 MMA takes about as long to issue as a 256-wide one.
-constexpr int DKV_THREADS = BWD_THREADS + 32;
-constexpr int DKV_PRODUCTS_WARP = DKV_THREADS / 32 - 1;
+// dK/dV: each of the four accumulation chains (S^T, dP^T, dV, dK) is issued
+// by its own thread, in its own warp (warp 1 and three warps after the
+// softmax warps), so that their issue times overlap: a 128 x 64 x 16 MMA
+// takes about as long to issue as a 256-wide one.  The barriers a pair of
+// chains completes together (s_full, pt_free, qd_empty, mma_done, s_done)
+// count two arrivals.
+constexpr int DKV_THREADS = BWD_THREADS + 96;
+constexpr int DKV_DV_WARP = 2 + BWD_SOFTMAX_WARPS;  // 18
+constexpr int DKV_DPT_WARP = DKV_DV_WARP + 1;       // 19
+constexpr int DKV_DK_WARP = DKV_DV_WARP + 2;        // 20
 
 __global__ void __launch_bounds__(DKV_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
@@ -647,13 +651,13 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     mbar_init(kv_full, 1);
     for (int s = 0; s < 2; s++) {
       mbar_init(&qd_full[s], 1);
-      mbar_init(&qd_empty[s], 1);
-      mbar_init(&s_full[s], 1);
+      mbar_init(&qd_empty[s], 2);                  // the dV and dK issuers
+      mbar_init(&s_full[s], 2);                    // the S^T and dP^T issuers
       mbar_init(&st_ready[s], BWD_SOFTMAX_WARPS);  // one arrival per softmax warp
-      mbar_init(&pt_free[s], 1);
+      mbar_init(&pt_free[s], 2);                   // the dV and dK issuers
     }
-    mbar_init(mma_done, 1);
-    mbar_init(s_done, 1);
+    mbar_init(mma_done, 2);
+    mbar_init(s_done, 2);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -693,60 +697,47 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         for (int i = max(0, issued - 2); i < issued; i++) mbar_wait_drain(&qd_full[i & 1], (i >> 1) & 1);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- scores issuer ----------------
+  } else if (warp == 1 || warp == DKV_DPT_WARP) {
+    // ---------------- scores issuers: S^T = K Q^T (warp 1), dP^T = V dO^T ----------------
     if (lane == 0) {
-      const uint32_t sk = smem_u32(smem + OFF_K), sv = smem_u32(smem + OFF_V);
-      // scores of sub-tile i into TMEM buffer i & 1
-      auto issue_s = [&](int i) -> bool {
-        const int it = i >> 1, s = it & 1, u = i & 1;
-        if (u == 0 && !mbar_wait(&qd_full[s], (it >> 1) & 1, abort_flag, p.err)) return false;
-        tc_fence_after();
-        const uint32_t sq = smem_u32(smem + OFF_Q + s * TILE_BYTES) + u * (TILE_BYTES / 2);
-        const uint32_t sdo = smem_u32(smem + OFF_DO + s * TILE_BYTES) + u * (TILE_BYTES / 2);
-        const uint32_t t_st = tmem + (i & 1) * 128, t_dpt = t_st + SUB;
-#pragma unroll
-        for (int kk = 0; kk < HS / 16; kk++) {
-          mma_bf16(t_st, desc_sw128(sk + kk * 32, 16, 1024), desc_sw128(sq + kk * 32, 16, 1024), IDESC_S64,
-                   kk > 0 ? 1u : 0u);
-          mma_bf16(t_dpt, desc_sw128(sv + kk * 32, 16, 1024), desc_sw128(sdo + kk * 32, 16, 1024), IDESC_S64,
-                   kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&s_full[i & 1]);
-        return true;
-      };
-      bool ok = mbar_wait(kv_full, 0, abort_flag, p.err) && issue_s(0);
-      for (int j = 1; j < nsub && ok; j++) {
+      const bool dpt = warp == DKV_DPT_WARP;
+      const uint32_t sa = smem_u32(smem + (dpt ? OFF_V : OFF_K));
+      bool ok = mbar_wait(kv_full, 0, abort_flag, p.err);
+      for (int j = 0; j < nsub && ok; j++) {
+        const int it = j >> 1, s = it & 1, u = j & 1;
         // TMEM buffer j & 1 was read out by the softmax warps before st_ready(j - 2)
         if (j >= 2 && !mbar_wait(&st_ready[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err)) break;
+        if (u == 0 && !mbar_wait(&qd_full[s], (it >> 1) & 1, abort_flag, p.err)) break;
         tc_fence_after();
-        ok = issue_s(j);
+        const uint32_t sb = smem_u32(smem + (dpt ? OFF_DO : OFF_Q) + s * TILE_BYTES) + u * (TILE_BYTES / 2);
+        const uint32_t t_acc = tmem + (j & 1) * 128 + (dpt ? SUB : 0);
+#pragma unroll
+        for (int kk = 0; kk < HS / 16; kk++)
+          mma_bf16(t_acc, desc_sw128(sa + kk * 32, 16, 1024), desc_sw128(sb + kk * 32, 16, 1024), IDESC_S64,
+                   kk > 0 ? 1u : 0u);
+        mma_commit(&s_full[j & 1]);
       }
-      // the scores this thread issued land before the CTA's resources go
+      // the scores these threads issued land before the CTA's resources go
       mma_commit(s_done);
       mbar_wait_drain(s_done, 0);
     }
-  } else if (warp == DKV_PRODUCTS_WARP) {
-    // ---------------- products issuer ----------------
+  } else if (warp == DKV_DV_WARP || warp == DKV_DK_WARP) {
+    // ---------------- products issuers: dV += P^T dO, dK += dS^T Q ----------------
     // (a sub-tile's scores have completed by the time its st_ready fires: the
     // softmax warps waited for them, so these commits cover the tile's Q/dO)
     if (lane == 0) {
+      const bool dk = warp == DKV_DK_WARP;
+      const uint32_t t_acc = dk ? T_DK : T_DV;
       for (int i = 0; i < nsub; i++) {
         if (!mbar_wait(&st_ready[i & 1], (i >> 1) & 1, abort_flag, p.err)) break;
         tc_fence_after();
         const int it = i >> 1, s = it & 1, u = i & 1;
-        const uint32_t sq = smem_u32(smem + OFF_Q + s * TILE_BYTES) + u * (TILE_BYTES / 2);
-        const uint32_t sdo = smem_u32(smem + OFF_DO + s * TILE_BYTES) + u * (TILE_BYTES / 2);
-        const uint32_t spt = smem_u32(smem + OFF_PT + (i & 1) * SUB_BYTES);
-        const uint32_t sdst = smem_u32(smem + OFF_DST + (i & 1) * SUB_BYTES);
+        const uint32_t sb = smem_u32(smem + (dk ? OFF_Q : OFF_DO) + s * TILE_BYTES) + u * (TILE_BYTES / 2);
+        const uint32_t sa = smem_u32(smem + (dk ? OFF_DST : OFF_PT) + (i & 1) * SUB_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < SUB / 16; kk++) {
-          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          mma_bf16(T_DV, desc_sw128(spt + kk * 32, 16, 1024), desc_sw128(sdo + kk * 2048, 8192, 1024), IDESC_ACC,
-                   acc);
-          mma_bf16(T_DK, desc_sw128(sdst + kk * 32, 16, 1024), desc_sw128(sq + kk * 2048, 8192, 1024), IDESC_ACC,
-                   acc);
-        }
+        for (int kk = 0; kk < SUB / 16; kk++)
+          mma_bf16(t_acc, desc_sw128(sa + kk * 32, 16, 1024), desc_sw128(sb + kk * 2048, 8192, 1024), IDESC_ACC,
+                   (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&pt_free[i & 1]);
         if (u == 1) mma_commit(&qd_empty[s]);
       }
@@ -867,10 +858,12 @@ constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 }  // namespace dqk
 
-// dQ: the scores (S, dP) and the dQ products issued by two threads in
-// different warps, as in the dK/dV kernel.
-constexpr int DQ_THREADS = BWD_THREADS + 32;
-constexpr int DQ_PRODUCTS_WARP = DQ_THREADS / 32 - 1;
+// dQ: the three accumulation chains (S, dP, dQ) issued by three threads in
+// different warps (warp 1 and two warps after the softmax warps), as in the
+// dK/dV kernel; s_full and s_done count the two scores issuers.
+constexpr int DQ_THREADS = BWD_THREADS + 64;
+constexpr int DQ_DQ_WARP = 2 + BWD_SOFTMAX_WARPS;  // 18
+constexpr int DQ_DP_WARP = DQ_DQ_WARP + 1;         // 19
 
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
@@ -904,12 +897,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     for (int s = 0; s < 2; s++) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
-      mbar_init(&s_full[s], 1);
+      mbar_init(&s_full[s], 2);                    // the S and dP issuers
       mbar_init(&ds_ready[s], BWD_SOFTMAX_WARPS);  // one arrival per softmax warp
       mbar_init(&ds_free[s], 1);
     }
     mbar_init(mma_done, 1);
-    mbar_init(s_done, 1);
+    mbar_init(s_done, 2);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -946,39 +939,30 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         for (int j = max(0, issued - 2); j < issued; j++) mbar_wait_drain(&kv_full[j & 1], (j >> 1) & 1);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- scores issuer ----------------
+  } else if (warp == 1 || warp == DQ_DP_WARP) {
+    // ---------------- scores issuers: S = Q K^T (warp 1), dP = dO V^T ----------------
     if (lane == 0) {
-      const uint32_t sq = smem_u32(smem + OFF_Q), sdo = smem_u32(smem + OFF_DO);
-      // scores of sub-tile i (keys 64 u .. of key tile i >> 1) into TMEM buffer i & 1
-      auto issue_s = [&](int i) -> bool {
+      const bool dpr = warp == DQ_DP_WARP;
+      const uint32_t sa = smem_u32(smem + (dpr ? OFF_DO : OFF_Q));
+      bool ok = mbar_wait(qd_full, 0, abort_flag, p.err);
+      for (int i = 0; i < nsub && ok; i++) {
         const int j = i >> 1, s = j & 1, u = i & 1;
-        if (u == 0 && !mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.err)) return false;
+        // TMEM buffer i & 1 was read out by the softmax warps before ds_ready(i - 2)
+        if (i >= 2 && !mbar_wait(&ds_ready[i & 1], ((i - 2) >> 1) & 1, abort_flag, p.err)) break;
+        if (u == 0 && !mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t sk = smem_u32(smem + OFF_K + s * TILE_BYTES) + u * (TILE_BYTES / 2);
-        const uint32_t sv = smem_u32(smem + OFF_V + s * TILE_BYTES) + u * (TILE_BYTES / 2);
-        const uint32_t t_s = tmem + (i & 1) * 128, t_dp = t_s + SUB;
+        const uint32_t sb = smem_u32(smem + (dpr ? OFF_V : OFF_K) + s * TILE_BYTES) + u * (TILE_BYTES / 2);
+        const uint32_t t_acc = tmem + (i & 1) * 128 + (dpr ? SUB : 0);
 #pragma unroll
-        for (int kk = 0; kk < HS / 16; kk++) {
-          mma_bf16(t_s, desc_sw128(sq + kk * 32, 16, 1024), desc_sw128(sk + kk * 32, 16, 1024), IDESC_S64,
+        for (int kk = 0; kk < HS / 16; kk++)
+          mma_bf16(t_acc, desc_sw128(sa + kk * 32, 16, 1024), desc_sw128(sb + kk * 32, 16, 1024), IDESC_S64,
                    kk > 0 ? 1u : 0u);
-          mma_bf16(t_dp, desc_sw128(sdo + kk * 32, 16, 1024), desc_sw128(sv + kk * 32, 16, 1024), IDESC_S64,
-                   kk > 0 ? 1u : 0u);
-        }
         mma_commit(&s_full[i & 1]);
-        return true;
-      };
-      bool ok = mbar_wait(qd_full, 0, abort_flag, p.err) && issue_s(0);
-      for (int j = 1; j < nsub && ok; j++) {
-        // TMEM buffer j & 1 was read out by the softmax warps before ds_ready(j - 2)
-        if (j >= 2 && !mbar_wait(&ds_ready[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err)) break;
-        tc_fence_after();
-        ok = issue_s(j);
       }
       mma_commit(s_done);
       mbar_wait_drain(s_done, 0);
     }
-  } else if (warp == DQ_PRODUCTS_WARP) {
+  } else if (warp == DQ_DQ_WARP) {
     // ---------------- dQ products issuer ----------------
     // (a sub-tile's scores have completed by the time its ds_ready fires, so
     // these commits cover the key tile's K and V)
