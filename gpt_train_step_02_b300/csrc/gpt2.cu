@@ -647,14 +647,14 @@ struct Bf16Plan {
 
 // Relative time of a plan: the waves of (tile, split) units times the K tiles
 // each unit walks, a 128-wide tile's K tile costing 0.625 of a 256-wide one
-// (half the MMA work at about 0.8 of the rate), plus the last arrival's
+// (half the MMA work at about 0.8 of the rate), a 192-wide one 0.88 of it, plus the last arrival's
 // reduction of the fp32 partials (3 or 1.5 K-tile times per split).  The
 // constants are fitted to the kernel timed alone on the GPT-2 product shapes.
 static double bf16_plan_cost(int M, int N, int K, int BN, int splits, int num_sms) {
   const long long tiles = (long long)ceil_div(M, tcb::BM) * ceil_div(N, BN);
   const int kt = ceil_div(K, tcb::BK), per = ceil_div(kt, splits);
   const long long waves = (tiles * splits + num_sms - 1) / num_sms;
-  const double c = BN == 256 ? 1.0 : 0.625, r = BN == 256 ? 3.0 : 1.5;
+  const double c = BN == 256 ? 1.0 : (BN == 192 ? 0.88 : 0.625), r = BN * 3.0 / 256.0;
   return (double)waves * per * c + (splits > 1 ? splits * r : 0.0);
 }
 
@@ -673,11 +673,14 @@ static int bf16_splits(int M, int N, int K, int BN, bool no_split, long long ws_
 }
 
 // 256-wide tiles when they fill at least two thirds of a wave, else 128-wide,
-// with the K split above.  The other width (or a smaller split) replaces
-// that plan only when its modelled time is at least 10% lower: on the GPT-2
-// shapes this turns the 124M weight gradients into 256-wide tiles split in
-// two (one wave of 256-wide tiles instead of one of 128-wide tiles).
-static Bf16Plan plan_bf16(int M, int N, int K, bool no_split, long long ws_floats, int num_sms) {
+// with the K split above.  Another width (128, 192 or 256, the 192-wide one
+// unless excluded) or a smaller split replaces that plan only when its
+// modelled time is at least 10% lower.  On the GPT-2 shapes this turns the
+// 124M weight gradients into 256-wide tiles split in two (one wave of
+// 256-wide tiles instead of one of 128-wide tiles), and the 774M products
+// with N = 1280 at B*T = 4096 into 192-wide tiles (224 tiles in two waves
+// instead of 160 256-wide ones, the second nearly empty).
+static Bf16Plan plan_bf16(int M, int N, int K, bool no_split, long long ws_floats, int num_sms, bool allow192 = true) {
   const long long tiles256 = (long long)ceil_div(M, tcb::BM) * ceil_div(N, 256);
   const int BN = (N > 128 && 3 * tiles256 >= 2 * num_sms) ? 256 : 128;
   const Bf16Plan plan = {BN, bf16_splits(M, N, K, BN, no_split, ws_floats, num_sms)};
@@ -685,8 +688,9 @@ static Bf16Plan plan_bf16(int M, int N, int K, bool no_split, long long ws_float
   const int kt = ceil_div(K, tcb::BK);
   double best = base;
   Bf16Plan alt = plan;
-  for (int bn = 128; bn <= 256; bn *= 2) {
-    if (bn == 256 && N <= 128) break;
+  for (int bn = 128; bn <= 256; bn += 64) {
+    if (bn > 128 && N <= 128) break;
+    if (bn == 192 && !allow192) continue;
     const int smax = bf16_splits(M, N, K, bn, no_split, ws_floats, num_sms);
     for (int s = 1; s <= smax; s++) {
       const int sp = ceil_div(kt, ceil_div(kt, s));
@@ -707,7 +711,8 @@ static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int
   if (!d.Abf || !d.Bbf) return -1;
   // column sums and the row statistics are taken in the warp epilogue, which a K split bypasses
   const bool no_split = d.epi.colsum || d.epi.epi == EPI_LOGITS;
-  const Bf16Plan plan = plan_bf16(d.M, d.N, d.K, no_split, ws_floats, dev_info().num_sms);
+  // the LM head's row statistics are per half of a 256-wide tile
+  const Bf16Plan plan = plan_bf16(d.M, d.N, d.K, no_split, ws_floats, dev_info().num_sms, d.epi.epi != EPI_LOGITS);
   const int BN = plan.BN;
   CUtensorMap ta, tb;
   if (!make_bf16_map(&ta, d.Abf, d.a_kmajor, d.a_kmajor ? d.M : d.K, d.a_kmajor ? d.K : d.M, d.lda, tcb::BM))
@@ -735,6 +740,7 @@ static int launch_matmul_bf16(const MatmulDesc& d, float* ws, int* tile_ctr, int
   const int nsm = dev_info().num_sms;
   int grid = p.units < nsm ? p.units : nsm;
   if (BN == 256) launch_bf16_kernel<256>(ta, tb, p, grid, s);
+  else if (BN == 192) launch_bf16_kernel<192>(ta, tb, p, grid, s);
   else launch_bf16_kernel<128>(ta, tb, p, grid, s);
   return 1;
 }
@@ -1182,6 +1188,7 @@ static int set_kernel_attributes() {
                                tc::pers::SMEM_BYTES);
     if (e == cudaSuccess) e = query_cluster_limits(dev, di);
     if (e == cudaSuccess) e = set_bf16_smem<256>();
+    if (e == cudaSuccess) e = set_bf16_smem<192>();
     if (e == cudaSuccess) e = set_bf16_smem<128>();
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tca::attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1368,7 +1375,7 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
   m->logits_in_bf = xbf ? 1 : 0;
   if (xbf) {
     // the LM head's tile width, as its launch chose it (EPI_LOGITS: no split)
-    const int bn = plan_bf16(N, Vp, C, true, SPLITK_WS_FLOATS, dev_info().num_sms).BN;
+    const int bn = plan_bf16(N, Vp, C, true, SPLITK_WS_FLOATS, dev_info().num_sms, false).BN;
     const int nblk = ceil_div(Vp, bn / 2), ldxs = (int)xstats_pitch(Vp);
     // reads the bf16 logits and the statistics, writes the bf16 dlogits
     timer_begin(m, TK_XENT, (double)N * (4.0 * Vp + 8.0 * nblk + 8.0));

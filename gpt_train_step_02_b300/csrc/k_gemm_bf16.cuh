@@ -13,7 +13,7 @@
 // through the matrix descriptor's MN-major layout (instruction-descriptor
 // transpose bits).
 //
-// Work unit = (128 x BN output tile, K split); a CTA walks the units
+// Work unit = (128 x BN output tile, BN = 128, 192 or 256; K split); a CTA walks the units
 // blockIdx.x, blockIdx.x + gridDim.x, ...  Ten or fourteen warps:
 //   warp 0      one lane issues the TMA loads into a STAGES-deep ring
 //   warp 1      allocates TMEM; one lane issues the MMAs (K = 16 per
@@ -81,11 +81,14 @@ struct Cfg {
   static constexpr int EPI_WARPS = 4 * EPI_GROUPS;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int THREADS = 64 + EPI_THREADS;
-  // as many 64-wide K tiles in flight as fit 227 KB beside the epilogue's staging
-  static constexpr int STAGES = BN == 256 ? (EG > 2 ? 3 : 4) : (EG > 2 ? 5 : 6);
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  // as many 64-wide K tiles in flight (at most 6) as fit 227 KB beside the
+  // epilogue's staging, the barriers and the alignment slack
+  static constexpr int STAGING_BYTES = EPI_WARPS * EPI_STAGE_FLOATS * 4;
+  static constexpr int STAGES_FIT = (232448 - 1024 - 256 - STAGING_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT < 6 ? STAGES_FIT : 6;
   static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
   // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], mma_done
   static constexpr int NUM_BARS = 2 * STAGES + 5;
@@ -93,7 +96,7 @@ struct Cfg {
   static constexpr int OFF_EPI = (OFF_MISC + 64 + 15) / 16 * 16;  // the epilogue warps' staging
   static constexpr int SMEM_BYTES = OFF_EPI + EPI_WARPS * EPI_STAGE_FLOATS * 4 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "227 KB of shared memory per CTA");
-  static constexpr int TMEM_COLS = 2 * BN;                  // two accumulators
+  static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // two accumulators (a power of two)
 };
 
 struct Params {

@@ -95,6 +95,11 @@ SHAPES_BF16 = [  # (N rows, IC, OC); IC and OC multiples of 8 (16-byte bf16 rows
     (1024, 4096, 1024),  # 350M MLP output projection (K = 4096)
     (1024, 1280, 3840),  # 774M QKV (K = 1280)
     (1024, 5120, 1280),  # 774M MLP output projection (K = 5120)
+    # 774M at B*T = 4096: 192-wide column tiles (the forward's K-major and the
+    # input gradient's MN-major B), 192-wide tiles split in two for the
+    # attention projection's weight gradient
+    (4096, 1280, 1280),
+    (4096, 5120, 1280),
 ]
 
 
