@@ -220,14 +220,15 @@ struct Params {
   int* err;
 };
 
-// Common prologue: barriers, TMEM allocation (ncols), PDL wait.
+// Common prologue: barriers, TMEM allocation (ncols), PDL wait.  The MMA
+// completion barrier counts one commit per issuing thread (issuers).
 template <int NT>
-GPT2_DEV uint32_t prologue(uint8_t* smem, int ncols) {
+GPT2_DEV uint32_t prologue(uint8_t* smem, int ncols, int issuers = 1) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<NT>::OFF_BAR);
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + Smem<NT>::OFF_BAR + 16);
   if (threadIdx.x == 0) {
     mbar_init(&bars[0], 1);  // TMA
-    mbar_init(&bars[1], 1);  // MMA completion
+    mbar_init(&bars[1], issuers);  // MMA completion
     *reinterpret_cast<volatile int*>(smem + Smem<NT>::OFF_BAR + 24) = 0;  // abort flag
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -411,7 +412,7 @@ GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const CU
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem<DKV_TILES>::OFF_BAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<DKV_TILES>::OFF_BAR + 24);
   float* xa = reinterpret_cast<float*>(smem + Smem<DKV_TILES>::OFF_VEC);  // [2][64] half-row D partials
-  const uint32_t tmem = prologue<DKV_TILES>(smem, 512);
+  const uint32_t tmem = prologue<DKV_TILES>(smem, 512, 2);
 
   const int h = blockIdx.x, b = blockIdx.y, T = p.T, C = p.C;
   const int Tp = (T + 15) & ~15;
@@ -451,8 +452,11 @@ GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const CU
       split_tile_to(v_raw, v_hi, v_lo, helper_index());
     }
     publish_operands();
+    // the two products' 24-MMA chains issued by two threads in different warps
     if (threadIdx.x == 0) {
       mma3(tmem, 0, 128, 192, k_hi, k_lo, HS / 8, Tp);   // S = Q K^T
+      mma_commit(&bars[1]);
+    } else if (threadIdx.x == 32) {
       mma3(tmem, 64, 256, 320, v_hi, v_lo, HS / 8, Tp);  // dP = dY V^T
       mma_commit(&bars[1]);
     }
@@ -478,6 +482,8 @@ GPT2_DEV void bwd_dq(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const CU
     if (threadIdx.x == 0) {
       mma3(tmem, 0, 128, 192, kt_hi, kt_lo, Tp / 8, HS);  // dQ = dS K, over S's columns
       mma_commit(&bars[1]);
+    } else if (threadIdx.x == 32) {
+      mma_commit(&bars[1]);  // the second issuer's arrival (no MMA of its own pending)
     }
     mma_phase = 1;
     ok = wait_all(&bars[1], 1, abort_flag, p.err);
@@ -522,7 +528,7 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const C
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Smem<DKV_TILES>::OFF_BAR + 24);
   float* xa = reinterpret_cast<float*>(smem + Smem<DKV_TILES>::OFF_VEC);  // [2][64] D partials per query
   float* lse_s = xa + 256;                                                  // [64]
-  const uint32_t tmem = prologue<DKV_TILES>(smem, 512);
+  const uint32_t tmem = prologue<DKV_TILES>(smem, 512, 2);
 
   const int h = blockIdx.x, b = blockIdx.y, T = p.T, C = p.C;
   const int Tp = (T + 15) & ~15;
@@ -567,8 +573,11 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const C
       split_tile_to(dy_raw, dy_hi, dy_lo, helper_index());
     }
     publish_operands();
+    // the two products' 24-MMA chains issued by two threads in different warps
     if (threadIdx.x == 0) {
       mma3(tmem, 0, 128, 192, q_hi, q_lo, HS / 8, Tp);     // S^T = K Q^T
+      mma_commit(&bars[1]);
+    } else if (threadIdx.x == 32) {
       mma3(tmem, 64, 256, 320, dy_hi, dy_lo, HS / 8, Tp);  // dP^T = V dY^T
       mma_commit(&bars[1]);
     }
@@ -596,6 +605,8 @@ GPT2_DEV void bwd_dkv(const CUtensorMap* tmQKV, const CUtensorMap* tmDY, const C
     publish_operands();
     if (threadIdx.x == 0) {
       mma3(tmem, 0, 128, 192, dyt_hi, dyt_lo, Tp / 8, HS);  // dV = P^T dY
+      mma_commit(&bars[1]);
+    } else if (threadIdx.x == 32) {
       mma3(tmem, 64, 256, 320, qt_hi, qt_lo, Tp / 8, HS);   // dK = dS^T Q
       mma_commit(&bars[1]);
     }
