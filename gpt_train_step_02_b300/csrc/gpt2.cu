@@ -1088,7 +1088,8 @@ static void attn_forward(gpt2_t* m, float* atty, uint16_t* attybf, float* lse, c
 // the CUDA-core kernels.  Returns the number of launches, or -1.
 static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float* dy, const uint16_t* dy_bf,
                            const float* qkv, const uint16_t* qkv_bf, const float* atty, const float* lse, int B, int T,
-                           int C, int NH, int bf, int* err, cudaStream_t s, float* colsum = nullptr) {
+                           int C, int NH, int bf, int* err, cudaStream_t s, float* colsum = nullptr,
+                           const uint16_t* atty_bf = nullptr) {
   const int hs = C / NH;
   const int grid = ceil_div((long long)B * NH * T * 32, 256);
   const bool tc_path = bf && qkv_bf && dy_bf && hs == tca::HS && T % tca::BQ == 0;
@@ -1113,7 +1114,11 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
   }
   // D holds 2 B NH T floats: the (-lse log2 e, -D) pairs of the tensor-core path
   const int ldg = ceil_div((long long)B * T, tca::LD_WARPS);
-  if (tc_path && C <= 1024)
+  if (tc_path && atty_bf && C <= 1024)  // from the bf16 copies of dO and y (the fp32 ones are not written)
+    launch_k(tca::attn_bwd_ld_bf16_kernel<8>, ldg, tca::LD_WARPS * 32, 0, s, (float2*)D, lse, dy_bf, atty_bf, B, T, C);
+  else if (tc_path && atty_bf && C <= 2048)
+    launch_k(tca::attn_bwd_ld_bf16_kernel<16>, ldg, tca::LD_WARPS * 32, 0, s, (float2*)D, lse, dy_bf, atty_bf, B, T, C);
+  else if (tc_path && C <= 1024)
     launch_k(tca::attn_bwd_ld_kernel<8>, ldg, tca::LD_WARPS * 32, 0, s, (float2*)D, lse, dy, atty, B, T, C);
   else if (tc_path && C <= 2048)
     launch_k(tca::attn_bwd_ld_kernel<16>, ldg, tca::LD_WARPS * 32, 0, s, (float2*)D, lse, dy, atty, B, T, C);
@@ -1152,15 +1157,15 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
 // fuse_bias: the tensor-core kernels leave the 128-row column sums of dqkv in
 // m->scratch (the QKV bias gradient's first stage) and skip the fp32 dqkv,
 // which nothing else reads in bf16 precision
-static void attn_backward(gpt2_t* m, const float* qkv, const uint16_t* qkv_bf, const float* atty, const float* lse,
-                          int B, int T, int bf, bool fuse_bias) {
+static void attn_backward(gpt2_t* m, const float* qkv, const uint16_t* qkv_bf, const float* atty,
+                          const uint16_t* atty_bf, const float* lse, int B, int T, int bf, bool fuse_bias) {
   int C = m->cfg.channels, NH = m->cfg.num_heads, hs = C / NH;
   side_wait(m, &m->rd_dqkv);
   side_wait(m, &m->wd_dqkv);
   if (fuse_bias) side_wait(m, &m->rd_scratch);
   timer_begin(m, TK_ATTN_BWD, 8.0 * (double)B * NH * T * (T + 1) / 2.0 * hs);
   int n = launch_attn_bwd(fuse_bias ? nullptr : m->dqkv, m->dqkv_bf, m->attD, m->datty, m->datty_bf, qkv, qkv_bf, atty,
-                          lse, B, T, C, NH, bf, m->err, m->stream, fuse_bias ? m->scratch : nullptr);
+                          lse, B, T, C, NH, bf, m->err, m->stream, fuse_bias ? m->scratch : nullptr, atty_bf);
   timer_end(m, TK_ATTN_BWD);
   if (n < 0) {
     m->poisoned = GPT2_ERR_CUDA;
@@ -1341,7 +1346,8 @@ static int enqueue_forward(gpt2_t* m, const int* d_in, const int* d_tgt, int B, 
                T, C, c.num_heads, 0);
       m->launches++;
     }
-    attn_forward(m, a.atty, a.atty_bf, a.lse, a.qkv, a.qkv_bf, B, T, bf);
+    // with the tensor-core attention only the bf16 copy of its output is read
+    attn_forward(m, tc_attn ? nullptr : a.atty, a.atty_bf, a.lse, a.qkv, a.qkv_bf, B, T, bf);
     mm_forward(m, a.res2, nullptr, {a.atty, a.atty_bf}, wparam(m, P_ATTPROJW, l * CC), bias(P_ATTPROJB, (size_t)l * C),
                N, C, C, EPI_BIAS_RESID, a.x, nullptr);
     ln_forward(m, bf ? nullptr : a.ln2, a.ln2_bf, a.ln2_mean, a.ln2_rstd, a.res2, m->P[P_LN2W] + (size_t)l * C,
@@ -1419,7 +1425,8 @@ static int enqueue_backward(gpt2_t* m) {
   // the fused column sums need 32-column-aligned rows of 16-byte-aligned floats
   const bool fuse_fcb = bf && !ll && (4 * C) % 32 == 0;
   // the tensor-core attention backward (bf16, hs = 64, T % 128 == 0) takes the QKV bias column sums
-  const bool fuse_qkvb = bf && !ll && C / c.num_heads == tca::HS && T % tca::BQ == 0;
+  const bool tc_attn = bf && C / c.num_heads == tca::HS && T % tca::BQ == 0;  // the tensor-core attention
+  const bool fuse_qkvb = tc_attn && !ll;
   auto gbias = [&](int which, size_t off) -> float* { return ll ? nullptr : G[which] + off; };
   if (m->upd_layers) {
     int rc = mark_touched_rows(m, N);
@@ -1457,9 +1464,10 @@ static int enqueue_backward(gpt2_t* m) {
                 gbias(P_ATTPROJB, (size_t)l * C), m->dln, a.res2, P[P_LN2W] + (size_t)l * C, a.ln2_mean, a.ln2_rstd, N);
     // attention output projection: res2 = x + atty attprojw^T + attprojb
     mm_dw_side(m, G[P_ATTPROJW] + l * CC, dres, {a.atty, a.atty_bf}, N, C, C, &m->wd_dres);
-    mm_dx(m, m->datty, m->datty_bf, dres, wparam(m, P_ATTPROJW, l * CC), N, C, C, nullptr);
+    // (the tensor-core attention backward reads only the bf16 copy of datty)
+    mm_dx(m, tc_attn ? nullptr : m->datty, m->datty_bf, dres, wparam(m, P_ATTPROJW, l * CC), N, C, C, nullptr);
     // attention
-    attn_backward(m, a.qkv, a.qkv_bf, a.atty, a.lse, B, T, bf, fuse_qkvb);
+    attn_backward(m, a.qkv, a.qkv_bf, tc_attn ? nullptr : a.atty, a.atty_bf, a.lse, B, T, bf, fuse_qkvb);
     if (ll) {  // q and k were rotated after the matmul: turn their gradients back (the transpose)
       launch_k(rope_kernel, grid_for((long long)N * C / 2, 256), 256, 0, s, m->dqkv, m->dqkv_bf, (const float2*)m->rope,
                B, T, C, c.num_heads, 1);

@@ -105,7 +105,7 @@ constexpr int TMEM_COLS = 256;  // forward: S in columns [0, 128), P V in [128, 
 struct Params {
   int B, T, C, NH;
   float scale;     // 1/sqrt(hs)
-  float* y;        // (B, T, C) fp32
+  float* y;        // (B, T, C) fp32, or NULL
   uint16_t* ybf;   // (B, T, C) bf16 copy, or NULL
   float* lse;      // (B, NH, T)
   int* err;
@@ -375,9 +375,11 @@ __global__ void __launch_bounds__(THREADS, 2)
       fold_pv(corr_prev);
       const float inv = 1.f / lrow;
       const size_t yo = (size_t)(b * p.T + qt * BQ + r) * p.C + h * HS;
+      if (p.y) {  // NULL when only the bf16 copy is read downstream
 #pragma unroll
-      for (int d = 0; d < HS; d += 4)
-        *reinterpret_cast<float4*>(p.y + yo + d) = make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+        for (int d = 0; d < HS; d += 4)
+          *reinterpret_cast<float4*>(p.y + yo + d) = make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+      }
       if (p.ybf) {
 #pragma unroll
         for (int d = 0; d < HS; d += 8)
@@ -575,6 +577,50 @@ __global__ void __launch_bounds__(LD_WARPS * 32)
       const float4 a = __ldg(reinterpret_cast<const float4*>(dr + d));
       const float4 c = __ldg(reinterpret_cast<const float4*>(yr + d));
       sum[k] = a.x * c.x + a.y * c.y + a.z * c.z + a.w * c.w;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < MAXK; k++) {
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) sum[k] += __shfl_xor_sync(0xffffffffu, sum[k], o);
+  }
+#pragma unroll
+  for (int k = 0; k < MAXK; k++) {
+    const int d = 128 * k + 4 * lane, h = 2 * k + (lane >> 4);
+    if ((lane & 15) == 0 && d < C) {
+      const size_t i = ((size_t)b * NH + h) * T + t;
+      LD[i] = make_float2(-lse[i] * 1.4426950408889634f, -sum[k]);
+    }
+  }
+}
+
+// The same pairs from the bf16 copies of dO and y (the model's bf16 path,
+// where the fp32 ones are not written): lane l reads 4 bf16 (8 bytes) of each
+// at dims 128 k + 4 l .. +3, as above.
+template <int MAXK>  // C <= 128 MAXK
+__global__ void __launch_bounds__(LD_WARPS * 32)
+    attn_bwd_ld_bf16_kernel(float2* __restrict__ LD, const float* __restrict__ lse, const uint16_t* __restrict__ dy,
+                            const uint16_t* __restrict__ y, int B, int T, int C) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * LD_WARPS + (threadIdx.x >> 5);  // token b*T + t
+  if (row >= (long long)B * T) return;
+  const int b = (int)(row / T), t = (int)(row % T), NH = C / HS;
+  const uint16_t* dr = dy + row * C;
+  const uint16_t* yr = y + row * C;
+  float sum[MAXK];
+#pragma unroll
+  for (int k = 0; k < MAXK; k++) {
+    const int d = 128 * k + 4 * lane;
+    sum[k] = 0.f;
+    if (d < C) {
+      const uint2 a = __ldg(reinterpret_cast<const uint2*>(dr + d));
+      const uint2 c = __ldg(reinterpret_cast<const uint2*>(yr + d));
+      sum[k] = __uint_as_float(a.x << 16) * __uint_as_float(c.x << 16) +
+               __uint_as_float(a.x & 0xffff0000u) * __uint_as_float(c.x & 0xffff0000u) +
+               __uint_as_float(a.y << 16) * __uint_as_float(c.y << 16) +
+               __uint_as_float(a.y & 0xffff0000u) * __uint_as_float(c.y & 0xffff0000u);
     }
   }
 #pragma unroll
