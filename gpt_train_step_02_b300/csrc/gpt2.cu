@@ -1041,10 +1041,10 @@ static int launch_attn_fwd(float* atty, uint16_t* attybf, float* lse, const floa
     p.B = B; p.T = T; p.C = C; p.NH = NH;
     p.scale = 1.0f / sqrtf((float)hs);
     p.y = atty; p.ybf = attybf; p.lse = lse; p.err = err;
-    // persistent: two CTAs on each of the 148 SMs walk the (query tile, head, batch) items
-    const long long items = (long long)(T / tca::BQ) * NH * B;
-    launch_k(tca::attn_fwd_tc_kernel, (int)(items < 2 * 148 ? items : 2 * 148), tca::THREADS, tca::fwd::SMEM_BYTES, s,
-             tm, p);
+    // persistent: two CTAs on each SM walk the (query tile, head, batch) items
+    const long long items = (long long)(T / tca::BQ) * NH * B, slots = 2LL * dev_info().num_sms;
+    launch_k(tca::attn_fwd_tc_kernel, (int)(items < slots ? items : slots), tca::THREADS, tca::fwd::SMEM_BYTES, s, tm,
+             p);
     return 1;
   }
   if (attn_tf32_path(bf, hs, T)) {  // fp32, short sequences: one CTA per (head, batch), 3xTF32 products
@@ -1126,16 +1126,21 @@ static int launch_attn_bwd(float* dqkv, uint16_t* dqkv_bf, float* D, const float
     launch_k(attn_bwd_D_kernel, grid, 256, 0, s, tc_path ? nullptr : D, tc_path ? (float2*)D : nullptr, lse, dy, atty,
              B, T, C, NH);
   if (tc_path) {
-    CUtensorMap tq, td;
+    // qkv and dO with 128-row boxes (whole tiles) and 64-row boxes (sub-tiles)
+    CUtensorMap tq, tq64, td, td64;
     if (!make_bf16_map(&tq, qkv_bf, 1, (long long)B * T, 3LL * C, 3LL * C, tca::BQ)) return -1;
+    if (!make_bf16_map(&tq64, qkv_bf, 1, (long long)B * T, 3LL * C, 3LL * C, tca::SUB)) return -1;
     if (!make_bf16_map(&td, dy_bf, 1, (long long)B * T, C, C, tca::BQ)) return -1;
+    if (!make_bf16_map(&td64, dy_bf, 1, (long long)B * T, C, C, tca::SUB)) return -1;
     tca::BwdParams p;
     p.B = B; p.T = T; p.C = C; p.NH = NH;
     p.scale = 1.0f / sqrtf((float)hs);
     p.LD = (const float2*)D; p.dqkv = dqkv; p.dqkv_bf = dqkv_bf; p.colsum = colsum; p.err = err;
-    dim3 g(T / tca::BQ, NH, B);
-    launch_k(tca::attn_bwd_dkv_tc_kernel, g, tca::DKV_THREADS, tca::dkv::SMEM_BYTES, s, tq, td, p);
-    launch_k(tca::attn_bwd_dq_tc_kernel, g, tca::DQ_THREADS, tca::dqk::SMEM_BYTES, s, tq, td, p);
+    // persistent: one CTA per SM walks the (tile, head, batch) items
+    const long long items = (long long)(T / tca::BQ) * NH * B, nsm = dev_info().num_sms;
+    const int g = (int)(items < nsm ? items : nsm);
+    launch_k(tca::attn_bwd_dkv_tc_kernel, g, tca::DKV_THREADS, tca::dkv::SMEM_BYTES, s, tq, tq64, td64, p);
+    launch_k(tca::attn_bwd_dq_tc_kernel, g, tca::DQ_THREADS, tca::dqk::SMEM_BYTES, s, tq, tq64, td, p);
     return 3;
   }
   if (!dqkv || colsum) return -1;  // the CUDA-core kernels store fp32 dqkv only

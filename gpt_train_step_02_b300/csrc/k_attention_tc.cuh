@@ -535,21 +535,23 @@ constexpr uint32_t IDESC_ACC = IDESC_PV;  // 128 x 64 accumulation, B MN-major
 // log-sum-exp, dP = dO V^T, D = rowsum(dO o y) and dS = P o (dP - D):
 //   dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K.
 // Two kernels, each output row produced by one CTA (no atomics, so the
-// result is deterministic):
-//   attn_bwd_dkv_tc_kernel  CTA per (key tile, head, batch); walks the query
+// result is deterministic), both persistent (one CTA per SM walks the work
+// items, longest first):
+//   attn_bwd_dkv_tc_kernel  item (key tile, head, batch); walks the query
 //       tiles at or after the key tile in sub-tiles of 64 queries:
 //       S^T = K Q^T, dP^T = V dO^T into one of two TMEM buffers, P^T and
 //       dS^T (bf16) into one of two shared-memory buffers, dV += P^T dO and
 //       dK += dS^T Q accumulated in TMEM.
-//   attn_bwd_dq_tc_kernel   CTA per (query tile, head, batch); walks the key
+//   attn_bwd_dq_tc_kernel   item (query tile, head, batch); walks the key
 //       tiles at or before it in sub-tiles of 64 keys: S = Q K^T, dP = dO V^T,
 //       dS staged, dQ += dS K in TMEM.
-// The MMA warp issues the scores of sub-tile i+1 before the products of
-// sub-tile i, so the tensor core computes the next scores while the sixteen
-// softmax warps (four per TMEM lane quarter, 16 columns each) work on the
-// current ones.  Operand tiles come from the bf16 copies of qkv and of dO
-// (the gradient of the attention output, (B*T, C)) through TMA maps with
-// 64 x 128 boxes; a 64-row sub-tile starts 8 KB into its 128-row tile.
+// The scores of sub-tile i+1 are issued before the products of sub-tile i,
+// so the tensor core computes the next scores while the sixteen softmax
+// warps (four per TMEM lane quarter, 16 columns each) work on the current
+// ones.  Operand tiles come from the bf16 copies of qkv and of dO (the
+// gradient of the attention output, (B*T, C)) through TMA maps with 64 x 128
+// boxes for the item's fixed tile and 64 x 64 boxes for the streamed
+// sub-tiles.
 // The per-query pairs LD[b,h,t] = (-lse log2 e, -D) with D = sum_d dO y over
 // the head's 64 dims (the rowsum the backward subtracts from dP).  One warp
 // per token: lane l reads dims 128 k + 4 l .. +3 of dO and y (all loads
@@ -638,69 +640,110 @@ __global__ void __launch_bounds__(LD_WARPS * 32)
   }
 }
 
+// Work item r of this CTA in the persistent backward kernels: items are
+// numbered w = 0 .. (T/128) B NH - 1 with rank w / (B NH) (0 = the most
+// causal work: key tile 0 for dK/dV, the last query tile for dQ) and
+// head/batch w % (B NH); CTA c of G takes w = r G + c in even rounds r and
+// r G + G-1-c in odd ones (a snake that evens out the causal lengths).
+GPT2_DEV bool bwd_item(const BwdParams& p, int r, int& rank, int& h, int& b) {
+  const int BH = p.B * p.NH, nitems = (p.T / BQ) * BH, G = gridDim.x, c = blockIdx.x;
+  const int w = r * G + ((r & 1) ? G - 1 - c : c);
+  if (w >= nitems) return false;
+  rank = w / BH;
+  h = (w % BH) % p.NH;
+  b = (w % BH) / p.NH;
+  return true;
+}
+
 namespace dkv {
+// The query side streams through a ring of NSQ stages of one 64-query
+// sub-tile each (Q, dO and their (-lse log2 e, -D) pairs): a stage is
+// refilled as soon as its sub-tile's dV / dK products have read it, so a
+// copy has about NSQ - 2 sub-tile periods to land.
+constexpr int NSQ = 5;
+constexpr int SUBT_BYTES = SUB * HS * 2;           // 8 KB: 64 rows of 64 bf16
 constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + TILE_BYTES;
-constexpr int OFF_Q = OFF_V + TILE_BYTES;          // 2 stages
-constexpr int OFF_DO = OFF_Q + 2 * TILE_BYTES;     // 2 stages
+constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;      // K and V: 2 stages (one per item in flight)
+constexpr int OFF_Q = OFF_V + 2 * TILE_BYTES;      // NSQ stages
+constexpr int OFF_DO = OFF_Q + NSQ * SUBT_BYTES;   // NSQ stages
 constexpr int SUB_BYTES = 128 * SUB * 2;           // 16 KB: a 128 x 64 bf16 P^T or dS^T
-constexpr int OFF_PT = OFF_DO + 2 * TILE_BYTES;    // 2 buffers
+constexpr int OFF_PT = OFF_DO + NSQ * SUBT_BYTES;  // 2 buffers
 constexpr int OFF_DST = OFF_PT + 2 * SUB_BYTES;    // 2 buffers
-constexpr int LD_BYTES = 128 * 8;                  // (-lse log2 e, -D) of one query tile
-constexpr int OFF_LD = OFF_DST + 2 * SUB_BYTES;    // 2 stages
-constexpr int OFF_BAR = OFF_LD + 2 * LD_BYTES;
-// kv_full, qd_full[2], qd_empty[2], s_full[2], st_ready[2], pt_free[2], mma_done, s_done
-constexpr int NUM_BARS = 13;
+constexpr int LD_BYTES = SUB * 8;                  // (-lse log2 e, -D) of one sub-tile
+constexpr int OFF_LD = OFF_DST + 2 * SUB_BYTES;    // NSQ stages
+constexpr int RED_BYTES = 2 * 4 * 4 * 16 * 4;      // column-sum partials [dK, dV][qs][q4][16]
+constexpr int OFF_RED = OFF_LD + NSQ * LD_BYTES;   // 2 buffers (items alternate)
+constexpr int OFF_BAR = OFF_RED + 2 * RED_BYTES;
+// kv_full[2], kv_empty[2], qd_full[NSQ], qd_empty[NSQ], s_full[2],
+// st_ready[2], pt_free[2], acc_full[2], acc_empty[2], mma_done, s_done
+constexpr int NUM_BARS = 16 + 2 * NSQ;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 }  // namespace dkv
 
 // dK/dV: each of the four accumulation chains (S^T, dP^T, dV, dK) is issued
-// by its own thread, in its own warp (warp 1 and three warps after the
-// softmax warps), so that their issue times overlap: a 128 x 64 x 16 MMA
-// takes about as long to issue as a 256-wide one.  The barriers a pair of
-// chains completes together (s_full, pt_free, qd_empty, mma_done, s_done)
+// by its own thread, in its own warp, so that their issue times overlap: a
+// 128 x 64 x 16 MMA takes about as long to issue as a 256-wide one.  The
+// four threads sit on the four SM sub-partitions (warp w runs on w mod 4:
+// dK warp 0, S^T warp 1, dV warp 18, dP^T warp 19), one each: a
+// sub-partition that hosted two such polling threads started its softmax
+// warps about 0.45 us late on every sub-tile.  So there is no separate
+// copy thread: the S^T issuer loads the next item's K and V, the dV issuer
+// refills the query-side stages.  The barriers a pair of chains completes
+// together (s_full, kv_empty, pt_free, qd_empty, acc_full, mma_done, s_done)
 // count two arrivals.
-constexpr int DKV_THREADS = BWD_THREADS + 96;
+constexpr int DKV_THREADS = BWD_THREADS + 64;
+constexpr int DKV_DK_WARP = 0;
 constexpr int DKV_DV_WARP = 2 + BWD_SOFTMAX_WARPS;  // 18
 constexpr int DKV_DPT_WARP = DKV_DV_WARP + 1;       // 19
-constexpr int DKV_DK_WARP = DKV_DV_WARP + 2;        // 20
 
+// Persistent: one CTA per SM walks the (key tile, head, batch) items (see
+// bwd_item).  Counters run on across items: item n uses K/V stage and
+// accumulator pair n & 1; sub-tile number g (over all of the CTA's items)
+// uses Q/dO/LD stage g % NSQ, score buffer and P^T/dS^T buffer g & 1.  So the
+// next item's K and V load, and its first scores compute, while the softmax
+// warps finish the current item and read its dV and dK out of tensor memory.
+// tmKV: qkv with 128-row boxes (K, V tiles); tmQ, tmDO: qkv and dO with
+// 64-row boxes (query sub-tiles).
 __global__ void __launch_bounds__(DKV_THREADS, 1)
-    attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
-                           const __grid_constant__ BwdParams p) {
+    attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmQ,
+                           const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ BwdParams p) {
   pdl_launch_dependents();
   using namespace dkv;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* kv_full = bars;
-  uint64_t* qd_full = bars + 1;
-  uint64_t* qd_empty = bars + 3;
-  uint64_t* s_full = bars + 5;
-  uint64_t* st_ready = bars + 7;
-  uint64_t* pt_free = bars + 9;
-  uint64_t* mma_done = bars + 11;
-  uint64_t* s_done = bars + 12;
+  uint64_t* kv_empty = bars + 2;
+  uint64_t* qd_full = bars + 4;
+  uint64_t* qd_empty = qd_full + NSQ;
+  uint64_t* s_full = qd_empty + NSQ;
+  uint64_t* st_ready = s_full + 2;
+  uint64_t* pt_free = s_full + 4;
+  uint64_t* acc_full = s_full + 6;
+  uint64_t* acc_empty = s_full + 8;
+  uint64_t* mma_done = s_full + 10;
+  uint64_t* s_done = s_full + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = p.T / BKV;
-  const int kt = (int)blockIdx.x;  // key tile; walks query tiles kt .. nt-1
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int niter = nt - kt;       // query tiles
-  const int nsub = 2 * niter;      // 64-query sub-tiles
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    for (int s = 0; s < 2; s++) {
+    for (int s = 0; s < NSQ; s++) {
       mbar_init(&qd_full[s], 1);
       mbar_init(&qd_empty[s], 2);                  // the dV and dK issuers
+    }
+    for (int s = 0; s < 2; s++) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 2);                  // the S^T and dP^T issuers
       mbar_init(&s_full[s], 2);                    // the S^T and dP^T issuers
       mbar_init(&st_ready[s], BWD_SOFTMAX_WARPS);  // one arrival per softmax warp
       mbar_init(&pt_free[s], 2);                   // the dV and dK issuers
+      mbar_init(&acc_full[s], 2);                  // the dV and dK issuers
+      mbar_init(&acc_empty[s], BWD_SOFTMAX_WARPS); // one arrival per softmax warp
     }
     mbar_init(mma_done, 2);
     mbar_init(s_done, 2);
@@ -718,165 +761,227 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the first global-memory access comes after this
-  // TMEM: buffer x in columns [128 x, 128 x + 128): S^T then dP^T (64 each); dV, dK
-  const uint32_t T_DV = tmem + 256, T_DK = tmem + 320;
-  const size_t bh = ((size_t)b * p.NH + h) * p.T;
+  // TMEM: score buffer x in columns [128 x, 128 x + 128): S^T then dP^T (64
+  // each); accumulator pair a in [256 + 128 a, 384 + 128 a): dV then dK
+  auto t_dv = [&](int a) { return tmem + 256 + 128 * a; };
 
-  if (warp == 0) {
-    if (lane == 0) {
-      const int krow = b * p.T + kt * BKV;
-      mbar_expect_tx(kv_full, 2 * TILE_BYTES);
-      tma_load_2d(smem + OFF_K, &tmQKV, p.C + h * HS, krow, kv_full);
-      tma_load_2d(smem + OFF_V, &tmQKV, 2 * p.C + h * HS, krow, kv_full);
-      int issued = 0;
-      for (int i = 0; i < niter; i++) {
-        const int s = i & 1, qt = kt + i, qrow = b * p.T + qt * BQ;
-        if (!mbar_wait(&qd_empty[s], ((i >> 1) & 1) ^ 1, abort_flag, p.err)) break;
-        mbar_expect_tx(&qd_full[s], 2 * TILE_BYTES + LD_BYTES);
-        tma_load_2d(smem + OFF_Q + s * TILE_BYTES, &tmQKV, h * HS, qrow, &qd_full[s]);
-        tma_load_2d(smem + OFF_DO + s * TILE_BYTES, &tmDO, h * HS, qrow, &qd_full[s]);
-        bulk_load(smem + OFF_LD + s * LD_BYTES, p.LD + bh + qt * BQ, LD_BYTES, &qd_full[s]);
-        issued = i + 1;
-      }
-      if (*abort_flag) {
-        mbar_wait_drain(kv_full, 0);
-        for (int i = max(0, issued - 2); i < issued; i++) mbar_wait_drain(&qd_full[i & 1], (i >> 1) & 1);
-      }
-    }
-  } else if (warp == 1 || warp == DKV_DPT_WARP) {
+  if (warp == 1 || warp == DKV_DPT_WARP) {
     // ---------------- scores issuers: S^T = K Q^T (warp 1), dP^T = V dO^T ----------------
+    // The S^T issuer also loads K and V: item 0's at the start, item n + 1's
+    // once item n's first scores are issued (item n - 1's have completed by
+    // then, so its stage is free).
     if (lane == 0) {
       const bool dpt = warp == DKV_DPT_WARP;
-      const uint32_t sa = smem_u32(smem + (dpt ? OFF_V : OFF_K));
-      bool ok = mbar_wait(kv_full, 0, abort_flag, p.err);
-      for (int j = 0; j < nsub && ok; j++) {
-        const int it = j >> 1, s = it & 1, u = j & 1;
-        // TMEM buffer j & 1 was read out by the softmax warps before st_ready(j - 2)
-        if (j >= 2 && !mbar_wait(&st_ready[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.err)) break;
-        if (u == 0 && !mbar_wait(&qd_full[s], (it >> 1) & 1, abort_flag, p.err)) break;
-        tc_fence_after();
-        const uint32_t sb = smem_u32(smem + (dpt ? OFF_DO : OFF_Q) + s * TILE_BYTES) + u * (TILE_BYTES / 2);
-        const uint32_t t_acc = tmem + (j & 1) * 128 + (dpt ? SUB : 0);
+      int g = 0, nkv = 0;  // nkv: K/V stage fills issued (S^T issuer)
+      bool ok = true;
+      int kt, h, b;
+      auto load_kv = [&](int n) {  // item n's K and V into stage n & 1, if the item exists
+        int kt2, h2, b2;
+        if (!bwd_item(p, n, kt2, h2, b2)) return true;
+        const int y = n & 1, krow = b2 * p.T + kt2 * BKV;
+        if (n >= 2 && !mbar_wait(&kv_empty[y], ((n >> 1) & 1) ^ 1, abort_flag, p.err)) return false;
+        mbar_expect_tx(&kv_full[y], 2 * TILE_BYTES);
+        tma_load_2d(smem + OFF_K + y * TILE_BYTES, &tmKV, p.C + h2 * HS, krow, &kv_full[y]);
+        tma_load_2d(smem + OFF_V + y * TILE_BYTES, &tmKV, 2 * p.C + h2 * HS, krow, &kv_full[y]);
+        nkv = n + 1;
+        return true;
+      };
+      if (!dpt) ok = load_kv(0);
+      for (int n = 0; ok && bwd_item(p, n, kt, h, b); n++) {
+        const int x = n & 1;
+        if (!(ok = mbar_wait(&kv_full[x], (n >> 1) & 1, abort_flag, p.err))) break;
+        const uint32_t sa = smem_u32(smem + (dpt ? OFF_V : OFF_K) + x * TILE_BYTES);
+        for (int qt = kt; ok && qt < nt; qt++) {
+          for (int u = 0; u < 2; u++, g++) {
+            const int s = g % NSQ;
+            // score buffer g & 1 was read out by the softmax warps before st_ready(g - 2)
+            if (g >= 2 && !(ok = mbar_wait(&st_ready[g & 1], ((g - 2) >> 1) & 1, abort_flag, p.err))) break;
+            if (!(ok = mbar_wait(&qd_full[s], (g / NSQ) & 1, abort_flag, p.err))) break;
+            tc_fence_after();
+            const uint32_t sb = smem_u32(smem + (dpt ? OFF_DO : OFF_Q) + s * SUBT_BYTES);
+            const uint32_t t_acc = tmem + (g & 1) * 128 + (dpt ? SUB : 0);
 #pragma unroll
-        for (int kk = 0; kk < HS / 16; kk++)
-          mma_bf16(t_acc, desc_sw128(sa + kk * 32, 16, 1024), desc_sw128(sb + kk * 32, 16, 1024), IDESC_S64,
-                   kk > 0 ? 1u : 0u);
-        mma_commit(&s_full[j & 1]);
+            for (int kk = 0; kk < HS / 16; kk++)
+              mma_bf16(t_acc, desc_sw128(sa + kk * 32, 16, 1024), desc_sw128(sb + kk * 32, 16, 1024), IDESC_S64,
+                       kk > 0 ? 1u : 0u);
+            mma_commit(&s_full[g & 1]);
+            if (!dpt && qt == kt && u == 0 && !(ok = load_kv(n + 1))) break;
+          }
+        }
+        if (ok) mma_commit(&kv_empty[x]);  // the item's K (V) stage is free once these scores complete
       }
-      // the scores these threads issued land before the CTA's resources go
+      // the scores these threads issued land before the CTA's resources go,
+      // and so do the K/V copies still in flight (the latest fill of each stage)
       mma_commit(s_done);
       mbar_wait_drain(s_done, 0);
+      for (int i = max(0, nkv - 2); i < nkv; i++) mbar_wait_drain(&kv_full[i & 1], (i >> 1) & 1);
     }
   } else if (warp == DKV_DV_WARP || warp == DKV_DK_WARP) {
     // ---------------- products issuers: dV += P^T dO, dK += dS^T Q ----------------
     // (a sub-tile's scores have completed by the time its st_ready fires: the
-    // softmax warps waited for them, so these commits cover the tile's Q/dO)
+    // softmax warps waited for them, so these commits cover the tile's Q/dO.)
+    // The dV issuer also fills the query-side stages: fill f (the CTA's f-th
+    // 64-query sub-tile in walk order) goes to stage f % NSQ; the first NSQ at
+    // the start, then after sub-tile g's products the fill that reuses the
+    // stage of sub-tile g - 1 (whose products have completed by then).
     if (lane == 0) {
       const bool dk = warp == DKV_DK_WARP;
-      const uint32_t t_acc = dk ? T_DK : T_DV;
-      for (int i = 0; i < nsub; i++) {
-        if (!mbar_wait(&st_ready[i & 1], (i >> 1) & 1, abort_flag, p.err)) break;
-        tc_fence_after();
-        const int it = i >> 1, s = it & 1, u = i & 1;
-        const uint32_t sb = smem_u32(smem + (dk ? OFF_Q : OFF_DO) + s * TILE_BYTES) + u * (TILE_BYTES / 2);
-        const uint32_t sa = smem_u32(smem + (dk ? OFF_DST : OFF_PT) + (i & 1) * SUB_BYTES);
+      int g = 0, nfill = 0;
+      bool ok = true;
+      int kt, h, b;
+      int fn = 0, fkt = 0, fh = 0, fb = 0;  // the next fill: item fn, query position fq0
+      bool fmore = !dk && bwd_item(p, 0, fkt, fh, fb);
+      int fq0 = fkt * BQ;
+      auto fill = [&]() {
+        const int s = nfill % NSQ;
+        const size_t bh = ((size_t)fb * p.NH + fh) * p.T;
+        mbar_expect_tx(&qd_full[s], 2 * SUBT_BYTES + LD_BYTES);
+        tma_load_2d(smem + OFF_Q + s * SUBT_BYTES, &tmQ, fh * HS, fb * p.T + fq0, &qd_full[s]);
+        tma_load_2d(smem + OFF_DO + s * SUBT_BYTES, &tmDO, fh * HS, fb * p.T + fq0, &qd_full[s]);
+        bulk_load(smem + OFF_LD + s * LD_BYTES, p.LD + bh + fq0, LD_BYTES, &qd_full[s]);
+        nfill++;
+        fq0 += SUB;
+        if (fq0 >= p.T) {
+          fmore = bwd_item(p, ++fn, fkt, fh, fb);
+          fq0 = fkt * BQ;
+        }
+      };
+      while (fmore && nfill < NSQ) fill();
+      for (int n = 0; ok && bwd_item(p, n, kt, h, b); n++) {
+        const int x = n & 1;
+        const uint32_t t_acc = t_dv(x) + (dk ? HS : 0);
+        // accumulator pair x was read out by the softmax warps of item n - 2
+        if (!(ok = mbar_wait(&acc_empty[x], ((n >> 1) & 1) ^ 1, abort_flag, p.err))) break;
+        for (int qt = kt; ok && qt < nt; qt++) {
+          for (int u = 0; u < 2; u++, g++) {
+            const int s = g % NSQ;
+            if (!(ok = mbar_wait(&st_ready[g & 1], (g >> 1) & 1, abort_flag, p.err))) break;
+            tc_fence_after();
+            const uint32_t sb = smem_u32(smem + (dk ? OFF_Q : OFF_DO) + s * SUBT_BYTES);
+            const uint32_t sa = smem_u32(smem + (dk ? OFF_DST : OFF_PT) + (g & 1) * SUB_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < SUB / 16; kk++)
-          mma_bf16(t_acc, desc_sw128(sa + kk * 32, 16, 1024), desc_sw128(sb + kk * 2048, 8192, 1024), IDESC_ACC,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&pt_free[i & 1]);
-        if (u == 1) mma_commit(&qd_empty[s]);
+            for (int kk = 0; kk < SUB / 16; kk++)
+              mma_bf16(t_acc, desc_sw128(sa + kk * 32, 16, 1024), desc_sw128(sb + kk * 2048, 8192, 1024), IDESC_ACC,
+                       (qt > kt || u > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&pt_free[g & 1]);
+            mma_commit(&qd_empty[s]);
+            if (fmore && nfill - NSQ < g) {  // refill the stage of sub-tile nfill - NSQ (= g - 1)
+              const int f0 = nfill - NSQ;
+              if (!(ok = mbar_wait(&qd_empty[f0 % NSQ], (f0 / NSQ) & 1, abort_flag, p.err))) break;
+              fill();
+            }
+          }
+        }
+        if (ok) mma_commit(&acc_full[x]);
       }
       mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0);
+      // the query-side copies still in flight land before the CTA's memory goes
+      for (int i = max(0, nfill - NSQ); i < nfill; i++) mbar_wait_drain(&qd_full[i % NSQ], (i / NSQ) & 1);
     }
   } else {
+    // ---------------- softmax warps, then each item's dV / dK read-out ----------------
     const int q4 = warp & 3, qs = (warp - 2) >> 2;  // TMEM lane quarter; 16-column slice
     const int r = q4 * 32 + lane;  // key row within the tile = TMEM lane
-    const int k = kt * BKV + r;    // key position
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const float sl2 = p.scale * 1.4426950408889634f;
     const float2 sl2v = make_float2(sl2, sl2);
     bool ok = true;
-    for (int i = 0; i < nsub; i++) {
-      const int it = i >> 1, s = it & 1, u = i & 1;
-      // one decision per warp: the TMEM loads below are warp-collective
-      const bool got = mbar_wait(&s_full[i & 1], (i >> 1) & 1, abort_flag, p.err) &&
-                       mbar_wait(&qd_full[s], (it >> 1) & 1, abort_flag, p.err) &&
-                       (i < 2 || mbar_wait(&pt_free[i & 1], ((i - 2) >> 1) & 1, abort_flag, p.err));
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float st[BWD_CW], dpt[BWD_CW];
-      const uint32_t t_st = tmem + (i & 1) * 128 + lane_off + qs * BWD_CW;
-      tmem_ld16x2(t_st, t_st + SUB, st, dpt);
-      // queries u*64 + qs*16 + c of this query tile; before the key (masked) only in the first
-      const float4* ld = reinterpret_cast<const float4*>(smem + OFF_LD + s * LD_BYTES) + (u * SUB + qs * BWD_CW) / 2;
-      if (it == 0) {
-        const int lim = r - u * SUB - qs * BWD_CW;  // column c is masked when c < lim
+    int g = 0;
+    int kt, h, b;
+    for (int n = 0; bwd_item(p, n, kt, h, b); n++) {
+      const int x = n & 1;
+      for (int qt = kt; qt < nt; qt++) {
+        for (int u = 0; u < 2; u++, g++) {
+          if (!ok) continue;  // after a timeout: count through to the item's end
+          const int s = g % NSQ;
+          // one decision per warp: the TMEM loads below are warp-collective
+          const bool got = mbar_wait(&s_full[g & 1], (g >> 1) & 1, abort_flag, p.err) &&
+                           mbar_wait(&qd_full[s], (g / NSQ) & 1, abort_flag, p.err) &&
+                           (g < 2 || mbar_wait(&pt_free[g & 1], ((g - 2) >> 1) & 1, abort_flag, p.err));
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+          float st[BWD_CW], dpt[BWD_CW];
+          const uint32_t t_st = tmem + (g & 1) * 128 + lane_off + qs * BWD_CW;
+          tmem_ld16x2(t_st, t_st + SUB, st, dpt);
+          // queries u*64 + qs*16 + c of this query tile; before the key (masked) only on the diagonal
+          const float4* ld = reinterpret_cast<const float4*>(smem + OFF_LD + s * LD_BYTES) + qs * BWD_CW / 2;
+          if (qt == kt) {
+            const int lim = r - u * SUB - qs * BWD_CW;  // column c is masked when c < lim
 #pragma unroll
-        for (int c = 0; c < BWD_CW; c++)
-          if (c < lim) st[c] = -INFINITY;
-      }
-      uint32_t wp[BWD_CW / 2], wd[BWD_CW / 2];
+            for (int c = 0; c < BWD_CW; c++)
+              if (c < lim) st[c] = -INFINITY;
+          }
+          uint32_t wp[BWD_CW / 2], wd[BWD_CW / 2];
 #pragma unroll
-      for (int e = 0; e < BWD_CW / 2; e++) {
-        const float4 v = ld[e];  // (-lse2, -D) of queries 2e, 2e+1
-        const float2 x = fma2(make_float2(st[2 * e], st[2 * e + 1]), sl2v, make_float2(v.x, v.z));
-        const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-        const float2 ds = mul2(pp, add2(make_float2(dpt[2 * e], dpt[2 * e + 1]), make_float2(v.y, v.w)));
-        wp[e] = cvt_bf16x2(pp.x, pp.y);
-        wd[e] = cvt_bf16x2(ds.x, ds.y);
-      }
-      st_quarter_row_sw128(smem + OFF_PT + (i & 1) * SUB_BYTES, r, qs, wp);
-      st_quarter_row_sw128(smem + OFF_DST + (i & 1) * SUB_BYTES, r, qs, wd);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc_fence_before();
-      tc::mbar_arrive_warp(&st_ready[i & 1]);
-    }
-    if (tc::epi_bar_and<32 * BWD_SOFTMAX_WARPS>(ok && mbar_wait(mma_done, 0, abort_flag, p.err) && !*abort_flag)) {
-      tc_fence_after();
-      float dv[BWD_CW], dk[BWD_CW];
-      tmem_ld16x2(T_DV + lane_off + qs * BWD_CW, T_DK + lane_off + qs * BWD_CW, dv, dk);
-#pragma unroll
-      for (int d = 0; d < BWD_CW; d++) dk[d] *= p.scale;
-      const size_t o = ((size_t)b * p.T + k) * 3 * p.C + h * HS + qs * BWD_CW;
-      if (p.dqkv) {
-#pragma unroll
-        for (int d = 0; d < BWD_CW; d += 4) {
-          *reinterpret_cast<float4*>(p.dqkv + o + p.C + d) = make_float4(dk[d], dk[d + 1], dk[d + 2], dk[d + 3]);
-          *reinterpret_cast<float4*>(p.dqkv + o + 2 * p.C + d) = make_float4(dv[d], dv[d + 1], dv[d + 2], dv[d + 3]);
+          for (int e = 0; e < BWD_CW / 2; e++) {
+            const float4 v = ld[e];  // (-lse2, -D) of queries 2e, 2e+1
+            const float2 xx = fma2(make_float2(st[2 * e], st[2 * e + 1]), sl2v, make_float2(v.x, v.z));
+            const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
+            const float2 ds = mul2(pp, add2(make_float2(dpt[2 * e], dpt[2 * e + 1]), make_float2(v.y, v.w)));
+            wp[e] = cvt_bf16x2(pp.x, pp.y);
+            wd[e] = cvt_bf16x2(ds.x, ds.y);
+          }
+          st_quarter_row_sw128(smem + OFF_PT + (g & 1) * SUB_BYTES, r, qs, wp);
+          st_quarter_row_sw128(smem + OFF_DST + (g & 1) * SUB_BYTES, r, qs, wd);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tc_fence_before();
+          tc::mbar_arrive_warp(&st_ready[g & 1]);
         }
       }
-      if (p.dqkv_bf) {
+      // the item's dK then dV (accumulator pair x, one half at a time to
+      // keep registers down), then the pair is released
+      const bool got = __all_sync(0xffffffffu, ok && mbar_wait(&acc_full[x], (n >> 1) & 1, abort_flag, p.err));
+      float* red = reinterpret_cast<float*>(smem + OFF_RED + x * RED_BYTES);  // [dK, dV][qs][q4][16]
+      if (got) {
+        tc_fence_after();
+        const size_t o = ((size_t)b * p.T + kt * BKV + r) * 3 * p.C + h * HS + qs * BWD_CW;
+#pragma unroll 1
+        for (int arr = 0; arr < 2; arr++) {  // 0: dK (scaled), 1: dV
+          float v[BWD_CW];
+          tmem_ld16(t_dv(x) + (arr == 0 ? HS : 0) + lane_off + qs * BWD_CW, v);
+          if (arr == 1) {
+            tc_fence_before();
+            tc::mbar_arrive_warp(&acc_empty[x]);
+          } else {
 #pragma unroll
-        for (int d = 0; d < BWD_CW; d += 8) {
-          *reinterpret_cast<uint4*>(p.dqkv_bf + o + p.C + d) =
-              make_uint4(cvt_bf16x2(dk[d], dk[d + 1]), cvt_bf16x2(dk[d + 2], dk[d + 3]), cvt_bf16x2(dk[d + 4], dk[d + 5]),
-                         cvt_bf16x2(dk[d + 6], dk[d + 7]));
-          *reinterpret_cast<uint4*>(p.dqkv_bf + o + 2 * p.C + d) =
-              make_uint4(cvt_bf16x2(dv[d], dv[d + 1]), cvt_bf16x2(dv[d + 2], dv[d + 3]), cvt_bf16x2(dv[d + 4], dv[d + 5]),
-                         cvt_bf16x2(dv[d + 6], dv[d + 7]));
+            for (int d = 0; d < BWD_CW; d++) v[d] *= p.scale;
+          }
+          const size_t oa = o + (1 + arr) * p.C;
+          if (p.dqkv) {
+#pragma unroll
+            for (int d = 0; d < BWD_CW; d += 4)
+              *reinterpret_cast<float4*>(p.dqkv + oa + d) = make_float4(v[d], v[d + 1], v[d + 2], v[d + 3]);
+          }
+          if (p.dqkv_bf) {
+#pragma unroll
+            for (int d = 0; d < BWD_CW; d += 8)
+              *reinterpret_cast<uint4*>(p.dqkv_bf + oa + d) =
+                  make_uint4(cvt_bf16x2(v[d], v[d + 1]), cvt_bf16x2(v[d + 2], v[d + 3]),
+                             cvt_bf16x2(v[d + 4], v[d + 5]), cvt_bf16x2(v[d + 6], v[d + 7]));
+          }
+          if (p.colsum) {
+            // the 128 key rows' column sums: warp butterflies here, then the
+            // four lane quarters in order through this item's partials buffer
+            const float sc = warp_colsum16(v, lane);
+            if (lane < 16) red[((arr * 4 + qs) * 4 + q4) * 16 + lane] = sc;
+          }
         }
       }
       if (p.colsum) {
-        // the 128 key rows' column sums: warp butterflies, then the four lane
-        // quarters in order, through the (-lse, -D) staging area (free now)
-        float* red = reinterpret_cast<float*>(smem + OFF_LD);  // [dK, dV][qs][q4][16]
-        const float sk = warp_colsum16(dk, lane), sv = warp_colsum16(dv, lane);
-        if (lane < 16) {
-          red[((0 * 4 + qs) * 4 + q4) * 16 + lane] = sk;
-          red[((1 * 4 + qs) * 4 + q4) * 16 + lane] = sv;
-        }
-        tc::epi_bar<32 * BWD_SOFTMAX_WARPS>();
+        // all sixteen warps take every item's barrier; a timeout anywhere ends the walk for all
+        if (!tc::epi_bar_and<32 * BWD_SOFTMAX_WARPS>(got)) break;
         const int t2 = threadIdx.x - 64;
         if (t2 < 128) {
           const int arr = t2 >> 6, col = t2 & 63, base = (arr * 4 + (col >> 4)) * 4 * 16 + (col & 15);
           const float sum = ((red[base] + red[base + 16]) + red[base + 32]) + red[base + 48];
           p.colsum[((size_t)b * nt + kt) * 3 * p.C + (1 + arr) * p.C + h * HS + col] = sum;
         }
+      } else if (!got) {
+        break;
       }
     }
   }
@@ -890,15 +995,22 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
 }
 
 namespace dqk {
-constexpr int OFF_Q = 0;
-constexpr int OFF_DO = OFF_Q + TILE_BYTES;
-constexpr int OFF_K = OFF_DO + TILE_BYTES;      // 2 stages
-constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;   // 2 stages
+// The key side streams through a ring of NSK stages of one 64-key sub-tile
+// each (K and V), refilled as soon as the sub-tile's dQ product has read it.
+constexpr int NSK = 6;
+constexpr int SUBT_BYTES = SUB * HS * 2;          // 8 KB: 64 rows of 64 bf16
+constexpr int OFF_Q = 0;                          // 2 stages (one per item in flight)
+constexpr int OFF_DO = OFF_Q + 2 * TILE_BYTES;    // 2 stages
+constexpr int OFF_K = OFF_DO + 2 * TILE_BYTES;    // NSK stages
+constexpr int OFF_V = OFF_K + NSK * SUBT_BYTES;   // NSK stages
 constexpr int SUB_BYTES = 128 * SUB * 2;
-constexpr int OFF_DS = OFF_V + 2 * TILE_BYTES;  // dS, 2 buffers of 128 x 64 bf16
-constexpr int OFF_BAR = OFF_DS + 2 * SUB_BYTES;
-// qd_full, kv_full[2], kv_empty[2], s_full[2], ds_ready[2], ds_free[2], mma_done, s_done
-constexpr int NUM_BARS = 13;
+constexpr int OFF_DS = OFF_V + NSK * SUBT_BYTES;  // dS, 2 buffers of 128 x 64 bf16
+constexpr int RED_BYTES = 4 * 4 * 16 * 4;         // column-sum partials [qs][q4][16]
+constexpr int OFF_RED = OFF_DS + 2 * SUB_BYTES;   // 2 buffers (items alternate)
+constexpr int OFF_BAR = OFF_RED + 2 * RED_BYTES;
+// qd_full[2], qd_empty[2], kv_full[NSK], kv_empty[NSK], s_full[2],
+// ds_ready[2], ds_free[2], acc_full[2], acc_empty[2], mma_done, s_done
+constexpr int NUM_BARS = 16 + 2 * NSK;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -906,46 +1018,53 @@ static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 // dQ: the three accumulation chains (S, dP, dQ) issued by three threads in
 // different warps (warp 1 and two warps after the softmax warps), as in the
-// dK/dV kernel; s_full and s_done count the two scores issuers.
+// dK/dV kernel; s_full, qd_empty and s_done count the two scores issuers.
 constexpr int DQ_THREADS = BWD_THREADS + 64;
 constexpr int DQ_DQ_WARP = 2 + BWD_SOFTMAX_WARPS;  // 18
 constexpr int DQ_DP_WARP = DQ_DQ_WARP + 1;         // 19
 
+// Persistent like the dK/dV kernel: item n of the CTA uses Q/dO stage and dQ
+// accumulator n & 1, sub-tile number g (over all of its items) K/V stage
+// g % NSK, score buffer and dS buffer g & 1.  tmQ, tmDO: qkv and dO with
+// 128-row boxes (query tiles); tmKV: qkv with 64-row boxes (key sub-tiles).
 __global__ void __launch_bounds__(DQ_THREADS, 1)
-    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
-                          const __grid_constant__ BwdParams p) {
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
+                          const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ BwdParams p) {
   pdl_launch_dependents();
   using namespace dqk;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* qd_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = bars + 3;
-  uint64_t* s_full = bars + 5;
-  uint64_t* ds_ready = bars + 7;
-  uint64_t* ds_free = bars + 9;
-  uint64_t* mma_done = bars + 11;
-  uint64_t* s_done = bars + 12;
+  uint64_t* qd_empty = bars + 2;
+  uint64_t* kv_full = bars + 4;
+  uint64_t* kv_empty = kv_full + NSK;
+  uint64_t* s_full = kv_empty + NSK;
+  uint64_t* ds_ready = s_full + 2;
+  uint64_t* ds_free = s_full + 4;
+  uint64_t* acc_full = s_full + 6;
+  uint64_t* acc_empty = s_full + 8;
+  uint64_t* mma_done = s_full + 10;
+  uint64_t* s_done = s_full + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = p.T / BQ;
-  const int qt = nt - 1 - (int)blockIdx.x;  // longest rows first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int niter = qt + 1;                 // key tiles 0 .. qt
-  const int nsub = 2 * niter;               // 64-key sub-tiles
-  const int qrow = b * p.T + qt * BQ;
 
   if (threadIdx.x == 0) {
-    mbar_init(qd_full, 1);
-    for (int s = 0; s < 2; s++) {
+    for (int s = 0; s < NSK; s++) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; s++) {
+      mbar_init(&qd_full[s], 1);
+      mbar_init(&qd_empty[s], 2);                  // the S and dP issuers
       mbar_init(&s_full[s], 2);                    // the S and dP issuers
       mbar_init(&ds_ready[s], BWD_SOFTMAX_WARPS);  // one arrival per softmax warp
       mbar_init(&ds_free[s], 1);
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], BWD_SOFTMAX_WARPS); // one arrival per softmax warp
     }
     mbar_init(mma_done, 1);
     mbar_init(s_done, 2);
@@ -963,47 +1082,63 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the first global-memory access comes after this
-  // TMEM: buffer x in columns [128 x, 128 x + 128): S then dP (64 each); dQ
-  const uint32_t T_DQ = tmem + 256;
+  // TMEM: score buffer x in columns [128 x, 128 x + 128): S then dP (64
+  // each); dQ accumulator a in [256 + 64 a, 320 + 64 a)
+  auto t_dq = [&](int a) { return tmem + 256 + HS * a; };
 
   if (warp == 0) {
+    // ---------------- TMA producer ----------------
     if (lane == 0) {
-      mbar_expect_tx(qd_full, 2 * TILE_BYTES);
-      tma_load_2d(smem + OFF_Q, &tmQKV, h * HS, qrow, qd_full);
-      tma_load_2d(smem + OFF_DO, &tmDO, h * HS, qrow, qd_full);
-      int issued = 0;
-      for (int j = 0; j < niter; j++) {
-        const int s = j & 1, krow = b * p.T + j * BKV;
-        if (!mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1, abort_flag, p.err)) break;
-        mbar_expect_tx(&kv_full[s], 2 * TILE_BYTES);
-        tma_load_2d(smem + OFF_K + s * TILE_BYTES, &tmQKV, p.C + h * HS, krow, &kv_full[s]);
-        tma_load_2d(smem + OFF_V + s * TILE_BYTES, &tmQKV, 2 * p.C + h * HS, krow, &kv_full[s]);
-        issued = j + 1;
+      int nqd = 0, nsub = 0;  // Q/dO and K/V stage fills issued
+      bool ok = true;
+      int rank, h, b;
+      for (int n = 0; ok && bwd_item(p, n, rank, h, b); n++) {
+        const int x = n & 1, qt = nt - 1 - rank, qrow = b * p.T + qt * BQ;
+        if (!(ok = mbar_wait(&qd_empty[x], ((n >> 1) & 1) ^ 1, abort_flag, p.err))) break;
+        mbar_expect_tx(&qd_full[x], 2 * TILE_BYTES);
+        tma_load_2d(smem + OFF_Q + x * TILE_BYTES, &tmQ, h * HS, qrow, &qd_full[x]);
+        tma_load_2d(smem + OFF_DO + x * TILE_BYTES, &tmDO, h * HS, qrow, &qd_full[x]);
+        nqd = n + 1;
+        for (int k0 = 0; ok && k0 < (qt + 1) * BKV; k0 += SUB) {  // the item's 64-key sub-tiles
+          const int s = nsub % NSK, krow = b * p.T + k0;
+          if (!(ok = mbar_wait(&kv_empty[s], ((nsub / NSK) & 1) ^ 1, abort_flag, p.err))) break;
+          mbar_expect_tx(&kv_full[s], 2 * SUBT_BYTES);
+          tma_load_2d(smem + OFF_K + s * SUBT_BYTES, &tmKV, p.C + h * HS, krow, &kv_full[s]);
+          tma_load_2d(smem + OFF_V + s * SUBT_BYTES, &tmKV, 2 * p.C + h * HS, krow, &kv_full[s]);
+          nsub++;
+        }
       }
-      if (*abort_flag) {
-        mbar_wait_drain(qd_full, 0);
-        for (int j = max(0, issued - 2); j < issued; j++) mbar_wait_drain(&kv_full[j & 1], (j >> 1) & 1);
-      }
+      for (int i = max(0, nqd - 2); i < nqd; i++) mbar_wait_drain(&qd_full[i & 1], (i >> 1) & 1);
+      for (int i = max(0, nsub - NSK); i < nsub; i++) mbar_wait_drain(&kv_full[i % NSK], (i / NSK) & 1);
     }
   } else if (warp == 1 || warp == DQ_DP_WARP) {
     // ---------------- scores issuers: S = Q K^T (warp 1), dP = dO V^T ----------------
     if (lane == 0) {
       const bool dpr = warp == DQ_DP_WARP;
-      const uint32_t sa = smem_u32(smem + (dpr ? OFF_DO : OFF_Q));
-      bool ok = mbar_wait(qd_full, 0, abort_flag, p.err);
-      for (int i = 0; i < nsub && ok; i++) {
-        const int j = i >> 1, s = j & 1, u = i & 1;
-        // TMEM buffer i & 1 was read out by the softmax warps before ds_ready(i - 2)
-        if (i >= 2 && !mbar_wait(&ds_ready[i & 1], ((i - 2) >> 1) & 1, abort_flag, p.err)) break;
-        if (u == 0 && !mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.err)) break;
-        tc_fence_after();
-        const uint32_t sb = smem_u32(smem + (dpr ? OFF_V : OFF_K) + s * TILE_BYTES) + u * (TILE_BYTES / 2);
-        const uint32_t t_acc = tmem + (i & 1) * 128 + (dpr ? SUB : 0);
+      int g = 0;
+      bool ok = true;
+      int rank, h, b;
+      for (int n = 0; ok && bwd_item(p, n, rank, h, b); n++) {
+        const int x = n & 1, qt = nt - 1 - rank;
+        if (!(ok = mbar_wait(&qd_full[x], (n >> 1) & 1, abort_flag, p.err))) break;
+        const uint32_t sa = smem_u32(smem + (dpr ? OFF_DO : OFF_Q) + x * TILE_BYTES);
+        for (int j = 0; ok && j <= qt; j++) {
+          for (int u = 0; u < 2; u++, g++) {
+            const int s = g % NSK;
+            // score buffer g & 1 was read out by the softmax warps before ds_ready(g - 2)
+            if (g >= 2 && !(ok = mbar_wait(&ds_ready[g & 1], ((g - 2) >> 1) & 1, abort_flag, p.err))) break;
+            if (!(ok = mbar_wait(&kv_full[s], (g / NSK) & 1, abort_flag, p.err))) break;
+            tc_fence_after();
+            const uint32_t sb = smem_u32(smem + (dpr ? OFF_V : OFF_K) + s * SUBT_BYTES);
+            const uint32_t t_acc = tmem + (g & 1) * 128 + (dpr ? SUB : 0);
 #pragma unroll
-        for (int kk = 0; kk < HS / 16; kk++)
-          mma_bf16(t_acc, desc_sw128(sa + kk * 32, 16, 1024), desc_sw128(sb + kk * 32, 16, 1024), IDESC_S64,
-                   kk > 0 ? 1u : 0u);
-        mma_commit(&s_full[i & 1]);
+            for (int kk = 0; kk < HS / 16; kk++)
+              mma_bf16(t_acc, desc_sw128(sa + kk * 32, 16, 1024), desc_sw128(sb + kk * 32, 16, 1024), IDESC_S64,
+                       kk > 0 ? 1u : 0u);
+            mma_commit(&s_full[g & 1]);
+          }
+        }
+        if (ok) mma_commit(&qd_empty[x]);  // the item's Q (dO) stage is free once these scores complete
       }
       mma_commit(s_done);
       mbar_wait_drain(s_done, 0);
@@ -1013,93 +1148,122 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     // (a sub-tile's scores have completed by the time its ds_ready fires, so
     // these commits cover the key tile's K and V)
     if (lane == 0) {
-      for (int i = 0; i < nsub; i++) {
-        if (!mbar_wait(&ds_ready[i & 1], (i >> 1) & 1, abort_flag, p.err)) break;
-        tc_fence_after();
-        const int j = i >> 1, s = j & 1, u = i & 1;
-        const uint32_t sk = smem_u32(smem + OFF_K + s * TILE_BYTES) + u * (TILE_BYTES / 2);
-        const uint32_t sds = smem_u32(smem + OFF_DS + (i & 1) * SUB_BYTES);
+      int g = 0;
+      bool ok = true;
+      int rank, h, b;
+      for (int n = 0; ok && bwd_item(p, n, rank, h, b); n++) {
+        const int x = n & 1, qt = nt - 1 - rank;
+        // accumulator x was read out by the softmax warps of item n - 2
+        if (!(ok = mbar_wait(&acc_empty[x], ((n >> 1) & 1) ^ 1, abort_flag, p.err))) break;
+        for (int j = 0; ok && j <= qt; j++) {
+          for (int u = 0; u < 2; u++, g++) {
+            const int s = g % NSK;
+            if (!(ok = mbar_wait(&ds_ready[g & 1], (g >> 1) & 1, abort_flag, p.err))) break;
+            tc_fence_after();
+            const uint32_t sk = smem_u32(smem + OFF_K + s * SUBT_BYTES);
+            const uint32_t sds = smem_u32(smem + OFF_DS + (g & 1) * SUB_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < SUB / 16; kk++)
-          mma_bf16(T_DQ, desc_sw128(sds + kk * 32, 16, 1024), desc_sw128(sk + kk * 2048, 8192, 1024), IDESC_ACC,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&ds_free[i & 1]);
-        if (u == 1) mma_commit(&kv_empty[s]);
+            for (int kk = 0; kk < SUB / 16; kk++)
+              mma_bf16(t_dq(x), desc_sw128(sds + kk * 32, 16, 1024), desc_sw128(sk + kk * 2048, 8192, 1024),
+                       IDESC_ACC, (j > 0 || u > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&ds_free[g & 1]);
+            mma_commit(&kv_empty[s]);
+          }
+        }
+        if (ok) mma_commit(&acc_full[x]);
       }
       mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0);
     }
   } else {
+    // ---------------- softmax warps, then each item's dQ read-out ----------------
     const int q4 = warp & 3, qs = (warp - 2) >> 2;  // TMEM lane quarter; 16-column slice
     const int r = q4 * 32 + lane;  // query row within the tile = TMEM lane
-    const int t = qt * BQ + r;     // query position
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const float sl2 = p.scale * 1.4426950408889634f;
-    const float2 ldr = p.LD[((size_t)b * p.NH + h) * p.T + t];  // (-lse2, -D) of this query
-    const float2 sl2v = make_float2(sl2, sl2), nlv = make_float2(ldr.x, ldr.x), ndv = make_float2(ldr.y, ldr.y);
+    const float2 sl2v = make_float2(sl2, sl2);
     bool ok = true;
-    for (int i = 0; i < nsub; i++) {
-      const int j = i >> 1, u = i & 1;
-      const bool got = mbar_wait(&s_full[i & 1], (i >> 1) & 1, abort_flag, p.err) &&
-                       (i < 2 || mbar_wait(&ds_free[i & 1], ((i - 2) >> 1) & 1, abort_flag, p.err));
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float sv[BWD_CW], dp[BWD_CW];
-      const uint32_t t_s = tmem + (i & 1) * 128 + lane_off + qs * BWD_CW;
-      tmem_ld16x2(t_s, t_s + SUB, sv, dp);
-      if (j == qt) {  // keys after the query are masked: column c when u*64 + qs*16 + c > r
-        const int lim = r - u * SUB - qs * BWD_CW;
+    int g = 0;
+    int rank, h, b;
+    for (int n = 0; bwd_item(p, n, rank, h, b); n++) {
+      const int x = n & 1, qt = nt - 1 - rank;
+      const int t = qt * BQ + r;  // query position
+      const float2 ldr = p.LD[((size_t)b * p.NH + h) * p.T + t];  // (-lse2, -D) of this query
+      const float2 nlv = make_float2(ldr.x, ldr.x), ndv = make_float2(ldr.y, ldr.y);
+      for (int j = 0; j <= qt; j++) {
+        for (int u = 0; u < 2; u++, g++) {
+          if (!ok) continue;  // after a timeout: count through to the item's end
+          const bool got = mbar_wait(&s_full[g & 1], (g >> 1) & 1, abort_flag, p.err) &&
+                           (g < 2 || mbar_wait(&ds_free[g & 1], ((g - 2) >> 1) & 1, abort_flag, p.err));
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+          float sv[BWD_CW], dp[BWD_CW];
+          const uint32_t t_s = tmem + (g & 1) * 128 + lane_off + qs * BWD_CW;
+          tmem_ld16x2(t_s, t_s + SUB, sv, dp);
+          if (j == qt) {  // keys after the query are masked: column c when u*64 + qs*16 + c > r
+            const int lim = r - u * SUB - qs * BWD_CW;
 #pragma unroll
-        for (int c = 0; c < BWD_CW; c++)
-          if (c > lim) sv[c] = -INFINITY;
-      }
-      uint32_t wd[BWD_CW / 2];
+            for (int c = 0; c < BWD_CW; c++)
+              if (c > lim) sv[c] = -INFINITY;
+          }
+          uint32_t wd[BWD_CW / 2];
 #pragma unroll
-      for (int e = 0; e < BWD_CW / 2; e++) {
-        const float2 x = fma2(make_float2(sv[2 * e], sv[2 * e + 1]), sl2v, nlv);
-        const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-        const float2 ds = mul2(pp, add2(make_float2(dp[2 * e], dp[2 * e + 1]), ndv));
-        wd[e] = cvt_bf16x2(ds.x, ds.y);
+          for (int e = 0; e < BWD_CW / 2; e++) {
+            const float2 xx = fma2(make_float2(sv[2 * e], sv[2 * e + 1]), sl2v, nlv);
+            const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
+            const float2 ds = mul2(pp, add2(make_float2(dp[2 * e], dp[2 * e + 1]), ndv));
+            wd[e] = cvt_bf16x2(ds.x, ds.y);
+          }
+          st_quarter_row_sw128(smem + OFF_DS + (g & 1) * SUB_BYTES, r, qs, wd);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tc_fence_before();
+          tc::mbar_arrive_warp(&ds_ready[g & 1]);
+        }
       }
-      st_quarter_row_sw128(smem + OFF_DS + (i & 1) * SUB_BYTES, r, qs, wd);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc_fence_before();
-      tc::mbar_arrive_warp(&ds_ready[i & 1]);
-    }
-    if (tc::epi_bar_and<32 * BWD_SOFTMAX_WARPS>(ok && mbar_wait(mma_done, 0, abort_flag, p.err) && !*abort_flag)) {
-      tc_fence_after();
+      // the item's dQ (accumulator x), then the accumulator is released
+      const bool got = __all_sync(0xffffffffu, ok && mbar_wait(&acc_full[x], (n >> 1) & 1, abort_flag, p.err));
       float dq[BWD_CW];
-      tmem_ld16(T_DQ + lane_off + qs * BWD_CW, dq);
+      if (got) {
+        tc_fence_after();
+        tmem_ld16(t_dq(x) + lane_off + qs * BWD_CW, dq);
+        tc_fence_before();
+        tc::mbar_arrive_warp(&acc_empty[x]);
 #pragma unroll
-      for (int d = 0; d < BWD_CW; d++) dq[d] *= p.scale;
-      const size_t o = ((size_t)b * p.T + t) * 3 * p.C + h * HS + qs * BWD_CW;
-      if (p.dqkv) {
+        for (int d = 0; d < BWD_CW; d++) dq[d] *= p.scale;
+        const size_t o = ((size_t)b * p.T + t) * 3 * p.C + h * HS + qs * BWD_CW;
+        if (p.dqkv) {
 #pragma unroll
-        for (int d = 0; d < BWD_CW; d += 4)
-          *reinterpret_cast<float4*>(p.dqkv + o + d) = make_float4(dq[d], dq[d + 1], dq[d + 2], dq[d + 3]);
-      }
-      if (p.dqkv_bf) {
+          for (int d = 0; d < BWD_CW; d += 4)
+            *reinterpret_cast<float4*>(p.dqkv + o + d) = make_float4(dq[d], dq[d + 1], dq[d + 2], dq[d + 3]);
+        }
+        if (p.dqkv_bf) {
 #pragma unroll
-        for (int d = 0; d < BWD_CW; d += 8)
-          *reinterpret_cast<uint4*>(p.dqkv_bf + o + d) =
-              make_uint4(cvt_bf16x2(dq[d], dq[d + 1]), cvt_bf16x2(dq[d + 2], dq[d + 3]), cvt_bf16x2(dq[d + 4], dq[d + 5]),
-                         cvt_bf16x2(dq[d + 6], dq[d + 7]));
+          for (int d = 0; d < BWD_CW; d += 8)
+            *reinterpret_cast<uint4*>(p.dqkv_bf + o + d) =
+                make_uint4(cvt_bf16x2(dq[d], dq[d + 1]), cvt_bf16x2(dq[d + 2], dq[d + 3]),
+                           cvt_bf16x2(dq[d + 4], dq[d + 5]), cvt_bf16x2(dq[d + 6], dq[d + 7]));
+        }
       }
       if (p.colsum) {
-        // the 128 query rows' column sums, through the dS buffers (free now)
-        float* red = reinterpret_cast<float*>(smem + OFF_DS);  // [qs][q4][16]
-        const float sq = warp_colsum16(dq, lane);
-        if (lane < 16) red[(qs * 4 + q4) * 16 + lane] = sq;
-        tc::epi_bar<32 * BWD_SOFTMAX_WARPS>();
+        // the 128 query rows' column sums, through this item's partials buffer
+        float* red = reinterpret_cast<float*>(smem + OFF_RED + x * RED_BYTES);  // [qs][q4][16]
+        if (got) {
+          const float sq = warp_colsum16(dq, lane);
+          if (lane < 16) red[(qs * 4 + q4) * 16 + lane] = sq;
+        }
+        // all sixteen warps take every item's barrier; a timeout anywhere ends the walk for all
+        if (!tc::epi_bar_and<32 * BWD_SOFTMAX_WARPS>(got)) break;
         const int t2 = threadIdx.x - 64;
         if (t2 < 64) {
           const int base = (t2 >> 4) * 4 * 16 + (t2 & 15);
           const float sum = ((red[base] + red[base + 16]) + red[base + 32]) + red[base + 48];
           p.colsum[((size_t)b * nt + qt) * 3 * p.C + h * HS + t2] = sum;
         }
+      } else if (!got) {
+        break;
       }
     }
   }

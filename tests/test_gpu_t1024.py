@@ -173,6 +173,43 @@ def test_wide_channel_layer_parity(C, NH, T, prec):
         assert e <= (1e-3 if fp32 else 3e-2), (name, e)
 
 
+def test_tc_attention_backward_many_items_layer_parity():
+    """One bf16 layer at the 124M channel count with B = 6, T = 512: 288
+    (tile, head, batch) items for the persistent tensor-core attention
+    backward, so most CTAs walk two items of different causal lengths (the
+    second round in reverse order), and the QKV bias gradient comes from the
+    kernels' per-item column sums.  Loss 2e-2, every gradient 3e-2 relative L2."""
+    import gpt_train_step_02_b300 as g
+
+    w = synth.Workload("tc_items_C768_bf16", 1, 768, 12, 512, 512, 512, 6, 512, "bf16", "uniform", 1)
+    p0 = synth.init_params(w)
+    rng = np.random.default_rng(13)
+    for name, (o, n) in synth.param_offsets(w).items():
+        if name in ("ln1w", "ln2w", "lnfw"):
+            p0[o:o + n] += (0.1 * rng.standard_normal(n)).astype(np.float32)
+        elif name in ("ln1b", "ln2b", "lnfb", "qkvb", "attprojb", "fcb", "fcprojb"):
+            p0[o:o + n] = (0.02 * rng.standard_normal(n)).astype(np.float32)
+    inp, tgt = synth.batch(w)
+    m = g.GPT2(w)
+    m.set_params(p0)
+    o = ref.RefModel(ref.config_from(w), w.B, w.T, np.float32)
+    o.set_params(p0)
+    lg = m.forward(inp, tgt)
+    lo = o.forward(inp, tgt)
+    assert abs(lg - lo) <= 2e-2, (lg, lo)
+    m.zero_grad()
+    m.backward()
+    o.zero_grad()
+    o.backward()
+    gg, go = m.get_grads(), o.grads.copy()
+    m.close()
+    o.close()
+    worst = {name: rel_l2(gg[off:off + n], go[off:off + n]) for name, (off, n) in synth.param_offsets(w).items()}
+    print("tc attention many items, grad rel-L2:", {k: f"{v:.2e}" for k, v in worst.items()})
+    for name, e in worst.items():
+        assert e <= 3e-2, (name, e)
+
+
 @pytest.mark.parametrize("C,NH,llama", [(768, 12, 0), (1024, 16, 0), (1280, 20, 0), (1024, 16, 1)])
 def test_layernorm_backward_many_rows(C, NH, llama):
     """2560 rows (B = 40, T = 64): more row groups of eight than twice the SM

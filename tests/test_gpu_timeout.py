@@ -9,7 +9,8 @@ tests lower the limit to 1 ns through ``gpt2_set_wait_limit_ns`` -- below
 1 us every wait gives up at its first call -- and check that:
 
 * the per-layer calls (a split-K 3xTF32 matmul, the fp32 tensor-core
-  attention) return GPT2_ERR_DEVICE_TIMEOUT;
+  attention, the persistent bf16 tensor-core attention forward and
+  backward) return GPT2_ERR_DEVICE_TIMEOUT;
 * a model step reports GPT2_ERR_DEVICE_TIMEOUT at its synchronisation, the
   handle is poisoned (every later call returns the same status);
 * with the default limit restored, the context is still usable: the same
@@ -35,6 +36,19 @@ def short_waits():
         yield g
     finally:
         g.set_wait_limit_ns(0)  # back to the 1 s default, whatever happened
+
+
+def bf16(a):
+    """Round to the nearest bf16 (ties to even), returned as float32."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return np.linalg.norm(a - b) / np.linalg.norm(b)
 
 
 def rel_err(a, b):
@@ -76,6 +90,35 @@ def test_fp32_tensor_core_attention_times_out_then_recovers(short_waits):
     g.attention_forward(y, lse, tq, NH)
     ry, _, _ = OPS.attention_forward(qkv, NH)
     assert np.abs(y.cpu().numpy() - ry).max() <= 1e-5 * max(np.abs(ry).max(), 1.0)
+
+
+def test_bf16_tensor_core_attention_times_out_then_recovers(short_waits):
+    """The persistent tensor-core attention kernels (bf16 operands, head size
+    64, T % 128 == 0): the forward, the dK/dV and the dQ kernel all give up,
+    each of their threads drains what it issued, and the same call then
+    matches the oracle fed the bf16-rounded inputs (bars of the attention
+    backward parity test: 1e-2 relative L2 per block, 3e-2 entrywise)."""
+    import torch
+
+    g = short_waits
+    B, T, C, NH = 2, 256, 128, 2
+    qkv = synth.randn(505, (B, T, 3 * C))
+    dy = synth.randn(506, (B, T, C))
+    tq, td = torch.tensor(qkv, device="cuda"), torch.tensor(dy, device="cuda")
+    dqkv = torch.zeros_like(tq)
+    with pytest.raises(g.GPT2Error) as e:
+        g.attention_backward(dqkv, td, tq, NH, precision=g.GPT2_PREC_BF16)
+    assert e.value.status == g.GPT2_ERR_DEVICE_TIMEOUT
+    g.set_wait_limit_ns(0)
+    g.attention_backward(dqkv, td, tq, NH, precision=g.GPT2_PREC_BF16)
+    got = dqkv.cpu().numpy()
+    q, d = bf16(qkv), bf16(dy)
+    _, _, att = OPS.attention_forward(q, NH)
+    ref_d = OPS.attention_backward(d, q, att, NH)
+    for part in range(3):
+        gp, rp = got[..., part * C:(part + 1) * C], ref_d[..., part * C:(part + 1) * C]
+        assert rel_l2(gp, rp) <= 1e-2, (part, rel_l2(gp, rp))
+        assert np.abs(gp - rp).max() <= 3e-2 * np.abs(rp).max(), part
 
 
 def test_model_step_timeout_poisons_the_handle(short_waits):
