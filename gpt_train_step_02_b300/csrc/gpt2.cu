@@ -1035,16 +1035,18 @@ static int launch_attn_fwd(float* atty, uint16_t* attybf, float* lse, const floa
                            int T, int C, int NH, int bf, int* err, cudaStream_t s) {
   const int hs = C / NH;
   if (bf && qkv_bf && hs == tca::HS && T % tca::BQ == 0) {
-    CUtensorMap tm;
-    if (!make_bf16_map(&tm, qkv_bf, 1, (long long)B * T, 3LL * C, 3LL * C, tca::BQ)) return -1;
+    // qkv with 128-row boxes (Q tiles) and 64-row boxes (K, V tiles)
+    CUtensorMap tq, tkv;
+    if (!make_bf16_map(&tq, qkv_bf, 1, (long long)B * T, 3LL * C, 3LL * C, tca::BQ)) return -1;
+    if (!make_bf16_map(&tkv, qkv_bf, 1, (long long)B * T, 3LL * C, 3LL * C, tca::fwd::FKV)) return -1;
     tca::Params p;
     p.B = B; p.T = T; p.C = C; p.NH = NH;
     p.scale = 1.0f / sqrtf((float)hs);
     p.y = atty; p.ybf = attybf; p.lse = lse; p.err = err;
     // persistent: two CTAs on each SM walk the (query tile, head, batch) items
     const long long items = (long long)(T / tca::BQ) * NH * B, slots = 2LL * dev_info().num_sms;
-    launch_k(tca::attn_fwd_tc_kernel, (int)(items < slots ? items : slots), tca::THREADS, tca::fwd::SMEM_BYTES, s, tm,
-             p);
+    launch_k(tca::attn_fwd_tc_kernel, (int)(items < slots ? items : slots), tca::THREADS, tca::fwd::SMEM_BYTES, s, tq,
+             tkv, p);
     return 1;
   }
   if (attn_tf32_path(bf, hs, T)) {  // fp32, short sequences: one CTA per (head, batch), 3xTF32 products

@@ -1,26 +1,29 @@
 // k_attention_tc.cuh -- causal attention forward on the tensor cores (bf16
 // operands, fp32 softmax), head size 64, T a multiple of 128.
 //
-// Per (batch b, head h, tile of 128 queries): for each key tile j <= the
-// query tile (causal),
+// Per (batch b, head h, tile of 128 queries): for each key tile j of 64
+// keys up to the query tile's end (causal),
 //   S   = Q K_j^T * scale                  tcgen05.mma kind::f16 -> TMEM
 //   m'  = max(m, rowmax S);  P = exp(S - m');  l = l e^(m-m') + rowsum P
-//   O   = O e^(m-m') + P V_j                P (bf16) staged in shared memory,
+//   O   = O e^(m-m') + P V_j                P (bf16) written to TMEM,
 //                                           P V_j -> TMEM -> registers
 // and at the end y = O / l, lse = m + log l (the log-sum-exp of the scaled
-// scores, as the backward pass expects).  Keys t2 > t of the diagonal tile
+// scores, as the backward pass expects).  Keys t2 > t of the last two tiles
 // are masked.  This is the online-softmax form of attention (the page «llm.c：
 // Andrej Karpathy带你从零复现LLM», section «核心代码解读：train_gpt2.c», item 1,
 // attention_forward computes the same causal softmax(q k^T / sqrt(hs)) v).
 //
-// Operands come from a bf16 copy of qkv, (B*T, 3C) row-major, through one
-// TMA map with 64 x 128 boxes (128-byte swizzle): Q and K tiles are K-major
-// (a row of 64 head dims per token); the V tile is read MN-major by the PV
-// product (rows of 64 head dims per key = the N dimension contiguous).
-// Six warps: warp 0 issues the TMA loads (Q once per item, K double-buffered,
-// V single-buffered so that two CTAs fit one SM); warp 1 allocates TMEM and
-// issues the MMAs; warps 2..5 own one query row per thread (TMEM lane = row)
-// for the softmax and the output.
+// Operands come from a bf16 copy of qkv, (B*T, 3C) row-major, through TMA
+// maps with 64 x 128 boxes (Q tiles) and 64 x 64 boxes (K and V tiles),
+// 128-byte swizzle: Q and K tiles are K-major (a row of 64 head dims per
+// token); the V tile is read MN-major by the PV product (rows of 64 head
+// dims per key = the N dimension contiguous).  Six warps: warp 0 issues the
+// TMA loads (Q double-buffered per item, K and V through four stages each);
+// warp 1 allocates TMEM and issues the MMAs; warps 2..5 own one query row
+// per thread (TMEM lane = row) for the softmax and the output.  S and P
+// each have two TMEM buffers: the scores of tile j + 2 are issued with the
+// P V product of tile j, so the softmax warps find each tile's scores
+// computed.
 // mbarrier wait is bounded (1 s); on expiry the CTA records DEV_ERR_TIMEOUT,
 // drains its copies and MMAs and returns.
 #pragma once
@@ -84,23 +87,29 @@ GPT2_DEV void mask_after(float* v, int lim) {
 }
 
 constexpr int BQ = 128;   // queries per CTA
-constexpr int BKV = 128;  // keys per tile
+constexpr int BKV = 128;  // keys per tile of the backward
 constexpr int HS = 64;    // head size
 constexpr int THREADS = 192;  // forward: TMA warp, MMA warp, 4 softmax warps
-constexpr int TILE_BYTES = 128 * HS * 2;  // 16 KB: a Q, K or V tile
+constexpr int TILE_BYTES = 128 * HS * 2;  // 16 KB: a 128-row Q, K or V tile
 namespace fwd {
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE_BYTES;          // 2 stages
-constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;      // 1 stage (its load waits only on the previous P V)
-constexpr int OFF_P = OFF_V + TILE_BYTES;          // 128 x 128 bf16 = two 16 KB K chunks
-constexpr int OFF_BAR = OFF_P + 2 * TILE_BYTES;
-// q_full, q_empty, k_full[2], k_empty[2], v_full, v_empty, s_full, p_full, pv_full, mma_done
-constexpr int NUM_BARS = 12;
+constexpr int FKV = 64;                      // keys per forward tile
+constexpr int KT_BYTES = FKV * HS * 2;       // 8 KB: a 64-row K or V tile
+constexpr int NK = 4;                        // K stages
+constexpr int NV = 4;                        // V stages
+constexpr int OFF_Q = 0;                     // 2 stages (one per item in flight)
+constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+constexpr int OFF_V = OFF_K + NK * KT_BYTES;
+constexpr int OFF_BAR = OFF_V + NV * KT_BYTES;
+// q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
+// s_full[2], p_full[2], pv_full[2], mma_done
+constexpr int NUM_BARS = 11 + 2 * NK + 2 * NV;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES + 1024 <= 233472 / 2, "two CTAs per SM");
 }  // namespace fwd
-constexpr int TMEM_COLS = 256;  // forward: S in columns [0, 128), P V in [128, 192)
+// forward TMEM: S of tile t in columns [64 (t & 1), +64); P V in [128, 192);
+// P of tile t (bf16 pairs) in [192 + 32 (t & 1), +32)
+constexpr int TMEM_COLS = 256;
 
 struct Params {
   int B, T, C, NH;
@@ -111,9 +120,10 @@ struct Params {
   int* err;
 };
 
-// Instruction descriptors: S = Q K^T (M 128, N 128, both K-major);
-// O += P V (M 128, N 64, V MN-major).
-constexpr uint32_t IDESC_S = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BKV >> 3) << 17) | ((uint32_t)(BQ >> 4) << 24);
+// Instruction descriptors: S = Q K^T (M 128, N 64, both K-major);
+// O += P V (M 128, N 64, P from TMEM, V MN-major).
+constexpr uint32_t IDESC_FS =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(fwd::FKV >> 3) << 17) | ((uint32_t)(BQ >> 4) << 24);
 constexpr uint32_t IDESC_PV =
     (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(HS >> 3) << 17) | ((uint32_t)(BQ >> 4) << 24);
 
@@ -131,39 +141,82 @@ GPT2_DEV bool fwd_item(const Params& p, int r, int& qt, int& h, int& b) {
   return true;
 }
 
+// D += A B with A (M = 128 rows, K = 16 bf16) in TMEM at a_tmem: row i in
+// lane i, two K values per 32-bit column, so 8 columns per MMA.
+GPT2_DEV void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of the warp's 32 lanes (one per
+// thread), then a wait for the stores to complete
+GPT2_DEV void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// The CTA's key tiles in walk order: item n, its key tile j (64 keys), and
+// whether j is the item's first / last (item n has 2 (qt + 1) tiles).
+struct FwdWalk {
+  int n = 0, j = 0, qt = 0, h = 0, b = 0;
+  bool valid = false;
+  GPT2_DEV void start(const Params& p) { n = 0; j = 0; valid = fwd_item(p, 0, qt, h, b); }
+  GPT2_DEV int ntiles() const { return 2 * (qt + 1); }
+  GPT2_DEV void next(const Params& p) {
+    if (++j == ntiles()) {
+      j = 0;
+      valid = fwd_item(p, ++n, qt, h, b);
+    }
+  }
+};
+
 __global__ void __launch_bounds__(THREADS, 2)
-    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ Params p) {
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
+                       const __grid_constant__ Params p) {
   pdl_launch_dependents();
   using namespace fwd;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
-  uint64_t* k_empty = bars + 4;
-  uint64_t* v_full = bars + 6;
-  uint64_t* v_empty = bars + 7;
-  uint64_t* s_full = bars + 8;
-  uint64_t* p_full = bars + 9;
-  uint64_t* pv_full = bars + 10;
-  uint64_t* mma_done = bars + 11;
+  uint64_t* q_empty = bars + 2;
+  uint64_t* k_full = bars + 4;
+  uint64_t* k_empty = k_full + NK;
+  uint64_t* v_full = k_empty + NK;
+  uint64_t* v_empty = v_full + NV;
+  uint64_t* s_full = v_empty + NV;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* pv_full = s_full + 4;
+  uint64_t* mma_done = s_full + 6;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
     for (int s = 0; s < 2; s++) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 4);  // one arrival per softmax warp
+      mbar_init(&pv_full[s], 1);
+    }
+    for (int s = 0; s < NK; s++) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
     }
-    mbar_init(v_full, 1);
-    mbar_init(v_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 4);  // one arrival per softmax warp
-    mbar_init(pv_full, 1);
+    for (int s = 0; s < NV; s++) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -180,94 +233,98 @@ __global__ void __launch_bounds__(THREADS, 2)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the first global-memory access comes after this
 
-  // Barrier phases run on across work items: item n of this CTA uses phase n
-  // of q_full/q_empty; its key tiles continue the running tile count g of the
-  // K ring (stage g & 1), the V buffer and s_full/p_full/pv_full.
+  // Counters run on across the CTA's items: item n uses Q stage n & 1; key
+  // tile number t (over all items) uses K stage t % NK, V stage t % NV and
+  // the S, P and P V buffers t & 1.
   if (warp == 0) {
     // ---------------- TMA producer ----------------
+    // K runs two tiles ahead of V (the scores of tile t + 2 are issued with
+    // the P V product of tile t); Q is loaded with its item's first K.
     if (lane == 0) {
-      int nq = 0, nk = 0, nv = 0;  // Q, K and V tiles issued (nk - nv is 0 or 1)
-      int qt, h, b;
-      bool ok = true;
-      for (int r = 0; ok && fwd_item(p, r, qt, h, b); r++) {
-        ok = mbar_wait(q_empty, (r & 1) ^ 1, abort_flag, p.err);
-        if (!ok) break;
-        mbar_expect_tx(q_full, TILE_BYTES);
-        tma_load_2d(smem + OFF_Q, &tmQKV, h * HS, b * p.T + qt * BQ, q_full);
-        nq++;
-        for (int j = 0; j <= qt; j++) {
-          const int krow = b * p.T + j * BKV;
-          ok = mbar_wait(&k_empty[nk & 1], ((nk >> 1) & 1) ^ 1, abort_flag, p.err);
-          if (!ok) break;
-          mbar_expect_tx(&k_full[nk & 1], TILE_BYTES);
-          tma_load_2d(smem + OFF_K + (nk & 1) * TILE_BYTES, &tmQKV, p.C + h * HS, krow, &k_full[nk & 1]);
-          nk++;
-          ok = mbar_wait(v_empty, (nv & 1) ^ 1, abort_flag, p.err);
-          if (!ok) break;
-          mbar_expect_tx(v_full, TILE_BYTES);
-          tma_load_2d(smem + OFF_V, &tmQKV, 2 * p.C + h * HS, krow, v_full);
-          nv++;
+      int nq = 0, nk = 0, nv = 0;  // Q, K and V stage fills issued
+      FwdWalk wk, wv;
+      wk.start(p);
+      wv.start(p);
+      auto load_k = [&]() -> bool {
+        if (!wk.valid) return true;
+        if (wk.j == 0) {
+          const int x = wk.n & 1;
+          if (!mbar_wait(&q_empty[x], ((wk.n >> 1) & 1) ^ 1, abort_flag, p.err)) return false;
+          mbar_expect_tx(&q_full[x], TILE_BYTES);
+          tma_load_2d(smem + OFF_Q + x * TILE_BYTES, &tmQ, wk.h * HS, wk.b * p.T + wk.qt * BQ, &q_full[x]);
+          nq = wk.n + 1;
         }
+        const int s = nk % NK;
+        if (!mbar_wait(&k_empty[s], ((nk / NK) & 1) ^ 1, abort_flag, p.err)) return false;
+        mbar_expect_tx(&k_full[s], KT_BYTES);
+        tma_load_2d(smem + OFF_K + s * KT_BYTES, &tmKV, p.C + wk.h * HS, wk.b * p.T + wk.j * FKV, &k_full[s]);
+        nk++;
+        wk.next(p);
+        return true;
+      };
+      bool ok = load_k() && load_k();
+      for (; ok && wv.valid; wv.next(p)) {
+        const int s = nv % NV;
+        if (!(ok = mbar_wait(&v_empty[s], ((nv / NV) & 1) ^ 1, abort_flag, p.err))) break;
+        mbar_expect_tx(&v_full[s], KT_BYTES);
+        tma_load_2d(smem + OFF_V + s * KT_BYTES, &tmKV, 2 * p.C + wv.h * HS, wv.b * p.T + wv.j * FKV, &v_full[s]);
+        nv++;
+        ok = load_k();
       }
-      if (*abort_flag) {
-        // wait for the copies still in flight before the CTA's memory goes away
-        if (nq > 0) mbar_wait_drain(q_full, (nq - 1) & 1);
-        for (int i = max(0, nk - 2); i < nk; i++) mbar_wait_drain(&k_full[i & 1], (i >> 1) & 1);
-        if (nv > 0) mbar_wait_drain(v_full, (nv - 1) & 1);
-      }
+      // the copies still in flight land before the CTA's memory goes away
+      // (the latest fill of each stage; on the normal path they have landed)
+      for (int i = max(0, nq - 2); i < nq; i++) mbar_wait_drain(&q_full[i & 1], (i >> 1) & 1);
+      for (int i = max(0, nk - NK); i < nk; i++) mbar_wait_drain(&k_full[i % NK], (i / NK) & 1);
+      for (int i = max(0, nv - NV); i < nv; i++) mbar_wait_drain(&v_full[i % NV], (i / NV) & 1);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    // Per key tile j: wait for P_j (the softmax warps have also read S_j out
-    // of TMEM by then), issue S_{j+1} = Q K_{j+1}^T into the freed S columns,
-    // then O_j = P_j V_j.  The softmax warps get S_{j+1} while P_j V_j runs;
-    // the first S of the next item follows the last P V of this one.
+    // S of tile t + 2 is issued right after P V of tile t, into the S buffer
+    // tile t's softmax has just released, so the softmax warps find the next
+    // scores computed; P V of tile t waits only for P_t.
     if (lane == 0) {
-      const uint32_t sq = smem_u32(smem + OFF_Q), sp = smem_u32(smem + OFF_P), sv = smem_u32(smem + OFF_V);
-      const uint32_t t_s = tmem, t_pv = tmem + 128;
-      auto issue_s = [&](int g) -> bool {
-        const int s = g & 1;
-        if (!mbar_wait(&k_full[s], (g >> 1) & 1, abort_flag, p.err)) return false;
+      const uint32_t sq = smem_u32(smem + OFF_Q);
+      FwdWalk ws;  // the tile whose scores are issued next (two ahead of P V)
+      ws.start(p);
+      int ts = 0;
+      auto issue_s = [&]() -> bool {
+        if (!ws.valid) return true;
+        const int x = ws.n & 1, s = ts % NK;
+        if (ws.j == 0 && !mbar_wait(&q_full[x], (ws.n >> 1) & 1, abort_flag, p.err)) return false;
+        if (!mbar_wait(&k_full[s], (ts / NK) & 1, abort_flag, p.err)) return false;
         tc_fence_after();
-        const uint32_t sk = smem_u32(smem + OFF_K + s * TILE_BYTES);
-        // S = Q K^T over the 64 head dims (four K = 16 steps along the 128-byte rows)
+        const uint32_t qa = sq + x * TILE_BYTES, kb = smem_u32(smem + OFF_K + s * KT_BYTES);
+        const uint32_t t_s = tmem + (ts & 1) * FKV;
 #pragma unroll
         for (int kk = 0; kk < HS / 16; kk++)
-          mma_bf16(t_s, desc_sw128(sq + kk * 32, 16, 1024), desc_sw128(sk + kk * 32, 16, 1024), IDESC_S,
+          mma_bf16(t_s, desc_sw128(qa + kk * 32, 16, 1024), desc_sw128(kb + kk * 32, 16, 1024), IDESC_FS,
                    kk > 0 ? 1u : 0u);
-        mma_commit(s_full);
+        mma_commit(&s_full[ts & 1]);
         mma_commit(&k_empty[s]);
+        if (ws.j == ws.ntiles() - 1) mma_commit(&q_empty[x]);  // the item's last scores read Q
+        ws.next(p);
+        ts++;
         return true;
       };
-      int g = 0;
-      bool ok = true;
-      int qt, h, b;
-      for (int r = 0; ok && fwd_item(p, r, qt, h, b); r++) {
-        const int nkt = qt + 1;
-        ok = mbar_wait(q_full, r & 1, abort_flag, p.err) && issue_s(g);
-        if (ok && nkt == 1) mma_commit(q_empty);  // the item's last S reads Q
-        for (int j = 0; j < nkt && ok; j++, g++) {
-          ok = mbar_wait(p_full, g & 1, abort_flag, p.err);
-          if (!ok) break;
-          tc_fence_after();
-          if (j + 1 < nkt) {
-            ok = issue_s(g + 1);
-            if (!ok) break;
-            if (j + 2 == nkt) mma_commit(q_empty);
-          }
-          ok = mbar_wait(v_full, g & 1, abort_flag, p.err);
-          if (!ok) break;
-          tc_fence_after();
-          // P (two 64-key chunks, K-major) times V (MN-major) over the 128 keys
+      bool ok = issue_s() && issue_s();
+      FwdWalk w;
+      int t = 0;
+      for (w.start(p); ok && w.valid; w.next(p), t++) {
+        const int s = t % NV;
+        ok = mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag, p.err) &&
+             mbar_wait(&v_full[s], (t / NV) & 1, abort_flag, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        // P (in TMEM, buffer t & 1) times V (MN-major) into the P V columns,
+        // which the softmax warps read out (P_{t-1} V) before releasing P_t
+        const uint32_t vb = smem_u32(smem + OFF_V + s * KT_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BKV / 16; kk++) {
-            const uint32_t pa = sp + (kk >> 2) * TILE_BYTES + (kk & 3) * 32;
-            mma_bf16(t_pv, desc_sw128(pa, 16, 1024), desc_sw128(sv + kk * 2048, 8192, 1024), IDESC_PV,
-                     kk > 0 ? 1u : 0u);
-          }
-          mma_commit(pv_full);
-          mma_commit(v_empty);
-        }
+        for (int kk = 0; kk < FKV / 16; kk++)
+          mma_bf16_ts(tmem + 2 * FKV, tmem + 3 * FKV + (t & 1) * (FKV / 2) + kk * 8, desc_sw128(vb + kk * 2048, 8192, 1024),
+                      IDESC_PV, kk > 0 ? 1u : 0u);
+        mma_commit(&pv_full[t & 1]);
+        mma_commit(&v_empty[s]);
+        ok = issue_s();
       }
       mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0);
@@ -276,103 +333,80 @@ __global__ void __launch_bounds__(THREADS, 2)
     // ---------------- softmax + output: one query row per thread ----------------
     // Scores are kept in base 2: x = s * scale * log2(e), m = running max of x,
     // P = 2^(x - m) rounded to bf16 for the P V product, l = running fp32 sum
-    // of P, O accumulated in registers in the basis of m.  Tile j: (1) row max
-    // of S_j; (2) fold in P_{j-1} V_{j-1}, rescaled by the correction of tile
-    // j-1, which also frees the P buffer; (3) write P_j.  Waits are decided
-    // per warp (the TMEM loads are warp-collective); the warps meet only at
-    // the end of the kernel, so a timeout cannot split a barrier.
+    // of P, O accumulated in registers in the basis of m.  Tile t: row max of
+    // S_t, P_t written to TMEM, P_{t-1} V folded into O with the correction of
+    // tile t-1 (which frees the P V columns), then P_t released to the MMA
+    // warp.  Waits are decided per warp (the TMEM loads are warp-collective);
+    // the warps meet only at the end of the kernel, so a timeout cannot split
+    // a barrier.
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;  // row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const uint32_t t_s = tmem + lane_off, t_pv = tmem + 128 + lane_off;
     const float sl2 = p.scale * 1.4426950408889634f;  // scale * log2(e)
     const float2 sl2v = make_float2(sl2, sl2);
-    uint8_t* prow = smem + OFF_P + r * 128;
     float o[HS];
-    auto fold_pv = [&](float corr) {
+    auto fold_pv = [&](int t, float corr) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(&pv_full[t & 1], (t >> 1) & 1, abort_flag, p.err))) return false;
+      tc_fence_after();
       float pv[HS];
-      tmem_ld64(t_pv, pv);
+      tmem_ld64(tmem + 2 * FKV + lane_off, pv);
 #pragma unroll
       for (int d = 0; d < HS; d += 2) {
         const float2 u = fma2(make_float2(o[d], o[d + 1]), make_float2(corr, corr), make_float2(pv[d], pv[d + 1]));
         o[d] = u.x;
         o[d + 1] = u.y;
       }
+      return true;
     };
-    int g = 0;
+    int t = 0;
     bool ok = true;
     int qt, h, b;
     for (int it = 0; ok && fwd_item(p, it, qt, h, b); it++) {
-      const int nkt = qt + 1;
+      const int nkt = 2 * (qt + 1);
 #pragma unroll
       for (int d = 0; d < HS; d++) o[d] = 0.f;
       float m2 = -INFINITY, lrow = 0.f, corr_prev = 0.f;
-      for (int j = 0; j < nkt; j++, g++) {
-        if (!__all_sync(0xffffffffu, mbar_wait(s_full, g & 1, abort_flag, p.err))) {
+      for (int j = 0; j < nkt; j++, t++) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const bool diag = j == qt;  // keys k > r of the diagonal tile follow the query
+        float sv[FKV];
+        tmem_ld64(tmem + (t & 1) * FKV + lane_off, sv);
+        // keys of the query tile's own 128 (the last two tiles): key c follows row r when c > lim
+        if (j >= nkt - 2) mask_after(sv, r - (j - (nkt - 2)) * FKV);
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-        for (int c = 0; c < BKV / 64; c++) {
-          float sv[64];
-          tmem_ld64(t_s + c * 64, sv);
-          if (diag) mask_after(sv, r - c * 64);
 #pragma unroll
-          for (int k = 0; k < 64; k += 8) {
-            mx[0] = max3(mx[0], sv[k], sv[k + 1]);
-            mx[1] = max3(mx[1], sv[k + 2], sv[k + 3]);
-            mx[2] = max3(mx[2], sv[k + 4], sv[k + 5]);
-            mx[3] = max3(mx[3], sv[k + 6], sv[k + 7]);
-          }
+        for (int k = 0; k < FKV; k += 8) {
+          mx[0] = max3(mx[0], sv[k], sv[k + 1]);
+          mx[1] = max3(mx[1], sv[k + 2], sv[k + 3]);
+          mx[2] = max3(mx[2], sv[k + 4], sv[k + 5]);
+          mx[3] = max3(mx[3], sv[k + 6], sv[k + 7]);
         }
         const float mnew = fmaxf(m2, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2);
         const float corr = ex2(m2 - mnew);  // 0 on the first tile (m2 = -inf)
-        if (j > 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait(pv_full, (g - 1) & 1, abort_flag, p.err))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          fold_pv(corr_prev);
-        }
         const float2 nm = make_float2(-mnew, -mnew);
         float2 ls = make_float2(0.f, 0.f);
-#pragma unroll 1
-        for (int c = 0; c < BKV / 64; c++) {
-          float sv[64];
-          tmem_ld64(t_s + c * 64, sv);
-          if (diag) mask_after(sv, r - c * 64);
+        uint32_t pw[FKV / 2];  // P of this row, bf16 pairs in key order
 #pragma unroll
-          for (int gg = 0; gg < 8; gg++) {  // 8 keys = one 16-byte group of the swizzled row
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-              const int k = gg * 8 + 2 * e;
-              const float2 x = fma2(make_float2(sv[k], sv[k + 1]), sl2v, nm);
-              const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-              w[e] = cvt_bf16x2(pp.x, pp.y);
-              ls = add2(ls, pp);
-            }
-            *reinterpret_cast<uint4*>(prow + c * TILE_BYTES + ((gg ^ (r & 7)) << 4)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-          }
+        for (int k = 0; k < FKV; k += 2) {
+          const float2 x = fma2(make_float2(sv[k], sv[k + 1]), sl2v, nm);
+          const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+          pw[k / 2] = cvt_bf16x2(pp.x, pp.y);
+          ls = add2(ls, pp);
         }
+        // P buffer t & 1 was last read by P_{t-2} V, folded at tile t - 1
+        tmem_st32(tmem + 3 * FKV + (t & 1) * (FKV / 2) + lane_off, pw);
+        if (j > 0 && !(ok = fold_pv(t - 1, corr_prev))) break;
+        tc_fence_before();
+        tc::mbar_arrive_warp(&p_full[t & 1]);
         lrow = lrow * corr + (ls.x + ls.y);
         m2 = mnew;
         corr_prev = corr;
-        // make the generic-proxy P writes visible to the tensor core
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-        tc::mbar_arrive_warp(p_full);
       }
       if (!ok) break;
-      ok = __all_sync(0xffffffffu, mbar_wait(pv_full, (g - 1) & 1, abort_flag, p.err));
-      if (!ok) break;
-      tc_fence_after();
-      fold_pv(corr_prev);
+      if (!(ok = fold_pv(t - 1, corr_prev))) break;
       const float inv = 1.f / lrow;
       const size_t yo = (size_t)(b * p.T + qt * BQ + r) * p.C + h * HS;
       if (p.y) {  // NULL when only the bf16 copy is read downstream
