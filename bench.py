@@ -413,6 +413,8 @@ KERNEL_SOURCES = {
     "layernorm": [("k_layernorm.cuh", "layernorm_fwd_kernel"), ("k_layernorm.cuh", "layernorm_bwd_kernel"),
                   ("k_layernorm.cuh", "layernorm_bwd_stride_kernel"), ("k_misc.cuh", "col_finish_kernel")],
     "encoder": [("k_misc.cuh", "encoder_fwd_kernel")],
+    "attn_fwd": ["k_attention_tc.cuh", "k_attention_tf32.cuh"],
+    "attn_bwd": ["k_attention_tc.cuh", "k_attention_tf32.cuh"],
 }
 
 
@@ -501,9 +503,9 @@ def roofline_for(kind, k, peaks, w):
         achieved = k["work_per_launch"] / (k["avg_launch_ms"] * 1e-3) / 1e12
         hs = w.channels // w.num_heads
         if w.precision == "bf16" and hs == 64 and w.T % 128 == 0:  # tcgen05 kind::f16 products
-            return tensor_line(kind, achieved, peaks, w, False)
+            return tensor_line(kind, achieved, peaks, w, False, recorded_traffic(kind, w))
         if w.precision == "fp32" and hs == 64 and w.T <= 64:  # tcgen05 kind::tf32, 3xTF32 products
-            return tensor_line(kind, achieved, peaks, w, True)
+            return tensor_line(kind, achieved, peaks, w, True, recorded_traffic(kind, w))
         # CUDA-core fp32: 148 SMs x 128 FMA lanes x 2 FLOPs x the maximum SM clock
         peak = 148 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
         return {"kernel": kind, "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -519,7 +521,15 @@ TRAFFIC_KERNELS = {"gemm": ("gemm_tf32x3", "gemm_bf16"),
                    "adamw": ("adamw_kernel", "adamw_rows_kernel", "adamw_sorted_rows_kernel"),
                    "xent": ("xent_fused_kernel", "xent_bf16_kernel"),
                    "layernorm": ("layernorm_fwd_kernel", "layernorm_bwd_kernel", "layernorm_bwd_stride_kernel"),
-                   "encoder": ("encoder_fwd_kernel",)}
+                   "encoder": ("encoder_fwd_kernel",),
+                   "attn_fwd": ("attn_fwd_tc_kernel", "attn_fwd_tf32_kernel"),
+                   "attn_bwd": ("attn_bwd_ld_bf16_kernel", "attn_bwd_dkv_tc_kernel", "attn_bwd_dq_tc_kernel",
+                                "attn_bwd_tf32_kernel")}
+# Classes whose timed launch is one layer's attention op: one launch of each of
+# the class's kernels that the path takes (the bf16 backward: the (-lse log2 e,
+# -D) pass, dK/dV and dQ).  Their record is the sum, over the kernels seen in
+# the capture, of each kernel's mean DRAM bytes per launch.
+TRAFFIC_PER_OP = ("attn_fwd", "attn_bwd")
 BYTE_UNITS = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
 
 
@@ -529,25 +539,34 @@ def record_traffic(csv_path, w, kind="gemm"):
     (``--metrics dram__bytes_read.sum,dram__bytes_write.sum --csv``), stored
     in profiles/roofline_traffic.json with the hash of the kernel sources it
     was taken on.  Every step launches the same sequence, so any run of one
-    step's launch count covers each launch of a step once."""
+    step's launch count covers each launch of a step once.  For the attention
+    classes (TRAFFIC_PER_OP) one timed launch is one layer's op, several
+    kernels: the record sums the kernels' means."""
     import csv as _csv
 
     rows = list(_csv.DictReader(l for l in open(csv_path) if not l.startswith("==")))
     launches = {}
     for r in rows:
         name = r["Kernel Name"]
-        if not any(k in name for k in TRAFFIC_KERNELS[kind]):
+        hit = [k for k in TRAFFIC_KERNELS[kind] if k in name]
+        if not hit:
             continue
         m = r["Metric Name"]
         if m not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
             continue
         v = float(r["Metric Value"].replace(",", "")) * BYTE_UNITS[r["Metric Unit"]]
-        launches.setdefault(int(r["ID"]), {})[m] = v
-    full = [d for d in launches.values() if len(d) == 2]
+        launches.setdefault(int(r["ID"]), {"kernel": hit[0]})[m] = v
+    full = [d for d in launches.values() if len(d) == 3]
     if not full:
         print(f"no {kind} launches with both DRAM metrics in {csv_path}", file=sys.stderr)
         return 1
-    per_launch = sum(d["dram__bytes_read.sum"] + d["dram__bytes_write.sum"] for d in full) / len(full)
+    if kind in TRAFFIC_PER_OP:
+        by_kernel = {}
+        for d in full:
+            by_kernel.setdefault(d["kernel"], []).append(d["dram__bytes_read.sum"] + d["dram__bytes_write.sum"])
+        per_launch = sum(sum(v) / len(v) for v in by_kernel.values())
+    else:
+        per_launch = sum(d["dram__bytes_read.sum"] + d["dram__bytes_write.sum"] for d in full) / len(full)
     path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
     data = json.load(open(path)) if os.path.exists(path) else {}
     data.setdefault(w.name, {})[kind] = {

@@ -118,3 +118,28 @@ def test_traffic_record_averages_matmul_launches_and_goes_stale(bench, tmp_path,
     sha["v"] = "bbbb"  # the kernel sources changed since the capture
     assert bench.recorded_traffic("gemm", w) is None
     assert bench.recorded_traffic("gemm", synth.WORKLOADS["gpt2_124m_B16_T1024_bf16"]) is None
+
+
+def test_attention_traffic_is_per_layer_op(bench, tmp_path, monkeypatch):
+    # one timed attention-backward launch is a layer's op: the (-lse log2 e,
+    # -D) pass, dK/dV and dQ, so the record sums the kernels' means; a
+    # capture window that cuts a layer's op in two does not bias it
+    os.makedirs(tmp_path / "profiles")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_sha", lambda kind: "cccc")
+    cap = tmp_path / "cap.csv"
+    write_capture(cap, [("tca::attn_bwd_dkv_tc_kernel(...)", "100", "20000"),  # window starts mid-op
+                        ("tca::attn_bwd_dq_tc_kernel(...)", "100", "8000"),
+                        ("void tca::attn_bwd_ld_bf16_kernel<8>(...)", "50", "0"),
+                        ("tca::attn_bwd_dkv_tc_kernel(...)", "104", "20000"),
+                        ("tca::attn_bwd_dq_tc_kernel(...)", "100", "8000"),
+                        ("tca::attn_fwd_tc_kernel(...)", "77", "1000"),
+                        ("tcb::gemm_bf16_kernel<256, 0, 2>(...)", "999", "0")])
+    w = synth.WORKLOADS["gpt2_124m_B16_T1024_bf16"]
+    assert bench.record_traffic(str(cap), w, "attn_bwd") == 0
+    assert bench.recorded_traffic("attn_bwd", w) == pytest.approx(50e6 + 122e6 + 108e6)
+    assert bench.record_traffic(str(cap), w, "attn_fwd") == 0
+    assert bench.recorded_traffic("attn_fwd", w) == pytest.approx(78e6)
+    peaks = dict(PEAKS)
+    r = bench.roofline_for("attn_bwd", k(1.0e9, 1.0), peaks, w)
+    assert r["traffic"] == pytest.approx(280e6)
