@@ -936,6 +936,13 @@ static K ln_pick(int C, K k1, K k2, K k4, K k6, K k8, K k10) {
   return v <= 1 ? k1 : v <= 2 ? k2 : v <= 4 ? k4 : v <= 6 ? k6 : v <= 8 ? k8 : k10;
 }
 
+// Layernorm forward blocks: four warps (rows).  Block residency is counted in
+// whole blocks, so small blocks keep more rows in flight: at C = 1280 (72
+// registers a thread) seven 4-warp blocks fit an SM, 1036 on the GPU, and a
+// 4096-row launch runs in one wave, where 8-warp blocks (three an SM) left
+// 68 blocks for a second one.
+#define LNF_WARPS 4
+
 static void ln_forward(gpt2_t* m, float* y, uint16_t* ybf, float* mean, float* rstd, const float* x, const float* w,
                        const float* b, int N) {
   int C = m->cfg.channels;
@@ -944,11 +951,12 @@ static void ln_forward(gpt2_t* m, float* y, uint16_t* ybf, float* mean, float* r
   if (m->cfg.llama) {  // RMSNorm: no mean, no shift
     auto k = ln_pick(C, layernorm_fwd_kernel<1, true>, layernorm_fwd_kernel<2, true>, layernorm_fwd_kernel<4, true>,
                      layernorm_fwd_kernel<6, true>, layernorm_fwd_kernel<8, true>, layernorm_fwd_kernel<10, true>);
-    launch_k(k, ceil_div(N, 8), 256, 0, m->stream, y, ybf, mean, rstd, x, w, (const float*)nullptr, N, C);
+    launch_k(k, ceil_div(N, LNF_WARPS), LNF_WARPS * 32, 0, m->stream, y, ybf, mean, rstd, x, w, (const float*)nullptr, N,
+             C);
   } else {
     auto k = ln_pick(C, layernorm_fwd_kernel<1, false>, layernorm_fwd_kernel<2, false>, layernorm_fwd_kernel<4, false>,
                      layernorm_fwd_kernel<6, false>, layernorm_fwd_kernel<8, false>, layernorm_fwd_kernel<10, false>);
-    launch_k(k, ceil_div(N, 8), 256, 0, m->stream, y, ybf, mean, rstd, x, w, b, N, C);
+    launch_k(k, ceil_div(N, LNF_WARPS), LNF_WARPS * 32, 0, m->stream, y, ybf, mean, rstd, x, w, b, N, C);
   }
   timer_end(m, TK_LAYERNORM);
   m->launches++;

@@ -1,9 +1,12 @@
 """Op-level cases for profiling one kernel family in isolation (for example
 under ncu): a linear-layer forward, or a causal attention backward (which runs
-the attention forward first), on seeded normal inputs, through the C ABI.
+the attention forward first), on seeded normal inputs, through the C ABI; or
+whole training steps of a named workload with fewer layers, which runs every
+per-layer kernel at the workload's shapes while holding a few GB on the device.
 
     python -m gpt_train_step_02_b300.opcase matmul --N 16384 --IC 768 --OC 3072 --precision bf16
     python -m gpt_train_step_02_b300.opcase attention --B 16 --T 1024 --C 768 --NH 12 --precision bf16
+    python -m gpt_train_step_02_b300.opcase step --workload gpt2_774m_B4_T1024_bf16 --layers 2
 
 Each case runs --repeat times (default 3) on cuda:0, then synchronises.
 """
@@ -25,8 +28,33 @@ def main(argv=None) -> int:
     at.add_argument("--NH", type=int, default=12)
     for p in (mm, at):
         p.add_argument("--precision", choices=["fp32", "bf16"], default="bf16")
+    st = sub.add_parser("step", help="training steps (forward, zero_grad, backward, AdamW) of a workload")
+    st.add_argument("--workload", default="gpt2_774m_B4_T1024_bf16")
+    st.add_argument("--layers", type=int, default=0, help="layer count in place of the workload's (0: its own)")
+    for p in (mm, at, st):
         p.add_argument("--repeat", type=int, default=3)
     args = ap.parse_args(argv)
+
+    if args.case == "step":
+        import dataclasses
+
+        import torch
+
+        import gpt_train_step_02_b300 as g
+        import synth
+
+        w = synth.WORKLOADS[args.workload]
+        if args.layers:
+            w = dataclasses.replace(w, name=f"{w.name}_L{args.layers}", num_layers=args.layers)
+        m = g.GPT2(w, seed=synth.INIT_SEED)
+        inp, tgt = synth.batch(w)
+        for t in range(1, args.repeat + 1):
+            m.train_step(inp, tgt, t, w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+        m.sync()
+        m.close()
+        torch.cuda.synchronize()
+        print("ok", args.case, w.name)
+        return 0
 
     import torch
 
