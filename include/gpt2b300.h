@@ -271,7 +271,8 @@ int gpt2op_attention_forward(float* y, float* lse, const float* qkv, int B, int 
  * dS = P o (dy v^T - D), dq = dS k / sqrt(hs), dk = dS^T q / sqrt(hs),
  * dv = P^T dy.  precision and requirements as gpt2op_attention_forward (bf16:
  * qkv and dy rounded to bf16; with hs = 64 and T % 128 == 0 the tensor-core
- * kernels, one CTA per output row tile, no atomics).  dqkv is overwritten.
+ * kernels: persistent CTAs, one per SM, walk the output row tiles, each tile
+ * written by one CTA, no atomics).  dqkv is overwritten.
  * workspace: gpt2op_attention_backward_workspace_bytes(B, T, C, NH) device
  * bytes.  Synchronises the stream. */
 size_t gpt2op_attention_backward_workspace_bytes(int B, int T, int C, int NH);
