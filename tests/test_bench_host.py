@@ -36,6 +36,7 @@ def test_hbm_roofline_is_bytes_over_time(bench):
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
     assert r["achieved"] == pytest.approx(6000.0)
     assert r["frac"] == pytest.approx(1.0)
+    assert r["frac_of_nominal"] == pytest.approx(6000.0 / 7700.0)  # beside it: the 7.7 TB/s datasheet figure
 
 
 def test_fp32_matmul_peak_is_tf32_from_bf16(bench):
