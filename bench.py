@@ -133,6 +133,20 @@ def oracle_sample_run(w, seconds_target: float = 12.0, max_steps: int = 50, B_sa
     return B * w.T * steps / el, steps, B * w.T, el
 
 
+def oracle_one_thread(w, seconds: float = 4.0):
+    """The oracle on one host thread, beside the all-cores figure: the same
+    kind of sample (training steps on one sequence of the batch) in a child
+    process started with OMP_NUM_THREADS=1, which OpenMP reads at start-up.
+    Returns the child's JSON record, or None when it did not complete."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--workload", w.name, "--oracle-one-thread", str(seconds)]
+    try:
+        out = subprocess.run(cmd, env=dict(os.environ, OMP_NUM_THREADS="1"), capture_output=True, text=True,
+                             timeout=60.0 + 10.0 * seconds)
+        return json.loads(out.stdout.strip().splitlines()[-1]) if out.returncode == 0 else None
+    except (subprocess.TimeoutExpired, ValueError, IndexError):
+        return None
+
+
 def cpu_cores() -> int:
     n = int(os.environ.get("OMP_NUM_THREADS", "0") or 0)
     return n if n > 0 else len(os.sched_getaffinity(0))
@@ -374,7 +388,8 @@ def run_ours(args, w):
         v, steps, tok, el = oracle_sample_run(w, seconds_target=args.cpu_seconds)
         cpu = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{steps} full oracle training step(s) of the same workload ({tok} tokens each), "
-                         f"{el:.1f} s of CPU time"}
+                         f"{el:.1f} s of CPU time",
+               "one_thread": oracle_one_thread(w)}
     line = {
         "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
@@ -603,9 +618,19 @@ def main():
                     help="store the DRAM bytes per launch of one kernel class (--traffic-kind) from an ncu capture "
                          "of --workload and exit")
     ap.add_argument("--traffic-kind", default="gemm", choices=sorted(TRAFFIC_KERNELS))
+    ap.add_argument("--oracle-one-thread", type=float, metavar="SECONDS",
+                    help="time the oracle alone for about SECONDS on one sequence of --workload's batch, print "
+                         "one JSON record and exit (the cpu_baseline's one-thread figure runs this with "
+                         "OMP_NUM_THREADS=1)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     w = synth.WORKLOADS[args.workload]
+    if args.oracle_one_thread is not None:
+        v, steps, tok, el = oracle_sample_run(w, seconds_target=args.oracle_one_thread, B_sample=1)
+        print(json.dumps({"value": v, "unit": "tokens/s", "cores": cpu_cores(),
+                          "sample": f"{steps} oracle training step(s) on one sequence ({tok} tokens each), "
+                                    f"{el:.1f} s"}))
+        return 0
     if args.record_traffic:
         return record_traffic(args.record_traffic, w, args.traffic_kind)
     if args.impl == "reference":

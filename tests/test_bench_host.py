@@ -144,3 +144,11 @@ def test_attention_traffic_is_per_layer_op(bench, tmp_path, monkeypatch):
     peaks = dict(PEAKS)
     r = bench.roofline_for("attn_bwd", k(1.0e9, 1.0), peaks, w)
     assert r["traffic"] == pytest.approx(280e6)
+
+
+def test_oracle_one_thread_sample_runs_in_a_child_with_one_thread(bench):
+    # the cpu_baseline's one-thread figure: a child process with
+    # OMP_NUM_THREADS=1 times the oracle and reports one core
+    rec = bench.oracle_one_thread(synth.WORKLOADS["tiny_L2_C64"], seconds=0.2)
+    assert rec is not None
+    assert rec["cores"] == 1 and rec["unit"] == "tokens/s" and rec["value"] > 0
