@@ -43,6 +43,7 @@ EXPORTS = [
     "gpt2_kernel_timer_read", "gpt2op_matmul_workspace_bytes", "gpt2op_matmul_forward", "gpt2op_matmul_backward",
     "gpt2op_matmul_backward_noalloc", "gpt2op_attention_workspace_bytes", "gpt2op_attention_forward",
     "gpt2op_attention_backward_workspace_bytes", "gpt2op_attention_backward", "gpt2_set_wait_limit_ns",
+    "gpt2_plan_bf16_matmul",
 ]
 
 
@@ -93,6 +94,7 @@ def lib() -> ct.CDLL:
             "gpt2_train_step": (I, [P, P, P, I, I, F, F, F, F, F, I, P]),
             "gpt2_kernel_timer": (I, [P, I]),
             "gpt2_set_wait_limit_ns": (I, [ct.c_ulonglong]),
+            "gpt2_plan_bf16_matmul": (I, [I, I, I, I, I, I, P, P]),
             "gpt2op_matmul_workspace_bytes": (SZ, [I, I, I]),
             "gpt2op_matmul_forward": (I, [P, P, P, P, I, I, I, I, P, P]),
             "gpt2op_matmul_backward": (I, [P, P, P, P, P, P, I, I, I, I, P, P]),
@@ -226,6 +228,16 @@ def gpt2_kernel_timer_read(h):
 def set_wait_limit_ns(ns: int) -> None:
     """Limit of the device-side pipeline waits (0 restores the 1 s default)."""
     _check(lib().gpt2_set_wait_limit_ns(int(ns)), "gpt2_set_wait_limit_ns")
+
+
+def plan_bf16_matmul(M: int, N: int, K: int, no_split: bool = False, logits: bool = False,
+                     num_sms: int = 148) -> tuple:
+    """(tile width, K splits) the bf16 tensor-core matmul takes for an M x N x K
+    product on num_sms SMs.  Host-side: no device is touched."""
+    bn, sp = ct.c_int(0), ct.c_int(0)
+    _check(lib().gpt2_plan_bf16_matmul(int(M), int(N), int(K), int(bool(no_split)), int(bool(logits)), int(num_sms),
+                                       ct.byref(bn), ct.byref(sp)), "gpt2_plan_bf16_matmul")
+    return int(bn.value), int(sp.value)
 
 
 def gpt2_free(h) -> None:

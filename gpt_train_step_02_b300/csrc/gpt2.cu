@@ -2140,6 +2140,14 @@ EXPORT int gpt2_set_wait_limit_ns(unsigned long long ns) {
   return cudaDeviceSynchronize() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
+EXPORT int gpt2_plan_bf16_matmul(int M, int N, int K, int no_split, int logits, int num_sms, int* BN, int* splits) {
+  if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0 || !BN || !splits) return GPT2_ERR_ARG;
+  const Bf16Plan plan = plan_bf16(M, N, K, no_split || logits, SPLITK_WS_FLOATS, num_sms, !logits);
+  *BN = plan.BN;
+  *splits = plan.splits;
+  return GPT2_OK;
+}
+
 EXPORT long long gpt2_num_parameters(const gpt2_t* m) { return m ? m->np : -1; }
 
 EXPORT long long gpt2_last_launch_count(const gpt2_t* m) { return m ? m->launches : -1; }

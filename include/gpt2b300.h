@@ -202,6 +202,19 @@ int gpt2_kernel_timer_read(gpt2_t* m, double* total_ms, long long* launches, dou
  * handle and call on it; synchronises the device. */
 int gpt2_set_wait_limit_ns(unsigned long long ns);
 
+/* The tile plan of the bf16 tensor-core matmul for an M x N x K product
+ * (out[M][N] = sum over K), as the model's steps and gpt2op_matmul_* take it
+ * on a GPU with num_sms SMs (148 on a B300).  A host-side query: no device,
+ * handle or memory is touched.  *BN receives the output tile width (128, 192
+ * or 256; tiles are 128 rows high), *splits the number of K ranges reduced
+ * through the split-K workspace (1: none).  no_split != 0: an epilogue that
+ * takes column sums (bias gradients), which a K split would bypass.
+ * logits != 0: the LM head's epilogue with per-half-tile row statistics (no
+ * K split, no 192-wide tiles).  Returns GPT2_ERR_ARG for a non-positive size
+ * or SM count or a NULL output.  The pages have no counterpart: it exposes
+ * the library's own wave and K-tile cost model for inspection and tests. */
+int gpt2_plan_bf16_matmul(int M, int N, int K, int no_split, int logits, int num_sms, int* BN, int* splits);
+
 /* Frees the handle (and the arena if the library allocated it). */
 int gpt2_free(gpt2_t* m);
 

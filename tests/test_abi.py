@@ -85,3 +85,50 @@ def test_build_rejects_bad_arguments_without_touching_the_device():
     assert L.gpt2_update(None, 1e-4, 0.9, 0.999, 1e-8, 0.0, 1) == g.GPT2_ERR_ARG
     assert L.gpt2_free(None) == g.GPT2_ERR_ARG
     assert L.gpt2_num_parameters(None) == -1
+
+
+# The bf16 matmul planner (host logic, no device): the plans the design notes
+# and the launch lists record for the GPT-2 product shapes on 148 SMs.
+PLAN_CASES = [
+    # (M, N, K): (tile width, K splits)
+    ((4096, 1280, 1280), (192, 1)),    # 774M attention projection, B*T = 4096: 224 tiles, not 160 of 256
+    ((4096, 1280, 5120), (192, 1)),    # 774M MLP output projection
+    ((2304, 768, 16384), (192, 2)),    # 124M QKV weight gradient
+    ((768, 768, 16384), (128, 4)),     # 124M attention-projection weight gradient
+    ((3072, 768, 16384), (256, 2)),    # 124M MLP weight gradients
+    ((768, 3072, 16384), (256, 2)),
+    ((16384, 3072, 768), (256, 1)),    # 124M MLP input projection, forward
+    ((16384, 768, 50304), (256, 1)),   # 124M LM-head input gradient
+]
+
+
+@pytest.mark.parametrize("mnk,plan", PLAN_CASES)
+def test_bf16_matmul_plans_of_the_gpt2_products(mnk, plan):
+    assert g.plan_bf16_matmul(*mnk) == plan
+
+
+@pytest.mark.parametrize("mnk", [c[0] for c in PLAN_CASES] + [(256, 768, 768), (300, 96, 260), (128, 64, 64)])
+def test_bf16_matmul_plan_invariants(mnk):
+    M, N, K = mnk
+    bn, s = g.plan_bf16_matmul(M, N, K)
+    assert bn in (128, 192, 256) and s >= 1
+    kt = -(-K // 64)
+    if s > 1:
+        # only grids below one wave are split, at least four K tiles a split,
+        # the fp32 partials within the 8M-float workspace
+        assert -(-M // 128) * -(-N // bn) < 148
+        assert kt // s >= 4 or -(-kt // s) >= 4
+        assert s * M * N <= 8 << 20
+    # epilogues that take column sums are never split; the LM head's
+    # row-statistics epilogue is never split and never 192 wide
+    assert g.plan_bf16_matmul(M, N, K, no_split=True)[1] == 1
+    bn_l, s_l = g.plan_bf16_matmul(M, N, K, logits=True)
+    assert s_l == 1 and bn_l in (128, 256)
+
+
+def test_bf16_matmul_plan_rejects_bad_arguments():
+    for args in [(0, 768, 768), (256, 0, 768), (256, 768, -1)]:
+        with pytest.raises(g.GPT2Error):
+            g.plan_bf16_matmul(*args)
+    with pytest.raises(g.GPT2Error):
+        g.plan_bf16_matmul(256, 768, 768, num_sms=0)
